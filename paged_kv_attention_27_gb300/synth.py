@@ -1,0 +1,283 @@
+"""Seeded synthetic paged-KV batches: the one input source shared by the oracle
+side and the CUDA side of every test and of the benchmark.
+
+This module builds inputs only. It holds none of the attention arithmetic:
+no scores, no softmax, no merge. Everything it returns is plain numpy:
+
+* values are standard normal draws from numpy's counter-based Philox
+  generator, rounded to bf16 (round-to-nearest-even) and stored as raw
+  ``uint16`` bit patterns;
+* the page table is the CSR triple ``page_indptr`` / ``page_indices`` /
+  ``last_page_len`` of a paged KV cache (pages of ``page_size`` token slots,
+  allocated on demand, "FlashInfer kernel library deep-dive", section
+  "PageAttention"), with the physical pages handed out in a seeded random
+  order so that no request's pages are contiguous;
+* the two cache layouts are named as on that page (section "KV cache layout"):
+  NHD = ``[page][slot][kv_head][dim]``, HND = ``[page][kv_head][slot][dim]``;
+* query rows of all requests are packed back to back (``qo_indptr``), the
+  variable-length form with prefix-sum offsets used by the varlen prefill
+  wrapper in "FlashAttention-3 kernel integration in inference engines",
+  section 2.
+
+The workload builders at the bottom give the shapes of the pages' workloads
+(Llama-7B and Llama2-70B head shapes, 1K-32K contexts); no model weights or
+datasets are involved.
+"""
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass, field
+
+import numpy as np
+
+NHD = "NHD"
+HND = "HND"
+
+
+def philox(seed: int) -> np.random.Generator:
+    """numpy Generator over the Philox-4x64 counter-based bit generator."""
+    return np.random.Generator(np.random.Philox(key=int(seed)))
+
+
+def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
+    """Round float32 values to bf16 (round to nearest, ties to even).
+
+    Returns the bf16 bit patterns as uint16. NaN stays a quiet NaN.
+    """
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    u = x.view(np.uint32).astype(np.uint64)
+    bias = ((u >> 16) & 1) + 0x7FFF
+    out = ((u + bias) >> 16).astype(np.uint16)
+    nan = np.isnan(x)
+    if nan.any():
+        out[nan] = 0x7FC0
+    return out
+
+
+def normal_bf16(gen: np.random.Generator, shape, chunk: int = 1 << 24) -> np.ndarray:
+    """Standard normal values of ``shape`` as bf16 bit patterns (uint16)."""
+    n = int(np.prod(shape, dtype=np.int64))
+    out = np.empty(n, dtype=np.uint16)
+    for s in range(0, n, chunk):
+        c = min(chunk, n - s)
+        out[s:s + c] = f32_to_bf16_bits(gen.standard_normal(c, dtype=np.float32))
+    return out.reshape(shape)
+
+
+@dataclass
+class PagedBatch:
+    """One batch of requests over a paged KV cache (all arrays host numpy)."""
+
+    name: str
+    num_qo_heads: int
+    num_kv_heads: int
+    head_dim: int
+    page_size: int
+    layout: str                  # NHD or HND
+    sm_scale: float
+    causal: bool
+    kv_lens: np.ndarray          # int64 [B]   (what the page table encodes)
+    qo_lens: np.ndarray          # int64 [B]
+    qo_indptr: np.ndarray        # int32 [B+1]
+    page_indptr: np.ndarray      # int32 [B+1]
+    page_indices: np.ndarray     # int32 [nnz]
+    last_page_len: np.ndarray    # int32 [B]
+    q: np.ndarray                # uint16 bf16 bits [sum qo, Hq, d]
+    k_cache: np.ndarray          # uint16 bf16 bits, layout-dependent 4-D
+    v_cache: np.ndarray
+    shared_prefix_pages: int = 0
+    meta: dict = field(default_factory=dict)
+
+    @property
+    def batch(self) -> int:
+        return int(self.kv_lens.shape[0])
+
+    @property
+    def num_pages(self) -> int:
+        return int(self.k_cache.shape[0])
+
+    @property
+    def is_decode(self) -> bool:
+        return bool(np.all(self.qo_lens == 1))
+
+
+def make_batch(name: str, kv_lens, qo_lens, num_qo_heads: int, num_kv_heads: int,
+               head_dim: int, page_size: int, layout: str, sm_scale: float | None,
+               causal: bool, seed: int, shared_prefix_requests: int = 0,
+               shared_prefix_tokens: int = 0, tail_fill: str = "normal",
+               extra_pages: int = 0) -> PagedBatch:
+    """Build a paged batch with seeded values and a shuffled page table.
+
+    ``shared_prefix_requests`` requests (the first ones) map their first
+    ``shared_prefix_tokens // page_size`` logical pages onto the same physical
+    pages. ``tail_fill`` chooses what sits in the unused slots of every last
+    page: "normal" (more random values) or "nan" (quiet NaN bits, to show that
+    nothing past ``last_page_len`` is read). ``extra_pages`` physical pages that
+    no request uses are added to the pool.
+    """
+    gen = philox(seed)
+    kv_lens = np.asarray(kv_lens, dtype=np.int64)
+    qo_lens = np.asarray(qo_lens, dtype=np.int64)
+    B = kv_lens.shape[0]
+    assert qo_lens.shape == (B,)
+    P = page_size
+    npages = np.where(kv_lens > 0, (kv_lens + P - 1) // P, 0)
+    last = np.where(kv_lens > 0, kv_lens - (npages - 1) * P, 0)
+
+    prefix_pages = shared_prefix_tokens // P if shared_prefix_requests else 0
+    if prefix_pages:
+        assert shared_prefix_tokens % P == 0
+        assert np.all(kv_lens[:shared_prefix_requests] >= shared_prefix_tokens)
+    own = npages.copy()
+    own[:shared_prefix_requests] -= prefix_pages
+    num_phys = int(prefix_pages + own.sum()) + int(extra_pages)
+    perm = gen.permutation(num_phys).astype(np.int32)
+
+    page_lists = []
+    cursor = prefix_pages
+    for b in range(B):
+        pl = []
+        if b < shared_prefix_requests and prefix_pages:
+            pl.extend(perm[:prefix_pages].tolist())
+        pl.extend(perm[cursor:cursor + own[b]].tolist())
+        cursor += int(own[b])
+        page_lists.append(pl)
+    page_indptr = np.zeros(B + 1, dtype=np.int32)
+    page_indptr[1:] = np.cumsum([len(p) for p in page_lists])
+    page_indices = np.array([p for pl in page_lists for p in pl], dtype=np.int32)
+    qo_indptr = np.zeros(B + 1, dtype=np.int32)
+    qo_indptr[1:] = np.cumsum(qo_lens)
+
+    Hkv, d = num_kv_heads, head_dim
+    shape = (num_phys, P, Hkv, d) if layout == NHD else (num_phys, Hkv, P, d)
+    k_cache = normal_bf16(gen, shape)
+    v_cache = normal_bf16(gen, shape)
+    q = normal_bf16(gen, (int(qo_lens.sum()), num_qo_heads, d))
+    if tail_fill == "nan":
+        for b in range(B):
+            if npages[b] == 0 or last[b] == P:
+                continue
+            p = page_lists[b][-1]
+            for cache in (k_cache, v_cache):
+                if layout == NHD:
+                    cache[p, last[b]:, :, :] = 0x7FC0
+                else:
+                    cache[p, :, last[b]:, :] = 0x7FC0
+    if sm_scale is None:
+        sm_scale = 1.0 / math.sqrt(head_dim)
+    return PagedBatch(name=name, num_qo_heads=num_qo_heads, num_kv_heads=num_kv_heads,
+                      head_dim=head_dim, page_size=P, layout=layout, sm_scale=float(sm_scale),
+                      causal=bool(causal), kv_lens=kv_lens, qo_lens=qo_lens, qo_indptr=qo_indptr,
+                      page_indptr=page_indptr, page_indices=page_indices,
+                      last_page_len=last.astype(np.int32), q=q, k_cache=k_cache, v_cache=v_cache,
+                      shared_prefix_pages=int(prefix_pages),
+                      meta={"seed": seed, "shared_prefix_requests": shared_prefix_requests})
+
+
+# ----------------------------------------------------------------------------
+# Workloads shaped like the pages' (head shapes of Llama-7B / Llama2-70B,
+# contexts from 1K to 32K).
+# ----------------------------------------------------------------------------
+
+def tiny_decode(seed: int = 0) -> PagedBatch:
+    """4 requests, 8 q / 2 kv heads, d=64, P=16, KV lengths {1,17,64,100}, NHD, scale 1/8."""
+    return make_batch("tiny batch decode B4 Hq8 Hkv2 d64 P16 kv{1,17,64,100} NHD",
+                      [1, 17, 64, 100], [1, 1, 1, 1], 8, 2, 64, 16, NHD, 1.0 / 8, False, seed)
+
+
+def llama7b_decode(seed: int = 1, batch: int = 64) -> PagedBatch:
+    """Llama-7B-shaped decode: 32/32 heads, d=128, P=16, KV ~ U[512,4096], NHD."""
+    g = philox(seed + 1000)
+    kv = g.integers(512, 4097, size=batch)
+    return make_batch(f"Llama-7B-shaped batch decode B{batch} Hq32 Hkv32 d128 P16 kv~U[512,4096] NHD",
+                      kv, np.ones(batch, np.int64), 32, 32, 128, 16, NHD, None, False, seed)
+
+
+def lognormal_lengths(gen, n, median=2048, sigma=1.0, lo=1, hi=32768):
+    x = np.exp(math.log(median) + sigma * gen.standard_normal(n))
+    return np.clip(np.rint(x), lo, hi).astype(np.int64)
+
+
+def llama70b_gqa_decode(seed: int = 2, batch: int = 128, shared: int = 32) -> PagedBatch:
+    """Llama2-70B-shaped GQA decode: 64/8 heads, d=128, P=16, HND,
+    KV ~ lognormal(median 2048, sigma 1) clipped to [1,32768]; the first 32
+    requests share the physical pages of one 1024-token prefix."""
+    g = philox(seed + 1000)
+    kv = lognormal_lengths(g, batch)
+    kv[:shared] = np.maximum(kv[:shared], 1024)
+    return make_batch(f"Llama2-70B-shaped GQA decode B{batch} Hq64 Hkv8 d128 P16 HND lognormal(2048) "
+                      f"{shared} share a 1024-token prefix",
+                      kv, np.ones(batch, np.int64), 64, 8, 128, 16, HND, None, False, seed,
+                      shared_prefix_requests=shared, shared_prefix_tokens=1024)
+
+
+def causal_prefill(seq_len: int, batch: int = 8, seed: int = 3) -> PagedBatch:
+    """Causal prefill, 70B shape: 64/8 heads, d=128, P=16, qo_len = kv_len = seq_len."""
+    L = np.full(batch, seq_len, np.int64)
+    return make_batch(f"causal prefill B{batch} L{seq_len} Hq64 Hkv8 d128 P16 NHD",
+                      L, L, 64, 8, 128, 16, NHD, None, True, seed + seq_len)
+
+
+def ragged_prefill(seed: int = 4, batch: int = 16) -> PagedBatch:
+    """Causal varlen prefill, 70B shape, 16 requests with L ~ U[128,8192]."""
+    g = philox(seed + 1000)
+    L = g.integers(128, 8193, size=batch)
+    return make_batch(f"ragged causal prefill B{batch} L~U[128,8192] Hq64 Hkv8 d128 P16 NHD",
+                      L, L, 64, 8, 128, 16, NHD, None, True, seed)
+
+
+def mixed_chunk_decode(seed: int = 5, chunks: int = 8, decodes: int = 56,
+                       chunk_len: int = 512) -> PagedBatch:
+    """Chunked prefill + decode in one batch: 16/8 heads, d=256, P=32.
+
+    ``chunks`` requests each append a ``chunk_len``-token causal chunk to an
+    existing KV of U[4096,32768] tokens; ``decodes`` requests decode one token
+    against KV ~ U[1,32768]."""
+    g = philox(seed + 1000)
+    existing = g.integers(4096, 32769, size=chunks)
+    dec_kv = g.integers(1, 32769, size=decodes)
+    kv = np.concatenate([existing + chunk_len, dec_kv])
+    qo = np.concatenate([np.full(chunks, chunk_len, np.int64), np.ones(decodes, np.int64)])
+    return make_batch(f"mixed chunked-prefill+decode {chunks}x{chunk_len}-token chunks on U[4K,32K] "
+                      f"+ {decodes} decodes kv~U[1,32K] Hq16 Hkv8 d256 P32 NHD",
+                      kv, qo, 16, 8, 256, 32, NHD, None, True, seed)
+
+
+def small_mixed(seed: int = 6) -> PagedBatch:
+    """The mixed batch at a size the oracle finishes in seconds (same shape rules)."""
+    g = philox(seed + 1000)
+    existing = g.integers(100, 700, size=3)
+    dec_kv = g.integers(1, 900, size=5)
+    kv = np.concatenate([existing + 96, dec_kv])
+    qo = np.concatenate([np.full(3, 96, np.int64), np.ones(5, np.int64)])
+    return make_batch("small mixed chunked-prefill+decode Hq16 Hkv8 d256 P32 NHD",
+                      kv, qo, 16, 8, 256, 32, NHD, None, True, seed)
+
+
+def sub_batch(src: PagedBatch, requests) -> PagedBatch:
+    """Copy the listed requests of ``src`` into a compact batch of their own
+    (pages renumbered densely, order kept). Used to draw bounded samples."""
+    requests = list(requests)
+    pages, pl_lens = [], []
+    for b in requests:
+        lo, hi = int(src.page_indptr[b]), int(src.page_indptr[b + 1])
+        pages.extend(src.page_indices[lo:hi].tolist())
+        pl_lens.append(hi - lo)
+    uniq = sorted(set(pages))
+    remap = {p: i for i, p in enumerate(uniq)}
+    page_indices = np.array([remap[p] for p in pages], dtype=np.int32)
+    page_indptr = np.zeros(len(requests) + 1, np.int32)
+    page_indptr[1:] = np.cumsum(pl_lens)
+    qo_lens = src.qo_lens[requests]
+    qo_indptr = np.zeros(len(requests) + 1, np.int32)
+    qo_indptr[1:] = np.cumsum(qo_lens)
+    q = np.concatenate([src.q[src.qo_indptr[b]:src.qo_indptr[b + 1]] for b in requests], axis=0)
+    idx = np.array(uniq, dtype=np.int64)
+    return PagedBatch(name=src.name + f" [sample of {len(requests)} requests]",
+                      num_qo_heads=src.num_qo_heads, num_kv_heads=src.num_kv_heads,
+                      head_dim=src.head_dim, page_size=src.page_size, layout=src.layout,
+                      sm_scale=src.sm_scale, causal=src.causal, kv_lens=src.kv_lens[requests].copy(),
+                      qo_lens=qo_lens.copy(), qo_indptr=qo_indptr, page_indptr=page_indptr,
+                      page_indices=page_indices, last_page_len=src.last_page_len[requests].copy(),
+                      q=q, k_cache=src.k_cache[idx], v_cache=src.v_cache[idx],
+                      meta=dict(src.meta, sample=requests))
