@@ -1,0 +1,258 @@
+/*
+ * fi.h — C ABI of the paged-KV attention library (libfi.so), GB300 / sm_103a.
+ *
+ * The library computes attention over a paged KV cache,
+ *     O = softmax(sm_scale * Q K^T + mask) V        (per query head),
+ * with the K/V rows of each request reached through a page table. The
+ * source pages describe the problem, not a C interface:
+ *   - "FlashInfer kernel library deep-dive", section "PageAttention": the KV
+ *     cache is cut into fixed-size pages allocated on demand;
+ *   - same page, section "KV cache layout": the NHD and HND layouts;
+ *   - same page, section "core API usage": single/batch decode and batch
+ *     prefill entry points;
+ *   - "FlashAttention-3 kernel integration in inference engines", section 2:
+ *     variable-length prefill over prefix-sum offsets (cu_seqlens), causal
+ *     flag, softmax_scale defaulting to 1/sqrt(head_dim), continuous
+ *     batching with chunked prefill over paged KV;
+ *   - "FlashInfer Attention Kernel optimisation analysis", section 2.2:
+ *     scheduling by sequence length (here: the host planner splits long KV
+ *     across CTAs and the partial results are merged by log-sum-exp).
+ *
+ * Conventions used by every call below
+ * ------------------------------------
+ * Page table (CSR, int32): request b owns page_indices[page_indptr[b] ..
+ *   page_indptr[b+1]-1]; every page is full except the last, which holds
+ *   last_page_len[b] in [1, page_size] tokens. kv_len[b] =
+ *   (n_pages-1)*page_size + last_page_len[b], or 0 for a request with no
+ *   pages (its last_page_len is then ignored). Key t of request b lives on
+ *   page page_indices[page_indptr[b] + t/page_size], slot t%page_size.
+ * KV layouts (bf16): FI_LAYOUT_NHD = [page][slot][kv_head][dim],
+ *   FI_LAYOUT_HND = [page][kv_head][slot][dim]. K and V are separate
+ *   buffers of the same layout; page_stride_elems is the distance between
+ *   consecutive pages in elements (0 = dense: page_size*num_kv_heads*head_dim),
+ *   so K and V may also be two views into one [num_pages][2][...] buffer.
+ * Heads: num_qo_heads = g * num_kv_heads; query head h reads kv head h/g.
+ * Queries (bf16): decode q is [batch][num_qo_heads][head_dim]; prefill q is
+ *   the ragged packing [sum qo_len][num_qo_heads][head_dim] with request b
+ *   on rows qo_indptr[b] .. qo_indptr[b+1]-1. out has q's shape (bf16).
+ * Causal (prefill): row i of a request with qo_len rows sees keys
+ *   t <= kv_len - qo_len + i (the chunk's queries are the last qo_len
+ *   positions of its KV); qo_len > kv_len is rejected.
+ * lse (fp32, optional, may be NULL): natural log of the sum over visible
+ *   keys of exp(sm_scale * <q,k>). A row with no visible key gets out = 0
+ *   and lse = -inf.
+ * Supported shapes: head_dim in {64, 128, 256}; page_size in {16, 32};
+ *   g in {1, 2, 4, 8}. Anything else returns FI_ERR_UNSUPPORTED.
+ * Memory: every device buffer (inputs, outputs, workspace) is owned by the
+ *   caller. The run calls allocate nothing. A plan owns host memory only.
+ * Streams: `stream` is a cudaStream_t (NULL = the legacy default stream).
+ *   Every run call is asynchronous and stream-ordered; host-side argument
+ *   errors are returned before anything is enqueued.
+ * Device errors: kernels never trap and never wait without a bound. A
+ *   page index outside [0, num_pages) is skipped and recorded; a bounded
+ *   wait that runs out is recorded. fi_check_device_status() reports
+ *   either after the stream has been synchronised.
+ */
+#ifndef FI_H
+#define FI_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  FI_OK = 0,
+  FI_ERR_INVALID_ARG = 1,         /* malformed sizes, page table or pointers */
+  FI_ERR_UNSUPPORTED = 2,         /* valid but not built: head_dim, page_size, g */
+  FI_ERR_WORKSPACE_TOO_SMALL = 3, /* workspace_bytes below what fi_plan asked for */
+  FI_ERR_CUDA = 4,                /* a CUDA call failed; see fi_last_error_string() */
+  FI_ERR_DEVICE_TIMEOUT = 5,      /* a kernel's bounded wait ran out */
+  FI_ERR_DEVICE_BOUNDS = 6,       /* a kernel met a page index outside the cache */
+  FI_ERR_NO_DEVICE = 7            /* no usable CUDA device for a run call */
+} fi_status;
+
+typedef enum { FI_LAYOUT_NHD = 0, FI_LAYOUT_HND = 1 } fi_kv_layout;
+typedef enum { FI_MODE_DECODE = 0, FI_MODE_PREFILL = 1 } fi_mode;
+
+typedef struct fi_plan_s* fi_plan_t;
+
+/* Summary of a plan, for logging and tests. */
+typedef struct {
+  int32_t mode;             /* fi_mode */
+  int32_t batch_size;
+  int32_t num_items;        /* CTAs of the main attention launch(es) */
+  int32_t num_decode_items; /* of which single-row (decode) work */
+  int32_t num_prefill_items;
+  int32_t chunk_tokens;     /* split-KV chunk length of decode work (0 = no split) */
+  int32_t num_split_requests;
+  int32_t num_partial_slots;/* rows of fp32 partial states in the workspace */
+  int64_t workspace_bytes;
+  int64_t total_kv_tokens;  /* sum of kv_len */
+} fi_plan_info;
+
+/*
+ * fi_plan — host-side planning of one batch (no CUDA call, no device memory).
+ *
+ * Reads the host copies of the page table (and, for prefill, qo_indptr),
+ * validates them, decides how each request's KV is split across CTAs for
+ * load balance ("FlashInfer Attention Kernel optimisation analysis",
+ * section 2.2; "FlashInfer kernel library deep-dive", section
+ * "load-balanced scheduling"), builds the work list and sizes the
+ * workspace the run calls need.
+ *   mode             FI_MODE_DECODE (one query row per request; qo_indptr_h
+ *                    must be NULL) or FI_MODE_PREFILL (qo_indptr_h required;
+ *                    requests with one row are planned as decode work).
+ *   batch_size       number of requests B >= 0 (0 gives an empty plan).
+ *   qo_indptr_h      host int32 [B+1], non-decreasing, qo_indptr_h[0] == 0.
+ *   page_indptr_h    host int32 [B+1], non-decreasing, page_indptr_h[0] >= 0.
+ *   last_page_len_h  host int32 [B].
+ *   causal           prefill only; ignored for decode.
+ *   num_sms          SMs of the device the plan will run on (>0).
+ *   out_plan         receives the plan; free it with fi_plan_destroy.
+ *   workspace_bytes  receives the device workspace size the runs need.
+ * The device copies of the same arrays passed to a run must hold the same
+ * values (caller contract). A plan is immutable and may be run any number
+ * of times, with any inputs of the same page-table structure.
+ * Errors: FI_ERR_INVALID_ARG (NULL pointers, negative sizes, decreasing
+ * indptr, last_page_len outside [1,page_size] for a request with pages,
+ * causal with qo_len > kv_len, num_qo_heads not a multiple of
+ * num_kv_heads), FI_ERR_UNSUPPORTED (head_dim, page_size or g not built).
+ */
+fi_status fi_plan(int32_t mode, int32_t batch_size, const int32_t* qo_indptr_h,
+                  const int32_t* page_indptr_h, const int32_t* last_page_len_h,
+                  int32_t num_qo_heads, int32_t num_kv_heads, int32_t head_dim,
+                  int32_t page_size, int32_t causal, int32_t num_sms,
+                  fi_plan_t* out_plan, size_t* workspace_bytes);
+
+/* Frees a plan (NULL is accepted). */
+fi_status fi_plan_destroy(fi_plan_t plan);
+
+/* Copies a summary of the plan into *info. */
+fi_status fi_plan_get_info(fi_plan_t plan, fi_plan_info* info);
+
+/*
+ * Copies the plan's work list to host memory: 8 int32 per item, in launch
+ * order: {request, kv_head (decode) or qo_head (prefill), first page index
+ * (into page_indices), number of pages, first token, end token, partial
+ * slot or -1, first query row within the request (prefill) or 0}.
+ * `capacity` is in items; *num_items receives the plan's item count.
+ */
+fi_status fi_plan_get_work(fi_plan_t plan, int32_t* items_h, int32_t capacity,
+                           int32_t* num_items);
+
+/*
+ * fi_batch_decode_paged — batch decode over a paged KV cache.
+ *
+ * One query token per request ("FlashInfer kernel library deep-dive",
+ * sections "single-request layer" and "batch layer"): for every request b
+ * and query head h, out[b][h] = softmax(sm_scale * q[b][h] K_b^T) V_b over
+ * all kv_len[b] keys of kv head h/g. Each K/V page is loaded once and
+ * shared by the g query heads of its group. Long requests are split over
+ * several CTAs as the plan says; their fp32 partial states are merged by
+ * log-sum-exp into out/lse before the call's work completes on the stream.
+ *   plan             from fi_plan(FI_MODE_DECODE, ...).
+ *   q                device bf16 [B][num_qo_heads][head_dim].
+ *   k_cache, v_cache device bf16 paged caches (layout, page_stride_elems
+ *                    as in the conventions above), num_pages pages each.
+ *   page_indptr_d, page_indices_d, last_page_len_d  device int32 copies of
+ *                    the planned page table.
+ *   sm_scale         score scale (1/sqrt(head_dim) is the usual value).
+ *   out              device bf16 [B][num_qo_heads][head_dim].
+ *   lse              device fp32 [B][num_qo_heads] or NULL.
+ *   workspace        device buffer of at least the planned size, 256-byte
+ *                    aligned; its contents between calls belong to the
+ *                    library (it caches the uploaded work list there).
+ * Errors: FI_ERR_INVALID_ARG (NULL or misaligned pointers — q, caches and
+ * out need 16-byte alignment —, a plan of the other mode, page_stride_elems
+ * not a multiple of 8), FI_ERR_WORKSPACE_TOO_SMALL, FI_ERR_NO_DEVICE,
+ * FI_ERR_CUDA (launch failure).
+ */
+fi_status fi_batch_decode_paged(fi_plan_t plan, const void* q, const void* k_cache,
+                                const void* v_cache, int32_t kv_layout,
+                                int64_t page_stride_elems, int32_t num_pages,
+                                const int32_t* page_indptr_d, const int32_t* page_indices_d,
+                                const int32_t* last_page_len_d, float sm_scale, void* out,
+                                float* lse, void* workspace, size_t workspace_bytes,
+                                void* stream);
+
+/*
+ * fi_batch_prefill_paged — causal (or full) variable-length batch prefill
+ * over a paged KV cache, the varlen form of "FlashAttention-3 kernel
+ * integration in inference engines", section 2 (cu_seqlens_q is
+ * qo_indptr; the keys come from the page table instead of cu_seqlens_k).
+ * Requests may mix prompt chunks and single decode rows in one call
+ * (continuous batching with chunked prefill, same section).
+ *   plan         from fi_plan(FI_MODE_PREFILL, ...); carries `causal`.
+ *   q            device bf16 [sum qo_len][num_qo_heads][head_dim].
+ *   qo_indptr_d  device int32 copy of the planned qo_indptr.
+ *   other arguments as for fi_batch_decode_paged; out has q's shape and
+ *   lse is fp32 [sum qo_len][num_qo_heads] or NULL.
+ * Errors: as for fi_batch_decode_paged.
+ */
+fi_status fi_batch_prefill_paged(fi_plan_t plan, const void* q, const int32_t* qo_indptr_d,
+                                 const void* k_cache, const void* v_cache, int32_t kv_layout,
+                                 int64_t page_stride_elems, int32_t num_pages,
+                                 const int32_t* page_indptr_d, const int32_t* page_indices_d,
+                                 const int32_t* last_page_len_d, float sm_scale, void* out,
+                                 float* lse, void* workspace, size_t workspace_bytes,
+                                 void* stream);
+
+/*
+ * fi_merge_states — combine attention states computed over disjoint key
+ * sets (split-KV partials) by log-sum-exp. The pages do not spell this
+ * step out; it is the standard identity behind tiled online softmax
+ * ("FlashAttention-3 kernel integration in inference engines", section 1:
+ * softmax aggregated in place across tiles). For row r, head h:
+ *   M = max_i s[r][i][h];  w_i = exp(s[r][i][h] - M);
+ *   out[r][h] = sum_i w_i v[r][i][h] / sum_i w_i;  lse = M + ln sum_i w_i.
+ * States with s = -inf weigh nothing; if all are -inf, out = 0, lse = -inf.
+ *   v        device fp32 [n][S][H][d];   s  device fp32 [n][S][H].
+ *   out      device bf16 [n][H][d] (16-byte aligned); lse_out fp32 [n][H] or NULL.
+ *   d        multiple of 4, at most 1024; n, S, H >= 0 (n == 0 or H == 0: no-op).
+ * Errors: FI_ERR_INVALID_ARG, FI_ERR_NO_DEVICE, FI_ERR_CUDA.
+ */
+fi_status fi_merge_states(const float* v, const float* s, int32_t n, int32_t S, int32_t H,
+                          int32_t d, void* out, float* lse_out, void* stream);
+
+/*
+ * fi_check_device_status — synchronises `stream`, reads and clears the
+ * device error word kept at the start of `workspace` by the runs that used
+ * it. Returns FI_OK, FI_ERR_DEVICE_TIMEOUT (a bounded wait ran out) or
+ * FI_ERR_DEVICE_BOUNDS (a page index outside the cache was skipped), or
+ * FI_ERR_CUDA if the synchronisation itself failed.
+ */
+fi_status fi_check_device_status(void* workspace, void* stream);
+
+/* Static description of a status code. */
+const char* fi_status_string(fi_status status);
+
+/* Message of the last CUDA error seen by this thread's calls (or ""). */
+const char* fi_last_error_string(void);
+
+/*
+ * Test hook for the failure path. kind 0 = normal operation; kind 1 = the
+ * next decode launch's producer skips its first tile load, so that the
+ * consumers' bounded wait runs out after about `wait_limit` polls and the
+ * kernel reports FI_ERR_DEVICE_TIMEOUT instead of hanging. wait_limit <= 0
+ * restores the default bound. Not thread-safe; meant for tests only.
+ */
+fi_status fi_debug_set_fault(int32_t kind, int64_t wait_limit);
+
+/*
+ * Profiling hook: the next paged run call made by this thread records
+ * start_event (a cudaEvent_t) on its stream just before its first attention
+ * kernel and stop_event just after its last attention kernel (before any
+ * merge), so that a caller can time the main kernel alone with
+ * cudaEventElapsedTime. One-shot; NULL for both clears a pending request.
+ * Errors from the event records are returned by that run call as FI_ERR_CUDA.
+ */
+fi_status fi_profile_next_launch(void* start_event, void* stop_event);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FI_H */

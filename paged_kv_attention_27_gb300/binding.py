@@ -1,0 +1,227 @@
+"""ctypes binding of libfi.so: the C ABI of include/fi.h under the same names.
+
+Argument marshalling only. Device buffers may be torch tensors (their
+``data_ptr()`` is passed), raw integer addresses or None (NULL); host arrays
+for ``fi_plan`` are numpy arrays (converted to contiguous int32). Every
+computation happens in the library's CUDA kernels; if the library has not
+been built, loading it raises instead of falling back to anything.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import numpy as np
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "lib", "libfi.so")
+
+FI_OK = 0
+FI_ERR_INVALID_ARG = 1
+FI_ERR_UNSUPPORTED = 2
+FI_ERR_WORKSPACE_TOO_SMALL = 3
+FI_ERR_CUDA = 4
+FI_ERR_DEVICE_TIMEOUT = 5
+FI_ERR_DEVICE_BOUNDS = 6
+FI_ERR_NO_DEVICE = 7
+
+FI_LAYOUT_NHD = 0
+FI_LAYOUT_HND = 1
+FI_MODE_DECODE = 0
+FI_MODE_PREFILL = 1
+
+LAYOUTS = {"NHD": FI_LAYOUT_NHD, "HND": FI_LAYOUT_HND}
+
+# every symbol include/fi.h declares
+EXPORTED = ["fi_plan", "fi_plan_destroy", "fi_plan_get_info", "fi_plan_get_work",
+            "fi_batch_decode_paged", "fi_batch_prefill_paged", "fi_merge_states",
+            "fi_check_device_status", "fi_status_string", "fi_last_error_string",
+            "fi_debug_set_fault", "fi_profile_next_launch"]
+
+
+class FiError(RuntimeError):
+    def __init__(self, status: int, where: str, detail: str = ""):
+        self.status = status
+        msg = f"{where}: {status_string(status)} ({status})"
+        if detail:
+            msg += f": {detail}"
+        super().__init__(msg)
+
+
+class PlanInfo(ctypes.Structure):
+    _fields_ = [("mode", ctypes.c_int32), ("batch_size", ctypes.c_int32),
+                ("num_items", ctypes.c_int32), ("num_decode_items", ctypes.c_int32),
+                ("num_prefill_items", ctypes.c_int32), ("chunk_tokens", ctypes.c_int32),
+                ("num_split_requests", ctypes.c_int32), ("num_partial_slots", ctypes.c_int32),
+                ("workspace_bytes", ctypes.c_int64), ("total_kv_tokens", ctypes.c_int64)]
+
+
+_lib = None
+_P = ctypes.c_void_p
+_I32 = ctypes.c_int32
+_I64 = ctypes.c_int64
+
+
+def lib():
+    """Load libfi.so once; raises if it has not been built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(f"{LIB_PATH} is missing: build it with "
+                           "paged_kv_attention_27_gb300.build.build() first")
+    L = ctypes.CDLL(LIB_PATH)
+    L.fi_plan.argtypes = [_I32, _I32, _P, _P, _P, _I32, _I32, _I32, _I32, _I32, _I32,
+                          ctypes.POINTER(_P), ctypes.POINTER(ctypes.c_size_t)]
+    L.fi_plan_destroy.argtypes = [_P]
+    L.fi_plan_get_info.argtypes = [_P, ctypes.POINTER(PlanInfo)]
+    L.fi_plan_get_work.argtypes = [_P, _P, _I32, ctypes.POINTER(_I32)]
+    L.fi_batch_decode_paged.argtypes = [_P, _P, _P, _P, _I32, _I64, _I32, _P, _P, _P,
+                                        ctypes.c_float, _P, _P, _P, ctypes.c_size_t, _P]
+    L.fi_batch_prefill_paged.argtypes = [_P, _P, _P, _P, _P, _I32, _I64, _I32, _P, _P, _P,
+                                         ctypes.c_float, _P, _P, _P, ctypes.c_size_t, _P]
+    L.fi_merge_states.argtypes = [_P, _P, _I32, _I32, _I32, _I32, _P, _P, _P]
+    L.fi_check_device_status.argtypes = [_P, _P]
+    L.fi_status_string.argtypes = [_I32]
+    L.fi_status_string.restype = ctypes.c_char_p
+    L.fi_last_error_string.argtypes = []
+    L.fi_last_error_string.restype = ctypes.c_char_p
+    L.fi_debug_set_fault.argtypes = [_I32, _I64]
+    L.fi_profile_next_launch.argtypes = [_P, _P]
+    for name in EXPORTED:
+        if name not in ("fi_status_string", "fi_last_error_string"):
+            getattr(L, name).restype = _I32
+    _lib = L
+    return L
+
+
+def status_string(status: int) -> str:
+    return lib().fi_status_string(int(status)).decode()
+
+
+def last_error_string() -> str:
+    return lib().fi_last_error_string().decode()
+
+
+def _check(status: int, where: str):
+    if status != FI_OK:
+        raise FiError(status, where, last_error_string() if status == FI_ERR_CUDA else "")
+
+
+def _ptr(x):
+    """Device/host address of a tensor, numpy array, int, or None."""
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    if hasattr(x, "data_ptr"):
+        return x.data_ptr()
+    if isinstance(x, np.ndarray):
+        return x.ctypes.data
+    raise TypeError(f"cannot take the address of {type(x)}")
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if hasattr(stream, "cuda_stream"):
+        return stream.cuda_stream
+    return stream
+
+
+def _i32(a):
+    return None if a is None else np.ascontiguousarray(a, dtype=np.int32)
+
+
+class Plan:
+    """Owns an fi_plan_t handle (destroyed with the object)."""
+
+    def __init__(self, handle: int, workspace_bytes: int):
+        self.handle = handle
+        self.workspace_bytes = workspace_bytes
+
+    def __del__(self):
+        if self.handle and _lib is not None:
+            _lib.fi_plan_destroy(self.handle)
+            self.handle = None
+
+
+def fi_plan(mode, batch_size, qo_indptr_h, page_indptr_h, last_page_len_h, num_qo_heads,
+            num_kv_heads, head_dim, page_size, causal, num_sms) -> Plan:
+    qo, pi, lp = _i32(qo_indptr_h), _i32(page_indptr_h), _i32(last_page_len_h)
+    h = _P()
+    ws = ctypes.c_size_t()
+    st = lib().fi_plan(int(mode), int(batch_size), _ptr(qo), _ptr(pi), _ptr(lp), int(num_qo_heads),
+                       int(num_kv_heads), int(head_dim), int(page_size), int(bool(causal)),
+                       int(num_sms), ctypes.byref(h), ctypes.byref(ws))
+    _check(st, "fi_plan")
+    return Plan(h.value, ws.value)
+
+
+def fi_plan_destroy(plan: Plan):
+    if plan.handle:
+        _check(lib().fi_plan_destroy(plan.handle), "fi_plan_destroy")
+        plan.handle = None
+
+
+def fi_plan_get_info(plan: Plan) -> dict:
+    info = PlanInfo()
+    _check(lib().fi_plan_get_info(plan.handle, ctypes.byref(info)), "fi_plan_get_info")
+    return {k: getattr(info, k) for k, _ in PlanInfo._fields_}
+
+
+def fi_plan_get_work(plan: Plan) -> np.ndarray:
+    n = _I32()
+    _check(lib().fi_plan_get_work(plan.handle, None, 0, ctypes.byref(n)), "fi_plan_get_work")
+    out = np.zeros((max(n.value, 1), 8), dtype=np.int32)
+    _check(lib().fi_plan_get_work(plan.handle, out.ctypes.data, n.value, ctypes.byref(n)),
+           "fi_plan_get_work")
+    return out[:n.value]
+
+
+def fi_batch_decode_paged(plan: Plan, q, k_cache, v_cache, kv_layout, page_stride_elems,
+                          num_pages, page_indptr_d, page_indices_d, last_page_len_d, sm_scale,
+                          out, lse, workspace, workspace_bytes=None, stream=None):
+    wsb = plan.workspace_bytes if workspace_bytes is None else workspace_bytes
+    st = lib().fi_batch_decode_paged(plan.handle, _ptr(q), _ptr(k_cache), _ptr(v_cache),
+                                     int(kv_layout), int(page_stride_elems), int(num_pages),
+                                     _ptr(page_indptr_d), _ptr(page_indices_d),
+                                     _ptr(last_page_len_d), float(sm_scale), _ptr(out), _ptr(lse),
+                                     _ptr(workspace), int(wsb), _stream(stream))
+    _check(st, "fi_batch_decode_paged")
+
+
+def fi_batch_prefill_paged(plan: Plan, q, qo_indptr_d, k_cache, v_cache, kv_layout,
+                           page_stride_elems, num_pages, page_indptr_d, page_indices_d,
+                           last_page_len_d, sm_scale, out, lse, workspace, workspace_bytes=None,
+                           stream=None):
+    wsb = plan.workspace_bytes if workspace_bytes is None else workspace_bytes
+    st = lib().fi_batch_prefill_paged(plan.handle, _ptr(q), _ptr(qo_indptr_d), _ptr(k_cache),
+                                      _ptr(v_cache), int(kv_layout), int(page_stride_elems),
+                                      int(num_pages), _ptr(page_indptr_d), _ptr(page_indices_d),
+                                      _ptr(last_page_len_d), float(sm_scale), _ptr(out),
+                                      _ptr(lse), _ptr(workspace), int(wsb), _stream(stream))
+    _check(st, "fi_batch_prefill_paged")
+
+
+def fi_merge_states(v, s, n, S, H, d, out, lse_out, stream=None):
+    st = lib().fi_merge_states(_ptr(v), _ptr(s), int(n), int(S), int(H), int(d), _ptr(out),
+                               _ptr(lse_out), _stream(stream))
+    _check(st, "fi_merge_states")
+
+
+def fi_check_device_status(workspace, stream=None) -> int:
+    """Returns the status code (does not raise on device-side errors)."""
+    return lib().fi_check_device_status(_ptr(workspace), _stream(stream))
+
+
+def fi_debug_set_fault(kind: int, wait_limit_ns: int = 0):
+    _check(lib().fi_debug_set_fault(int(kind), int(wait_limit_ns)), "fi_debug_set_fault")
+
+
+def fi_profile_next_launch(start_event, stop_event):
+    """torch.cuda.Event objects (or raw cudaEvent_t addresses, or None)."""
+    sp = start_event.cuda_event if hasattr(start_event, "cuda_event") else start_event
+    ep = stop_event.cuda_event if hasattr(stop_event, "cuda_event") else stop_event
+    _check(lib().fi_profile_next_launch(sp, ep), "fi_profile_next_launch")

@@ -1,0 +1,359 @@
+// The C ABI (include/fi.h): argument validation, tensor-map construction,
+// work-list upload and kernel launches. Every numeric step runs in the
+// CUDA kernels; this file only checks arguments and enqueues work.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <cstring>
+#include <mutex>
+#include <new>
+#include <string>
+
+#include "fi_internal.h"
+#include "kernels.cuh"
+
+namespace {
+
+thread_local std::string g_last_error;
+int32_t g_fault_kind = 0;
+uint64_t g_wait_limit_ns = fi::kDefaultWaitLimitNs;
+thread_local cudaEvent_t g_prof_start = nullptr, g_prof_stop = nullptr;
+
+fi_status cuda_fail(cudaError_t e, const char* what) {
+  g_last_error = std::string(what) + ": " + cudaGetErrorString(e);
+  return FI_ERR_CUDA;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// Tensor map over a paged K or V cache that fetches one (page, kv head)
+// block of page_size rows x 64 dims (128 bytes, 128-byte swizzled) per box.
+fi_status make_kv_map(CUtensorMap* map, const void* base, int layout, int num_pages, int P,
+                      int Hkv, int d, int64_t page_stride) {
+  auto enc = encode_fn();
+  if (!enc) {
+    g_last_error = "cuTensorMapEncodeTiled is not available from the driver";
+    return FI_ERR_CUDA;
+  }
+  cuuint64_t dims[4];
+  cuuint64_t strides[3];
+  cuuint32_t box[4];
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  if (layout == FI_LAYOUT_NHD) {
+    dims[0] = d; dims[1] = Hkv; dims[2] = P; dims[3] = num_pages;
+    strides[0] = cuuint64_t(d) * 2;
+    strides[1] = cuuint64_t(Hkv) * d * 2;
+    box[0] = 64; box[1] = 1; box[2] = P; box[3] = 1;
+  } else {
+    dims[0] = d; dims[1] = P; dims[2] = Hkv; dims[3] = num_pages;
+    strides[0] = cuuint64_t(d) * 2;
+    strides[1] = cuuint64_t(P) * d * 2;
+    box[0] = 64; box[1] = P; box[2] = 1; box[3] = 1;
+  }
+  strides[2] = cuuint64_t(page_stride) * 2;
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims,
+                   strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    g_last_error = "cuTensorMapEncodeTiled failed for the KV cache (code " + std::to_string(int(r)) + ")";
+    return FI_ERR_CUDA;
+  }
+  return FI_OK;
+}
+
+fi_status check_device() {
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    g_last_error = std::string("no CUDA device: ") + cudaGetErrorString(e);
+    return FI_ERR_NO_DEVICE;
+  }
+  return FI_OK;
+}
+
+// Shared body of the two paged run calls.
+fi_status run_paged(fi_plan_t plan, bool prefill_call, const void* q, const int32_t* qo_indptr_d,
+                    const void* k_cache, const void* v_cache, int32_t kv_layout,
+                    int64_t page_stride_elems, int32_t num_pages, const int32_t* page_indptr_d,
+                    const int32_t* page_indices_d, const int32_t* last_page_len_d, float sm_scale,
+                    void* out, float* lse, void* workspace, size_t workspace_bytes,
+                    void* stream_ptr) {
+  if (!plan) return FI_ERR_INVALID_ARG;
+  const fi::Plan& P = plan->p;
+  if (P.mode != (prefill_call ? FI_MODE_PREFILL : FI_MODE_DECODE)) return FI_ERR_INVALID_ARG;
+  if (P.batch == 0) return FI_OK;
+  if (!q || !k_cache || !v_cache || !out || !workspace || !page_indptr_d || !last_page_len_d)
+    return FI_ERR_INVALID_ARG;
+  if (prefill_call && !qo_indptr_d) return FI_ERR_INVALID_ARG;
+  if (P.total_kv > 0 && (!page_indices_d || num_pages <= 0)) return FI_ERR_INVALID_ARG;
+  if (num_pages < 0) return FI_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16) ||
+      !aligned(workspace, 256) || (lse && !aligned(lse, 4)))
+    return FI_ERR_INVALID_ARG;
+  if (kv_layout != FI_LAYOUT_NHD && kv_layout != FI_LAYOUT_HND) return FI_ERR_INVALID_ARG;
+  const int64_t page_elems = int64_t(P.page_size) * P.num_kv_heads * P.head_dim;
+  if (page_stride_elems == 0) page_stride_elems = page_elems;
+  if (page_stride_elems < page_elems || page_stride_elems % 8 != 0) return FI_ERR_INVALID_ARG;
+  if (workspace_bytes < P.ws.total) return FI_ERR_WORKSPACE_TOO_SMALL;
+  fi_status st = check_device();
+  if (st != FI_OK) return st;
+
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+
+  // Upload header (zeroed error word) + work lists + merge tasks in one copy.
+  const auto& image = plan->image;
+  cudaError_t e = cudaMemcpyAsync(ws, image.data(), image.size(), cudaMemcpyHostToDevice, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "work-list upload");
+
+  CUtensorMap kmap, vmap;
+  if (P.total_kv > 0) {
+    st = make_kv_map(&kmap, k_cache, kv_layout, num_pages, P.page_size, P.num_kv_heads,
+                     P.head_dim, page_stride_elems);
+    if (st != FI_OK) return st;
+    st = make_kv_map(&vmap, v_cache, kv_layout, num_pages, P.page_size, P.num_kv_heads,
+                     P.head_dim, page_stride_elems);
+    if (st != FI_OK) return st;
+  } else {
+    std::memset(&kmap, 0, sizeof(kmap));
+    std::memset(&vmap, 0, sizeof(vmap));
+  }
+  uint32_t* err = reinterpret_cast<uint32_t*>(ws);
+  float* partial_o = reinterpret_cast<float*>(ws + P.ws.partial_o);
+  float* partial_lse = reinterpret_cast<float*>(ws + P.ws.partial_lse);
+
+  if (!P.prefill_items.empty()) {
+    g_last_error = "prefill work items are not supported by this build";
+    return FI_ERR_UNSUPPORTED;
+  }
+
+  cudaEvent_t prof_start = g_prof_start, prof_stop = g_prof_stop;
+  g_prof_start = g_prof_stop = nullptr;
+  if (prof_start) {
+    e = cudaEventRecord(prof_start, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "profiling event");
+  }
+
+  if (!P.decode_items.empty()) {
+    fi::DecodeParams dp;
+    dp.items = reinterpret_cast<const fi::WorkItem*>(ws + P.ws.decode_items);
+    dp.q = q;
+    dp.page_indices = page_indices_d;
+    dp.num_pages = num_pages;
+    dp.page_size = P.page_size;
+    dp.num_qo_heads = P.num_qo_heads;
+    dp.layout = kv_layout;
+    dp.sm_scale = sm_scale;
+    dp.out = out;
+    dp.lse = lse;
+    dp.partial_o = partial_o;
+    dp.partial_lse = partial_lse;
+    dp.err = err;
+    dp.wait_limit_ns = g_wait_limit_ns;
+    dp.fault_kind = g_fault_kind;
+    g_fault_kind = 0;  // one-shot
+    e = fi::launch_decode(P.head_dim, P.num_qo_heads / P.num_kv_heads, kmap, vmap, dp,
+                          int(P.decode_items.size()), stream);
+    if (e != cudaSuccess) return cuda_fail(e, "decode launch");
+  }
+  if (prof_stop) {
+    e = cudaEventRecord(prof_stop, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "profiling event");
+  }
+  if (!P.merges.empty()) {
+    fi::MergeParams mp;
+    mp.v = partial_o;
+    mp.s = partial_lse;
+    mp.tasks = reinterpret_cast<const fi::MergeTask*>(ws + P.ws.merges);
+    mp.S = 0;
+    mp.H = P.num_qo_heads;
+    mp.d = P.head_dim;
+    mp.out = out;
+    mp.lse = lse;
+    e = fi::launch_merge(mp, int(P.merges.size()), stream);
+    if (e != cudaSuccess) return cuda_fail(e, "merge launch");
+  }
+  return FI_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+fi_status fi_plan(int32_t mode, int32_t batch_size, const int32_t* qo_indptr_h,
+                  const int32_t* page_indptr_h, const int32_t* last_page_len_h,
+                  int32_t num_qo_heads, int32_t num_kv_heads, int32_t head_dim,
+                  int32_t page_size, int32_t causal, int32_t num_sms, fi_plan_t* out_plan,
+                  size_t* workspace_bytes) {
+  if (!out_plan || !workspace_bytes) return FI_ERR_INVALID_ARG;
+  *out_plan = nullptr;
+  fi_plan_s* p = new (std::nothrow) fi_plan_s;
+  if (!p) return FI_ERR_INVALID_ARG;
+  fi_status st = fi::build_plan(mode, batch_size, qo_indptr_h, page_indptr_h, last_page_len_h,
+                                num_qo_heads, num_kv_heads, head_dim, page_size, causal, num_sms,
+                                &p->p);
+  if (st != FI_OK) {
+    delete p;
+    return st;
+  }
+  // Host image of the workspace prefix: zeroed header, work lists, merge tasks.
+  const fi::Plan& P = p->p;
+  p->image.assign(P.ws.partial_o, 0);
+  if (!P.decode_items.empty())
+    std::memcpy(p->image.data() + P.ws.decode_items, P.decode_items.data(),
+                P.decode_items.size() * sizeof(fi::WorkItem));
+  if (!P.prefill_items.empty())
+    std::memcpy(p->image.data() + P.ws.prefill_items, P.prefill_items.data(),
+                P.prefill_items.size() * sizeof(fi::WorkItem));
+  if (!P.merges.empty())
+    std::memcpy(p->image.data() + P.ws.merges, P.merges.data(),
+                P.merges.size() * sizeof(fi::MergeTask));
+  *out_plan = p;
+  *workspace_bytes = P.ws.total;
+  return FI_OK;
+}
+
+fi_status fi_plan_destroy(fi_plan_t plan) {
+  delete plan;
+  return FI_OK;
+}
+
+fi_status fi_plan_get_info(fi_plan_t plan, fi_plan_info* info) {
+  if (!plan || !info) return FI_ERR_INVALID_ARG;
+  const fi::Plan& P = plan->p;
+  info->mode = P.mode;
+  info->batch_size = P.batch;
+  info->num_decode_items = int32_t(P.decode_items.size());
+  info->num_prefill_items = int32_t(P.prefill_items.size());
+  info->num_items = info->num_decode_items + info->num_prefill_items;
+  info->chunk_tokens = P.chunk_tokens;
+  info->num_split_requests = P.num_split;
+  info->num_partial_slots = P.num_slots;
+  info->workspace_bytes = int64_t(P.ws.total);
+  info->total_kv_tokens = P.total_kv;
+  return FI_OK;
+}
+
+fi_status fi_plan_get_work(fi_plan_t plan, int32_t* items_h, int32_t capacity,
+                           int32_t* num_items) {
+  if (!plan || !num_items) return FI_ERR_INVALID_ARG;
+  const fi::Plan& P = plan->p;
+  const int32_t n = int32_t(P.decode_items.size() + P.prefill_items.size());
+  *num_items = n;
+  if (!items_h) return FI_OK;
+  if (capacity < n) return FI_ERR_INVALID_ARG;
+  std::memcpy(items_h, P.decode_items.data(), P.decode_items.size() * sizeof(fi::WorkItem));
+  std::memcpy(items_h + 8 * P.decode_items.size(), P.prefill_items.data(),
+              P.prefill_items.size() * sizeof(fi::WorkItem));
+  return FI_OK;
+}
+
+fi_status fi_batch_decode_paged(fi_plan_t plan, const void* q, const void* k_cache,
+                                const void* v_cache, int32_t kv_layout,
+                                int64_t page_stride_elems, int32_t num_pages,
+                                const int32_t* page_indptr_d, const int32_t* page_indices_d,
+                                const int32_t* last_page_len_d, float sm_scale, void* out,
+                                float* lse, void* workspace, size_t workspace_bytes,
+                                void* stream) {
+  return run_paged(plan, false, q, nullptr, k_cache, v_cache, kv_layout, page_stride_elems,
+                   num_pages, page_indptr_d, page_indices_d, last_page_len_d, sm_scale, out, lse,
+                   workspace, workspace_bytes, stream);
+}
+
+fi_status fi_batch_prefill_paged(fi_plan_t plan, const void* q, const int32_t* qo_indptr_d,
+                                 const void* k_cache, const void* v_cache, int32_t kv_layout,
+                                 int64_t page_stride_elems, int32_t num_pages,
+                                 const int32_t* page_indptr_d, const int32_t* page_indices_d,
+                                 const int32_t* last_page_len_d, float sm_scale, void* out,
+                                 float* lse, void* workspace, size_t workspace_bytes,
+                                 void* stream) {
+  return run_paged(plan, true, q, qo_indptr_d, k_cache, v_cache, kv_layout, page_stride_elems,
+                   num_pages, page_indptr_d, page_indices_d, last_page_len_d, sm_scale, out, lse,
+                   workspace, workspace_bytes, stream);
+}
+
+fi_status fi_merge_states(const float* v, const float* s, int32_t n, int32_t S, int32_t H,
+                          int32_t d, void* out, float* lse_out, void* stream) {
+  if (n < 0 || S < 0 || H < 0 || d <= 0 || d % 4 != 0 || d > 1024) return FI_ERR_INVALID_ARG;
+  if (n == 0 || H == 0) return FI_OK;
+  if (!out || (S > 0 && (!v || !s))) return FI_ERR_INVALID_ARG;
+  if (!aligned(out, 16) || (v && !aligned(v, 16)) || (s && !aligned(s, 4)) ||
+      (lse_out && !aligned(lse_out, 4)))
+    return FI_ERR_INVALID_ARG;
+  fi_status st = check_device();
+  if (st != FI_OK) return st;
+  fi::MergeParams mp;
+  mp.v = v;
+  mp.s = s;
+  mp.tasks = nullptr;
+  mp.S = S;
+  mp.H = H;
+  mp.d = d;
+  mp.out = out;
+  mp.lse = lse_out;
+  cudaError_t e = fi::launch_merge(mp, n, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "merge launch");
+  return FI_OK;
+}
+
+fi_status fi_check_device_status(void* workspace, void* stream_ptr) {
+  if (!workspace) return FI_ERR_INVALID_ARG;
+  fi_status st = check_device();
+  if (st != FI_OK) return st;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+  uint32_t word = 0;
+  cudaError_t e = cudaMemcpyAsync(&word, workspace, sizeof(word), cudaMemcpyDeviceToHost, stream);
+  if (e == cudaSuccess) e = cudaMemsetAsync(workspace, 0, sizeof(word), stream);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+  if (e != cudaSuccess) return cuda_fail(e, "device status read");
+  if (word & fi::kErrTimeout) return FI_ERR_DEVICE_TIMEOUT;
+  if (word & fi::kErrBounds) return FI_ERR_DEVICE_BOUNDS;
+  return FI_OK;
+}
+
+const char* fi_status_string(fi_status status) {
+  switch (status) {
+    case FI_OK: return "ok";
+    case FI_ERR_INVALID_ARG: return "invalid argument";
+    case FI_ERR_UNSUPPORTED: return "unsupported configuration";
+    case FI_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
+    case FI_ERR_CUDA: return "CUDA error";
+    case FI_ERR_DEVICE_TIMEOUT: return "device wait timed out";
+    case FI_ERR_DEVICE_BOUNDS: return "page index outside the cache";
+    case FI_ERR_NO_DEVICE: return "no CUDA device";
+  }
+  return "unknown status";
+}
+
+const char* fi_last_error_string(void) { return g_last_error.c_str(); }
+
+fi_status fi_profile_next_launch(void* start_event, void* stop_event) {
+  g_prof_start = static_cast<cudaEvent_t>(start_event);
+  g_prof_stop = static_cast<cudaEvent_t>(stop_event);
+  return FI_OK;
+}
+
+fi_status fi_debug_set_fault(int32_t kind, int64_t wait_limit) {
+  if (kind < 0 || kind > 1) return FI_ERR_INVALID_ARG;
+  g_fault_kind = kind;
+  g_wait_limit_ns = wait_limit > 0 ? uint64_t(wait_limit) : fi::kDefaultWaitLimitNs;
+  return FI_OK;
+}
+
+}  // extern "C"

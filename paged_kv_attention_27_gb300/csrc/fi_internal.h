@@ -1,0 +1,85 @@
+// Internal declarations shared by the host planner (plan.cpp), the C ABI
+// (api.cu) and the kernels. Nothing here is part of the public ABI.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <string>
+#include <vector>
+
+#include "fi.h"
+
+namespace fi {
+
+// One CTA's work. Decode items: tokens [tok_begin, tok_end) of request
+// `req` for kv head `head` (all g query heads of its group), pages
+// page_indices[page_begin .. page_begin+n_pages), writing either the final
+// output row `q_row` (slot < 0) or partial-state slot `slot`. Prefill
+// items: query rows [q_row, q_row + rows) of request `req` (absolute rows of
+// q/out, at most kPrefillTileM) for query head `head`, over keys
+// [0, tok_end) — tok_end already clipped to the causal bound of the tile's
+// last row.
+struct WorkItem {
+  int32_t req;
+  int32_t head;
+  int32_t page_begin;
+  int32_t n_pages;
+  int32_t tok_begin;
+  int32_t tok_end;
+  int32_t slot;
+  int32_t q_row;
+};
+static_assert(sizeof(WorkItem) == 32, "work item is 8 int32");
+
+// A row whose decode work was split: merge states [slot_base, slot_base +
+// n_states) (each [num_qo_heads][head_dim] fp32) into output row out_row.
+struct MergeTask {
+  int32_t out_row;
+  int32_t slot_base;
+  int32_t n_states;
+  int32_t pad;
+};
+
+constexpr int kPrefillTileM = 128;         // query rows per prefill CTA
+constexpr size_t kHeaderBytes = 256;       // device error word + reserved
+constexpr size_t kAlign = 256;
+
+// Error bits in the first word of the workspace.
+constexpr uint32_t kErrTimeout = 1u;
+constexpr uint32_t kErrBounds = 2u;
+
+inline int decode_tile_tokens(int head_dim) { return 8192 / head_dim; }  // 32 KB of K+V
+inline int prefill_kv_tile(int head_dim) { return head_dim <= 128 ? 128 : 64; }
+
+struct WorkspaceLayout {
+  size_t decode_items = 0, prefill_items = 0, merges = 0, partial_o = 0, partial_lse = 0;
+  size_t total = 0;
+};
+
+struct Plan {
+  int32_t mode = 0, batch = 0, num_qo_heads = 0, num_kv_heads = 0, head_dim = 0;
+  int32_t page_size = 0, causal = 0, num_sms = 0;
+  std::vector<WorkItem> decode_items;    // launch order
+  std::vector<WorkItem> prefill_items;   // launch order
+  std::vector<MergeTask> merges;
+  int32_t chunk_tokens = 0;
+  int32_t num_split = 0;
+  int32_t num_slots = 0;
+  int64_t total_kv = 0;
+  WorkspaceLayout ws;
+};
+
+// plan.cpp
+fi_status build_plan(int32_t mode, int32_t batch, const int32_t* qo_indptr,
+                     const int32_t* page_indptr, const int32_t* last_page_len,
+                     int32_t num_qo_heads, int32_t num_kv_heads, int32_t head_dim,
+                     int32_t page_size, int32_t causal, int32_t num_sms, Plan* plan);
+
+}  // namespace fi
+
+struct fi_plan_s {
+  fi::Plan p;
+  // Host image of the workspace prefix (zeroed header, work lists, merge
+  // tasks), uploaded by every run call in one stream-ordered copy.
+  std::vector<uint8_t> image;
+};

@@ -1,0 +1,46 @@
+// Launch parameters and host-side launchers of the CUDA kernels.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "fi_internal.h"
+
+namespace fi {
+
+constexpr uint64_t kDefaultWaitLimitNs = 1000000000ull;  // 1 s per bounded wait
+
+struct DecodeParams {
+  const WorkItem* items;
+  const void* q;
+  const int32_t* page_indices;
+  int32_t num_pages;
+  int32_t page_size;
+  int32_t num_qo_heads;
+  int32_t layout;
+  float sm_scale;
+  void* out;
+  float* lse;
+  float* partial_o;
+  float* partial_lse;
+  uint32_t* err;
+  uint64_t wait_limit_ns;
+  int32_t fault_kind;
+};
+
+struct MergeParams {
+  const float* v;          // states [slot][H][d]
+  const float* s;          // lse    [slot][H]
+  const MergeTask* tasks;  // per output row; null = row r uses slots [r*S, r*S+S)
+  int32_t S;
+  int32_t H;
+  int32_t d;
+  void* out;               // bf16 [row][H][d]
+  float* lse;              // [row][H] or null
+};
+
+cudaError_t launch_decode(int head_dim, int group, const CUtensorMap& km, const CUtensorMap& vm,
+                          const DecodeParams& p, int n_items, cudaStream_t stream);
+cudaError_t launch_merge(const MergeParams& p, int n_rows, cudaStream_t stream);
+
+}  // namespace fi

@@ -1,0 +1,181 @@
+// Host planner: validation, split-KV decisions, work list and workspace
+// sizing. Pure host code (no CUDA calls), so it runs and is tested on a
+// machine without a GPU.
+//
+// Scheduling by sequence length follows the idea of "FlashInfer Attention
+// Kernel optimisation analysis", section 2.2 (dynamic load balancing by
+// sequence length) and "FlashInfer kernel library deep-dive", section
+// "load-balanced scheduling": long KV is cut into chunks so that no CTA
+// carries far more than the average load, and the largest items launch
+// first (longest-processing-time order), which bounds the tail.
+#include <algorithm>
+#include <cstring>
+
+#include "fi_internal.h"
+
+namespace fi {
+
+namespace {
+
+inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+inline size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+
+bool supported_group(int g) { return g == 1 || g == 2 || g == 4 || g == 8; }
+
+}  // namespace
+
+fi_status build_plan(int32_t mode, int32_t batch, const int32_t* qo_indptr,
+                     const int32_t* page_indptr, const int32_t* last_page_len,
+                     int32_t num_qo_heads, int32_t num_kv_heads, int32_t head_dim,
+                     int32_t page_size, int32_t causal, int32_t num_sms, Plan* out) {
+  if (!out) return FI_ERR_INVALID_ARG;
+  if (mode != FI_MODE_DECODE && mode != FI_MODE_PREFILL) return FI_ERR_INVALID_ARG;
+  if (batch < 0 || num_sms <= 0) return FI_ERR_INVALID_ARG;
+  if (num_qo_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 || page_size <= 0)
+    return FI_ERR_INVALID_ARG;
+  if (num_qo_heads % num_kv_heads != 0) return FI_ERR_INVALID_ARG;
+  if (batch > 0 && (!page_indptr || !last_page_len)) return FI_ERR_INVALID_ARG;
+  if (mode == FI_MODE_DECODE && qo_indptr) return FI_ERR_INVALID_ARG;
+  if (mode == FI_MODE_PREFILL && batch > 0 && !qo_indptr) return FI_ERR_INVALID_ARG;
+  if (head_dim != 64 && head_dim != 128 && head_dim != 256) return FI_ERR_UNSUPPORTED;
+  if (page_size != 16 && page_size != 32) return FI_ERR_UNSUPPORTED;
+  const int g = num_qo_heads / num_kv_heads;
+  if (!supported_group(g)) return FI_ERR_UNSUPPORTED;
+
+  Plan p;
+  p.mode = mode;
+  p.batch = batch;
+  p.num_qo_heads = num_qo_heads;
+  p.num_kv_heads = num_kv_heads;
+  p.head_dim = head_dim;
+  p.page_size = page_size;
+  p.causal = (mode == FI_MODE_PREFILL) ? (causal ? 1 : 0) : 0;
+  p.num_sms = num_sms;
+
+  // ---- validate the page table and the query packing; kv_len per request
+  std::vector<int64_t> kv_len(batch), qo_len(batch), qo_start(batch);
+  if (batch > 0 && page_indptr[0] < 0) return FI_ERR_INVALID_ARG;
+  if (mode == FI_MODE_PREFILL && batch > 0 && qo_indptr[0] != 0) return FI_ERR_INVALID_ARG;
+  int64_t total_q = 0;
+  for (int b = 0; b < batch; ++b) {
+    const int64_t np = int64_t(page_indptr[b + 1]) - page_indptr[b];
+    if (np < 0) return FI_ERR_INVALID_ARG;
+    if (np > 0) {
+      if (last_page_len[b] < 1 || last_page_len[b] > page_size) return FI_ERR_INVALID_ARG;
+      kv_len[b] = (np - 1) * page_size + last_page_len[b];
+    } else {
+      if (last_page_len[b] < 0 || last_page_len[b] > page_size) return FI_ERR_INVALID_ARG;
+      kv_len[b] = 0;
+    }
+    if (kv_len[b] > INT32_MAX / 2) return FI_ERR_INVALID_ARG;
+    if (mode == FI_MODE_PREFILL) {
+      qo_len[b] = int64_t(qo_indptr[b + 1]) - qo_indptr[b];
+      if (qo_len[b] < 0) return FI_ERR_INVALID_ARG;
+      if (p.causal && qo_len[b] > kv_len[b]) return FI_ERR_INVALID_ARG;
+      qo_start[b] = qo_indptr[b];
+    } else {
+      qo_len[b] = 1;
+      qo_start[b] = b;
+    }
+    total_q += qo_len[b];
+    p.total_kv += kv_len[b];
+  }
+  if (total_q > INT32_MAX) return FI_ERR_INVALID_ARG;
+
+  // ---- decode work: every request with exactly one query row
+  const int tile = decode_tile_tokens(head_dim);
+  std::vector<int> dec;
+  int64_t dec_tiles = 0;
+  for (int b = 0; b < batch; ++b) {
+    if (qo_len[b] == 1) {
+      dec.push_back(b);
+      dec_tiles += std::max<int64_t>(1, ceil_div(kv_len[b], tile)) * num_kv_heads;
+    }
+  }
+  if (!dec.empty()) {
+    // Aim for ~4 items per resident decode CTA (2 per SM), so that the
+    // largest item is a small fraction of one CTA's share, but never cut
+    // chunks below 512 tokens (per-CTA setup would dominate).
+    const int64_t target = int64_t(num_sms) * 2 * 4;
+    const int64_t min_chunk_tiles = std::max<int64_t>(1, 512 / tile);
+    const int64_t chunk_tiles = std::max(min_chunk_tiles, ceil_div(dec_tiles, target));
+    const int64_t chunk = chunk_tiles * tile;  // a multiple of the page size
+    p.chunk_tokens = int32_t(std::min<int64_t>(chunk, INT32_MAX));
+    for (int b : dec) {
+      const int64_t n_chunks = std::max<int64_t>(1, ceil_div(kv_len[b], chunk));
+      int32_t slot_base = -1;
+      if (n_chunks > 1) {
+        slot_base = p.num_slots;
+        p.num_slots += int32_t(n_chunks);
+        p.num_split += 1;
+        p.merges.push_back(MergeTask{int32_t(qo_start[b]), slot_base, int32_t(n_chunks), 0});
+      }
+      for (int kh = 0; kh < num_kv_heads; ++kh) {
+        for (int64_t c = 0; c < n_chunks; ++c) {
+          const int64_t t0 = c * chunk;
+          const int64_t t1 = std::min<int64_t>(kv_len[b], t0 + chunk);
+          WorkItem w;
+          w.req = b;
+          w.head = kh;
+          w.page_begin = int32_t(page_indptr[b] + t0 / page_size);
+          w.n_pages = int32_t(t1 > t0 ? ceil_div(t1 - t0, page_size) : 0);
+          w.tok_begin = int32_t(t0);
+          w.tok_end = int32_t(std::max(t0, t1));
+          w.slot = n_chunks > 1 ? int32_t(slot_base + c) : -1;
+          w.q_row = int32_t(qo_start[b]);
+          p.decode_items.push_back(w);
+        }
+      }
+    }
+    std::stable_sort(p.decode_items.begin(), p.decode_items.end(),
+                     [](const WorkItem& a, const WorkItem& b) {
+                       return (a.tok_end - a.tok_begin) > (b.tok_end - b.tok_begin);
+                     });
+  }
+
+  // ---- prefill work: requests with two or more query rows, one item per
+  //      (query tile of kPrefillTileM rows, query head)
+  for (int b = 0; b < batch; ++b) {
+    if (qo_len[b] < 2) continue;
+    const int64_t n_qt = ceil_div(qo_len[b], kPrefillTileM);
+    for (int64_t qt = 0; qt < n_qt; ++qt) {
+      const int64_t r0 = qt * kPrefillTileM;
+      const int64_t r_last = std::min<int64_t>(qo_len[b], r0 + kPrefillTileM) - 1;
+      int64_t kv_end = kv_len[b];
+      if (p.causal) kv_end = std::min<int64_t>(kv_len[b], kv_len[b] - qo_len[b] + r_last + 1);
+      for (int h = 0; h < num_qo_heads; ++h) {
+        WorkItem w;
+        w.req = b;
+        w.head = h;
+        w.page_begin = page_indptr[b];
+        w.n_pages = int32_t(ceil_div(kv_end, page_size));
+        w.tok_begin = 0;
+        w.tok_end = int32_t(kv_end);
+        w.slot = -1;
+        w.q_row = int32_t(qo_start[b] + r0);
+        p.prefill_items.push_back(w);
+      }
+    }
+  }
+  std::stable_sort(p.prefill_items.begin(), p.prefill_items.end(),
+                   [](const WorkItem& a, const WorkItem& b) { return a.tok_end > b.tok_end; });
+
+  // ---- workspace: header | decode items | prefill items | merges | partial o | partial lse
+  size_t off = kHeaderBytes;
+  p.ws.decode_items = off;
+  off = align_up(off + p.decode_items.size() * sizeof(WorkItem));
+  p.ws.prefill_items = off;
+  off = align_up(off + p.prefill_items.size() * sizeof(WorkItem));
+  p.ws.merges = off;
+  off = align_up(off + p.merges.size() * sizeof(MergeTask));
+  p.ws.partial_o = off;
+  off = align_up(off + size_t(p.num_slots) * num_qo_heads * head_dim * sizeof(float));
+  p.ws.partial_lse = off;
+  off = align_up(off + size_t(p.num_slots) * num_qo_heads * sizeof(float));
+  p.ws.total = off;
+
+  *out = std::move(p);
+  return FI_OK;
+}
+
+}  // namespace fi

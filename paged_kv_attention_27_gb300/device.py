@@ -1,0 +1,74 @@
+"""Moving a synthetic PagedBatch to the GPU and calling the C ABI on it.
+
+Marshalling only: numpy bf16 bit patterns become torch bf16 tensors on the
+device, outputs and the workspace are allocated with torch, and the calls go
+through ``binding`` (libfi.so). No attention arithmetic happens here.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+from . import binding as B
+from .synth import PagedBatch
+
+
+def bf16_tensor(bits: np.ndarray, device="cuda") -> torch.Tensor:
+    """uint16 bf16 bit patterns -> torch.bfloat16 tensor on `device`."""
+    t = torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16)
+    return t.to(device)
+
+
+def i32_tensor(a: np.ndarray, device="cuda") -> torch.Tensor:
+    return torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).to(device)
+
+
+def num_sms(device="cuda") -> int:
+    return torch.cuda.get_device_properties(device).multi_processor_count
+
+
+class DeviceBatch:
+    """A PagedBatch resident on the GPU, with its plan, outputs and workspace."""
+
+    def __init__(self, b: PagedBatch, device="cuda", mode=None, sms=None, lse=True):
+        self.b = b
+        self.device = device
+        self.q = bf16_tensor(b.q, device)
+        self.k = bf16_tensor(b.k_cache, device)
+        self.v = bf16_tensor(b.v_cache, device)
+        self.page_indptr = i32_tensor(b.page_indptr, device)
+        self.page_indices = i32_tensor(b.page_indices if b.page_indices.size else np.zeros(1),
+                                       device)
+        self.last_page_len = i32_tensor(b.last_page_len, device)
+        self.qo_indptr = i32_tensor(b.qo_indptr, device)
+        if mode is None:
+            mode = B.FI_MODE_DECODE if (b.is_decode and not b.causal) else B.FI_MODE_PREFILL
+        self.mode = mode
+        self.plan = B.fi_plan(mode, b.batch, b.qo_indptr if mode == B.FI_MODE_PREFILL else None,
+                              b.page_indptr, b.last_page_len, b.num_qo_heads, b.num_kv_heads,
+                              b.head_dim, b.page_size, b.causal, sms or num_sms(device))
+        self.workspace = torch.empty(max(self.plan.workspace_bytes, 256), dtype=torch.uint8,
+                                     device=device)
+        rows = int(b.qo_lens.sum())
+        self.out = torch.empty((rows, b.num_qo_heads, b.head_dim), dtype=torch.bfloat16,
+                               device=device)
+        self.lse = torch.empty((rows, b.num_qo_heads), dtype=torch.float32,
+                               device=device) if lse else None
+
+    def run(self, stream=None):
+        b = self.b
+        layout = B.LAYOUTS[b.layout]
+        if self.mode == B.FI_MODE_DECODE:
+            B.fi_batch_decode_paged(self.plan, self.q, self.k, self.v, layout, 0, b.num_pages,
+                                    self.page_indptr, self.page_indices, self.last_page_len,
+                                    b.sm_scale, self.out, self.lse, self.workspace,
+                                    stream=stream)
+        else:
+            B.fi_batch_prefill_paged(self.plan, self.q, self.qo_indptr, self.k, self.v, layout, 0,
+                                     b.num_pages, self.page_indptr, self.page_indices,
+                                     self.last_page_len, b.sm_scale, self.out, self.lse,
+                                     self.workspace, stream=stream)
+        return self.out, self.lse
+
+    def status(self, stream=None) -> int:
+        return B.fi_check_device_status(self.workspace, stream)

@@ -45,22 +45,39 @@ def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
     Returns the bf16 bit patterns as uint16. NaN stays a quiet NaN.
     """
     x = np.ascontiguousarray(x, dtype=np.float32)
-    u = x.view(np.uint32).astype(np.uint64)
-    bias = ((u >> 16) & 1) + 0x7FFF
-    out = ((u + bias) >> 16).astype(np.uint16)
+    u = x.view(np.uint32)
+    bias = ((u >> np.uint32(16)) & np.uint32(1)) + np.uint32(0x7FFF)
+    out = ((u + bias) >> np.uint32(16)).astype(np.uint16)
     nan = np.isnan(x)
     if nan.any():
         out[nan] = 0x7FC0
     return out
 
 
-def normal_bf16(gen: np.random.Generator, shape, chunk: int = 1 << 24) -> np.ndarray:
-    """Standard normal values of ``shape`` as bf16 bit patterns (uint16)."""
+_CHUNK = 1 << 22
+
+
+def normal_bf16(seed: int, stream: int, shape) -> np.ndarray:
+    """Standard normal values of ``shape`` as bf16 bit patterns (uint16).
+
+    Element block j (of 2^22 elements) is drawn from its own Philox stream
+    keyed by (seed, stream, j), so the values do not depend on how many
+    threads fill the array; blocks are filled in parallel.
+    """
+    import concurrent.futures as cf
+    import os
     n = int(np.prod(shape, dtype=np.int64))
     out = np.empty(n, dtype=np.uint16)
-    for s in range(0, n, chunk):
-        c = min(chunk, n - s)
-        out[s:s + c] = f32_to_bf16_bits(gen.standard_normal(c, dtype=np.float32))
+
+    def fill(j):
+        s = j * _CHUNK
+        c = min(_CHUNK, n - s)
+        g = np.random.Generator(np.random.Philox(key=[int(seed) * 64 + int(stream), j]))
+        out[s:s + c] = f32_to_bf16_bits(g.standard_normal(c, dtype=np.float32))
+
+    blocks = range((n + _CHUNK - 1) // _CHUNK)
+    with cf.ThreadPoolExecutor(max_workers=min(32, os.cpu_count() or 1)) as ex:
+        list(ex.map(fill, blocks))
     return out.reshape(shape)
 
 
@@ -150,9 +167,9 @@ def make_batch(name: str, kv_lens, qo_lens, num_qo_heads: int, num_kv_heads: int
 
     Hkv, d = num_kv_heads, head_dim
     shape = (num_phys, P, Hkv, d) if layout == NHD else (num_phys, Hkv, P, d)
-    k_cache = normal_bf16(gen, shape)
-    v_cache = normal_bf16(gen, shape)
-    q = normal_bf16(gen, (int(qo_lens.sum()), num_qo_heads, d))
+    k_cache = normal_bf16(seed, 1, shape)
+    v_cache = normal_bf16(seed, 2, shape)
+    q = normal_bf16(seed, 3, (int(qo_lens.sum()), num_qo_heads, d))
     if tail_fill == "nan":
         for b in range(B):
             if npages[b] == 0 or last[b] == P:

@@ -1,0 +1,35 @@
+"""Helpers shared by the GPU parity tests: build/load the library, compare
+GPU results with the fp64 oracle under the stated tolerances."""
+import numpy as np
+
+# bf16 outputs against the unrounded fp64 oracle; fp32 lse absolute
+OUT_MAX_ABS = 1e-2
+OUT_MEAN_ABS = 1e-3
+LSE_MAX_ABS = 1e-3
+
+
+def ensure_built():
+    from paged_kv_attention_27_gb300 import build
+    build.build()
+
+
+def compare(out_gpu, lse_gpu, out_ref, lse_ref, rows=None, what=""):
+    """Element-wise comparison on the rows given (all rows if None)."""
+    o = out_gpu.float().cpu().numpy().astype(np.float64)
+    l = lse_gpu.float().cpu().numpy().astype(np.float64) if lse_gpu is not None else None
+    if rows is not None:
+        o, out_ref = o[rows], out_ref[rows]
+        if l is not None:
+            l, lse_ref = l[rows], lse_ref[rows]
+    assert np.all(np.isfinite(o)), f"{what}: non-finite output"
+    err = np.abs(o - out_ref)
+    assert err.max() <= OUT_MAX_ABS, f"{what}: max-abs {err.max():.3e}"
+    assert err.mean() <= OUT_MEAN_ABS, f"{what}: mean-abs {err.mean():.3e}"
+    if l is not None:
+        inf_ref = np.isneginf(lse_ref)
+        assert np.array_equal(np.isneginf(l), inf_ref), f"{what}: -inf lse pattern differs"
+        fin = ~inf_ref
+        if fin.any():
+            le = np.abs(l[fin] - lse_ref[fin])
+            assert le.max() <= LSE_MAX_ABS, f"{what}: lse max-abs {le.max():.3e}"
+    return float(err.max()), float(err.mean())

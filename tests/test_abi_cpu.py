@@ -1,0 +1,240 @@
+"""CPU-only checks of the C ABI: the library loads and exports every symbol
+include/fi.h declares; the host planner's work lists cover every
+(request, head, key) exactly once with page-aligned splits; argument
+validation returns the documented status codes. No kernel is launched."""
+import os
+import re
+
+import numpy as np
+import pytest
+
+from paged_kv_attention_27_gb300 import binding as B
+from paged_kv_attention_27_gb300 import synth
+
+from ._gpu import ensure_built
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    ensure_built()
+    return B.lib()
+
+
+def test_exports_every_declared_symbol():
+    header = open(os.path.join(ROOT, "include", "fi.h")).read()
+    declared = set(re.findall(r"^\s*(?:fi_status|const char\*)\s+(fi_\w+)\s*\(", header, re.M))
+    assert declared, "no declarations parsed"
+    assert declared == set(B.EXPORTED)
+    L = B.lib()
+    for name in declared:
+        assert hasattr(L, name), name
+
+
+def test_status_strings():
+    for code in range(8):
+        assert B.status_string(code) != "unknown status"
+    assert B.status_string(99) == "unknown status"
+
+
+def _plan(b, mode=None, sms=152):
+    if mode is None:
+        mode = B.FI_MODE_DECODE if (b.is_decode and not b.causal) else B.FI_MODE_PREFILL
+    return B.fi_plan(mode, b.batch, b.qo_indptr if mode == B.FI_MODE_PREFILL else None,
+                     b.page_indptr, b.last_page_len, b.num_qo_heads, b.num_kv_heads, b.head_dim,
+                     b.page_size, b.causal, sms)
+
+
+def _check_decode_cover(b, plan):
+    """Each (request, kv head, token) exactly once; chunks start on page and
+    tile boundaries; pages named are the request's own."""
+    info = B.fi_plan_get_info(plan)
+    work = B.fi_plan_get_work(plan)
+    dec = work[:info["num_decode_items"]]
+    seen = {}
+    for req, kh, pb, npg, t0, t1, slot, qrow in dec.tolist():
+        assert t0 % b.page_size == 0
+        assert pb == b.page_indptr[req] + t0 // b.page_size
+        assert npg == -(-(t1 - t0) // b.page_size)
+        assert pb + npg <= b.page_indptr[req + 1]
+        assert qrow == b.qo_indptr[req]
+        for t in range(t0, t1):
+            seen[(req, kh, t)] = seen.get((req, kh, t), 0) + 1
+    want = {(r, h, t) for r in range(b.batch) if b.qo_lens[r] == 1
+            for h in range(b.num_kv_heads) for t in range(int(b.kv_lens[r]))}
+    assert set(seen) == want
+    assert all(c == 1 for c in seen.values())
+    # every decode request appears for every kv head (also empty ones)
+    per = {}
+    for req, kh, *_ in dec.tolist():
+        per.setdefault(req, set()).add(kh)
+    for r in range(b.batch):
+        if b.qo_lens[r] == 1:
+            assert per[r] == set(range(b.num_kv_heads))
+    # longest items first
+    lens = dec[:, 5] - dec[:, 4]
+    assert np.all(np.diff(lens) <= 0)
+    # split requests own consecutive slots, one per chunk
+    slots = dec[dec[:, 6] >= 0]
+    if len(slots):
+        assert info["num_partial_slots"] == len(set(slots[:, 6].tolist()))
+    return info
+
+
+@pytest.mark.parametrize("name", ["tiny", "7b", "70b"])
+def test_decode_plans_cover_every_key_once(name):
+    if name == "tiny":
+        b = synth.tiny_decode()
+    elif name == "7b":
+        g = synth.philox(1001)
+        b = _table_only(g.integers(512, 4097, size=64), 32, 32, 128, 16)
+    else:
+        g = synth.philox(1002)
+        b = _table_only(synth.lognormal_lengths(g, 128), 64, 8, 128, 16)
+    plan = _plan(b)
+    info = _check_decode_cover(b, plan)
+    assert info["workspace_bytes"] >= 256
+    if name == "70b":
+        assert info["num_split_requests"] > 0
+
+
+def _table_only(kv, hq, hkv, d, P, qo=None):
+    """A batch with a page table but a one-page dummy cache (planning only)."""
+    kv = np.asarray(kv, np.int64)
+    qo = np.ones_like(kv) if qo is None else np.asarray(qo, np.int64)
+    npg = np.where(kv > 0, (kv + P - 1) // P, 0)
+    indptr = np.zeros(len(kv) + 1, np.int32)
+    indptr[1:] = np.cumsum(npg)
+    qo_indptr = np.zeros(len(kv) + 1, np.int32)
+    qo_indptr[1:] = np.cumsum(qo)
+    last = np.where(kv > 0, kv - (npg - 1) * P, 0).astype(np.int32)
+    z = np.zeros((1, P, hkv, d), np.uint16)
+    return synth.PagedBatch("table", hq, hkv, d, P, synth.NHD, 0.1, bool((qo > 1).any()), kv, qo,
+                            qo_indptr, indptr, np.arange(int(npg.sum()), dtype=np.int32), last,
+                            np.zeros((int(qo.sum()), hq, d), np.uint16), z, z)
+
+
+@pytest.mark.parametrize("sms", [1, 7, 152])
+def test_split_decisions_scale_with_sm_count(sms):
+    b = _table_only([1, 0, 33, 4096, 32768, 700], 32, 8, 128, 16)
+    plan = _plan(b, sms=sms)
+    info = _check_decode_cover(b, plan)
+    assert info["chunk_tokens"] % 16 == 0
+    assert info["chunk_tokens"] >= 512
+
+
+def test_prefill_plan_tiles_and_causal_bounds():
+    kv = [300, 1, 129, 77, 5000]
+    qo = [300, 1, 100, 77, 4]
+    b = _table_only(kv, 8, 2, 128, 16, qo)
+    plan = _plan(b, B.FI_MODE_PREFILL)
+    info = B.fi_plan_get_info(plan)
+    work = B.fi_plan_get_work(plan)
+    pre = work[info["num_decode_items"]:]
+    rows = {}
+    for req, h, pb, npg, t0, t1, slot, qrow in pre.tolist():
+        qo_len, kv_len = qo[req], kv[req]
+        r0 = qrow - b.qo_indptr[req]
+        r_last = min(qo_len, r0 + 128) - 1
+        assert t0 == 0 and slot == -1
+        assert t1 == min(kv_len, kv_len - qo_len + r_last + 1)   # causal bound of the last row
+        assert npg == -(-t1 // 16)
+        for r in range(r0, r_last + 1):
+            rows[(req, h, r)] = rows.get((req, h, r), 0) + 1
+    want = {(r, h, i) for r in range(len(kv)) if qo[r] >= 2 for h in range(8)
+            for i in range(qo[r])}
+    assert set(rows) == want and all(c == 1 for c in rows.values())
+    # the single-row request is decode work
+    _check_decode_cover(b, plan)
+    assert np.all(np.diff(pre[:, 5]) <= 0)
+
+
+@pytest.mark.parametrize("case,status", [
+    ("last_page_len_zero", B.FI_ERR_INVALID_ARG),
+    ("last_page_len_big", B.FI_ERR_INVALID_ARG),
+    ("decreasing_indptr", B.FI_ERR_INVALID_ARG),
+    ("causal_qo_gt_kv", B.FI_ERR_INVALID_ARG),
+    ("heads_not_multiple", B.FI_ERR_INVALID_ARG),
+    ("head_dim_96", B.FI_ERR_UNSUPPORTED),
+    ("page_size_8", B.FI_ERR_UNSUPPORTED),
+    ("group_3", B.FI_ERR_UNSUPPORTED),
+    ("decode_with_qo_indptr", B.FI_ERR_INVALID_ARG),
+    ("prefill_without_qo_indptr", B.FI_ERR_INVALID_ARG),
+    ("qo_indptr_not_zero_based", B.FI_ERR_INVALID_ARG),
+    ("no_sms", B.FI_ERR_INVALID_ARG),
+])
+def test_plan_validation(case, status):
+    args = dict(mode=B.FI_MODE_DECODE, batch_size=2, qo_indptr_h=None,
+                page_indptr_h=[0, 2, 3], last_page_len_h=[5, 16], num_qo_heads=8,
+                num_kv_heads=2, head_dim=128, page_size=16, causal=0, num_sms=152)
+    if case == "last_page_len_zero":
+        args["last_page_len_h"] = [0, 16]
+    elif case == "last_page_len_big":
+        args["last_page_len_h"] = [17, 16]
+    elif case == "decreasing_indptr":
+        args["page_indptr_h"] = [0, 3, 2]
+    elif case == "causal_qo_gt_kv":
+        args.update(mode=B.FI_MODE_PREFILL, qo_indptr_h=[0, 22, 23], causal=1)
+    elif case == "heads_not_multiple":
+        args["num_qo_heads"] = 7
+    elif case == "head_dim_96":
+        args["head_dim"] = 96
+    elif case == "page_size_8":
+        args["page_size"] = 8
+    elif case == "group_3":
+        args.update(num_qo_heads=6, num_kv_heads=2)
+    elif case == "decode_with_qo_indptr":
+        args["qo_indptr_h"] = [0, 1, 2]
+    elif case == "prefill_without_qo_indptr":
+        args["mode"] = B.FI_MODE_PREFILL
+    elif case == "qo_indptr_not_zero_based":
+        args.update(mode=B.FI_MODE_PREFILL, qo_indptr_h=[1, 2, 3])
+    elif case == "no_sms":
+        args["num_sms"] = 0
+    with pytest.raises(B.FiError) as e:
+        B.fi_plan(**args)
+    assert e.value.status == status
+
+
+def test_valid_edge_plans():
+    # empty batch; a request without pages (last_page_len ignored in [0, P])
+    p = B.fi_plan(B.FI_MODE_DECODE, 0, None, [0], [], 8, 2, 64, 16, 0, 4)
+    assert B.fi_plan_get_info(p)["num_items"] == 0
+    p = B.fi_plan(B.FI_MODE_DECODE, 2, None, [0, 0, 1], [0, 3], 8, 2, 64, 16, 0, 4)
+    info = B.fi_plan_get_info(p)
+    assert info["total_kv_tokens"] == 3 and info["num_decode_items"] == 4
+
+
+def test_workspace_too_small_and_bad_args_return_before_any_launch():
+    """Host-side checks happen before the device is touched; on a machine
+    without a GPU, a well-formed call reports that there is no device."""
+    torch = pytest.importorskip("torch")
+    if torch.cuda.is_available():
+        pytest.skip("uses fake device addresses; only meaningful without a GPU")
+    p = B.fi_plan(B.FI_MODE_DECODE, 2, None, [0, 2, 3], [5, 16], 8, 2, 128, 16, 0, 4)
+    fake = 1 << 20   # aligned, never dereferenced: every call below returns first
+    args = [p, fake, fake, fake, B.FI_LAYOUT_NHD, 0, 4, fake, fake, fake, 0.1, fake, fake, fake]
+    with pytest.raises(B.FiError) as e:
+        B.fi_batch_decode_paged(*args, workspace_bytes=16, stream=0)
+    assert e.value.status == B.FI_ERR_WORKSPACE_TOO_SMALL
+    bad = list(args)
+    bad[1] = fake + 2          # misaligned q
+    with pytest.raises(B.FiError) as e:
+        B.fi_batch_decode_paged(*bad, stream=0)
+    assert e.value.status == B.FI_ERR_INVALID_ARG
+    bad = list(args)
+    bad[4] = 7                 # unknown layout
+    with pytest.raises(B.FiError) as e:
+        B.fi_batch_decode_paged(*bad, stream=0)
+    assert e.value.status == B.FI_ERR_INVALID_ARG
+    with pytest.raises(B.FiError) as e:      # prefill call with a decode plan
+        B.fi_batch_prefill_paged(p, fake, fake, fake, fake, 0, 0, 4, fake, fake, fake, 0.1,
+                                 fake, fake, fake, stream=0)
+    assert e.value.status == B.FI_ERR_INVALID_ARG
+    with pytest.raises(B.FiError) as e:
+        B.fi_batch_decode_paged(*args, stream=0)
+    assert e.value.status == B.FI_ERR_NO_DEVICE
+    with pytest.raises(B.FiError) as e:
+        B.fi_merge_states(fake, fake, 2, 3, 4, 6, fake, None, stream=0)   # d % 4 != 0
+    assert e.value.status == B.FI_ERR_INVALID_ARG

@@ -1,0 +1,186 @@
+"""GPU parity of batch decode (and merge_states) against the fp64 oracle,
+through the C ABI. Same seeded inputs on both sides; bf16 outputs within
+max-abs 1e-2 / mean-abs 1e-3 of the unrounded oracle, lse within 1e-3."""
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+
+import oracle  # noqa: E402
+from paged_kv_attention_27_gb300 import binding as B  # noqa: E402
+from paged_kv_attention_27_gb300 import synth  # noqa: E402
+
+from ._gpu import compare, ensure_built  # noqa: E402
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    ensure_built()
+    B.lib()
+
+
+def _dev(b, **kw):
+    from paged_kv_attention_27_gb300.device import DeviceBatch
+    return DeviceBatch(b, **kw)
+
+
+def _oracle(b, requests=None):
+    return oracle.batch_attention(b.q, b.qo_indptr, b.k_cache, b.v_cache, b.layout, b.page_indptr,
+                                  b.page_indices, b.last_page_len, b.num_qo_heads, b.num_kv_heads,
+                                  b.page_size, b.sm_scale, b.causal, requests=requests)
+
+
+def _rows(b, requests):
+    return np.concatenate([np.arange(b.qo_indptr[r], b.qo_indptr[r + 1]) for r in requests])
+
+
+def check(b, requests=None, sms=None, what=None):
+    db = _dev(b, sms=sms)
+    out, lse = db.run()
+    torch.cuda.synchronize()
+    assert db.status() == B.FI_OK
+    ref_o, ref_l = _oracle(b, requests)
+    rows = None if requests is None else _rows(b, requests)
+    return compare(out, lse, ref_o, ref_l, rows=rows, what=what or b.name), db
+
+
+def test_tiny_decode():
+    check(synth.tiny_decode())
+
+
+def test_llama7b_decode_full_size_sampled():
+    b = synth.llama7b_decode()
+    order = np.argsort(-b.kv_lens)
+    sample = sorted(set(order[:4].tolist() + order[-4:].tolist() + list(range(0, 64, 9))))
+    check(b, requests=sample)
+
+
+def test_llama70b_gqa_decode_full_size_sampled():
+    b = synth.llama70b_gqa_decode()
+    order = np.argsort(-b.kv_lens)
+    sample = sorted(set(order[:3].tolist() + order[-3:].tolist() + [0, 5, 31, 32, 77]))
+    (_, _), db = check(b, requests=sample)
+    info = B.fi_plan_get_info(db.plan)
+    assert info["num_split_requests"] > 0        # long requests really were split
+
+
+@pytest.mark.parametrize("d", [64, 128, 256])
+@pytest.mark.parametrize("g", [1, 2, 4, 8])
+@pytest.mark.parametrize("P", [16, 32])
+def test_shapes(d, g, P):
+    hkv = 2
+    kv = [0, 1, P - 1, P, P + 1, 3 * P + 5, 700, 2049]
+    b = synth.make_batch(f"shape d{d} g{g} P{P}", kv, [1] * len(kv), g * hkv, hkv, d, P,
+                         synth.NHD if (d + g) % 2 == 0 else synth.HND, None, False, d * 31 + g + P)
+    check(b)
+
+
+@pytest.mark.parametrize("sms", [1, 3, 2000])
+def test_split_kv_matches_oracle_for_any_split(sms):
+    kv = [5000, 33, 1, 0, 2600, 17000]
+    b = synth.make_batch("splits", kv, [1] * len(kv), 16, 4, 128, 16, synth.HND, None, False, 77)
+    (_, _), db = check(b, sms=sms)
+    if sms == 2000:
+        assert B.fi_plan_get_info(db.plan)["num_split_requests"] >= 3
+
+
+def test_nan_in_unused_tail_slots_is_never_read():
+    kv = [3, 17, 45, 100, 513]
+    b = synth.make_batch("nan tail", kv, [1] * len(kv), 8, 2, 128, 16, synth.NHD, None, False, 5,
+                         tail_fill="nan")
+    check(b)
+    b = synth.make_batch("nan tail HND", kv, [1] * len(kv), 8, 8, 64, 32, synth.HND, None, False,
+                         6, tail_fill="nan")
+    check(b)
+
+
+def test_deterministic_run_to_run():
+    b = synth.make_batch("det", [9000, 300, 4100], [1, 1, 1], 32, 8, 128, 16, synth.NHD, None,
+                         False, 8)
+    db = _dev(b, sms=200)
+    o1 = db.run()[0].clone()
+    l1 = db.lse.clone()
+    o2, l2 = db.run()
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+def test_layouts_agree_and_page_stride_views():
+    b = synth.make_batch("nhd", [70, 300, 1], [1, 1, 1], 8, 2, 128, 16, synth.NHD, None, False, 9)
+    db = _dev(b)
+    o_nhd = db.run()[0].clone()
+    bh = synth.PagedBatch(**{**b.__dict__, "layout": synth.HND,
+                             "k_cache": np.ascontiguousarray(b.k_cache.transpose(0, 2, 1, 3)),
+                             "v_cache": np.ascontiguousarray(b.v_cache.transpose(0, 2, 1, 3))})
+    o_hnd = _dev(bh).run()[0]
+    torch.cuda.synchronize()
+    assert torch.equal(o_nhd, o_hnd)
+    # K and V interleaved in one [num_pages][2][P][Hkv][d] buffer
+    from paged_kv_attention_27_gb300.device import bf16_tensor
+    kv = np.stack([b.k_cache, b.v_cache], axis=1)
+    kvt = bf16_tensor(kv)
+    page_elems = 16 * 2 * 128
+    out = torch.empty_like(db.out)
+    B.fi_batch_decode_paged(db.plan, db.q, kvt[:, 0], kvt[:, 1], B.FI_LAYOUT_NHD, 2 * page_elems,
+                            b.num_pages, db.page_indptr, db.page_indices, db.last_page_len,
+                            b.sm_scale, out, None, db.workspace)
+    torch.cuda.synchronize()
+    assert torch.equal(out, o_nhd)
+
+
+@pytest.mark.parametrize("n,S,H,d", [(5, 3, 4, 128), (2, 1, 8, 64), (3, 7, 2, 256), (1, 0, 2, 64)])
+def test_merge_states_abi(n, S, H, d):
+    rng = np.random.default_rng(n * 1000 + S)
+    # |o| ~ 0.25: at |o| ~ 1 the bf16 rounding of the output alone would use
+    # up the mean-abs budget (2^-9 relative), hiding any real error
+    v = (0.25 * rng.normal(size=(n, S, H, d))).astype(np.float32)
+    s = (rng.normal(size=(n, S, H)) * 4).astype(np.float32)
+    if S >= 2:
+        s[0, 1, :] = -np.inf             # an empty state
+        s[-1, :, 0] = -np.inf            # a row with every state empty
+    if S == 0:     # no states at all: the empty merge, o = 0 and lse = -inf
+        ref_o, ref_l = np.zeros((n, H, d)), np.full((n, H), -np.inf)
+    else:
+        ref_o, ref_l = oracle.merge_states(np.moveaxis(v.astype(np.float64), 1, 0),
+                                           np.moveaxis(s.astype(np.float64), 1, 0))
+    vt = torch.from_numpy(v).cuda()
+    st = torch.from_numpy(s).cuda()
+    out = torch.empty((n, H, d), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((n, H), dtype=torch.float32, device="cuda")
+    B.fi_merge_states(vt, st, n, S, H, d, out, lse)
+    torch.cuda.synchronize()
+    compare(out, lse, ref_o, ref_l, what="merge_states")
+
+
+def test_bounded_wait_times_out_and_context_survives():
+    b = synth.make_batch("timeout", [4000, 100], [1, 1], 8, 2, 128, 16, synth.NHD, None, False, 10)
+    db = _dev(b)
+    B.fi_debug_set_fault(1, 2_000_000)          # 2 ms bound; producer skips one load
+    try:
+        db.run()
+        assert db.status() == B.FI_ERR_DEVICE_TIMEOUT
+    finally:
+        B.fi_debug_set_fault(0, 0)
+    out, lse = db.run()                          # same context, normal run
+    torch.cuda.synchronize()
+    assert db.status() == B.FI_OK
+    ref_o, ref_l = _oracle(b)
+    compare(out, lse, ref_o, ref_l, what="after timeout")
+
+
+def test_out_of_range_page_index_is_reported_not_read():
+    b = synth.make_batch("bounds", [40, 40], [1, 1], 8, 2, 64, 16, synth.NHD, None, False, 11)
+    db = _dev(b)
+    bad = b.page_indices.copy()
+    bad[1] = b.num_pages + 1000
+    db.page_indices.copy_(torch.from_numpy(bad))
+    db.run()
+    assert db.status() == B.FI_ERR_DEVICE_BOUNDS
+    # request 1 is untouched by the bad index
+    torch.cuda.synchronize()
+    ref_o, ref_l = _oracle(b, [1])
+    compare(db.out, db.lse, ref_o, ref_l, rows=np.array([1]), what="bounds, clean request")
