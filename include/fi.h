@@ -179,6 +179,34 @@ fi_status fi_batch_decode_paged(fi_plan_t plan, const void* q, const void* k_cac
                                 void* stream);
 
 /*
+ * fi_batch_decode_paged_noalloc — fi_batch_decode_paged without a workspace
+ * argument, for callers that cannot allocate device memory where they run
+ * attention (an engine plugin whose framework owns all device memory and
+ * exposes no scratch allocator; a latency-critical loop where a cudaMalloc,
+ * which can synchronise the device, is not acceptable). The paper has no
+ * counterpart to this call; it is an interface convenience.
+ * The scratch (work list, error word, fp32 split partials) is a 16 MiB
+ * array inside the library, held by every GPU that loads the library until
+ * the process exits. This call allocates nothing itself.
+ *   Arguments: as for fi_batch_decode_paged, minus the workspace.
+ *   First call on a device: looks up that device's address of the array
+ *   (cudaGetSymbolAddress) and caches it — make it before any stream capture.
+ *   Sharing: every call uses the same array, so calls whose GPU work can
+ *   overlap (unordered streams) race; order them on one stream.
+ *   Limits: a plan whose workspace_bytes exceeds 16 MiB returns
+ *   FI_ERR_WORKSPACE_TOO_SMALL before anything is enqueued. Device-side
+ *   error flags of this call cannot be read with fi_check_device_status.
+ * Errors: as for fi_batch_decode_paged.
+ */
+fi_status fi_batch_decode_paged_noalloc(fi_plan_t plan, const void* q, const void* k_cache,
+                                        const void* v_cache, int32_t kv_layout,
+                                        int64_t page_stride_elems, int32_t num_pages,
+                                        const int32_t* page_indptr_d,
+                                        const int32_t* page_indices_d,
+                                        const int32_t* last_page_len_d, float sm_scale,
+                                        void* out, float* lse, void* stream);
+
+/*
  * fi_batch_prefill_paged — causal (or full) variable-length batch prefill
  * over a paged KV cache, the varlen form of "FlashAttention-3 kernel
  * integration in inference engines", section 2 (cu_seqlens_q is

@@ -36,7 +36,7 @@ LAYOUTS = {"NHD": FI_LAYOUT_NHD, "HND": FI_LAYOUT_HND}
 EXPORTED = ["fi_plan", "fi_plan_destroy", "fi_plan_get_info", "fi_plan_get_work",
             "fi_batch_decode_paged", "fi_batch_prefill_paged", "fi_merge_states",
             "fi_check_device_status", "fi_status_string", "fi_last_error_string",
-            "fi_debug_set_fault", "fi_profile_next_launch"]
+            "fi_debug_set_fault", "fi_profile_next_launch", "fi_batch_decode_paged_noalloc"]
 
 
 class FiError(RuntimeError):
@@ -88,6 +88,8 @@ def lib():
     L.fi_last_error_string.restype = ctypes.c_char_p
     L.fi_debug_set_fault.argtypes = [_I32, _I64]
     L.fi_profile_next_launch.argtypes = [_P, _P]
+    L.fi_batch_decode_paged_noalloc.argtypes = [_P, _P, _P, _P, _I32, _I64, _I32, _P, _P, _P,
+                                                ctypes.c_float, _P, _P, _P]
     for name in EXPORTED:
         if name not in ("fi_status_string", "fi_last_error_string"):
             getattr(L, name).restype = _I32
@@ -225,3 +227,16 @@ def fi_profile_next_launch(start_event, stop_event):
     sp = start_event.cuda_event if hasattr(start_event, "cuda_event") else start_event
     ep = stop_event.cuda_event if hasattr(stop_event, "cuda_event") else stop_event
     _check(lib().fi_profile_next_launch(sp, ep), "fi_profile_next_launch")
+
+
+def fi_batch_decode_paged_noalloc(plan: Plan, q, k_cache, v_cache, kv_layout, page_stride_elems,
+                                  num_pages, page_indptr_d, page_indices_d, last_page_len_d,
+                                  sm_scale, out, lse, stream=None):
+    """fi_batch_decode_paged with the library's own static scratch (no workspace)."""
+    st = lib().fi_batch_decode_paged_noalloc(plan.handle, _ptr(q), _ptr(k_cache), _ptr(v_cache),
+                                             int(kv_layout), int(page_stride_elems),
+                                             int(num_pages), _ptr(page_indptr_d),
+                                             _ptr(page_indices_d), _ptr(last_page_len_d),
+                                             float(sm_scale), _ptr(out), _ptr(lse),
+                                             _stream(stream))
+    _check(st, "fi_batch_decode_paged_noalloc")
