@@ -76,6 +76,28 @@ fi_status make_kv_map(CUtensorMap* map, const void* base, int layout, int num_pa
   return FI_OK;
 }
 
+// Tensor map over the packed queries [rows][num_qo_heads][head_dim] that
+// fetches 128 rows x 64 dims of one head per box (128-byte swizzled).
+fi_status make_q_map(CUtensorMap* map, const void* q, int64_t rows, int Hq, int d) {
+  auto enc = encode_fn();
+  if (!enc) {
+    g_last_error = "cuTensorMapEncodeTiled is not available from the driver";
+    return FI_ERR_CUDA;
+  }
+  const cuuint64_t dims[3] = {cuuint64_t(d), cuuint64_t(Hq), cuuint64_t(rows)};
+  const cuuint64_t strides[2] = {cuuint64_t(d) * 2, cuuint64_t(Hq) * d * 2};
+  const cuuint32_t box[3] = {64, 1, cuuint32_t(fi::kPrefillTileM)};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(q), dims, strides,
+                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    g_last_error = "cuTensorMapEncodeTiled failed for q (code " + std::to_string(int(r)) + ")";
+    return FI_ERR_CUDA;
+  }
+  return FI_OK;
+}
+
 fi_status check_device() {
   int dev = -1;
   cudaError_t e = cudaGetDevice(&dev);
@@ -138,9 +160,10 @@ fi_status run_paged(fi_plan_t plan, bool prefill_call, const void* q, const int3
   float* partial_o = reinterpret_cast<float*>(ws + P.ws.partial_o);
   float* partial_lse = reinterpret_cast<float*>(ws + P.ws.partial_lse);
 
+  CUtensorMap qmap;
   if (!P.prefill_items.empty()) {
-    g_last_error = "prefill work items are not supported by this build";
-    return FI_ERR_UNSUPPORTED;
+    st = make_q_map(&qmap, q, P.total_q, P.num_qo_heads, P.head_dim);
+    if (st != FI_OK) return st;
   }
 
   cudaEvent_t prof_start = g_prof_start, prof_stop = g_prof_stop;
@@ -150,6 +173,27 @@ fi_status run_paged(fi_plan_t plan, bool prefill_call, const void* q, const int3
     if (e != cudaSuccess) return cuda_fail(e, "profiling event");
   }
 
+  if (!P.prefill_items.empty()) {
+    fi::PrefillParams pp;
+    pp.items = reinterpret_cast<const fi::WorkItem*>(ws + P.ws.prefill_items);
+    pp.qo_indptr = qo_indptr_d;
+    pp.page_indptr = page_indptr_d;
+    pp.last_page_len = last_page_len_d;
+    pp.page_indices = page_indices_d;
+    pp.num_pages = num_pages;
+    pp.page_size = P.page_size;
+    pp.num_qo_heads = P.num_qo_heads;
+    pp.group = P.num_qo_heads / P.num_kv_heads;
+    pp.layout = kv_layout;
+    pp.causal = P.causal;
+    pp.sm_scale = sm_scale;
+    pp.out = out;
+    pp.lse = lse;
+    pp.err = err;
+    pp.wait_limit_ns = g_wait_limit_ns;
+    e = fi::launch_prefill(P.head_dim, qmap, kmap, vmap, pp, int(P.prefill_items.size()), stream);
+    if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
+  }
   if (!P.decode_items.empty()) {
     fi::DecodeParams dp;
     dp.items = reinterpret_cast<const fi::WorkItem*>(ws + P.ws.decode_items);

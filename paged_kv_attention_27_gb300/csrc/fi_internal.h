@@ -66,6 +66,7 @@ struct Plan {
   int32_t num_split = 0;
   int32_t num_slots = 0;
   int64_t total_kv = 0;
+  int64_t total_q = 0;                   // rows of q / out
   WorkspaceLayout ws;
 };
 

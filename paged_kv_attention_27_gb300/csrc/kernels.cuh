@@ -39,6 +39,28 @@ struct MergeParams {
   float* lse;              // [row][H] or null
 };
 
+struct PrefillParams {
+  const WorkItem* items;
+  const int32_t* qo_indptr;
+  const int32_t* page_indptr;
+  const int32_t* last_page_len;
+  const int32_t* page_indices;
+  int32_t num_pages;
+  int32_t page_size;
+  int32_t num_qo_heads;
+  int32_t group;
+  int32_t layout;
+  int32_t causal;
+  float sm_scale;
+  void* out;
+  float* lse;
+  uint32_t* err;
+  uint64_t wait_limit_ns;
+};
+
+cudaError_t launch_prefill(int head_dim, const CUtensorMap& qm, const CUtensorMap& km,
+                           const CUtensorMap& vm, const PrefillParams& p, int n_items,
+                           cudaStream_t stream);
 cudaError_t launch_decode(int head_dim, int group, const CUtensorMap& km, const CUtensorMap& vm,
                           const DecodeParams& p, int n_items, cudaStream_t stream);
 cudaError_t launch_merge(const MergeParams& p, int n_rows, cudaStream_t stream);

@@ -81,6 +81,7 @@ fi_status build_plan(int32_t mode, int32_t batch, const int32_t* qo_indptr,
     p.total_kv += kv_len[b];
   }
   if (total_q > INT32_MAX) return FI_ERR_INVALID_ARG;
+  p.total_q = total_q;
 
   // ---- decode work: every request with exactly one query row
   const int tile = decode_tile_tokens(head_dim);

@@ -1,0 +1,464 @@
+// Causal variable-length batch prefill over a paged KV cache, on the
+// 5th-generation tensor cores (tcgen05.mma, accumulators in tensor memory).
+//
+// One CTA per planned work item: 128 query rows of one request and one query
+// head, against keys [0, tok_end) of that request (tok_end already clipped to
+// the causal bound of the tile's last row). Warp-specialised, as the
+// FlashAttention-3 page describes for Hopper (section 1: TMA producer warps,
+// consumer warps driving the tensor cores, hardware barriers between them,
+// ping-pong buffers), rebuilt for sm_103a:
+//   * warp 4 (producer): TMA loads of the Q tile (once) and, per KV tile of
+//     N tokens, one 128B-swizzled box per (page, 64-dim slice) of K and of V
+//     into two-deep K and V rings;
+//   * warp 5 (MMA issuer; also owns the TMEM allocation): one thread issues
+//     S_j = Q K_j^T into a double-buffered S region of TMEM, then
+//     O += P_{j-1} V_{j-1} into an O region of TMEM, so that the tensor core
+//     computes the next scores while the softmax warps work;
+//   * warps 0-3 (softmax, thread = query row = TMEM lane): read the S row
+//     with tcgen05.ld, apply the causal mask, keep the running max and sums
+//     (online softmax, the section-1 FA-1/2 idea), write P as bf16 into a
+//     swizzled shared-memory tile for the PV MMA, and rescale the O row in
+//     TMEM only when the running max grew by more than 2^8 (the rescale guard
+//     the same page's section 4 says must stay on; skipping smaller growths
+//     is exact because O and the row sums share the stale reference);
+//   * the same warps finish with O / l, write bf16 out and the fp32 lse.
+// Fully masked KV tiles are never visited: the planner clips tok_end.
+#include <cuda_bf16.h>
+
+#include "fi_internal.h"
+#include "kernels.cuh"
+#include "ptx.cuh"
+
+namespace fi {
+
+namespace {
+
+using namespace dev;
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kRescaleThreshold = 8.0f;   // log2 units: rescale when the max grows by > 2^8
+
+template <int HEAD_DIM>
+struct PrefillCfg {
+  static constexpr int M = kPrefillTileM;                   // 128 query rows
+  static constexpr int N = HEAD_DIM <= 128 ? 128 : 64;      // KV tokens per tile
+  static constexpr int DBLK = HEAD_DIM / 64;                // 128-byte slices of a row
+  static constexpr int THREADS = 192;                       // 4 softmax + producer + MMA warps
+  static constexpr int Q_BYTES = DBLK * M * 128;
+  static constexpr int KV_BYTES = DBLK * N * 128;           // one K (or V) tile
+  static constexpr int P_BYTES = (N / 64) * M * 128;
+  static constexpr int OFF_Q = 0;
+  static constexpr int OFF_K = OFF_Q + Q_BYTES;
+  static constexpr int OFF_V = OFF_K + 2 * KV_BYTES;
+  static constexpr int OFF_P = OFF_V + 2 * KV_BYTES;
+  static constexpr int USED = OFF_P + P_BYTES;
+  // keep one CTA per SM (each CTA takes all 512 TMEM columns)
+  static constexpr int SMEM_BYTES = (USED < 120 * 1024 ? 120 * 1024 : USED) + 1024;
+  static constexpr uint32_t TMEM_COLS = 512;
+  static constexpr uint32_t COL_S = 0;                      // two S buffers: [0,N), [N,2N)
+  static constexpr uint32_t COL_O = 2 * N;                  // O: [2N, 2N+HEAD_DIM)
+  static_assert(COL_O + HEAD_DIM <= TMEM_COLS, "TMEM budget");
+  static_assert(SMEM_BYTES <= 227 * 1024, "shared-memory budget");
+  static constexpr uint32_t IDESC_QK = idesc_bf16(M, N, 0, 0);          // K-major Q and K
+  static constexpr uint32_t IDESC_PV = idesc_bf16(M, HEAD_DIM, 0, 1);   // K-major P, MN-major V
+};
+
+struct PrefillBarriers {
+  uint64_t q_full;
+  uint64_t k_full[2], k_empty[2];
+  uint64_t v_full[2], v_empty[2];
+  uint64_t s_full[2], s_free[2];
+  uint64_t p_full, pv_done, o_final, drain;
+};
+
+__device__ __forceinline__ uint32_t swz(int r, int c8) {
+  return uint32_t(r * 128 + ((c8 ^ (r & 7)) << 4));
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
+                                             uint32_t d) {
+  asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
+               "r"(d)
+               : "memory");
+}
+
+template <int HEAD_DIM>
+__global__ void __launch_bounds__(PrefillCfg<HEAD_DIM>::THREADS, 1)
+prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant__ CUtensorMap k_map,
+               const __grid_constant__ CUtensorMap v_map, PrefillParams prm) {
+  using C = PrefillCfg<HEAD_DIM>;
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ __align__(8) PrefillBarriers bars;
+  __shared__ uint32_t tmem_base_sh;
+  __shared__ int abort_flag;
+
+  const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const WorkItem item = prm.items[blockIdx.x];
+  const int req = item.req, head = item.head, kv_head = head / prm.group;
+  const int n_tiles = (item.tok_end + C::N - 1) / C::N;
+  const uint64_t limit = prm.wait_limit_ns;
+
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&bars.q_full), 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(smem_u32(&bars.k_full[s]), 1);
+      mbar_init(smem_u32(&bars.k_empty[s]), 1);
+      mbar_init(smem_u32(&bars.v_full[s]), 1);
+      mbar_init(smem_u32(&bars.v_empty[s]), 1);
+      mbar_init(smem_u32(&bars.s_full[s]), 1);
+      mbar_init(smem_u32(&bars.s_free[s]), 4);
+    }
+    mbar_init(smem_u32(&bars.p_full), 4);
+    mbar_init(smem_u32(&bars.pv_done), 1);
+    mbar_init(smem_u32(&bars.o_final), 1);
+    mbar_init(smem_u32(&bars.drain), 1);
+    abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 5) {
+    tmem_alloc(smem_u32(&tmem_base_sh), C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_base_sh;
+
+  if (warp == 4) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      prefetch_tensormap(&q_map);
+      prefetch_tensormap(&k_map);
+      prefetch_tensormap(&v_map);
+      const uint32_t qb = smem_u32(&bars.q_full);
+      mbar_arrive_expect_tx(qb, C::Q_BYTES);
+#pragma unroll
+      for (int c = 0; c < C::DBLK; ++c)
+        tma_load_3d(base + C::OFF_Q + c * C::M * 128, &q_map, qb, c * 64, head, item.q_row);
+    }
+    const int P = prm.page_size;
+    const int ppt = C::N / P;
+    const uint32_t box = uint32_t(P) * 128u;
+    int issued_k = 0, issued_v = 0;
+    bool ok = true;
+    for (int j = 0; j < n_tiles; ++j) {
+      const int st = j & 1;
+      const int ntok = min(C::N, item.tok_end - j * C::N);
+      const int np = (ntok + P - 1) / P;
+      int page = -1;
+      bool valid = false;
+      if (lane < np) {
+        page = prm.page_indices[item.page_begin + j * ppt + lane];
+        valid = page >= 0 && page < prm.num_pages;
+        if (!valid) atomicOr(prm.err, kErrBounds);
+      }
+      const uint32_t bytes =
+          uint32_t(__popc(__ballot_sync(0xffffffffu, valid))) * C::DBLK * box;
+      const int c1 = prm.layout == FI_LAYOUT_NHD ? kv_head : 0;
+      const int c2 = prm.layout == FI_LAYOUT_NHD ? 0 : kv_head;
+      if (j >= 2 && !mbar_wait_warp(smem_u32(&bars.k_empty[st]), ((j >> 1) & 1) ^ 1, limit,
+                                    &abort_flag)) {
+        ok = false;
+        break;
+      }
+      const uint32_t kf = smem_u32(&bars.k_full[st]);
+      if (lane == 0) mbar_arrive_expect_tx(kf, bytes);
+      __syncwarp();
+      if (valid) {
+        const uint32_t dst = base + C::OFF_K + st * C::KV_BYTES + lane * box;
+#pragma unroll
+        for (int c = 0; c < C::DBLK; ++c)
+          tma_load_4d(dst + c * C::N * 128, &k_map, kf, c * 64, c1, c2, page);
+      }
+      issued_k = j + 1;
+      if (j >= 2 && !mbar_wait_warp(smem_u32(&bars.v_empty[st]), ((j >> 1) & 1) ^ 1, limit,
+                                    &abort_flag)) {
+        ok = false;
+        break;
+      }
+      const uint32_t vf = smem_u32(&bars.v_full[st]);
+      if (lane == 0) mbar_arrive_expect_tx(vf, bytes);
+      __syncwarp();
+      if (valid) {
+        const uint32_t dst = base + C::OFF_V + st * C::KV_BYTES + lane * box;
+#pragma unroll
+        for (int c = 0; c < C::DBLK; ++c)
+          tma_load_4d(dst + c * C::N * 128, &v_map, vf, c * 64, c1, c2, page);
+      }
+      issued_v = j + 1;
+    }
+    if (!ok) {
+      if (lane == 0) { abort_flag = 1; atomicOr(prm.err, kErrTimeout); }
+      // let every copy this CTA issued land before the CTA exits
+      for (int j = max(0, issued_k - 2); j < issued_k; ++j)
+        mbar_wait_bounded(smem_u32(&bars.k_full[j & 1]), (j >> 1) & 1, limit, nullptr);
+      for (int j = max(0, issued_v - 2); j < issued_v; ++j)
+        mbar_wait_bounded(smem_u32(&bars.v_full[j & 1]), (j >> 1) & 1, limit, nullptr);
+    }
+    if (lane == 0) mbar_wait_bounded(smem_u32(&bars.q_full), 0, limit, nullptr);
+    __syncwarp();
+  } else if (warp == 5) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      bool ok = mbar_wait_bounded(smem_u32(&bars.q_full), 0, limit, &abort_flag);
+      const uint32_t q_base = base + C::OFF_Q;
+      for (int j = 0; ok && j <= n_tiles; ++j) {
+        if (j < n_tiles) {
+          const int st = j & 1;
+          ok = mbar_wait_bounded(smem_u32(&bars.k_full[st]), (j >> 1) & 1, limit, &abort_flag);
+          if (ok && j >= 2)
+            ok = mbar_wait_bounded(smem_u32(&bars.s_free[st]), ((j >> 1) & 1) ^ 1, limit,
+                                   &abort_flag);
+          if (!ok) break;
+          tc_fence_after();
+          const uint32_t k_base = base + C::OFF_K + st * C::KV_BYTES;
+          const uint32_t s_col = tmem + C::COL_S + st * C::N;
+#pragma unroll
+          for (int k = 0; k < HEAD_DIM / 16; ++k) {
+            const uint64_t a = sdesc_sw128(q_base + (k >> 2) * C::M * 128 + (k & 3) * 32, 16, 1024);
+            const uint64_t bd =
+                sdesc_sw128(k_base + (k >> 2) * C::N * 128 + (k & 3) * 32, 16, 1024);
+            tc_mma_ss(s_col, a, bd, C::IDESC_QK, k > 0 ? 1u : 0u);
+          }
+          tc_commit(smem_u32(&bars.s_full[st]));
+          tc_commit(smem_u32(&bars.k_empty[st]));
+        }
+        if (j >= 1) {
+          const int jj = j - 1, st = jj & 1;
+          ok = mbar_wait_bounded(smem_u32(&bars.p_full), jj & 1, limit, &abort_flag);
+          if (ok)
+            ok = mbar_wait_bounded(smem_u32(&bars.v_full[st]), (jj >> 1) & 1, limit,
+                                   &abort_flag);
+          if (!ok) break;
+          tc_fence_after();
+          const uint32_t v_base = base + C::OFF_V + st * C::KV_BYTES;
+#pragma unroll
+          for (int k = 0; k < C::N / 16; ++k) {
+            const uint64_t a =
+                sdesc_sw128(base + C::OFF_P + (k >> 2) * C::M * 128 + (k & 3) * 32, 16, 1024);
+            // MN-major V: 16 tokens per step; the next 64 dims one K-tile slice further
+            const uint64_t bd = sdesc_sw128(v_base + k * 16 * 128, C::N * 128, 1024);
+            tc_mma_ss(tmem + C::COL_O, a, bd, C::IDESC_PV, (jj > 0 || k > 0) ? 1u : 0u);
+          }
+          tc_commit(smem_u32(&bars.v_empty[st]));
+          tc_commit(smem_u32(&bars.pv_done));
+        }
+      }
+      if (ok) {
+        tc_commit(smem_u32(&bars.o_final));
+      } else {
+        abort_flag = 1;
+        atomicOr(prm.err, kErrTimeout);
+        // every MMA issued so far completes before the TMEM is released
+        tc_commit(smem_u32(&bars.drain));
+        mbar_wait_bounded(smem_u32(&bars.drain), 0, limit, nullptr);
+      }
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ softmax + epilogue
+    const int t = threadIdx.x;                       // query row of the tile = TMEM lane
+    const uint32_t lane_off = uint32_t(warp * 32) << 16;
+    const int q_start = prm.qo_indptr[req], q_end = prm.qo_indptr[req + 1];
+    const int qo_len = q_end - q_start;
+    const int np_req = prm.page_indptr[req + 1] - prm.page_indptr[req];
+    const int kv_len = np_req > 0 ? (np_req - 1) * prm.page_size + prm.last_page_len[req] : 0;
+    const int i_req = item.q_row - q_start + t;      // row index within the request
+    int t_max = prm.causal ? (kv_len - qo_len + i_req) : (kv_len - 1);
+    t_max = min(t_max, kv_len - 1);                  // last visible key of this row
+    const float scale = prm.sm_scale * kLog2e;
+    // l: sum of the exact weights (gives lse); lp: sum of the bf16-rounded
+    // weights the PV MMA multiplies (normalises O)
+    float m = -INFINITY, l = 0.f, lp = 0.f;
+    bool ok = true;
+
+    for (int j = 0; j < n_tiles; ++j) {
+      const int st = j & 1;
+      if (!mbar_wait_warp(smem_u32(&bars.s_full[st]), (j >> 1) & 1, limit, &abort_flag)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      uint32_t sr[C::N / 32][32];
+#pragma unroll
+      for (int c = 0; c < C::N / 32; ++c)
+        tmem_ld32(tmem + lane_off + C::COL_S + st * C::N + c * 32, sr[c]);
+      tmem_wait_ld();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&bars.s_free[st]));
+
+      const int col0 = j * C::N;
+      float s[C::N];
+      float mx = -INFINITY;
+#pragma unroll
+      for (int k = 0; k < C::N; ++k) {
+        const float v = __uint_as_float(sr[k >> 5][k & 31]) * scale;
+        s[k] = (col0 + k <= t_max) ? v : -INFINITY;
+        mx = fmaxf(mx, s[k]);
+      }
+      const float m_new = fmaxf(m, mx);
+      const bool grow = m_new > m + kRescaleThreshold;
+      const bool o_live = grow && (m != -INFINITY);  // O row holds data that must be rescaled
+      float alpha = 1.f;
+      if (grow) {
+        alpha = ex2(m - m_new);
+        l *= alpha;
+        lp *= alpha;
+        m = m_new;
+      }
+      const float ref = (m == -INFINITY) ? 0.f : m;
+      float rs = 0.f;
+#pragma unroll
+      for (int k = 0; k < C::N; ++k) {
+        s[k] = ex2(s[k] - ref);
+        rs += s[k];
+      }
+      l += rs;
+
+      // P buffer and O are free once the previous PV has completed
+      if (j >= 1) {
+        if (!mbar_wait_warp(smem_u32(&bars.pv_done), (j - 1) & 1, limit, &abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        if (__any_sync(0xffffffffu, o_live)) {
+#pragma unroll 1
+          for (int c = 0; c < HEAD_DIM / 32; ++c) {
+            uint32_t r[32];
+            tmem_ld32(tmem + lane_off + C::COL_O + c * 32, r);
+            tmem_wait_ld();
+#pragma unroll
+            for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
+            tmem_st32(tmem + lane_off + C::COL_O + c * 32, r);
+          }
+          tmem_wait_st();
+        }
+      }
+      // Last tile: V rows past the valid keys may hold unused page slots or
+      // stale data; zero them so that P = 0 there cannot meet a NaN.
+      const int valid = item.tok_end - col0;
+      if (valid < C::N) {
+        if (!mbar_wait_warp(smem_u32(&bars.v_full[st]), (j >> 1) & 1, limit, &abort_flag)) {
+          ok = false;
+          break;
+        }
+        if (t >= valid && t < C::N) {
+#pragma unroll
+          for (int c = 0; c < C::DBLK; ++c)
+#pragma unroll
+            for (int c8 = 0; c8 < 8; ++c8)
+              st_shared_v4(base + C::OFF_V + st * C::KV_BYTES + c * C::N * 128 + t * 128 + c8 * 16,
+                           0u, 0u, 0u, 0u);
+        }
+      }
+      // P row t as bf16, K-major 128B-swizzled (A operand of the PV MMA).
+      // lp adds the same rounded values the tensor core multiplies, so that
+      // the final division normalises exactly the weights applied.
+      float rsp = 0.f;
+#pragma unroll
+      for (int kb = 0; kb < C::N / 64; ++kb) {
+#pragma unroll
+        for (int c8 = 0; c8 < 8; ++c8) {
+          const int k0 = kb * 64 + c8 * 8;
+          const uint32_t w0 = pack_bf16x2(s[k0], s[k0 + 1]);
+          const uint32_t w1 = pack_bf16x2(s[k0 + 2], s[k0 + 3]);
+          const uint32_t w2 = pack_bf16x2(s[k0 + 4], s[k0 + 5]);
+          const uint32_t w3 = pack_bf16x2(s[k0 + 6], s[k0 + 7]);
+          rsp += (bf16lo(w0) + bf16hi(w0)) + (bf16lo(w1) + bf16hi(w1)) +
+                 (bf16lo(w2) + bf16hi(w2)) + (bf16lo(w3) + bf16hi(w3));
+          st_shared_v4(base + C::OFF_P + kb * C::M * 128 + swz(t, c8), w0, w1, w2, w3);
+        }
+      }
+      lp += rsp;
+      fence_proxy_async_smem();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&bars.p_full));
+    }
+
+    if (ok && n_tiles > 0) {
+      ok = mbar_wait_warp(smem_u32(&bars.o_final), 0, limit, &abort_flag);
+      tc_fence_after();
+    }
+    if (!ok) {
+      if (lane == 0) { abort_flag = 1; atomicOr(prm.err, kErrTimeout); }
+    } else {
+      const int rows = min(C::M, q_end - item.q_row);
+      const bool row_ok = t < rows;
+      const float inv = lp > 0.f ? 1.f / lp : 0.f;
+      const size_t out_row = size_t(item.q_row) + t;
+      __nv_bfloat16* op = reinterpret_cast<__nv_bfloat16*>(prm.out) +
+                          (out_row * prm.num_qo_heads + head) * HEAD_DIM;
+#pragma unroll 1
+      for (int c = 0; c < HEAD_DIM / 32; ++c) {
+        uint32_t r[32];
+        if (n_tiles > 0) {
+          tmem_ld32(tmem + lane_off + C::COL_O + c * 32, r);
+          tmem_wait_ld();
+        } else {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) r[e] = 0u;
+        }
+        if (row_ok) {
+          uint4* dst = reinterpret_cast<uint4*>(op + c * 32);
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4) {
+            const float* f = reinterpret_cast<const float*>(r) + q4 * 8;
+            dst[q4] = make_uint4(pack_bf16x2(f[0] * inv, f[1] * inv),
+                                 pack_bf16x2(f[2] * inv, f[3] * inv),
+                                 pack_bf16x2(f[4] * inv, f[5] * inv),
+                                 pack_bf16x2(f[6] * inv, f[7] * inv));
+          }
+        }
+      }
+      if (row_ok && prm.lse)
+        prm.lse[out_row * prm.num_qo_heads + head] =
+            l > 0.f ? (m + lg2(l)) * kLn2 : -INFINITY;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 5) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+}
+
+template <int HEAD_DIM>
+cudaError_t launch_prefill_t(const CUtensorMap& qm, const CUtensorMap& km, const CUtensorMap& vm,
+                             const PrefillParams& p, int n_items, cudaStream_t stream) {
+  using C = PrefillCfg<HEAD_DIM>;
+  auto kern = prefill_kernel<HEAD_DIM>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       C::SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  kern<<<n_items, C::THREADS, C::SMEM_BYTES, stream>>>(qm, km, vm, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_prefill(int head_dim, const CUtensorMap& qm, const CUtensorMap& km,
+                           const CUtensorMap& vm, const PrefillParams& p, int n_items,
+                           cudaStream_t stream) {
+  if (n_items <= 0) return cudaSuccess;
+  switch (head_dim) {
+    case 64: return launch_prefill_t<64>(qm, km, vm, p, n_items, stream);
+    case 128: return launch_prefill_t<128>(qm, km, vm, p, n_items, stream);
+    case 256: return launch_prefill_t<256>(qm, km, vm, p, n_items, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace fi

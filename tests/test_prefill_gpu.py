@@ -1,0 +1,165 @@
+"""GPU parity of causal variable-length prefill (and mixed prefill + decode
+batches) against the fp64 oracle, through fi_batch_prefill_paged. Small
+cases are compared on every row; the full-size workloads on sampled rows
+(first/last rows, tile and page boundaries, random rows) that the oracle
+computes one by one."""
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+
+import oracle  # noqa: E402
+from paged_kv_attention_27_gb300 import binding as B  # noqa: E402
+from paged_kv_attention_27_gb300 import synth  # noqa: E402
+
+from ._gpu import compare, ensure_built  # noqa: E402
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    ensure_built()
+    B.lib()
+
+
+def _run(b, sms=None):
+    from paged_kv_attention_27_gb300.device import DeviceBatch
+    db = DeviceBatch(b, mode=B.FI_MODE_PREFILL, sms=sms)
+    out, lse = db.run()
+    torch.cuda.synchronize()
+    assert db.status() == B.FI_OK
+    return db, out, lse
+
+
+def _oracle(b, rows=None, requests=None):
+    return oracle.batch_attention(b.q, b.qo_indptr, b.k_cache, b.v_cache, b.layout, b.page_indptr,
+                                  b.page_indices, b.last_page_len, b.num_qo_heads, b.num_kv_heads,
+                                  b.page_size, b.sm_scale, b.causal, requests=requests, rows=rows)
+
+
+def check_full(b, what=None):
+    db, out, lse = _run(b)
+    ref_o, ref_l = _oracle(b)
+    compare(out, lse, ref_o, ref_l, what=what or b.name)
+    return db
+
+
+def sample_rows(b, per_request=24, seed=0):
+    """Rows per request: first, last, around 128-row tile boundaries and the
+    first page boundary, plus random rows."""
+    rng = np.random.default_rng(seed)
+    rows = {}
+    for r in range(b.batch):
+        n = int(b.qo_lens[r])
+        if n == 0:
+            continue
+        s = {0, n - 1, min(n - 1, 1)}
+        for t in range(127, n, 128):
+            s.update({t, min(n - 1, t + 1)})
+            if len(s) > per_request // 2:
+                break
+        s.update({min(n - 1, b.page_size - 1), min(n - 1, b.page_size)})
+        s.update(rng.integers(0, n, size=per_request // 2).tolist())
+        rows[r] = sorted(s)
+    return rows
+
+
+def check_sampled(b, per_request=24, requests=None):
+    db, out, lse = _run(b)
+    rows = sample_rows(b, per_request)
+    if requests is not None:
+        rows = {r: v for r, v in rows.items() if r in requests}
+    ref_o, ref_l = _oracle(b, rows=rows, requests=sorted(rows))
+    flat = np.concatenate([b.qo_indptr[r] + np.asarray(v) for r, v in rows.items()])
+    compare(out, lse, ref_o, ref_l, rows=flat, what=b.name)
+    return db
+
+
+@pytest.mark.parametrize("d,P", [(128, 16), (64, 16), (256, 32), (128, 32), (64, 32), (256, 16)])
+def test_causal_prefill_small(d, P):
+    kv = [1, 2, 17, 128, 129, 300, 513]
+    b = synth.make_batch(f"prefill d{d} P{P}", kv, kv, 8, 2, d, P,
+                         synth.NHD if d != 64 else synth.HND, None, True, 100 + d + P)
+    check_full(b)
+
+
+def test_chunked_prefill_bottom_right_causal():
+    kv = [700, 200, 129, 1000]
+    qo = [37, 200, 128, 300]          # chunks appended to existing KV
+    b = synth.make_batch("chunks", kv, qo, 16, 4, 128, 16, synth.HND, None, True, 7)
+    check_full(b)
+
+
+def test_non_causal_prefill_including_empty_kv():
+    kv = [0, 50, 300, 5]
+    qo = [3, 80, 17, 130]
+    b = synth.make_batch("full attention", kv, qo, 8, 8, 128, 16, synth.NHD, None, False, 8)
+    check_full(b)
+
+
+@pytest.mark.parametrize("g", [1, 2, 4, 8])
+def test_group_sizes(g):
+    kv = [255, 64, 390]
+    b = synth.make_batch(f"prefill g{g}", kv, kv, 2 * g, 2, 128, 16, synth.NHD, None, True, 9 + g)
+    check_full(b)
+
+
+def test_nan_tail_slots_never_reach_the_output():
+    kv = [3, 17, 45, 100, 200]
+    b = synth.make_batch("prefill nan tail", kv, kv, 8, 2, 128, 16, synth.NHD, None, True, 12,
+                         tail_fill="nan")
+    check_full(b)
+    b = synth.make_batch("prefill nan tail d256", kv, kv, 4, 2, 256, 32, synth.HND, None, True,
+                         13, tail_fill="nan")
+    check_full(b)
+
+
+def test_small_mixed_batch_one_call():
+    b = synth.small_mixed()
+    db = check_full(b)
+    info = B.fi_plan_get_info(db.plan)
+    assert info["num_decode_items"] > 0 and info["num_prefill_items"] > 0
+
+
+def test_deterministic():
+    kv = [900, 300]
+    b = synth.make_batch("det", kv, kv, 8, 2, 128, 16, synth.NHD, None, True, 14)
+    db, out, lse = _run(b)
+    o1, l1 = out.clone(), lse.clone()
+    o2, l2 = db.run()
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+def test_large_scores_stay_finite_with_rescale():
+    """Keys scaled page by page from 0x to 6x (sm_scale 1): scores span
+    hundreds of log2 units, the running max jumps many times (the lazy
+    rescale fires), yet outputs match the oracle."""
+    kv = [600, 1000]
+    b = synth.make_batch("big scores", kv, kv, 4, 2, 128, 16, synth.NHD, 1.0, True, 15)
+    ramp = np.linspace(0, 6, b.k_cache.shape[0] * 16, dtype=np.float32).reshape(-1, 16)
+    kf = oracle.bf16_to_f64(b.k_cache).astype(np.float32) * ramp[:, :, None, None]
+    b.k_cache = synth.f32_to_bf16_bits(kf)
+    # |o| ~ 0.25 keeps the bf16 rounding of the nearly one-hot outputs well
+    # inside the mean-abs budget
+    b.v_cache = synth.f32_to_bf16_bits(oracle.bf16_to_f64(b.v_cache).astype(np.float32) * 0.25)
+    check_full(b)
+
+
+# ---- full-size workloads, sampled rows ------------------------------------
+
+@pytest.mark.parametrize("L", [1024, 4096, 16384])
+def test_causal_prefill_70b_full_size(L):
+    check_sampled(synth.causal_prefill(L), per_request=16 if L > 4096 else 24)
+
+
+def test_ragged_prefill_full_size():
+    check_sampled(synth.ragged_prefill(), per_request=16)
+
+
+def test_mixed_chunk_decode_full_size():
+    b = synth.mixed_chunk_decode()
+    check_sampled(b, per_request=16, requests=set(range(8)) | {8, 9, 20, 33, 63})
