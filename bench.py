@@ -47,8 +47,9 @@ def parse_args():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="llama7b_decode",
-                    choices=["llama7b_decode", "llama70b_gqa_decode", "tiny_decode"])
+    ap.add_argument("--workload", default="llama7b_decode", choices=sorted(WORKLOADS))
+    ap.add_argument("--no-secondary", action="store_true",
+                    help="skip the 4K causal prefill measurement added to the default line")
     ap.add_argument("--batch", type=int, default=None,
                     help="override the workload's request count (smaller profiling cases)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -65,10 +66,45 @@ def peaks():
         return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, "fallback"
 
 
+WORKLOADS = {
+    "llama7b_decode": ("llama7b_decode", {}),
+    "llama70b_gqa_decode": ("llama70b_gqa_decode", {}),
+    "tiny_decode": ("tiny_decode", {}),
+    "causal_prefill_1k": ("causal_prefill", {"seq_len": 1024}),
+    "causal_prefill_4k": ("causal_prefill", {"seq_len": 4096}),
+    "causal_prefill_16k": ("causal_prefill", {"seq_len": 16384}),
+    "ragged_prefill": ("ragged_prefill", {}),
+    "mixed_chunk_decode": ("mixed_chunk_decode", {}),
+}
+
+
 def make_workload(name, batch=None):
     from paged_kv_attention_27_gb300 import synth
-    fn = getattr(synth, name)
-    return fn() if batch is None else fn(batch=batch)
+    fn_name, kw = WORKLOADS[name]
+    kw = dict(kw)
+    if batch is not None:
+        kw["batch"] = batch
+    return getattr(synth, fn_name)(**kw)
+
+
+def visible_pairs(b):
+    """(query row, key) pairs the mask leaves visible, summed over requests."""
+    total = 0
+    for qo, kv in zip(b.qo_lens.tolist(), b.kv_lens.tolist()):
+        if not b.causal:
+            total += qo * kv
+            continue
+        first = kv - qo + 1            # keys seen by row 0; row i sees first + i (<= kv)
+        if first >= 1:
+            total += qo * first + qo * (qo - 1) // 2
+        else:
+            total += sum(min(kv, max(0, first + i)) for i in range(qo))
+    return total
+
+
+def attention_flops(b):
+    """Causal-triangle FLOPs: 2*d for QK^T plus 2*d for PV per visible pair per head."""
+    return 4 * b.head_dim * b.num_qo_heads * visible_pairs(b)
 
 
 def kv_bytes(b):
@@ -92,6 +128,7 @@ def io_bytes(b):
 
 KERNEL_SOURCES = {
     "decode_kernel": ["decode.cu", "ptx.cuh", "kernels.cuh", "fi_internal.h"],
+    "prefill_kernel": ["prefill.cu", "ptx.cuh", "kernels.cuh", "fi_internal.h"],
 }
 
 
@@ -254,13 +291,105 @@ def run_reference(args, rank, world):
 # our arm
 # ----------------------------------------------------------------------------
 
+def time_steps(db, K, W, dist=None, sampler=None):
+    """W untimed steps, then K steps bracketed by a barrier and a device
+    synchronisation on both sides, timed with CUDA events on the launching
+    stream. Returns (ms for the K steps, mean ms of the attention kernels
+    alone, from events the library records around them)."""
+    import torch
+    from paged_kv_attention_27_gb300 import binding as B
+
+    stream = torch.cuda.current_stream()
+    for _ in range(max(W, 1)):
+        db.run()
+    torch.cuda.synchronize()
+    st = db.status()
+    assert st == B.FI_OK, B.status_string(st)
+    ks = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ke = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    for ev in ks + ke:          # create the CUDA events (torch creates them on first record)
+        ev.record(stream)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    if sampler:
+        sampler.mark_start()
+    t_start.record(stream)
+    for i in range(K):
+        B.fi_profile_next_launch(ks[i], ke[i])
+        db.run()
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    if sampler:
+        sampler.mark_end()
+    if dist:
+        dist.barrier()
+    st = db.status()
+    assert st == B.FI_OK, B.status_string(st)
+    ms_total = t_start.elapsed_time(t_end)
+    kern_ms = sum(a.elapsed_time(e) for a, e in zip(ks, ke)) / K
+    if dist:
+        t = torch.tensor([ms_total], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_total = float(t.item())
+    return ms_total, kern_ms
+
+
+def config_of(b, info, kvb, flops):
+    return {"workload": b.name, "batch": b.batch, "num_qo_heads": b.num_qo_heads,
+            "num_kv_heads": b.num_kv_heads, "head_dim": b.head_dim, "page_size": b.page_size,
+            "layout": b.layout, "causal": b.causal, "kv_tokens": int(b.kv_lens.sum()),
+            "q_rows": int(b.qo_lens.sum()), "kv_bytes_per_step": kvb,
+            "attention_flops_per_step": flops, "io_bytes_per_step": io_bytes(b),
+            "l2": f"inputs larger than L2 ({(kvb + io_bytes(b)) / 1e9:.2f} GB of KV, q and out "
+                  "per step vs 129 MB L2): no flush",
+            "plan": {k: info[k] for k in ("num_decode_items", "num_prefill_items",
+                                          "chunk_tokens", "num_split_requests")}}
+
+
+def roofline_of(b, kvb, flops, kern_ms, kernel_names, workload):
+    hbm, bf16, src = peaks()
+    try:
+        bf16_sus = float(json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
+                         ["bf16_tflops_sustained"])
+    except Exception:
+        bf16_sus = 1700.0
+    gbs = kvb / (kern_ms / 1e3) / 1e9
+    tfs = flops / (kern_ms / 1e3) / 1e12
+    f_hbm, f_tc = gbs / hbm, tfs / bf16_sus
+    label = "of measured" if src == "measured" else "of fallback"
+    if f_hbm >= f_tc:
+        r = {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s", "frac": f_hbm,
+             "peak_source": f"hbm_gbs {label} (MEASURED_PEAKS.json)"}
+    else:
+        r = {"bound": "tensor", "achieved": tfs, "peak": bf16_sus, "unit": "TFLOP/s",
+             "frac": f_tc, "peak_source": f"bf16_tflops_sustained {label} (the kernel runs back "
+                                          "to back for the whole timed loop)"}
+    r["traffic"] = committed_traffic(workload, kernel_names[0]) if kernel_names else None
+    r["kernel"] = "+".join(kernel_names)
+    r["kernel_ms"] = kern_ms
+    r["hbm_frac"] = f_hbm
+    r["tensor_frac"] = f_tc
+    return r
+
+
+def kernels_of(b, info):
+    names = []
+    if info["num_prefill_items"]:
+        names.append("prefill_kernel")
+    if info["num_decode_items"]:
+        names.append("decode_kernel")
+    return names
+
+
 def run_ours(args, rank, world, local_rank):
-    import numpy as np
     import torch
 
     from paged_kv_attention_27_gb300 import binding as B
     from paged_kv_attention_27_gb300 import build as _build
-    from paged_kv_attention_27_gb300.device import DeviceBatch, num_sms
+    from paged_kv_attention_27_gb300.device import DeviceBatch
 
     torch.cuda.set_device(local_rank)
     _build.build()
@@ -274,106 +403,136 @@ def run_ours(args, rank, world, local_rank):
     db = DeviceBatch(b, device=f"cuda:{local_rank}")
     info = B.fi_plan_get_info(db.plan)
     kvb = kv_bytes(b)
-    iob = io_bytes(b)
+    flops = attention_flops(b)
     launches_per_step = (1 if info["num_decode_items"] else 0) + \
                         (1 if info["num_prefill_items"] else 0) + \
                         (1 if info["num_split_requests"] else 0)
 
-    # cpu baseline first (rank 0, N = 1 only), before the device is busy
+    # CPU baseline first (rank 0, N = 1 only), before the device is busy
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        v, dt, thr, done = oracle_sample(b)
-        cpu = {"value": v, "unit": "GB/s", "cores": thr, "kind": "oracle",
-               "sample": f"fp64 oracle over {len(done)} of {b.batch} requests of the same batch "
-                         f"(batch order, {thr} threads, {dt:.1f} s)"}
-
-    stream = torch.cuda.current_stream()
-    for _ in range(max(args.warmup, 1)):
-        db.run()
-    torch.cuda.synchronize()
-    assert db.status() == B.FI_OK
+        cpu = cpu_baseline(b)
 
     sampler = ClockSampler(local_rank)
     sampler.start()
     time.sleep(0.3)
     K = args.steps
-    ks = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
-    ke = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
-    t_start = torch.cuda.Event(enable_timing=True)
-    t_end = torch.cuda.Event(enable_timing=True)
-    for ev in ks + ke:          # create the CUDA events (torch creates them on first record)
-        ev.record(stream)
-    if dist:
-        dist.barrier()
-    torch.cuda.synchronize()
-    sampler.mark_start()
-    t_start.record(stream)
-    for i in range(K):
-        B.fi_profile_next_launch(ks[i], ke[i])
-        db.run()
-    t_end.record(stream)
-    torch.cuda.synchronize()
-    sampler.mark_end()
-    if dist:
-        dist.barrier()
+    ms_total, kern_ms = time_steps(db, K, args.warmup, dist, sampler)
     sampler.stop()
-    st = db.status()
-    assert st == B.FI_OK, B.status_string(st)
-    ms_total = t_start.elapsed_time(t_end)
-    kern_ms = sum(s.elapsed_time(e) for s, e in zip(ks, ke)) / K
-    if dist:
-        t = torch.tensor([ms_total], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_total = float(t.item())
     ms_step = ms_total / K
-    value = kvb * world / (ms_step / 1e3) / 1e9
+    if info["num_decode_items"]:          # decode or mixed: HBM-bound, KV GB/s
+        value, unit = kvb * world / (ms_step / 1e3) / 1e9, "GB/s"
+    else:                                 # prefill: tensor-bound, TFLOP/s
+        value, unit = flops * world / (ms_step / 1e3) / 1e12, "TFLOP/s"
 
-    # end to end through the C ABI with host buffers
     e2e = None
     if not args.no_e2e:
-        e2e = run_e2e(b, db, K, local_rank)
+        e2e = run_e2e(b, db, K, local_rank, unit)
 
-    hbm, bf16, src = peaks()
-    achieved = kvb / (kern_ms / 1e3) / 1e9
-    kernel_key = f"decode_kernel<{b.head_dim},{b.num_qo_heads // b.num_kv_heads}>"
-    traffic = committed_traffic(args.workload, "decode_kernel")
-    clocks = sampler.summary()
+    secondary = None
+    if args.workload == "llama7b_decode" and args.batch is None and not args.no_secondary:
+        del db
+        torch.cuda.empty_cache()
+        secondary = measure_secondary("causal_prefill_4k", max(5, min(K, 30)), args.warmup, dist)
+
     line = {
-        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": K,
+        "metric": METRIC, "value": value, "unit": unit, "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded Philox normals rounded to bf16, shuffled page table)",
-        "config": {"workload": b.name, "batch": b.batch, "num_qo_heads": b.num_qo_heads,
-                   "num_kv_heads": b.num_kv_heads, "head_dim": b.head_dim,
-                   "page_size": b.page_size, "layout": b.layout,
-                   "kv_tokens": int(b.kv_lens.sum()), "kv_bytes_per_step": kvb,
-                   "io_bytes_per_step": iob,
-                   "l2": f"inputs larger than L2 ({kvb / 1e9:.2f} GB of KV per step vs 129 MB "
-                         "L2): no flush",
-                   "plan": {k: info[k] for k in ("num_decode_items", "num_prefill_items",
-                                                 "chunk_tokens", "num_split_requests")}},
-        "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
-                     "frac": achieved / hbm, "traffic": traffic,
-                     "kernel": kernel_key, "kernel_ms": kern_ms,
-                     "peak_source": f"{src} hbm_gbs (MEASURED_PEAKS.json)" if src == "measured"
-                     else "fallback 6.8 TB/s"},
-        "tokens_per_s": b.batch * world / (ms_step / 1e3),
+        "config": config_of(b, info, kvb, flops),
+        "roofline": roofline_of(b, kvb, flops, kern_ms, kernels_of(b, info), args.workload),
+        "tflops": flops * world / (ms_step / 1e3) / 1e12,
+        "kv_gbs": kvb * world / (ms_step / 1e3) / 1e9,
+        "tokens_per_s": int(b.qo_lens.sum()) * world / (ms_step / 1e3),
         "cpu_baseline": cpu,
         "e2e": e2e,
         "gpu_launches": launches_per_step * K,
-        "clocks": clocks,
+        "clocks": sampler.summary(),
     }
+    if secondary:
+        line["prefill_4k"] = secondary
     if rank == 0:
         print(json.dumps(line), flush=True)
     if dist:
         dist.destroy_process_group()
 
 
-def run_e2e(b, db, K, local_rank):
-    """KV GB/s of a serving step through the C ABI: plan from the host page
-    table, copy q and the page table from pinned host memory, run, copy out
-    and lse back, synchronise. The KV cache stays resident in HBM (it is the
-    cache); only the step's own inputs and outputs cross the host link."""
+def measure_secondary(workload, K, W, dist):
+    """A second workload timed the same way (no CPU baseline, no e2e)."""
+    from paged_kv_attention_27_gb300 import binding as B
+    from paged_kv_attention_27_gb300.device import DeviceBatch
+    b = make_workload(workload)
+    db = DeviceBatch(b)
+    info = B.fi_plan_get_info(db.plan)
+    kvb, flops = kv_bytes(b), attention_flops(b)
+    ms_total, kern_ms = time_steps(db, K, W, dist)
+    ms_step = ms_total / K
+    return {"workload": b.name, "value": flops / (ms_step / 1e3) / 1e12, "unit": "TFLOP/s",
+            "steps": K, "ms_per_step": ms_step, "attention_flops_per_step": flops,
+            "roofline": roofline_of(b, kvb, flops, kern_ms, kernels_of(b, info), workload)}
+
+
+def cpu_baseline(b):
+    """The fp64 oracle on a bounded sample of the same batch."""
+    if b.is_decode and not b.causal:
+        v, dt, thr, done = oracle_sample(b)
+        return {"value": v, "unit": "GB/s", "cores": thr, "kind": "oracle",
+                "sample": f"fp64 oracle over {len(done)} of {b.batch} requests of the same batch "
+                          f"(batch order, {thr} threads, {dt:.1f} s)"}
+    v, dt, thr, nrows = oracle_rows_sample(b)
+    return {"value": v, "unit": "TFLOP/s", "cores": thr, "kind": "oracle",
+            "sample": f"fp64 oracle over {nrows} query rows (the last rows of each request, "
+                      f"which see the most keys; {thr} threads, {dt:.1f} s)"}
+
+
+def oracle_rows_sample(b, budget_s=12.0):
+    """TFLOP/s of the oracle on sampled query rows: the visible pairs of the
+    rows it completed within the budget, over the wall time."""
+    import oracle
+    threads = os.cpu_count() or 1
+    tasks = []
+    for r in range(b.batch):
+        n = int(b.qo_lens[r])
+        for i in range(max(0, n - 64), n):
+            tasks.append((r, i))
+
+    def one(task):
+        r, i = task
+        oracle.batch_attention(b.q, b.qo_indptr, b.k_cache, b.v_cache, b.layout, b.page_indptr,
+                               b.page_indices, b.last_page_len, b.num_qo_heads, b.num_kv_heads,
+                               b.page_size, b.sm_scale, b.causal, requests=[r], rows={r: [i]})
+        qo, kv = int(b.qo_lens[r]), int(b.kv_lens[r])
+        vis = min(kv, kv - qo + i + 1) if b.causal else kv
+        return 4 * b.head_dim * b.num_qo_heads * max(vis, 0)
+
+    done_flops, n = 0, 0
+    t0 = time.perf_counter()
+    with cf.ThreadPoolExecutor(max_workers=threads) as ex:
+        nxt = 0
+        pending = set()
+        while nxt < len(tasks) and len(pending) < threads:
+            pending.add(ex.submit(one, tasks[nxt]))
+            nxt += 1
+        while pending:
+            fin, pending = cf.wait(pending, return_when=cf.FIRST_COMPLETED)
+            for f in fin:
+                done_flops += f.result()
+                n += 1
+            while nxt < len(tasks) and len(pending) < threads and \
+                    time.perf_counter() - t0 < budget_s:
+                pending.add(ex.submit(one, tasks[nxt]))
+                nxt += 1
+    dt = time.perf_counter() - t0
+    return done_flops / dt / 1e12, dt, threads, n
+
+
+def run_e2e(b, db, K, local_rank, unit):
+    """The same metric for a serving step through the C ABI: plan from the
+    host page table, copy q and the page table (and qo_indptr) from pinned
+    host memory, run, copy out and lse back, synchronise. The KV cache stays
+    resident in HBM (it is the cache); only the step's own inputs and
+    outputs cross the host link."""
     import numpy as np
     import torch
 
@@ -386,24 +545,34 @@ def run_e2e(b, db, K, local_rank):
     indptr_h = pin(torch.from_numpy(b.page_indptr.astype(np.int32)))
     indices_h = pin(torch.from_numpy(b.page_indices.astype(np.int32)))
     last_h = pin(torch.from_numpy(b.last_page_len.astype(np.int32)))
+    qo_h = pin(torch.from_numpy(b.qo_indptr.astype(np.int32)))
     out_h = pin(torch.empty_like(db.out, device="cpu"))
     lse_h = pin(torch.empty_like(db.lse, device="cpu"))
     sms = num_sms(dev)
-    h2d = sum(t.numel() * t.element_size() for t in (q_h, indptr_h, indices_h, last_h))
+    decode = db.mode == B.FI_MODE_DECODE
+    ins = (q_h, indptr_h, indices_h, last_h) + (() if decode else (qo_h,))
+    h2d = sum(t.numel() * t.element_size() for t in ins)
     d2h = out_h.numel() * out_h.element_size() + lse_h.numel() * lse_h.element_size()
     layout = B.LAYOUTS[b.layout]
 
     def step():
-        plan = B.fi_plan(B.FI_MODE_DECODE, b.batch, None, indptr_h.numpy(), last_h.numpy(),
-                         b.num_qo_heads, b.num_kv_heads, b.head_dim, b.page_size, 0, sms)
+        plan = B.fi_plan(db.mode, b.batch, None if decode else qo_h.numpy(), indptr_h.numpy(),
+                         last_h.numpy(), b.num_qo_heads, b.num_kv_heads, b.head_dim,
+                         b.page_size, b.causal, sms)
         assert plan.workspace_bytes <= db.workspace.numel()
         db.q.copy_(q_h, non_blocking=True)
         db.page_indptr.copy_(indptr_h, non_blocking=True)
         db.page_indices.copy_(indices_h, non_blocking=True)
         db.last_page_len.copy_(last_h, non_blocking=True)
-        B.fi_batch_decode_paged(plan, db.q, db.k, db.v, layout, 0, b.num_pages, db.page_indptr,
-                                db.page_indices, db.last_page_len, b.sm_scale, db.out, db.lse,
-                                db.workspace)
+        if decode:
+            B.fi_batch_decode_paged(plan, db.q, db.k, db.v, layout, 0, b.num_pages,
+                                    db.page_indptr, db.page_indices, db.last_page_len,
+                                    b.sm_scale, db.out, db.lse, db.workspace)
+        else:
+            db.qo_indptr.copy_(qo_h, non_blocking=True)
+            B.fi_batch_prefill_paged(plan, db.q, db.qo_indptr, db.k, db.v, layout, 0,
+                                     b.num_pages, db.page_indptr, db.page_indices,
+                                     db.last_page_len, b.sm_scale, db.out, db.lse, db.workspace)
         out_h.copy_(db.out, non_blocking=True)
         lse_h.copy_(db.lse, non_blocking=True)
         torch.cuda.current_stream().synchronize()
@@ -415,9 +584,10 @@ def run_e2e(b, db, K, local_rank):
     for _ in range(n):
         step()
     dt = (time.perf_counter() - t0) / n
-    return {"value": kv_bytes(b) / dt / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d,
+    value = kv_bytes(b) / dt / 1e9 if unit == "GB/s" else attention_flops(b) / dt / 1e12
+    return {"value": value, "unit": unit, "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "ms_per_step": dt * 1e3, "steps": n,
-            "includes": "fi_plan on the host + H2D of q and page table + kernels + D2H of "
+            "includes": "fi_plan on the host + H2D of q and the page table + kernels + D2H of "
                         "out and lse, wall clock"}
 
 
