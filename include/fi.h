@@ -159,7 +159,8 @@ fi_status fi_plan_get_work(fi_plan_t plan, int32_t* items_h, int32_t capacity,
  *                    as in the conventions above), num_pages pages each.
  *   page_indptr_d, page_indices_d, last_page_len_d  device int32 copies of
  *                    the planned page table.
- *   sm_scale         score scale (1/sqrt(head_dim) is the usual value).
+ *   sm_scale         score scale, finite and >= 0 (1/sqrt(head_dim) is the
+ *                    usual value); anything else is FI_ERR_INVALID_ARG.
  *   out              device bf16 [B][num_qo_heads][head_dim].
  *   lse              device fp32 [B][num_qo_heads] or NULL.
  *   workspace        device buffer of at least the planned size, 256-byte

@@ -129,6 +129,7 @@ fi_status run_paged(fi_plan_t plan, bool prefill_call, const void* q, const int3
       !aligned(workspace, 256) || (lse && !aligned(lse, 4)))
     return FI_ERR_INVALID_ARG;
   if (kv_layout != FI_LAYOUT_NHD && kv_layout != FI_LAYOUT_HND) return FI_ERR_INVALID_ARG;
+  if (!(sm_scale >= 0.f) || sm_scale > 3.0e38f) return FI_ERR_INVALID_ARG;  // also rejects NaN
   const int64_t page_elems = int64_t(P.page_size) * P.num_kv_heads * P.head_dim;
   if (page_stride_elems == 0) page_stride_elems = page_elems;
   if (page_stride_elems < page_elems || page_stride_elems % 8 != 0) return FI_ERR_INVALID_ARG;

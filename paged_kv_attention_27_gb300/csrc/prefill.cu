@@ -296,16 +296,28 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&bars.s_free[st]));
 
+      // Row max of the raw scores (sm_scale >= 0 commutes with max). Eight
+      // independent accumulators keep the dependency chains short; the mask
+      // is applied only in tiles that cross this warp's causal bound.
       const int col0 = j * C::N;
-      float s[C::N];
-      float mx = -INFINITY;
+      const bool need_mask = __any_sync(0xffffffffu, col0 + C::N - 1 > t_max);
+      float mx8[8];
 #pragma unroll
-      for (int k = 0; k < C::N; ++k) {
-        const float v = __uint_as_float(sr[k >> 5][k & 31]) * scale;
-        s[k] = (col0 + k <= t_max) ? v : -INFINITY;
-        mx = fmaxf(mx, s[k]);
+      for (int i = 0; i < 8; ++i) mx8[i] = -INFINITY;
+      if (need_mask) {
+#pragma unroll
+        for (int k = 0; k < C::N; ++k) {
+          const float v = (col0 + k <= t_max) ? __uint_as_float(sr[k >> 5][k & 31]) : -INFINITY;
+          mx8[k & 7] = fmaxf(mx8[k & 7], v);
+        }
+      } else {
+#pragma unroll
+        for (int k = 0; k < C::N; ++k) mx8[k & 7] = fmaxf(mx8[k & 7], __uint_as_float(sr[k >> 5][k & 31]));
       }
-      const float m_new = fmaxf(m, mx);
+      const float mx_raw = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                                 fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+      const float m_tile = (mx_raw == -INFINITY) ? -INFINITY : mx_raw * scale;
+      const float m_new = fmaxf(m, m_tile);
       const bool grow = m_new > m + kRescaleThreshold;
       const bool o_live = grow && (m != -INFINITY);  // O row holds data that must be rescaled
       float alpha = 1.f;
@@ -316,13 +328,20 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
         m = m_new;
       }
       const float ref = (m == -INFINITY) ? 0.f : m;
-      float rs = 0.f;
+      // p = 2^(s * scale - ref): one FFMA and one ex2 per score
+      float s[C::N];
+      float rs8[8];
 #pragma unroll
-      for (int k = 0; k < C::N; ++k) {
-        s[k] = ex2(s[k] - ref);
-        rs += s[k];
+      for (int i = 0; i < 8; ++i) rs8[i] = 0.f;
+#pragma unroll
+      for (int k = 0; k < C::N; ++k) s[k] = ex2(fmaf(__uint_as_float(sr[k >> 5][k & 31]), scale, -ref));
+      if (need_mask) {
+#pragma unroll
+        for (int k = 0; k < C::N; ++k) s[k] = (col0 + k <= t_max) ? s[k] : 0.f;
       }
-      l += rs;
+#pragma unroll
+      for (int k = 0; k < C::N; ++k) rs8[k & 7] += s[k];
+      l += ((rs8[0] + rs8[1]) + (rs8[2] + rs8[3])) + ((rs8[4] + rs8[5]) + (rs8[6] + rs8[7]));
 
       // P buffer and O are free once the previous PV has completed
       if (j >= 1) {
@@ -364,7 +383,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
       // P row t as bf16, K-major 128B-swizzled (A operand of the PV MMA).
       // lp adds the same rounded values the tensor core multiplies, so that
       // the final division normalises exactly the weights applied.
-      float rsp = 0.f;
+      float rsp4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int kb = 0; kb < C::N / 64; ++kb) {
 #pragma unroll
@@ -374,12 +393,14 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
           const uint32_t w1 = pack_bf16x2(s[k0 + 2], s[k0 + 3]);
           const uint32_t w2 = pack_bf16x2(s[k0 + 4], s[k0 + 5]);
           const uint32_t w3 = pack_bf16x2(s[k0 + 6], s[k0 + 7]);
-          rsp += (bf16lo(w0) + bf16hi(w0)) + (bf16lo(w1) + bf16hi(w1)) +
-                 (bf16lo(w2) + bf16hi(w2)) + (bf16lo(w3) + bf16hi(w3));
+          rsp4[0] += bf16lo(w0) + bf16hi(w0);
+          rsp4[1] += bf16lo(w1) + bf16hi(w1);
+          rsp4[2] += bf16lo(w2) + bf16hi(w2);
+          rsp4[3] += bf16lo(w3) + bf16hi(w3);
           st_shared_v4(base + C::OFF_P + kb * C::M * 128 + swz(t, c8), w0, w1, w2, w3);
         }
       }
-      lp += rsp;
+      lp += (rsp4[0] + rsp4[1]) + (rsp4[2] + rsp4[3]);
       fence_proxy_async_smem();
       tc_fence_before();
       __syncwarp();

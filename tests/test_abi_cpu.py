@@ -232,6 +232,12 @@ def test_workspace_too_small_and_bad_args_return_before_any_launch():
         B.fi_batch_prefill_paged(p, fake, fake, fake, fake, 0, 0, 4, fake, fake, fake, 0.1,
                                  fake, fake, fake, stream=0)
     assert e.value.status == B.FI_ERR_INVALID_ARG
+    for bad_scale in (-0.1, float("nan"), float("inf")):
+        bad = list(args)
+        bad[10] = bad_scale    # sm_scale must be finite and >= 0
+        with pytest.raises(B.FiError) as e:
+            B.fi_batch_decode_paged(*bad, stream=0)
+        assert e.value.status == B.FI_ERR_INVALID_ARG
     with pytest.raises(B.FiError) as e:
         B.fi_batch_decode_paged(*args, stream=0)
     assert e.value.status == B.FI_ERR_NO_DEVICE
