@@ -9,15 +9,19 @@
 // ping-pong buffers), rebuilt for sm_103a:
 //   * warp 4 (producer): TMA loads of the Q tile (once) and, per KV tile of
 //     N tokens, one 128B-swizzled box per (page, 64-dim slice) of K and of V
-//     into two-deep K and V rings;
+//     into K and V rings (three deep for head_dim <= 128);
 //   * warp 5 (MMA issuer; also owns the TMEM allocation): one thread issues
 //     S_j = Q K_j^T into a double-buffered S region of TMEM, then
 //     O += P_{j-1} V_{j-1} into an O region of TMEM, so that the tensor core
-//     computes the next scores while the softmax warps work;
-//   * warps 0-3 (softmax, thread = query row = TMEM lane): read the S row
-//     with tcgen05.ld, apply the causal mask, keep the running max and sums
-//     (online softmax, the section-1 FA-1/2 idea), write P as bf16 into a
-//     swizzled shared-memory tile for the PV MMA, and rescale the O row in
+//     computes the next scores while the softmax warps work. The A operands
+//     (Q for head_dim <= 128, and P) are read from TMEM: with both operands
+//     in shared memory an M=128, N=128 MMA alone would use all of the shared
+//     memory bandwidth, which the K/V copies also need;
+//   * warps 0-3 (softmax, thread = query row = TMEM lane): copy their Q row
+//     into TMEM once, then per tile read the S row with tcgen05.ld, apply the
+//     causal mask, keep the running max and sums (online softmax, the
+//     section-1 FA-1/2 idea), write P as packed bf16 into TMEM for the PV
+//     MMA, and rescale the O row in
 //     TMEM only when the running max grew by more than 2^8 (the rescale guard
 //     the same page's section 4 says must stay on; skipping smaller growths
 //     is exact because O and the row sums share the stale reference);
@@ -45,32 +49,37 @@ struct PrefillCfg {
   static constexpr int N = HEAD_DIM <= 128 ? 128 : 64;      // KV tokens per tile
   static constexpr int DBLK = HEAD_DIM / 64;                // 128-byte slices of a row
   static constexpr int THREADS = 192;                       // 4 softmax + producer + MMA warps
+  static constexpr bool Q_TMEM = HEAD_DIM <= 128;           // Q as a TMEM operand
+  static constexpr int NST = HEAD_DIM <= 128 ? 3 : 2;       // K (and V) ring depth
   static constexpr int Q_BYTES = DBLK * M * 128;
   static constexpr int KV_BYTES = DBLK * N * 128;           // one K (or V) tile
-  static constexpr int P_BYTES = (N / 64) * M * 128;
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_K = OFF_Q + Q_BYTES;
-  static constexpr int OFF_V = OFF_K + 2 * KV_BYTES;
-  static constexpr int OFF_P = OFF_V + 2 * KV_BYTES;
-  static constexpr int USED = OFF_P + P_BYTES;
+  static constexpr int OFF_V = OFF_K + NST * KV_BYTES;
+  static constexpr int USED = OFF_V + NST * KV_BYTES;
   // keep one CTA per SM (each CTA takes all 512 TMEM columns)
   static constexpr int SMEM_BYTES = (USED < 120 * 1024 ? 120 * 1024 : USED) + 1024;
   static constexpr uint32_t TMEM_COLS = 512;
-  static constexpr uint32_t COL_S = 0;                      // two S buffers: [0,N), [N,2N)
-  static constexpr uint32_t COL_O = 2 * N;                  // O: [2N, 2N+HEAD_DIM)
-  static_assert(COL_O + HEAD_DIM <= TMEM_COLS, "TMEM budget");
+  // TMEM columns: two S buffers, O, then (packed bf16 pairs) Q and P
+  static constexpr uint32_t COL_S = 0;                      // [0,N), [N,2N)
+  static constexpr uint32_t COL_O = 2 * N;                  // [2N, 2N+HEAD_DIM)
+  static constexpr uint32_t COL_Q = COL_O + HEAD_DIM;       // HEAD_DIM/2 columns if Q_TMEM
+  static constexpr uint32_t COL_P = COL_Q + (Q_TMEM ? HEAD_DIM / 2 : 0);  // N/2 columns
+  static_assert(COL_P + N / 2 <= TMEM_COLS, "TMEM budget");
   static_assert(SMEM_BYTES <= 227 * 1024, "shared-memory budget");
   static constexpr uint32_t IDESC_QK = idesc_bf16(M, N, 0, 0);          // K-major Q and K
   static constexpr uint32_t IDESC_PV = idesc_bf16(M, HEAD_DIM, 0, 1);   // K-major P, MN-major V
 };
 
+template <int NST>
 struct PrefillBarriers {
-  uint64_t q_full;
-  uint64_t k_full[2], k_empty[2];
-  uint64_t v_full[2], v_empty[2];
+  uint64_t q_full, q_tmem;
+  uint64_t k_full[NST], k_empty[NST];
+  uint64_t v_full[NST], v_empty[NST];
   uint64_t s_full[2], s_free[2];
   uint64_t p_full, pv_done, o_final, drain;
 };
+
 
 __device__ __forceinline__ uint32_t swz(int r, int c8) {
   return uint32_t(r * 128 + ((c8 ^ (r & 7)) << 4));
@@ -94,7 +103,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
                const __grid_constant__ CUtensorMap v_map, PrefillParams prm) {
   using C = PrefillCfg<HEAD_DIM>;
   extern __shared__ uint8_t smem_raw[];
-  __shared__ __align__(8) PrefillBarriers bars;
+  __shared__ __align__(8) PrefillBarriers<C::NST> bars;
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_flag;
 
@@ -108,11 +117,14 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
 
   if (threadIdx.x == 0) {
     mbar_init(smem_u32(&bars.q_full), 1);
-    for (int s = 0; s < 2; ++s) {
+    mbar_init(smem_u32(&bars.q_tmem), 4);
+    for (int s = 0; s < C::NST; ++s) {
       mbar_init(smem_u32(&bars.k_full[s]), 1);
       mbar_init(smem_u32(&bars.k_empty[s]), 1);
       mbar_init(smem_u32(&bars.v_full[s]), 1);
       mbar_init(smem_u32(&bars.v_empty[s]), 1);
+    }
+    for (int s = 0; s < 2; ++s) {
       mbar_init(smem_u32(&bars.s_full[s]), 1);
       mbar_init(smem_u32(&bars.s_free[s]), 4);
     }
@@ -150,7 +162,8 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
     int issued_k = 0, issued_v = 0;
     bool ok = true;
     for (int j = 0; j < n_tiles; ++j) {
-      const int st = j & 1;
+      const int st = j % C::NST;
+      const uint32_t empty_par = ((j / C::NST) & 1) ^ 1;
       const int ntok = min(C::N, item.tok_end - j * C::N);
       const int np = (ntok + P - 1) / P;
       int page = -1;
@@ -164,8 +177,8 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
           uint32_t(__popc(__ballot_sync(0xffffffffu, valid))) * C::DBLK * box;
       const int c1 = prm.layout == FI_LAYOUT_NHD ? kv_head : 0;
       const int c2 = prm.layout == FI_LAYOUT_NHD ? 0 : kv_head;
-      if (j >= 2 && !mbar_wait_warp(smem_u32(&bars.k_empty[st]), ((j >> 1) & 1) ^ 1, limit,
-                                    &abort_flag)) {
+      if (j >= C::NST && !mbar_wait_warp(smem_u32(&bars.k_empty[st]), empty_par, limit,
+                                         &abort_flag)) {
         ok = false;
         break;
       }
@@ -179,8 +192,8 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
           tma_load_4d(dst + c * C::N * 128, &k_map, kf, c * 64, c1, c2, page);
       }
       issued_k = j + 1;
-      if (j >= 2 && !mbar_wait_warp(smem_u32(&bars.v_empty[st]), ((j >> 1) & 1) ^ 1, limit,
-                                    &abort_flag)) {
+      if (j >= C::NST && !mbar_wait_warp(smem_u32(&bars.v_empty[st]), empty_par, limit,
+                                         &abort_flag)) {
         ok = false;
         break;
       }
@@ -198,55 +211,62 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
     if (!ok) {
       if (lane == 0) { abort_flag = 1; atomicOr(prm.err, kErrTimeout); }
       // let every copy this CTA issued land before the CTA exits
-      for (int j = max(0, issued_k - 2); j < issued_k; ++j)
-        mbar_wait_bounded(smem_u32(&bars.k_full[j & 1]), (j >> 1) & 1, limit, nullptr);
-      for (int j = max(0, issued_v - 2); j < issued_v; ++j)
-        mbar_wait_bounded(smem_u32(&bars.v_full[j & 1]), (j >> 1) & 1, limit, nullptr);
+      for (int j = max(0, issued_k - C::NST); j < issued_k; ++j)
+        mbar_wait_bounded(smem_u32(&bars.k_full[j % C::NST]), (j / C::NST) & 1, limit, nullptr);
+      for (int j = max(0, issued_v - C::NST); j < issued_v; ++j)
+        mbar_wait_bounded(smem_u32(&bars.v_full[j % C::NST]), (j / C::NST) & 1, limit, nullptr);
     }
     if (lane == 0) mbar_wait_bounded(smem_u32(&bars.q_full), 0, limit, nullptr);
     __syncwarp();
   } else if (warp == 5) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      bool ok = mbar_wait_bounded(smem_u32(&bars.q_full), 0, limit, &abort_flag);
+      bool ok = C::Q_TMEM
+                    ? mbar_wait_bounded(smem_u32(&bars.q_tmem), 0, limit, &abort_flag)
+                    : mbar_wait_bounded(smem_u32(&bars.q_full), 0, limit, &abort_flag);
       const uint32_t q_base = base + C::OFF_Q;
       for (int j = 0; ok && j <= n_tiles; ++j) {
         if (j < n_tiles) {
-          const int st = j & 1;
-          ok = mbar_wait_bounded(smem_u32(&bars.k_full[st]), (j >> 1) & 1, limit, &abort_flag);
+          const int st = j % C::NST, sb = j & 1;
+          ok = mbar_wait_bounded(smem_u32(&bars.k_full[st]), (j / C::NST) & 1, limit,
+                                 &abort_flag);
           if (ok && j >= 2)
-            ok = mbar_wait_bounded(smem_u32(&bars.s_free[st]), ((j >> 1) & 1) ^ 1, limit,
+            ok = mbar_wait_bounded(smem_u32(&bars.s_free[sb]), ((j >> 1) & 1) ^ 1, limit,
                                    &abort_flag);
           if (!ok) break;
           tc_fence_after();
           const uint32_t k_base = base + C::OFF_K + st * C::KV_BYTES;
-          const uint32_t s_col = tmem + C::COL_S + st * C::N;
+          const uint32_t s_col = tmem + C::COL_S + sb * C::N;
 #pragma unroll
           for (int k = 0; k < HEAD_DIM / 16; ++k) {
-            const uint64_t a = sdesc_sw128(q_base + (k >> 2) * C::M * 128 + (k & 3) * 32, 16, 1024);
             const uint64_t bd =
                 sdesc_sw128(k_base + (k >> 2) * C::N * 128 + (k & 3) * 32, 16, 1024);
-            tc_mma_ss(s_col, a, bd, C::IDESC_QK, k > 0 ? 1u : 0u);
+            if constexpr (C::Q_TMEM) {
+              tc_mma_ts(s_col, tmem + C::COL_Q + k * 8, bd, C::IDESC_QK, k > 0 ? 1u : 0u);
+            } else {
+              const uint64_t a =
+                  sdesc_sw128(q_base + (k >> 2) * C::M * 128 + (k & 3) * 32, 16, 1024);
+              tc_mma_ss(s_col, a, bd, C::IDESC_QK, k > 0 ? 1u : 0u);
+            }
           }
-          tc_commit(smem_u32(&bars.s_full[st]));
+          tc_commit(smem_u32(&bars.s_full[sb]));
           tc_commit(smem_u32(&bars.k_empty[st]));
         }
         if (j >= 1) {
-          const int jj = j - 1, st = jj & 1;
+          const int jj = j - 1, st = jj % C::NST;
           ok = mbar_wait_bounded(smem_u32(&bars.p_full), jj & 1, limit, &abort_flag);
           if (ok)
-            ok = mbar_wait_bounded(smem_u32(&bars.v_full[st]), (jj >> 1) & 1, limit,
+            ok = mbar_wait_bounded(smem_u32(&bars.v_full[st]), (jj / C::NST) & 1, limit,
                                    &abort_flag);
           if (!ok) break;
           tc_fence_after();
           const uint32_t v_base = base + C::OFF_V + st * C::KV_BYTES;
 #pragma unroll
           for (int k = 0; k < C::N / 16; ++k) {
-            const uint64_t a =
-                sdesc_sw128(base + C::OFF_P + (k >> 2) * C::M * 128 + (k & 3) * 32, 16, 1024);
             // MN-major V: 16 tokens per step; the next 64 dims one K-tile slice further
             const uint64_t bd = sdesc_sw128(v_base + k * 16 * 128, C::N * 128, 1024);
-            tc_mma_ss(tmem + C::COL_O, a, bd, C::IDESC_PV, (jj > 0 || k > 0) ? 1u : 0u);
+            tc_mma_ts(tmem + C::COL_O, tmem + C::COL_P + k * 8, bd, C::IDESC_PV,
+                      (jj > 0 || k > 0) ? 1u : 0u);
           }
           tc_commit(smem_u32(&bars.v_empty[st]));
           tc_commit(smem_u32(&bars.pv_done));
@@ -280,8 +300,33 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
     float m = -INFINITY, l = 0.f, lp = 0.f;
     bool ok = true;
 
-    for (int j = 0; j < n_tiles; ++j) {
-      const int st = j & 1;
+    if constexpr (C::Q_TMEM) {
+      // this thread's Q row, from the swizzled TMA tile into TMEM (bf16 pairs)
+      ok = mbar_wait_warp(smem_u32(&bars.q_full), 0, limit, &abort_flag);
+      if (ok) {
+#pragma unroll
+        for (int b = 0; b < C::DBLK; ++b) {
+          uint32_t r[32];
+#pragma unroll
+          for (int c8 = 0; c8 < 8; ++c8) {
+            const uint4 v = lds128(base + C::OFF_Q + b * C::M * 128 + swz(t, c8));
+            r[c8 * 4 + 0] = v.x;
+            r[c8 * 4 + 1] = v.y;
+            r[c8 * 4 + 2] = v.z;
+            r[c8 * 4 + 3] = v.w;
+          }
+          tmem_st32(tmem + lane_off + C::COL_Q + b * 32, r);
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&bars.q_tmem));
+      }
+    }
+
+    for (int j = 0; ok && j < n_tiles; ++j) {
+      const int st = j & 1;                 // S buffer
+      const int kvst = j % C::NST;          // K/V ring stage
       if (!mbar_wait_warp(smem_u32(&bars.s_full[st]), (j >> 1) & 1, limit, &abort_flag)) {
         ok = false;
         break;
@@ -367,7 +412,8 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
       // stale data; zero them so that P = 0 there cannot meet a NaN.
       const int valid = item.tok_end - col0;
       if (valid < C::N) {
-        if (!mbar_wait_warp(smem_u32(&bars.v_full[st]), (j >> 1) & 1, limit, &abort_flag)) {
+        if (!mbar_wait_warp(smem_u32(&bars.v_full[kvst]), (j / C::NST) & 1, limit,
+                            &abort_flag)) {
           ok = false;
           break;
         }
@@ -376,32 +422,27 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
           for (int c = 0; c < C::DBLK; ++c)
 #pragma unroll
             for (int c8 = 0; c8 < 8; ++c8)
-              st_shared_v4(base + C::OFF_V + st * C::KV_BYTES + c * C::N * 128 + t * 128 + c8 * 16,
-                           0u, 0u, 0u, 0u);
+              st_shared_v4(base + C::OFF_V + kvst * C::KV_BYTES + c * C::N * 128 + t * 128 +
+                               c8 * 16, 0u, 0u, 0u, 0u);
         }
       }
-      // P row t as bf16, K-major 128B-swizzled (A operand of the PV MMA).
-      // lp adds the same rounded values the tensor core multiplies, so that
-      // the final division normalises exactly the weights applied.
+      // P row t as packed bf16 pairs into TMEM (the A operand of the PV
+      // MMA). lp adds the same rounded values the tensor core multiplies, so
+      // that the final division normalises exactly the weights applied.
       float rsp4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int kb = 0; kb < C::N / 64; ++kb) {
+        uint32_t w[32];
 #pragma unroll
-        for (int c8 = 0; c8 < 8; ++c8) {
-          const int k0 = kb * 64 + c8 * 8;
-          const uint32_t w0 = pack_bf16x2(s[k0], s[k0 + 1]);
-          const uint32_t w1 = pack_bf16x2(s[k0 + 2], s[k0 + 3]);
-          const uint32_t w2 = pack_bf16x2(s[k0 + 4], s[k0 + 5]);
-          const uint32_t w3 = pack_bf16x2(s[k0 + 6], s[k0 + 7]);
-          rsp4[0] += bf16lo(w0) + bf16hi(w0);
-          rsp4[1] += bf16lo(w1) + bf16hi(w1);
-          rsp4[2] += bf16lo(w2) + bf16hi(w2);
-          rsp4[3] += bf16lo(w3) + bf16hi(w3);
-          st_shared_v4(base + C::OFF_P + kb * C::M * 128 + swz(t, c8), w0, w1, w2, w3);
+        for (int e = 0; e < 32; ++e) {
+          w[e] = pack_bf16x2(s[kb * 64 + 2 * e], s[kb * 64 + 2 * e + 1]);
+          rsp4[e & 3] += bf16lo(w[e]) + bf16hi(w[e]);
         }
+        tmem_st32(tmem + lane_off + C::COL_P + kb * 32, w);
       }
+      tmem_wait_st();
       lp += (rsp4[0] + rsp4[1]) + (rsp4[2] + rsp4[3]);
-      fence_proxy_async_smem();
+      fence_proxy_async_smem();   // zeroed V rows (generic writes) before the MMA reads them
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&bars.p_full));
