@@ -49,14 +49,167 @@ struct DecodeCfg {
   static constexpr int KBYTES = TILE * HEAD_DIM * 2;   // one K (or V) stage
   static constexpr int STAGE_BYTES = 2 * KBYTES;
   static constexpr int SMEM_BYTES = NSTAGE * STAGE_BYTES + 1024;  // + alignment slack
+  // GQA groups of 4 or 8 heads at head_dim <= 128 use the tensor cores: the
+  // g heads are the M rows of m16n8k16 MMAs (padded to 16), 16 tokens per step
+  static constexpr bool MMA = GROUP >= 4 && HEAD_DIM <= 128;
   static_assert(PASSES % SUB == 0, "");
-  static_assert(NCW * GROUP * HEAD_DIM * 4 + 2 * NCW * GROUP * 4 <= NSTAGE * STAGE_BYTES, "");
+  static_assert(!MMA || TOK_PER_WARP % 16 == 0, "");
+  static_assert(NCW * GROUP * HEAD_DIM * 4 + 3 * NCW * GROUP * 4 <= NSTAGE * STAGE_BYTES, "");
 };
 
 // Byte offset of 16-byte chunk `c8` (0..7) of row `r` inside a 128-byte-row
 // slice written by TMA with 128-byte swizzling (slice base 1024-aligned).
 __device__ __forceinline__ uint32_t swz(int r, int c8) {
   return uint32_t(r * 128 + ((c8 ^ (r & 7)) << 4));
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// Tensor-core consumer warp for GQA groups of 4 or 8 heads. Per 16-token
+// chunk of its share of a stage: S (16 x 16, rows = the group's heads padded
+// with zeros) = Q K^T by m16n8k16 MMAs with K read by ldmatrix from the
+// swizzled stage; an online softmax per head row (a quad of lanes holds a
+// row); P rounded to bf16 is reused as the A fragment of O += P V, with V
+// read by ldmatrix.trans. Leaves the warp's (m, l, lp, O) in shared memory
+// and returns whether any consumer aborted (voted, so all agree).
+template <int HEAD_DIM, int GROUP>
+__device__ __forceinline__ bool mma_consumer(const DecodeParams& prm, const WorkItem& item,
+                                             int n_tok, int n_tiles, uint32_t smem_base,
+                                             uint64_t* full_bar, uint64_t* empty_bar,
+                                             int* abort_flag, float* red_o, float* red_m,
+                                             float* red_l, float* red_lp) {
+  using C = DecodeCfg<HEAD_DIM, GROUP>;
+  constexpr int KS = HEAD_DIM / 16;       // k-steps of QK^T
+  constexpr int NTO = HEAD_DIM / 8;       // 8-dim tiles of O
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int r = lane >> 2;                // head row of this lane (valid if < GROUP)
+  const int k0 = (lane & 3) * 2;          // first of the lane's two columns
+  const int mi = lane >> 3, rr = lane & 7;   // ldmatrix: matrix and row this lane addresses
+  const float scale = prm.sm_scale * kLog2e;
+
+  uint32_t qa[KS][4];
+  {
+    const uint32_t* qp = reinterpret_cast<const uint32_t*>(
+        reinterpret_cast<const __nv_bfloat16*>(prm.q) +
+        (size_t(item.q_row) * prm.num_qo_heads + item.head * GROUP + (r < GROUP ? r : 0)) *
+            HEAD_DIM);
+#pragma unroll
+    for (int ks = 0; ks < KS; ++ks) {
+      qa[ks][0] = r < GROUP ? qp[(ks * 16 + k0) >> 1] : 0u;
+      qa[ks][1] = 0u;
+      qa[ks][2] = r < GROUP ? qp[(ks * 16 + 8 + k0) >> 1] : 0u;
+      qa[ks][3] = 0u;
+    }
+  }
+  float o[NTO][4];
+#pragma unroll
+  for (int t = 0; t < NTO; ++t) o[t][0] = o[t][1] = o[t][2] = o[t][3] = 0.f;
+  float m = -INFINITY, l = 0.f, lp = 0.f;
+
+  for (int i = 0; i < n_tiles; ++i) {
+    const int s = i % C::NSTAGE;
+    if (!mbar_wait_warp(smem_u32(&full_bar[s]), (i / C::NSTAGE) & 1, prm.wait_limit_ns,
+                        abort_flag)) {
+      if (lane == 0) { *abort_flag = 1; atomicOr(prm.err, kErrTimeout); }
+      break;
+    }
+    const int ntok = min(C::TILE, n_tok - i * C::TILE);
+    const uint32_t kbase = smem_base + s * C::STAGE_BYTES;
+    const uint32_t vbase = kbase + C::KBYTES;
+#pragma unroll 1
+    for (int cb = warp * C::TOK_PER_WARP; cb < (warp + 1) * C::TOK_PER_WARP; cb += 16) {
+      if (cb >= ntok) break;
+      if (cb + 16 > ntok) {
+        // V rows past the last key hold unused slots or stale data: zero them
+        // so that P = 0 there cannot meet a NaN in the MMA
+        for (int idx = lane; idx < 16 * (HEAD_DIM / 8); idx += 32) {
+          const int row = cb + idx / (HEAD_DIM / 8), c = idx % (HEAD_DIM / 8);
+          if (row >= ntok) {
+            const uint32_t a = vbase + (c >> 3) * C::TILE * 128 + swz(row, c & 7);
+            asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(a), "r"(0u) : "memory");
+          }
+        }
+        __syncwarp();
+      }
+      float sacc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+      for (int ks = 0; ks < KS; ++ks) {
+        const int tok = cb + (mi >> 1) * 8 + rr;
+        const int dim = ks * 16 + (mi & 1) * 8;
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4(kbase + (dim >> 6) * C::TILE * 128 + swz(tok, (dim & 63) >> 3), b0, b1, b2, b3);
+        mma_bf16_16816(sacc[0], qa[ks], b0, b1);
+        mma_bf16_16816(sacc[1], qa[ks], b2, b3);
+      }
+      float sv[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int tok = cb + (e >> 1) * 8 + k0 + (e & 1);
+        sv[e] = tok < ntok ? sacc[e >> 1][e & 1] * scale : -INFINITY;
+      }
+      float mx = fmaxf(fmaxf(sv[0], sv[1]), fmaxf(sv[2], sv[3]));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+      const float m_new = fmaxf(m, mx);
+      if (m_new > m + 8.0f) {        // lazy rescale: only when the max grew by > 2^8
+        const float alpha = ex2(m - m_new);
+        l *= alpha;
+        lp *= alpha;
+#pragma unroll
+        for (int t = 0; t < NTO; ++t) {
+          o[t][0] *= alpha;
+          o[t][1] *= alpha;
+        }
+        m = m_new;
+      }
+      const float ref = (m == -INFINITY) ? 0.f : m;
+      float p[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) p[e] = ex2(sv[e] - ref);
+      l += (p[0] + p[1]) + (p[2] + p[3]);
+      uint32_t pa[4];
+      pa[0] = pack_bf16x2(p[0], p[1]);
+      pa[1] = 0u;
+      pa[2] = pack_bf16x2(p[2], p[3]);
+      pa[3] = 0u;
+      lp += (bf16lo(pa[0]) + bf16hi(pa[0])) + (bf16lo(pa[2]) + bf16hi(pa[2]));
+#pragma unroll
+      for (int n2 = 0; n2 < NTO / 2; ++n2) {
+        const int tok = cb + (mi & 1) * 8 + rr;
+        const int dim = (2 * n2 + (mi >> 1)) * 8;
+        uint32_t v0, v1, v2, v3;
+        ldsm_x4_trans(vbase + (dim >> 6) * C::TILE * 128 + swz(tok, (dim & 63) >> 3), v0, v1, v2,
+                      v3);
+        mma_bf16_16816(o[2 * n2], pa, v0, v1);
+        mma_bf16_16816(o[2 * n2 + 1], pa, v2, v3);
+      }
+    }
+    fence_proxy_async_smem();   // any zeroed rows before the producer's next TMA into the stage
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_u32(&empty_bar[s]));
+  }
+  // a head row's sums are spread over the four lanes of its quad
+  l += __shfl_xor_sync(0xffffffffu, l, 1);
+  l += __shfl_xor_sync(0xffffffffu, l, 2);
+  lp += __shfl_xor_sync(0xffffffffu, lp, 1);
+  lp += __shfl_xor_sync(0xffffffffu, lp, 2);
+  const bool aborted = named_bar_or(1, C::NCW * 32, *abort_flag != 0);
+  if (!aborted && r < GROUP) {
+#pragma unroll
+    for (int t = 0; t < NTO; ++t) {
+      red_o[(warp * GROUP + r) * HEAD_DIM + t * 8 + k0] = o[t][0];
+      red_o[(warp * GROUP + r) * HEAD_DIM + t * 8 + k0 + 1] = o[t][1];
+    }
+    if ((lane & 3) == 0) {
+      red_m[warp * GROUP + r] = m;
+      red_l[warp * GROUP + r] = l;
+      red_lp[warp * GROUP + r] = lp;
+    }
+  }
+  return aborted;
 }
 
 template <int HEAD_DIM, int GROUP>
@@ -149,6 +302,13 @@ decode_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant__
     }
   } else {
     // ------------------------------------------------------------ consumers
+    // per-warp states for the cross-warp merge (the ring is idle by then)
+    float* red_o = reinterpret_cast<float*>(smem_gen);               // [NCW][GROUP][D]
+    float* red_m = red_o + C::NCW * GROUP * HEAD_DIM;                // [NCW][GROUP]
+    float* red_l = red_m + C::NCW * GROUP;                           // exact weight sums
+    float* red_lp = red_l + C::NCW * GROUP;                          // weights applied to O
+    bool aborted = false;
+    if constexpr (!C::MMA) {
     const int ch = lane % C::LPT;            // 16-byte chunk of the row this lane owns
     const int ts = lane / C::LPT;            // token slot within a pass
     const int blk = ch >> 3, c8 = ch & 7;
@@ -258,26 +418,29 @@ decode_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant__
       }
     }
 
-    // merge the consumer warps through shared memory (the ring is idle now)
     // every consumer thread takes the same decision (abort_flag may still
     // change while warps arrive, so it is voted on at the barrier)
-    const bool aborted = named_bar_or(1, C::NCW * 32, abort_flag != 0);
-    if (!aborted) {
-      float* red_o = reinterpret_cast<float*>(smem_gen);               // [NCW][GROUP][D]
-      float* red_m = red_o + C::NCW * GROUP * HEAD_DIM;                // [NCW][GROUP]
-      float* red_l = red_m + C::NCW * GROUP;
-      if (lane < C::LPT) {
+    aborted = named_bar_or(1, C::NCW * 32, abort_flag != 0);
+    if (!aborted && lane < C::LPT) {
 #pragma unroll
-        for (int h = 0; h < GROUP; ++h) {
-          float4* dst = reinterpret_cast<float4*>(red_o + (warp * GROUP + h) * HEAD_DIM + ch * 8);
-          dst[0] = make_float4(acc[h][0], acc[h][1], acc[h][2], acc[h][3]);
-          dst[1] = make_float4(acc[h][4], acc[h][5], acc[h][6], acc[h][7]);
-          if (lane == 0) {
-            red_m[warp * GROUP + h] = m[h];
-            red_l[warp * GROUP + h] = l[h];
-          }
+      for (int h = 0; h < GROUP; ++h) {
+        float4* dst = reinterpret_cast<float4*>(red_o + (warp * GROUP + h) * HEAD_DIM + ch * 8);
+        dst[0] = make_float4(acc[h][0], acc[h][1], acc[h][2], acc[h][3]);
+        dst[1] = make_float4(acc[h][4], acc[h][5], acc[h][6], acc[h][7]);
+        if (lane == 0) {
+          red_m[warp * GROUP + h] = m[h];
+          red_l[warp * GROUP + h] = l[h];
+          red_lp[warp * GROUP + h] = l[h];
         }
       }
+    }
+    } else {
+      aborted = mma_consumer<HEAD_DIM, GROUP>(prm, item, n_tok, n_tiles, smem_base, full_bar,
+                                              empty_bar, &abort_flag, red_o, red_m, red_l, red_lp);
+    }
+
+    // merge the consumer warps' states
+    if (!aborted) {
       named_bar_sync(1, C::NCW * 32);
       const int tid = threadIdx.x;
       for (int idx = tid; idx < GROUP * HEAD_DIM; idx += C::NCW * 32) {
@@ -286,14 +449,15 @@ decode_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant__
 #pragma unroll
         for (int w = 0; w < C::NCW; ++w) M = fmaxf(M, red_m[w * GROUP + h]);
         const float rf = (M == -INFINITY) ? 0.f : M;
-        float L = 0.f, O = 0.f;
+        float L = 0.f, LP = 0.f, O = 0.f;
 #pragma unroll
         for (int w = 0; w < C::NCW; ++w) {
           const float sc = ex2(red_m[w * GROUP + h] - rf);
           L = fmaf(red_l[w * GROUP + h], sc, L);
+          LP = fmaf(red_lp[w * GROUP + h], sc, LP);
           O = fmaf(red_o[(w * GROUP + h) * HEAD_DIM + dd], sc, O);
         }
-        const float o = (L > 0.f) ? O / L : 0.f;
+        const float o = (LP > 0.f) ? O / LP : 0.f;
         const float lse = (L > 0.f) ? (rf + lg2(L)) * kLn2 : -INFINITY;
         const int hq = item.head * GROUP + h;
         if (item.slot < 0) {
