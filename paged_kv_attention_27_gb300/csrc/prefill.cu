@@ -161,18 +161,24 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
     const uint32_t box = uint32_t(P) * 128u;
     int issued_k = 0, issued_v = 0;
     bool ok = true;
+    // page ids of tile j+1 are loaded while tile j's copies are issued, so
+    // the dependent global load is off the producer's critical path
+    auto pages_in = [&](int j) { return (min(C::N, item.tok_end - j * C::N) + P - 1) / P; };
+    int next_page = -1;
+    if (n_tiles > 0 && lane < pages_in(0)) next_page = prm.page_indices[item.page_begin + lane];
     for (int j = 0; j < n_tiles; ++j) {
       const int st = j % C::NST;
       const uint32_t empty_par = ((j / C::NST) & 1) ^ 1;
-      const int ntok = min(C::N, item.tok_end - j * C::N);
-      const int np = (ntok + P - 1) / P;
+      const int np = pages_in(j);
       int page = -1;
       bool valid = false;
       if (lane < np) {
-        page = prm.page_indices[item.page_begin + j * ppt + lane];
+        page = next_page;
         valid = page >= 0 && page < prm.num_pages;
         if (!valid) atomicOr(prm.err, kErrBounds);
       }
+      if (j + 1 < n_tiles && lane < pages_in(j + 1))
+        next_page = prm.page_indices[item.page_begin + (j + 1) * ppt + lane];
       const uint32_t bytes =
           uint32_t(__popc(__ballot_sync(0xffffffffu, valid))) * C::DBLK * box;
       const int c1 = prm.layout == FI_LAYOUT_NHD ? kv_head : 0;
@@ -386,7 +392,9 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
       }
 #pragma unroll
       for (int k = 0; k < C::N; ++k) rs8[k & 7] += s[k];
-      l += ((rs8[0] + rs8[1]) + (rs8[2] + rs8[3])) + ((rs8[4] + rs8[5]) + (rs8[6] + rs8[7]));
+      const float rs_tile =
+          ((rs8[0] + rs8[1]) + (rs8[2] + rs8[3])) + ((rs8[4] + rs8[5]) + (rs8[6] + rs8[7]));
+      l += rs_tile;
 
       // P buffer and O are free once the previous PV has completed
       if (j >= 1) {
@@ -429,19 +437,23 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
       // P row t as packed bf16 pairs into TMEM (the A operand of the PV
       // MMA). lp adds the same rounded values the tensor core multiplies, so
       // that the final division normalises exactly the weights applied.
+      // In tiles on the causal diagonal a row may have only a few visible
+      // keys, so lp adds exactly the rounded values there; elsewhere the
+      // rounding errors of many weights average out and the exact sum is used.
       float rsp4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int kb = 0; kb < C::N / 64; ++kb) {
         uint32_t w[32];
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          w[e] = pack_bf16x2(s[kb * 64 + 2 * e], s[kb * 64 + 2 * e + 1]);
-          rsp4[e & 3] += bf16lo(w[e]) + bf16hi(w[e]);
+        for (int e = 0; e < 32; ++e) w[e] = pack_bf16x2(s[kb * 64 + 2 * e], s[kb * 64 + 2 * e + 1]);
+        if (need_mask) {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) rsp4[e & 3] += bf16lo(w[e]) + bf16hi(w[e]);
         }
         tmem_st32(tmem + lane_off + C::COL_P + kb * 32, w);
       }
       tmem_wait_st();
-      lp += (rsp4[0] + rsp4[1]) + (rsp4[2] + rsp4[3]);
+      lp += need_mask ? (rsp4[0] + rsp4[1]) + (rsp4[2] + rsp4[3]) : rs_tile;
       fence_proxy_async_smem();   // zeroed V rows (generic writes) before the MMA reads them
       tc_fence_before();
       __syncwarp();
