@@ -7,9 +7,10 @@
 // FlashAttention-3 page describes for Hopper (section 1: TMA producer warps,
 // consumer warps driving the tensor cores, hardware barriers between them,
 // ping-pong buffers), rebuilt for sm_103a:
-//   * warp 4 (producer): TMA loads of the Q tile (once) and, per KV tile of
-//     N tokens, one 128B-swizzled box per (page, 64-dim slice) of K and of V
-//     into K and V rings (three deep for head_dim <= 128);
+//   * warps 4 and 6 (producers): TMA loads of the Q tile (once) and, per KV
+//     tile of N tokens, one 128B-swizzled box per (page, 64-dim slice) of K
+//     (warp 4) and of V (warp 6) into K and V rings (three deep for
+//     head_dim <= 128);
 //   * warp 5 (MMA issuer; also owns the TMEM allocation): one thread issues
 //     S_j = Q K_j^T into a double-buffered S region of TMEM, then
 //     O += P_{j-1} V_{j-1} into an O region of TMEM, so that the tensor core
@@ -48,7 +49,7 @@ struct PrefillCfg {
   static constexpr int M = kPrefillTileM;                   // 128 query rows
   static constexpr int N = HEAD_DIM <= 128 ? 128 : 64;      // KV tokens per tile
   static constexpr int DBLK = HEAD_DIM / 64;                // 128-byte slices of a row
-  static constexpr int THREADS = 192;                       // 4 softmax + producer + MMA warps
+  static constexpr int THREADS = 224;     // 4 softmax warps, K producer, MMA issuer, V producer
   static constexpr bool Q_TMEM = HEAD_DIM <= 128;           // Q as a TMEM operand
   static constexpr int NST = HEAD_DIM <= 128 ? 3 : 2;       // K (and V) ring depth
   static constexpr int Q_BYTES = DBLK * M * 128;
@@ -144,22 +145,32 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
   tc_fence_after();
   const uint32_t tmem = tmem_base_sh;
 
-  if (warp == 4) {
-    // ------------------------------------------------------------ producer
-    if (lane == 0) {
+  if (warp == 4 || warp == 6) {
+    // ------------------------------------------------------------ producers
+    // Warp 4 loads Q and the K tiles, warp 6 the V tiles: each page needs one
+    // TMA instruction per 64-dim slice, and their issue, not the bytes,
+    // bounded a single producer warp.
+    const bool is_v = warp == 6;
+    if (lane == 0 && !is_v) {
       prefetch_tensormap(&q_map);
       prefetch_tensormap(&k_map);
-      prefetch_tensormap(&v_map);
       const uint32_t qb = smem_u32(&bars.q_full);
       mbar_arrive_expect_tx(qb, C::Q_BYTES);
 #pragma unroll
       for (int c = 0; c < C::DBLK; ++c)
         tma_load_3d(base + C::OFF_Q + c * C::M * 128, &q_map, qb, c * 64, head, item.q_row);
     }
+    if (lane == 0 && is_v) prefetch_tensormap(&v_map);
+    const CUtensorMap* map = is_v ? &v_map : &k_map;
+    uint64_t* full = is_v ? bars.v_full : bars.k_full;
+    uint64_t* empty = is_v ? bars.v_empty : bars.k_empty;
+    const uint32_t ring = base + (is_v ? C::OFF_V : C::OFF_K);
     const int P = prm.page_size;
     const int ppt = C::N / P;
     const uint32_t box = uint32_t(P) * 128u;
-    int issued_k = 0, issued_v = 0;
+    const int c1 = prm.layout == FI_LAYOUT_NHD ? kv_head : 0;
+    const int c2 = prm.layout == FI_LAYOUT_NHD ? 0 : kv_head;
+    int issued = 0;
     bool ok = true;
     // page ids of tile j+1 are loaded while tile j's copies are issued, so
     // the dependent global load is off the producer's critical path
@@ -168,61 +179,41 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
     if (n_tiles > 0 && lane < pages_in(0)) next_page = prm.page_indices[item.page_begin + lane];
     for (int j = 0; j < n_tiles; ++j) {
       const int st = j % C::NST;
-      const uint32_t empty_par = ((j / C::NST) & 1) ^ 1;
       const int np = pages_in(j);
       int page = -1;
       bool valid = false;
       if (lane < np) {
         page = next_page;
         valid = page >= 0 && page < prm.num_pages;
-        if (!valid) atomicOr(prm.err, kErrBounds);
+        if (!valid && !is_v) atomicOr(prm.err, kErrBounds);
       }
       if (j + 1 < n_tiles && lane < pages_in(j + 1))
         next_page = prm.page_indices[item.page_begin + (j + 1) * ppt + lane];
       const uint32_t bytes =
           uint32_t(__popc(__ballot_sync(0xffffffffu, valid))) * C::DBLK * box;
-      const int c1 = prm.layout == FI_LAYOUT_NHD ? kv_head : 0;
-      const int c2 = prm.layout == FI_LAYOUT_NHD ? 0 : kv_head;
-      if (j >= C::NST && !mbar_wait_warp(smem_u32(&bars.k_empty[st]), empty_par, limit,
+      if (j >= C::NST && !mbar_wait_warp(smem_u32(&empty[st]), ((j / C::NST) & 1) ^ 1, limit,
                                          &abort_flag)) {
         ok = false;
         break;
       }
-      const uint32_t kf = smem_u32(&bars.k_full[st]);
-      if (lane == 0) mbar_arrive_expect_tx(kf, bytes);
+      const uint32_t fb = smem_u32(&full[st]);
+      if (lane == 0) mbar_arrive_expect_tx(fb, bytes);
       __syncwarp();
       if (valid) {
-        const uint32_t dst = base + C::OFF_K + st * C::KV_BYTES + lane * box;
+        const uint32_t dst = ring + st * C::KV_BYTES + lane * box;
 #pragma unroll
         for (int c = 0; c < C::DBLK; ++c)
-          tma_load_4d(dst + c * C::N * 128, &k_map, kf, c * 64, c1, c2, page);
+          tma_load_4d(dst + c * C::N * 128, map, fb, c * 64, c1, c2, page);
       }
-      issued_k = j + 1;
-      if (j >= C::NST && !mbar_wait_warp(smem_u32(&bars.v_empty[st]), empty_par, limit,
-                                         &abort_flag)) {
-        ok = false;
-        break;
-      }
-      const uint32_t vf = smem_u32(&bars.v_full[st]);
-      if (lane == 0) mbar_arrive_expect_tx(vf, bytes);
-      __syncwarp();
-      if (valid) {
-        const uint32_t dst = base + C::OFF_V + st * C::KV_BYTES + lane * box;
-#pragma unroll
-        for (int c = 0; c < C::DBLK; ++c)
-          tma_load_4d(dst + c * C::N * 128, &v_map, vf, c * 64, c1, c2, page);
-      }
-      issued_v = j + 1;
+      issued = j + 1;
     }
     if (!ok) {
       if (lane == 0) { abort_flag = 1; atomicOr(prm.err, kErrTimeout); }
-      // let every copy this CTA issued land before the CTA exits
-      for (int j = max(0, issued_k - C::NST); j < issued_k; ++j)
-        mbar_wait_bounded(smem_u32(&bars.k_full[j % C::NST]), (j / C::NST) & 1, limit, nullptr);
-      for (int j = max(0, issued_v - C::NST); j < issued_v; ++j)
-        mbar_wait_bounded(smem_u32(&bars.v_full[j % C::NST]), (j / C::NST) & 1, limit, nullptr);
+      // let every copy this warp issued land before the CTA exits
+      for (int j = max(0, issued - C::NST); j < issued; ++j)
+        mbar_wait_bounded(smem_u32(&full[j % C::NST]), (j / C::NST) & 1, limit, nullptr);
     }
-    if (lane == 0) mbar_wait_bounded(smem_u32(&bars.q_full), 0, limit, nullptr);
+    if (lane == 0 && !is_v) mbar_wait_bounded(smem_u32(&bars.q_full), 0, limit, nullptr);
     __syncwarp();
   } else if (warp == 5) {
     // ------------------------------------------------------------ MMA issuer
