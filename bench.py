@@ -291,6 +291,24 @@ def run_reference(args, rank, world):
 # our arm
 # ----------------------------------------------------------------------------
 
+def reduce_max(x, dist, device="cpu"):
+    """Max of a per-rank scalar over all ranks (the step time the whole job
+    waits for); identity when running alone. Timing plumbing only: no data
+    of the attention path crosses ranks."""
+    if dist is None:
+        return float(x)
+    import torch
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(units_per_rank, world, ms_per_step_max):
+    """Units per second for the whole job: every rank processes its own batch
+    (weak scaling), and the job takes as long as its slowest rank."""
+    return units_per_rank * world / (ms_per_step_max / 1e3)
+
+
 def time_steps(db, K, W, dist=None, sampler=None):
     """W untimed steps, then K steps bracketed by a barrier and a device
     synchronisation on both sides, timed with CUDA events on the launching
@@ -330,10 +348,7 @@ def time_steps(db, K, W, dist=None, sampler=None):
     assert st == B.FI_OK, B.status_string(st)
     ms_total = t_start.elapsed_time(t_end)
     kern_ms = sum(a.elapsed_time(e) for a, e in zip(ks, ke)) / K
-    if dist:
-        t = torch.tensor([ms_total], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_total = float(t.item())
+    ms_total = reduce_max(ms_total, dist, "cuda")
     return ms_total, kern_ms
 
 
@@ -421,9 +436,9 @@ def run_ours(args, rank, world, local_rank):
     sampler.stop()
     ms_step = ms_total / K
     if info["num_decode_items"]:          # decode or mixed: HBM-bound, KV GB/s
-        value, unit = kvb * world / (ms_step / 1e3) / 1e9, "GB/s"
+        value, unit = whole_job_rate(kvb, world, ms_step) / 1e9, "GB/s"
     else:                                 # prefill: tensor-bound, TFLOP/s
-        value, unit = flops * world / (ms_step / 1e3) / 1e12, "TFLOP/s"
+        value, unit = whole_job_rate(flops, world, ms_step) / 1e12, "TFLOP/s"
 
     e2e = None
     if not args.no_e2e:
