@@ -222,6 +222,11 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
                     ? mbar_wait_bounded(smem_u32(&bars.q_tmem), 0, limit, &abort_flag)
                     : mbar_wait_bounded(smem_u32(&bars.q_full), 0, limit, &abort_flag);
       const uint32_t q_base = base + C::OFF_Q;
+      // descriptors are linear in the address field (bits 0-13 = addr >> 4),
+      // so each MMA's descriptor is a base plus a compile-time offset
+      const uint64_t qd0 = sdesc_sw128(q_base, 16, 1024);
+      const uint64_t kd0 = sdesc_sw128(base + C::OFF_K, 16, 1024);
+      const uint64_t vd0 = sdesc_sw128(base + C::OFF_V, C::N * 128, 1024);
       for (int j = 0; ok && j <= n_tiles; ++j) {
         if (j < n_tiles) {
           const int st = j % C::NST, sb = j & 1;
@@ -232,17 +237,15 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
                                    &abort_flag);
           if (!ok) break;
           tc_fence_after();
-          const uint32_t k_base = base + C::OFF_K + st * C::KV_BYTES;
+          const uint64_t kd = kd0 + uint64_t((st * C::KV_BYTES) >> 4);
           const uint32_t s_col = tmem + C::COL_S + sb * C::N;
 #pragma unroll
           for (int k = 0; k < HEAD_DIM / 16; ++k) {
-            const uint64_t bd =
-                sdesc_sw128(k_base + (k >> 2) * C::N * 128 + (k & 3) * 32, 16, 1024);
+            const uint64_t bd = kd + uint64_t(((k >> 2) * C::N * 128 + (k & 3) * 32) >> 4);
             if constexpr (C::Q_TMEM) {
               tc_mma_ts(s_col, tmem + C::COL_Q + k * 8, bd, C::IDESC_QK, k > 0 ? 1u : 0u);
             } else {
-              const uint64_t a =
-                  sdesc_sw128(q_base + (k >> 2) * C::M * 128 + (k & 3) * 32, 16, 1024);
+              const uint64_t a = qd0 + uint64_t(((k >> 2) * C::M * 128 + (k & 3) * 32) >> 4);
               tc_mma_ss(s_col, a, bd, C::IDESC_QK, k > 0 ? 1u : 0u);
             }
           }
@@ -257,11 +260,11 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
                                    &abort_flag);
           if (!ok) break;
           tc_fence_after();
-          const uint32_t v_base = base + C::OFF_V + st * C::KV_BYTES;
+          const uint64_t vd = vd0 + uint64_t((st * C::KV_BYTES) >> 4);
 #pragma unroll
           for (int k = 0; k < C::N / 16; ++k) {
             // MN-major V: 16 tokens per step; the next 64 dims one K-tile slice further
-            const uint64_t bd = sdesc_sw128(v_base + k * 16 * 128, C::N * 128, 1024);
+            const uint64_t bd = vd + uint64_t((k * 16 * 128) >> 4);
             tc_mma_ts(tmem + C::COL_O, tmem + C::COL_P + k * 8, bd, C::IDESC_PV,
                       (jj > 0 || k > 0) ? 1u : 0u);
           }
