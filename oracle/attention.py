@@ -77,13 +77,22 @@ def gather_kv(cache_bits: np.ndarray, layout: str, page_indptr, page_indices,
     return bf16_to_f64(rows)
 
 
-def visible_keys(qo_len: int, kv_len: int, causal: bool) -> np.ndarray:
-    """Boolean ``[qo_len, kv_len]``: may query row i see key t?"""
-    if not causal:
-        return np.ones((qo_len, kv_len), dtype=bool)
+def visible_keys(qo_len: int, kv_len: int, causal: bool, window_left: int = -1) -> np.ndarray:
+    """Boolean ``[qo_len, kv_len]``: may query row i see key t?
+
+    Row i stands at key position ``pos = kv_len - qo_len + i`` (bottom-right
+    alignment). Causal: ``t <= pos``. A left window (``window_left >= 0``,
+    the left half of the ``window_size`` pair of the FlashAttention-3 page's
+    varlen call, section 2; -1 = unbounded) also hides ``t < pos -
+    window_left``, so a causal row sees at most ``window_left + 1`` keys.
+    """
     i = np.arange(qo_len)[:, None]
     t = np.arange(kv_len)[None, :]
-    return t <= kv_len - qo_len + i
+    pos = kv_len - qo_len + i
+    vis = (t <= pos) if causal else np.ones((qo_len, kv_len), dtype=bool)
+    if window_left >= 0:
+        vis = vis & (t >= pos - window_left)
+    return vis
 
 
 # --------------------------------------------------------------------------
@@ -120,14 +129,15 @@ def softmax_attention(q: np.ndarray, k: np.ndarray, v: np.ndarray, sm_scale: flo
 def batch_attention(q_bits, qo_indptr, k_cache_bits, v_cache_bits, layout: str,
                     page_indptr, page_indices, last_page_len, num_qo_heads: int,
                     num_kv_heads: int, page_size: int, sm_scale: float, causal: bool,
-                    requests=None, rows=None):
+                    requests=None, rows=None, window_left: int = -1):
     """Paged attention for a packed batch.
 
     q_bits ``[sum qo_len, Hq, d]`` bf16 bits; caches as laid out by ``layout``.
     Returns ``out [sum qo_len, Hq, d]`` and ``lse [sum qo_len, Hq]`` in
     float64. ``requests`` limits the work to some requests (other rows stay
     NaN); ``rows`` maps a request to the list of its row indices to compute
-    (for sampled checks of large batches).
+    (for sampled checks of large batches); ``window_left`` as in
+    ``visible_keys``.
     """
     if num_qo_heads % num_kv_heads:
         raise ValueError("num_qo_heads must be a multiple of num_kv_heads")
@@ -144,7 +154,7 @@ def batch_attention(q_bits, qo_indptr, k_cache_bits, v_cache_bits, layout: str,
         if qo_len == 0:
             continue
         sel = np.arange(qo_len) if rows is None or b not in rows else np.asarray(rows[b])
-        vis = visible_keys(qo_len, int(kv_len[b]), causal)[sel]
+        vis = visible_keys(qo_len, int(kv_len[b]), causal, window_left)[sel]
         for kh in range(num_kv_heads):
             k = gather_kv(k_cache_bits, layout, page_indptr, page_indices, b, kh,
                           int(kv_len[b]), page_size)
@@ -160,13 +170,15 @@ def batch_attention(q_bits, qo_indptr, k_cache_bits, v_cache_bits, layout: str,
 
 def batch_decode(q_bits, k_cache_bits, v_cache_bits, layout: str, page_indptr,
                  page_indices, last_page_len, num_qo_heads: int, num_kv_heads: int,
-                 page_size: int, sm_scale: float, requests=None):
+                 page_size: int, sm_scale: float, requests=None, window_left: int = -1):
     """One query token per request: q_bits ``[B, Hq, d]``; out ``[B, Hq, d]``,
-    lse ``[B, Hq]``. Every key of the request is visible."""
+    lse ``[B, Hq]``. Every key of the request is visible, or with a left
+    window only the last ``window_left + 1``."""
     B = q_bits.shape[0]
     return batch_attention(q_bits, np.arange(B + 1), k_cache_bits, v_cache_bits, layout,
                            page_indptr, page_indices, last_page_len, num_qo_heads,
-                           num_kv_heads, page_size, sm_scale, False, requests=requests)
+                           num_kv_heads, page_size, sm_scale, False, requests=requests,
+                           window_left=window_left)
 
 
 # --------------------------------------------------------------------------

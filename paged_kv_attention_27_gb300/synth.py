@@ -104,6 +104,7 @@ class PagedBatch:
     v_cache: np.ndarray
     shared_prefix_pages: int = 0
     meta: dict = field(default_factory=dict)
+    window_left: int = -1        # left attention window (-1 = unbounded)
 
     @property
     def batch(self) -> int:
@@ -122,7 +123,7 @@ def make_batch(name: str, kv_lens, qo_lens, num_qo_heads: int, num_kv_heads: int
                head_dim: int, page_size: int, layout: str, sm_scale: float | None,
                causal: bool, seed: int, shared_prefix_requests: int = 0,
                shared_prefix_tokens: int = 0, tail_fill: str = "normal",
-               extra_pages: int = 0) -> PagedBatch:
+               extra_pages: int = 0, window_left: int = -1) -> PagedBatch:
     """Build a paged batch with seeded values and a shuffled page table.
 
     ``shared_prefix_requests`` requests (the first ones) map their first
@@ -188,7 +189,8 @@ def make_batch(name: str, kv_lens, qo_lens, num_qo_heads: int, num_kv_heads: int
                       page_indptr=page_indptr, page_indices=page_indices,
                       last_page_len=last.astype(np.int32), q=q, k_cache=k_cache, v_cache=v_cache,
                       shared_prefix_pages=int(prefix_pages),
-                      meta={"seed": seed, "shared_prefix_requests": shared_prefix_requests})
+                      meta={"seed": seed, "shared_prefix_requests": shared_prefix_requests},
+                      window_left=int(window_left))
 
 
 # ----------------------------------------------------------------------------
@@ -297,4 +299,4 @@ def sub_batch(src: PagedBatch, requests) -> PagedBatch:
                       qo_lens=qo_lens.copy(), qo_indptr=qo_indptr, page_indptr=page_indptr,
                       page_indices=page_indices, last_page_len=src.last_page_len[requests].copy(),
                       q=q, k_cache=src.k_cache[idx], v_cache=src.v_cache[idx],
-                      meta=dict(src.meta, sample=requests))
+                      meta=dict(src.meta, sample=requests), window_left=src.window_left)

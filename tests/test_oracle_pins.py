@@ -201,7 +201,8 @@ def test_one_dominant_score_is_overflow_safe():
 def _run(b, requests=None):
     return oracle.batch_attention(b.q, b.qo_indptr, b.k_cache, b.v_cache, b.layout, b.page_indptr,
                                   b.page_indices, b.last_page_len, b.num_qo_heads, b.num_kv_heads,
-                                  b.page_size, b.sm_scale, b.causal, requests=requests)
+                                  b.page_size, b.sm_scale, b.causal, requests=requests,
+                                  window_left=b.window_left)
 
 
 def test_permuting_physical_pages_changes_nothing():
@@ -303,6 +304,91 @@ def test_causal_matches_explicit_mask(qo, kv):
     # the last row always sees every key; the first sees kv-qo+1 of them
     assert oracle.visible_keys(qo, kv, True)[-1].all()
     assert oracle.visible_keys(qo, kv, True)[0].sum() == kv - qo + 1
+
+
+# --------------------------------------------------------------------------
+# the left attention window (window_size of the FlashAttention-3 page's
+# varlen call, section 2): closed forms and reductions
+# --------------------------------------------------------------------------
+
+@pytest.mark.parametrize("qo,kv", [(1, 1), (4, 9), (12, 12), (5, 40)])
+def test_window_zero_sees_only_its_own_position(qo, kv):
+    """Causal with window_left = 0: row i sees exactly key kv-qo+i, so its
+    output is that V row and its lse that one scaled score."""
+    rng = np.random.default_rng(qo * 7 + kv)
+    q, k, v = rng.normal(size=(qo, 8)), rng.normal(size=(kv, 8)), rng.normal(size=(kv, 8))
+    o, l = oracle.softmax_attention(q, k, v, 0.7, oracle.visible_keys(qo, kv, True, 0))
+    for i in range(qo):
+        t = kv - qo + i
+        np.testing.assert_allclose(o[i], v[t], rtol=0, atol=1e-14)
+        assert abs(l[i] - 0.7 * float(q[i] @ k[t])) < 1e-12
+
+
+@pytest.mark.parametrize("w", [0, 1, 15, 16, 17, 63, 99, 100, 5000])
+def test_windowed_decode_is_attention_over_the_last_keys(w):
+    """Decode with window_left = w equals plain (unwindowed) attention over
+    the last min(w+1, kv_len) keys, sliced out of a dense copy made by
+    walking the pages in order (no page arithmetic shared with the oracle)."""
+    b = synth.tiny_decode()
+    b.window_left = w
+    out, lse = _run(b)
+    g = b.num_qo_heads // b.num_kv_heads
+    for r in range(b.batch):
+        kv = int(b.kv_lens[r])
+        pages = b.page_indices[int(b.page_indptr[r]):int(b.page_indptr[r + 1])]
+        dk = np.concatenate([b.k_cache[p] for p in pages], axis=0)[:kv]   # NHD: [t, Hkv, d]
+        dv = np.concatenate([b.v_cache[p] for p in pages], axis=0)[:kv]
+        keep = min(w + 1, kv)
+        for h in range(b.num_qo_heads):
+            kh = h // g
+            k = oracle.bf16_to_f64(dk[kv - keep:, kh])
+            v = oracle.bf16_to_f64(dv[kv - keep:, kh])
+            q = oracle.bf16_to_f64(b.q[r, h])[None]
+            ro, rl = brute_force(q.tolist(), k.tolist(), v.tolist(), b.sm_scale,
+                                 [[True] * keep])
+            np.testing.assert_allclose(out[r, h], ro[0], rtol=0, atol=1e-12)
+            assert abs(lse[r, h] - rl[0]) < 1e-12
+
+
+def test_window_wider_than_the_context_changes_nothing():
+    b = synth.make_batch("w", [40, 130, 17], [40, 33, 1], 8, 2, 32, 16, synth.NHD, None, True, 31)
+    o0, l0 = _run(b)
+    b.window_left = 129
+    o1, l1 = _run(b)
+    np.testing.assert_array_equal(o0, o1)
+    np.testing.assert_array_equal(l0, l1)
+
+
+@pytest.mark.parametrize("causal", [True, False])
+@pytest.mark.parametrize("w", [0, 3, 31, 32])
+def test_window_matches_torch_band_mask(causal, w):
+    """torch SDPA in float64 with a band mask built by torch.tril/triu
+    diagonals (an independent construction of the same visibility)."""
+    torch = pytest.importorskip("torch")
+    b = synth.make_batch("band", [70, 45], [20, 45], 4, 2, 32, 16, synth.NHD, None, causal, 32,
+                         window_left=w)
+    out, lse = _run(b)
+    g = b.num_qo_heads // b.num_kv_heads
+    for r in range(b.batch):
+        kv, qo = int(b.kv_lens[r]), int(b.qo_lens[r])
+        pages = b.page_indices[int(b.page_indptr[r]):int(b.page_indptr[r + 1])]
+        to = lambda x: torch.from_numpy(np.ascontiguousarray(x).view(np.int16)).view(
+            torch.bfloat16).to(torch.float64)
+        dk = to(np.concatenate([b.k_cache[p] for p in pages], axis=0)[:kv]).transpose(0, 1)
+        dv = to(np.concatenate([b.v_cache[p] for p in pages], axis=0)[:kv]).transpose(0, 1)
+        qt = to(b.q[int(b.qo_indptr[r]):int(b.qo_indptr[r + 1])]).transpose(0, 1)
+        ones = torch.ones(qo, kv, dtype=torch.bool)
+        # diagonal kv-qo of an (qo x kv) matrix is the key aligned with each row
+        mask = ones.tril(kv - qo) if causal else ones.clone()
+        mask &= ones.triu(kv - qo - w)
+        kt, vt = dk.repeat_interleave(g, 0), dv.repeat_interleave(g, 0)
+        so = torch.nn.functional.scaled_dot_product_attention(qt, kt, vt, attn_mask=mask,
+                                                              scale=b.sm_scale)
+        sc = (qt @ kt.transpose(-1, -2)) * b.sm_scale
+        sl = torch.logsumexp(sc.masked_fill(~mask, -math.inf), dim=-1)
+        rows = slice(int(b.qo_indptr[r]), int(b.qo_indptr[r + 1]))
+        np.testing.assert_allclose(out[rows], so.transpose(0, 1).numpy(), rtol=0, atol=1e-12)
+        np.testing.assert_allclose(lse[rows], sl.transpose(0, 1).numpy(), rtol=0, atol=1e-12)
 
 
 # --------------------------------------------------------------------------
@@ -422,6 +508,17 @@ def test_planted_mistakes_are_caught(monkeypatch):
     with monkeypatch.context() as m:
         m.setattr(oracle, "merge_states", bad_merge)
         assert _raises(lambda: test_split_kv_merge_equals_unsplit(2))
+
+    # 7. window bound off by one (one key too many on the left)
+    real_vis = OA.visible_keys
+
+    def wide_window(qo_len, kv_len, causal, window_left=-1):
+        return real_vis(qo_len, kv_len, causal, window_left + 1 if window_left >= 0 else -1)
+    with monkeypatch.context() as m:
+        m.setattr(oracle, "visible_keys", wide_window)
+        m.setattr(OA, "visible_keys", wide_window)
+        assert _raises(lambda: test_window_zero_sees_only_its_own_position(4, 9))
+        assert _raises(lambda: test_windowed_decode_is_attention_over_the_last_keys(15))
 
     # 6. K and V swapped (transposed operand roles)
     def kv_swapped(q, k, v, sm_scale, visible):
