@@ -69,10 +69,12 @@ def peaks():
 WORKLOADS = {
     "llama7b_decode": ("llama7b_decode", {}),
     "llama70b_gqa_decode": ("llama70b_gqa_decode", {}),
+    "llama70b_gqa_decode_window4k": ("llama70b_gqa_decode", {"window_left": 4095}),
     "tiny_decode": ("tiny_decode", {}),
     "causal_prefill_1k": ("causal_prefill", {"seq_len": 1024}),
     "causal_prefill_4k": ("causal_prefill", {"seq_len": 4096}),
     "causal_prefill_16k": ("causal_prefill", {"seq_len": 16384}),
+    "causal_prefill_16k_window4k": ("causal_prefill", {"seq_len": 16384, "window_left": 4095}),
     "ragged_prefill": ("ragged_prefill", {}),
     "mixed_chunk_decode": ("mixed_chunk_decode", {}),
 }
@@ -88,17 +90,16 @@ def make_workload(name, batch=None):
 
 
 def visible_pairs(b):
-    """(query row, key) pairs the mask leaves visible, summed over requests."""
+    """(query row, key) pairs the mask leaves visible, summed over requests.
+    Row i stands at key position pos = kv - qo + i; causal rows see keys up
+    to pos, and a left window hides keys below pos - window_left."""
+    import numpy as np
     total = 0
     for qo, kv in zip(b.qo_lens.tolist(), b.kv_lens.tolist()):
-        if not b.causal:
-            total += qo * kv
-            continue
-        first = kv - qo + 1            # keys seen by row 0; row i sees first + i (<= kv)
-        if first >= 1:
-            total += qo * first + qo * (qo - 1) // 2
-        else:
-            total += sum(min(kv, max(0, first + i)) for i in range(qo))
+        pos = kv - qo + np.arange(qo, dtype=np.int64)
+        hi = np.minimum(pos, kv - 1) if (b.causal and qo > 1) else np.full(qo, kv - 1)
+        lo = np.maximum(0, pos - b.window_left) if b.window_left >= 0 else np.zeros(qo, np.int64)
+        total += int(np.maximum(0, hi - lo + 1).sum())
     return total
 
 
@@ -108,16 +109,17 @@ def attention_flops(b):
 
 
 def kv_bytes(b):
-    """K+V bytes a pass reads: every request's kv_len rows of K and V for
-    every kv head (bf16). Shared prefix pages are counted once."""
-    seen = {}
+    """K+V bytes a pass reads: the rows of K and V that some query row of a
+    request may see (all kv_len of them without a left window), for every
+    kv head (bf16). A page slot shared by several requests counts once."""
+    seen = set()
     for r in range(b.batch):
-        lo, hi = int(b.page_indptr[r]), int(b.page_indptr[r + 1])
-        for j in range(lo, hi):
-            used = b.page_size if j < hi - 1 else int(b.last_page_len[r])
-            p = int(b.page_indices[j])
-            seen[p] = max(seen.get(p, 0), used)
-    return sum(seen.values()) * 2 * b.num_kv_heads * b.head_dim * 2
+        kv, qo = int(b.kv_lens[r]), int(b.qo_lens[r])
+        first = max(0, kv - qo - b.window_left) if b.window_left >= 0 else 0
+        lo = int(b.page_indptr[r])
+        for t in range(first, kv):
+            seen.add((int(b.page_indices[lo + t // b.page_size]), t % b.page_size))
+    return len(seen) * 2 * b.num_kv_heads * b.head_dim * 2
 
 
 def io_bytes(b):
@@ -232,7 +234,8 @@ def oracle_sample(b, budget_s=12.0, threads=None):
     def one(r):
         oracle.batch_attention(b.q, b.qo_indptr, b.k_cache, b.v_cache, b.layout, b.page_indptr,
                                b.page_indices, b.last_page_len, b.num_qo_heads, b.num_kv_heads,
-                               b.page_size, b.sm_scale, b.causal, requests=[r])
+                               b.page_size, b.sm_scale, b.causal, requests=[r],
+                               window_left=b.window_left)
         return r
 
     done = []
@@ -250,7 +253,9 @@ def oracle_sample(b, budget_s=12.0, threads=None):
                 pending.add(ex.submit(one, nxt))
                 nxt += 1
     dt = time.perf_counter() - t0
-    kvb = sum(int(b.kv_lens[r]) for r in done) * 2 * b.num_kv_heads * b.head_dim * 2
+    w = b.window_left
+    keys = [int(b.kv_lens[r]) if w < 0 else min(int(b.kv_lens[r]), w + 1) for r in done]
+    kvb = sum(keys) * 2 * b.num_kv_heads * b.head_dim * 2
     return kvb / dt / 1e9, dt, threads, sorted(done)
 
 
@@ -516,10 +521,13 @@ def oracle_rows_sample(b, budget_s=12.0):
         r, i = task
         oracle.batch_attention(b.q, b.qo_indptr, b.k_cache, b.v_cache, b.layout, b.page_indptr,
                                b.page_indices, b.last_page_len, b.num_qo_heads, b.num_kv_heads,
-                               b.page_size, b.sm_scale, b.causal, requests=[r], rows={r: [i]})
+                               b.page_size, b.sm_scale, b.causal, requests=[r], rows={r: [i]},
+                               window_left=b.window_left)
         qo, kv = int(b.qo_lens[r]), int(b.kv_lens[r])
-        vis = min(kv, kv - qo + i + 1) if b.causal else kv
-        return 4 * b.head_dim * b.num_qo_heads * max(vis, 0)
+        pos = kv - qo + i
+        hi = min(kv - 1, pos) if b.causal else kv - 1
+        lo = max(0, pos - b.window_left) if b.window_left >= 0 else 0
+        return 4 * b.head_dim * b.num_qo_heads * max(hi - lo + 1, 0)
 
     done_flops, n = 0, 0
     t0 = time.perf_counter()
@@ -552,7 +560,7 @@ def run_e2e(b, db, K, local_rank, unit):
     import torch
 
     from paged_kv_attention_27_gb300 import binding as B
-    from paged_kv_attention_27_gb300.device import num_sms
+    from paged_kv_attention_27_gb300.device import num_sms, plan_options
 
     dev = f"cuda:{local_rank}"
     pin = lambda t: t.pin_memory()
@@ -573,7 +581,7 @@ def run_e2e(b, db, K, local_rank, unit):
     def step():
         plan = B.fi_plan(db.mode, b.batch, None if decode else qo_h.numpy(), indptr_h.numpy(),
                          last_h.numpy(), b.num_qo_heads, b.num_kv_heads, b.head_dim,
-                         b.page_size, b.causal, sms)
+                         b.page_size, b.causal, plan_options(b), sms)
         assert plan.workspace_bytes <= db.workspace.numel()
         db.q.copy_(q_h, non_blocking=True)
         db.page_indptr.copy_(indptr_h, non_blocking=True)

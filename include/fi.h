@@ -26,18 +26,21 @@
  *   (n_pages-1)*page_size + last_page_len[b], or 0 for a request with no
  *   pages (its last_page_len is then ignored). Key t of request b lives on
  *   page page_indices[page_indptr[b] + t/page_size], slot t%page_size.
- * KV layouts (bf16): FI_LAYOUT_NHD = [page][slot][kv_head][dim],
+ * KV layouts (the plan's fi_dtype, bf16 by default):
+ *   FI_LAYOUT_NHD = [page][slot][kv_head][dim],
  *   FI_LAYOUT_HND = [page][kv_head][slot][dim]. K and V are separate
  *   buffers of the same layout; page_stride_elems is the distance between
  *   consecutive pages in elements (0 = dense: page_size*num_kv_heads*head_dim),
  *   so K and V may also be two views into one [num_pages][2][...] buffer.
  * Heads: num_qo_heads = g * num_kv_heads; query head h reads kv head h/g.
- * Queries (bf16): decode q is [batch][num_qo_heads][head_dim]; prefill q is
- *   the ragged packing [sum qo_len][num_qo_heads][head_dim] with request b
- *   on rows qo_indptr[b] .. qo_indptr[b+1]-1. out has q's shape (bf16).
+ * Queries (same type as K/V): decode q is [batch][num_qo_heads][head_dim];
+ *   prefill q is the ragged packing [sum qo_len][num_qo_heads][head_dim]
+ *   with request b on rows qo_indptr[b] .. qo_indptr[b+1]-1. out has q's
+ *   shape and type.
  * Causal (prefill): row i of a request with qo_len rows sees keys
  *   t <= kv_len - qo_len + i (the chunk's queries are the last qo_len
- *   positions of its KV); qo_len > kv_len is rejected.
+ *   positions of its KV); qo_len > kv_len is rejected. A left window
+ *   (fi_plan_options) also hides t < kv_len - qo_len + i - window_left.
  * lse (fp32, optional, may be NULL): natural log of the sum over visible
  *   keys of exp(sm_scale * <q,k>). A row with no visible key gets out = 0
  *   and lse = -inf.
@@ -77,6 +80,28 @@ typedef enum {
 typedef enum { FI_LAYOUT_NHD = 0, FI_LAYOUT_HND = 1 } fi_kv_layout;
 typedef enum { FI_MODE_DECODE = 0, FI_MODE_PREFILL = 1 } fi_mode;
 
+/* Element type of q, K, V and out (lse and partial states are fp32). */
+typedef enum { FI_DTYPE_BF16 = 0, FI_DTYPE_FP16 = 1 } fi_dtype;
+
+/*
+ * Options of a plan. Start from FI_PLAN_OPTIONS_DEFAULT (a zero-filled
+ * struct means a window of 0, not "no window").
+ *   window_left  -1: no window. >= 0: the left half of the window_size pair
+ *                of the varlen call on the "FlashAttention-3 kernel
+ *                integration in inference engines" page, section 2: the row
+ *                standing at key position pos = kv_len - qo_len + i also
+ *                loses every key t < pos - window_left, so a causal row sees
+ *                at most window_left + 1 keys (a decode row: the last
+ *                window_left + 1). The right side is set by `causal`.
+ *   dtype        fi_dtype of q, K, V and out.
+ */
+typedef struct {
+  int32_t window_left;
+  int32_t dtype;
+} fi_plan_options;
+
+#define FI_PLAN_OPTIONS_DEFAULT {-1, FI_DTYPE_BF16}
+
 typedef struct fi_plan_s* fi_plan_t;
 
 /* Summary of a plan, for logging and tests. */
@@ -110,6 +135,8 @@ typedef struct {
  *   page_indptr_h    host int32 [B+1], non-decreasing, page_indptr_h[0] >= 0.
  *   last_page_len_h  host int32 [B].
  *   causal           prefill only; ignored for decode.
+ *   options          window and element type (see fi_plan_options); NULL
+ *                    gives FI_PLAN_OPTIONS_DEFAULT. Copied into the plan.
  *   num_sms          SMs of the device the plan will run on (>0).
  *   out_plan         receives the plan; free it with fi_plan_destroy.
  *   workspace_bytes  receives the device workspace size the runs need.
@@ -119,13 +146,14 @@ typedef struct {
  * Errors: FI_ERR_INVALID_ARG (NULL pointers, negative sizes, decreasing
  * indptr, last_page_len outside [1,page_size] for a request with pages,
  * causal with qo_len > kv_len, num_qo_heads not a multiple of
- * num_kv_heads), FI_ERR_UNSUPPORTED (head_dim, page_size or g not built).
+ * num_kv_heads, window_left < -1, dtype not an fi_dtype),
+ * FI_ERR_UNSUPPORTED (head_dim, page_size or g not built).
  */
 fi_status fi_plan(int32_t mode, int32_t batch_size, const int32_t* qo_indptr_h,
                   const int32_t* page_indptr_h, const int32_t* last_page_len_h,
                   int32_t num_qo_heads, int32_t num_kv_heads, int32_t head_dim,
-                  int32_t page_size, int32_t causal, int32_t num_sms,
-                  fi_plan_t* out_plan, size_t* workspace_bytes);
+                  int32_t page_size, int32_t causal, const fi_plan_options* options,
+                  int32_t num_sms, fi_plan_t* out_plan, size_t* workspace_bytes);
 
 /* Frees a plan (NULL is accepted). */
 fi_status fi_plan_destroy(fi_plan_t plan);
@@ -136,8 +164,10 @@ fi_status fi_plan_get_info(fi_plan_t plan, fi_plan_info* info);
 /*
  * Copies the plan's work list to host memory: 8 int32 per item, in launch
  * order: {request, kv_head (decode) or qo_head (prefill), first page index
- * (into page_indices), number of pages, first token, end token, partial
- * slot or -1, first query row within the request (prefill) or 0}.
+ * (into page_indices), number of pages, first key, end key, partial slot or
+ * -1, first row of q}. Keys are token positions within the request; the
+ * first page holds the first key at slot (first key % page_size), earlier
+ * slots of that page lie outside the item's window.
  * `capacity` is in items; *num_items receives the plan's item count.
  */
 fi_status fi_plan_get_work(fi_plan_t plan, int32_t* items_h, int32_t capacity,
@@ -262,9 +292,10 @@ const char* fi_status_string(fi_status status);
 const char* fi_last_error_string(void);
 
 /*
- * Test hook for the failure path. kind 0 = normal operation; kind 1 = the
- * next decode launch's producer skips its first tile load, so that the
- * consumers' bounded wait runs out after about `wait_limit` polls and the
+ * Test hook for the failure path. kind 0 = normal operation; kind 1 = in the
+ * next paged run call, the first CTA of each attention kernel (decode, and
+ * prefill: its K producer) skips its first tile load, so that the waiting
+ * warps' bounded waits run out after about `wait_limit` nanoseconds and the
  * kernel reports FI_ERR_DEVICE_TIMEOUT instead of hanging. wait_limit <= 0
  * restores the default bound. Not thread-safe; meant for tests only.
  */

@@ -25,6 +25,9 @@ FI_ERR_DEVICE_TIMEOUT = 5
 FI_ERR_DEVICE_BOUNDS = 6
 FI_ERR_NO_DEVICE = 7
 
+FI_DTYPE_BF16 = 0
+FI_DTYPE_FP16 = 1
+
 FI_LAYOUT_NHD = 0
 FI_LAYOUT_HND = 1
 FI_MODE_DECODE = 0
@@ -46,6 +49,11 @@ class FiError(RuntimeError):
         if detail:
             msg += f": {detail}"
         super().__init__(msg)
+
+
+class PlanOptions(ctypes.Structure):
+    """fi_plan_options: window_left (-1 = none) and dtype (FI_DTYPE_*)."""
+    _fields_ = [("window_left", ctypes.c_int32), ("dtype", ctypes.c_int32)]
 
 
 class PlanInfo(ctypes.Structure):
@@ -71,8 +79,9 @@ def lib():
         raise RuntimeError(f"{LIB_PATH} is missing: build it with "
                            "paged_kv_attention_27_gb300.build.build() first")
     L = ctypes.CDLL(LIB_PATH)
-    L.fi_plan.argtypes = [_I32, _I32, _P, _P, _P, _I32, _I32, _I32, _I32, _I32, _I32,
-                          ctypes.POINTER(_P), ctypes.POINTER(ctypes.c_size_t)]
+    L.fi_plan.argtypes = [_I32, _I32, _P, _P, _P, _I32, _I32, _I32, _I32, _I32,
+                          ctypes.POINTER(PlanOptions), _I32, ctypes.POINTER(_P),
+                          ctypes.POINTER(ctypes.c_size_t)]
     L.fi_plan_destroy.argtypes = [_P]
     L.fi_plan_get_info.argtypes = [_P, ctypes.POINTER(PlanInfo)]
     L.fi_plan_get_work.argtypes = [_P, _P, _I32, ctypes.POINTER(_I32)]
@@ -150,13 +159,20 @@ class Plan:
 
 
 def fi_plan(mode, batch_size, qo_indptr_h, page_indptr_h, last_page_len_h, num_qo_heads,
-            num_kv_heads, head_dim, page_size, causal, num_sms) -> Plan:
+            num_kv_heads, head_dim, page_size, causal, options, num_sms) -> Plan:
+    """``options``: None (the defaults) or a dict with any of ``window_left``
+    and ``dtype``."""
     qo, pi, lp = _i32(qo_indptr_h), _i32(page_indptr_h), _i32(last_page_len_h)
+    opt = None
+    if options is not None:
+        opt = PlanOptions(int(options.get("window_left", -1)),
+                          int(options.get("dtype", FI_DTYPE_BF16)))
     h = _P()
     ws = ctypes.c_size_t()
     st = lib().fi_plan(int(mode), int(batch_size), _ptr(qo), _ptr(pi), _ptr(lp), int(num_qo_heads),
                        int(num_kv_heads), int(head_dim), int(page_size), int(bool(causal)),
-                       int(num_sms), ctypes.byref(h), ctypes.byref(ws))
+                       None if opt is None else ctypes.byref(opt), int(num_sms),
+                       ctypes.byref(h), ctypes.byref(ws))
     _check(st, "fi_plan")
     return Plan(h.value, ws.value)
 

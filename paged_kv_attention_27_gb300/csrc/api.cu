@@ -197,6 +197,8 @@ fi_status run_paged(fi_plan_t plan, bool prefill_call, const void* q, const int3
 
   cudaEvent_t prof_start = g_prof_start, prof_stop = g_prof_stop;
   g_prof_start = g_prof_stop = nullptr;
+  const int32_t fault_kind = g_fault_kind;
+  g_fault_kind = 0;  // one-shot
   if (prof_start) {
     e = cudaEventRecord(prof_start, stream);
     if (e != cudaSuccess) return cuda_fail(e, "profiling event");
@@ -231,11 +233,13 @@ fi_status run_paged(fi_plan_t plan, bool prefill_call, const void* q, const int3
     pp.group = P.num_qo_heads / P.num_kv_heads;
     pp.layout = kv_layout;
     pp.causal = P.causal;
+    pp.window_left = P.window_left;
     pp.sm_scale = sm_scale;
     pp.out = out;
     pp.lse = lse;
     pp.err = err;
     pp.wait_limit_ns = g_wait_limit_ns;
+    pp.fault_kind = fault_kind;
     e = fi::launch_prefill(P.head_dim, qmap, kmap, vmap, pp, int(P.prefill_items.size()), stream);
     if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
   }
@@ -255,8 +259,7 @@ fi_status run_paged(fi_plan_t plan, bool prefill_call, const void* q, const int3
     dp.partial_lse = partial_lse;
     dp.err = err;
     dp.wait_limit_ns = g_wait_limit_ns;
-    dp.fault_kind = g_fault_kind;
-    g_fault_kind = 0;  // one-shot
+    dp.fault_kind = fault_kind;
     e = fi::launch_decode(P.head_dim, P.num_qo_heads / P.num_kv_heads, kmap, vmap, dp,
                           int(P.decode_items.size()), dstream);
     if (e != cudaSuccess) return cuda_fail(e, "decode launch");
@@ -293,15 +296,15 @@ extern "C" {
 fi_status fi_plan(int32_t mode, int32_t batch_size, const int32_t* qo_indptr_h,
                   const int32_t* page_indptr_h, const int32_t* last_page_len_h,
                   int32_t num_qo_heads, int32_t num_kv_heads, int32_t head_dim,
-                  int32_t page_size, int32_t causal, int32_t num_sms, fi_plan_t* out_plan,
-                  size_t* workspace_bytes) {
+                  int32_t page_size, int32_t causal, const fi_plan_options* options,
+                  int32_t num_sms, fi_plan_t* out_plan, size_t* workspace_bytes) {
   if (!out_plan || !workspace_bytes) return FI_ERR_INVALID_ARG;
   *out_plan = nullptr;
   fi_plan_s* p = new (std::nothrow) fi_plan_s;
   if (!p) return FI_ERR_INVALID_ARG;
   fi_status st = fi::build_plan(mode, batch_size, qo_indptr_h, page_indptr_h, last_page_len_h,
-                                num_qo_heads, num_kv_heads, head_dim, page_size, causal, num_sms,
-                                &p->p);
+                                num_qo_heads, num_kv_heads, head_dim, page_size, causal, options,
+                                num_sms, &p->p);
   if (st != FI_OK) {
     delete p;
     return st;

@@ -77,7 +77,8 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 // and returns whether any consumer aborted (voted, so all agree).
 template <int HEAD_DIM, int GROUP>
 __device__ __forceinline__ bool mma_consumer(const DecodeParams& prm, const WorkItem& item,
-                                             int n_tok, int n_tiles, uint32_t smem_base,
+                                             int n_tok, int lead, int n_tiles,
+                                             uint32_t smem_base,
                                              uint64_t* full_bar, uint64_t* empty_bar,
                                              int* abort_flag, float* red_o, float* red_m,
                                              float* red_l, float* red_lp) {
@@ -117,6 +118,7 @@ __device__ __forceinline__ bool mma_consumer(const DecodeParams& prm, const Work
       break;
     }
     const int ntok = min(C::TILE, n_tok - i * C::TILE);
+    const int lo = i == 0 ? lead : 0;        // rows below lo are outside the window
     const uint32_t kbase = smem_base + s * C::STAGE_BYTES;
     const uint32_t vbase = kbase + C::KBYTES;
 #pragma unroll 1
@@ -148,7 +150,7 @@ __device__ __forceinline__ bool mma_consumer(const DecodeParams& prm, const Work
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const int tok = cb + (e >> 1) * 8 + k0 + (e & 1);
-        sv[e] = tok < ntok ? sacc[e >> 1][e & 1] * scale : -INFINITY;
+        sv[e] = (tok < ntok && tok >= lo) ? sacc[e >> 1][e & 1] * scale : -INFINITY;
       }
       float mx = fmaxf(fmaxf(sv[0], sv[1]), fmaxf(sv[2], sv[3]));
       mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
@@ -227,7 +229,10 @@ decode_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant__
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const WorkItem item = prm.items[blockIdx.x];
-  const int n_tok = item.tok_end - item.tok_begin;
+  // Tokens are counted from the start of the item's first page; the first
+  // `lead` slots of that page precede the first visible key (a left window).
+  const int lead = item.tok_begin % prm.page_size;
+  const int n_tok = item.tok_end - item.tok_begin + lead;
   const int n_tiles = (n_tok + C::TILE - 1) / C::TILE;
 
   if (threadIdx.x == 0) {
@@ -258,7 +263,7 @@ decode_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant__
           break;
         }
       }
-      const int tok0 = i * C::TILE;                         // relative to tok_begin
+      const int tok0 = i * C::TILE;                 // relative to the first page
       const int tok_in_tile = min(C::TILE, n_tok - tok0);
       const int np = (tok_in_tile + prm.page_size - 1) / prm.page_size;
       int page = -1;
@@ -291,8 +296,10 @@ decode_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant__
       }
       issued = i + 1;
     }
-    // Before leaving, make sure no copy this CTA issued is still in flight.
-    if (abort_flag) {
+    // Before leaving, make sure no copy this CTA issued is still in flight,
+    // whether or not a consumer gave up (in a normal run the consumers have
+    // already seen these phases complete, so the waits return at once).
+    if (lane == 0) {
       for (int i = max(0, issued - C::NSTAGE); i < issued; ++i) {
         const bool skipped = (prm.fault_kind == 1 && blockIdx.x == 0 && i == 0);
         if (skipped) continue;
@@ -343,6 +350,7 @@ decode_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant__
         break;
       }
       const int ntok = min(C::TILE, n_tok - i * C::TILE);
+      const int lo = i == 0 ? lead : 0;      // rows below lo are outside the window
       const uint32_t kbase = smem_base + s * C::STAGE_BYTES + blk * C::TILE * 128;
       const uint32_t vbase = kbase + C::KBYTES;
 #pragma unroll
@@ -361,7 +369,7 @@ decode_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant__
 #pragma unroll
             for (int off = C::LPT / 2; off >= 1; off >>= 1)
               d0 += __shfl_xor_sync(0xffffffffu, d0, off);
-            sc[p][h] = (r < ntok) ? d0 : -INFINITY;
+            sc[p][h] = (r < ntok && r >= lo) ? d0 : -INFINITY;
           }
         }
         float ref[GROUP];
@@ -435,8 +443,9 @@ decode_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant__
       }
     }
     } else {
-      aborted = mma_consumer<HEAD_DIM, GROUP>(prm, item, n_tok, n_tiles, smem_base, full_bar,
-                                              empty_bar, &abort_flag, red_o, red_m, red_l, red_lp);
+      aborted = mma_consumer<HEAD_DIM, GROUP>(prm, item, n_tok, lead, n_tiles, smem_base,
+                                              full_bar, empty_bar, &abort_flag, red_o, red_m,
+                                              red_l, red_lp);
     }
 
     // merge the consumer warps' states

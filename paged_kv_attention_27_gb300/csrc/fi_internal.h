@@ -59,6 +59,8 @@ struct WorkspaceLayout {
 struct Plan {
   int32_t mode = 0, batch = 0, num_qo_heads = 0, num_kv_heads = 0, head_dim = 0;
   int32_t page_size = 0, causal = 0, num_sms = 0;
+  int32_t window_left = -1;              // -1: no window
+  int32_t dtype = FI_DTYPE_BF16;
   std::vector<WorkItem> decode_items;    // launch order
   std::vector<WorkItem> prefill_items;   // launch order
   std::vector<MergeTask> merges;
@@ -74,7 +76,8 @@ struct Plan {
 fi_status build_plan(int32_t mode, int32_t batch, const int32_t* qo_indptr,
                      const int32_t* page_indptr, const int32_t* last_page_len,
                      int32_t num_qo_heads, int32_t num_kv_heads, int32_t head_dim,
-                     int32_t page_size, int32_t causal, int32_t num_sms, Plan* plan);
+                     int32_t page_size, int32_t causal, const fi_plan_options* options,
+                     int32_t num_sms, Plan* plan);
 
 }  // namespace fi
 

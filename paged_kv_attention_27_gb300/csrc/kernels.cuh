@@ -51,11 +51,13 @@ struct PrefillParams {
   int32_t group;
   int32_t layout;
   int32_t causal;
+  int32_t window_left;  // -1: none; else row at key position pos keeps t >= pos - window_left
   float sm_scale;
   void* out;
   float* lse;
   uint32_t* err;
   uint64_t wait_limit_ns;
+  int32_t fault_kind;   // test hook: 1 = CTA 0's K producer skips its first tile
 };
 
 cudaError_t launch_prefill(int head_dim, const CUtensorMap& qm, const CUtensorMap& km,

@@ -27,8 +27,12 @@ bool supported_group(int g) { return g == 1 || g == 2 || g == 4 || g == 8; }
 fi_status build_plan(int32_t mode, int32_t batch, const int32_t* qo_indptr,
                      const int32_t* page_indptr, const int32_t* last_page_len,
                      int32_t num_qo_heads, int32_t num_kv_heads, int32_t head_dim,
-                     int32_t page_size, int32_t causal, int32_t num_sms, Plan* out) {
+                     int32_t page_size, int32_t causal, const fi_plan_options* options,
+                     int32_t num_sms, Plan* out) {
   if (!out) return FI_ERR_INVALID_ARG;
+  const fi_plan_options opt = options ? *options : fi_plan_options FI_PLAN_OPTIONS_DEFAULT;
+  if (opt.window_left < -1) return FI_ERR_INVALID_ARG;
+  if (opt.dtype != FI_DTYPE_BF16 && opt.dtype != FI_DTYPE_FP16) return FI_ERR_INVALID_ARG;
   if (mode != FI_MODE_DECODE && mode != FI_MODE_PREFILL) return FI_ERR_INVALID_ARG;
   if (batch < 0 || num_sms <= 0) return FI_ERR_INVALID_ARG;
   if (num_qo_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 || page_size <= 0)
@@ -51,6 +55,8 @@ fi_status build_plan(int32_t mode, int32_t batch, const int32_t* qo_indptr,
   p.page_size = page_size;
   p.causal = (mode == FI_MODE_PREFILL) ? (causal ? 1 : 0) : 0;
   p.num_sms = num_sms;
+  p.window_left = opt.window_left;
+  p.dtype = opt.dtype;
 
   // ---- validate the page table and the query packing; kv_len per request
   std::vector<int64_t> kv_len(batch), qo_len(batch), qo_start(batch);
@@ -83,14 +89,23 @@ fi_status build_plan(int32_t mode, int32_t batch, const int32_t* qo_indptr,
   if (total_q > INT32_MAX) return FI_ERR_INVALID_ARG;
   p.total_q = total_q;
 
-  // ---- decode work: every request with exactly one query row
+  // ---- the keys a row may see: [first_key, ...). A left window moves the
+  //      start; the row at key position pos keeps keys t >= pos - window_left
+  auto first_key = [&](int b, int64_t row) -> int64_t {
+    if (p.window_left < 0) return 0;
+    return std::max<int64_t>(0, kv_len[b] - qo_len[b] + row - p.window_left);
+  };
+
+  // ---- decode work: every request with exactly one query row. Chunks start
+  //      on page boundaries from the page holding the first visible key.
   const int tile = decode_tile_tokens(head_dim);
   std::vector<int> dec;
   int64_t dec_tiles = 0;
   for (int b = 0; b < batch; ++b) {
     if (qo_len[b] == 1) {
       dec.push_back(b);
-      dec_tiles += std::max<int64_t>(1, ceil_div(kv_len[b], tile)) * num_kv_heads;
+      const int64_t s0 = first_key(b, 0) / page_size * page_size;
+      dec_tiles += std::max<int64_t>(1, ceil_div(kv_len[b] - s0, tile)) * num_kv_heads;
     }
   }
   if (!dec.empty()) {
@@ -103,7 +118,9 @@ fi_status build_plan(int32_t mode, int32_t batch, const int32_t* qo_indptr,
     const int64_t chunk = chunk_tiles * tile;  // a multiple of the page size
     p.chunk_tokens = int32_t(std::min<int64_t>(chunk, INT32_MAX));
     for (int b : dec) {
-      const int64_t n_chunks = std::max<int64_t>(1, ceil_div(kv_len[b], chunk));
+      const int64_t w0 = first_key(b, 0);
+      const int64_t s0 = w0 / page_size * page_size;
+      const int64_t n_chunks = std::max<int64_t>(1, ceil_div(kv_len[b] - s0, chunk));
       int32_t slot_base = -1;
       if (n_chunks > 1) {
         slot_base = p.num_slots;
@@ -113,14 +130,14 @@ fi_status build_plan(int32_t mode, int32_t batch, const int32_t* qo_indptr,
       }
       for (int kh = 0; kh < num_kv_heads; ++kh) {
         for (int64_t c = 0; c < n_chunks; ++c) {
-          const int64_t t0 = c * chunk;
+          const int64_t t0 = s0 + c * chunk;     // page-aligned start of the chunk
           const int64_t t1 = std::min<int64_t>(kv_len[b], t0 + chunk);
           WorkItem w;
           w.req = b;
           w.head = kh;
           w.page_begin = int32_t(page_indptr[b] + t0 / page_size);
           w.n_pages = int32_t(t1 > t0 ? ceil_div(t1 - t0, page_size) : 0);
-          w.tok_begin = int32_t(t0);
+          w.tok_begin = int32_t(c == 0 ? w0 : t0);   // first visible key
           w.tok_end = int32_t(std::max(t0, t1));
           w.slot = n_chunks > 1 ? int32_t(slot_base + c) : -1;
           w.q_row = int32_t(qo_start[b]);
@@ -144,13 +161,16 @@ fi_status build_plan(int32_t mode, int32_t batch, const int32_t* qo_indptr,
       const int64_t r_last = std::min<int64_t>(qo_len[b], r0 + kPrefillTileM) - 1;
       int64_t kv_end = kv_len[b];
       if (p.causal) kv_end = std::min<int64_t>(kv_len[b], kv_len[b] - qo_len[b] + r_last + 1);
+      // the tile's first row has the smallest window start; tiles of keys
+      // begin on the page that holds it
+      const int64_t kv_begin = std::min(kv_end, first_key(b, r0)) / page_size * page_size;
       for (int h = 0; h < num_qo_heads; ++h) {
         WorkItem w;
         w.req = b;
         w.head = h;
-        w.page_begin = page_indptr[b];
-        w.n_pages = int32_t(ceil_div(kv_end, page_size));
-        w.tok_begin = 0;
+        w.page_begin = int32_t(page_indptr[b] + kv_begin / page_size);
+        w.n_pages = int32_t(ceil_div(kv_end - kv_begin, page_size));
+        w.tok_begin = int32_t(kv_begin);
         w.tok_end = int32_t(kv_end);
         w.slot = -1;
         w.q_row = int32_t(qo_start[b] + r0);
@@ -159,7 +179,9 @@ fi_status build_plan(int32_t mode, int32_t batch, const int32_t* qo_indptr,
     }
   }
   std::stable_sort(p.prefill_items.begin(), p.prefill_items.end(),
-                   [](const WorkItem& a, const WorkItem& b) { return a.tok_end > b.tok_end; });
+                   [](const WorkItem& a, const WorkItem& b) {
+                     return (a.tok_end - a.tok_begin) > (b.tok_end - b.tok_begin);
+                   });
 
   // ---- workspace: header | decode items | prefill items | merges | partial o | partial lse
   size_t off = kHeaderBytes;

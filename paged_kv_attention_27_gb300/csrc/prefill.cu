@@ -28,6 +28,8 @@
 //     is exact because O and the row sums share the stale reference);
 //   * the same warps finish with O / l, write bf16 out and the fp32 lse.
 // Fully masked KV tiles are never visited: the planner clips tok_end.
+#include <climits>
+
 #include <cuda_bf16.h>
 
 #include "fi_internal.h"
@@ -113,7 +115,8 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
   const int lane = threadIdx.x & 31;
   const WorkItem item = prm.items[blockIdx.x];
   const int req = item.req, head = item.head, kv_head = head / prm.group;
-  const int n_tiles = (item.tok_end + C::N - 1) / C::N;
+  // key tiles start at the item's first key (page-aligned; 0 without a window)
+  const int n_tiles = (item.tok_end - item.tok_begin + C::N - 1) / C::N;
   const uint64_t limit = prm.wait_limit_ns;
 
   if (threadIdx.x == 0) {
@@ -144,6 +147,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_base_sh;
+  int issued = 0;   // producers: tiles whose copies this warp has issued
 
   if (warp == 4 || warp == 6) {
     // ------------------------------------------------------------ producers
@@ -170,11 +174,12 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
     const uint32_t box = uint32_t(P) * 128u;
     const int c1 = prm.layout == FI_LAYOUT_NHD ? kv_head : 0;
     const int c2 = prm.layout == FI_LAYOUT_NHD ? 0 : kv_head;
-    int issued = 0;
     bool ok = true;
     // page ids of tile j+1 are loaded while tile j's copies are issued, so
     // the dependent global load is off the producer's critical path
-    auto pages_in = [&](int j) { return (min(C::N, item.tok_end - j * C::N) + P - 1) / P; };
+    auto pages_in = [&](int j) {
+      return (min(C::N, item.tok_end - item.tok_begin - j * C::N) + P - 1) / P;
+    };
     int next_page = -1;
     if (n_tiles > 0 && lane < pages_in(0)) next_page = prm.page_indices[item.page_begin + lane];
     for (int j = 0; j < n_tiles; ++j) {
@@ -197,9 +202,10 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
         break;
       }
       const uint32_t fb = smem_u32(&full[st]);
-      if (lane == 0) mbar_arrive_expect_tx(fb, bytes);
+      const bool skip = !is_v && j == 0 && prm.fault_kind == 1 && blockIdx.x == 0;
+      if (lane == 0 && !skip) mbar_arrive_expect_tx(fb, bytes);
       __syncwarp();
-      if (valid) {
+      if (valid && !skip) {
         const uint32_t dst = ring + st * C::KV_BYTES + lane * box;
 #pragma unroll
         for (int c = 0; c < C::DBLK; ++c)
@@ -207,12 +213,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
       }
       issued = j + 1;
     }
-    if (!ok) {
-      if (lane == 0) { abort_flag = 1; atomicOr(prm.err, kErrTimeout); }
-      // let every copy this warp issued land before the CTA exits
-      for (int j = max(0, issued - C::NST); j < issued; ++j)
-        mbar_wait_bounded(smem_u32(&full[j % C::NST]), (j / C::NST) & 1, limit, nullptr);
-    }
+    if (!ok && lane == 0) { abort_flag = 1; atomicOr(prm.err, kErrTimeout); }
     if (lane == 0 && !is_v) mbar_wait_bounded(smem_u32(&bars.q_full), 0, limit, nullptr);
     __syncwarp();
   } else if (warp == 5) {
@@ -292,8 +293,11 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
     const int np_req = prm.page_indptr[req + 1] - prm.page_indptr[req];
     const int kv_len = np_req > 0 ? (np_req - 1) * prm.page_size + prm.last_page_len[req] : 0;
     const int i_req = item.q_row - q_start + t;      // row index within the request
-    int t_max = prm.causal ? (kv_len - qo_len + i_req) : (kv_len - 1);
+    const int pos = kv_len - qo_len + i_req;         // key position of this row
+    int t_max = prm.causal ? pos : (kv_len - 1);
     t_max = min(t_max, kv_len - 1);                  // last visible key of this row
+    // first visible key (left window); below 0 means no lower bound
+    const int t_min = prm.window_left >= 0 ? pos - prm.window_left : INT_MIN;
     const float scale = prm.sm_scale * kLog2e;
     // l: sum of the exact weights (gives lse); lp: sum of the bf16-rounded
     // weights the PV MMA multiplies (normalises O)
@@ -344,15 +348,16 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
       // Row max of the raw scores (sm_scale >= 0 commutes with max). Eight
       // independent accumulators keep the dependency chains short; the mask
       // is applied only in tiles that cross this warp's causal bound.
-      const int col0 = j * C::N;
-      const bool need_mask = __any_sync(0xffffffffu, col0 + C::N - 1 > t_max);
+      const int col0 = item.tok_begin + j * C::N;   // key position of column 0
+      const bool need_mask = __any_sync(0xffffffffu, col0 + C::N - 1 > t_max || col0 < t_min);
       float mx8[8];
 #pragma unroll
       for (int i = 0; i < 8; ++i) mx8[i] = -INFINITY;
       if (need_mask) {
 #pragma unroll
         for (int k = 0; k < C::N; ++k) {
-          const float v = (col0 + k <= t_max) ? __uint_as_float(sr[k >> 5][k & 31]) : -INFINITY;
+          const bool vis = col0 + k <= t_max && col0 + k >= t_min;
+          const float v = vis ? __uint_as_float(sr[k >> 5][k & 31]) : -INFINITY;
           mx8[k & 7] = fmaxf(mx8[k & 7], v);
         }
       } else {
@@ -382,7 +387,8 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
       for (int k = 0; k < C::N; ++k) s[k] = ex2(fmaf(__uint_as_float(sr[k >> 5][k & 31]), scale, -ref));
       if (need_mask) {
 #pragma unroll
-        for (int k = 0; k < C::N; ++k) s[k] = (col0 + k <= t_max) ? s[k] : 0.f;
+        for (int k = 0; k < C::N; ++k)
+          s[k] = (col0 + k <= t_max && col0 + k >= t_min) ? s[k] : 0.f;
       }
 #pragma unroll
       for (int k = 0; k < C::N; ++k) rs8[k & 7] += s[k];
@@ -500,6 +506,17 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
   if (warp == 5) {
     tc_fence_after();
     tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+  // Each producer lets every copy it issued land before the CTA exits, also
+  // after a timeout anywhere in the CTA (in a normal run the MMA issuer has
+  // already seen these phases complete, so the waits return at once).
+  if ((warp == 4 || warp == 6) && lane == 0) {
+    const bool is_v = warp == 6;
+    uint64_t* full = is_v ? bars.v_full : bars.k_full;
+    for (int j = max(0, issued - C::NST); j < issued; ++j) {
+      if (!is_v && j == 0 && prm.fault_kind == 1 && blockIdx.x == 0) continue;  // never issued
+      mbar_wait_bounded(smem_u32(&full[j % C::NST]), (j / C::NST) & 1, limit, nullptr);
+    }
   }
 }
 

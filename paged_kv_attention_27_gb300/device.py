@@ -23,6 +23,11 @@ def i32_tensor(a: np.ndarray, device="cuda") -> torch.Tensor:
     return torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).to(device)
 
 
+def plan_options(b: PagedBatch):
+    """fi_plan options of a batch (None = the defaults)."""
+    return {"window_left": int(b.window_left)} if b.window_left >= 0 else None
+
+
 def num_sms(device="cuda") -> int:
     return torch.cuda.get_device_properties(device).multi_processor_count
 
@@ -46,7 +51,8 @@ class DeviceBatch:
         self.mode = mode
         self.plan = B.fi_plan(mode, b.batch, b.qo_indptr if mode == B.FI_MODE_PREFILL else None,
                               b.page_indptr, b.last_page_len, b.num_qo_heads, b.num_kv_heads,
-                              b.head_dim, b.page_size, b.causal, sms or num_sms(device))
+                              b.head_dim, b.page_size, b.causal, plan_options(b),
+                              sms or num_sms(device))
         self.workspace = torch.empty(max(self.plan.workspace_bytes, 256), dtype=torch.uint8,
                                      device=device)
         rows = int(b.qo_lens.sum())

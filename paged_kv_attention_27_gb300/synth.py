@@ -217,24 +217,32 @@ def lognormal_lengths(gen, n, median=2048, sigma=1.0, lo=1, hi=32768):
     return np.clip(np.rint(x), lo, hi).astype(np.int64)
 
 
-def llama70b_gqa_decode(seed: int = 2, batch: int = 128, shared: int = 32) -> PagedBatch:
+def llama70b_gqa_decode(seed: int = 2, batch: int = 128, shared: int = 32,
+                        window_left: int = -1) -> PagedBatch:
     """Llama2-70B-shaped GQA decode: 64/8 heads, d=128, P=16, HND,
     KV ~ lognormal(median 2048, sigma 1) clipped to [1,32768]; the first 32
-    requests share the physical pages of one 1024-token prefix."""
+    requests share the physical pages of one 1024-token prefix. Optionally a
+    left window of ``window_left`` keys."""
     g = philox(seed + 1000)
     kv = lognormal_lengths(g, batch)
     kv[:shared] = np.maximum(kv[:shared], 1024)
+    wname = f" window {window_left + 1}" if window_left >= 0 else ""
     return make_batch(f"Llama2-70B-shaped GQA decode B{batch} Hq64 Hkv8 d128 P16 HND lognormal(2048) "
-                      f"{shared} share a 1024-token prefix",
+                      f"{shared} share a 1024-token prefix{wname}",
                       kv, np.ones(batch, np.int64), 64, 8, 128, 16, HND, None, False, seed,
-                      shared_prefix_requests=shared, shared_prefix_tokens=1024)
+                      shared_prefix_requests=shared, shared_prefix_tokens=1024,
+                      window_left=window_left)
 
 
-def causal_prefill(seq_len: int, batch: int = 8, seed: int = 3) -> PagedBatch:
-    """Causal prefill, 70B shape: 64/8 heads, d=128, P=16, qo_len = kv_len = seq_len."""
+def causal_prefill(seq_len: int, batch: int = 8, seed: int = 3,
+                   window_left: int = -1) -> PagedBatch:
+    """Causal prefill, 70B shape: 64/8 heads, d=128, P=16, qo_len = kv_len =
+    seq_len; optionally a left window of ``window_left`` keys."""
     L = np.full(batch, seq_len, np.int64)
-    return make_batch(f"causal prefill B{batch} L{seq_len} Hq64 Hkv8 d128 P16 NHD",
-                      L, L, 64, 8, 128, 16, NHD, None, True, seed + seq_len)
+    wname = f" window {window_left + 1}" if window_left >= 0 else ""
+    return make_batch(f"causal prefill B{batch} L{seq_len} Hq64 Hkv8 d128 P16 NHD{wname}",
+                      L, L, 64, 8, 128, 16, NHD, None, True, seed + seq_len,
+                      window_left=window_left)
 
 
 def ragged_prefill(seed: int = 4, batch: int = 16) -> PagedBatch:

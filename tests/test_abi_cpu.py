@@ -10,6 +10,7 @@ import pytest
 
 from paged_kv_attention_27_gb300 import binding as B
 from paged_kv_attention_27_gb300 import synth
+from paged_kv_attention_27_gb300.device import plan_options
 
 from ._gpu import ensure_built
 
@@ -43,26 +44,30 @@ def _plan(b, mode=None, sms=152):
         mode = B.FI_MODE_DECODE if (b.is_decode and not b.causal) else B.FI_MODE_PREFILL
     return B.fi_plan(mode, b.batch, b.qo_indptr if mode == B.FI_MODE_PREFILL else None,
                      b.page_indptr, b.last_page_len, b.num_qo_heads, b.num_kv_heads, b.head_dim,
-                     b.page_size, b.causal, sms)
+                     b.page_size, b.causal, plan_options(b), sms)
 
 
 def _check_decode_cover(b, plan):
-    """Each (request, kv head, token) exactly once; chunks start on page and
-    tile boundaries; pages named are the request's own."""
+    """Each visible (request, kv head, key) exactly once; chunks start on
+    page boundaries (the first one of a windowed request inside its first
+    page); pages named are the request's own."""
     info = B.fi_plan_get_info(plan)
     work = B.fi_plan_get_work(plan)
     dec = work[:info["num_decode_items"]]
     seen = {}
     for req, kh, pb, npg, t0, t1, slot, qrow in dec.tolist():
-        assert t0 % b.page_size == 0
-        assert pb == b.page_indptr[req] + t0 // b.page_size
-        assert npg == -(-(t1 - t0) // b.page_size)
+        a = t0 - t0 % b.page_size                   # start of the page holding t0
+        assert pb == b.page_indptr[req] + a // b.page_size
+        assert npg == -(-(t1 - a) // b.page_size)
         assert pb + npg <= b.page_indptr[req + 1]
         assert qrow == b.qo_indptr[req]
         for t in range(t0, t1):
             seen[(req, kh, t)] = seen.get((req, kh, t), 0) + 1
+
+    def first(r):      # first visible key of a decode row
+        return 0 if b.window_left < 0 else max(0, int(b.kv_lens[r]) - 1 - b.window_left)
     want = {(r, h, t) for r in range(b.batch) if b.qo_lens[r] == 1
-            for h in range(b.num_kv_heads) for t in range(int(b.kv_lens[r]))}
+            for h in range(b.num_kv_heads) for t in range(first(r), int(b.kv_lens[r]))}
     assert set(seen) == want
     assert all(c == 1 for c in seen.values())
     # every decode request appears for every kv head (also empty ones)
@@ -150,6 +155,44 @@ def test_prefill_plan_tiles_and_causal_bounds():
     assert np.all(np.diff(pre[:, 5]) <= 0)
 
 
+@pytest.mark.parametrize("w", [0, 1, 15, 16, 17, 600, 5000])
+def test_windowed_decode_plans_cover_the_window_once(w):
+    b = _table_only([1, 0, 33, 4096, 32768, 700, 17], 32, 8, 128, 16)
+    b.window_left = w
+    for sms in (1, 152):
+        _check_decode_cover(b, _plan(b, sms=sms))
+
+
+@pytest.mark.parametrize("causal", [True, False])
+@pytest.mark.parametrize("w", [0, 100, 127, 128, 1000])
+def test_windowed_prefill_items_start_on_the_page_of_the_first_row_window(causal, w):
+    kv = [300, 129, 77, 5000, 2000]
+    qo = [300, 100, 77, 4, 700]
+    b = _table_only(kv, 8, 2, 128, 16, qo)
+    b.causal = causal
+    b.window_left = w
+    plan = _plan(b, B.FI_MODE_PREFILL)
+    info = B.fi_plan_get_info(plan)
+    pre = B.fi_plan_get_work(plan)[info["num_decode_items"]:]
+    rows = {}
+    for req, h, pb, npg, t0, t1, slot, qrow in pre.tolist():
+        qo_len, kv_len = qo[req], kv[req]
+        r0 = qrow - b.qo_indptr[req]
+        r_last = min(qo_len, r0 + 128) - 1
+        first = max(0, kv_len - qo_len + r0 - w)          # first key of the tile's first row
+        assert t0 % 16 == 0 and t0 <= first < t0 + 16 or (t0 == t1 == 0)
+        assert t1 == (min(kv_len, kv_len - qo_len + r_last + 1) if causal else kv_len)
+        assert pb == b.page_indptr[req] + t0 // 16
+        assert npg == -(-(t1 - t0) // 16)
+        for r in range(r0, r_last + 1):
+            rows[(req, h, r)] = rows.get((req, h, r), 0) + 1
+    want = {(r, h, i) for r in range(len(kv)) if qo[r] >= 2 for h in range(8)
+            for i in range(qo[r])}
+    assert set(rows) == want and all(c == 1 for c in rows.values())
+    lens = pre[:, 5] - pre[:, 4]
+    assert np.all(np.diff(lens) <= 0)
+
+
 @pytest.mark.parametrize("case,status", [
     ("last_page_len_zero", B.FI_ERR_INVALID_ARG),
     ("last_page_len_big", B.FI_ERR_INVALID_ARG),
@@ -163,11 +206,14 @@ def test_prefill_plan_tiles_and_causal_bounds():
     ("prefill_without_qo_indptr", B.FI_ERR_INVALID_ARG),
     ("qo_indptr_not_zero_based", B.FI_ERR_INVALID_ARG),
     ("no_sms", B.FI_ERR_INVALID_ARG),
+    ("window_below_minus_one", B.FI_ERR_INVALID_ARG),
+    ("dtype_unknown", B.FI_ERR_INVALID_ARG),
 ])
 def test_plan_validation(case, status):
     args = dict(mode=B.FI_MODE_DECODE, batch_size=2, qo_indptr_h=None,
                 page_indptr_h=[0, 2, 3], last_page_len_h=[5, 16], num_qo_heads=8,
-                num_kv_heads=2, head_dim=128, page_size=16, causal=0, num_sms=152)
+                num_kv_heads=2, head_dim=128, page_size=16, causal=0, options=None,
+                num_sms=152)
     if case == "last_page_len_zero":
         args["last_page_len_h"] = [0, 16]
     elif case == "last_page_len_big":
@@ -192,6 +238,10 @@ def test_plan_validation(case, status):
         args.update(mode=B.FI_MODE_PREFILL, qo_indptr_h=[1, 2, 3])
     elif case == "no_sms":
         args["num_sms"] = 0
+    elif case == "window_below_minus_one":
+        args["options"] = {"window_left": -2}
+    elif case == "dtype_unknown":
+        args["options"] = {"dtype": 7}
     with pytest.raises(B.FiError) as e:
         B.fi_plan(**args)
     assert e.value.status == status
@@ -199,9 +249,9 @@ def test_plan_validation(case, status):
 
 def test_valid_edge_plans():
     # empty batch; a request without pages (last_page_len ignored in [0, P])
-    p = B.fi_plan(B.FI_MODE_DECODE, 0, None, [0], [], 8, 2, 64, 16, 0, 4)
+    p = B.fi_plan(B.FI_MODE_DECODE, 0, None, [0], [], 8, 2, 64, 16, 0, None, 4)
     assert B.fi_plan_get_info(p)["num_items"] == 0
-    p = B.fi_plan(B.FI_MODE_DECODE, 2, None, [0, 0, 1], [0, 3], 8, 2, 64, 16, 0, 4)
+    p = B.fi_plan(B.FI_MODE_DECODE, 2, None, [0, 0, 1], [0, 3], 8, 2, 64, 16, 0, None, 4)
     info = B.fi_plan_get_info(p)
     assert info["total_kv_tokens"] == 3 and info["num_decode_items"] == 4
 
@@ -212,7 +262,7 @@ def test_workspace_too_small_and_bad_args_return_before_any_launch():
     torch = pytest.importorskip("torch")
     if torch.cuda.is_available():
         pytest.skip("uses fake device addresses; only meaningful without a GPU")
-    p = B.fi_plan(B.FI_MODE_DECODE, 2, None, [0, 2, 3], [5, 16], 8, 2, 128, 16, 0, 4)
+    p = B.fi_plan(B.FI_MODE_DECODE, 2, None, [0, 2, 3], [5, 16], 8, 2, 128, 16, 0, None, 4)
     fake = 1 << 20   # aligned, never dereferenced: every call below returns first
     args = [p, fake, fake, fake, B.FI_LAYOUT_NHD, 0, 4, fake, fake, fake, 0.1, fake, fake, fake]
     with pytest.raises(B.FiError) as e:

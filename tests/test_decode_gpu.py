@@ -10,7 +10,7 @@ import oracle  # noqa: E402
 from paged_kv_attention_27_gb300 import binding as B  # noqa: E402
 from paged_kv_attention_27_gb300 import synth  # noqa: E402
 
-from ._gpu import compare, ensure_built  # noqa: E402
+from ._gpu import compare, ensure_built, scale_v  # noqa: E402
 
 pytestmark = pytest.mark.gpu
 
@@ -31,7 +31,8 @@ def _dev(b, **kw):
 def _oracle(b, requests=None):
     return oracle.batch_attention(b.q, b.qo_indptr, b.k_cache, b.v_cache, b.layout, b.page_indptr,
                                   b.page_indices, b.last_page_len, b.num_qo_heads, b.num_kv_heads,
-                                  b.page_size, b.sm_scale, b.causal, requests=requests)
+                                  b.page_size, b.sm_scale, b.causal, requests=requests,
+                                  window_left=b.window_left)
 
 
 def _rows(b, requests):
@@ -184,3 +185,17 @@ def test_out_of_range_page_index_is_reported_not_read():
     torch.cuda.synchronize()
     ref_o, ref_l = _oracle(b, [1])
     compare(db.out, db.lse, ref_o, ref_l, rows=np.array([1]), what="bounds, clean request")
+
+
+@pytest.mark.parametrize("g,d", [(1, 128), (8, 128), (2, 256), (4, 64)])
+@pytest.mark.parametrize("w", [0, 1, 15, 16, 17, 300, 5000])
+def test_sliding_window_decode(g, d, w):
+    """Left window: a decode row sees its last w+1 keys. Covers a window
+    start inside a page, on a page boundary, inside the first chunk of a
+    split request, and wider than the context."""
+    hkv = 2
+    kv = [1, 16, 17, 40, 700, 9000]
+    b = synth.make_batch(f"window {w} g{g} d{d}", kv, [1] * len(kv), g * hkv, hkv, d, 16,
+                         synth.NHD if g % 2 else synth.HND, None, False, 200 + w + g,
+                         window_left=w)
+    check(scale_v(b), sms=8)

@@ -12,7 +12,7 @@ import oracle  # noqa: E402
 from paged_kv_attention_27_gb300 import binding as B  # noqa: E402
 from paged_kv_attention_27_gb300 import synth  # noqa: E402
 
-from ._gpu import compare, ensure_built  # noqa: E402
+from ._gpu import compare, ensure_built, scale_v  # noqa: E402
 
 pytestmark = pytest.mark.gpu
 
@@ -37,7 +37,8 @@ def _run(b, sms=None):
 def _oracle(b, rows=None, requests=None):
     return oracle.batch_attention(b.q, b.qo_indptr, b.k_cache, b.v_cache, b.layout, b.page_indptr,
                                   b.page_indices, b.last_page_len, b.num_qo_heads, b.num_kv_heads,
-                                  b.page_size, b.sm_scale, b.causal, requests=requests, rows=rows)
+                                  b.page_size, b.sm_scale, b.causal, requests=requests, rows=rows,
+                                  window_left=b.window_left)
 
 
 def check_full(b, what=None):
@@ -62,6 +63,9 @@ def sample_rows(b, per_request=24, seed=0):
             if len(s) > per_request // 2:
                 break
         s.update({min(n - 1, b.page_size - 1), min(n - 1, b.page_size)})
+        if b.window_left >= 0:       # rows where the window starts to cut keys off
+            w = b.window_left
+            s.update({min(n - 1, x) for x in (w, w + 1, w + 127, w + 128, w + 129)})
         s.update(rng.integers(0, n, size=per_request // 2).tolist())
         rows[r] = sorted(s)
     return rows
@@ -149,6 +153,31 @@ def test_large_scores_stay_finite_with_rescale():
     check_full(b)
 
 
+@pytest.mark.parametrize("d", [64, 128, 256])
+@pytest.mark.parametrize("w", [0, 1, 63, 127, 128, 129, 500])
+def test_sliding_window_causal_prefill(d, w):
+    kv = [1, 17, 200, 700, 1000]
+    qo = [1, 17, 200, 300, 1000]      # one decode row, full prefills and a chunk
+    b = synth.make_batch(f"window {w} d{d}", kv, qo, 8, 2, d, 16 if d < 256 else 32,
+                         synth.NHD, None, True, 300 + w + d, window_left=w)
+    check_full(scale_v(b))
+
+
+@pytest.mark.parametrize("w", [0, 40, 260])
+def test_sliding_window_non_causal_prefill(w):
+    kv = [0, 50, 300, 600]
+    qo = [3, 80, 17, 130]
+    b = synth.make_batch(f"window {w} non-causal", kv, qo, 8, 8, 128, 16, synth.HND, None, False,
+                         400 + w, window_left=w)
+    check_full(scale_v(b))
+
+
+def test_sliding_window_mixed_batch():
+    b = synth.small_mixed()
+    b.window_left = 100
+    check_full(b)
+
+
 # ---- full-size workloads, sampled rows ------------------------------------
 
 @pytest.mark.parametrize("L", [1024, 4096, 16384])
@@ -163,3 +192,36 @@ def test_ragged_prefill_full_size():
 def test_mixed_chunk_decode_full_size():
     b = synth.mixed_chunk_decode()
     check_sampled(b, per_request=16, requests=set(range(8)) | {8, 9, 20, 33, 63})
+
+
+# ---- failure path: a bounded wait that runs out ----------------------------
+
+@pytest.mark.parametrize("case", ["d128", "d256", "mixed"])
+def test_bounded_wait_times_out_and_context_survives(case):
+    """The test hook makes the first CTA's K producer skip its first tile, so
+    the MMA issuer's bounded wait on that tile runs out: the call must report
+    FI_ERR_DEVICE_TIMEOUT (no hang, no fault), and the next call in the same
+    context must be correct."""
+    from paged_kv_attention_27_gb300.device import DeviceBatch
+    if case == "mixed":
+        b = synth.small_mixed()
+    else:
+        d = int(case[1:])
+        kv = [900, 300]
+        b = synth.make_batch(f"timeout {case}", kv, kv, 8, 2, d, 16, synth.NHD, None, True, 16)
+    db = DeviceBatch(b, mode=B.FI_MODE_PREFILL)
+    B.fi_debug_set_fault(1, 2_000_000)          # 2 ms bound
+    try:
+        db.run()
+        assert db.status() == B.FI_ERR_DEVICE_TIMEOUT
+    finally:
+        B.fi_debug_set_fault(0, 0)
+    out, lse = db.run()
+    torch.cuda.synchronize()
+    assert db.status() == B.FI_OK
+    ref_o, ref_l = _oracle(b)
+    compare(out, lse, ref_o, ref_l, what=f"after timeout ({case})")
+
+
+def test_sliding_window_prefill_16k_full_size():
+    check_sampled(synth.causal_prefill(16384, window_left=4095), per_request=16)

@@ -77,7 +77,7 @@ def test_noalloc_rejects_plans_beyond_its_scratch():
     pi = np.zeros(513, np.int32)
     pi[1:] = np.cumsum(np.full(512, 32768 // 32))
     plan = B.fi_plan(B.FI_MODE_DECODE, 512, None, pi, np.full(512, 32, np.int32), 16, 8, 256, 32,
-                     0, 100000)
+                     0, None, 100000)
     assert plan.workspace_bytes > (16 << 20)
     x = torch.empty(16, device="cuda")
     with pytest.raises(B.FiError) as e:
