@@ -53,6 +53,29 @@ def bf16_to_f64(bits: np.ndarray) -> np.ndarray:
     return (bits.astype(np.uint32) << np.uint32(16)).view(np.float32).astype(np.float64)
 
 
+def f16_to_f64(bits: np.ndarray) -> np.ndarray:
+    """Exact value of IEEE binary16 bit patterns (uint16) as float64, from
+    the format's definition: sign bit, 5 exponent bits (bias 15), 10
+    fraction bits; exponent 0 is subnormal (2^-14 * f/1024), 31 is inf/NaN."""
+    b = np.asarray(bits, dtype=np.uint16).astype(np.int64)
+    sign = np.where(b >> 15, -1.0, 1.0)
+    e = (b >> 10) & 0x1F
+    f = (b & 0x3FF).astype(np.float64)
+    normal = sign * np.ldexp(1.0 + f / 1024.0, (e - 15).astype(np.int32))
+    sub = sign * np.ldexp(f / 1024.0, -14)
+    special = np.where(f == 0, sign * np.inf, np.nan)
+    return np.where(e == 0, sub, np.where(e == 31, special, normal))
+
+
+def to_f64(bits: np.ndarray, dtype: str) -> np.ndarray:
+    """Exact value of bf16 or fp16 bit patterns as float64."""
+    if dtype == "bf16":
+        return bf16_to_f64(bits)
+    if dtype == "fp16":
+        return f16_to_f64(bits)
+    raise ValueError(dtype)
+
+
 def kv_lengths(page_indptr, last_page_len, page_size: int) -> np.ndarray:
     """Tokens held by each request's pages (all pages full but the last)."""
     page_indptr = np.asarray(page_indptr, dtype=np.int64)
@@ -62,9 +85,10 @@ def kv_lengths(page_indptr, last_page_len, page_size: int) -> np.ndarray:
 
 
 def gather_kv(cache_bits: np.ndarray, layout: str, page_indptr, page_indices,
-              b: int, kv_head: int, kv_len: int, page_size: int) -> np.ndarray:
+              b: int, kv_head: int, kv_len: int, page_size: int,
+              dtype: str = "bf16") -> np.ndarray:
     """Rows 0..kv_len-1 of kv head ``kv_head`` of request ``b``, in token
-    order, as float64 ``[kv_len, d]``."""
+    order, as float64 ``[kv_len, d]`` (cache elements of ``dtype``)."""
     t = np.arange(kv_len, dtype=np.int64)
     pages = np.asarray(page_indices, dtype=np.int64)[int(page_indptr[b]) + t // page_size]
     slots = t % page_size
@@ -74,7 +98,7 @@ def gather_kv(cache_bits: np.ndarray, layout: str, page_indptr, page_indices,
         rows = cache_bits[pages, kv_head, slots, :]
     else:
         raise ValueError(layout)
-    return bf16_to_f64(rows)
+    return to_f64(rows, dtype)
 
 
 def visible_keys(qo_len: int, kv_len: int, causal: bool, window_left: int = -1) -> np.ndarray:
@@ -129,10 +153,11 @@ def softmax_attention(q: np.ndarray, k: np.ndarray, v: np.ndarray, sm_scale: flo
 def batch_attention(q_bits, qo_indptr, k_cache_bits, v_cache_bits, layout: str,
                     page_indptr, page_indices, last_page_len, num_qo_heads: int,
                     num_kv_heads: int, page_size: int, sm_scale: float, causal: bool,
-                    requests=None, rows=None, window_left: int = -1):
+                    requests=None, rows=None, window_left: int = -1, dtype: str = "bf16"):
     """Paged attention for a packed batch.
 
-    q_bits ``[sum qo_len, Hq, d]`` bf16 bits; caches as laid out by ``layout``.
+    q_bits ``[sum qo_len, Hq, d]`` bit patterns of ``dtype`` ("bf16" or
+    "fp16", as are the caches); caches as laid out by ``layout``.
     Returns ``out [sum qo_len, Hq, d]`` and ``lse [sum qo_len, Hq]`` in
     float64. ``requests`` limits the work to some requests (other rows stay
     NaN); ``rows`` maps a request to the list of its row indices to compute
@@ -157,11 +182,11 @@ def batch_attention(q_bits, qo_indptr, k_cache_bits, v_cache_bits, layout: str,
         vis = visible_keys(qo_len, int(kv_len[b]), causal, window_left)[sel]
         for kh in range(num_kv_heads):
             k = gather_kv(k_cache_bits, layout, page_indptr, page_indices, b, kh,
-                          int(kv_len[b]), page_size)
+                          int(kv_len[b]), page_size, dtype)
             v = gather_kv(v_cache_bits, layout, page_indptr, page_indices, b, kh,
-                          int(kv_len[b]), page_size)
+                          int(kv_len[b]), page_size, dtype)
             for h in range(kh * group, (kh + 1) * group):
-                qh = bf16_to_f64(q_bits[q0 + sel, h, :])
+                qh = to_f64(q_bits[q0 + sel, h, :], dtype)
                 o, l = softmax_attention(qh, k, v, sm_scale, vis)
                 out[q0 + sel, h] = o
                 lse[q0 + sel, h] = l
@@ -170,7 +195,8 @@ def batch_attention(q_bits, qo_indptr, k_cache_bits, v_cache_bits, layout: str,
 
 def batch_decode(q_bits, k_cache_bits, v_cache_bits, layout: str, page_indptr,
                  page_indices, last_page_len, num_qo_heads: int, num_kv_heads: int,
-                 page_size: int, sm_scale: float, requests=None, window_left: int = -1):
+                 page_size: int, sm_scale: float, requests=None, window_left: int = -1,
+                 dtype: str = "bf16"):
     """One query token per request: q_bits ``[B, Hq, d]``; out ``[B, Hq, d]``,
     lse ``[B, Hq]``. Every key of the request is visible, or with a left
     window only the last ``window_left + 1``."""
@@ -178,7 +204,7 @@ def batch_decode(q_bits, k_cache_bits, v_cache_bits, layout: str, page_indptr,
     return batch_attention(q_bits, np.arange(B + 1), k_cache_bits, v_cache_bits, layout,
                            page_indptr, page_indices, last_page_len, num_qo_heads,
                            num_kv_heads, page_size, sm_scale, False, requests=requests,
-                           window_left=window_left)
+                           window_left=window_left, dtype=dtype)
 
 
 # --------------------------------------------------------------------------

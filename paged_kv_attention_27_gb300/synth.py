@@ -5,8 +5,8 @@ This module builds inputs only. It holds none of the attention arithmetic:
 no scores, no softmax, no merge. Everything it returns is plain numpy:
 
 * values are standard normal draws from numpy's counter-based Philox
-  generator, rounded to bf16 (round-to-nearest-even) and stored as raw
-  ``uint16`` bit patterns;
+  generator, rounded to bf16 or fp16 (round-to-nearest-even) and stored as
+  raw ``uint16`` bit patterns;
 * the page table is the CSR triple ``page_indptr`` / ``page_indices`` /
   ``last_page_len`` of a paged KV cache (pages of ``page_size`` token slots,
   allocated on demand, "FlashInfer kernel library deep-dive", section
@@ -54,11 +54,29 @@ def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
     return out
 
 
+def f32_to_f16_bits(x: np.ndarray) -> np.ndarray:
+    """Round float32 values to IEEE fp16 (numpy's conversion: round to
+    nearest, ties to even; overflow to inf). Returns uint16 bit patterns."""
+    return np.ascontiguousarray(x, dtype=np.float32).astype(np.float16).view(np.uint16)
+
+
+def to_bits(x: np.ndarray, dtype: str) -> np.ndarray:
+    """float32 values -> bit patterns of ``dtype`` ("bf16" or "fp16")."""
+    if dtype == "bf16":
+        return f32_to_bf16_bits(x)
+    if dtype == "fp16":
+        return f32_to_f16_bits(x)
+    raise ValueError(dtype)
+
+
+QNAN_BITS = {"bf16": 0x7FC0, "fp16": 0x7E00}
+
 _CHUNK = 1 << 22
 
 
-def normal_bf16(seed: int, stream: int, shape) -> np.ndarray:
-    """Standard normal values of ``shape`` as bf16 bit patterns (uint16).
+def normal_bf16(seed: int, stream: int, shape, dtype: str = "bf16") -> np.ndarray:
+    """Standard normal values of ``shape`` as bit patterns (uint16) of
+    ``dtype`` (bf16 by default, or fp16).
 
     Element block j (of 2^22 elements) is drawn from its own Philox stream
     keyed by (seed, stream, j), so the values do not depend on how many
@@ -73,7 +91,7 @@ def normal_bf16(seed: int, stream: int, shape) -> np.ndarray:
         s = j * _CHUNK
         c = min(_CHUNK, n - s)
         g = np.random.Generator(np.random.Philox(key=[int(seed) * 64 + int(stream), j]))
-        out[s:s + c] = f32_to_bf16_bits(g.standard_normal(c, dtype=np.float32))
+        out[s:s + c] = to_bits(g.standard_normal(c, dtype=np.float32), dtype)
 
     blocks = range((n + _CHUNK - 1) // _CHUNK)
     with cf.ThreadPoolExecutor(max_workers=min(32, os.cpu_count() or 1)) as ex:
@@ -105,6 +123,7 @@ class PagedBatch:
     shared_prefix_pages: int = 0
     meta: dict = field(default_factory=dict)
     window_left: int = -1        # left attention window (-1 = unbounded)
+    dtype: str = "bf16"          # element type of q, K, V ("bf16" or "fp16")
 
     @property
     def batch(self) -> int:
@@ -123,7 +142,8 @@ def make_batch(name: str, kv_lens, qo_lens, num_qo_heads: int, num_kv_heads: int
                head_dim: int, page_size: int, layout: str, sm_scale: float | None,
                causal: bool, seed: int, shared_prefix_requests: int = 0,
                shared_prefix_tokens: int = 0, tail_fill: str = "normal",
-               extra_pages: int = 0, window_left: int = -1) -> PagedBatch:
+               extra_pages: int = 0, window_left: int = -1,
+               dtype: str = "bf16") -> PagedBatch:
     """Build a paged batch with seeded values and a shuffled page table.
 
     ``shared_prefix_requests`` requests (the first ones) map their first
@@ -168,9 +188,9 @@ def make_batch(name: str, kv_lens, qo_lens, num_qo_heads: int, num_kv_heads: int
 
     Hkv, d = num_kv_heads, head_dim
     shape = (num_phys, P, Hkv, d) if layout == NHD else (num_phys, Hkv, P, d)
-    k_cache = normal_bf16(seed, 1, shape)
-    v_cache = normal_bf16(seed, 2, shape)
-    q = normal_bf16(seed, 3, (int(qo_lens.sum()), num_qo_heads, d))
+    k_cache = normal_bf16(seed, 1, shape, dtype)
+    v_cache = normal_bf16(seed, 2, shape, dtype)
+    q = normal_bf16(seed, 3, (int(qo_lens.sum()), num_qo_heads, d), dtype)
     if tail_fill == "nan":
         for b in range(B):
             if npages[b] == 0 or last[b] == P:
@@ -178,9 +198,9 @@ def make_batch(name: str, kv_lens, qo_lens, num_qo_heads: int, num_kv_heads: int
             p = page_lists[b][-1]
             for cache in (k_cache, v_cache):
                 if layout == NHD:
-                    cache[p, last[b]:, :, :] = 0x7FC0
+                    cache[p, last[b]:, :, :] = QNAN_BITS[dtype]
                 else:
-                    cache[p, :, last[b]:, :] = 0x7FC0
+                    cache[p, :, last[b]:, :] = QNAN_BITS[dtype]
     if sm_scale is None:
         sm_scale = 1.0 / math.sqrt(head_dim)
     return PagedBatch(name=name, num_qo_heads=num_qo_heads, num_kv_heads=num_kv_heads,
@@ -190,7 +210,7 @@ def make_batch(name: str, kv_lens, qo_lens, num_qo_heads: int, num_kv_heads: int
                       last_page_len=last.astype(np.int32), q=q, k_cache=k_cache, v_cache=v_cache,
                       shared_prefix_pages=int(prefix_pages),
                       meta={"seed": seed, "shared_prefix_requests": shared_prefix_requests},
-                      window_left=int(window_left))
+                      window_left=int(window_left), dtype=dtype)
 
 
 # ----------------------------------------------------------------------------
@@ -307,4 +327,5 @@ def sub_batch(src: PagedBatch, requests) -> PagedBatch:
                       qo_lens=qo_lens.copy(), qo_indptr=qo_indptr, page_indptr=page_indptr,
                       page_indices=page_indices, last_page_len=src.last_page_len[requests].copy(),
                       q=q, k_cache=src.k_cache[idx], v_cache=src.v_cache[idx],
-                      meta=dict(src.meta, sample=requests), window_left=src.window_left)
+                      meta=dict(src.meta, sample=requests), window_left=src.window_left,
+                      dtype=src.dtype)

@@ -66,6 +66,52 @@ def test_bf16_bit_patterns():
     assert math.copysign(1.0, got[-1]) == -1.0
 
 
+def test_fp16_bit_patterns():
+    """Hand-decoded IEEE binary16 values, then every pattern against numpy's
+    own float16 type (an independent decoder)."""
+    bits = np.array([0x3C00, 0xC000, 0x3555, 0x7BFF, 0x0001, 0x03FF, 0x0400, 0x7C00, 0xFC00,
+                     0x0000, 0x8000], dtype=np.uint16)
+    want = [1.0, -2.0, 0.333251953125, 65504.0, 2.0 ** -24, 1023 * 2.0 ** -24, 2.0 ** -14,
+            math.inf, -math.inf, 0.0, -0.0]
+    got = oracle.f16_to_f64(bits)
+    for g, w in zip(got, want):
+        assert g == w
+    assert math.copysign(1.0, got[-1]) == -1.0
+    allbits = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
+    ref = allbits.view(np.float16).astype(np.float64)
+    mine = oracle.f16_to_f64(allbits)
+    same = (mine == ref) | (np.isnan(mine) & np.isnan(ref))
+    assert same.all()
+
+
+def test_fp16_inputs_match_torch_sdpa_float64():
+    """A prefill batch in fp16 against torch SDPA in float64 on tensors that
+    torch decodes from the same bits itself."""
+    torch = pytest.importorskip("torch")
+    b = synth.make_batch("fp16", [40, 130], [40, 33], 8, 2, 32, 16, synth.NHD, None, True, 23,
+                         dtype="fp16")
+    out, lse = _run(b)
+    g = b.num_qo_heads // b.num_kv_heads
+    for r in range(b.batch):
+        kv, qo = int(b.kv_lens[r]), int(b.qo_lens[r])
+        pages = b.page_indices[int(b.page_indptr[r]):int(b.page_indptr[r + 1])]
+        to = lambda x: torch.from_numpy(np.ascontiguousarray(x).view(np.int16)).view(
+            torch.float16).to(torch.float64)
+        kt = to(np.concatenate([b.k_cache[p] for p in pages], axis=0)[:kv]).transpose(0, 1)
+        vt = to(np.concatenate([b.v_cache[p] for p in pages], axis=0)[:kv]).transpose(0, 1)
+        qt = to(b.q[int(b.qo_indptr[r]):int(b.qo_indptr[r + 1])]).transpose(0, 1)
+        kt, vt = kt.repeat_interleave(g, 0), vt.repeat_interleave(g, 0)
+        mask = torch.ones(qo, kv, dtype=torch.bool).tril(kv - qo)
+        so = torch.nn.functional.scaled_dot_product_attention(qt, kt, vt, attn_mask=mask,
+                                                              scale=b.sm_scale)
+        rows = slice(int(b.qo_indptr[r]), int(b.qo_indptr[r + 1]))
+        np.testing.assert_allclose(out[rows], so.transpose(0, 1).numpy(), rtol=0, atol=1e-12)
+    # the same draws rounded to bf16 give a different (but close) answer
+    b16 = synth.make_batch("bf16", [40, 130], [40, 33], 8, 2, 32, 16, synth.NHD, None, True, 23)
+    o16, _ = _run(b16)
+    assert not np.array_equal(o16, out) and np.abs(o16 - out).max() < 0.05
+
+
 def test_kv_lengths_of_tiny_config():
     b = synth.tiny_decode()
     # pages {1,2,4,7}, last page lengths {1,1,16,4} for KV lengths {1,17,64,100}
@@ -202,7 +248,7 @@ def _run(b, requests=None):
     return oracle.batch_attention(b.q, b.qo_indptr, b.k_cache, b.v_cache, b.layout, b.page_indptr,
                                   b.page_indices, b.last_page_len, b.num_qo_heads, b.num_kv_heads,
                                   b.page_size, b.sm_scale, b.causal, requests=requests,
-                                  window_left=b.window_left)
+                                  window_left=b.window_left, dtype=b.dtype)
 
 
 def test_permuting_physical_pages_changes_nothing():
