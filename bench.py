@@ -75,6 +75,8 @@ WORKLOADS = {
     "causal_prefill_4k": ("causal_prefill", {"seq_len": 4096}),
     "causal_prefill_16k": ("causal_prefill", {"seq_len": 16384}),
     "causal_prefill_16k_window4k": ("causal_prefill", {"seq_len": 16384, "window_left": 4095}),
+    "causal_prefill_4k_fp16": ("causal_prefill", {"seq_len": 4096, "dtype": "fp16"}),
+    "llama7b_decode_fp16": ("llama7b_decode", {"dtype": "fp16"}),
     "ragged_prefill": ("ragged_prefill", {}),
     "mixed_chunk_decode": ("mixed_chunk_decode", {}),
 }
@@ -458,8 +460,8 @@ def run_ours(args, rank, world, local_rank):
     line = {
         "metric": METRIC, "value": value, "unit": unit, "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-        "data": "synthetic (seeded Philox normals rounded to bf16, shuffled page table)",
+        "scaling": "weak", "vs_baseline": None, "dtype": b.dtype,
+        "data": f"synthetic (seeded Philox normals rounded to {b.dtype}, shuffled page table)",
         "config": config_of(b, info, kvb, flops),
         "roofline": roofline_of(b, kvb, flops, kern_ms, kernels_of(b, info), args.workload),
         "tflops": flops * world / (ms_step / 1e3) / 1e12,

@@ -179,19 +179,21 @@ fi_status fi_plan_get_work(fi_plan_t plan, int32_t* items_h, int32_t capacity,
  * One query token per request ("FlashInfer kernel library deep-dive",
  * sections "single-request layer" and "batch layer"): for every request b
  * and query head h, out[b][h] = softmax(sm_scale * q[b][h] K_b^T) V_b over
- * all kv_len[b] keys of kv head h/g. Each K/V page is loaded once and
+ * all kv_len[b] keys of kv head h/g (the last window_left + 1 of them with
+ * a left window). Each K/V page is loaded once and
  * shared by the g query heads of its group. Long requests are split over
  * several CTAs as the plan says; their fp32 partial states are merged by
  * log-sum-exp into out/lse before the call's work completes on the stream.
  *   plan             from fi_plan(FI_MODE_DECODE, ...).
- *   q                device bf16 [B][num_qo_heads][head_dim].
- *   k_cache, v_cache device bf16 paged caches (layout, page_stride_elems
- *                    as in the conventions above), num_pages pages each.
+ *   q                device [B][num_qo_heads][head_dim] of the plan's dtype.
+ *   k_cache, v_cache device paged caches of the plan's dtype (layout,
+ *                    page_stride_elems as in the conventions above),
+ *                    num_pages pages each.
  *   page_indptr_d, page_indices_d, last_page_len_d  device int32 copies of
  *                    the planned page table.
  *   sm_scale         score scale, finite and >= 0 (1/sqrt(head_dim) is the
  *                    usual value); anything else is FI_ERR_INVALID_ARG.
- *   out              device bf16 [B][num_qo_heads][head_dim].
+ *   out              device [B][num_qo_heads][head_dim], the plan's dtype.
  *   lse              device fp32 [B][num_qo_heads] or NULL.
  *   workspace        device buffer of at least the planned size, 256-byte
  *                    aligned; its contents between calls belong to the
@@ -245,7 +247,8 @@ fi_status fi_batch_decode_paged_noalloc(fi_plan_t plan, const void* q, const voi
  * Requests may mix prompt chunks and single decode rows in one call
  * (continuous batching with chunked prefill, same section).
  *   plan         from fi_plan(FI_MODE_PREFILL, ...); carries `causal`.
- *   q            device bf16 [sum qo_len][num_qo_heads][head_dim].
+ *   q            device [sum qo_len][num_qo_heads][head_dim] of the plan's
+ *                dtype.
  *   qo_indptr_d  device int32 copy of the planned qo_indptr.
  *   other arguments as for fi_batch_decode_paged; out has q's shape and
  *   lse is fp32 [sum qo_len][num_qo_heads] or NULL.
@@ -269,12 +272,14 @@ fi_status fi_batch_prefill_paged(fi_plan_t plan, const void* q, const int32_t* q
  *   out[r][h] = sum_i w_i v[r][i][h] / sum_i w_i;  lse = M + ln sum_i w_i.
  * States with s = -inf weigh nothing; if all are -inf, out = 0, lse = -inf.
  *   v        device fp32 [n][S][H][d];   s  device fp32 [n][S][H].
- *   out      device bf16 [n][H][d] (16-byte aligned); lse_out fp32 [n][H] or NULL.
+ *   out_dtype  fi_dtype of out (bf16 or fp16).
+ *   out      device [n][H][d] of out_dtype (16-byte aligned); lse_out fp32
+ *            [n][H] or NULL.
  *   d        multiple of 4, at most 1024; n, S, H >= 0 (n == 0 or H == 0: no-op).
  * Errors: FI_ERR_INVALID_ARG, FI_ERR_NO_DEVICE, FI_ERR_CUDA.
  */
 fi_status fi_merge_states(const float* v, const float* s, int32_t n, int32_t S, int32_t H,
-                          int32_t d, void* out, float* lse_out, void* stream);
+                          int32_t d, int32_t out_dtype, void* out, float* lse_out, void* stream);
 
 /*
  * fi_check_device_status — synchronises `stream`, reads and clears the

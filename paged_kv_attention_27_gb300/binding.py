@@ -89,7 +89,7 @@ def lib():
                                         ctypes.c_float, _P, _P, _P, ctypes.c_size_t, _P]
     L.fi_batch_prefill_paged.argtypes = [_P, _P, _P, _P, _P, _I32, _I64, _I32, _P, _P, _P,
                                          ctypes.c_float, _P, _P, _P, ctypes.c_size_t, _P]
-    L.fi_merge_states.argtypes = [_P, _P, _I32, _I32, _I32, _I32, _P, _P, _P]
+    L.fi_merge_states.argtypes = [_P, _P, _I32, _I32, _I32, _I32, _I32, _P, _P, _P]
     L.fi_check_device_status.argtypes = [_P, _P]
     L.fi_status_string.argtypes = [_I32]
     L.fi_status_string.restype = ctypes.c_char_p
@@ -223,9 +223,9 @@ def fi_batch_prefill_paged(plan: Plan, q, qo_indptr_d, k_cache, v_cache, kv_layo
     _check(st, "fi_batch_prefill_paged")
 
 
-def fi_merge_states(v, s, n, S, H, d, out, lse_out, stream=None):
-    st = lib().fi_merge_states(_ptr(v), _ptr(s), int(n), int(S), int(H), int(d), _ptr(out),
-                               _ptr(lse_out), _stream(stream))
+def fi_merge_states(v, s, n, S, H, d, out_dtype, out, lse_out, stream=None):
+    st = lib().fi_merge_states(_ptr(v), _ptr(s), int(n), int(S), int(H), int(d), int(out_dtype),
+                               _ptr(out), _ptr(lse_out), _stream(stream))
     _check(st, "fi_merge_states")
 
 

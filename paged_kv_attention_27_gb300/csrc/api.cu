@@ -71,8 +71,12 @@ bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 
 // Tensor map over a paged K or V cache that fetches one (page, kv head)
 // block of page_size rows x 64 dims (128 bytes, 128-byte swizzled) per box.
+CUtensorMapDataType tma_type(int dtype) {
+  return dtype == FI_DTYPE_FP16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+}
+
 fi_status make_kv_map(CUtensorMap* map, const void* base, int layout, int num_pages, int P,
-                      int Hkv, int d, int64_t page_stride) {
+                      int Hkv, int d, int64_t page_stride, int dtype) {
   auto enc = encode_fn();
   if (!enc) {
     g_last_error = "cuTensorMapEncodeTiled is not available from the driver";
@@ -94,7 +98,7 @@ fi_status make_kv_map(CUtensorMap* map, const void* base, int layout, int num_pa
     box[0] = 64; box[1] = P; box[2] = 1; box[3] = 1;
   }
   strides[2] = cuuint64_t(page_stride) * 2;
-  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims,
+  CUresult r = enc(map, tma_type(dtype), 4, const_cast<void*>(base), dims,
                    strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) {
@@ -106,7 +110,7 @@ fi_status make_kv_map(CUtensorMap* map, const void* base, int layout, int num_pa
 
 // Tensor map over the packed queries [rows][num_qo_heads][head_dim] that
 // fetches 128 rows x 64 dims of one head per box (128-byte swizzled).
-fi_status make_q_map(CUtensorMap* map, const void* q, int64_t rows, int Hq, int d) {
+fi_status make_q_map(CUtensorMap* map, const void* q, int64_t rows, int Hq, int d, int dtype) {
   auto enc = encode_fn();
   if (!enc) {
     g_last_error = "cuTensorMapEncodeTiled is not available from the driver";
@@ -116,7 +120,7 @@ fi_status make_q_map(CUtensorMap* map, const void* q, int64_t rows, int Hq, int 
   const cuuint64_t strides[2] = {cuuint64_t(d) * 2, cuuint64_t(Hq) * d * 2};
   const cuuint32_t box[3] = {64, 1, cuuint32_t(fi::kPrefillTileM)};
   const cuuint32_t estr[3] = {1, 1, 1};
-  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(q), dims, strides,
+  CUresult r = enc(map, tma_type(dtype), 3, const_cast<void*>(q), dims, strides,
                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) {
@@ -176,10 +180,10 @@ fi_status run_paged(fi_plan_t plan, bool prefill_call, const void* q, const int3
   CUtensorMap kmap, vmap;
   if (P.total_kv > 0) {
     st = make_kv_map(&kmap, k_cache, kv_layout, num_pages, P.page_size, P.num_kv_heads,
-                     P.head_dim, page_stride_elems);
+                     P.head_dim, page_stride_elems, P.dtype);
     if (st != FI_OK) return st;
     st = make_kv_map(&vmap, v_cache, kv_layout, num_pages, P.page_size, P.num_kv_heads,
-                     P.head_dim, page_stride_elems);
+                     P.head_dim, page_stride_elems, P.dtype);
     if (st != FI_OK) return st;
   } else {
     std::memset(&kmap, 0, sizeof(kmap));
@@ -191,7 +195,7 @@ fi_status run_paged(fi_plan_t plan, bool prefill_call, const void* q, const int3
 
   CUtensorMap qmap;
   if (!P.prefill_items.empty()) {
-    st = make_q_map(&qmap, q, P.total_q, P.num_qo_heads, P.head_dim);
+    st = make_q_map(&qmap, q, P.total_q, P.num_qo_heads, P.head_dim, P.dtype);
     if (st != FI_OK) return st;
   }
 
@@ -240,7 +244,8 @@ fi_status run_paged(fi_plan_t plan, bool prefill_call, const void* q, const int3
     pp.err = err;
     pp.wait_limit_ns = g_wait_limit_ns;
     pp.fault_kind = fault_kind;
-    e = fi::launch_prefill(P.head_dim, qmap, kmap, vmap, pp, int(P.prefill_items.size()), stream);
+    e = fi::launch_prefill(P.head_dim, P.dtype, qmap, kmap, vmap, pp,
+                           int(P.prefill_items.size()), stream);
     if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
   }
   if (!P.decode_items.empty()) {
@@ -260,7 +265,7 @@ fi_status run_paged(fi_plan_t plan, bool prefill_call, const void* q, const int3
     dp.err = err;
     dp.wait_limit_ns = g_wait_limit_ns;
     dp.fault_kind = fault_kind;
-    e = fi::launch_decode(P.head_dim, P.num_qo_heads / P.num_kv_heads, kmap, vmap, dp,
+    e = fi::launch_decode(P.head_dim, P.num_qo_heads / P.num_kv_heads, P.dtype, kmap, vmap, dp,
                           int(P.decode_items.size()), dstream);
     if (e != cudaSuccess) return cuda_fail(e, "decode launch");
   }
@@ -283,6 +288,7 @@ fi_status run_paged(fi_plan_t plan, bool prefill_call, const void* q, const int3
     mp.d = P.head_dim;
     mp.out = out;
     mp.lse = lse;
+    mp.dtype = P.dtype;
     e = fi::launch_merge(mp, int(P.merges.size()), stream);
     if (e != cudaSuccess) return cuda_fail(e, "merge launch");
   }
@@ -386,8 +392,9 @@ fi_status fi_batch_prefill_paged(fi_plan_t plan, const void* q, const int32_t* q
 }
 
 fi_status fi_merge_states(const float* v, const float* s, int32_t n, int32_t S, int32_t H,
-                          int32_t d, void* out, float* lse_out, void* stream) {
+                          int32_t d, int32_t out_dtype, void* out, float* lse_out, void* stream) {
   if (n < 0 || S < 0 || H < 0 || d <= 0 || d % 4 != 0 || d > 1024) return FI_ERR_INVALID_ARG;
+  if (out_dtype != FI_DTYPE_BF16 && out_dtype != FI_DTYPE_FP16) return FI_ERR_INVALID_ARG;
   if (n == 0 || H == 0) return FI_OK;
   if (!out || (S > 0 && (!v || !s))) return FI_ERR_INVALID_ARG;
   if (!aligned(out, 16) || (v && !aligned(v, 16)) || (s && !aligned(s, 4)) ||
@@ -404,6 +411,7 @@ fi_status fi_merge_states(const float* v, const float* s, int32_t n, int32_t S, 
   mp.d = d;
   mp.out = out;
   mp.lse = lse_out;
+  mp.dtype = out_dtype;
   cudaError_t e = fi::launch_merge(mp, n, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "merge launch");
   return FI_OK;

@@ -16,11 +16,10 @@
 //     running max / sum / accumulator (the online softmax of section 1 of the
 //     FlashAttention-3 page), rescaling whenever the max grows;
 //   * the warps' states are merged in shared memory; the CTA writes either
-//     the final bf16 row + lse, or an fp32 partial state that the merge
+//     the final row (bf16 or fp16, the inputs' type) + lse, or an fp32 partial state that the merge
 //     kernel combines by log-sum-exp.
 // Scores are kept in the log2 domain (q pre-scaled by sm_scale*log2(e)).
-#include <cuda_bf16.h>
-
+#include "elem.cuh"
 #include "fi_internal.h"
 #include "kernels.cuh"
 #include "ptx.cuh"
@@ -63,19 +62,14 @@ __device__ __forceinline__ uint32_t swz(int r, int c8) {
   return uint32_t(r * 128 + ((c8 ^ (r & 7)) << 4));
 }
 
-__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
-  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
-  return *reinterpret_cast<uint32_t*>(&v);
-}
-
 // Tensor-core consumer warp for GQA groups of 4 or 8 heads. Per 16-token
 // chunk of its share of a stage: S (16 x 16, rows = the group's heads padded
 // with zeros) = Q K^T by m16n8k16 MMAs with K read by ldmatrix from the
 // swizzled stage; an online softmax per head row (a quad of lanes holds a
-// row); P rounded to bf16 is reused as the A fragment of O += P V, with V
+// row); P rounded to the element type is reused as the A fragment of O += P V, with V
 // read by ldmatrix.trans. Leaves the warp's (m, l, lp, O) in shared memory
 // and returns whether any consumer aborted (voted, so all agree).
-template <int HEAD_DIM, int GROUP>
+template <int HEAD_DIM, int GROUP, class E>
 __device__ __forceinline__ bool mma_consumer(const DecodeParams& prm, const WorkItem& item,
                                              int n_tok, int lead, int n_tiles,
                                              uint32_t smem_base,
@@ -94,7 +88,7 @@ __device__ __forceinline__ bool mma_consumer(const DecodeParams& prm, const Work
   uint32_t qa[KS][4];
   {
     const uint32_t* qp = reinterpret_cast<const uint32_t*>(
-        reinterpret_cast<const __nv_bfloat16*>(prm.q) +
+        reinterpret_cast<const uint16_t*>(prm.q) +
         (size_t(item.q_row) * prm.num_qo_heads + item.head * GROUP + (r < GROUP ? r : 0)) *
             HEAD_DIM);
 #pragma unroll
@@ -143,8 +137,8 @@ __device__ __forceinline__ bool mma_consumer(const DecodeParams& prm, const Work
         const int dim = ks * 16 + (mi & 1) * 8;
         uint32_t b0, b1, b2, b3;
         ldsm_x4(kbase + (dim >> 6) * C::TILE * 128 + swz(tok, (dim & 63) >> 3), b0, b1, b2, b3);
-        mma_bf16_16816(sacc[0], qa[ks], b0, b1);
-        mma_bf16_16816(sacc[1], qa[ks], b2, b3);
+        E::mma16816(sacc[0], qa[ks], b0, b1);
+        E::mma16816(sacc[1], qa[ks], b2, b3);
       }
       float sv[4];
 #pragma unroll
@@ -173,11 +167,11 @@ __device__ __forceinline__ bool mma_consumer(const DecodeParams& prm, const Work
       for (int e = 0; e < 4; ++e) p[e] = ex2(sv[e] - ref);
       l += (p[0] + p[1]) + (p[2] + p[3]);
       uint32_t pa[4];
-      pa[0] = pack_bf16x2(p[0], p[1]);
+      pa[0] = E::pack2(p[0], p[1]);
       pa[1] = 0u;
-      pa[2] = pack_bf16x2(p[2], p[3]);
+      pa[2] = E::pack2(p[2], p[3]);
       pa[3] = 0u;
-      lp += (bf16lo(pa[0]) + bf16hi(pa[0])) + (bf16lo(pa[2]) + bf16hi(pa[2]));
+      lp += (E::lo(pa[0]) + E::hi(pa[0])) + (E::lo(pa[2]) + E::hi(pa[2]));
 #pragma unroll
       for (int n2 = 0; n2 < NTO / 2; ++n2) {
         const int tok = cb + (mi & 1) * 8 + rr;
@@ -185,8 +179,8 @@ __device__ __forceinline__ bool mma_consumer(const DecodeParams& prm, const Work
         uint32_t v0, v1, v2, v3;
         ldsm_x4_trans(vbase + (dim >> 6) * C::TILE * 128 + swz(tok, (dim & 63) >> 3), v0, v1, v2,
                       v3);
-        mma_bf16_16816(o[2 * n2], pa, v0, v1);
-        mma_bf16_16816(o[2 * n2 + 1], pa, v2, v3);
+        E::mma16816(o[2 * n2], pa, v0, v1);
+        E::mma16816(o[2 * n2 + 1], pa, v2, v3);
       }
     }
     fence_proxy_async_smem();   // any zeroed rows before the producer's next TMA into the stage
@@ -214,7 +208,7 @@ __device__ __forceinline__ bool mma_consumer(const DecodeParams& prm, const Work
   return aborted;
 }
 
-template <int HEAD_DIM, int GROUP>
+template <int HEAD_DIM, int GROUP, class E>
 __global__ void __launch_bounds__(DecodeCfg<HEAD_DIM, GROUP>::THREADS, 2)
 decode_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant__ CUtensorMap v_map,
               DecodeParams prm) {
@@ -322,13 +316,13 @@ decode_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant__
     const float qscale = prm.sm_scale * kLog2e;
     float q[GROUP][8];
     {
-      const __nv_bfloat16* qp = reinterpret_cast<const __nv_bfloat16*>(prm.q) +
+      const uint16_t* qp = reinterpret_cast<const uint16_t*>(prm.q) +
                                 (size_t(item.q_row) * prm.num_qo_heads + item.head * GROUP) * HEAD_DIM +
                                 ch * 8;
 #pragma unroll
       for (int h = 0; h < GROUP; ++h) {
         const uint4 u = *reinterpret_cast<const uint4*>(qp + h * HEAD_DIM);
-        unpack8(u, q[h]);
+        unpack8<E>(u, q[h]);
 #pragma unroll
         for (int j = 0; j < 8; ++j) q[h][j] *= qscale;
       }
@@ -360,7 +354,7 @@ decode_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant__
         for (int p = 0; p < C::SUB; ++p) {
           const int r = warp * C::TOK_PER_WARP + (p0 + p) * C::TPP + ts;
           float kf[8];
-          unpack8(lds128(kbase + swz(r, c8)), kf);
+          unpack8<E>(lds128(kbase + swz(r, c8)), kf);
 #pragma unroll
           for (int h = 0; h < GROUP; ++h) {
             float d0 = 0.f;
@@ -391,7 +385,7 @@ decode_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant__
           const int r = warp * C::TOK_PER_WARP + (p0 + p) * C::TPP + ts;
           if (r < ntok) {
             float vf[8];
-            unpack8(lds128(vbase + swz(r, c8)), vf);
+            unpack8<E>(lds128(vbase + swz(r, c8)), vf);
 #pragma unroll
             for (int h = 0; h < GROUP; ++h) {
               const float pr = ex2(sc[p][h] - ref[h]);
@@ -443,7 +437,7 @@ decode_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant__
       }
     }
     } else {
-      aborted = mma_consumer<HEAD_DIM, GROUP>(prm, item, n_tok, lead, n_tiles, smem_base,
+      aborted = mma_consumer<HEAD_DIM, GROUP, E>(prm, item, n_tok, lead, n_tiles, smem_base,
                                               full_bar, empty_bar, &abort_flag, red_o, red_m,
                                               red_l, red_lp);
     }
@@ -470,8 +464,8 @@ decode_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant__
         const float lse = (L > 0.f) ? (rf + lg2(L)) * kLn2 : -INFINITY;
         const int hq = item.head * GROUP + h;
         if (item.slot < 0) {
-          reinterpret_cast<__nv_bfloat16*>(prm.out)[(size_t(item.q_row) * prm.num_qo_heads + hq) *
-                                                        HEAD_DIM + dd] = __float2bfloat16_rn(o);
+          reinterpret_cast<uint16_t*>(prm.out)[(size_t(item.q_row) * prm.num_qo_heads + hq) *
+                                                   HEAD_DIM + dd] = E::one(o);
           if (dd == 0 && prm.lse) prm.lse[size_t(item.q_row) * prm.num_qo_heads + hq] = lse;
         } else {
           prm.partial_o[(size_t(item.slot) * prm.num_qo_heads + hq) * HEAD_DIM + dd] = o;
@@ -482,11 +476,11 @@ decode_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant__
   }
 }
 
-template <int HEAD_DIM, int GROUP>
+template <int HEAD_DIM, int GROUP, class E>
 cudaError_t launch_decode_t(const CUtensorMap& km, const CUtensorMap& vm, const DecodeParams& p,
                             int n_items, cudaStream_t stream) {
   using C = DecodeCfg<HEAD_DIM, GROUP>;
-  auto kern = decode_kernel<HEAD_DIM, GROUP>;
+  auto kern = decode_kernel<HEAD_DIM, GROUP, E>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        C::SMEM_BYTES);
   if (e != cudaSuccess) return e;
@@ -494,27 +488,38 @@ cudaError_t launch_decode_t(const CUtensorMap& km, const CUtensorMap& vm, const 
   return cudaGetLastError();
 }
 
-template <int HEAD_DIM>
+template <int HEAD_DIM, class E>
 cudaError_t launch_decode_d(int group, const CUtensorMap& km, const CUtensorMap& vm,
                             const DecodeParams& p, int n_items, cudaStream_t stream) {
   switch (group) {
-    case 1: return launch_decode_t<HEAD_DIM, 1>(km, vm, p, n_items, stream);
-    case 2: return launch_decode_t<HEAD_DIM, 2>(km, vm, p, n_items, stream);
-    case 4: return launch_decode_t<HEAD_DIM, 4>(km, vm, p, n_items, stream);
-    case 8: return launch_decode_t<HEAD_DIM, 8>(km, vm, p, n_items, stream);
+    case 1: return launch_decode_t<HEAD_DIM, 1, E>(km, vm, p, n_items, stream);
+    case 2: return launch_decode_t<HEAD_DIM, 2, E>(km, vm, p, n_items, stream);
+    case 4: return launch_decode_t<HEAD_DIM, 4, E>(km, vm, p, n_items, stream);
+    case 8: return launch_decode_t<HEAD_DIM, 8, E>(km, vm, p, n_items, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+template <class E>
+cudaError_t launch_decode_e(int head_dim, int group, const CUtensorMap& km, const CUtensorMap& vm,
+                            const DecodeParams& p, int n_items, cudaStream_t stream) {
+  switch (head_dim) {
+    case 64: return launch_decode_d<64, E>(group, km, vm, p, n_items, stream);
+    case 128: return launch_decode_d<128, E>(group, km, vm, p, n_items, stream);
+    case 256: return launch_decode_d<256, E>(group, km, vm, p, n_items, stream);
     default: return cudaErrorInvalidValue;
   }
 }
 
 }  // namespace
 
-cudaError_t launch_decode(int head_dim, int group, const CUtensorMap& km, const CUtensorMap& vm,
-                          const DecodeParams& p, int n_items, cudaStream_t stream) {
+cudaError_t launch_decode(int head_dim, int group, int dtype, const CUtensorMap& km,
+                          const CUtensorMap& vm, const DecodeParams& p, int n_items,
+                          cudaStream_t stream) {
   if (n_items <= 0) return cudaSuccess;
-  switch (head_dim) {
-    case 64: return launch_decode_d<64>(group, km, vm, p, n_items, stream);
-    case 128: return launch_decode_d<128>(group, km, vm, p, n_items, stream);
-    case 256: return launch_decode_d<256>(group, km, vm, p, n_items, stream);
+  switch (dtype) {
+    case FI_DTYPE_BF16: return launch_decode_e<Bf16>(head_dim, group, km, vm, p, n_items, stream);
+    case FI_DTYPE_FP16: return launch_decode_e<Fp16>(head_dim, group, km, vm, p, n_items, stream);
     default: return cudaErrorInvalidValue;
   }
 }

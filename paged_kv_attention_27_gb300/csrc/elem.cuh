@@ -1,0 +1,78 @@
+// Element types of q, K, V and out: bf16 or fp16. Both are 16-bit words;
+// the kernels move them untouched (TMA, ldmatrix, tcgen05 operands) and only
+// convert where they do arithmetic, so every kernel takes one of these two
+// traits structs as a template parameter.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <stdint.h>
+
+namespace fi {
+namespace dev {
+
+struct Bf16 {
+  static constexpr int kDtype = 0;          // FI_DTYPE_BF16
+  static constexpr uint32_t kMmaFmt = 1;    // tcgen05 kind::f16 A/B format code
+  // the two halves of a packed pair, exactly
+  __device__ static __forceinline__ float lo(uint32_t w) { return __uint_as_float(w << 16); }
+  __device__ static __forceinline__ float hi(uint32_t w) {
+    return __uint_as_float(w & 0xffff0000u);
+  }
+  // round-to-nearest-even into a packed pair / one element
+  __device__ static __forceinline__ uint32_t pack2(float l, float h) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(l, h);
+    return *reinterpret_cast<uint32_t*>(&v);
+  }
+  __device__ static __forceinline__ uint16_t one(float x) {
+    __nv_bfloat16 v = __float2bfloat16_rn(x);
+    return *reinterpret_cast<uint16_t*>(&v);
+  }
+  // D (16x8, fp32) += A (16x16) B (16x8), warp-level
+  __device__ static __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4],
+                                                  uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+        "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+  }
+};
+
+struct Fp16 {
+  static constexpr int kDtype = 1;          // FI_DTYPE_FP16
+  static constexpr uint32_t kMmaFmt = 0;
+  __device__ static __forceinline__ float lo(uint32_t w) {
+    return __half2float(__ushort_as_half(uint16_t(w & 0xffffu)));
+  }
+  __device__ static __forceinline__ float hi(uint32_t w) {
+    return __half2float(__ushort_as_half(uint16_t(w >> 16)));
+  }
+  __device__ static __forceinline__ uint32_t pack2(float l, float h) {
+    __half2 v = __floats2half2_rn(l, h);
+    return *reinterpret_cast<uint32_t*>(&v);
+  }
+  __device__ static __forceinline__ uint16_t one(float x) {
+    return __half_as_ushort(__float2half_rn(x));
+  }
+  __device__ static __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4],
+                                                  uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
+        "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+  }
+};
+
+// Eight packed elements (one 16-byte chunk) -> eight floats.
+template <class E>
+__device__ __forceinline__ void unpack8(const uint4& u, float (&f)[8]) {
+  f[0] = E::lo(u.x); f[1] = E::hi(u.x);
+  f[2] = E::lo(u.y); f[3] = E::hi(u.y);
+  f[4] = E::lo(u.z); f[5] = E::hi(u.z);
+  f[6] = E::lo(u.w); f[7] = E::hi(u.w);
+}
+
+}  // namespace dev
+}  // namespace fi

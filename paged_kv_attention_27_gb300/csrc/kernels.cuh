@@ -35,8 +35,9 @@ struct MergeParams {
   int32_t S;
   int32_t H;
   int32_t d;
-  void* out;               // bf16 [row][H][d]
+  void* out;               // [row][H][d], bf16 or fp16
   float* lse;              // [row][H] or null
+  int32_t dtype;           // fi_dtype of out
 };
 
 struct PrefillParams {
@@ -60,11 +61,13 @@ struct PrefillParams {
   int32_t fault_kind;   // test hook: 1 = CTA 0's K producer skips its first tile
 };
 
-cudaError_t launch_prefill(int head_dim, const CUtensorMap& qm, const CUtensorMap& km,
+cudaError_t launch_prefill(int head_dim, int dtype, const CUtensorMap& qm, const CUtensorMap& km,
                            const CUtensorMap& vm, const PrefillParams& p, int n_items,
                            cudaStream_t stream);
-cudaError_t launch_decode(int head_dim, int group, const CUtensorMap& km, const CUtensorMap& vm,
-                          const DecodeParams& p, int n_items, cudaStream_t stream);
+// `dtype` (fi_dtype) selects the element type of q, K, V and out.
+cudaError_t launch_decode(int head_dim, int group, int dtype, const CUtensorMap& km,
+                          const CUtensorMap& vm, const DecodeParams& p, int n_items,
+                          cudaStream_t stream);
 cudaError_t launch_merge(const MergeParams& p, int n_rows, cudaStream_t stream);
 
 }  // namespace fi

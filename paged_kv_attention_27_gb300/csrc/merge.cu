@@ -3,8 +3,7 @@
 // w_i = exp(lse_i - M): o = sum_i w_i o_i / sum_i w_i, lse = M + ln sum_i w_i.
 // The split order is fixed (i = 0, 1, ...), so results are deterministic.
 // Used both as the ABI call fi_merge_states and after split-KV decode.
-#include <cuda_bf16.h>
-
+#include "elem.cuh"
 #include "kernels.cuh"
 #include "ptx.cuh"
 
@@ -18,6 +17,7 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr int kMergeThreads = 128;
 
+template <class E>
 __global__ void __launch_bounds__(kMergeThreads) merge_kernel(MergeParams p) {
   const int r = blockIdx.x;
   int out_row = r, base = r * p.S, n = p.S;
@@ -48,12 +48,10 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(MergeParams p) {
       }
     }
     const float inv = sw > 0.f ? 1.f / sw : 0.f;
-    __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
-    __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z * inv, acc.w * inv);
     uint2 packed;
-    packed.x = *reinterpret_cast<uint32_t*>(&lo);
-    packed.y = *reinterpret_cast<uint32_t*>(&hi);
-    reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(p.out) +
+    packed.x = E::pack2(acc.x * inv, acc.y * inv);
+    packed.y = E::pack2(acc.z * inv, acc.w * inv);
+    reinterpret_cast<uint2*>(reinterpret_cast<uint16_t*>(p.out) +
                              (size_t(out_row) * p.H + h) * p.d)[c] = packed;
     if (c == 0 && p.lse)
       p.lse[size_t(out_row) * p.H + h] = sw > 0.f ? M + lg2(sw) * kLn2 : -INFINITY;
@@ -64,7 +62,11 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(MergeParams p) {
 
 cudaError_t launch_merge(const MergeParams& p, int n_rows, cudaStream_t stream) {
   if (n_rows <= 0 || p.H <= 0) return cudaSuccess;
-  merge_kernel<<<n_rows, kMergeThreads, 0, stream>>>(p);
+  switch (p.dtype) {
+    case FI_DTYPE_BF16: merge_kernel<Bf16><<<n_rows, kMergeThreads, 0, stream>>>(p); break;
+    case FI_DTYPE_FP16: merge_kernel<Fp16><<<n_rows, kMergeThreads, 0, stream>>>(p); break;
+    default: return cudaErrorInvalidValue;
+  }
   return cudaGetLastError();
 }
 

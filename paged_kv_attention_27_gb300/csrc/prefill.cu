@@ -21,17 +21,17 @@
 //   * warps 0-3 (softmax, thread = query row = TMEM lane): copy their Q row
 //     into TMEM once, then per tile read the S row with tcgen05.ld, apply the
 //     causal mask, keep the running max and sums (online softmax, the
-//     section-1 FA-1/2 idea), write P as packed bf16 into TMEM for the PV
-//     MMA, and rescale the O row in
+//     section-1 FA-1/2 idea), write P as packed 16-bit pairs (the inputs'
+//     type, bf16 or fp16) into TMEM for the PV MMA, and rescale the O row in
 //     TMEM only when the running max grew by more than 2^8 (the rescale guard
 //     the same page's section 4 says must stay on; skipping smaller growths
 //     is exact because O and the row sums share the stale reference);
-//   * the same warps finish with O / l, write bf16 out and the fp32 lse.
+//   * the same warps finish with O / l, write out (inputs' type) and the
+//     fp32 lse.
 // Fully masked KV tiles are never visited: the planner clips tok_end.
 #include <climits>
 
-#include <cuda_bf16.h>
-
+#include "elem.cuh"
 #include "fi_internal.h"
 #include "kernels.cuh"
 #include "ptx.cuh"
@@ -46,7 +46,7 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;   // log2 units: rescale when the max grows by > 2^8
 
-template <int HEAD_DIM>
+template <int HEAD_DIM, class E>
 struct PrefillCfg {
   static constexpr int M = kPrefillTileM;                   // 128 query rows
   static constexpr int N = HEAD_DIM <= 128 ? 128 : 64;      // KV tokens per tile
@@ -63,15 +63,16 @@ struct PrefillCfg {
   // keep one CTA per SM (each CTA takes all 512 TMEM columns)
   static constexpr int SMEM_BYTES = (USED < 120 * 1024 ? 120 * 1024 : USED) + 1024;
   static constexpr uint32_t TMEM_COLS = 512;
-  // TMEM columns: two S buffers, O, then (packed bf16 pairs) Q and P
+  // TMEM columns: two S buffers, O, then (packed 16-bit pairs) Q and P
   static constexpr uint32_t COL_S = 0;                      // [0,N), [N,2N)
   static constexpr uint32_t COL_O = 2 * N;                  // [2N, 2N+HEAD_DIM)
   static constexpr uint32_t COL_Q = COL_O + HEAD_DIM;       // HEAD_DIM/2 columns if Q_TMEM
   static constexpr uint32_t COL_P = COL_Q + (Q_TMEM ? HEAD_DIM / 2 : 0);  // N/2 columns
   static_assert(COL_P + N / 2 <= TMEM_COLS, "TMEM budget");
   static_assert(SMEM_BYTES <= 227 * 1024, "shared-memory budget");
-  static constexpr uint32_t IDESC_QK = idesc_bf16(M, N, 0, 0);          // K-major Q and K
-  static constexpr uint32_t IDESC_PV = idesc_bf16(M, HEAD_DIM, 0, 1);   // K-major P, MN-major V
+  // K-major Q and K; K-major P with MN-major V; A and B of the element type
+  static constexpr uint32_t IDESC_QK = idesc_f16kind(M, N, 0, 0, E::kMmaFmt);
+  static constexpr uint32_t IDESC_PV = idesc_f16kind(M, HEAD_DIM, 0, 1, E::kMmaFmt);
 };
 
 template <int NST>
@@ -88,10 +89,6 @@ __device__ __forceinline__ uint32_t swz(int r, int c8) {
   return uint32_t(r * 128 + ((c8 ^ (r & 7)) << 4));
 }
 
-__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
-  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
-  return *reinterpret_cast<uint32_t*>(&v);
-}
 
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
                                              uint32_t d) {
@@ -100,11 +97,11 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
                : "memory");
 }
 
-template <int HEAD_DIM>
-__global__ void __launch_bounds__(PrefillCfg<HEAD_DIM>::THREADS, 1)
+template <int HEAD_DIM, class E>
+__global__ void __launch_bounds__(PrefillCfg<HEAD_DIM, E>::THREADS, 1)
 prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant__ CUtensorMap k_map,
                const __grid_constant__ CUtensorMap v_map, PrefillParams prm) {
-  using C = PrefillCfg<HEAD_DIM>;
+  using C = PrefillCfg<HEAD_DIM, E>;
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) PrefillBarriers<C::NST> bars;
   __shared__ uint32_t tmem_base_sh;
@@ -299,13 +296,13 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
     // first visible key (left window); below 0 means no lower bound
     const int t_min = prm.window_left >= 0 ? pos - prm.window_left : INT_MIN;
     const float scale = prm.sm_scale * kLog2e;
-    // l: sum of the exact weights (gives lse); lp: sum of the bf16-rounded
+    // l: sum of the exact weights (gives lse); lp: sum of the rounded
     // weights the PV MMA multiplies (normalises O)
     float m = -INFINITY, l = 0.f, lp = 0.f;
     bool ok = true;
 
     if constexpr (C::Q_TMEM) {
-      // this thread's Q row, from the swizzled TMA tile into TMEM (bf16 pairs)
+      // this thread's Q row, from the swizzled TMA tile into TMEM (16-bit pairs)
       ok = mbar_wait_warp(smem_u32(&bars.q_full), 0, limit, &abort_flag);
       if (ok) {
 #pragma unroll
@@ -434,7 +431,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
                                c8 * 16, 0u, 0u, 0u, 0u);
         }
       }
-      // P row t as packed bf16 pairs into TMEM (the A operand of the PV
+      // P row t as packed 16-bit pairs into TMEM (the A operand of the PV
       // MMA). lp adds the same rounded values the tensor core multiplies, so
       // that the final division normalises exactly the weights applied.
       // In tiles on the causal diagonal a row may have only a few visible
@@ -445,10 +442,10 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
       for (int kb = 0; kb < C::N / 64; ++kb) {
         uint32_t w[32];
 #pragma unroll
-        for (int e = 0; e < 32; ++e) w[e] = pack_bf16x2(s[kb * 64 + 2 * e], s[kb * 64 + 2 * e + 1]);
+        for (int e = 0; e < 32; ++e) w[e] = E::pack2(s[kb * 64 + 2 * e], s[kb * 64 + 2 * e + 1]);
         if (need_mask) {
 #pragma unroll
-          for (int e = 0; e < 32; ++e) rsp4[e & 3] += bf16lo(w[e]) + bf16hi(w[e]);
+          for (int e = 0; e < 32; ++e) rsp4[e & 3] += E::lo(w[e]) + E::hi(w[e]);
         }
         tmem_st32(tmem + lane_off + C::COL_P + kb * 32, w);
       }
@@ -471,7 +468,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
       const bool row_ok = t < rows;
       const float inv = lp > 0.f ? 1.f / lp : 0.f;
       const size_t out_row = size_t(item.q_row) + t;
-      __nv_bfloat16* op = reinterpret_cast<__nv_bfloat16*>(prm.out) +
+      uint16_t* op = reinterpret_cast<uint16_t*>(prm.out) +
                           (out_row * prm.num_qo_heads + head) * HEAD_DIM;
 #pragma unroll 1
       for (int c = 0; c < HEAD_DIM / 32; ++c) {
@@ -488,10 +485,10 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
 #pragma unroll
           for (int q4 = 0; q4 < 4; ++q4) {
             const float* f = reinterpret_cast<const float*>(r) + q4 * 8;
-            dst[q4] = make_uint4(pack_bf16x2(f[0] * inv, f[1] * inv),
-                                 pack_bf16x2(f[2] * inv, f[3] * inv),
-                                 pack_bf16x2(f[4] * inv, f[5] * inv),
-                                 pack_bf16x2(f[6] * inv, f[7] * inv));
+            dst[q4] = make_uint4(E::pack2(f[0] * inv, f[1] * inv),
+                                 E::pack2(f[2] * inv, f[3] * inv),
+                                 E::pack2(f[4] * inv, f[5] * inv),
+                                 E::pack2(f[6] * inv, f[7] * inv));
           }
         }
       }
@@ -520,11 +517,11 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
   }
 }
 
-template <int HEAD_DIM>
+template <int HEAD_DIM, class E>
 cudaError_t launch_prefill_t(const CUtensorMap& qm, const CUtensorMap& km, const CUtensorMap& vm,
                              const PrefillParams& p, int n_items, cudaStream_t stream) {
-  using C = PrefillCfg<HEAD_DIM>;
-  auto kern = prefill_kernel<HEAD_DIM>;
+  using C = PrefillCfg<HEAD_DIM, E>;
+  auto kern = prefill_kernel<HEAD_DIM, E>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        C::SMEM_BYTES);
   if (e != cudaSuccess) return e;
@@ -532,16 +529,27 @@ cudaError_t launch_prefill_t(const CUtensorMap& qm, const CUtensorMap& km, const
   return cudaGetLastError();
 }
 
+template <class E>
+cudaError_t launch_prefill_e(int head_dim, const CUtensorMap& qm, const CUtensorMap& km,
+                             const CUtensorMap& vm, const PrefillParams& p, int n_items,
+                             cudaStream_t stream) {
+  switch (head_dim) {
+    case 64: return launch_prefill_t<64, E>(qm, km, vm, p, n_items, stream);
+    case 128: return launch_prefill_t<128, E>(qm, km, vm, p, n_items, stream);
+    case 256: return launch_prefill_t<256, E>(qm, km, vm, p, n_items, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
 }  // namespace
 
-cudaError_t launch_prefill(int head_dim, const CUtensorMap& qm, const CUtensorMap& km,
+cudaError_t launch_prefill(int head_dim, int dtype, const CUtensorMap& qm, const CUtensorMap& km,
                            const CUtensorMap& vm, const PrefillParams& p, int n_items,
                            cudaStream_t stream) {
   if (n_items <= 0) return cudaSuccess;
-  switch (head_dim) {
-    case 64: return launch_prefill_t<64>(qm, km, vm, p, n_items, stream);
-    case 128: return launch_prefill_t<128>(qm, km, vm, p, n_items, stream);
-    case 256: return launch_prefill_t<256>(qm, km, vm, p, n_items, stream);
+  switch (dtype) {
+    case FI_DTYPE_BF16: return launch_prefill_e<Bf16>(head_dim, qm, km, vm, p, n_items, stream);
+    case FI_DTYPE_FP16: return launch_prefill_e<Fp16>(head_dim, qm, km, vm, p, n_items, stream);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -1,10 +1,9 @@
 // Inline-PTX helpers for sm_103a: mbarriers with bounded waits, TMA tensor
-// loads, proxy fences, bf16 unpacking and the fast exp2/log2 instructions.
+// loads, proxy fences, ldmatrix, tcgen05 and the fast exp2/log2 instructions.
 #pragma once
 
 #include <cstdint>
 #include <cuda.h>
-#include <cuda_bf16.h>
 
 namespace fi {
 namespace dev {
@@ -142,17 +141,6 @@ __device__ __forceinline__ float lg2(float x) {
   return y;
 }
 
-// Two bf16 packed in a 32-bit word -> two floats (exact).
-__device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
-__device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
-
-__device__ __forceinline__ void unpack8(const uint4& u, float (&f)[8]) {
-  f[0] = bf16lo(u.x); f[1] = bf16hi(u.x);
-  f[2] = bf16lo(u.y); f[3] = bf16hi(u.y);
-  f[4] = bf16lo(u.z); f[5] = bf16hi(u.z);
-  f[6] = bf16lo(u.w); f[7] = bf16hi(u.w);
-}
-
 __device__ __forceinline__ uint4 lds128(uint32_t addr) {
   uint4 v;
   asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
@@ -161,16 +149,7 @@ __device__ __forceinline__ uint4 lds128(uint32_t addr) {
   return v;
 }
 
-// ---- warp-level bf16 MMA (m16n8k16) and matrix loads from shared memory ---
-__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
-                                               uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
-      "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-
+// ---- matrix loads from shared memory for warp-level MMA -----------------
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
                                         uint32_t& r3) {
   asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
@@ -211,7 +190,7 @@ __device__ __forceinline__ void tc_fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
-// D[tmem] (+)= A[smem] * B[smem], kind::f16 (bf16 inputs, fp32 accumulate).
+// D[tmem] (+)= A[smem] * B[smem], kind::f16 (16-bit inputs, fp32 accumulate).
 __device__ __forceinline__ void tc_mma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
                                           uint32_t idesc, uint32_t accumulate) {
   asm volatile(
@@ -272,7 +251,7 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t* r) {
 }
 
 // D[tmem] (+)= A[tmem] * B[smem], kind::f16: A read from tensor memory
-// (rows in lanes, two bf16 per 32-bit column along K).
+// (rows in lanes, two 16-bit elements per 32-bit column along K).
 __device__ __forceinline__ void tc_mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
                                           uint32_t idesc, uint32_t accumulate) {
   asm volatile(
@@ -291,7 +270,7 @@ __device__ __forceinline__ void tmem_wait_st() {
 }
 
 // Shared-memory matrix descriptor for tcgen05.mma, 128-byte swizzle.
-// K-major operand: rows of 128 B (64 bf16 along K), 8-row atoms `sbo` = 1024 B
+// K-major operand: rows of 128 B (64 elements along K), 8-row atoms `sbo` = 1024 B
 // apart; the leading byte offset is unused for this layout.
 // MN-major operand: 128 B along MN per row of K; 8-row atoms along K are
 // `sbo` apart and 64-element atoms along MN are `lbo` apart.
@@ -305,12 +284,14 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t smem_addr, uint32_t lbo
   return d;
 }
 
-// Instruction descriptor, kind::f16: bf16 A and B, fp32 accumulator, M x N.
-// a_mn / b_mn select MN-major (transposed) operands.
-__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, int a_mn, int b_mn) {
+// Instruction descriptor, kind::f16: A and B of one 16-bit type (`fmt`: 0 =
+// fp16, 1 = bf16), fp32 accumulator, M x N. a_mn / b_mn select MN-major
+// (transposed) operands.
+__host__ __device__ constexpr uint32_t idesc_f16kind(int M, int N, int a_mn, int b_mn,
+                                                     uint32_t fmt) {
   return (1u << 4)                       // D format: f32
-         | (1u << 7)                     // A format: bf16
-         | (1u << 10)                    // B format: bf16
+         | (fmt << 7)                    // A format
+         | (fmt << 10)                   // B format
          | (uint32_t(a_mn) << 15) | (uint32_t(b_mn) << 16)
          | (uint32_t(N >> 3) << 17)      // N / 8
          | (uint32_t(M >> 4) << 24);     // M / 16

@@ -1,8 +1,9 @@
 """Moving a synthetic PagedBatch to the GPU and calling the C ABI on it.
 
-Marshalling only: numpy bf16 bit patterns become torch bf16 tensors on the
-device, outputs and the workspace are allocated with torch, and the calls go
-through ``binding`` (libfi.so). No attention arithmetic happens here.
+Marshalling only: numpy bf16 / fp16 bit patterns become torch bfloat16 /
+float16 tensors on the device, outputs and the workspace are allocated with
+torch, and the calls go through ``binding`` (libfi.so). No attention
+arithmetic happens here.
 """
 from __future__ import annotations
 
@@ -13,9 +14,14 @@ from . import binding as B
 from .synth import PagedBatch
 
 
-def bf16_tensor(bits: np.ndarray, device="cuda") -> torch.Tensor:
-    """uint16 bf16 bit patterns -> torch.bfloat16 tensor on `device`."""
-    t = torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16)
+TORCH_DTYPES = {"bf16": torch.bfloat16, "fp16": torch.float16}
+FI_DTYPES = {"bf16": B.FI_DTYPE_BF16, "fp16": B.FI_DTYPE_FP16}
+
+
+def bf16_tensor(bits: np.ndarray, device="cuda", dtype: str = "bf16") -> torch.Tensor:
+    """uint16 bit patterns of `dtype` (bf16 by default, or fp16) -> a torch
+    tensor of that type on `device`."""
+    t = torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(TORCH_DTYPES[dtype])
     return t.to(device)
 
 
@@ -25,7 +31,9 @@ def i32_tensor(a: np.ndarray, device="cuda") -> torch.Tensor:
 
 def plan_options(b: PagedBatch):
     """fi_plan options of a batch (None = the defaults)."""
-    return {"window_left": int(b.window_left)} if b.window_left >= 0 else None
+    if b.window_left < 0 and b.dtype == "bf16":
+        return None
+    return {"window_left": int(b.window_left), "dtype": FI_DTYPES[b.dtype]}
 
 
 def num_sms(device="cuda") -> int:
@@ -38,9 +46,9 @@ class DeviceBatch:
     def __init__(self, b: PagedBatch, device="cuda", mode=None, sms=None, lse=True):
         self.b = b
         self.device = device
-        self.q = bf16_tensor(b.q, device)
-        self.k = bf16_tensor(b.k_cache, device)
-        self.v = bf16_tensor(b.v_cache, device)
+        self.q = bf16_tensor(b.q, device, b.dtype)
+        self.k = bf16_tensor(b.k_cache, device, b.dtype)
+        self.v = bf16_tensor(b.v_cache, device, b.dtype)
         self.page_indptr = i32_tensor(b.page_indptr, device)
         self.page_indices = i32_tensor(b.page_indices if b.page_indices.size else np.zeros(1),
                                        device)
@@ -56,7 +64,7 @@ class DeviceBatch:
         self.workspace = torch.empty(max(self.plan.workspace_bytes, 256), dtype=torch.uint8,
                                      device=device)
         rows = int(b.qo_lens.sum())
-        self.out = torch.empty((rows, b.num_qo_heads, b.head_dim), dtype=torch.bfloat16,
+        self.out = torch.empty((rows, b.num_qo_heads, b.head_dim), dtype=TORCH_DTYPES[b.dtype],
                                device=device)
         self.lse = torch.empty((rows, b.num_qo_heads), dtype=torch.float32,
                                device=device) if lse else None

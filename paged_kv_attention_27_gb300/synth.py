@@ -224,12 +224,15 @@ def tiny_decode(seed: int = 0) -> PagedBatch:
                       [1, 17, 64, 100], [1, 1, 1, 1], 8, 2, 64, 16, NHD, 1.0 / 8, False, seed)
 
 
-def llama7b_decode(seed: int = 1, batch: int = 64) -> PagedBatch:
+def llama7b_decode(seed: int = 1, batch: int = 64, dtype: str = "bf16") -> PagedBatch:
     """Llama-7B-shaped decode: 32/32 heads, d=128, P=16, KV ~ U[512,4096], NHD."""
     g = philox(seed + 1000)
     kv = g.integers(512, 4097, size=batch)
-    return make_batch(f"Llama-7B-shaped batch decode B{batch} Hq32 Hkv32 d128 P16 kv~U[512,4096] NHD",
-                      kv, np.ones(batch, np.int64), 32, 32, 128, 16, NHD, None, False, seed)
+    tname = "" if dtype == "bf16" else f" {dtype}"
+    return make_batch(f"Llama-7B-shaped batch decode B{batch} Hq32 Hkv32 d128 P16 kv~U[512,4096] "
+                      f"NHD{tname}",
+                      kv, np.ones(batch, np.int64), 32, 32, 128, 16, NHD, None, False, seed,
+                      dtype=dtype)
 
 
 def lognormal_lengths(gen, n, median=2048, sigma=1.0, lo=1, hi=32768):
@@ -255,14 +258,15 @@ def llama70b_gqa_decode(seed: int = 2, batch: int = 128, shared: int = 32,
 
 
 def causal_prefill(seq_len: int, batch: int = 8, seed: int = 3,
-                   window_left: int = -1) -> PagedBatch:
+                   window_left: int = -1, dtype: str = "bf16") -> PagedBatch:
     """Causal prefill, 70B shape: 64/8 heads, d=128, P=16, qo_len = kv_len =
     seq_len; optionally a left window of ``window_left`` keys."""
     L = np.full(batch, seq_len, np.int64)
     wname = f" window {window_left + 1}" if window_left >= 0 else ""
-    return make_batch(f"causal prefill B{batch} L{seq_len} Hq64 Hkv8 d128 P16 NHD{wname}",
+    tname = "" if dtype == "bf16" else f" {dtype}"
+    return make_batch(f"causal prefill B{batch} L{seq_len} Hq64 Hkv8 d128 P16 NHD{wname}{tname}",
                       L, L, 64, 8, 128, 16, NHD, None, True, seed + seq_len,
-                      window_left=window_left)
+                      window_left=window_left, dtype=dtype)
 
 
 def ragged_prefill(seed: int = 4, batch: int = 16) -> PagedBatch:

@@ -292,5 +292,8 @@ def test_workspace_too_small_and_bad_args_return_before_any_launch():
         B.fi_batch_decode_paged(*args, stream=0)
     assert e.value.status == B.FI_ERR_NO_DEVICE
     with pytest.raises(B.FiError) as e:
-        B.fi_merge_states(fake, fake, 2, 3, 4, 6, fake, None, stream=0)   # d % 4 != 0
+        B.fi_merge_states(fake, fake, 2, 3, 4, 6, B.FI_DTYPE_BF16, fake, None, stream=0)  # d % 4
+    assert e.value.status == B.FI_ERR_INVALID_ARG
+    with pytest.raises(B.FiError) as e:
+        B.fi_merge_states(fake, fake, 2, 3, 4, 8, 5, fake, None, stream=0)   # unknown dtype
     assert e.value.status == B.FI_ERR_INVALID_ARG

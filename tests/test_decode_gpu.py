@@ -32,7 +32,7 @@ def _oracle(b, requests=None):
     return oracle.batch_attention(b.q, b.qo_indptr, b.k_cache, b.v_cache, b.layout, b.page_indptr,
                                   b.page_indices, b.last_page_len, b.num_qo_heads, b.num_kv_heads,
                                   b.page_size, b.sm_scale, b.causal, requests=requests,
-                                  window_left=b.window_left)
+                                  window_left=b.window_left, dtype=b.dtype)
 
 
 def _rows(b, requests):
@@ -152,7 +152,7 @@ def test_merge_states_abi(n, S, H, d):
     st = torch.from_numpy(s).cuda()
     out = torch.empty((n, H, d), dtype=torch.bfloat16, device="cuda")
     lse = torch.empty((n, H), dtype=torch.float32, device="cuda")
-    B.fi_merge_states(vt, st, n, S, H, d, out, lse)
+    B.fi_merge_states(vt, st, n, S, H, d, B.FI_DTYPE_BF16, out, lse)
     torch.cuda.synchronize()
     compare(out, lse, ref_o, ref_l, what="merge_states")
 
@@ -199,3 +199,30 @@ def test_sliding_window_decode(g, d, w):
                          synth.NHD if g % 2 else synth.HND, None, False, 200 + w + g,
                          window_left=w)
     check(scale_v(b), sms=8)
+
+
+@pytest.mark.parametrize("g,d", [(1, 128), (8, 128), (2, 256), (4, 64), (1, 64), (8, 256)])
+def test_fp16_decode(g, d):
+    """fp16 q/K/V/out through the same kernels (fp16 MMAs and conversions)."""
+    hkv = 2
+    kv = [1, 16, 17, 300, 2049, 9000]
+    b = synth.make_batch(f"fp16 g{g} d{d}", kv, [1] * len(kv), g * hkv, hkv, d, 16,
+                         synth.NHD if g % 2 else synth.HND, None, False, 500 + g + d,
+                         dtype="fp16", tail_fill="nan")
+    (_, _), db = check(b, sms=8)
+    assert db.out.dtype == torch.float16
+
+
+def test_fp16_merge_states_abi():
+    rng = np.random.default_rng(5)
+    n, S, H, d = 4, 3, 4, 128
+    v = (0.25 * rng.normal(size=(n, S, H, d))).astype(np.float32)
+    s = (rng.normal(size=(n, S, H)) * 4).astype(np.float32)
+    ref_o, ref_l = oracle.merge_states(np.moveaxis(v.astype(np.float64), 1, 0),
+                                       np.moveaxis(s.astype(np.float64), 1, 0))
+    out = torch.empty((n, H, d), dtype=torch.float16, device="cuda")
+    lse = torch.empty((n, H), dtype=torch.float32, device="cuda")
+    B.fi_merge_states(torch.from_numpy(v).cuda(), torch.from_numpy(s).cuda(), n, S, H, d,
+                      B.FI_DTYPE_FP16, out, lse)
+    torch.cuda.synchronize()
+    compare(out, lse, ref_o, ref_l, what="merge_states fp16")

@@ -38,7 +38,7 @@ def _oracle(b, rows=None, requests=None):
     return oracle.batch_attention(b.q, b.qo_indptr, b.k_cache, b.v_cache, b.layout, b.page_indptr,
                                   b.page_indices, b.last_page_len, b.num_qo_heads, b.num_kv_heads,
                                   b.page_size, b.sm_scale, b.causal, requests=requests, rows=rows,
-                                  window_left=b.window_left)
+                                  window_left=b.window_left, dtype=b.dtype)
 
 
 def check_full(b, what=None):
@@ -225,3 +225,28 @@ def test_bounded_wait_times_out_and_context_survives(case):
 
 def test_sliding_window_prefill_16k_full_size():
     check_sampled(synth.causal_prefill(16384, window_left=4095), per_request=16)
+
+
+# ---- fp16 inputs -----------------------------------------------------------
+
+@pytest.mark.parametrize("d,P", [(64, 16), (128, 16), (256, 32)])
+def test_fp16_causal_prefill(d, P):
+    kv = [1, 2, 17, 128, 129, 300, 513]
+    b = synth.make_batch(f"fp16 prefill d{d}", kv, kv, 8, 2, d, P, synth.HND, None, True,
+                         600 + d, dtype="fp16", tail_fill="nan")
+    db = check_full(b)
+    assert db.out.dtype == torch.float16
+
+
+def test_fp16_mixed_batch_with_window():
+    b = synth.small_mixed()
+    b = synth.make_batch("fp16 mixed window", b.kv_lens, b.qo_lens, 16, 8, 256, 32, synth.NHD,
+                         None, True, 601, dtype="fp16", window_left=200)
+    check_full(b)
+
+
+def test_fp16_prefill_4k_full_size():
+    b = synth.causal_prefill(4096, batch=2)
+    b = synth.make_batch("fp16 causal prefill B2 L4096", b.kv_lens, b.qo_lens, 64, 8, 128, 16,
+                         synth.NHD, None, True, 602, dtype="fp16")
+    check_sampled(b, per_request=16)
