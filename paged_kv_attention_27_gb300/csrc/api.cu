@@ -244,8 +244,9 @@ fi_status run_paged(fi_plan_t plan, bool prefill_call, const void* q, const int3
     pp.err = err;
     pp.wait_limit_ns = g_wait_limit_ns;
     pp.fault_kind = fault_kind;
-    e = fi::launch_prefill(P.head_dim, P.dtype, qmap, kmap, vmap, pp,
-                           int(P.prefill_items.size()), stream);
+    pp.n_items = int(P.prefill_items.size());
+    pp.work_counter = reinterpret_cast<uint32_t*>(ws + fi::kWorkCounterOffset);
+    e = fi::launch_prefill(P.head_dim, P.dtype, qmap, kmap, vmap, pp, P.num_sms, stream);
     if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
   }
   if (!P.decode_items.empty()) {

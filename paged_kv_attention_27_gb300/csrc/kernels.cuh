@@ -41,7 +41,9 @@ struct MergeParams {
 };
 
 struct PrefillParams {
-  const WorkItem* items;
+  const WorkItem* items;    // longest first
+  int32_t n_items;
+  uint32_t* work_counter;   // zero before the launch: items past the first wave taken so far
   const int32_t* qo_indptr;
   const int32_t* page_indptr;
   const int32_t* last_page_len;
@@ -61,8 +63,10 @@ struct PrefillParams {
   int32_t fault_kind;   // test hook: 1 = CTA 0's K producer skips its first tile
 };
 
+// Persistent launch: min(grid, p.n_items) CTAs, one per SM; CTA c starts
+// with item c and takes the next ones from p.work_counter.
 cudaError_t launch_prefill(int head_dim, int dtype, const CUtensorMap& qm, const CUtensorMap& km,
-                           const CUtensorMap& vm, const PrefillParams& p, int n_items,
+                           const CUtensorMap& vm, const PrefillParams& p, int grid,
                            cudaStream_t stream);
 // `dtype` (fi_dtype) selects the element type of q, K, V and out.
 cudaError_t launch_decode(int head_dim, int group, int dtype, const CUtensorMap& km,

@@ -1,16 +1,21 @@
 // Causal variable-length batch prefill over a paged KV cache, on the
 // 5th-generation tensor cores (tcgen05.mma, accumulators in tensor memory).
 //
-// One CTA per planned work item: 128 query rows of one request and one query
-// head, against keys [0, tok_end) of that request (tok_end already clipped to
-// the causal bound of the tile's last row). Warp-specialised, as the
-// FlashAttention-3 page describes for Hopper (section 1: TMA producer warps,
-// consumer warps driving the tensor cores, hardware barriers between them,
-// ping-pong buffers), rebuilt for sm_103a:
-//   * warps 4 and 6 (producers): TMA loads of the Q tile (once) and, per KV
+// A work item is 128 query rows of one request and one query head, against
+// keys [tok_begin, tok_end) of that request (tok_end clipped to the causal
+// bound of the tile's last row, tok_begin to the left window of its first).
+// The launch is persistent: one CTA per SM works through items in the
+// planner's longest-first order, taking the next one from a global counter
+// when it starts loading the current one, so that one item's epilogue and
+// the next item's first loads and scores overlap, and the per-CTA setup
+// (barriers, TMEM allocation, pipeline fill) is paid once per SM.
+// Warp-specialised, as the FlashAttention-3 page describes for Hopper
+// (section 1: TMA producer warps, consumer warps driving the tensor cores,
+// hardware barriers between them, ping-pong buffers), rebuilt for sm_103a:
+//   * warps 4 and 6 (producers): TMA loads of each item's Q tile and, per KV
 //     tile of N tokens, one 128B-swizzled box per (page, 64-dim slice) of K
 //     (warp 4) and of V (warp 6) into K and V rings (three deep for
-//     head_dim <= 128);
+//     head_dim <= 128) that run on across items;
 //   * warp 5 (MMA issuer; also owns the TMEM allocation): one thread issues
 //     S_j = Q K_j^T into a double-buffered S region of TMEM, then
 //     O += P_{j-1} V_{j-1} into an O region of TMEM, so that the tensor core
@@ -19,7 +24,7 @@
 //     in shared memory an M=128, N=128 MMA alone would use all of the shared
 //     memory bandwidth, which the K/V copies also need;
 //   * warps 0-3 (softmax, thread = query row = TMEM lane): copy their Q row
-//     into TMEM once, then per tile read the S row with tcgen05.ld, apply the
+//     into TMEM per item, then per tile read the S row with tcgen05.ld, apply the
 //     causal mask, keep the running max and sums (online softmax, the
 //     section-1 FA-1/2 idea), write P as packed 16-bit pairs (the inputs'
 //     type, bf16 or fp16) into TMEM for the PV MMA, and rescale the O row in
@@ -75,9 +80,12 @@ struct PrefillCfg {
   static constexpr uint32_t IDESC_PV = idesc_f16kind(M, HEAD_DIM, 0, 1, E::kMmaFmt);
 };
 
+constexpr int kItemRing = 8;   // item indices handed from the K producer to the other roles
+
 template <int NST>
 struct PrefillBarriers {
-  uint64_t q_full, q_tmem;
+  uint64_t item_full[kItemRing], item_empty[kItemRing];
+  uint64_t q_full, q_tmem, q_empty;
   uint64_t k_full[NST], k_empty[NST];
   uint64_t v_full[NST], v_empty[NST];
   uint64_t s_full[2], s_free[2];
@@ -97,6 +105,12 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
                : "memory");
 }
 
+// Number of KV tiles of an item: keys [tok_begin, tok_end), N per tile.
+template <int N>
+__device__ __forceinline__ int item_tiles(const WorkItem& w) {
+  return (w.tok_end - w.tok_begin + N - 1) / N;
+}
+
 template <int HEAD_DIM, class E>
 __global__ void __launch_bounds__(PrefillCfg<HEAD_DIM, E>::THREADS, 1)
 prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant__ CUtensorMap k_map,
@@ -106,19 +120,39 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
   __shared__ __align__(8) PrefillBarriers<C::NST> bars;
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_flag;
+  __shared__ int item_ring[kItemRing];
 
   const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const WorkItem item = prm.items[blockIdx.x];
-  const int req = item.req, head = item.head, kv_head = head / prm.group;
-  // key tiles start at the item's first key (page-aligned; 0 without a window)
-  const int n_tiles = (item.tok_end - item.tok_begin + C::N - 1) / C::N;
+  const int n_items = prm.n_items;
   const uint64_t limit = prm.wait_limit_ns;
+  // Items are handed out in the planner's longest-first order as CTAs get
+  // free: a CTA's first item is blockIdx.x, later ones come from a global
+  // counter, so the items in flight across the GPU stay neighbours in the
+  // list (they share K/V through the L2) and the load stays balanced. The K
+  // producer takes the indices and publishes them, one item ahead, in a
+  // small shared-memory ring that the other roles read in order; all
+  // barrier phases count this CTA's items (n) or KV tiles (g).
+  auto item_at = [&](int n, int& idx) {   // consumer side, one thread per role-warp
+    if (!mbar_wait_bounded(smem_u32(&bars.item_full[n % kItemRing]), (n / kItemRing) & 1,
+                           limit, &abort_flag))
+      return false;
+    idx = *reinterpret_cast<volatile int*>(&item_ring[n % kItemRing]);
+    return true;
+  };
+  auto item_done = [&](int n) {
+    mbar_arrive(smem_u32(&bars.item_empty[n % kItemRing]));
+  };
 
   if (threadIdx.x == 0) {
+    for (int s = 0; s < kItemRing; ++s) {
+      mbar_init(smem_u32(&bars.item_full[s]), 1);
+      mbar_init(smem_u32(&bars.item_empty[s]), 6);   // V producer, MMA issuer, 4 softmax warps
+    }
     mbar_init(smem_u32(&bars.q_full), 1);
     mbar_init(smem_u32(&bars.q_tmem), 4);
+    mbar_init(smem_u32(&bars.q_empty), 1);
     for (int s = 0; s < C::NST; ++s) {
       mbar_init(smem_u32(&bars.k_full[s]), 1);
       mbar_init(smem_u32(&bars.k_empty[s]), 1);
@@ -144,24 +178,21 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_base_sh;
-  int issued = 0;   // producers: tiles whose copies this warp has issued
+  int issued = 0;   // producers: KV tiles whose copies this warp has issued
+  int q_loads = 0;  // K producer: Q tiles it has loaded
 
   if (warp == 4 || warp == 6) {
     // ------------------------------------------------------------ producers
     // Warp 4 loads Q and the K tiles, warp 6 the V tiles: each page needs one
     // TMA instruction per 64-dim slice, and their issue, not the bytes,
-    // bounded a single producer warp.
+    // bounded a single producer warp. Copies run ahead across item
+    // boundaries: the next item's Q and first tiles load while the current
+    // item is still computing.
     const bool is_v = warp == 6;
-    if (lane == 0 && !is_v) {
-      prefetch_tensormap(&q_map);
-      prefetch_tensormap(&k_map);
-      const uint32_t qb = smem_u32(&bars.q_full);
-      mbar_arrive_expect_tx(qb, C::Q_BYTES);
-#pragma unroll
-      for (int c = 0; c < C::DBLK; ++c)
-        tma_load_3d(base + C::OFF_Q + c * C::M * 128, &q_map, qb, c * 64, head, item.q_row);
+    if (lane == 0) {
+      prefetch_tensormap(is_v ? &v_map : &k_map);
+      if (!is_v) prefetch_tensormap(&q_map);
     }
-    if (lane == 0 && is_v) prefetch_tensormap(&v_map);
     const CUtensorMap* map = is_v ? &v_map : &k_map;
     uint64_t* full = is_v ? bars.v_full : bars.k_full;
     uint64_t* empty = is_v ? bars.v_empty : bars.k_empty;
@@ -169,110 +200,195 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
     const int P = prm.page_size;
     const int ppt = C::N / P;
     const uint32_t box = uint32_t(P) * 128u;
-    const int c1 = prm.layout == FI_LAYOUT_NHD ? kv_head : 0;
-    const int c2 = prm.layout == FI_LAYOUT_NHD ? 0 : kv_head;
-    bool ok = true;
-    // page ids of tile j+1 are loaded while tile j's copies are issued, so
-    // the dependent global load is off the producer's critical path
-    auto pages_in = [&](int j) {
-      return (min(C::N, item.tok_end - item.tok_begin - j * C::N) + P - 1) / P;
+    auto pages_in = [&](const WorkItem& w, int j) {
+      return (min(C::N, w.tok_end - w.tok_begin - j * C::N) + P - 1) / P;
     };
+    bool ok = true;
+    int g = 0;
+    // K producer, lane 0: publish item n's index in the ring (-1: no more)
+    auto publish = [&](int n, int value) {
+      if (n >= kItemRing &&
+          !mbar_wait_bounded(smem_u32(&bars.item_empty[n % kItemRing]),
+                             ((n / kItemRing) & 1) ^ 1, limit, &abort_flag))
+        return false;
+      item_ring[n % kItemRing] = value;
+      mbar_arrive(smem_u32(&bars.item_full[n % kItemRing]));   // release: the index is visible
+      return true;
+    };
+    // index of item 0 (both producers)
+    int it = blockIdx.x;
+    if (is_v) {
+      int v = -1;
+      if (lane == 0) {
+        ok = item_at(0, v);
+        item_done(0);
+      }
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      it = __shfl_sync(0xffffffffu, v, 0);
+    } else if (lane == 0) {
+      ok = publish(0, it);
+    }
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    WorkItem w;
+    if (ok && it >= 0) w = prm.items[it];
+    // page ids of the next tile are loaded while the current tile's copies
+    // are issued, so the dependent global load is off the critical path
     int next_page = -1;
-    if (n_tiles > 0 && lane < pages_in(0)) next_page = prm.page_indices[item.page_begin + lane];
-    for (int j = 0; j < n_tiles; ++j) {
-      const int st = j % C::NST;
-      const int np = pages_in(j);
-      int page = -1;
-      bool valid = false;
-      if (lane < np) {
-        page = next_page;
-        valid = page >= 0 && page < prm.num_pages;
-        if (!valid && !is_v) atomicOr(prm.err, kErrBounds);
+    if (ok && it >= 0 && item_tiles<C::N>(w) > 0 && lane < pages_in(w, 0))
+      next_page = prm.page_indices[w.page_begin + lane];
+    for (int n = 0; ok && it >= 0; ++n) {
+      const int nt = item_tiles<C::N>(w);
+      const int kv_head = w.head / prm.group;
+      const int c1 = prm.layout == FI_LAYOUT_NHD ? kv_head : 0;
+      const int c2 = prm.layout == FI_LAYOUT_NHD ? 0 : kv_head;
+      // the next item: taken from the counter and published by the K
+      // producer, read from the ring by the V producer
+      int it_next = -1;
+      if (lane == 0) {
+        if (is_v) {
+          ok = item_at(n + 1, it_next);
+          item_done(n + 1);
+        } else {
+          it_next = int(gridDim.x + atomicAdd(prm.work_counter, 1u));
+          if (it_next >= n_items) it_next = -1;
+          ok = publish(n + 1, it_next);
+        }
       }
-      if (j + 1 < n_tiles && lane < pages_in(j + 1))
-        next_page = prm.page_indices[item.page_begin + (j + 1) * ppt + lane];
-      const uint32_t bytes =
-          uint32_t(__popc(__ballot_sync(0xffffffffu, valid))) * C::DBLK * box;
-      if (j >= C::NST && !mbar_wait_warp(smem_u32(&empty[st]), ((j / C::NST) & 1) ^ 1, limit,
-                                         &abort_flag)) {
-        ok = false;
-        break;
-      }
-      const uint32_t fb = smem_u32(&full[st]);
-      const bool skip = !is_v && j == 0 && prm.fault_kind == 1 && blockIdx.x == 0;
-      if (lane == 0 && !skip) mbar_arrive_expect_tx(fb, bytes);
-      __syncwarp();
-      if (valid && !skip) {
-        const uint32_t dst = ring + st * C::KV_BYTES + lane * box;
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      it_next = __shfl_sync(0xffffffffu, it_next, 0);
+      if (!ok) break;
+      WorkItem wn;
+      if (it_next >= 0) wn = prm.items[it_next];
+      if (!is_v) {
+        // Q of item n, once the buffer is free: its previous contents were
+        // copied into TMEM (head_dim <= 128) or read by the last QK MMA
+        if (n >= 1) {
+          ok = mbar_wait_warp(smem_u32(C::Q_TMEM ? &bars.q_tmem : &bars.q_empty),
+                              (n - 1) & 1, limit, &abort_flag);
+          if (!ok) break;
+        }
+        if (lane == 0) {
+          const uint32_t qb = smem_u32(&bars.q_full);
+          mbar_arrive_expect_tx(qb, C::Q_BYTES);
 #pragma unroll
-        for (int c = 0; c < C::DBLK; ++c)
-          tma_load_4d(dst + c * C::N * 128, map, fb, c * 64, c1, c2, page);
+          for (int c = 0; c < C::DBLK; ++c)
+            tma_load_3d(base + C::OFF_Q + c * C::M * 128, &q_map, qb, c * 64, w.head, w.q_row);
+        }
+        q_loads = n + 1;
       }
-      issued = j + 1;
+      for (int j = 0; j < nt; ++j, ++g) {
+        const int st = g % C::NST;
+        const int np = pages_in(w, j);
+        int page = -1;
+        bool valid = false;
+        if (lane < np) {
+          page = next_page;
+          valid = page >= 0 && page < prm.num_pages;
+          if (!valid && !is_v) atomicOr(prm.err, kErrBounds);
+        }
+        if (j + 1 < nt) {
+          if (lane < pages_in(w, j + 1))
+            next_page = prm.page_indices[w.page_begin + (j + 1) * ppt + lane];
+        } else if (it_next >= 0 && item_tiles<C::N>(wn) > 0 && lane < pages_in(wn, 0)) {
+          next_page = prm.page_indices[wn.page_begin + lane];
+        }
+        const uint32_t bytes =
+            uint32_t(__popc(__ballot_sync(0xffffffffu, valid))) * C::DBLK * box;
+        if (g >= C::NST && !mbar_wait_warp(smem_u32(&empty[st]), ((g / C::NST) & 1) ^ 1,
+                                           limit, &abort_flag)) {
+          ok = false;
+          break;
+        }
+        const uint32_t fb = smem_u32(&full[st]);
+        const bool skip = !is_v && g == 0 && prm.fault_kind == 1 && blockIdx.x == 0;
+        if (lane == 0 && !skip) mbar_arrive_expect_tx(fb, bytes);
+        __syncwarp();
+        if (valid && !skip) {
+          const uint32_t dst = ring + st * C::KV_BYTES + lane * box;
+#pragma unroll
+          for (int c = 0; c < C::DBLK; ++c)
+            tma_load_4d(dst + c * C::N * 128, map, fb, c * 64, c1, c2, page);
+        }
+        issued = g + 1;
+      }
+      if (nt == 0 && it_next >= 0 && item_tiles<C::N>(wn) > 0 && lane < pages_in(wn, 0))
+        next_page = prm.page_indices[wn.page_begin + lane];
+      w = wn;
+      it = it_next;
     }
     if (!ok && lane == 0) { abort_flag = 1; atomicOr(prm.err, kErrTimeout); }
-    if (lane == 0 && !is_v) mbar_wait_bounded(smem_u32(&bars.q_full), 0, limit, nullptr);
     __syncwarp();
   } else if (warp == 5) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      bool ok = C::Q_TMEM
-                    ? mbar_wait_bounded(smem_u32(&bars.q_tmem), 0, limit, &abort_flag)
-                    : mbar_wait_bounded(smem_u32(&bars.q_full), 0, limit, &abort_flag);
       const uint32_t q_base = base + C::OFF_Q;
       // descriptors are linear in the address field (bits 0-13 = addr >> 4),
       // so each MMA's descriptor is a base plus a compile-time offset
       const uint64_t qd0 = sdesc_sw128(q_base, 16, 1024);
       const uint64_t kd0 = sdesc_sw128(base + C::OFF_K, 16, 1024);
       const uint64_t vd0 = sdesc_sw128(base + C::OFF_V, C::N * 128, 1024);
-      for (int j = 0; ok && j <= n_tiles; ++j) {
-        if (j < n_tiles) {
-          const int st = j % C::NST, sb = j & 1;
-          ok = mbar_wait_bounded(smem_u32(&bars.k_full[st]), (j / C::NST) & 1, limit,
-                                 &abort_flag);
-          if (ok && j >= 2)
-            ok = mbar_wait_bounded(smem_u32(&bars.s_free[sb]), ((j >> 1) & 1) ^ 1, limit,
+      bool ok = true;
+      int g = 0;   // KV tiles of earlier items
+      for (int n = 0; ok; ++n) {
+        int it = -1;
+        ok = item_at(n, it);
+        item_done(n);
+        if (!ok || it < 0) break;
+        const int nt = item_tiles<C::N>(prm.items[it]);
+        ok = C::Q_TMEM ? mbar_wait_bounded(smem_u32(&bars.q_tmem), n & 1, limit, &abort_flag)
+                       : mbar_wait_bounded(smem_u32(&bars.q_full), n & 1, limit, &abort_flag);
+        for (int j = 0; ok && j <= nt; ++j) {
+          if (j < nt) {
+            const int gq = g + j, st = gq % C::NST, sb = gq & 1;
+            ok = mbar_wait_bounded(smem_u32(&bars.k_full[st]), (gq / C::NST) & 1, limit,
                                    &abort_flag);
-          if (!ok) break;
-          tc_fence_after();
-          const uint64_t kd = kd0 + uint64_t((st * C::KV_BYTES) >> 4);
-          const uint32_t s_col = tmem + C::COL_S + sb * C::N;
+            if (ok && gq >= 2)
+              ok = mbar_wait_bounded(smem_u32(&bars.s_free[sb]), ((gq >> 1) & 1) ^ 1, limit,
+                                     &abort_flag);
+            if (!ok) break;
+            tc_fence_after();
+            const uint64_t kd = kd0 + uint64_t((st * C::KV_BYTES) >> 4);
+            const uint32_t s_col = tmem + C::COL_S + sb * C::N;
 #pragma unroll
-          for (int k = 0; k < HEAD_DIM / 16; ++k) {
-            const uint64_t bd = kd + uint64_t(((k >> 2) * C::N * 128 + (k & 3) * 32) >> 4);
-            if constexpr (C::Q_TMEM) {
-              tc_mma_ts(s_col, tmem + C::COL_Q + k * 8, bd, C::IDESC_QK, k > 0 ? 1u : 0u);
-            } else {
-              const uint64_t a = qd0 + uint64_t(((k >> 2) * C::M * 128 + (k & 3) * 32) >> 4);
-              tc_mma_ss(s_col, a, bd, C::IDESC_QK, k > 0 ? 1u : 0u);
+            for (int k = 0; k < HEAD_DIM / 16; ++k) {
+              const uint64_t bd = kd + uint64_t(((k >> 2) * C::N * 128 + (k & 3) * 32) >> 4);
+              if constexpr (C::Q_TMEM) {
+                tc_mma_ts(s_col, tmem + C::COL_Q + k * 8, bd, C::IDESC_QK, k > 0 ? 1u : 0u);
+              } else {
+                const uint64_t a = qd0 + uint64_t(((k >> 2) * C::M * 128 + (k & 3) * 32) >> 4);
+                tc_mma_ss(s_col, a, bd, C::IDESC_QK, k > 0 ? 1u : 0u);
+              }
             }
+            tc_commit(smem_u32(&bars.s_full[sb]));
+            tc_commit(smem_u32(&bars.k_empty[st]));
+            if (!C::Q_TMEM && j == nt - 1) tc_commit(smem_u32(&bars.q_empty));
           }
-          tc_commit(smem_u32(&bars.s_full[sb]));
-          tc_commit(smem_u32(&bars.k_empty[st]));
-        }
-        if (j >= 1) {
-          const int jj = j - 1, st = jj % C::NST;
-          ok = mbar_wait_bounded(smem_u32(&bars.p_full), jj & 1, limit, &abort_flag);
-          if (ok)
-            ok = mbar_wait_bounded(smem_u32(&bars.v_full[st]), (jj / C::NST) & 1, limit,
-                                   &abort_flag);
-          if (!ok) break;
-          tc_fence_after();
-          const uint64_t vd = vd0 + uint64_t((st * C::KV_BYTES) >> 4);
+          if (j >= 1) {
+            const int gp = g + j - 1, st = gp % C::NST;
+            ok = mbar_wait_bounded(smem_u32(&bars.p_full), gp & 1, limit, &abort_flag);
+            if (ok)
+              ok = mbar_wait_bounded(smem_u32(&bars.v_full[st]), (gp / C::NST) & 1, limit,
+                                     &abort_flag);
+            if (!ok) break;
+            tc_fence_after();
+            const uint64_t vd = vd0 + uint64_t((st * C::KV_BYTES) >> 4);
 #pragma unroll
-          for (int k = 0; k < C::N / 16; ++k) {
-            // MN-major V: 16 tokens per step; the next 64 dims one K-tile slice further
-            const uint64_t bd = vd + uint64_t((k * 16 * 128) >> 4);
-            tc_mma_ts(tmem + C::COL_O, tmem + C::COL_P + k * 8, bd, C::IDESC_PV,
-                      (jj > 0 || k > 0) ? 1u : 0u);
+            for (int k = 0; k < C::N / 16; ++k) {
+              // MN-major V: 16 tokens per step; the next 64 dims one K-tile slice further
+              const uint64_t bd = vd + uint64_t((k * 16 * 128) >> 4);
+              tc_mma_ts(tmem + C::COL_O, tmem + C::COL_P + k * 8, bd, C::IDESC_PV,
+                        (j > 1 || k > 0) ? 1u : 0u);
+            }
+            tc_commit(smem_u32(&bars.v_empty[st]));
+            tc_commit(smem_u32(&bars.pv_done));
           }
-          tc_commit(smem_u32(&bars.v_empty[st]));
-          tc_commit(smem_u32(&bars.pv_done));
         }
-      }
-      if (ok) {
+        if (!ok) break;
+        if (!C::Q_TMEM && nt == 0) tc_commit(smem_u32(&bars.q_empty));
         tc_commit(smem_u32(&bars.o_final));
-      } else {
+        g += nt;
+      }
+      if (!ok) {
         abort_flag = 1;
         atomicOr(prm.err, kErrTimeout);
         // every MMA issued so far completes before the TMEM is released
@@ -285,195 +401,248 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
     // ------------------------------------------------------------ softmax + epilogue
     const int t = threadIdx.x;                       // query row of the tile = TMEM lane
     const uint32_t lane_off = uint32_t(warp * 32) << 16;
-    const int q_start = prm.qo_indptr[req], q_end = prm.qo_indptr[req + 1];
-    const int qo_len = q_end - q_start;
-    const int np_req = prm.page_indptr[req + 1] - prm.page_indptr[req];
-    const int kv_len = np_req > 0 ? (np_req - 1) * prm.page_size + prm.last_page_len[req] : 0;
-    const int i_req = item.q_row - q_start + t;      // row index within the request
-    const int pos = kv_len - qo_len + i_req;         // key position of this row
-    int t_max = prm.causal ? pos : (kv_len - 1);
-    t_max = min(t_max, kv_len - 1);                  // last visible key of this row
-    // first visible key (left window); below 0 means no lower bound
-    const int t_min = prm.window_left >= 0 ? pos - prm.window_left : INT_MIN;
     const float scale = prm.sm_scale * kLog2e;
-    // l: sum of the exact weights (gives lse); lp: sum of the rounded
-    // weights the PV MMA multiplies (normalises O)
-    float m = -INFINITY, l = 0.f, lp = 0.f;
-    bool ok = true;
-
-    if constexpr (C::Q_TMEM) {
-      // this thread's Q row, from the swizzled TMA tile into TMEM (16-bit pairs)
-      ok = mbar_wait_warp(smem_u32(&bars.q_full), 0, limit, &abort_flag);
-      if (ok) {
+    // Row bounds of item w for this thread's row: the last key it may see
+    // (causal bound, clipped to the keys), the first (left window; INT_MIN:
+    // none) and the end of the request's rows.
+    struct RowBounds { int q_end, t_max, t_min; };
+    auto bounds_of = [&](const WorkItem& w) {
+      const int q_start = prm.qo_indptr[w.req], q_end = prm.qo_indptr[w.req + 1];
+      const int np_req = prm.page_indptr[w.req + 1] - prm.page_indptr[w.req];
+      const int kv_len =
+          np_req > 0 ? (np_req - 1) * prm.page_size + prm.last_page_len[w.req] : 0;
+      const int pos = kv_len - (q_end - q_start) + (w.q_row - q_start + t);  // key position
+      RowBounds r;
+      r.q_end = q_end;
+      r.t_max = min(prm.causal ? pos : kv_len - 1, kv_len - 1);
+      r.t_min = prm.window_left >= 0 ? pos - prm.window_left : INT_MIN;
+      return r;
+    };
+    // Q of item n: from the swizzled TMA tile into this thread's TMEM lane
+    // (16-bit pairs), then one arrival per warp on q_tmem.
+    auto copy_q = [&](int n) {
+      if (!mbar_wait_warp(smem_u32(&bars.q_full), n & 1, limit, &abort_flag)) return false;
 #pragma unroll
-        for (int b = 0; b < C::DBLK; ++b) {
-          uint32_t r[32];
+      for (int b = 0; b < C::DBLK; ++b) {
+        uint32_t r[32];
 #pragma unroll
-          for (int c8 = 0; c8 < 8; ++c8) {
-            const uint4 v = lds128(base + C::OFF_Q + b * C::M * 128 + swz(t, c8));
-            r[c8 * 4 + 0] = v.x;
-            r[c8 * 4 + 1] = v.y;
-            r[c8 * 4 + 2] = v.z;
-            r[c8 * 4 + 3] = v.w;
-          }
-          tmem_st32(tmem + lane_off + C::COL_Q + b * 32, r);
+        for (int c8 = 0; c8 < 8; ++c8) {
+          const uint4 v = lds128(base + C::OFF_Q + b * C::M * 128 + swz(t, c8));
+          r[c8 * 4 + 0] = v.x;
+          r[c8 * 4 + 1] = v.y;
+          r[c8 * 4 + 2] = v.z;
+          r[c8 * 4 + 3] = v.w;
         }
-        tmem_wait_st();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&bars.q_tmem));
+        tmem_st32(tmem + lane_off + C::COL_Q + b * 32, r);
       }
-    }
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&bars.q_tmem));
+      return true;
+    };
 
-    for (int j = 0; ok && j < n_tiles; ++j) {
-      const int st = j & 1;                 // S buffer
-      const int kvst = j % C::NST;          // K/V ring stage
-      if (!mbar_wait_warp(smem_u32(&bars.s_full[st]), (j >> 1) & 1, limit, &abort_flag)) {
+    // index of item n from the ring (lane 0 reads, the warp gets a copy)
+    auto take_item = [&](int n, int& idx) {
+      int v = -1;
+      bool good = true;
+      if (lane == 0) {
+        good = item_at(n, v);
+        item_done(n);
+      }
+      idx = __shfl_sync(0xffffffffu, v, 0);
+      return __shfl_sync(0xffffffffu, good, 0) != 0;
+    };
+    int g = 0;   // KV tiles of earlier items
+    int it = -1;
+    bool ok = take_item(0, it);
+    WorkItem w;
+    RowBounds rb;
+    if (ok && it >= 0) {
+      w = prm.items[it];
+      rb = bounds_of(w);
+      if constexpr (C::Q_TMEM) ok = copy_q(0);
+    }
+    for (int n = 0; ok && it >= 0; ++n) {
+      const int nt = item_tiles<C::N>(w);
+      int it_next = -1;
+      if (!take_item(n + 1, it_next)) {
         ok = false;
         break;
       }
-      tc_fence_after();
-      uint32_t sr[C::N / 32][32];
-#pragma unroll
-      for (int c = 0; c < C::N / 32; ++c)
-        tmem_ld32(tmem + lane_off + C::COL_S + st * C::N + c * 32, sr[c]);
-      tmem_wait_ld();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&bars.s_free[st]));
-
-      // Row max of the raw scores (sm_scale >= 0 commutes with max). Eight
-      // independent accumulators keep the dependency chains short; the mask
-      // is applied only in tiles that cross this warp's causal bound.
-      const int col0 = item.tok_begin + j * C::N;   // key position of column 0
-      const bool need_mask = __any_sync(0xffffffffu, col0 + C::N - 1 > t_max || col0 < t_min);
-      float mx8[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) mx8[i] = -INFINITY;
-      if (need_mask) {
-#pragma unroll
-        for (int k = 0; k < C::N; ++k) {
-          const bool vis = col0 + k <= t_max && col0 + k >= t_min;
-          const float v = vis ? __uint_as_float(sr[k >> 5][k & 31]) : -INFINITY;
-          mx8[k & 7] = fmaxf(mx8[k & 7], v);
-        }
-      } else {
-#pragma unroll
-        for (int k = 0; k < C::N; ++k) mx8[k & 7] = fmaxf(mx8[k & 7], __uint_as_float(sr[k >> 5][k & 31]));
-      }
-      const float mx_raw = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                                 fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
-      const float m_tile = (mx_raw == -INFINITY) ? -INFINITY : mx_raw * scale;
-      const float m_new = fmaxf(m, m_tile);
-      const bool grow = m_new > m + kRescaleThreshold;
-      const bool o_live = grow && (m != -INFINITY);  // O row holds data that must be rescaled
-      float alpha = 1.f;
-      if (grow) {
-        alpha = ex2(m - m_new);
-        l *= alpha;
-        lp *= alpha;
-        m = m_new;
-      }
-      const float ref = (m == -INFINITY) ? 0.f : m;
-      // p = 2^(s * scale - ref): one FFMA and one ex2 per score
-      float s[C::N];
-      float rs8[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) rs8[i] = 0.f;
-#pragma unroll
-      for (int k = 0; k < C::N; ++k) s[k] = ex2(fmaf(__uint_as_float(sr[k >> 5][k & 31]), scale, -ref));
-      if (need_mask) {
-#pragma unroll
-        for (int k = 0; k < C::N; ++k)
-          s[k] = (col0 + k <= t_max && col0 + k >= t_min) ? s[k] : 0.f;
-      }
-#pragma unroll
-      for (int k = 0; k < C::N; ++k) rs8[k & 7] += s[k];
-      const float rs_tile =
-          ((rs8[0] + rs8[1]) + (rs8[2] + rs8[3])) + ((rs8[4] + rs8[5]) + (rs8[6] + rs8[7]));
-      l += rs_tile;
-
-      // P buffer and O are free once the previous PV has completed
-      if (j >= 1) {
-        if (!mbar_wait_warp(smem_u32(&bars.pv_done), (j - 1) & 1, limit, &abort_flag)) {
+      const bool has_next = it_next >= 0;
+      // l: sum of the exact weights (gives lse); lp: sum of the rounded
+      // weights the PV MMA multiplies (normalises O)
+      float m = -INFINITY, l = 0.f, lp = 0.f;
+      for (int j = 0; j < nt; ++j, ++g) {
+        const int st = g & 1;                 // S buffer
+        const int kvst = g % C::NST;          // K/V ring stage
+        if (!mbar_wait_warp(smem_u32(&bars.s_full[st]), (g >> 1) & 1, limit, &abort_flag)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        if (__any_sync(0xffffffffu, o_live)) {
-#pragma unroll 1
-          for (int c = 0; c < HEAD_DIM / 32; ++c) {
-            uint32_t r[32];
-            tmem_ld32(tmem + lane_off + C::COL_O + c * 32, r);
-            tmem_wait_ld();
+        uint32_t sr[C::N / 32][32];
 #pragma unroll
-            for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
-            tmem_st32(tmem + lane_off + C::COL_O + c * 32, r);
-          }
-          tmem_wait_st();
-        }
-      }
-      // Last tile: V rows past the valid keys may hold unused page slots or
-      // stale data; zero them so that P = 0 there cannot meet a NaN.
-      const int valid = item.tok_end - col0;
-      if (valid < C::N) {
-        if (!mbar_wait_warp(smem_u32(&bars.v_full[kvst]), (j / C::NST) & 1, limit,
-                            &abort_flag)) {
-          ok = false;
-          break;
-        }
-        if (t >= valid && t < C::N) {
+        for (int c = 0; c < C::N / 32; ++c)
+          tmem_ld32(tmem + lane_off + C::COL_S + st * C::N + c * 32, sr[c]);
+        tmem_wait_ld();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&bars.s_free[st]));
+
+        // Row max of the raw scores (sm_scale >= 0 commutes with max). Eight
+        // independent accumulators keep the dependency chains short; the mask
+        // is applied only in tiles that cross this warp's bounds.
+        const int col0 = w.tok_begin + j * C::N;   // key position of column 0
+        const bool need_mask =
+            __any_sync(0xffffffffu, col0 + C::N - 1 > rb.t_max || col0 < rb.t_min);
+        float mx8[8];
 #pragma unroll
-          for (int c = 0; c < C::DBLK; ++c)
-#pragma unroll
-            for (int c8 = 0; c8 < 8; ++c8)
-              st_shared_v4(base + C::OFF_V + kvst * C::KV_BYTES + c * C::N * 128 + t * 128 +
-                               c8 * 16, 0u, 0u, 0u, 0u);
-        }
-      }
-      // P row t as packed 16-bit pairs into TMEM (the A operand of the PV
-      // MMA). lp adds the same rounded values the tensor core multiplies, so
-      // that the final division normalises exactly the weights applied.
-      // In tiles on the causal diagonal a row may have only a few visible
-      // keys, so lp adds exactly the rounded values there; elsewhere the
-      // rounding errors of many weights average out and the exact sum is used.
-      float rsp4[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-      for (int kb = 0; kb < C::N / 64; ++kb) {
-        uint32_t w[32];
-#pragma unroll
-        for (int e = 0; e < 32; ++e) w[e] = E::pack2(s[kb * 64 + 2 * e], s[kb * 64 + 2 * e + 1]);
+        for (int i = 0; i < 8; ++i) mx8[i] = -INFINITY;
         if (need_mask) {
 #pragma unroll
-          for (int e = 0; e < 32; ++e) rsp4[e & 3] += E::lo(w[e]) + E::hi(w[e]);
+          for (int k = 0; k < C::N; ++k) {
+            const bool vis = col0 + k <= rb.t_max && col0 + k >= rb.t_min;
+            const float v = vis ? __uint_as_float(sr[k >> 5][k & 31]) : -INFINITY;
+            mx8[k & 7] = fmaxf(mx8[k & 7], v);
+          }
+        } else {
+#pragma unroll
+          for (int k = 0; k < C::N; ++k)
+            mx8[k & 7] = fmaxf(mx8[k & 7], __uint_as_float(sr[k >> 5][k & 31]));
         }
-        tmem_st32(tmem + lane_off + C::COL_P + kb * 32, w);
-      }
-      tmem_wait_st();
-      lp += need_mask ? (rsp4[0] + rsp4[1]) + (rsp4[2] + rsp4[3]) : rs_tile;
-      fence_proxy_async_smem();   // zeroed V rows (generic writes) before the MMA reads them
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&bars.p_full));
-    }
+        const float mx_raw = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                                   fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+        const float m_tile = (mx_raw == -INFINITY) ? -INFINITY : mx_raw * scale;
+        const float m_new = fmaxf(m, m_tile);
+        const bool grow = m_new > m + kRescaleThreshold;
+        const bool o_live = grow && (m != -INFINITY);  // O row holds data that must be rescaled
+        float alpha = 1.f;
+        if (grow) {
+          alpha = ex2(m - m_new);
+          l *= alpha;
+          lp *= alpha;
+          m = m_new;
+        }
+        const float ref = (m == -INFINITY) ? 0.f : m;
+        // p = 2^(s * scale - ref): one FFMA and one ex2 per score
+        float s[C::N];
+        float rs8[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) rs8[i] = 0.f;
+#pragma unroll
+        for (int k = 0; k < C::N; ++k)
+          s[k] = ex2(fmaf(__uint_as_float(sr[k >> 5][k & 31]), scale, -ref));
+        if (need_mask) {
+#pragma unroll
+          for (int k = 0; k < C::N; ++k)
+            s[k] = (col0 + k <= rb.t_max && col0 + k >= rb.t_min) ? s[k] : 0.f;
+        }
+#pragma unroll
+        for (int k = 0; k < C::N; ++k) rs8[k & 7] += s[k];
+        const float rs_tile =
+            ((rs8[0] + rs8[1]) + (rs8[2] + rs8[3])) + ((rs8[4] + rs8[5]) + (rs8[6] + rs8[7]));
+        l += rs_tile;
 
-    if (ok && n_tiles > 0) {
-      ok = mbar_wait_warp(smem_u32(&bars.o_final), 0, limit, &abort_flag);
+        // P buffer and O are free once the previous PV of this item has
+        // completed (the last PV of the previous item completed before its
+        // epilogue read O)
+        if (j >= 1) {
+          if (!mbar_wait_warp(smem_u32(&bars.pv_done), (g - 1) & 1, limit, &abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          if (__any_sync(0xffffffffu, o_live)) {
+#pragma unroll 1
+            for (int c = 0; c < HEAD_DIM / 32; ++c) {
+              uint32_t r[32];
+              tmem_ld32(tmem + lane_off + C::COL_O + c * 32, r);
+              tmem_wait_ld();
+#pragma unroll
+              for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
+              tmem_st32(tmem + lane_off + C::COL_O + c * 32, r);
+            }
+            tmem_wait_st();
+          }
+        }
+        // Last tile: V rows past the valid keys may hold unused page slots or
+        // stale data; zero them so that P = 0 there cannot meet a NaN.
+        const int valid = w.tok_end - col0;
+        if (valid < C::N) {
+          if (!mbar_wait_warp(smem_u32(&bars.v_full[kvst]), (g / C::NST) & 1, limit,
+                              &abort_flag)) {
+            ok = false;
+            break;
+          }
+          if (t >= valid && t < C::N) {
+#pragma unroll
+            for (int c = 0; c < C::DBLK; ++c)
+#pragma unroll
+              for (int c8 = 0; c8 < 8; ++c8)
+                st_shared_v4(base + C::OFF_V + kvst * C::KV_BYTES + c * C::N * 128 + t * 128 +
+                                 c8 * 16, 0u, 0u, 0u, 0u);
+          }
+        }
+        // P row t as packed 16-bit pairs into TMEM (the A operand of the PV
+        // MMA). lp adds the same rounded values the tensor core multiplies, so
+        // that the final division normalises exactly the weights applied.
+        // In tiles on the causal diagonal a row may have only a few visible
+        // keys, so lp adds exactly the rounded values there; elsewhere the
+        // rounding errors of many weights average out and the exact sum is used.
+        float rsp4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int kb = 0; kb < C::N / 64; ++kb) {
+          uint32_t wv[32];
+#pragma unroll
+          for (int e = 0; e < 32; ++e) wv[e] = E::pack2(s[kb * 64 + 2 * e], s[kb * 64 + 2 * e + 1]);
+          if (need_mask) {
+#pragma unroll
+            for (int e = 0; e < 32; ++e) rsp4[e & 3] += E::lo(wv[e]) + E::hi(wv[e]);
+          }
+          tmem_st32(tmem + lane_off + C::COL_P + kb * 32, wv);
+        }
+        tmem_wait_st();
+        lp += need_mask ? (rsp4[0] + rsp4[1]) + (rsp4[2] + rsp4[3]) : rs_tile;
+        fence_proxy_async_smem();   // zeroed V rows (generic writes) before the MMA reads them
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&bars.p_full));
+      }
+      if (!ok) break;
+      // Every QK MMA of this item has completed (the last S was read), so the
+      // TMEM Q region may take the next item's Q now: the MMA issuer then
+      // computes the next item's first scores while this item's last PV
+      // and epilogue finish. (Copying it inside the tile loop instead, right
+      // after the last S read, made the loop measurably slower.)
+      if (C::Q_TMEM && has_next && !copy_q(n + 1)) {
+        ok = false;
+        break;
+      }
+      // the next item's bounds load while this item's last PV completes
+      WorkItem wn;
+      RowBounds rn;
+      if (has_next) {
+        wn = prm.items[it_next];
+        rn = bounds_of(wn);
+      }
+      if (!mbar_wait_warp(smem_u32(&bars.o_final), n & 1, limit, &abort_flag)) {
+        ok = false;
+        break;
+      }
       tc_fence_after();
-    }
-    if (!ok) {
-      if (lane == 0) { abort_flag = 1; atomicOr(prm.err, kErrTimeout); }
-    } else {
-      const int rows = min(C::M, q_end - item.q_row);
+      // ---- epilogue: O / lp (bf16 or fp16) and lse = ln(l) + m ln 2
+      const int rows = min(C::M, rb.q_end - w.q_row);
       const bool row_ok = t < rows;
       const float inv = lp > 0.f ? 1.f / lp : 0.f;
-      const size_t out_row = size_t(item.q_row) + t;
+      const size_t out_row = size_t(w.q_row) + t;
       uint16_t* op = reinterpret_cast<uint16_t*>(prm.out) +
-                          (out_row * prm.num_qo_heads + head) * HEAD_DIM;
+                     (out_row * prm.num_qo_heads + w.head) * HEAD_DIM;
 #pragma unroll 1
       for (int c = 0; c < HEAD_DIM / 32; ++c) {
         uint32_t r[32];
-        if (n_tiles > 0) {
+        if (nt > 0) {
           tmem_ld32(tmem + lane_off + C::COL_O + c * 32, r);
           tmem_wait_ld();
         } else {
@@ -485,16 +654,23 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
 #pragma unroll
           for (int q4 = 0; q4 < 4; ++q4) {
             const float* f = reinterpret_cast<const float*>(r) + q4 * 8;
-            dst[q4] = make_uint4(E::pack2(f[0] * inv, f[1] * inv),
-                                 E::pack2(f[2] * inv, f[3] * inv),
-                                 E::pack2(f[4] * inv, f[5] * inv),
-                                 E::pack2(f[6] * inv, f[7] * inv));
+            dst[q4] = make_uint4(E::pack2(f[0] * inv, f[1] * inv), E::pack2(f[2] * inv, f[3] * inv),
+                                 E::pack2(f[4] * inv, f[5] * inv), E::pack2(f[6] * inv, f[7] * inv));
           }
         }
       }
       if (row_ok && prm.lse)
-        prm.lse[out_row * prm.num_qo_heads + head] =
-            l > 0.f ? (m + lg2(l)) * kLn2 : -INFINITY;
+        prm.lse[out_row * prm.num_qo_heads + w.head] = l > 0.f ? (m + lg2(l)) * kLn2 : -INFINITY;
+      // O has been read: the next item's first PV (issued only after this
+      // warp's next p_full arrival) may overwrite it
+      tc_fence_before();
+      w = wn;
+      rb = rn;
+      it = it_next;
+    }
+    if (!ok && lane == 0) {
+      abort_flag = 1;
+      atomicOr(prm.err, kErrTimeout);
     }
   }
 
@@ -505,7 +681,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
     tmem_dealloc(tmem, C::TMEM_COLS);
   }
   // Each producer lets every copy it issued land before the CTA exits, also
-  // after a timeout anywhere in the CTA (in a normal run the MMA issuer has
+  // after a timeout anywhere in the CTA (in a normal run the consumers have
   // already seen these phases complete, so the waits return at once).
   if ((warp == 4 || warp == 6) && lane == 0) {
     const bool is_v = warp == 6;
@@ -514,29 +690,31 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
       if (!is_v && j == 0 && prm.fault_kind == 1 && blockIdx.x == 0) continue;  // never issued
       mbar_wait_bounded(smem_u32(&full[j % C::NST]), (j / C::NST) & 1, limit, nullptr);
     }
+    if (!is_v && q_loads > 0)
+      mbar_wait_bounded(smem_u32(&bars.q_full), (q_loads - 1) & 1, limit, nullptr);
   }
 }
 
 template <int HEAD_DIM, class E>
 cudaError_t launch_prefill_t(const CUtensorMap& qm, const CUtensorMap& km, const CUtensorMap& vm,
-                             const PrefillParams& p, int n_items, cudaStream_t stream) {
+                             const PrefillParams& p, int grid, cudaStream_t stream) {
   using C = PrefillCfg<HEAD_DIM, E>;
   auto kern = prefill_kernel<HEAD_DIM, E>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        C::SMEM_BYTES);
   if (e != cudaSuccess) return e;
-  kern<<<n_items, C::THREADS, C::SMEM_BYTES, stream>>>(qm, km, vm, p);
+  kern<<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(qm, km, vm, p);
   return cudaGetLastError();
 }
 
 template <class E>
 cudaError_t launch_prefill_e(int head_dim, const CUtensorMap& qm, const CUtensorMap& km,
-                             const CUtensorMap& vm, const PrefillParams& p, int n_items,
+                             const CUtensorMap& vm, const PrefillParams& p, int grid,
                              cudaStream_t stream) {
   switch (head_dim) {
-    case 64: return launch_prefill_t<64, E>(qm, km, vm, p, n_items, stream);
-    case 128: return launch_prefill_t<128, E>(qm, km, vm, p, n_items, stream);
-    case 256: return launch_prefill_t<256, E>(qm, km, vm, p, n_items, stream);
+    case 64: return launch_prefill_t<64, E>(qm, km, vm, p, grid, stream);
+    case 128: return launch_prefill_t<128, E>(qm, km, vm, p, grid, stream);
+    case 256: return launch_prefill_t<256, E>(qm, km, vm, p, grid, stream);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -544,12 +722,13 @@ cudaError_t launch_prefill_e(int head_dim, const CUtensorMap& qm, const CUtensor
 }  // namespace
 
 cudaError_t launch_prefill(int head_dim, int dtype, const CUtensorMap& qm, const CUtensorMap& km,
-                           const CUtensorMap& vm, const PrefillParams& p, int n_items,
+                           const CUtensorMap& vm, const PrefillParams& p, int grid,
                            cudaStream_t stream) {
-  if (n_items <= 0) return cudaSuccess;
+  if (p.n_items <= 0 || grid <= 0) return cudaSuccess;
+  grid = grid < p.n_items ? grid : p.n_items;
   switch (dtype) {
-    case FI_DTYPE_BF16: return launch_prefill_e<Bf16>(head_dim, qm, km, vm, p, n_items, stream);
-    case FI_DTYPE_FP16: return launch_prefill_e<Fp16>(head_dim, qm, km, vm, p, n_items, stream);
+    case FI_DTYPE_BF16: return launch_prefill_e<Bf16>(head_dim, qm, km, vm, p, grid, stream);
+    case FI_DTYPE_FP16: return launch_prefill_e<Fp16>(head_dim, qm, km, vm, p, grid, stream);
     default: return cudaErrorInvalidValue;
   }
 }
