@@ -5,8 +5,8 @@ Default workload: Llama-7B-shaped batch decode (64 requests, 32 q / 32 kv
 heads, head_dim 128, page size 16, KV lengths uniform in [512, 4096], NHD,
 shuffled page table), the configuration the headline metric is quoted on.
 One step = one pass of the hot path over that batch through the C ABI: the
-stream-ordered work-list upload, the decode kernel and, where the plan split
-long requests, the merge kernel. The plan itself is host work done once per
+stream-ordered work-list upload and the decode kernel (which also merges the
+partial states of split requests). The plan itself is host work done once per
 batch composition; it is inside the end-to-end number (`e2e`), which also
 copies the step's inputs from pinned host memory and its outputs back.
 
@@ -427,8 +427,7 @@ def run_ours(args, rank, world, local_rank):
     kvb = kv_bytes(b)
     flops = attention_flops(b)
     launches_per_step = (1 if info["num_decode_items"] else 0) + \
-                        (1 if info["num_prefill_items"] else 0) + \
-                        (1 if info["num_split_requests"] else 0)
+                        (1 if info["num_prefill_items"] else 0)
 
     # CPU baseline first (rank 0, N = 1 only), before the device is busy
     cpu = None

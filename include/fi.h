@@ -183,7 +183,8 @@ fi_status fi_plan_get_work(fi_plan_t plan, int32_t* items_h, int32_t capacity,
  * a left window). Each K/V page is loaded once and
  * shared by the g query heads of its group. Long requests are split over
  * several CTAs as the plan says; their fp32 partial states are merged by
- * log-sum-exp into out/lse before the call's work completes on the stream.
+ * log-sum-exp into out/lse inside the same kernel (the CTA that finishes a
+ * split's last chunk merges it).
  *   plan             from fi_plan(FI_MODE_DECODE, ...).
  *   q                device [B][num_qo_heads][head_dim] of the plan's dtype.
  *   k_cache, v_cache device paged caches of the plan's dtype (layout,
@@ -201,7 +202,12 @@ fi_status fi_plan_get_work(fi_plan_t plan, int32_t* items_h, int32_t capacity,
  * Errors: FI_ERR_INVALID_ARG (NULL or misaligned pointers — q, caches and
  * out need 16-byte alignment —, a plan of the other mode, page_stride_elems
  * not a multiple of 8), FI_ERR_WORKSPACE_TOO_SMALL, FI_ERR_NO_DEVICE,
- * FI_ERR_CUDA (launch failure).
+ * FI_ERR_UNSUPPORTED (the stream is being captured into a CUDA graph: the
+ * work-list upload reads a reused pinned staging buffer, so a replay would
+ * copy another call's list), FI_ERR_CUDA (launch failure).
+ * The host keeps, per thread and device, a small ring of pinned staging
+ * buffers for the work-list copy (allocated on first use, grown when a
+ * plan needs more, never freed).
  */
 fi_status fi_batch_decode_paged(fi_plan_t plan, const void* q, const void* k_cache,
                                 const void* v_cache, int32_t kv_layout,
@@ -309,8 +315,9 @@ fi_status fi_debug_set_fault(int32_t kind, int64_t wait_limit);
 /*
  * Profiling hook: the next paged run call made by this thread records
  * start_event (a cudaEvent_t) on its stream just before its first attention
- * kernel and stop_event just after its last attention kernel (before any
- * merge), so that a caller can time the main kernel alone with
+ * kernel and stop_event just after its last attention kernel, so that a
+ * caller can time the attention kernels alone (without the work-list
+ * upload) with
  * cudaEventElapsedTime. One-shot; NULL for both clears a pending request.
  * Errors from the event records are returned by that run call as FI_ERR_CUDA.
  */

@@ -69,6 +69,91 @@ fi_status side_stream(SideStream* out) {
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
+// Pinned staging for the work-list upload. A copy from pageable memory
+// makes the host wait until the driver has staged it, which delays the
+// kernel launches queued behind it; from pinned memory it is a plain
+// asynchronous DMA. Each host thread keeps a small ring of pinned slots for
+// its current device; a slot is refilled only once the copy that read it
+// has completed (one event per slot). Nothing is freed at exit.
+constexpr int kStagingSlots = 8;
+struct Staging {
+  int device = -1;
+  uint8_t* buf = nullptr;
+  size_t slot_bytes = 0;
+  cudaEvent_t done[kStagingSlots] = {};
+  bool pending[kStagingSlots] = {};
+  int next = 0;
+};
+thread_local Staging g_staging;
+
+// The workspace prefix a run uploads: zeroed header (error word, work
+// counter), work lists, merge tasks, zeroed merge counters; alignment gaps
+// zeroed too. `dst` holds P.ws.partial_o bytes.
+void fill_image(uint8_t* dst, const fi::Plan& P) {
+  const size_t n_dec = P.decode_items.size() * sizeof(fi::WorkItem);
+  const size_t n_pre = P.prefill_items.size() * sizeof(fi::WorkItem);
+  const size_t n_mrg = P.merges.size() * sizeof(fi::MergeTask);
+  std::memset(dst, 0, P.ws.decode_items);
+  if (n_dec) std::memcpy(dst + P.ws.decode_items, P.decode_items.data(), n_dec);
+  std::memset(dst + P.ws.decode_items + n_dec, 0, P.ws.prefill_items - P.ws.decode_items - n_dec);
+  if (n_pre) std::memcpy(dst + P.ws.prefill_items, P.prefill_items.data(), n_pre);
+  std::memset(dst + P.ws.prefill_items + n_pre, 0, P.ws.merges - P.ws.prefill_items - n_pre);
+  if (n_mrg) std::memcpy(dst + P.ws.merges, P.merges.data(), n_mrg);
+  std::memset(dst + P.ws.merges + n_mrg, 0, P.ws.partial_o - P.ws.merges - n_mrg);
+}
+
+fi_status upload_image(void* dst, const fi::Plan& P, cudaStream_t stream) {
+  Staging& s = g_staging;
+  const size_t bytes = P.ws.partial_o;
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return FI_ERR_NO_DEVICE;
+  if (s.device != dev || bytes > s.slot_bytes) {
+    // (re)build the ring once its copies have completed
+    for (int i = 0; i < kStagingSlots; ++i) {
+      if (s.done[i]) {
+        if (s.pending[i]) cudaEventSynchronize(s.done[i]);
+        cudaEventDestroy(s.done[i]);
+        s.done[i] = nullptr;
+      }
+      s.pending[i] = false;
+    }
+    if (s.buf) cudaFreeHost(s.buf);
+    s = Staging();
+    size_t slot = size_t(1) << 20;
+    while (slot < bytes) slot <<= 1;
+    void* p = nullptr;
+    bool ok = cudaHostAlloc(&p, slot * kStagingSlots, cudaHostAllocPortable) == cudaSuccess;
+    for (int i = 0; ok && i < kStagingSlots; ++i)
+      ok = cudaEventCreateWithFlags(&s.done[i], cudaEventDisableTiming) == cudaSuccess;
+    if (!ok) {
+      for (int i = 0; i < kStagingSlots; ++i)
+        if (s.done[i]) cudaEventDestroy(s.done[i]);
+      if (p) cudaFreeHost(p);
+      s = Staging();
+      cudaGetLastError();   // clear; fall back to a (synchronous) pageable copy
+      std::vector<uint8_t> image(bytes);
+      fill_image(image.data(), P);
+      const cudaError_t e = cudaMemcpy(dst, image.data(), bytes, cudaMemcpyHostToDevice);
+      return e == cudaSuccess ? FI_OK : cuda_fail(e, "work-list upload");
+    }
+    s.device = dev;
+    s.buf = static_cast<uint8_t*>(p);
+    s.slot_bytes = slot;
+  }
+  const int i = s.next;
+  s.next = (s.next + 1) % kStagingSlots;
+  cudaError_t e = cudaSuccess;
+  if (s.pending[i]) e = cudaEventSynchronize(s.done[i]);
+  if (e != cudaSuccess) return cuda_fail(e, "work-list staging");
+  uint8_t* src = s.buf + size_t(i) * s.slot_bytes;
+  fill_image(src, P);
+  e = cudaMemcpyAsync(dst, src, bytes, cudaMemcpyHostToDevice, stream);
+  if (e == cudaSuccess) e = cudaEventRecord(s.done[i], stream);
+  if (e != cudaSuccess) return cuda_fail(e, "work-list upload");
+  s.pending[i] = true;
+  return FI_OK;
+}
+
 // Tensor map over a paged K or V cache that fetches one (page, kv head)
 // block of page_size rows x 64 dims (128 bytes, 128-byte swizzled) per box.
 CUtensorMapDataType tma_type(int dtype) {
@@ -172,10 +257,18 @@ fi_status run_paged(fi_plan_t plan, bool prefill_call, const void* q, const int3
   cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
 
-  // Upload header (zeroed error word) + work lists + merge tasks in one copy.
-  const auto& image = plan->image;
-  cudaError_t e = cudaMemcpyAsync(ws, image.data(), image.size(), cudaMemcpyHostToDevice, stream);
-  if (e != cudaSuccess) return cuda_fail(e, "work-list upload");
+  // A captured copy would replay from a staging slot that later calls
+  // refill, so run calls refuse stream capture instead of recording it.
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(stream, &cap) != cudaSuccess || cap != cudaStreamCaptureStatusNone) {
+    g_last_error = "run calls cannot be captured into a CUDA graph";
+    return FI_ERR_UNSUPPORTED;
+  }
+  // Upload header (zeroed error word and counters) + work lists + merge
+  // tasks in one copy.
+  st = upload_image(ws, P, stream);
+  if (st != FI_OK) return st;
+  cudaError_t e = cudaSuccess;
 
   CUtensorMap kmap, vmap;
   if (P.total_kv > 0) {
@@ -211,8 +304,9 @@ fi_status run_paged(fi_plan_t plan, bool prefill_call, const void* q, const int3
   // With both kinds of work, the decode kernel (HBM-bound) runs on a side
   // stream concurrently with the prefill kernel (tensor-bound), which is
   // launched first (measured faster than the other order or a high-priority
-  // side stream); the streams join before the merge. Both kernels read the
-  // work lists uploaded above.
+  // side stream); the streams join at the end. Both kernels read the work
+  // lists uploaded above; split decode work is merged inside the decode
+  // kernel.
   const bool concurrent = !P.prefill_items.empty() && !P.decode_items.empty();
   SideStream side;
   cudaStream_t dstream = stream;
@@ -263,6 +357,8 @@ fi_status run_paged(fi_plan_t plan, bool prefill_call, const void* q, const int3
     dp.lse = lse;
     dp.partial_o = partial_o;
     dp.partial_lse = partial_lse;
+    dp.merges = reinterpret_cast<const fi::MergeTask*>(ws + P.ws.merges);
+    dp.merge_counters = reinterpret_cast<uint32_t*>(ws + P.ws.merge_counters);
     dp.err = err;
     dp.wait_limit_ns = g_wait_limit_ns;
     dp.fault_kind = fault_kind;
@@ -278,20 +374,6 @@ fi_status run_paged(fi_plan_t plan, bool prefill_call, const void* q, const int3
   if (prof_stop) {
     e = cudaEventRecord(prof_stop, stream);
     if (e != cudaSuccess) return cuda_fail(e, "profiling event");
-  }
-  if (!P.merges.empty()) {
-    fi::MergeParams mp;
-    mp.v = partial_o;
-    mp.s = partial_lse;
-    mp.tasks = reinterpret_cast<const fi::MergeTask*>(ws + P.ws.merges);
-    mp.S = 0;
-    mp.H = P.num_qo_heads;
-    mp.d = P.head_dim;
-    mp.out = out;
-    mp.lse = lse;
-    mp.dtype = P.dtype;
-    e = fi::launch_merge(mp, int(P.merges.size()), stream);
-    if (e != cudaSuccess) return cuda_fail(e, "merge launch");
   }
   return FI_OK;
 }
@@ -316,18 +398,7 @@ fi_status fi_plan(int32_t mode, int32_t batch_size, const int32_t* qo_indptr_h,
     delete p;
     return st;
   }
-  // Host image of the workspace prefix: zeroed header, work lists, merge tasks.
   const fi::Plan& P = p->p;
-  p->image.assign(P.ws.partial_o, 0);
-  if (!P.decode_items.empty())
-    std::memcpy(p->image.data() + P.ws.decode_items, P.decode_items.data(),
-                P.decode_items.size() * sizeof(fi::WorkItem));
-  if (!P.prefill_items.empty())
-    std::memcpy(p->image.data() + P.ws.prefill_items, P.prefill_items.data(),
-                P.prefill_items.size() * sizeof(fi::WorkItem));
-  if (!P.merges.empty())
-    std::memcpy(p->image.data() + P.ws.merges, P.merges.data(),
-                P.merges.size() * sizeof(fi::MergeTask));
   *out_plan = p;
   *workspace_bytes = P.ws.total;
   return FI_OK;
@@ -362,9 +433,16 @@ fi_status fi_plan_get_work(fi_plan_t plan, int32_t* items_h, int32_t capacity,
   *num_items = n;
   if (!items_h) return FI_OK;
   if (capacity < n) return FI_ERR_INVALID_ARG;
-  std::memcpy(items_h, P.decode_items.data(), P.decode_items.size() * sizeof(fi::WorkItem));
-  std::memcpy(items_h + 8 * P.decode_items.size(), P.prefill_items.data(),
-              P.prefill_items.size() * sizeof(fi::WorkItem));
+  // the first 8 fields of each item, as the header documents
+  int32_t* dst = items_h;
+  for (const auto* list : {&P.decode_items, &P.prefill_items}) {
+    for (const fi::WorkItem& w : *list) {
+      const int32_t f[8] = {w.req, w.head, w.page_begin, w.n_pages, w.tok_begin, w.tok_end,
+                            w.slot, w.q_row};
+      std::memcpy(dst, f, sizeof(f));
+      dst += 8;
+    }
+  }
   return FI_OK;
 }
 

@@ -217,6 +217,7 @@ decode_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant__
   __shared__ __align__(8) uint64_t full_bar[C::NSTAGE];
   __shared__ __align__(8) uint64_t empty_bar[C::NSTAGE];
   __shared__ int abort_flag;
+  __shared__ int merge_last;
 
   const uint32_t smem_base = (smem_u32(smem_raw) + 1023u) & ~1023u;
   uint8_t* smem_gen = smem_raw + (smem_base - smem_u32(smem_raw));
@@ -470,6 +471,73 @@ decode_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant__
         } else {
           prm.partial_o[(size_t(item.slot) * prm.num_qo_heads + hq) * HEAD_DIM + dd] = o;
           if (dd == 0) prm.partial_lse[size_t(item.slot) * prm.num_qo_heads + hq] = lse;
+        }
+      }
+      // Split request: the CTA that writes the last of its chunks' partial
+      // states (for this kv head) merges them, so no second launch is needed.
+      // Publication: the consumer threads' stores, a CTA barrier, then one
+      // thread's gpu-scope fence and arrival count; the thread that sees the
+      // final count fences before the CTA reads the other CTAs' states
+      // (bypassing L1). The merge order is fixed by the slots, so the result
+      // does not depend on which CTA comes last.
+      if (item.slot >= 0) {
+        named_bar_sync(1, C::NCW * 32);
+        if (tid == 0) {
+          const MergeTask mt = prm.merges[item.merge];
+          const int hkv = prm.num_qo_heads / GROUP;
+          __threadfence();
+          const uint32_t prev = atomicAdd(&prm.merge_counters[item.merge * hkv + item.head], 1u);
+          merge_last = prev == uint32_t(mt.n_states - 1);
+          if (merge_last) __threadfence();
+        }
+        named_bar_sync(1, C::NCW * 32);
+        if (merge_last) {
+          const MergeTask mt = prm.merges[item.merge];
+          // per head: M = max_i lse_i and w_i = exp(lse_i - M) / sum_j exp(lse_j - M),
+          // kept in shared memory (the reduction area is free again)
+          float* wgt = red_o;                       // [n_states][GROUP] when it fits
+          float* hm = red_m;                        // [GROUP]: M
+          float* hs = red_l;                        // [GROUP]: sum of exp(lse_i - M)
+          const bool fits = mt.n_states * GROUP <= C::NCW * GROUP * HEAD_DIM;
+          if (tid < GROUP) {
+            const int hq = item.head * GROUP + tid;
+            float M = -INFINITY;
+            for (int i = 0; i < mt.n_states; ++i)
+              M = fmaxf(M, __ldcg(&prm.partial_lse[size_t(mt.slot_base + i) * prm.num_qo_heads + hq]));
+            float sw = 0.f;
+            if (M != -INFINITY) {
+              for (int i = 0; i < mt.n_states; ++i) {
+                const float w = ex2((__ldcg(&prm.partial_lse[size_t(mt.slot_base + i) *
+                                                             prm.num_qo_heads + hq]) - M) * kLog2e);
+                if (fits) wgt[i * GROUP + tid] = w;   // -inf -> 0
+                sw += w;
+              }
+            } else if (fits) {
+              for (int i = 0; i < mt.n_states; ++i) wgt[i * GROUP + tid] = 0.f;
+            }
+            hm[tid] = M;
+            hs[tid] = sw;
+            const size_t orow = size_t(mt.out_row) * prm.num_qo_heads + hq;
+            if (prm.lse) prm.lse[orow] = sw > 0.f ? M + lg2(sw) * kLn2 : -INFINITY;
+          }
+          named_bar_sync(1, C::NCW * 32);
+          for (int idx = tid; idx < GROUP * HEAD_DIM; idx += C::NCW * 32) {
+            const int h = idx / HEAD_DIM, dd = idx % HEAD_DIM;
+            const int hq = item.head * GROUP + h;
+            const float M = hm[h], sw = hs[h];
+            float acc = 0.f;
+            if (sw > 0.f) {
+              for (int i = 0; i < mt.n_states; ++i) {
+                const size_t row = size_t(mt.slot_base + i) * prm.num_qo_heads + hq;
+                const float w = fits ? wgt[i * GROUP + h]
+                                     : ex2((__ldcg(&prm.partial_lse[row]) - M) * kLog2e);
+                acc = fmaf(w, __ldcg(&prm.partial_o[row * HEAD_DIM + dd]), acc);
+              }
+            }
+            const size_t orow = size_t(mt.out_row) * prm.num_qo_heads + hq;
+            reinterpret_cast<uint16_t*>(prm.out)[orow * HEAD_DIM + dd] =
+                E::one(sw > 0.f ? acc / sw : 0.f);
+          }
         }
       }
     }

@@ -14,11 +14,11 @@ namespace fi {
 // One CTA's work. Decode items: tokens [tok_begin, tok_end) of request
 // `req` for kv head `head` (all g query heads of its group), pages
 // page_indices[page_begin .. page_begin+n_pages), writing either the final
-// output row `q_row` (slot < 0) or partial-state slot `slot`. Prefill
-// items: query rows [q_row, q_row + rows) of request `req` (absolute rows of
-// q/out, at most kPrefillTileM) for query head `head`, over keys
-// [0, tok_end) — tok_end already clipped to the causal bound of the tile's
-// last row.
+// output row `q_row` (slot < 0) or partial-state slot `slot` of merge task
+// `merge`. Prefill items: query rows [q_row, q_row + rows) of request `req`
+// (absolute rows of q/out, at most kPrefillTileM) for query head `head`,
+// over keys [tok_begin, tok_end) — tok_end clipped to the causal bound of
+// the tile's last row, tok_begin to the page of its first row's window.
 struct WorkItem {
   int32_t req;
   int32_t head;
@@ -28,8 +28,9 @@ struct WorkItem {
   int32_t tok_end;
   int32_t slot;
   int32_t q_row;
+  int32_t merge;   // split decode work: index of its merge task; else -1
 };
-static_assert(sizeof(WorkItem) == 32, "work item is 8 int32");
+static_assert(sizeof(WorkItem) == 36, "work item is 9 int32");
 
 // A row whose decode work was split: merge states [slot_base, slot_base +
 // n_states) (each [num_qo_heads][head_dim] fp32) into output row out_row.
@@ -53,7 +54,8 @@ inline int decode_tile_tokens(int head_dim) { return 8192 / head_dim; }  // 32 K
 inline int prefill_kv_tile(int head_dim) { return head_dim <= 128 ? 128 : 64; }
 
 struct WorkspaceLayout {
-  size_t decode_items = 0, prefill_items = 0, merges = 0, partial_o = 0, partial_lse = 0;
+  size_t decode_items = 0, prefill_items = 0, merges = 0, merge_counters = 0, partial_o = 0,
+         partial_lse = 0;
   size_t total = 0;
 };
 
@@ -84,7 +86,4 @@ fi_status build_plan(int32_t mode, int32_t batch, const int32_t* qo_indptr,
 
 struct fi_plan_s {
   fi::Plan p;
-  // Host image of the workspace prefix (zeroed header, work lists, merge
-  // tasks), uploaded by every run call in one stream-ordered copy.
-  std::vector<uint8_t> image;
 };

@@ -23,6 +23,8 @@ struct DecodeParams {
   float* lse;
   float* partial_o;
   float* partial_lse;
+  const MergeTask* merges;    // split requests: slots and output row
+  uint32_t* merge_counters;   // [merge][kv head], zero at launch
   uint32_t* err;
   uint64_t wait_limit_ns;
   int32_t fault_kind;

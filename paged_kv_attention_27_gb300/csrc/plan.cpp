@@ -117,42 +117,62 @@ fi_status build_plan(int32_t mode, int32_t batch, const int32_t* qo_indptr,
     const int64_t chunk_tiles = std::max(min_chunk_tiles, ceil_div(dec_tiles, target));
     const int64_t chunk = chunk_tiles * tile;  // a multiple of the page size
     p.chunk_tokens = int32_t(std::min<int64_t>(chunk, INT32_MAX));
+    // Every kv head of a (request, chunk) gets an item of the same length,
+    // so the longest-first order is found by sorting the (request, chunk)
+    // groups, not the items.
+    struct Group { int64_t len; int32_t b, c; };
+    std::vector<Group> groups;
+    std::vector<int64_t> w0s(batch), s0s(batch);
+    std::vector<int32_t> slot_base(batch, -1), merge_of(batch, -1);
     for (int b : dec) {
       const int64_t w0 = first_key(b, 0);
       const int64_t s0 = w0 / page_size * page_size;
+      w0s[b] = w0;
+      s0s[b] = s0;
       const int64_t n_chunks = std::max<int64_t>(1, ceil_div(kv_len[b] - s0, chunk));
-      int32_t slot_base = -1;
       if (n_chunks > 1) {
-        slot_base = p.num_slots;
+        merge_of[b] = int32_t(p.merges.size());
+        slot_base[b] = p.num_slots;
         p.num_slots += int32_t(n_chunks);
         p.num_split += 1;
-        p.merges.push_back(MergeTask{int32_t(qo_start[b]), slot_base, int32_t(n_chunks), 0});
+        p.merges.push_back(MergeTask{int32_t(qo_start[b]), slot_base[b], int32_t(n_chunks), 0});
       }
-      for (int kh = 0; kh < num_kv_heads; ++kh) {
-        for (int64_t c = 0; c < n_chunks; ++c) {
-          const int64_t t0 = s0 + c * chunk;     // page-aligned start of the chunk
-          const int64_t t1 = std::min<int64_t>(kv_len[b], t0 + chunk);
-          WorkItem w;
-          w.req = b;
-          w.head = kh;
-          w.page_begin = int32_t(page_indptr[b] + t0 / page_size);
-          w.n_pages = int32_t(t1 > t0 ? ceil_div(t1 - t0, page_size) : 0);
-          w.tok_begin = int32_t(c == 0 ? w0 : t0);   // first visible key
-          w.tok_end = int32_t(std::max(t0, t1));
-          w.slot = n_chunks > 1 ? int32_t(slot_base + c) : -1;
-          w.q_row = int32_t(qo_start[b]);
-          p.decode_items.push_back(w);
-        }
+      for (int64_t c = 0; c < n_chunks; ++c) {
+        const int64_t t0 = s0 + c * chunk;
+        const int64_t t1 = std::min<int64_t>(kv_len[b], t0 + chunk);
+        groups.push_back(Group{std::max<int64_t>(0, t1 - (c == 0 ? w0 : t0)), b, int32_t(c)});
       }
     }
-    std::stable_sort(p.decode_items.begin(), p.decode_items.end(),
-                     [](const WorkItem& a, const WorkItem& b) {
-                       return (a.tok_end - a.tok_begin) > (b.tok_end - b.tok_begin);
-                     });
+    std::sort(groups.begin(), groups.end(), [](const Group& x, const Group& y) {
+      if (x.len != y.len) return x.len > y.len;
+      return x.b != y.b ? x.b < y.b : x.c < y.c;
+    });
+    p.decode_items.reserve(groups.size() * size_t(num_kv_heads));
+    for (const Group& g : groups) {
+      const int b = g.b;
+      const int64_t t0 = s0s[b] + int64_t(g.c) * chunk;   // page-aligned start of the chunk
+      const int64_t t1 = std::min<int64_t>(kv_len[b], t0 + chunk);
+      WorkItem w;
+      w.req = b;
+      w.page_begin = int32_t(page_indptr[b] + t0 / page_size);
+      w.n_pages = int32_t(t1 > t0 ? ceil_div(t1 - t0, page_size) : 0);
+      w.tok_begin = int32_t(g.c == 0 ? w0s[b] : t0);     // first visible key
+      w.tok_end = int32_t(std::max(t0, t1));
+      w.slot = slot_base[b] >= 0 ? slot_base[b] + g.c : -1;
+      w.q_row = int32_t(qo_start[b]);
+      w.merge = merge_of[b];
+      for (int kh = 0; kh < num_kv_heads; ++kh) {
+        w.head = kh;
+        p.decode_items.push_back(w);
+      }
+    }
   }
 
   // ---- prefill work: requests with two or more query rows, one item per
-  //      (query tile of kPrefillTileM rows, query head)
+  //      (query tile of kPrefillTileM rows, query head); the tiles are
+  //      ordered longest first, the heads of a tile stay together
+  struct Tile { int64_t len, kv_begin, kv_end; int32_t b, qt; };
+  std::vector<Tile> tiles;
   for (int b = 0; b < batch; ++b) {
     if (qo_len[b] < 2) continue;
     const int64_t n_qt = ceil_div(qo_len[b], kPrefillTileM);
@@ -164,26 +184,32 @@ fi_status build_plan(int32_t mode, int32_t batch, const int32_t* qo_indptr,
       // the tile's first row has the smallest window start; tiles of keys
       // begin on the page that holds it
       const int64_t kv_begin = std::min(kv_end, first_key(b, r0)) / page_size * page_size;
-      for (int h = 0; h < num_qo_heads; ++h) {
-        WorkItem w;
-        w.req = b;
-        w.head = h;
-        w.page_begin = int32_t(page_indptr[b] + kv_begin / page_size);
-        w.n_pages = int32_t(ceil_div(kv_end - kv_begin, page_size));
-        w.tok_begin = int32_t(kv_begin);
-        w.tok_end = int32_t(kv_end);
-        w.slot = -1;
-        w.q_row = int32_t(qo_start[b] + r0);
-        p.prefill_items.push_back(w);
-      }
+      tiles.push_back(Tile{kv_end - kv_begin, kv_begin, kv_end, b, int32_t(qt)});
     }
   }
-  std::stable_sort(p.prefill_items.begin(), p.prefill_items.end(),
-                   [](const WorkItem& a, const WorkItem& b) {
-                     return (a.tok_end - a.tok_begin) > (b.tok_end - b.tok_begin);
-                   });
+  std::sort(tiles.begin(), tiles.end(), [](const Tile& x, const Tile& y) {
+    if (x.len != y.len) return x.len > y.len;
+    return x.b != y.b ? x.b < y.b : x.qt < y.qt;
+  });
+  p.prefill_items.reserve(tiles.size() * size_t(num_qo_heads));
+  for (const Tile& t : tiles) {
+    WorkItem w;
+    w.req = t.b;
+    w.page_begin = int32_t(page_indptr[t.b] + t.kv_begin / page_size);
+    w.n_pages = int32_t(ceil_div(t.kv_end - t.kv_begin, page_size));
+    w.tok_begin = int32_t(t.kv_begin);
+    w.tok_end = int32_t(t.kv_end);
+    w.slot = -1;
+    w.q_row = int32_t(qo_start[t.b] + int64_t(t.qt) * kPrefillTileM);
+    w.merge = -1;
+    for (int h = 0; h < num_qo_heads; ++h) {
+      w.head = h;
+      p.prefill_items.push_back(w);
+    }
+  }
 
-  // ---- workspace: header | decode items | prefill items | merges | partial o | partial lse
+  // ---- workspace: header | decode items | prefill items | merges | merge counters |
+  //      partial o | partial lse
   size_t off = kHeaderBytes;
   p.ws.decode_items = off;
   off = align_up(off + p.decode_items.size() * sizeof(WorkItem));
@@ -191,6 +217,10 @@ fi_status build_plan(int32_t mode, int32_t batch, const int32_t* qo_indptr,
   off = align_up(off + p.prefill_items.size() * sizeof(WorkItem));
   p.ws.merges = off;
   off = align_up(off + p.merges.size() * sizeof(MergeTask));
+  // one arrival counter per (merge task, kv head), zero at the start of a
+  // run: the CTA that completes a split's last chunk merges it
+  p.ws.merge_counters = off;
+  off = align_up(off + p.merges.size() * size_t(num_kv_heads) * sizeof(uint32_t));
   p.ws.partial_o = off;
   off = align_up(off + size_t(p.num_slots) * num_qo_heads * head_dim * sizeof(float));
   p.ws.partial_lse = off;
