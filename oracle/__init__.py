@@ -6,7 +6,8 @@ shares no code with the CUDA path. Every function cites the passage of the
 source pages it restates; see ``oracle.attention``.
 """
 from .attention import (  # noqa: F401
-    HND, NHD, batch_attention, batch_decode, bf16_to_f64, causal_mask, f16_to_f64, gather_kv,
+    HND, NHD, batch_attention, batch_decode, bf16_to_f64, causal_mask, e4m3_to_f64, f16_to_f64,
+    gather_kv,
     kv_lengths, masked_attention, merge_states, online_softmax_attention,
     softmax_attention, split_kv_states, to_f64, visible_keys,
 )

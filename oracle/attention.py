@@ -67,12 +67,29 @@ def f16_to_f64(bits: np.ndarray) -> np.ndarray:
     return np.where(e == 0, sub, np.where(e == 31, special, normal))
 
 
+def e4m3_to_f64(bits: np.ndarray) -> np.ndarray:
+    """Exact value of FP8 E4M3 bit patterns (uint8) as float64, from the OCP
+    8-bit floating-point definition: sign bit, 4 exponent bits (bias 7), 3
+    fraction bits; exponent 0 is subnormal (2^-6 * f/8); no infinities, and
+    exponent 15 with fraction 7 is NaN (largest finite value 448)."""
+    b = np.asarray(bits, dtype=np.uint8).astype(np.int64)
+    sign = np.where(b >> 7, -1.0, 1.0)
+    e = (b >> 3) & 0xF
+    f = (b & 0x7).astype(np.float64)
+    normal = sign * np.ldexp(1.0 + f / 8.0, (e - 7).astype(np.int32))
+    sub = sign * np.ldexp(f / 8.0, -6)
+    val = np.where(e == 0, sub, normal)
+    return np.where((e == 15) & (f == 7), np.nan, val)
+
+
 def to_f64(bits: np.ndarray, dtype: str) -> np.ndarray:
-    """Exact value of bf16 or fp16 bit patterns as float64."""
+    """Exact value of bf16, fp16 or e4m3 bit patterns as float64."""
     if dtype == "bf16":
         return bf16_to_f64(bits)
     if dtype == "fp16":
         return f16_to_f64(bits)
+    if dtype == "e4m3":
+        return e4m3_to_f64(bits)
     raise ValueError(dtype)
 
 
@@ -153,11 +170,15 @@ def softmax_attention(q: np.ndarray, k: np.ndarray, v: np.ndarray, sm_scale: flo
 def batch_attention(q_bits, qo_indptr, k_cache_bits, v_cache_bits, layout: str,
                     page_indptr, page_indices, last_page_len, num_qo_heads: int,
                     num_kv_heads: int, page_size: int, sm_scale: float, causal: bool,
-                    requests=None, rows=None, window_left: int = -1, dtype: str = "bf16"):
+                    requests=None, rows=None, window_left: int = -1, dtype: str = "bf16",
+                    kv_dtype: str | None = None, k_scale: float = 1.0, v_scale: float = 1.0):
     """Paged attention for a packed batch.
 
     q_bits ``[sum qo_len, Hq, d]`` bit patterns of ``dtype`` ("bf16" or
-    "fp16", as are the caches); caches as laid out by ``layout``.
+    "fp16"); caches as laid out by ``layout``, of ``kv_dtype`` (default:
+    ``dtype``; "e4m3" for an FP8 cache). A quantised cache holds K / k_scale
+    and V / v_scale: the keys and values attended to are ``k_scale`` and
+    ``v_scale`` times the stored ones.
     Returns ``out [sum qo_len, Hq, d]`` and ``lse [sum qo_len, Hq]`` in
     float64. ``requests`` limits the work to some requests (other rows stay
     NaN); ``rows`` maps a request to the list of its row indices to compute
@@ -181,10 +202,10 @@ def batch_attention(q_bits, qo_indptr, k_cache_bits, v_cache_bits, layout: str,
         sel = np.arange(qo_len) if rows is None or b not in rows else np.asarray(rows[b])
         vis = visible_keys(qo_len, int(kv_len[b]), causal, window_left)[sel]
         for kh in range(num_kv_heads):
-            k = gather_kv(k_cache_bits, layout, page_indptr, page_indices, b, kh,
-                          int(kv_len[b]), page_size, dtype)
-            v = gather_kv(v_cache_bits, layout, page_indptr, page_indices, b, kh,
-                          int(kv_len[b]), page_size, dtype)
+            k = k_scale * gather_kv(k_cache_bits, layout, page_indptr, page_indices, b, kh,
+                                    int(kv_len[b]), page_size, kv_dtype or dtype)
+            v = v_scale * gather_kv(v_cache_bits, layout, page_indptr, page_indices, b, kh,
+                                    int(kv_len[b]), page_size, kv_dtype or dtype)
             for h in range(kh * group, (kh + 1) * group):
                 qh = to_f64(q_bits[q0 + sel, h, :], dtype)
                 o, l = softmax_attention(qh, k, v, sm_scale, vis)
@@ -196,7 +217,8 @@ def batch_attention(q_bits, qo_indptr, k_cache_bits, v_cache_bits, layout: str,
 def batch_decode(q_bits, k_cache_bits, v_cache_bits, layout: str, page_indptr,
                  page_indices, last_page_len, num_qo_heads: int, num_kv_heads: int,
                  page_size: int, sm_scale: float, requests=None, window_left: int = -1,
-                 dtype: str = "bf16"):
+                 dtype: str = "bf16", kv_dtype: str | None = None, k_scale: float = 1.0,
+                 v_scale: float = 1.0):
     """One query token per request: q_bits ``[B, Hq, d]``; out ``[B, Hq, d]``,
     lse ``[B, Hq]``. Every key of the request is visible, or with a left
     window only the last ``window_left + 1``."""
@@ -204,7 +226,8 @@ def batch_decode(q_bits, k_cache_bits, v_cache_bits, layout: str, page_indptr,
     return batch_attention(q_bits, np.arange(B + 1), k_cache_bits, v_cache_bits, layout,
                            page_indptr, page_indices, last_page_len, num_qo_heads,
                            num_kv_heads, page_size, sm_scale, False, requests=requests,
-                           window_left=window_left, dtype=dtype)
+                           window_left=window_left, dtype=dtype, kv_dtype=kv_dtype,
+                           k_scale=k_scale, v_scale=v_scale)
 
 
 # --------------------------------------------------------------------------

@@ -60,23 +60,52 @@ def f32_to_f16_bits(x: np.ndarray) -> np.ndarray:
     return np.ascontiguousarray(x, dtype=np.float32).astype(np.float16).view(np.uint16)
 
 
+def _e4m3_grid() -> np.ndarray:
+    """The 127 non-negative finite FP8 E4M3 values, indexed by their code
+    (0x00..0x7E): 2^-6 * m/8 for exponent field 0, 2^(e-7) * (1 + m/8) else."""
+    codes = np.arange(127)
+    e, m = codes >> 3, codes & 7
+    return np.where(e == 0, m / 8.0 * 2.0 ** -6, (1 + m / 8.0) * 2.0 ** (e - 7.0))
+
+
+_E4M3 = _e4m3_grid()
+
+
+def f32_to_e4m3_bits(x: np.ndarray) -> np.ndarray:
+    """Round float32 values to FP8 E4M3 (nearest, ties to the even code),
+    saturating at +-448; NaN becomes 0x7F. Returns uint8 codes."""
+    x = np.asarray(x, dtype=np.float64)
+    a = np.minimum(np.abs(x), 448.0)
+    hi = np.clip(np.searchsorted(_E4M3, a, side="left"), 1, 126)   # _E4M3[hi-1] < a <= _E4M3[hi]
+    lo = hi - 1
+    dlo, dhi = a - _E4M3[lo], _E4M3[hi] - a
+    code = np.where(dlo < dhi, lo, np.where(dhi < dlo, hi, np.where(lo % 2 == 0, lo, hi)))
+    code = np.where(a <= 0, 0, code)
+    out = (code | np.where(np.signbit(x), 0x80, 0)).astype(np.uint8)
+    out[np.isnan(x)] = 0x7F
+    return out
+
+
 def to_bits(x: np.ndarray, dtype: str) -> np.ndarray:
     """float32 values -> bit patterns of ``dtype`` ("bf16" or "fp16")."""
     if dtype == "bf16":
         return f32_to_bf16_bits(x)
     if dtype == "fp16":
         return f32_to_f16_bits(x)
+    if dtype == "e4m3":
+        return f32_to_e4m3_bits(x)
     raise ValueError(dtype)
 
 
-QNAN_BITS = {"bf16": 0x7FC0, "fp16": 0x7E00}
+QNAN_BITS = {"bf16": 0x7FC0, "fp16": 0x7E00, "e4m3": 0x7F}
 
 _CHUNK = 1 << 22
 
 
-def normal_bf16(seed: int, stream: int, shape, dtype: str = "bf16") -> np.ndarray:
-    """Standard normal values of ``shape`` as bit patterns (uint16) of
-    ``dtype`` (bf16 by default, or fp16).
+def normal_bf16(seed: int, stream: int, shape, dtype: str = "bf16",
+                scale: float = 1.0) -> np.ndarray:
+    """Standard normal values (times ``scale``) of ``shape`` as bit patterns
+    of ``dtype``: bf16 (default) or fp16 as uint16, e4m3 as uint8.
 
     Element block j (of 2^22 elements) is drawn from its own Philox stream
     keyed by (seed, stream, j), so the values do not depend on how many
@@ -85,13 +114,14 @@ def normal_bf16(seed: int, stream: int, shape, dtype: str = "bf16") -> np.ndarra
     import concurrent.futures as cf
     import os
     n = int(np.prod(shape, dtype=np.int64))
-    out = np.empty(n, dtype=np.uint16)
+    out = np.empty(n, dtype=np.uint8 if dtype == "e4m3" else np.uint16)
 
     def fill(j):
         s = j * _CHUNK
         c = min(_CHUNK, n - s)
         g = np.random.Generator(np.random.Philox(key=[int(seed) * 64 + int(stream), j]))
-        out[s:s + c] = to_bits(g.standard_normal(c, dtype=np.float32), dtype)
+        x = g.standard_normal(c, dtype=np.float32)
+        out[s:s + c] = to_bits(x * np.float32(scale) if scale != 1.0 else x, dtype)
 
     blocks = range((n + _CHUNK - 1) // _CHUNK)
     with cf.ThreadPoolExecutor(max_workers=min(32, os.cpu_count() or 1)) as ex:
@@ -123,7 +153,14 @@ class PagedBatch:
     shared_prefix_pages: int = 0
     meta: dict = field(default_factory=dict)
     window_left: int = -1        # left attention window (-1 = unbounded)
-    dtype: str = "bf16"          # element type of q, K, V ("bf16" or "fp16")
+    dtype: str = "bf16"          # element type of q and out ("bf16" or "fp16")
+    kv_dtype: str = ""           # element type of the caches ("" = dtype; "e4m3")
+    k_scale: float = 1.0         # attended keys / values = scale * stored ones
+    v_scale: float = 1.0
+
+    @property
+    def cache_dtype(self) -> str:
+        return self.kv_dtype or self.dtype
 
     @property
     def batch(self) -> int:
@@ -143,7 +180,7 @@ def make_batch(name: str, kv_lens, qo_lens, num_qo_heads: int, num_kv_heads: int
                causal: bool, seed: int, shared_prefix_requests: int = 0,
                shared_prefix_tokens: int = 0, tail_fill: str = "normal",
                extra_pages: int = 0, window_left: int = -1,
-               dtype: str = "bf16") -> PagedBatch:
+               dtype: str = "bf16", kv_dtype: str = "", kv_scale: float = 1.0) -> PagedBatch:
     """Build a paged batch with seeded values and a shuffled page table.
 
     ``shared_prefix_requests`` requests (the first ones) map their first
@@ -188,8 +225,10 @@ def make_batch(name: str, kv_lens, qo_lens, num_qo_heads: int, num_kv_heads: int
 
     Hkv, d = num_kv_heads, head_dim
     shape = (num_phys, P, Hkv, d) if layout == NHD else (num_phys, Hkv, P, d)
-    k_cache = normal_bf16(seed, 1, shape, dtype)
-    v_cache = normal_bf16(seed, 2, shape, dtype)
+    # an FP8 cache stores the draws divided by the per-tensor scale
+    cdt = kv_dtype or dtype
+    k_cache = normal_bf16(seed, 1, shape, cdt, 1.0 / kv_scale)
+    v_cache = normal_bf16(seed, 2, shape, cdt, 1.0 / kv_scale)
     q = normal_bf16(seed, 3, (int(qo_lens.sum()), num_qo_heads, d), dtype)
     if tail_fill == "nan":
         for b in range(B):
@@ -198,9 +237,9 @@ def make_batch(name: str, kv_lens, qo_lens, num_qo_heads: int, num_kv_heads: int
             p = page_lists[b][-1]
             for cache in (k_cache, v_cache):
                 if layout == NHD:
-                    cache[p, last[b]:, :, :] = QNAN_BITS[dtype]
+                    cache[p, last[b]:, :, :] = QNAN_BITS[cdt]
                 else:
-                    cache[p, :, last[b]:, :] = QNAN_BITS[dtype]
+                    cache[p, :, last[b]:, :] = QNAN_BITS[cdt]
     if sm_scale is None:
         sm_scale = 1.0 / math.sqrt(head_dim)
     return PagedBatch(name=name, num_qo_heads=num_qo_heads, num_kv_heads=num_kv_heads,
@@ -210,7 +249,8 @@ def make_batch(name: str, kv_lens, qo_lens, num_qo_heads: int, num_kv_heads: int
                       last_page_len=last.astype(np.int32), q=q, k_cache=k_cache, v_cache=v_cache,
                       shared_prefix_pages=int(prefix_pages),
                       meta={"seed": seed, "shared_prefix_requests": shared_prefix_requests},
-                      window_left=int(window_left), dtype=dtype)
+                      window_left=int(window_left), dtype=dtype, kv_dtype=kv_dtype,
+                      k_scale=float(kv_scale), v_scale=float(kv_scale))
 
 
 # ----------------------------------------------------------------------------
@@ -332,4 +372,5 @@ def sub_batch(src: PagedBatch, requests) -> PagedBatch:
                       page_indices=page_indices, last_page_len=src.last_page_len[requests].copy(),
                       q=q, k_cache=src.k_cache[idx], v_cache=src.v_cache[idx],
                       meta=dict(src.meta, sample=requests), window_left=src.window_left,
-                      dtype=src.dtype)
+                      dtype=src.dtype, kv_dtype=src.kv_dtype, k_scale=src.k_scale,
+                      v_scale=src.v_scale)

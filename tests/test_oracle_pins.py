@@ -112,6 +112,67 @@ def test_fp16_inputs_match_torch_sdpa_float64():
     assert not np.array_equal(o16, out) and np.abs(o16 - out).max() < 0.05
 
 
+def test_e4m3_bit_patterns():
+    """Hand-decoded OCP FP8 E4M3 values, then all 256 patterns against
+    torch's float8_e4m3fn (an independent decoder)."""
+    bits = np.array([0x38, 0xB8, 0x7E, 0x01, 0x07, 0x08, 0x3C, 0x7F, 0xFF, 0x00, 0x80], np.uint8)
+    want = [1.0, -1.0, 448.0, 2.0 ** -9, 7 * 2.0 ** -9, 2.0 ** -6, 1.5, math.nan, math.nan,
+            0.0, -0.0]
+    got = oracle.e4m3_to_f64(bits)
+    for g, w in zip(got, want):
+        assert (math.isnan(g) and math.isnan(w)) or g == w
+    assert math.copysign(1.0, got[-1]) == -1.0
+    torch = pytest.importorskip("torch")
+    if not hasattr(torch, "float8_e4m3fn"):
+        pytest.skip("torch without float8_e4m3fn")
+    allb = np.arange(256, dtype=np.uint8)
+    ref = torch.from_numpy(allb).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    mine = oracle.e4m3_to_f64(allb)
+    assert ((mine == ref) | (np.isnan(mine) & np.isnan(ref))).all()
+
+
+def test_kv_scales_fold_into_the_score_scale_and_the_output():
+    """k_scale multiplies every score, so it is the same as multiplying
+    sm_scale; v_scale multiplies the output and leaves lse unchanged."""
+    b = synth.make_batch("fp8", [70, 130, 1], [1, 1, 1], 8, 2, 64, 16, synth.NHD, 0.125, False,
+                         24, kv_dtype="e4m3")
+    o1, l1 = _run(b)
+    b.k_scale = 0.5
+    o2, l2 = _run(b)
+    b.k_scale, b.sm_scale = 1.0, 0.0625
+    o3, l3 = _run(b)
+    np.testing.assert_allclose(o2, o3, rtol=0, atol=1e-13)
+    np.testing.assert_allclose(l2, l3, rtol=0, atol=1e-13)
+    assert np.abs(o1 - o2).max() > 1e-3                     # the scale matters
+    b.sm_scale, b.v_scale = 0.125, 0.25
+    o4, l4 = _run(b)
+    np.testing.assert_allclose(o4, 0.25 * o1, rtol=0, atol=1e-15)
+    np.testing.assert_array_equal(l4, l1)
+
+
+def test_fp8_cache_matches_torch_sdpa_float64():
+    torch = pytest.importorskip("torch")
+    if not hasattr(torch, "float8_e4m3fn"):
+        pytest.skip("torch without float8_e4m3fn")
+    b = synth.make_batch("fp8 sdpa", [45, 300], [1, 1], 8, 2, 32, 16, synth.HND, None, False, 25,
+                         kv_dtype="e4m3", kv_scale=1 / 16)
+    assert b.k_cache.dtype == np.uint8 and b.k_scale == 1 / 16
+    out, lse = _run(b)
+    g = b.num_qo_heads // b.num_kv_heads
+    for r in range(b.batch):
+        kv = int(b.kv_lens[r])
+        pages = b.page_indices[int(b.page_indptr[r]):int(b.page_indptr[r + 1])]
+        dec = lambda x: torch.from_numpy(np.ascontiguousarray(x)).view(torch.float8_e4m3fn).to(
+            torch.float64)
+        kt = dec(np.concatenate([b.k_cache[p] for p in pages], axis=1)[:, :kv]) * b.k_scale
+        vt = dec(np.concatenate([b.v_cache[p] for p in pages], axis=1)[:, :kv]) * b.v_scale
+        qt = torch.from_numpy(b.q[r:r + 1].view(np.int16)).view(torch.bfloat16).to(
+            torch.float64).transpose(0, 1)                               # [Hq, 1, d]
+        kt, vt = kt.repeat_interleave(g, 0), vt.repeat_interleave(g, 0)
+        so = torch.nn.functional.scaled_dot_product_attention(qt, kt, vt, scale=b.sm_scale)
+        np.testing.assert_allclose(out[r], so[:, 0].numpy(), rtol=0, atol=1e-12)
+
+
 def test_kv_lengths_of_tiny_config():
     b = synth.tiny_decode()
     # pages {1,2,4,7}, last page lengths {1,1,16,4} for KV lengths {1,17,64,100}
@@ -248,7 +309,8 @@ def _run(b, requests=None):
     return oracle.batch_attention(b.q, b.qo_indptr, b.k_cache, b.v_cache, b.layout, b.page_indptr,
                                   b.page_indices, b.last_page_len, b.num_qo_heads, b.num_kv_heads,
                                   b.page_size, b.sm_scale, b.causal, requests=requests,
-                                  window_left=b.window_left, dtype=b.dtype)
+                                  window_left=b.window_left, dtype=b.dtype,
+                                  kv_dtype=b.cache_dtype, k_scale=b.k_scale, v_scale=b.v_scale)
 
 
 def test_permuting_physical_pages_changes_nothing():
