@@ -77,6 +77,8 @@ WORKLOADS = {
     "causal_prefill_16k_window4k": ("causal_prefill", {"seq_len": 16384, "window_left": 4095}),
     "causal_prefill_4k_fp16": ("causal_prefill", {"seq_len": 4096, "dtype": "fp16"}),
     "llama7b_decode_fp16": ("llama7b_decode", {"dtype": "fp16"}),
+    "llama7b_decode_fp8kv": ("llama7b_decode", {"kv_dtype": "e4m3"}),
+    "llama70b_gqa_decode_fp8kv": ("llama70b_gqa_decode", {"kv_dtype": "e4m3"}),
     "ragged_prefill": ("ragged_prefill", {}),
     "mixed_chunk_decode": ("mixed_chunk_decode", {}),
 }
@@ -110,6 +112,10 @@ def attention_flops(b):
     return 4 * b.head_dim * b.num_qo_heads * visible_pairs(b)
 
 
+def cache_elem_bytes(b):
+    return 1 if b.cache_dtype == "e4m3" else 2
+
+
 def kv_bytes(b):
     """K+V bytes a pass reads: the rows of K and V that some query row of a
     request may see (all kv_len of them without a left window), for every
@@ -121,7 +127,7 @@ def kv_bytes(b):
         lo = int(b.page_indptr[r])
         for t in range(first, kv):
             seen.add((int(b.page_indices[lo + t // b.page_size]), t % b.page_size))
-    return len(seen) * 2 * b.num_kv_heads * b.head_dim * 2
+    return len(seen) * 2 * b.num_kv_heads * b.head_dim * cache_elem_bytes(b)
 
 
 def io_bytes(b):
@@ -237,7 +243,8 @@ def oracle_sample(b, budget_s=12.0, threads=None):
         oracle.batch_attention(b.q, b.qo_indptr, b.k_cache, b.v_cache, b.layout, b.page_indptr,
                                b.page_indices, b.last_page_len, b.num_qo_heads, b.num_kv_heads,
                                b.page_size, b.sm_scale, b.causal, requests=[r],
-                               window_left=b.window_left)
+                               window_left=b.window_left, dtype=b.dtype,
+                               kv_dtype=b.cache_dtype, k_scale=b.k_scale, v_scale=b.v_scale)
         return r
 
     done = []
@@ -257,7 +264,7 @@ def oracle_sample(b, budget_s=12.0, threads=None):
     dt = time.perf_counter() - t0
     w = b.window_left
     keys = [int(b.kv_lens[r]) if w < 0 else min(int(b.kv_lens[r]), w + 1) for r in done]
-    kvb = sum(keys) * 2 * b.num_kv_heads * b.head_dim * 2
+    kvb = sum(keys) * 2 * b.num_kv_heads * b.head_dim * cache_elem_bytes(b)
     return kvb / dt / 1e9, dt, threads, sorted(done)
 
 
@@ -459,8 +466,9 @@ def run_ours(args, rank, world, local_rank):
     line = {
         "metric": METRIC, "value": value, "unit": unit, "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": b.dtype,
-        "data": f"synthetic (seeded Philox normals rounded to {b.dtype}, shuffled page table)",
+        "scaling": "weak", "vs_baseline": None,
+        "dtype": b.dtype if b.cache_dtype == b.dtype else f"{b.dtype} (cache {b.cache_dtype})",
+        "data": f"synthetic (seeded Philox normals rounded to {b.cache_dtype}, shuffled page table)",
         "config": config_of(b, info, kvb, flops),
         "roofline": roofline_of(b, kvb, flops, kern_ms, kernels_of(b, info), args.workload),
         "tflops": flops * world / (ms_step / 1e3) / 1e12,
@@ -523,7 +531,8 @@ def oracle_rows_sample(b, budget_s=12.0):
         oracle.batch_attention(b.q, b.qo_indptr, b.k_cache, b.v_cache, b.layout, b.page_indptr,
                                b.page_indices, b.last_page_len, b.num_qo_heads, b.num_kv_heads,
                                b.page_size, b.sm_scale, b.causal, requests=[r], rows={r: [i]},
-                               window_left=b.window_left)
+                               window_left=b.window_left, dtype=b.dtype,
+                               kv_dtype=b.cache_dtype, k_scale=b.k_scale, v_scale=b.v_scale)
         qo, kv = int(b.qo_lens[r]), int(b.kv_lens[r])
         pos = kv - qo + i
         hi = min(kv - 1, pos) if b.causal else kv - 1
@@ -591,12 +600,14 @@ def run_e2e(b, db, K, local_rank, unit):
         if decode:
             B.fi_batch_decode_paged(plan, db.q, db.k, db.v, layout, 0, b.num_pages,
                                     db.page_indptr, db.page_indices, db.last_page_len,
-                                    b.sm_scale, db.out, db.lse, db.workspace)
+                                    b.sm_scale, b.k_scale, b.v_scale, db.out, db.lse,
+                                    db.workspace)
         else:
             db.qo_indptr.copy_(qo_h, non_blocking=True)
             B.fi_batch_prefill_paged(plan, db.q, db.qo_indptr, db.k, db.v, layout, 0,
                                      b.num_pages, db.page_indptr, db.page_indices,
-                                     db.last_page_len, b.sm_scale, db.out, db.lse, db.workspace)
+                                     db.last_page_len, b.sm_scale, b.k_scale, b.v_scale, db.out,
+                                     db.lse, db.workspace)
         out_h.copy_(db.out, non_blocking=True)
         lse_h.copy_(db.lse, non_blocking=True)
         torch.cuda.current_stream().synchronize()

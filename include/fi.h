@@ -80,8 +80,10 @@ typedef enum {
 typedef enum { FI_LAYOUT_NHD = 0, FI_LAYOUT_HND = 1 } fi_kv_layout;
 typedef enum { FI_MODE_DECODE = 0, FI_MODE_PREFILL = 1 } fi_mode;
 
-/* Element type of q, K, V and out (lse and partial states are fp32). */
-typedef enum { FI_DTYPE_BF16 = 0, FI_DTYPE_FP16 = 1 } fi_dtype;
+/* Element types: q and out are bf16 or fp16; the K/V cache is the same type
+ * or FP8 E4M3 (OCP format; decode plans only). lse and partial states are
+ * fp32. */
+typedef enum { FI_DTYPE_BF16 = 0, FI_DTYPE_FP16 = 1, FI_DTYPE_E4M3 = 2 } fi_dtype;
 
 /*
  * Options of a plan. Start from FI_PLAN_OPTIONS_DEFAULT (a zero-filled
@@ -93,14 +95,19 @@ typedef enum { FI_DTYPE_BF16 = 0, FI_DTYPE_FP16 = 1 } fi_dtype;
  *                loses every key t < pos - window_left, so a causal row sees
  *                at most window_left + 1 keys (a decode row: the last
  *                window_left + 1). The right side is set by `causal`.
- *   dtype        fi_dtype of q, K, V and out.
+ *   dtype        fi_dtype of q and out (FI_DTYPE_BF16 or FI_DTYPE_FP16).
+ *   kv_dtype     fi_dtype of the K/V cache: -1 = dtype, or FI_DTYPE_E4M3 for
+ *                an FP8 cache (decode plans only; FI_ERR_UNSUPPORTED for
+ *                prefill plans). An FP8 cache holds K / k_scale and
+ *                V / v_scale; the run calls take the two scales.
  */
 typedef struct {
   int32_t window_left;
   int32_t dtype;
+  int32_t kv_dtype;
 } fi_plan_options;
 
-#define FI_PLAN_OPTIONS_DEFAULT {-1, FI_DTYPE_BF16}
+#define FI_PLAN_OPTIONS_DEFAULT {-1, FI_DTYPE_BF16, -1}
 
 typedef struct fi_plan_s* fi_plan_t;
 
@@ -194,6 +201,14 @@ fi_status fi_plan_get_work(fi_plan_t plan, int32_t* items_h, int32_t capacity,
  *                    the planned page table.
  *   sm_scale         score scale, finite and >= 0 (1/sqrt(head_dim) is the
  *                    usual value); anything else is FI_ERR_INVALID_ARG.
+ *   k_scale, v_scale dequantisation scales of the cache, finite and > 0:
+ *                    the keys and values attended to are k_scale and v_scale
+ *                    times the stored ones (1 for a bf16/fp16 cache). k_scale
+ *                    is folded into the score scale, v_scale into the output
+ *                    (the FP8 scale handling the "FlashAttention-3 kernel
+ *                    integration in inference engines" page describes in
+ *                    section 1: the quantisation scale fused with the softmax
+ *                    scaling instead of extra conversion passes).
  *   out              device [B][num_qo_heads][head_dim], the plan's dtype.
  *   lse              device fp32 [B][num_qo_heads] or NULL.
  *   workspace        device buffer of at least the planned size, 256-byte
@@ -213,9 +228,9 @@ fi_status fi_batch_decode_paged(fi_plan_t plan, const void* q, const void* k_cac
                                 const void* v_cache, int32_t kv_layout,
                                 int64_t page_stride_elems, int32_t num_pages,
                                 const int32_t* page_indptr_d, const int32_t* page_indices_d,
-                                const int32_t* last_page_len_d, float sm_scale, void* out,
-                                float* lse, void* workspace, size_t workspace_bytes,
-                                void* stream);
+                                const int32_t* last_page_len_d, float sm_scale, float k_scale,
+                                float v_scale, void* out, float* lse, void* workspace,
+                                size_t workspace_bytes, void* stream);
 
 /*
  * fi_batch_decode_paged_noalloc — fi_batch_decode_paged without a workspace
@@ -243,7 +258,8 @@ fi_status fi_batch_decode_paged_noalloc(fi_plan_t plan, const void* q, const voi
                                         const int32_t* page_indptr_d,
                                         const int32_t* page_indices_d,
                                         const int32_t* last_page_len_d, float sm_scale,
-                                        void* out, float* lse, void* stream);
+                                        float k_scale, float v_scale, void* out, float* lse,
+                                        void* stream);
 
 /*
  * fi_batch_prefill_paged — causal (or full) variable-length batch prefill
@@ -264,9 +280,9 @@ fi_status fi_batch_prefill_paged(fi_plan_t plan, const void* q, const int32_t* q
                                  const void* k_cache, const void* v_cache, int32_t kv_layout,
                                  int64_t page_stride_elems, int32_t num_pages,
                                  const int32_t* page_indptr_d, const int32_t* page_indices_d,
-                                 const int32_t* last_page_len_d, float sm_scale, void* out,
-                                 float* lse, void* workspace, size_t workspace_bytes,
-                                 void* stream);
+                                 const int32_t* last_page_len_d, float sm_scale, float k_scale,
+                                 float v_scale, void* out, float* lse, void* workspace,
+                                 size_t workspace_bytes, void* stream);
 
 /*
  * fi_merge_states — combine attention states computed over disjoint key

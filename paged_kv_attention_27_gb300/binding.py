@@ -27,6 +27,7 @@ FI_ERR_NO_DEVICE = 7
 
 FI_DTYPE_BF16 = 0
 FI_DTYPE_FP16 = 1
+FI_DTYPE_E4M3 = 2
 
 FI_LAYOUT_NHD = 0
 FI_LAYOUT_HND = 1
@@ -52,8 +53,10 @@ class FiError(RuntimeError):
 
 
 class PlanOptions(ctypes.Structure):
-    """fi_plan_options: window_left (-1 = none) and dtype (FI_DTYPE_*)."""
-    _fields_ = [("window_left", ctypes.c_int32), ("dtype", ctypes.c_int32)]
+    """fi_plan_options: window_left (-1 = none), dtype and kv_dtype (FI_DTYPE_*;
+    kv_dtype -1 = dtype)."""
+    _fields_ = [("window_left", ctypes.c_int32), ("dtype", ctypes.c_int32),
+                ("kv_dtype", ctypes.c_int32)]
 
 
 class PlanInfo(ctypes.Structure):
@@ -85,10 +88,11 @@ def lib():
     L.fi_plan_destroy.argtypes = [_P]
     L.fi_plan_get_info.argtypes = [_P, ctypes.POINTER(PlanInfo)]
     L.fi_plan_get_work.argtypes = [_P, _P, _I32, ctypes.POINTER(_I32)]
+    _F = ctypes.c_float
     L.fi_batch_decode_paged.argtypes = [_P, _P, _P, _P, _I32, _I64, _I32, _P, _P, _P,
-                                        ctypes.c_float, _P, _P, _P, ctypes.c_size_t, _P]
+                                        _F, _F, _F, _P, _P, _P, ctypes.c_size_t, _P]
     L.fi_batch_prefill_paged.argtypes = [_P, _P, _P, _P, _P, _I32, _I64, _I32, _P, _P, _P,
-                                         ctypes.c_float, _P, _P, _P, ctypes.c_size_t, _P]
+                                         _F, _F, _F, _P, _P, _P, ctypes.c_size_t, _P]
     L.fi_merge_states.argtypes = [_P, _P, _I32, _I32, _I32, _I32, _I32, _P, _P, _P]
     L.fi_check_device_status.argtypes = [_P, _P]
     L.fi_status_string.argtypes = [_I32]
@@ -98,7 +102,7 @@ def lib():
     L.fi_debug_set_fault.argtypes = [_I32, _I64]
     L.fi_profile_next_launch.argtypes = [_P, _P]
     L.fi_batch_decode_paged_noalloc.argtypes = [_P, _P, _P, _P, _I32, _I64, _I32, _P, _P, _P,
-                                                ctypes.c_float, _P, _P, _P]
+                                                _F, _F, _F, _P, _P, _P]
     for name in EXPORTED:
         if name not in ("fi_status_string", "fi_last_error_string"):
             getattr(L, name).restype = _I32
@@ -160,13 +164,14 @@ class Plan:
 
 def fi_plan(mode, batch_size, qo_indptr_h, page_indptr_h, last_page_len_h, num_qo_heads,
             num_kv_heads, head_dim, page_size, causal, options, num_sms) -> Plan:
-    """``options``: None (the defaults) or a dict with any of ``window_left``
-    and ``dtype``."""
+    """``options``: None (the defaults) or a dict with any of ``window_left``,
+    ``dtype`` and ``kv_dtype``."""
     qo, pi, lp = _i32(qo_indptr_h), _i32(page_indptr_h), _i32(last_page_len_h)
     opt = None
     if options is not None:
         opt = PlanOptions(int(options.get("window_left", -1)),
-                          int(options.get("dtype", FI_DTYPE_BF16)))
+                          int(options.get("dtype", FI_DTYPE_BF16)),
+                          int(options.get("kv_dtype", -1)))
     h = _P()
     ws = ctypes.c_size_t()
     st = lib().fi_plan(int(mode), int(batch_size), _ptr(qo), _ptr(pi), _ptr(lp), int(num_qo_heads),
@@ -200,26 +205,29 @@ def fi_plan_get_work(plan: Plan) -> np.ndarray:
 
 def fi_batch_decode_paged(plan: Plan, q, k_cache, v_cache, kv_layout, page_stride_elems,
                           num_pages, page_indptr_d, page_indices_d, last_page_len_d, sm_scale,
-                          out, lse, workspace, workspace_bytes=None, stream=None):
+                          k_scale, v_scale, out, lse, workspace, workspace_bytes=None,
+                          stream=None):
     wsb = plan.workspace_bytes if workspace_bytes is None else workspace_bytes
     st = lib().fi_batch_decode_paged(plan.handle, _ptr(q), _ptr(k_cache), _ptr(v_cache),
                                      int(kv_layout), int(page_stride_elems), int(num_pages),
                                      _ptr(page_indptr_d), _ptr(page_indices_d),
-                                     _ptr(last_page_len_d), float(sm_scale), _ptr(out), _ptr(lse),
-                                     _ptr(workspace), int(wsb), _stream(stream))
+                                     _ptr(last_page_len_d), float(sm_scale), float(k_scale),
+                                     float(v_scale), _ptr(out), _ptr(lse), _ptr(workspace),
+                                     int(wsb), _stream(stream))
     _check(st, "fi_batch_decode_paged")
 
 
 def fi_batch_prefill_paged(plan: Plan, q, qo_indptr_d, k_cache, v_cache, kv_layout,
                            page_stride_elems, num_pages, page_indptr_d, page_indices_d,
-                           last_page_len_d, sm_scale, out, lse, workspace, workspace_bytes=None,
-                           stream=None):
+                           last_page_len_d, sm_scale, k_scale, v_scale, out, lse, workspace,
+                           workspace_bytes=None, stream=None):
     wsb = plan.workspace_bytes if workspace_bytes is None else workspace_bytes
     st = lib().fi_batch_prefill_paged(plan.handle, _ptr(q), _ptr(qo_indptr_d), _ptr(k_cache),
                                       _ptr(v_cache), int(kv_layout), int(page_stride_elems),
                                       int(num_pages), _ptr(page_indptr_d), _ptr(page_indices_d),
-                                      _ptr(last_page_len_d), float(sm_scale), _ptr(out),
-                                      _ptr(lse), _ptr(workspace), int(wsb), _stream(stream))
+                                      _ptr(last_page_len_d), float(sm_scale), float(k_scale),
+                                      float(v_scale), _ptr(out), _ptr(lse), _ptr(workspace),
+                                      int(wsb), _stream(stream))
     _check(st, "fi_batch_prefill_paged")
 
 
@@ -247,12 +255,12 @@ def fi_profile_next_launch(start_event, stop_event):
 
 def fi_batch_decode_paged_noalloc(plan: Plan, q, k_cache, v_cache, kv_layout, page_stride_elems,
                                   num_pages, page_indptr_d, page_indices_d, last_page_len_d,
-                                  sm_scale, out, lse, stream=None):
+                                  sm_scale, k_scale, v_scale, out, lse, stream=None):
     """fi_batch_decode_paged with the library's own static scratch (no workspace)."""
     st = lib().fi_batch_decode_paged_noalloc(plan.handle, _ptr(q), _ptr(k_cache), _ptr(v_cache),
                                              int(kv_layout), int(page_stride_elems),
                                              int(num_pages), _ptr(page_indptr_d),
                                              _ptr(page_indices_d), _ptr(last_page_len_d),
-                                             float(sm_scale), _ptr(out), _ptr(lse),
-                                             _stream(stream))
+                                             float(sm_scale), float(k_scale), float(v_scale),
+                                             _ptr(out), _ptr(lse), _stream(stream))
     _check(st, "fi_batch_decode_paged_noalloc")

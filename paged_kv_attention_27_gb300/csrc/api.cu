@@ -155,10 +155,15 @@ fi_status upload_image(void* dst, const fi::Plan& P, cudaStream_t stream) {
 }
 
 // Tensor map over a paged K or V cache that fetches one (page, kv head)
-// block of page_size rows x 64 dims (128 bytes, 128-byte swizzled) per box.
+// block per box: page_size rows x 64 dims (128 bytes, 128-byte swizzled)
+// for a 16-bit cache; page_size whole rows of head_dim bytes for an FP8
+// cache (128-byte swizzled at head_dim 128, unswizzled otherwise).
 CUtensorMapDataType tma_type(int dtype) {
+  if (dtype == FI_DTYPE_E4M3) return CU_TENSOR_MAP_DATA_TYPE_UINT8;
   return dtype == FI_DTYPE_FP16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
 }
+
+int elem_bytes(int dtype) { return dtype == FI_DTYPE_E4M3 ? 1 : 2; }
 
 fi_status make_kv_map(CUtensorMap* map, const void* base, int layout, int num_pages, int P,
                       int Hkv, int d, int64_t page_stride, int dtype) {
@@ -171,20 +176,27 @@ fi_status make_kv_map(CUtensorMap* map, const void* base, int layout, int num_pa
   cuuint64_t strides[3];
   cuuint32_t box[4];
   const cuuint32_t estr[4] = {1, 1, 1, 1};
+  const cuuint64_t eb = cuuint64_t(elem_bytes(dtype));
+  const cuuint32_t inner = dtype == FI_DTYPE_E4M3 ? cuuint32_t(d) : 64u;
   if (layout == FI_LAYOUT_NHD) {
     dims[0] = d; dims[1] = Hkv; dims[2] = P; dims[3] = num_pages;
-    strides[0] = cuuint64_t(d) * 2;
-    strides[1] = cuuint64_t(Hkv) * d * 2;
-    box[0] = 64; box[1] = 1; box[2] = P; box[3] = 1;
+    strides[0] = cuuint64_t(d) * eb;
+    strides[1] = cuuint64_t(Hkv) * d * eb;
+    box[0] = inner; box[1] = 1; box[2] = P; box[3] = 1;
   } else {
     dims[0] = d; dims[1] = P; dims[2] = Hkv; dims[3] = num_pages;
-    strides[0] = cuuint64_t(d) * 2;
-    strides[1] = cuuint64_t(P) * d * 2;
-    box[0] = 64; box[1] = P; box[2] = 1; box[3] = 1;
+    strides[0] = cuuint64_t(d) * eb;
+    strides[1] = cuuint64_t(P) * d * eb;
+    box[0] = inner; box[1] = P; box[2] = 1; box[3] = 1;
   }
-  strides[2] = cuuint64_t(page_stride) * 2;
+  strides[2] = cuuint64_t(page_stride) * eb;
+  // FP8 rows of 128 bytes are swizzled too (the decode kernel reads MMA
+  // fragments from them); other FP8 row lengths are not
+  const CUtensorMapSwizzle swizzle = (dtype != FI_DTYPE_E4M3 || d == 128)
+                                         ? CU_TENSOR_MAP_SWIZZLE_128B
+                                         : CU_TENSOR_MAP_SWIZZLE_NONE;
   CUresult r = enc(map, tma_type(dtype), 4, const_cast<void*>(base), dims,
-                   strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) {
     g_last_error = "cuTensorMapEncodeTiled failed for the KV cache (code " + std::to_string(int(r)) + ")";
@@ -231,8 +243,8 @@ fi_status run_paged(fi_plan_t plan, bool prefill_call, const void* q, const int3
                     const void* k_cache, const void* v_cache, int32_t kv_layout,
                     int64_t page_stride_elems, int32_t num_pages, const int32_t* page_indptr_d,
                     const int32_t* page_indices_d, const int32_t* last_page_len_d, float sm_scale,
-                    void* out, float* lse, void* workspace, size_t workspace_bytes,
-                    void* stream_ptr) {
+                    float k_scale, float v_scale, void* out, float* lse, void* workspace,
+                    size_t workspace_bytes, void* stream_ptr) {
   if (!plan) return FI_ERR_INVALID_ARG;
   const fi::Plan& P = plan->p;
   if (P.mode != (prefill_call ? FI_MODE_PREFILL : FI_MODE_DECODE)) return FI_ERR_INVALID_ARG;
@@ -247,9 +259,13 @@ fi_status run_paged(fi_plan_t plan, bool prefill_call, const void* q, const int3
     return FI_ERR_INVALID_ARG;
   if (kv_layout != FI_LAYOUT_NHD && kv_layout != FI_LAYOUT_HND) return FI_ERR_INVALID_ARG;
   if (!(sm_scale >= 0.f) || sm_scale > 3.0e38f) return FI_ERR_INVALID_ARG;  // also rejects NaN
+  if (!(k_scale > 0.f) || k_scale > 3.0e38f || !(v_scale > 0.f) || v_scale > 3.0e38f)
+    return FI_ERR_INVALID_ARG;
   const int64_t page_elems = int64_t(P.page_size) * P.num_kv_heads * P.head_dim;
   if (page_stride_elems == 0) page_stride_elems = page_elems;
-  if (page_stride_elems < page_elems || page_stride_elems % 8 != 0) return FI_ERR_INVALID_ARG;
+  // page starts 16-byte aligned for TMA
+  if (page_stride_elems < page_elems || page_stride_elems % (16 / elem_bytes(P.kv_dtype)) != 0)
+    return FI_ERR_INVALID_ARG;
   if (workspace_bytes < P.ws.total) return FI_ERR_WORKSPACE_TOO_SMALL;
   fi_status st = check_device();
   if (st != FI_OK) return st;
@@ -273,10 +289,10 @@ fi_status run_paged(fi_plan_t plan, bool prefill_call, const void* q, const int3
   CUtensorMap kmap, vmap;
   if (P.total_kv > 0) {
     st = make_kv_map(&kmap, k_cache, kv_layout, num_pages, P.page_size, P.num_kv_heads,
-                     P.head_dim, page_stride_elems, P.dtype);
+                     P.head_dim, page_stride_elems, P.kv_dtype);
     if (st != FI_OK) return st;
     st = make_kv_map(&vmap, v_cache, kv_layout, num_pages, P.page_size, P.num_kv_heads,
-                     P.head_dim, page_stride_elems, P.dtype);
+                     P.head_dim, page_stride_elems, P.kv_dtype);
     if (st != FI_OK) return st;
   } else {
     std::memset(&kmap, 0, sizeof(kmap));
@@ -332,7 +348,8 @@ fi_status run_paged(fi_plan_t plan, bool prefill_call, const void* q, const int3
     pp.layout = kv_layout;
     pp.causal = P.causal;
     pp.window_left = P.window_left;
-    pp.sm_scale = sm_scale;
+    pp.sm_scale = sm_scale * k_scale;   // the key scale folds into the score scale
+    pp.v_scale = v_scale;
     pp.out = out;
     pp.lse = lse;
     pp.err = err;
@@ -352,7 +369,8 @@ fi_status run_paged(fi_plan_t plan, bool prefill_call, const void* q, const int3
     dp.page_size = P.page_size;
     dp.num_qo_heads = P.num_qo_heads;
     dp.layout = kv_layout;
-    dp.sm_scale = sm_scale;
+    dp.sm_scale = sm_scale * k_scale;   // the key scale folds into the score scale
+    dp.v_scale = v_scale;
     dp.out = out;
     dp.lse = lse;
     dp.partial_o = partial_o;
@@ -362,7 +380,8 @@ fi_status run_paged(fi_plan_t plan, bool prefill_call, const void* q, const int3
     dp.err = err;
     dp.wait_limit_ns = g_wait_limit_ns;
     dp.fault_kind = fault_kind;
-    e = fi::launch_decode(P.head_dim, P.num_qo_heads / P.num_kv_heads, P.dtype, kmap, vmap, dp,
+    e = fi::launch_decode(P.head_dim, P.num_qo_heads / P.num_kv_heads, P.dtype, P.kv_dtype, kmap,
+                          vmap, dp,
                           int(P.decode_items.size()), dstream);
     if (e != cudaSuccess) return cuda_fail(e, "decode launch");
   }
@@ -450,24 +469,24 @@ fi_status fi_batch_decode_paged(fi_plan_t plan, const void* q, const void* k_cac
                                 const void* v_cache, int32_t kv_layout,
                                 int64_t page_stride_elems, int32_t num_pages,
                                 const int32_t* page_indptr_d, const int32_t* page_indices_d,
-                                const int32_t* last_page_len_d, float sm_scale, void* out,
-                                float* lse, void* workspace, size_t workspace_bytes,
-                                void* stream) {
+                                const int32_t* last_page_len_d, float sm_scale, float k_scale,
+                                float v_scale, void* out, float* lse, void* workspace,
+                                size_t workspace_bytes, void* stream) {
   return run_paged(plan, false, q, nullptr, k_cache, v_cache, kv_layout, page_stride_elems,
-                   num_pages, page_indptr_d, page_indices_d, last_page_len_d, sm_scale, out, lse,
-                   workspace, workspace_bytes, stream);
+                   num_pages, page_indptr_d, page_indices_d, last_page_len_d, sm_scale, k_scale,
+                   v_scale, out, lse, workspace, workspace_bytes, stream);
 }
 
 fi_status fi_batch_prefill_paged(fi_plan_t plan, const void* q, const int32_t* qo_indptr_d,
                                  const void* k_cache, const void* v_cache, int32_t kv_layout,
                                  int64_t page_stride_elems, int32_t num_pages,
                                  const int32_t* page_indptr_d, const int32_t* page_indices_d,
-                                 const int32_t* last_page_len_d, float sm_scale, void* out,
-                                 float* lse, void* workspace, size_t workspace_bytes,
-                                 void* stream) {
+                                 const int32_t* last_page_len_d, float sm_scale, float k_scale,
+                                 float v_scale, void* out, float* lse, void* workspace,
+                                 size_t workspace_bytes, void* stream) {
   return run_paged(plan, true, q, qo_indptr_d, k_cache, v_cache, kv_layout, page_stride_elems,
-                   num_pages, page_indptr_d, page_indices_d, last_page_len_d, sm_scale, out, lse,
-                   workspace, workspace_bytes, stream);
+                   num_pages, page_indptr_d, page_indices_d, last_page_len_d, sm_scale, k_scale,
+                   v_scale, out, lse, workspace, workspace_bytes, stream);
 }
 
 fi_status fi_merge_states(const float* v, const float* s, int32_t n, int32_t S, int32_t H,

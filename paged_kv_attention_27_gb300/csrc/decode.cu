@@ -19,6 +19,8 @@
 //     the final row (bf16 or fp16, the inputs' type) + lse, or an fp32 partial state that the merge
 //     kernel combines by log-sum-exp.
 // Scores are kept in the log2 domain (q pre-scaled by sm_scale*log2(e)).
+#include <type_traits>
+
 #include "elem.cuh"
 #include "fi_internal.h"
 #include "kernels.cuh"
@@ -33,10 +35,10 @@ using namespace dev;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
-template <int HEAD_DIM, int GROUP>
+template <int HEAD_DIM, int GROUP, int KVB>   // KVB: bytes per cache element (2, or 1 for FP8)
 struct DecodeCfg {
-  static constexpr int TILE = 8192 / HEAD_DIM;         // tokens per stage (32 KB of K+V)
-  static constexpr int NSTAGE = 3;
+  static constexpr int TILE = 8192 / HEAD_DIM;         // tokens per stage (32 KB of 16-bit K+V)
+  static constexpr int NSTAGE = KVB == 2 ? 3 : 4;      // FP8: 16 KB stages, one deeper
   static constexpr int NCW = 4;                        // consumer warps
   static constexpr int THREADS = 32 * (NCW + 1);       // + one producer warp
   static constexpr int LPT = HEAD_DIM / 8;             // lanes per token row (8 dims each)
@@ -44,16 +46,26 @@ struct DecodeCfg {
   static constexpr int TOK_PER_WARP = TILE / NCW;
   static constexpr int PASSES = TOK_PER_WARP / TPP;    // 8 for every head_dim
   static constexpr int SUB = GROUP >= 8 ? 2 : (GROUP >= 4 ? 4 : 8);  // passes per softmax step
-  static constexpr int DBLK = HEAD_DIM / 64;           // 128-byte slices per row
-  static constexpr int KBYTES = TILE * HEAD_DIM * 2;   // one K (or V) stage
+  static constexpr int DBLK = HEAD_DIM / 64;           // 128-byte slices of a 16-bit row
+  static constexpr int KBYTES = TILE * HEAD_DIM * KVB; // one K (or V) stage
   static constexpr int STAGE_BYTES = 2 * KBYTES;
-  static constexpr int SMEM_BYTES = NSTAGE * STAGE_BYTES + 1024;  // + alignment slack
   // GQA groups of 4 or 8 heads at head_dim <= 128 use the tensor cores: the
   // g heads are the M rows of m16n8k16 MMAs (padded to 16), 16 tokens per step
   static constexpr bool MMA = GROUP >= 4 && HEAD_DIM <= 128;
+  // FP8 rows of 128 bytes (head_dim 128) arrive 128-byte swizzled, and the
+  // tensor-core consumer then loads its MMA fragments straight from them;
+  // at head_dim 64 it widens 16 tokens of K and of V at a time into 16-bit
+  // rows laid out as the TMA writes a 16-bit stage
+  static constexpr bool SWZ8 = KVB == 1 && HEAD_DIM == 128;
+  static constexpr int CONV_BYTES = (KVB == 1 && MMA && !SWZ8) ? NCW * 2 * 16 * HEAD_DIM * 2 : 0;
+  static constexpr int SMEM_BYTES = NSTAGE * STAGE_BYTES + CONV_BYTES + 1024;  // + alignment
+  // CTAs per SM: the FP8 SIMT consumer (65 KB) fits three, for more warps
+  // to hide its conversion work, where 1 or 2 heads leave registers to spare
+  static constexpr int MIN_BLOCKS = (KVB == 1 && !MMA && GROUP <= 2) ? 3 : 2;
   static_assert(PASSES % SUB == 0, "");
   static_assert(!MMA || TOK_PER_WARP % 16 == 0, "");
   static_assert(NCW * GROUP * HEAD_DIM * 4 + 3 * NCW * GROUP * 4 <= NSTAGE * STAGE_BYTES, "");
+  static_assert(SMEM_BYTES <= 113 * 1024, "two CTAs per SM");
 };
 
 // Byte offset of 16-byte chunk `c8` (0..7) of row `r` inside a 128-byte-row
@@ -67,16 +79,24 @@ __device__ __forceinline__ uint32_t swz(int r, int c8) {
 // with zeros) = Q K^T by m16n8k16 MMAs with K read by ldmatrix from the
 // swizzled stage; an online softmax per head row (a quad of lanes holds a
 // row); P rounded to the element type is reused as the A fragment of O += P V, with V
-// read by ldmatrix.trans. Leaves the warp's (m, l, lp, O) in shared memory
-// and returns whether any consumer aborted (voted, so all agree).
-template <int HEAD_DIM, int GROUP, class E>
+// read by ldmatrix.trans. With an FP8 cache the warp first widens each
+// 16-token chunk of K and V (exactly) into its own 16-bit scratch, laid out
+// as the TMA writes a 16-bit stage, and runs the same MMA code on it.
+// Leaves the warp's (m, l, lp, O) in shared memory and returns whether any
+// consumer aborted (voted, so all agree).
+template <int HEAD_DIM, int GROUP, class E, class KV>
 __device__ __forceinline__ bool mma_consumer(const DecodeParams& prm, const WorkItem& item,
                                              int n_tok, int lead, int n_tiles,
                                              uint32_t smem_base,
                                              uint64_t* full_bar, uint64_t* empty_bar,
                                              int* abort_flag, float* red_o, float* red_m,
                                              float* red_l, float* red_lp) {
-  using C = DecodeCfg<HEAD_DIM, GROUP>;
+  constexpr bool FP8 = std::is_same<KV, E4m3>::value;
+  using C = DecodeCfg<HEAD_DIM, GROUP, FP8 ? 1 : 2>;
+  // With an FP8 cache the MMAs run in fp16: e4m3 widens to fp16 in one
+  // instruction per pair, exactly; q (bf16 or fp16) is converted once (exact
+  // within fp16's range) and P is rounded to fp16.
+  using ME = std::conditional_t<FP8, Fp16, E>;
   constexpr int KS = HEAD_DIM / 16;       // k-steps of QK^T
   constexpr int NTO = HEAD_DIM / 8;       // 8-dim tiles of O
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -93,9 +113,21 @@ __device__ __forceinline__ bool mma_consumer(const DecodeParams& prm, const Work
             HEAD_DIM);
 #pragma unroll
     for (int ks = 0; ks < KS; ++ks) {
-      qa[ks][0] = r < GROUP ? qp[(ks * 16 + k0) >> 1] : 0u;
+      // With FP8 fragments loaded straight from the cache rows, k index 2c+j
+      // of a k-step is dim 4c+j and 2c+8+j is dim 4c+2+j (c = lane % 4): each
+      // lane's four consecutive bytes of a key row feed both of its
+      // B registers. Q's A fragment follows the same order.
+      const int w0i = C::SWZ8 ? (ks * 16 + 2 * k0) >> 1 : (ks * 16 + k0) >> 1;
+      const int w2i = C::SWZ8 ? w0i + 1 : (ks * 16 + 8 + k0) >> 1;
+      uint32_t w0 = r < GROUP ? qp[w0i] : 0u;
+      uint32_t w2 = r < GROUP ? qp[w2i] : 0u;
+      if constexpr (!std::is_same<ME, E>::value) {
+        w0 = ME::pack2(E::lo(w0), E::hi(w0));
+        w2 = ME::pack2(E::lo(w2), E::hi(w2));
+      }
+      qa[ks][0] = w0;
       qa[ks][1] = 0u;
-      qa[ks][2] = r < GROUP ? qp[(ks * 16 + 8 + k0) >> 1] : 0u;
+      qa[ks][2] = w2;
       qa[ks][3] = 0u;
     }
   }
@@ -113,12 +145,66 @@ __device__ __forceinline__ bool mma_consumer(const DecodeParams& prm, const Work
     }
     const int ntok = min(C::TILE, n_tok - i * C::TILE);
     const int lo = i == 0 ? lead : 0;        // rows below lo are outside the window
-    const uint32_t kbase = smem_base + s * C::STAGE_BYTES;
-    const uint32_t vbase = kbase + C::KBYTES;
+    const uint32_t kstage = smem_base + s * C::STAGE_BYTES;
+    const uint32_t vstage = kstage + C::KBYTES;
 #pragma unroll 1
     for (int cb = warp * C::TOK_PER_WARP; cb < (warp + 1) * C::TOK_PER_WARP; cb += 16) {
       if (cb >= ntok) break;
-      if (cb + 16 > ntok) {
+      // 16-bit K and V rows of this chunk: in the stage (row cb + t of slices
+      // TILE rows long) or, for FP8, in the warp's scratch (row t of 16-row slices)
+      uint32_t kbase = kstage, vbase = vstage, slice = C::TILE * 128;
+      int row0 = cb;
+      if constexpr (C::SWZ8) {
+        if (cb + 16 > ntok) {
+          // FP8 V rows past the last key: zero them (P = 0 must not meet a NaN)
+          for (int idx = lane; idx < 16 * 8; idx += 32) {
+            const int row = cb + idx / 8;
+            if (row >= ntok) {
+              const uint32_t a = vstage + row * 128 + (idx % 8) * 16;
+              asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(a), "r"(0u)
+                           : "memory");
+            }
+          }
+          __syncwarp();
+        }
+      } else if constexpr (FP8) {
+        kbase = smem_base + C::NSTAGE * C::STAGE_BYTES + warp * (2 * 16 * HEAD_DIM * 2);
+        vbase = kbase + 16 * HEAD_DIM * 2;
+        slice = 16 * 128;
+        row0 = 0;
+        // 16 tokens x HEAD_DIM bytes of each of K and V; one 16-byte FP8
+        // chunk becomes two 16-byte chunks of the 16-bit layout. Rows past
+        // the last key become zeros (P = 0 there must not meet a NaN).
+        constexpr int CPR = HEAD_DIM / 16;   // 16-byte FP8 chunks per row
+#pragma unroll 1
+        for (int idx = lane; idx < 2 * 16 * CPR; idx += 32) {
+          const int is_v = idx >= 16 * CPR;
+          const int rem = idx - is_v * 16 * CPR;
+          const int t = rem / CPR, c = rem % CPR;
+          uint32_t w[8];
+          if (cb + t < ntok) {
+            const uint4 u = lds128((is_v ? vstage : kstage) + (cb + t) * HEAD_DIM + c * 16);
+            const uint32_t uw[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              w[2 * e] = E4m3::to_f16x2(uw[e]);
+              w[2 * e + 1] = E4m3::to_f16x2(uw[e] >> 16);
+            }
+          } else {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) w[e] = 0u;
+          }
+          const uint32_t dst = (is_v ? vbase : kbase);
+          const int c8 = 2 * c;                       // first 8-dim chunk of the 16 dims
+          const uint32_t a0 = dst + (c8 >> 3) * slice + swz(t, c8 & 7);
+          const uint32_t a1 = dst + ((c8 + 1) >> 3) * slice + swz(t, (c8 + 1) & 7);
+          asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(a0), "r"(w[0]), "r"(w[1]),
+                       "r"(w[2]), "r"(w[3]) : "memory");
+          asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(a1), "r"(w[4]), "r"(w[5]),
+                       "r"(w[6]), "r"(w[7]) : "memory");
+        }
+        __syncwarp();
+      } else if (cb + 16 > ntok) {
         // V rows past the last key hold unused slots or stale data: zero them
         // so that P = 0 there cannot meet a NaN in the MMA
         for (int idx = lane; idx < 16 * (HEAD_DIM / 8); idx += 32) {
@@ -131,14 +217,32 @@ __device__ __forceinline__ bool mma_consumer(const DecodeParams& prm, const Work
         __syncwarp();
       }
       float sacc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+      // ldmatrix lanes 0-7 / 8-15 / 16-23 / 24-31 address matrices 0..3
+      const int ltok = (lane & 7) + ((lane >> 3) & 1) * 8;   // token row this lane addresses
+      if constexpr (C::SWZ8) {
+        // K straight from the FP8 rows: each 8x8 matrix of byte pairs is 8
+        // tokens x 16 dims; matrices (tokens 0-7 | 8-15) x (k-steps ks | ks+1)
+        const int tok = cb + ltok;
 #pragma unroll
-      for (int ks = 0; ks < KS; ++ks) {
-        const int tok = cb + (mi >> 1) * 8 + rr;
-        const int dim = ks * 16 + (mi & 1) * 8;
-        uint32_t b0, b1, b2, b3;
-        ldsm_x4(kbase + (dim >> 6) * C::TILE * 128 + swz(tok, (dim & 63) >> 3), b0, b1, b2, b3);
-        E::mma16816(sacc[0], qa[ks], b0, b1);
-        E::mma16816(sacc[1], qa[ks], b2, b3);
+        for (int ks = 0; ks < KS; ks += 2) {
+          const int step = ks + (lane >> 4);
+          uint32_t q0, q1, q2, q3;
+          ldsm_x4(kstage + tok * 128 + ((step ^ (tok & 7)) << 4), q0, q1, q2, q3);
+          ME::mma16816(sacc[0], qa[ks], E4m3::to_f16x2(q0), E4m3::to_f16x2(q0 >> 16));
+          ME::mma16816(sacc[1], qa[ks], E4m3::to_f16x2(q1), E4m3::to_f16x2(q1 >> 16));
+          ME::mma16816(sacc[0], qa[ks + 1], E4m3::to_f16x2(q2), E4m3::to_f16x2(q2 >> 16));
+          ME::mma16816(sacc[1], qa[ks + 1], E4m3::to_f16x2(q3), E4m3::to_f16x2(q3 >> 16));
+        }
+      } else {
+#pragma unroll
+        for (int ks = 0; ks < KS; ++ks) {
+          const int trow = row0 + (mi >> 1) * 8 + rr;
+          const int dim = ks * 16 + (mi & 1) * 8;
+          uint32_t b0, b1, b2, b3;
+          ldsm_x4(kbase + (dim >> 6) * slice + swz(trow, (dim & 63) >> 3), b0, b1, b2, b3);
+          ME::mma16816(sacc[0], qa[ks], b0, b1);
+          ME::mma16816(sacc[1], qa[ks], b2, b3);
+        }
       }
       float sv[4];
 #pragma unroll
@@ -167,20 +271,42 @@ __device__ __forceinline__ bool mma_consumer(const DecodeParams& prm, const Work
       for (int e = 0; e < 4; ++e) p[e] = ex2(sv[e] - ref);
       l += (p[0] + p[1]) + (p[2] + p[3]);
       uint32_t pa[4];
-      pa[0] = E::pack2(p[0], p[1]);
+      pa[0] = ME::pack2(p[0], p[1]);
       pa[1] = 0u;
-      pa[2] = E::pack2(p[2], p[3]);
+      pa[2] = ME::pack2(p[2], p[3]);
       pa[3] = 0u;
-      lp += (E::lo(pa[0]) + E::hi(pa[0])) + (E::lo(pa[2]) + E::hi(pa[2]));
+      lp += (ME::lo(pa[0]) + ME::hi(pa[0])) + (ME::lo(pa[2]) + ME::hi(pa[2]));
+      if constexpr (C::SWZ8) {
+        // V straight from the FP8 rows: a transposed 8x8 matrix of byte pairs
+        // gives a lane tokens 2c, 2c+1 of dims 2n, 2n+1 (n = lane / 4); the
+        // even dims and the odd dims become two n-tiles (O columns permuted,
+        // undone when O is written out). Matrices: (tokens 0-7 | 8-15) x
+        // (16-dim groups j | j+1).
+        const int tok = cb + ltok;
 #pragma unroll
-      for (int n2 = 0; n2 < NTO / 2; ++n2) {
-        const int tok = cb + (mi & 1) * 8 + rr;
-        const int dim = (2 * n2 + (mi >> 1)) * 8;
-        uint32_t v0, v1, v2, v3;
-        ldsm_x4_trans(vbase + (dim >> 6) * C::TILE * 128 + swz(tok, (dim & 63) >> 3), v0, v1, v2,
-                      v3);
-        E::mma16816(o[2 * n2], pa, v0, v1);
-        E::mma16816(o[2 * n2 + 1], pa, v2, v3);
+        for (int j = 0; j < HEAD_DIM / 16; j += 2) {
+          const int grp = j + (lane >> 4);
+          uint32_t v0, v1, v2, v3;
+          ldsm_x4_trans(vstage + tok * 128 + ((grp ^ (tok & 7)) << 4), v0, v1, v2, v3);
+          ME::mma16816(o[2 * j], pa, E4m3::to_f16x2(__byte_perm(v0, 0, 0x0020)),
+                       E4m3::to_f16x2(__byte_perm(v1, 0, 0x0020)));
+          ME::mma16816(o[2 * j + 1], pa, E4m3::to_f16x2(__byte_perm(v0, 0, 0x0031)),
+                       E4m3::to_f16x2(__byte_perm(v1, 0, 0x0031)));
+          ME::mma16816(o[2 * j + 2], pa, E4m3::to_f16x2(__byte_perm(v2, 0, 0x0020)),
+                       E4m3::to_f16x2(__byte_perm(v3, 0, 0x0020)));
+          ME::mma16816(o[2 * j + 3], pa, E4m3::to_f16x2(__byte_perm(v2, 0, 0x0031)),
+                       E4m3::to_f16x2(__byte_perm(v3, 0, 0x0031)));
+        }
+      } else {
+#pragma unroll
+        for (int n2 = 0; n2 < NTO / 2; ++n2) {
+          const int trow = row0 + (mi & 1) * 8 + rr;
+          const int dim = (2 * n2 + (mi >> 1)) * 8;
+          uint32_t v0, v1, v2, v3;
+          ldsm_x4_trans(vbase + (dim >> 6) * slice + swz(trow, (dim & 63) >> 3), v0, v1, v2, v3);
+          ME::mma16816(o[2 * n2], pa, v0, v1);
+          ME::mma16816(o[2 * n2 + 1], pa, v2, v3);
+        }
       }
     }
     fence_proxy_async_smem();   // any zeroed rows before the producer's next TMA into the stage
@@ -196,8 +322,12 @@ __device__ __forceinline__ bool mma_consumer(const DecodeParams& prm, const Work
   if (!aborted && r < GROUP) {
 #pragma unroll
     for (int t = 0; t < NTO; ++t) {
-      red_o[(warp * GROUP + r) * HEAD_DIM + t * 8 + k0] = o[t][0];
-      red_o[(warp * GROUP + r) * HEAD_DIM + t * 8 + k0 + 1] = o[t][1];
+      // column 2c (+1) of n-tile t is dim 8t + 2c (+1); with FP8 fragments,
+      // n-tile t holds dims 16(t/2) + 4c + (t%2) (and + 2)
+      const int d0 = C::SWZ8 ? 16 * (t >> 1) + 2 * k0 + (t & 1) : t * 8 + k0;
+      const int d1 = C::SWZ8 ? d0 + 2 : d0 + 1;
+      red_o[(warp * GROUP + r) * HEAD_DIM + d0] = o[t][0];
+      red_o[(warp * GROUP + r) * HEAD_DIM + d1] = o[t][1];
     }
     if ((lane & 3) == 0) {
       red_m[warp * GROUP + r] = m;
@@ -208,11 +338,14 @@ __device__ __forceinline__ bool mma_consumer(const DecodeParams& prm, const Work
   return aborted;
 }
 
-template <int HEAD_DIM, int GROUP, class E>
-__global__ void __launch_bounds__(DecodeCfg<HEAD_DIM, GROUP>::THREADS, 2)
+template <int HEAD_DIM, int GROUP, class E, class KV>
+__global__ void __launch_bounds__(
+    DecodeCfg<HEAD_DIM, GROUP, 2>::THREADS,
+    (DecodeCfg<HEAD_DIM, GROUP, std::is_same<KV, E4m3>::value ? 1 : 2>::MIN_BLOCKS))
 decode_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant__ CUtensorMap v_map,
               DecodeParams prm) {
-  using C = DecodeCfg<HEAD_DIM, GROUP>;
+  constexpr bool FP8 = std::is_same<KV, E4m3>::value;
+  using C = DecodeCfg<HEAD_DIM, GROUP, FP8 ? 1 : 2>;
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t full_bar[C::NSTAGE];
   __shared__ __align__(8) uint64_t empty_bar[C::NSTAGE];
@@ -247,7 +380,9 @@ decode_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant__
       prefetch_tensormap(&v_map);
     }
     const int pages_per_tile = C::TILE / prm.page_size;
-    const uint32_t box_bytes = uint32_t(prm.page_size) * 128u;
+    // one box per (page, 64-dim slice) of a 16-bit cache; per page for FP8
+    const uint32_t box_bytes = uint32_t(prm.page_size) * (FP8 ? HEAD_DIM : 128u);
+    constexpr int BOXES = FP8 ? 1 : C::DBLK;
     int issued = 0;
     for (int i = 0; i < n_tiles; ++i) {
       const int s = i % C::NSTAGE;
@@ -269,7 +404,7 @@ decode_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant__
         if (!valid) atomicOr(prm.err, kErrBounds);
       }
       const uint32_t vmask = __ballot_sync(0xffffffffu, valid);
-      const uint32_t bytes = uint32_t(__popc(vmask)) * 2u * C::DBLK * box_bytes;
+      const uint32_t bytes = uint32_t(__popc(vmask)) * 2u * BOXES * box_bytes;
       const uint32_t fb = smem_u32(&full_bar[s]);
       const bool skip = (prm.fault_kind == 1 && blockIdx.x == 0 && i == 0);
       if (lane == 0 && !skip) mbar_arrive_expect_tx(fb, bytes);
@@ -278,8 +413,8 @@ decode_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant__
         const uint32_t kdst = smem_base + s * C::STAGE_BYTES + lane * box_bytes;
         const uint32_t vdst = kdst + C::KBYTES;
 #pragma unroll
-        for (int c = 0; c < C::DBLK; ++c) {
-          const uint32_t off = uint32_t(c) * C::TILE * 128u;
+        for (int c = 0; c < BOXES; ++c) {
+          const uint32_t off = uint32_t(c) * C::TILE * 128u;   // 0 for FP8
           if (prm.layout == FI_LAYOUT_NHD) {
             tma_load_4d(kdst + off, &k_map, fb, c * 64, item.head, 0, page);
             tma_load_4d(vdst + off, &v_map, fb, c * 64, item.head, 0, page);
@@ -346,8 +481,15 @@ decode_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant__
       }
       const int ntok = min(C::TILE, n_tok - i * C::TILE);
       const int lo = i == 0 ? lead : 0;      // rows below lo are outside the window
-      const uint32_t kbase = smem_base + s * C::STAGE_BYTES + blk * C::TILE * 128;
+      // 16-bit cache: the lane's 16 bytes in its 64-dim slice (swizzled);
+      // FP8 cache: its 8 bytes of a HEAD_DIM-byte row (128-byte rows swizzled)
+      const uint32_t kbase =
+          smem_base + s * C::STAGE_BYTES + (FP8 ? 0 : blk * C::TILE * 128);
       const uint32_t vbase = kbase + C::KBYTES;
+      auto row8 = [&](int r) -> uint32_t {
+        return C::SWZ8 ? uint32_t(r * 128 + ((((ch >> 1) ^ (r & 7))) << 4) + (ch & 1) * 8)
+                       : uint32_t(r * HEAD_DIM + ch * 8);
+      };
 #pragma unroll
       for (int p0 = 0; p0 < C::PASSES; p0 += C::SUB) {
         float sc[C::SUB][GROUP];
@@ -355,7 +497,8 @@ decode_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant__
         for (int p = 0; p < C::SUB; ++p) {
           const int r = warp * C::TOK_PER_WARP + (p0 + p) * C::TPP + ts;
           float kf[8];
-          unpack8<E>(lds128(kbase + swz(r, c8)), kf);
+          if constexpr (FP8) E4m3::unpack8(lds64(kbase + row8(r)), kf);
+          else unpack8<E>(lds128(kbase + swz(r, c8)), kf);
 #pragma unroll
           for (int h = 0; h < GROUP; ++h) {
             float d0 = 0.f;
@@ -386,7 +529,8 @@ decode_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant__
           const int r = warp * C::TOK_PER_WARP + (p0 + p) * C::TPP + ts;
           if (r < ntok) {
             float vf[8];
-            unpack8<E>(lds128(vbase + swz(r, c8)), vf);
+            if constexpr (FP8) E4m3::unpack8(lds64(vbase + row8(r)), vf);
+            else unpack8<E>(lds128(vbase + swz(r, c8)), vf);
 #pragma unroll
             for (int h = 0; h < GROUP; ++h) {
               const float pr = ex2(sc[p][h] - ref[h]);
@@ -438,7 +582,7 @@ decode_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant__
       }
     }
     } else {
-      aborted = mma_consumer<HEAD_DIM, GROUP, E>(prm, item, n_tok, lead, n_tiles, smem_base,
+      aborted = mma_consumer<HEAD_DIM, GROUP, E, KV>(prm, item, n_tok, lead, n_tiles, smem_base,
                                               full_bar, empty_bar, &abort_flag, red_o, red_m,
                                               red_l, red_lp);
     }
@@ -461,7 +605,7 @@ decode_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant__
           LP = fmaf(red_lp[w * GROUP + h], sc, LP);
           O = fmaf(red_o[(w * GROUP + h) * HEAD_DIM + dd], sc, O);
         }
-        const float o = (LP > 0.f) ? O / LP : 0.f;
+        const float o = (LP > 0.f) ? O * (prm.v_scale / LP) : 0.f;
         const float lse = (L > 0.f) ? (rf + lg2(L)) * kLn2 : -INFINITY;
         const int hq = item.head * GROUP + h;
         if (item.slot < 0) {
@@ -544,11 +688,11 @@ decode_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant__
   }
 }
 
-template <int HEAD_DIM, int GROUP, class E>
+template <int HEAD_DIM, int GROUP, class E, class KV>
 cudaError_t launch_decode_t(const CUtensorMap& km, const CUtensorMap& vm, const DecodeParams& p,
                             int n_items, cudaStream_t stream) {
-  using C = DecodeCfg<HEAD_DIM, GROUP>;
-  auto kern = decode_kernel<HEAD_DIM, GROUP, E>;
+  using C = DecodeCfg<HEAD_DIM, GROUP, std::is_same<KV, E4m3>::value ? 1 : 2>;
+  auto kern = decode_kernel<HEAD_DIM, GROUP, E, KV>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        C::SMEM_BYTES);
   if (e != cudaSuccess) return e;
@@ -556,40 +700,43 @@ cudaError_t launch_decode_t(const CUtensorMap& km, const CUtensorMap& vm, const 
   return cudaGetLastError();
 }
 
-template <int HEAD_DIM, class E>
+template <int HEAD_DIM, class E, class KV>
 cudaError_t launch_decode_d(int group, const CUtensorMap& km, const CUtensorMap& vm,
                             const DecodeParams& p, int n_items, cudaStream_t stream) {
   switch (group) {
-    case 1: return launch_decode_t<HEAD_DIM, 1, E>(km, vm, p, n_items, stream);
-    case 2: return launch_decode_t<HEAD_DIM, 2, E>(km, vm, p, n_items, stream);
-    case 4: return launch_decode_t<HEAD_DIM, 4, E>(km, vm, p, n_items, stream);
-    case 8: return launch_decode_t<HEAD_DIM, 8, E>(km, vm, p, n_items, stream);
+    case 1: return launch_decode_t<HEAD_DIM, 1, E, KV>(km, vm, p, n_items, stream);
+    case 2: return launch_decode_t<HEAD_DIM, 2, E, KV>(km, vm, p, n_items, stream);
+    case 4: return launch_decode_t<HEAD_DIM, 4, E, KV>(km, vm, p, n_items, stream);
+    case 8: return launch_decode_t<HEAD_DIM, 8, E, KV>(km, vm, p, n_items, stream);
     default: return cudaErrorInvalidValue;
   }
 }
 
-template <class E>
+template <class E, class KV>
 cudaError_t launch_decode_e(int head_dim, int group, const CUtensorMap& km, const CUtensorMap& vm,
                             const DecodeParams& p, int n_items, cudaStream_t stream) {
   switch (head_dim) {
-    case 64: return launch_decode_d<64, E>(group, km, vm, p, n_items, stream);
-    case 128: return launch_decode_d<128, E>(group, km, vm, p, n_items, stream);
-    case 256: return launch_decode_d<256, E>(group, km, vm, p, n_items, stream);
+    case 64: return launch_decode_d<64, E, KV>(group, km, vm, p, n_items, stream);
+    case 128: return launch_decode_d<128, E, KV>(group, km, vm, p, n_items, stream);
+    case 256: return launch_decode_d<256, E, KV>(group, km, vm, p, n_items, stream);
     default: return cudaErrorInvalidValue;
   }
 }
 
 }  // namespace
 
-cudaError_t launch_decode(int head_dim, int group, int dtype, const CUtensorMap& km,
+cudaError_t launch_decode(int head_dim, int group, int dtype, int kv_dtype, const CUtensorMap& km,
                           const CUtensorMap& vm, const DecodeParams& p, int n_items,
                           cudaStream_t stream) {
   if (n_items <= 0) return cudaSuccess;
-  switch (dtype) {
-    case FI_DTYPE_BF16: return launch_decode_e<Bf16>(head_dim, group, km, vm, p, n_items, stream);
-    case FI_DTYPE_FP16: return launch_decode_e<Fp16>(head_dim, group, km, vm, p, n_items, stream);
-    default: return cudaErrorInvalidValue;
-  }
+  const bool fp8 = kv_dtype == FI_DTYPE_E4M3;
+  if (dtype == FI_DTYPE_BF16)
+    return fp8 ? launch_decode_e<Bf16, E4m3>(head_dim, group, km, vm, p, n_items, stream)
+               : launch_decode_e<Bf16, Bf16>(head_dim, group, km, vm, p, n_items, stream);
+  if (dtype == FI_DTYPE_FP16)
+    return fp8 ? launch_decode_e<Fp16, E4m3>(head_dim, group, km, vm, p, n_items, stream)
+               : launch_decode_e<Fp16, Fp16>(head_dim, group, km, vm, p, n_items, stream);
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace fi

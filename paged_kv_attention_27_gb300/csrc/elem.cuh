@@ -6,6 +6,7 @@
 
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
+#include <cuda_fp8.h>
 #include <stdint.h>
 
 namespace fi {
@@ -62,6 +63,30 @@ struct Fp16 {
         "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
         : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+  }
+};
+
+// FP8 E4M3 cache elements (OCP format): converted exactly to fp16 pairs by
+// the hardware conversion, then to floats.
+struct E4m3 {
+  static constexpr int kDtype = 2;          // FI_DTYPE_E4M3
+  // four packed e4m3 -> four floats (exact)
+  __device__ static __forceinline__ void unpack4(uint32_t w, float* f) {
+    const __half2_raw lo = __nv_cvt_fp8x2_to_halfraw2(__nv_fp8x2_storage_t(w & 0xffffu), __NV_E4M3);
+    const __half2_raw hi = __nv_cvt_fp8x2_to_halfraw2(__nv_fp8x2_storage_t(w >> 16), __NV_E4M3);
+    const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&lo));
+    const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&hi));
+    f[0] = a.x; f[1] = a.y; f[2] = b.x; f[3] = b.y;
+  }
+  // eight packed e4m3 (8 bytes) -> eight floats
+  __device__ static __forceinline__ void unpack8(const uint2& u, float (&f)[8]) {
+    unpack4(u.x, f);
+    unpack4(u.y, f + 4);
+  }
+  // two packed e4m3 (low 16 bits) -> an fp16 pair, first element low (exact)
+  __device__ static __forceinline__ uint32_t to_f16x2(uint32_t w) {
+    const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(__nv_fp8x2_storage_t(w & 0xffffu), __NV_E4M3);
+    return uint32_t(h.x) | (uint32_t(h.y) << 16);
   }
 };
 

@@ -63,7 +63,8 @@ struct Plan {
   int32_t mode = 0, batch = 0, num_qo_heads = 0, num_kv_heads = 0, head_dim = 0;
   int32_t page_size = 0, causal = 0, num_sms = 0;
   int32_t window_left = -1;              // -1: no window
-  int32_t dtype = FI_DTYPE_BF16;
+  int32_t dtype = FI_DTYPE_BF16;         // q and out
+  int32_t kv_dtype = FI_DTYPE_BF16;      // the K/V cache: dtype or FI_DTYPE_E4M3
   std::vector<WorkItem> decode_items;    // launch order
   std::vector<WorkItem> prefill_items;   // launch order
   std::vector<MergeTask> merges;

@@ -18,7 +18,8 @@ struct DecodeParams {
   int32_t page_size;
   int32_t num_qo_heads;
   int32_t layout;
-  float sm_scale;
+  float sm_scale;           // times the cache's key scale
+  float v_scale;            // the cache's value scale, applied to every output state
   void* out;
   float* lse;
   float* partial_o;
@@ -57,7 +58,8 @@ struct PrefillParams {
   int32_t layout;
   int32_t causal;
   int32_t window_left;  // -1: none; else row at key position pos keeps t >= pos - window_left
-  float sm_scale;
+  float sm_scale;       // times the cache's key scale
+  float v_scale;        // the cache's value scale
   void* out;
   float* lse;
   uint32_t* err;
@@ -70,8 +72,9 @@ struct PrefillParams {
 cudaError_t launch_prefill(int head_dim, int dtype, const CUtensorMap& qm, const CUtensorMap& km,
                            const CUtensorMap& vm, const PrefillParams& p, int grid,
                            cudaStream_t stream);
-// `dtype` (fi_dtype) selects the element type of q, K, V and out.
-cudaError_t launch_decode(int head_dim, int group, int dtype, const CUtensorMap& km,
+// `dtype` (fi_dtype) selects the element type of q and out, `kv_dtype` that
+// of the cache (dtype or FI_DTYPE_E4M3).
+cudaError_t launch_decode(int head_dim, int group, int dtype, int kv_dtype, const CUtensorMap& km,
                           const CUtensorMap& vm, const DecodeParams& p, int n_items,
                           cudaStream_t stream);
 cudaError_t launch_merge(const MergeParams& p, int n_rows, cudaStream_t stream);

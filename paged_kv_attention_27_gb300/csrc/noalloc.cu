@@ -46,8 +46,8 @@ void* g_scratch_ptr[kMaxDevices] = {};
 extern "C" fi_status fi_batch_decode_paged_noalloc(
     fi_plan_t plan, const void* q, const void* k_cache, const void* v_cache, int32_t kv_layout,
     int64_t page_stride_elems, int32_t num_pages, const int32_t* page_indptr_d,
-    const int32_t* page_indices_d, const int32_t* last_page_len_d, float sm_scale, void* out,
-    float* lse, void* stream) {
+    const int32_t* page_indices_d, const int32_t* last_page_len_d, float sm_scale, float k_scale,
+    float v_scale, void* out, float* lse, void* stream) {
   if (!plan) return FI_ERR_INVALID_ARG;
   if (plan->p.ws.total > kNoAllocScratchBytes) return FI_ERR_WORKSPACE_TOO_SMALL;
   int dev = -1;
@@ -71,5 +71,6 @@ extern "C" fi_status fi_batch_decode_paged_noalloc(
   }
   return fi_batch_decode_paged(plan, q, k_cache, v_cache, kv_layout, page_stride_elems,
                                num_pages, page_indptr_d, page_indices_d, last_page_len_d,
-                               sm_scale, out, lse, scratch, kNoAllocScratchBytes, stream);
+                               sm_scale, k_scale, v_scale, out, lse, scratch,
+                               kNoAllocScratchBytes, stream);
 }

@@ -33,6 +33,8 @@ fi_status build_plan(int32_t mode, int32_t batch, const int32_t* qo_indptr,
   const fi_plan_options opt = options ? *options : fi_plan_options FI_PLAN_OPTIONS_DEFAULT;
   if (opt.window_left < -1) return FI_ERR_INVALID_ARG;
   if (opt.dtype != FI_DTYPE_BF16 && opt.dtype != FI_DTYPE_FP16) return FI_ERR_INVALID_ARG;
+  const int32_t kv_dtype = opt.kv_dtype < 0 ? opt.dtype : opt.kv_dtype;
+  if (kv_dtype != opt.dtype && kv_dtype != FI_DTYPE_E4M3) return FI_ERR_INVALID_ARG;
   if (mode != FI_MODE_DECODE && mode != FI_MODE_PREFILL) return FI_ERR_INVALID_ARG;
   if (batch < 0 || num_sms <= 0) return FI_ERR_INVALID_ARG;
   if (num_qo_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 || page_size <= 0)
@@ -57,6 +59,9 @@ fi_status build_plan(int32_t mode, int32_t batch, const int32_t* qo_indptr,
   p.num_sms = num_sms;
   p.window_left = opt.window_left;
   p.dtype = opt.dtype;
+  p.kv_dtype = kv_dtype;
+  // an FP8 cache is read by the decode kernel only
+  if (kv_dtype == FI_DTYPE_E4M3 && mode != FI_MODE_DECODE) return FI_ERR_UNSUPPORTED;
 
   // ---- validate the page table and the query packing; kv_len per request
   std::vector<int64_t> kv_len(batch), qo_len(batch), qo_start(batch);

@@ -635,7 +635,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
       // ---- epilogue: O / lp (bf16 or fp16) and lse = ln(l) + m ln 2
       const int rows = min(C::M, rb.q_end - w.q_row);
       const bool row_ok = t < rows;
-      const float inv = lp > 0.f ? 1.f / lp : 0.f;
+      const float inv = lp > 0.f ? prm.v_scale / lp : 0.f;
       const size_t out_row = size_t(w.q_row) + t;
       uint16_t* op = reinterpret_cast<uint16_t*>(prm.out) +
                      (out_row * prm.num_qo_heads + w.head) * HEAD_DIM;

@@ -15,12 +15,15 @@ from .synth import PagedBatch
 
 
 TORCH_DTYPES = {"bf16": torch.bfloat16, "fp16": torch.float16}
-FI_DTYPES = {"bf16": B.FI_DTYPE_BF16, "fp16": B.FI_DTYPE_FP16}
+FI_DTYPES = {"bf16": B.FI_DTYPE_BF16, "fp16": B.FI_DTYPE_FP16, "e4m3": B.FI_DTYPE_E4M3}
 
 
 def bf16_tensor(bits: np.ndarray, device="cuda", dtype: str = "bf16") -> torch.Tensor:
-    """uint16 bit patterns of `dtype` (bf16 by default, or fp16) -> a torch
-    tensor of that type on `device`."""
+    """Bit patterns of `dtype` -> a torch tensor on `device`: bf16 / fp16
+    (uint16 patterns) as torch.bfloat16 / torch.float16, e4m3 (uint8 codes)
+    as raw uint8 bytes."""
+    if dtype == "e4m3":
+        return torch.from_numpy(np.ascontiguousarray(bits, dtype=np.uint8)).to(device)
     t = torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(TORCH_DTYPES[dtype])
     return t.to(device)
 
@@ -31,9 +34,10 @@ def i32_tensor(a: np.ndarray, device="cuda") -> torch.Tensor:
 
 def plan_options(b: PagedBatch):
     """fi_plan options of a batch (None = the defaults)."""
-    if b.window_left < 0 and b.dtype == "bf16":
+    if b.window_left < 0 and b.dtype == "bf16" and b.cache_dtype == "bf16":
         return None
-    return {"window_left": int(b.window_left), "dtype": FI_DTYPES[b.dtype]}
+    return {"window_left": int(b.window_left), "dtype": FI_DTYPES[b.dtype],
+            "kv_dtype": FI_DTYPES[b.cache_dtype]}
 
 
 def num_sms(device="cuda") -> int:
@@ -47,8 +51,8 @@ class DeviceBatch:
         self.b = b
         self.device = device
         self.q = bf16_tensor(b.q, device, b.dtype)
-        self.k = bf16_tensor(b.k_cache, device, b.dtype)
-        self.v = bf16_tensor(b.v_cache, device, b.dtype)
+        self.k = bf16_tensor(b.k_cache, device, b.cache_dtype)
+        self.v = bf16_tensor(b.v_cache, device, b.cache_dtype)
         self.page_indptr = i32_tensor(b.page_indptr, device)
         self.page_indices = i32_tensor(b.page_indices if b.page_indices.size else np.zeros(1),
                                        device)
@@ -75,13 +79,13 @@ class DeviceBatch:
         if self.mode == B.FI_MODE_DECODE:
             B.fi_batch_decode_paged(self.plan, self.q, self.k, self.v, layout, 0, b.num_pages,
                                     self.page_indptr, self.page_indices, self.last_page_len,
-                                    b.sm_scale, self.out, self.lse, self.workspace,
-                                    stream=stream)
+                                    b.sm_scale, b.k_scale, b.v_scale, self.out, self.lse,
+                                    self.workspace, stream=stream)
         else:
             B.fi_batch_prefill_paged(self.plan, self.q, self.qo_indptr, self.k, self.v, layout, 0,
                                      b.num_pages, self.page_indptr, self.page_indices,
-                                     self.last_page_len, b.sm_scale, self.out, self.lse,
-                                     self.workspace, stream=stream)
+                                     self.last_page_len, b.sm_scale, b.k_scale, b.v_scale,
+                                     self.out, self.lse, self.workspace, stream=stream)
         return self.out, self.lse
 
     def status(self, stream=None) -> int:

@@ -264,15 +264,22 @@ def tiny_decode(seed: int = 0) -> PagedBatch:
                       [1, 17, 64, 100], [1, 1, 1, 1], 8, 2, 64, 16, NHD, 1.0 / 8, False, seed)
 
 
-def llama7b_decode(seed: int = 1, batch: int = 64, dtype: str = "bf16") -> PagedBatch:
+def _fp8_scale(kv_dtype: str) -> float:
+    # an FP8 cache stores N(0,1) draws times 16 (|x| < 448 for any practical
+    # draw), so that the small values keep their 3 mantissa bits
+    return 1.0 / 16 if kv_dtype == "e4m3" else 1.0
+
+
+def llama7b_decode(seed: int = 1, batch: int = 64, dtype: str = "bf16",
+                   kv_dtype: str = "") -> PagedBatch:
     """Llama-7B-shaped decode: 32/32 heads, d=128, P=16, KV ~ U[512,4096], NHD."""
     g = philox(seed + 1000)
     kv = g.integers(512, 4097, size=batch)
-    tname = "" if dtype == "bf16" else f" {dtype}"
+    tname = ("" if dtype == "bf16" else f" {dtype}") + (f" {kv_dtype} cache" if kv_dtype else "")
     return make_batch(f"Llama-7B-shaped batch decode B{batch} Hq32 Hkv32 d128 P16 kv~U[512,4096] "
                       f"NHD{tname}",
                       kv, np.ones(batch, np.int64), 32, 32, 128, 16, NHD, None, False, seed,
-                      dtype=dtype)
+                      dtype=dtype, kv_dtype=kv_dtype, kv_scale=_fp8_scale(kv_dtype))
 
 
 def lognormal_lengths(gen, n, median=2048, sigma=1.0, lo=1, hi=32768):
@@ -281,7 +288,7 @@ def lognormal_lengths(gen, n, median=2048, sigma=1.0, lo=1, hi=32768):
 
 
 def llama70b_gqa_decode(seed: int = 2, batch: int = 128, shared: int = 32,
-                        window_left: int = -1) -> PagedBatch:
+                        window_left: int = -1, kv_dtype: str = "") -> PagedBatch:
     """Llama2-70B-shaped GQA decode: 64/8 heads, d=128, P=16, HND,
     KV ~ lognormal(median 2048, sigma 1) clipped to [1,32768]; the first 32
     requests share the physical pages of one 1024-token prefix. Optionally a
@@ -290,11 +297,13 @@ def llama70b_gqa_decode(seed: int = 2, batch: int = 128, shared: int = 32,
     kv = lognormal_lengths(g, batch)
     kv[:shared] = np.maximum(kv[:shared], 1024)
     wname = f" window {window_left + 1}" if window_left >= 0 else ""
+    wname += f" {kv_dtype} cache" if kv_dtype else ""
     return make_batch(f"Llama2-70B-shaped GQA decode B{batch} Hq64 Hkv8 d128 P16 HND lognormal(2048) "
                       f"{shared} share a 1024-token prefix{wname}",
                       kv, np.ones(batch, np.int64), 64, 8, 128, 16, HND, None, False, seed,
                       shared_prefix_requests=shared, shared_prefix_tokens=1024,
-                      window_left=window_left)
+                      window_left=window_left, kv_dtype=kv_dtype,
+                      kv_scale=_fp8_scale(kv_dtype))
 
 
 def causal_prefill(seq_len: int, batch: int = 8, seed: int = 3,

@@ -208,6 +208,9 @@ def test_windowed_prefill_items_start_on_the_page_of_the_first_row_window(causal
     ("no_sms", B.FI_ERR_INVALID_ARG),
     ("window_below_minus_one", B.FI_ERR_INVALID_ARG),
     ("dtype_unknown", B.FI_ERR_INVALID_ARG),
+    ("q_dtype_e4m3", B.FI_ERR_INVALID_ARG),
+    ("kv_dtype_other_16bit", B.FI_ERR_INVALID_ARG),
+    ("fp8_cache_prefill_plan", B.FI_ERR_UNSUPPORTED),
 ])
 def test_plan_validation(case, status):
     args = dict(mode=B.FI_MODE_DECODE, batch_size=2, qo_indptr_h=None,
@@ -242,6 +245,13 @@ def test_plan_validation(case, status):
         args["options"] = {"window_left": -2}
     elif case == "dtype_unknown":
         args["options"] = {"dtype": 7}
+    elif case == "q_dtype_e4m3":
+        args["options"] = {"dtype": B.FI_DTYPE_E4M3}
+    elif case == "kv_dtype_other_16bit":
+        args["options"] = {"dtype": B.FI_DTYPE_BF16, "kv_dtype": B.FI_DTYPE_FP16}
+    elif case == "fp8_cache_prefill_plan":
+        args.update(mode=B.FI_MODE_PREFILL, qo_indptr_h=[0, 2, 3],
+                    options={"kv_dtype": B.FI_DTYPE_E4M3})
     with pytest.raises(B.FiError) as e:
         B.fi_plan(**args)
     assert e.value.status == status
@@ -264,7 +274,8 @@ def test_workspace_too_small_and_bad_args_return_before_any_launch():
         pytest.skip("uses fake device addresses; only meaningful without a GPU")
     p = B.fi_plan(B.FI_MODE_DECODE, 2, None, [0, 2, 3], [5, 16], 8, 2, 128, 16, 0, None, 4)
     fake = 1 << 20   # aligned, never dereferenced: every call below returns first
-    args = [p, fake, fake, fake, B.FI_LAYOUT_NHD, 0, 4, fake, fake, fake, 0.1, fake, fake, fake]
+    args = [p, fake, fake, fake, B.FI_LAYOUT_NHD, 0, 4, fake, fake, fake, 0.1, 1.0, 1.0, fake,
+            fake, fake]
     with pytest.raises(B.FiError) as e:
         B.fi_batch_decode_paged(*args, workspace_bytes=16, stream=0)
     assert e.value.status == B.FI_ERR_WORKSPACE_TOO_SMALL
@@ -279,12 +290,18 @@ def test_workspace_too_small_and_bad_args_return_before_any_launch():
         B.fi_batch_decode_paged(*bad, stream=0)
     assert e.value.status == B.FI_ERR_INVALID_ARG
     with pytest.raises(B.FiError) as e:      # prefill call with a decode plan
-        B.fi_batch_prefill_paged(p, fake, fake, fake, fake, 0, 0, 4, fake, fake, fake, 0.1,
-                                 fake, fake, fake, stream=0)
+        B.fi_batch_prefill_paged(p, fake, fake, fake, fake, 0, 0, 4, fake, fake, fake, 0.1, 1.0,
+                                 1.0, fake, fake, fake, stream=0)
     assert e.value.status == B.FI_ERR_INVALID_ARG
     for bad_scale in (-0.1, float("nan"), float("inf")):
         bad = list(args)
         bad[10] = bad_scale    # sm_scale must be finite and >= 0
+        with pytest.raises(B.FiError) as e:
+            B.fi_batch_decode_paged(*bad, stream=0)
+        assert e.value.status == B.FI_ERR_INVALID_ARG
+    for pos, bad_scale in ((11, 0.0), (11, float("nan")), (12, -1.0), (12, float("inf"))):
+        bad = list(args)
+        bad[pos] = bad_scale   # k_scale and v_scale must be finite and > 0
         with pytest.raises(B.FiError) as e:
             B.fi_batch_decode_paged(*bad, stream=0)
         assert e.value.status == B.FI_ERR_INVALID_ARG

@@ -32,7 +32,8 @@ def _oracle(b, requests=None):
     return oracle.batch_attention(b.q, b.qo_indptr, b.k_cache, b.v_cache, b.layout, b.page_indptr,
                                   b.page_indices, b.last_page_len, b.num_qo_heads, b.num_kv_heads,
                                   b.page_size, b.sm_scale, b.causal, requests=requests,
-                                  window_left=b.window_left, dtype=b.dtype)
+                                  window_left=b.window_left, dtype=b.dtype,
+                                  kv_dtype=b.cache_dtype, k_scale=b.k_scale, v_scale=b.v_scale)
 
 
 def _rows(b, requests):
@@ -128,7 +129,7 @@ def test_layouts_agree_and_page_stride_views():
     out = torch.empty_like(db.out)
     B.fi_batch_decode_paged(db.plan, db.q, kvt[:, 0], kvt[:, 1], B.FI_LAYOUT_NHD, 2 * page_elems,
                             b.num_pages, db.page_indptr, db.page_indices, db.last_page_len,
-                            b.sm_scale, out, None, db.workspace)
+                            b.sm_scale, 1.0, 1.0, out, None, db.workspace)
     torch.cuda.synchronize()
     assert torch.equal(out, o_nhd)
 
@@ -226,3 +227,35 @@ def test_fp16_merge_states_abi():
                       B.FI_DTYPE_FP16, out, lse)
     torch.cuda.synchronize()
     compare(out, lse, ref_o, ref_l, what="merge_states fp16")
+
+
+# ---- FP8 (E4M3) cache --------------------------------------------------------
+
+@pytest.mark.parametrize("g,d", [(1, 128), (8, 128), (4, 64), (2, 256), (1, 64), (8, 256)])
+@pytest.mark.parametrize("dtype", ["bf16", "fp16"])
+def test_fp8_cache_decode(g, d, dtype):
+    """An E4M3 cache (stored values times 16) with the per-tensor scales
+    passed to the run call; SIMT and tensor-core consumers; splits; NaN in
+    the unused tail slots."""
+    hkv = 2
+    kv = [1, 16, 17, 300, 2049, 9000]
+    b = synth.make_batch(f"fp8 g{g} d{d} {dtype}", kv, [1] * len(kv), g * hkv, hkv, d, 16,
+                         synth.NHD if g % 2 else synth.HND, None, False, 700 + g + d,
+                         dtype=dtype, kv_dtype="e4m3", kv_scale=1 / 16, tail_fill="nan")
+    assert b.k_cache.dtype == np.uint8
+    check(b, sms=8)
+
+
+def test_fp8_cache_scales_and_window():
+    b = synth.make_batch("fp8 scales window", [5000, 77, 1300], [1, 1, 1], 16, 2, 128, 32,
+                         synth.HND, None, False, 710, kv_dtype="e4m3", kv_scale=1 / 8,
+                         window_left=1000)
+    b.k_scale, b.v_scale = 0.1, 0.3      # any positive scales: the kernel folds them
+    check(b, sms=16)
+
+
+def test_fp8_cache_70b_full_size_sampled():
+    b = synth.llama70b_gqa_decode(kv_dtype="e4m3")
+    order = np.argsort(-b.kv_lens)
+    sample = sorted(set(order[:3].tolist() + order[-3:].tolist() + [0, 5, 31, 32, 77]))
+    check(b, requests=sample)

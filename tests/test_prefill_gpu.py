@@ -38,7 +38,8 @@ def _oracle(b, rows=None, requests=None):
     return oracle.batch_attention(b.q, b.qo_indptr, b.k_cache, b.v_cache, b.layout, b.page_indptr,
                                   b.page_indices, b.last_page_len, b.num_qo_heads, b.num_kv_heads,
                                   b.page_size, b.sm_scale, b.causal, requests=requests, rows=rows,
-                                  window_left=b.window_left, dtype=b.dtype)
+                                  window_left=b.window_left, dtype=b.dtype,
+                                  kv_dtype=b.cache_dtype, k_scale=b.k_scale, v_scale=b.v_scale)
 
 
 def check_full(b, what=None):

@@ -32,7 +32,7 @@ def _both(b):
     lse = torch.full_like(db.lse, float("nan"))
     B.fi_batch_decode_paged_noalloc(db.plan, db.q, db.k, db.v, B.LAYOUTS[b.layout], 0,
                                     b.num_pages, db.page_indptr, db.page_indices,
-                                    db.last_page_len, b.sm_scale, out, lse)
+                                    db.last_page_len, b.sm_scale, 1.0, 1.0, out, lse)
     torch.cuda.synchronize()
     return db, out, lse, ref_out, ref_lse
 
@@ -81,6 +81,6 @@ def test_noalloc_rejects_plans_beyond_its_scratch():
     assert plan.workspace_bytes > (16 << 20)
     x = torch.empty(16, device="cuda")
     with pytest.raises(B.FiError) as e:
-        B.fi_batch_decode_paged_noalloc(plan, x, x, x, 0, 0, 1, x, x, x, 0.1, x, None)
+        B.fi_batch_decode_paged_noalloc(plan, x, x, x, 0, 0, 1, x, x, x, 0.1, 1.0, 1.0, x, None)
     assert e.value.status == B.FI_ERR_WORKSPACE_TOO_SMALL
     del kv
