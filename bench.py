@@ -78,6 +78,8 @@ WORKLOADS = {
     "causal_prefill_4k_fp16": ("causal_prefill", {"seq_len": 4096, "dtype": "fp16"}),
     "llama7b_decode_fp16": ("llama7b_decode", {"dtype": "fp16"}),
     "llama7b_decode_fp8kv": ("llama7b_decode", {"kv_dtype": "e4m3"}),
+    "shared_prefix_decode": ("shared_prefix_decode", {}),
+    "shared_prefix_decode_flat": ("shared_prefix_decode", {"cascade": False}),
     "llama70b_gqa_decode_fp8kv": ("llama70b_gqa_decode", {"kv_dtype": "e4m3"}),
     "ragged_prefill": ("ragged_prefill", {}),
     "mixed_chunk_decode": ("mixed_chunk_decode", {}),

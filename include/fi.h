@@ -100,14 +100,35 @@ typedef enum { FI_DTYPE_BF16 = 0, FI_DTYPE_FP16 = 1, FI_DTYPE_E4M3 = 2 } fi_dtyp
  *                an FP8 cache (decode plans only; FI_ERR_UNSUPPORTED for
  *                prefill plans). An FP8 cache holds K / k_scale and
  *                V / v_scale; the run calls take the two scales.
+ *   num_prefix_groups, prefix_group_indptr, prefix_pages
+ *                shared-prefix (cascade) decode: the "FlashInfer kernel
+ *                library deep-dive" page, section "batch layer", lists
+ *                shared-prefix optimisation (find the prefix that sequences
+ *                have in common and reuse it) among the batch kernels'
+ *                techniques. Group g is requests
+ *                prefix_group_indptr[g] .. prefix_group_indptr[g+1]-1 (host
+ *                int32 [num_prefix_groups+1], non-decreasing, groups of
+ *                consecutive requests), whose first prefix_pages[g] pages
+ *                (host int32 [num_prefix_groups], >= 1, full pages of every
+ *                request in the group) are the same physical pages (caller
+ *                contract: the library reads the group's first request's
+ *                page ids). The prefix is attended once per group for all of
+ *                the group's query rows on the tensor cores, each request's
+ *                own pages by the decode kernel, and the two states are
+ *                merged by log-sum-exp. Decode plans with a 16-bit cache and
+ *                no window only (else FI_ERR_UNSUPPORTED); 0 / NULL = none.
+ *                The arrays are read by fi_plan only.
  */
 typedef struct {
   int32_t window_left;
   int32_t dtype;
   int32_t kv_dtype;
+  int32_t num_prefix_groups;
+  const int32_t* prefix_group_indptr;
+  const int32_t* prefix_pages;
 } fi_plan_options;
 
-#define FI_PLAN_OPTIONS_DEFAULT {-1, FI_DTYPE_BF16, -1}
+#define FI_PLAN_OPTIONS_DEFAULT {-1, FI_DTYPE_BF16, -1, 0, NULL, NULL}
 
 typedef struct fi_plan_s* fi_plan_t;
 
@@ -115,14 +136,16 @@ typedef struct fi_plan_s* fi_plan_t;
 typedef struct {
   int32_t mode;             /* fi_mode */
   int32_t batch_size;
-  int32_t num_items;        /* CTAs of the main attention launch(es) */
+  int32_t num_items;        /* work items of all launches */
   int32_t num_decode_items; /* of which single-row (decode) work */
-  int32_t num_prefill_items;
+  int32_t num_prefill_items;/* multi-row (prefill) work */
   int32_t chunk_tokens;     /* split-KV chunk length of decode work (0 = no split) */
   int32_t num_split_requests;
   int32_t num_partial_slots;/* rows of fp32 partial states in the workspace */
   int64_t workspace_bytes;
   int64_t total_kv_tokens;  /* sum of kv_len */
+  int32_t num_prefix_items; /* shared-prefix work (prefix chunk x row tile x head) */
+  int32_t num_prefix_groups;
 } fi_plan_info;
 
 /*
@@ -174,7 +197,10 @@ fi_status fi_plan_get_info(fi_plan_t plan, fi_plan_info* info);
  * (into page_indices), number of pages, first key, end key, partial slot or
  * -1, first row of q}. Keys are token positions within the request; the
  * first page holds the first key at slot (first key % page_size), earlier
- * slots of that page lie outside the item's window.
+ * slots of that page lie outside the item's window. Decode items come
+ * first, then prefill items, then shared-prefix items (request = 2 x the
+ * group index, keys within the group's prefix, slot = the state slot of
+ * row 0 of q).
  * `capacity` is in items; *num_items receives the plan's item count.
  */
 fi_status fi_plan_get_work(fi_plan_t plan, int32_t* items_h, int32_t capacity,

@@ -54,9 +54,10 @@ class FiError(RuntimeError):
 
 class PlanOptions(ctypes.Structure):
     """fi_plan_options: window_left (-1 = none), dtype and kv_dtype (FI_DTYPE_*;
-    kv_dtype -1 = dtype)."""
+    kv_dtype -1 = dtype), and the shared-prefix groups."""
     _fields_ = [("window_left", ctypes.c_int32), ("dtype", ctypes.c_int32),
-                ("kv_dtype", ctypes.c_int32)]
+                ("kv_dtype", ctypes.c_int32), ("num_prefix_groups", ctypes.c_int32),
+                ("prefix_group_indptr", ctypes.c_void_p), ("prefix_pages", ctypes.c_void_p)]
 
 
 class PlanInfo(ctypes.Structure):
@@ -64,7 +65,8 @@ class PlanInfo(ctypes.Structure):
                 ("num_items", ctypes.c_int32), ("num_decode_items", ctypes.c_int32),
                 ("num_prefill_items", ctypes.c_int32), ("chunk_tokens", ctypes.c_int32),
                 ("num_split_requests", ctypes.c_int32), ("num_partial_slots", ctypes.c_int32),
-                ("workspace_bytes", ctypes.c_int64), ("total_kv_tokens", ctypes.c_int64)]
+                ("workspace_bytes", ctypes.c_int64), ("total_kv_tokens", ctypes.c_int64),
+                ("num_prefix_items", ctypes.c_int32), ("num_prefix_groups", ctypes.c_int32)]
 
 
 _lib = None
@@ -165,13 +167,22 @@ class Plan:
 def fi_plan(mode, batch_size, qo_indptr_h, page_indptr_h, last_page_len_h, num_qo_heads,
             num_kv_heads, head_dim, page_size, causal, options, num_sms) -> Plan:
     """``options``: None (the defaults) or a dict with any of ``window_left``,
-    ``dtype`` and ``kv_dtype``."""
+    ``dtype``, ``kv_dtype`` and the shared-prefix groups ``prefix_group_indptr``
+    / ``prefix_pages`` (host arrays)."""
     qo, pi, lp = _i32(qo_indptr_h), _i32(page_indptr_h), _i32(last_page_len_h)
     opt = None
+    keep = []
     if options is not None:
+        gi = options.get("prefix_group_indptr")
+        pg = options.get("prefix_pages")
+        n_groups = 0
+        if gi is not None:
+            gi, pg = _i32(gi), _i32(pg)
+            keep += [gi, pg]
+            n_groups = len(gi) - 1
         opt = PlanOptions(int(options.get("window_left", -1)),
                           int(options.get("dtype", FI_DTYPE_BF16)),
-                          int(options.get("kv_dtype", -1)))
+                          int(options.get("kv_dtype", -1)), n_groups, _ptr(gi), _ptr(pg))
     h = _P()
     ws = ctypes.c_size_t()
     st = lib().fi_plan(int(mode), int(batch_size), _ptr(qo), _ptr(pi), _ptr(lp), int(num_qo_heads),

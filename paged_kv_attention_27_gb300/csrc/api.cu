@@ -90,16 +90,24 @@ thread_local Staging g_staging;
 // counter), work lists, merge tasks, zeroed merge counters; alignment gaps
 // zeroed too. `dst` holds P.ws.partial_o bytes.
 void fill_image(uint8_t* dst, const fi::Plan& P) {
-  const size_t n_dec = P.decode_items.size() * sizeof(fi::WorkItem);
-  const size_t n_pre = P.prefill_items.size() * sizeof(fi::WorkItem);
-  const size_t n_mrg = P.merges.size() * sizeof(fi::MergeTask);
-  std::memset(dst, 0, P.ws.decode_items);
-  if (n_dec) std::memcpy(dst + P.ws.decode_items, P.decode_items.data(), n_dec);
-  std::memset(dst + P.ws.decode_items + n_dec, 0, P.ws.prefill_items - P.ws.decode_items - n_dec);
-  if (n_pre) std::memcpy(dst + P.ws.prefill_items, P.prefill_items.data(), n_pre);
-  std::memset(dst + P.ws.prefill_items + n_pre, 0, P.ws.merges - P.ws.prefill_items - n_pre);
-  if (n_mrg) std::memcpy(dst + P.ws.merges, P.merges.data(), n_mrg);
-  std::memset(dst + P.ws.merges + n_mrg, 0, P.ws.partial_o - P.ws.merges - n_mrg);
+  // consecutive regions [offset, next offset): the data, then zeros
+  struct Region { size_t off, end; const void* src; size_t bytes; };
+  const Region regions[] = {
+      {0, P.ws.decode_items, nullptr, 0},
+      {P.ws.decode_items, P.ws.prefill_items, P.decode_items.data(),
+       P.decode_items.size() * sizeof(fi::WorkItem)},
+      {P.ws.prefill_items, P.ws.prefix_items, P.prefill_items.data(),
+       P.prefill_items.size() * sizeof(fi::WorkItem)},
+      {P.ws.prefix_items, P.ws.prefix_tables, P.prefix_items.data(),
+       P.prefix_items.size() * sizeof(fi::WorkItem)},
+      {P.ws.prefix_tables, P.ws.merges, P.prefix_tables.data(),
+       P.prefix_tables.size() * sizeof(int32_t)},
+      {P.ws.merges, P.ws.partial_o, P.merges.data(), P.merges.size() * sizeof(fi::MergeTask)},
+  };
+  for (const Region& r : regions) {
+    if (r.bytes) std::memcpy(dst + r.off, r.src, r.bytes);
+    std::memset(dst + r.off + r.bytes, 0, r.end - r.off - r.bytes);
+  }
 }
 
 fi_status upload_image(void* dst, const fi::Plan& P, cudaStream_t stream) {
@@ -303,7 +311,7 @@ fi_status run_paged(fi_plan_t plan, bool prefill_call, const void* q, const int3
   float* partial_lse = reinterpret_cast<float*>(ws + P.ws.partial_lse);
 
   CUtensorMap qmap;
-  if (!P.prefill_items.empty()) {
+  if (!P.prefill_items.empty() || !P.prefix_items.empty()) {
     st = make_q_map(&qmap, q, P.total_q, P.num_qo_heads, P.head_dim, P.dtype);
     if (st != FI_OK) return st;
   }
@@ -357,8 +365,44 @@ fi_status run_paged(fi_plan_t plan, bool prefill_call, const void* q, const int3
     pp.fault_kind = fault_kind;
     pp.n_items = int(P.prefill_items.size());
     pp.work_counter = reinterpret_cast<uint32_t*>(ws + fi::kWorkCounterOffset);
+    pp.state_o = nullptr;
+    pp.state_lse = nullptr;
     e = fi::launch_prefill(P.head_dim, P.dtype, qmap, kmap, vmap, pp, P.num_sms, stream);
     if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
+  }
+  if (!P.prefix_items.empty()) {
+    // Shared prefixes: each group's rows of q against chunks of its prefix,
+    // on the prefill kernel, writing fp32 states (row r of q -> slot
+    // item.slot + r) that the decode kernel merges with the rest. Same
+    // stream, before the decode launch.
+    const int32_t* tables = reinterpret_cast<const int32_t*>(ws + P.ws.prefix_tables);
+    const int G2 = 2 * P.num_prefix_groups;
+    fi::PrefillParams pp;
+    pp.items = reinterpret_cast<const fi::WorkItem*>(ws + P.ws.prefix_items);
+    pp.qo_indptr = tables;
+    pp.page_indptr = tables + G2;
+    pp.last_page_len = tables + 2 * G2;
+    pp.page_indices = page_indices_d;
+    pp.num_pages = num_pages;
+    pp.page_size = P.page_size;
+    pp.num_qo_heads = P.num_qo_heads;
+    pp.group = P.num_qo_heads / P.num_kv_heads;
+    pp.layout = kv_layout;
+    pp.causal = 0;
+    pp.window_left = -1;
+    pp.sm_scale = sm_scale * k_scale;
+    pp.v_scale = v_scale;
+    pp.out = nullptr;
+    pp.lse = nullptr;
+    pp.state_o = partial_o;
+    pp.state_lse = partial_lse;
+    pp.err = err;
+    pp.wait_limit_ns = g_wait_limit_ns;
+    pp.fault_kind = 0;
+    pp.n_items = int(P.prefix_items.size());
+    pp.work_counter = reinterpret_cast<uint32_t*>(ws + fi::kWorkCounterOffset);
+    e = fi::launch_prefill(P.head_dim, P.dtype, qmap, kmap, vmap, pp, P.num_sms, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "shared-prefix launch");
   }
   if (!P.decode_items.empty()) {
     fi::DecodeParams dp;
@@ -435,7 +479,9 @@ fi_status fi_plan_get_info(fi_plan_t plan, fi_plan_info* info) {
   info->batch_size = P.batch;
   info->num_decode_items = int32_t(P.decode_items.size());
   info->num_prefill_items = int32_t(P.prefill_items.size());
-  info->num_items = info->num_decode_items + info->num_prefill_items;
+  info->num_prefix_items = int32_t(P.prefix_items.size());
+  info->num_prefix_groups = P.num_prefix_groups;
+  info->num_items = info->num_decode_items + info->num_prefill_items + info->num_prefix_items;
   info->chunk_tokens = P.chunk_tokens;
   info->num_split_requests = P.num_split;
   info->num_partial_slots = P.num_slots;
@@ -448,13 +494,14 @@ fi_status fi_plan_get_work(fi_plan_t plan, int32_t* items_h, int32_t capacity,
                            int32_t* num_items) {
   if (!plan || !num_items) return FI_ERR_INVALID_ARG;
   const fi::Plan& P = plan->p;
-  const int32_t n = int32_t(P.decode_items.size() + P.prefill_items.size());
+  const int32_t n =
+      int32_t(P.decode_items.size() + P.prefill_items.size() + P.prefix_items.size());
   *num_items = n;
   if (!items_h) return FI_OK;
   if (capacity < n) return FI_ERR_INVALID_ARG;
   // the first 8 fields of each item, as the header documents
   int32_t* dst = items_h;
-  for (const auto* list : {&P.decode_items, &P.prefill_items}) {
+  for (const auto* list : {&P.decode_items, &P.prefill_items, &P.prefix_items}) {
     for (const fi::WorkItem& w : *list) {
       const int32_t f[8] = {w.req, w.head, w.page_begin, w.n_pages, w.tok_begin, w.tok_end,
                             w.slot, w.q_row};

@@ -645,7 +645,13 @@ decode_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant__
           const bool fits = mt.n_states * GROUP <= C::NCW * GROUP * HEAD_DIM;
           if (tid < GROUP) {
             const int hq = item.head * GROUP + tid;
+            // the chunks' states, and the row's shared-prefix states (if any)
+            auto xlse = [&](int e) {
+              return __ldcg(&prm.partial_lse[size_t(mt.extra_slot + e * mt.extra_stride) *
+                                             prm.num_qo_heads + hq]);
+            };
             float M = -INFINITY;
+            for (int e = 0; e < mt.n_extra; ++e) M = fmaxf(M, xlse(e));
             for (int i = 0; i < mt.n_states; ++i)
               M = fmaxf(M, __ldcg(&prm.partial_lse[size_t(mt.slot_base + i) * prm.num_qo_heads + hq]));
             float sw = 0.f;
@@ -656,6 +662,7 @@ decode_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant__
                 if (fits) wgt[i * GROUP + tid] = w;   // -inf -> 0
                 sw += w;
               }
+              for (int e = 0; e < mt.n_extra; ++e) sw += ex2((xlse(e) - M) * kLog2e);
             } else if (fits) {
               for (int i = 0; i < mt.n_states; ++i) wgt[i * GROUP + tid] = 0.f;
             }
@@ -675,6 +682,11 @@ decode_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant__
                 const size_t row = size_t(mt.slot_base + i) * prm.num_qo_heads + hq;
                 const float w = fits ? wgt[i * GROUP + h]
                                      : ex2((__ldcg(&prm.partial_lse[row]) - M) * kLog2e);
+                acc = fmaf(w, __ldcg(&prm.partial_o[row * HEAD_DIM + dd]), acc);
+              }
+              for (int e = 0; e < mt.n_extra; ++e) {
+                const size_t row = size_t(mt.extra_slot + e * mt.extra_stride) * prm.num_qo_heads + hq;
+                const float w = ex2((__ldcg(&prm.partial_lse[row]) - M) * kLog2e);
                 acc = fmaf(w, __ldcg(&prm.partial_o[row * HEAD_DIM + dd]), acc);
               }
             }

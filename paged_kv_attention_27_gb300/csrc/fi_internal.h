@@ -37,8 +37,11 @@ static_assert(sizeof(WorkItem) == 36, "work item is 9 int32");
 struct MergeTask {
   int32_t out_row;
   int32_t slot_base;
-  int32_t n_states;
-  int32_t pad;
+  int32_t n_states;      // states in slots [slot_base, slot_base + n_states), one per decode CTA
+  int32_t extra_slot;    // first shared-prefix state of the row, or -1
+  int32_t n_extra;       // shared-prefix states: extra_slot + e * extra_stride, e < n_extra
+  int32_t extra_stride;
+  int32_t pad[2];
 };
 
 constexpr int kPrefillTileM = 128;         // query rows per prefill CTA
@@ -54,8 +57,8 @@ inline int decode_tile_tokens(int head_dim) { return 8192 / head_dim; }  // 32 K
 inline int prefill_kv_tile(int head_dim) { return head_dim <= 128 ? 128 : 64; }
 
 struct WorkspaceLayout {
-  size_t decode_items = 0, prefill_items = 0, merges = 0, merge_counters = 0, partial_o = 0,
-         partial_lse = 0;
+  size_t decode_items = 0, prefill_items = 0, prefix_items = 0, prefix_tables = 0, merges = 0,
+         merge_counters = 0, partial_o = 0, partial_lse = 0;
   size_t total = 0;
 };
 
@@ -68,6 +71,14 @@ struct Plan {
   std::vector<WorkItem> decode_items;    // launch order
   std::vector<WorkItem> prefill_items;   // launch order
   std::vector<MergeTask> merges;
+  // shared-prefix decode: prefill-kernel items over chunks of each group's
+  // prefix (virtual request 2g = group g: its rows of q, one head, the
+  // prefix keys; an item's `slot` plus a row of q is the row's state slot),
+  // and the virtual requests' qo_indptr / page_indptr / last_page_len (each
+  // 2 * groups entries, uploaded with the work lists)
+  std::vector<WorkItem> prefix_items;
+  std::vector<int32_t> prefix_tables;
+  int32_t num_prefix_groups = 0;
   int32_t chunk_tokens = 0;
   int32_t num_split = 0;
   int32_t num_slots = 0;

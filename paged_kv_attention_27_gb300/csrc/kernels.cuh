@@ -62,6 +62,11 @@ struct PrefillParams {
   float v_scale;        // the cache's value scale
   void* out;
   float* lse;
+  // when set, each row's state goes here instead of out / lse: fp32
+  // o [slot][head][d] (normalised, times v_scale) and lse [slot][head],
+  // slot = item.slot + row of q
+  float* state_o;
+  float* state_lse;
   uint32_t* err;
   uint64_t wait_limit_ns;
   int32_t fault_kind;   // test hook: 1 = CTA 0's K producer skips its first tile

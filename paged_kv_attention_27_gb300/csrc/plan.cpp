@@ -94,12 +94,63 @@ fi_status build_plan(int32_t mode, int32_t batch, const int32_t* qo_indptr,
   if (total_q > INT32_MAX) return FI_ERR_INVALID_ARG;
   p.total_q = total_q;
 
+  // ---- shared-prefix groups (decode plans): group g's requests share their
+  //      first prefix_pages[g] pages; the prefix is attended once per group
+  //      and each request's decode work starts after it
+  const int G = opt.num_prefix_groups;
+  std::vector<int64_t> prefix_tokens(batch, 0);
+  if (G < 0) return FI_ERR_INVALID_ARG;
+  if (G > 0) {
+    if (!opt.prefix_group_indptr || !opt.prefix_pages) return FI_ERR_INVALID_ARG;
+    if (mode != FI_MODE_DECODE || kv_dtype == FI_DTYPE_E4M3 || opt.window_left >= 0)
+      return FI_ERR_UNSUPPORTED;
+    const int32_t* gi = opt.prefix_group_indptr;
+    if (gi[0] < 0 || gi[G] > batch) return FI_ERR_INVALID_ARG;
+    for (int g = 0; g < G; ++g) {
+      if (gi[g + 1] < gi[g]) return FI_ERR_INVALID_ARG;
+      const int64_t pages = opt.prefix_pages[g];
+      if (pages < 1) return FI_ERR_INVALID_ARG;
+      for (int b = gi[g]; b < gi[g + 1]; ++b) {
+        const int64_t np = int64_t(page_indptr[b + 1]) - page_indptr[b];
+        // the prefix is made of full pages of every request in the group
+        if (np < pages || (np == pages && last_page_len[b] != page_size))
+          return FI_ERR_INVALID_ARG;
+        prefix_tokens[b] = pages * page_size;
+      }
+    }
+  }
+
   // ---- the keys a row may see: [first_key, ...). A left window moves the
-  //      start; the row at key position pos keeps keys t >= pos - window_left
+  //      start; the row at key position pos keeps keys t >= pos - window_left.
+  //      (For decode work of a shared-prefix request: the first key after
+  //      the prefix, which is attended separately.)
   auto first_key = [&](int b, int64_t row) -> int64_t {
+    if (prefix_tokens[b] > 0) return prefix_tokens[b];
     if (p.window_left < 0) return 0;
     return std::max<int64_t>(0, kv_len[b] - qo_len[b] + row - p.window_left);
   };
+  // Each group's prefix is cut into chunks so that its items fill about two
+  // waves of the GPU (the prefix can be long and the group small); chunk c
+  // of group g writes one state per row of the group, in slots
+  // pslot[g] + c * rows(g) + (row - first row). The decode merge adds them.
+  std::vector<int64_t> pchunk(std::max(G, 0), 0), pn(std::max(G, 0), 0), prow0(std::max(G, 0), 0),
+      pnrow(std::max(G, 0), 0), pslot(std::max(G, 0), 0);
+  std::vector<int32_t> group_of(batch, -1);
+  for (int g = 0; g < G; ++g) {
+    const int b0 = opt.prefix_group_indptr[g], b1 = opt.prefix_group_indptr[g + 1];
+    if (b1 <= b0) continue;
+    for (int b = b0; b < b1; ++b) group_of[b] = g;
+    const int64_t Lp = int64_t(opt.prefix_pages[g]) * page_size;
+    prow0[g] = qo_start[b0];
+    pnrow[g] = qo_start[b1 - 1] + 1 - prow0[g];
+    const int64_t per_chunk = ceil_div(pnrow[g], kPrefillTileM) * num_qo_heads;   // items
+    const int64_t want = std::max<int64_t>(1, ceil_div(int64_t(num_sms) * 2, per_chunk));
+    const int64_t n = std::min<int64_t>(want, std::max<int64_t>(1, Lp / 1024));
+    pchunk[g] = ceil_div(ceil_div(Lp, n), 128) * 128;   // whole KV tiles
+    pn[g] = ceil_div(Lp, pchunk[g]);
+    pslot[g] = p.num_slots;
+    p.num_slots += int32_t(pn[g] * pnrow[g]);
+  }
 
   // ---- decode work: every request with exactly one query row. Chunks start
   //      on page boundaries from the page holding the first visible key.
@@ -135,12 +186,22 @@ fi_status build_plan(int32_t mode, int32_t batch, const int32_t* qo_indptr,
       w0s[b] = w0;
       s0s[b] = s0;
       const int64_t n_chunks = std::max<int64_t>(1, ceil_div(kv_len[b] - s0, chunk));
-      if (n_chunks > 1) {
+      // split requests, and every request with a shared prefix, write
+      // partial states that the decode kernel merges (plus the prefix state)
+      const bool prefixed = prefix_tokens[b] > 0;
+      if (n_chunks > 1 || prefixed) {
         merge_of[b] = int32_t(p.merges.size());
         slot_base[b] = p.num_slots;
         p.num_slots += int32_t(n_chunks);
-        p.num_split += 1;
-        p.merges.push_back(MergeTask{int32_t(qo_start[b]), slot_base[b], int32_t(n_chunks), 0});
+        p.num_split += n_chunks > 1 ? 1 : 0;
+        MergeTask mt{int32_t(qo_start[b]), slot_base[b], int32_t(n_chunks), -1, 0, 0, {0, 0}};
+        if (prefixed) {
+          const int g = group_of[b];
+          mt.extra_slot = int32_t(pslot[g] + (qo_start[b] - prow0[g]));
+          mt.n_extra = int32_t(pn[g]);
+          mt.extra_stride = int32_t(pnrow[g]);
+        }
+        p.merges.push_back(mt);
       }
       for (int64_t c = 0; c < n_chunks; ++c) {
         const int64_t t0 = s0 + c * chunk;
@@ -169,6 +230,52 @@ fi_status build_plan(int32_t mode, int32_t batch, const int32_t* qo_indptr,
       for (int kh = 0; kh < num_kv_heads; ++kh) {
         w.head = kh;
         p.decode_items.push_back(w);
+      }
+    }
+  }
+
+  // ---- shared-prefix work: per group, the group's rows of q (one query
+  //      head per item, tiles of kPrefillTileM rows) against the prefix, on
+  //      the prefill kernel. Virtual request 2g describes group g to it:
+  //      rows [first, last) of q, prefix_pages full pages, not causal.
+  if (G > 0) {
+    p.num_prefix_groups = G;
+    p.prefix_tables.assign(size_t(6) * G, 0);
+    int32_t* vq = p.prefix_tables.data();          // qo_indptr   [2G]
+    int32_t* vp = vq + 2 * G;                      // page_indptr [2G]
+    int32_t* vl = vq + 4 * G;                      // last_page_len [2G]
+    struct PTile { int64_t len; int32_t g, c, r0; };
+    std::vector<PTile> ptiles;
+    for (int g = 0; g < G; ++g) {
+      vq[2 * g] = int32_t(prow0[g]);
+      vq[2 * g + 1] = int32_t(prow0[g] + pnrow[g]);
+      vp[2 * g] = 0;
+      vp[2 * g + 1] = opt.prefix_pages[g];
+      vl[2 * g] = page_size;
+      const int64_t Lp = int64_t(opt.prefix_pages[g]) * page_size;
+      for (int64_t c = 0; c < pn[g]; ++c)
+        for (int64_t r0 = prow0[g]; r0 < prow0[g] + pnrow[g]; r0 += kPrefillTileM)
+          ptiles.push_back(PTile{std::min(Lp, (c + 1) * pchunk[g]) - c * pchunk[g], g,
+                                 int32_t(c), int32_t(r0)});
+    }
+    std::stable_sort(ptiles.begin(), ptiles.end(),
+                     [](const PTile& x, const PTile& y) { return x.len > y.len; });
+    p.prefix_items.reserve(ptiles.size() * size_t(num_qo_heads));
+    for (const PTile& t : ptiles) {
+      const int64_t k0 = int64_t(t.c) * pchunk[t.g];
+      WorkItem w;
+      w.req = 2 * t.g;
+      // the group's first request holds the shared pages
+      w.page_begin = int32_t(page_indptr[opt.prefix_group_indptr[t.g]] + k0 / page_size);
+      w.n_pages = int32_t(ceil_div(t.len, page_size));
+      w.tok_begin = int32_t(k0);
+      w.tok_end = int32_t(k0 + t.len);
+      w.slot = int32_t(pslot[t.g] + int64_t(t.c) * pnrow[t.g] - prow0[t.g]);
+      w.q_row = t.r0;
+      w.merge = -1;
+      for (int h = 0; h < num_qo_heads; ++h) {
+        w.head = h;
+        p.prefix_items.push_back(w);
       }
     }
   }
@@ -213,13 +320,17 @@ fi_status build_plan(int32_t mode, int32_t batch, const int32_t* qo_indptr,
     }
   }
 
-  // ---- workspace: header | decode items | prefill items | merges | merge counters |
-  //      partial o | partial lse
+  // ---- workspace: header | decode items | prefill items | prefix items |
+  //      prefix tables | merges | merge counters | partial o | partial lse
   size_t off = kHeaderBytes;
   p.ws.decode_items = off;
   off = align_up(off + p.decode_items.size() * sizeof(WorkItem));
   p.ws.prefill_items = off;
   off = align_up(off + p.prefill_items.size() * sizeof(WorkItem));
+  p.ws.prefix_items = off;
+  off = align_up(off + p.prefix_items.size() * sizeof(WorkItem));
+  p.ws.prefix_tables = off;
+  off = align_up(off + p.prefix_tables.size() * sizeof(int32_t));
   p.ws.merges = off;
   off = align_up(off + p.merges.size() * sizeof(MergeTask));
   // one arrival counter per (merge task, kv head), zero at the start of a

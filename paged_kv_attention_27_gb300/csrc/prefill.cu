@@ -649,7 +649,17 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
 #pragma unroll
           for (int e = 0; e < 32; ++e) r[e] = 0u;
         }
-        if (row_ok) {
+        if (row_ok && prm.state_o) {
+          // fp32 state for a later log-sum-exp merge (shared-prefix decode)
+          const size_t srow = size_t(w.slot) + out_row;
+          float4* dst = reinterpret_cast<float4*>(
+              prm.state_o + (srow * prm.num_qo_heads + w.head) * HEAD_DIM + c * 32);
+#pragma unroll
+          for (int q4 = 0; q4 < 8; ++q4) {
+            const float* f = reinterpret_cast<const float*>(r) + q4 * 4;
+            dst[q4] = make_float4(f[0] * inv, f[1] * inv, f[2] * inv, f[3] * inv);
+          }
+        } else if (row_ok) {
           uint4* dst = reinterpret_cast<uint4*>(op + c * 32);
 #pragma unroll
           for (int q4 = 0; q4 < 4; ++q4) {
@@ -659,8 +669,10 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
           }
         }
       }
-      if (row_ok && prm.lse)
-        prm.lse[out_row * prm.num_qo_heads + w.head] = l > 0.f ? (m + lg2(l)) * kLn2 : -INFINITY;
+      float* lse_dst = prm.state_o ? prm.state_lse : prm.lse;
+      const size_t lrow = prm.state_o ? size_t(w.slot) + out_row : out_row;
+      if (row_ok && lse_dst)
+        lse_dst[lrow * prm.num_qo_heads + w.head] = l > 0.f ? (m + lg2(l)) * kLn2 : -INFINITY;
       // O has been read: the next item's first PV (issued only after this
       // warp's next p_full arrival) may overwrite it
       tc_fence_before();

@@ -33,11 +33,18 @@ def i32_tensor(a: np.ndarray, device="cuda") -> torch.Tensor:
 
 
 def plan_options(b: PagedBatch):
-    """fi_plan options of a batch (None = the defaults)."""
-    if b.window_left < 0 and b.dtype == "bf16" and b.cache_dtype == "bf16":
+    """fi_plan options of a batch (None = the defaults). A batch marked
+    `cascade` plans its shared prefix (the first requests' common leading
+    pages) as one shared-prefix group."""
+    cascade = b.cascade and b.shared_prefix_pages > 0
+    if b.window_left < 0 and b.dtype == "bf16" and b.cache_dtype == "bf16" and not cascade:
         return None
-    return {"window_left": int(b.window_left), "dtype": FI_DTYPES[b.dtype],
-            "kv_dtype": FI_DTYPES[b.cache_dtype]}
+    opt = {"window_left": int(b.window_left), "dtype": FI_DTYPES[b.dtype],
+           "kv_dtype": FI_DTYPES[b.cache_dtype]}
+    if cascade:
+        opt["prefix_group_indptr"] = [0, int(b.meta["shared_prefix_requests"])]
+        opt["prefix_pages"] = [int(b.shared_prefix_pages)]
+    return opt
 
 
 def num_sms(device="cuda") -> int:

@@ -157,6 +157,7 @@ class PagedBatch:
     kv_dtype: str = ""           # element type of the caches ("" = dtype; "e4m3")
     k_scale: float = 1.0         # attended keys / values = scale * stored ones
     v_scale: float = 1.0
+    cascade: bool = False        # plan the shared prefix as one group (shared-prefix decode)
 
     @property
     def cache_dtype(self) -> str:
@@ -306,6 +307,23 @@ def llama70b_gqa_decode(seed: int = 2, batch: int = 128, shared: int = 32,
                       kv_scale=_fp8_scale(kv_dtype))
 
 
+def shared_prefix_decode(seed: int = 7, batch: int = 64, prefix_tokens: int = 32768,
+                         cascade: bool = True) -> PagedBatch:
+    """Decode of ``batch`` requests that share one long prefix (a system
+    prompt or document, ``prefix_tokens`` tokens on the same physical pages)
+    followed by their own U[1, 2048] tokens; Llama2-70B head shape (64/8,
+    d=128, P=16, HND). ``cascade`` plans the prefix as one shared-prefix
+    group."""
+    g = philox(seed + 1000)
+    kv = prefix_tokens + g.integers(1, 2049, size=batch)
+    b = make_batch(f"shared-prefix decode B{batch} prefix {prefix_tokens} + U[1,2048] Hq64 Hkv8 "
+                   f"d128 P16 HND{' (cascade)' if cascade else ' (flat)'}",
+                   kv, np.ones(batch, np.int64), 64, 8, 128, 16, HND, None, False, seed,
+                   shared_prefix_requests=batch, shared_prefix_tokens=prefix_tokens)
+    b.cascade = cascade
+    return b
+
+
 def causal_prefill(seq_len: int, batch: int = 8, seed: int = 3,
                    window_left: int = -1, dtype: str = "bf16") -> PagedBatch:
     """Causal prefill, 70B shape: 64/8 heads, d=128, P=16, qo_len = kv_len =
@@ -382,4 +400,4 @@ def sub_batch(src: PagedBatch, requests) -> PagedBatch:
                       q=q, k_cache=src.k_cache[idx], v_cache=src.v_cache[idx],
                       meta=dict(src.meta, sample=requests), window_left=src.window_left,
                       dtype=src.dtype, kv_dtype=src.kv_dtype, k_scale=src.k_scale,
-                      v_scale=src.v_scale)
+                      v_scale=src.v_scale)   # the sample's pages are renumbered: no cascade

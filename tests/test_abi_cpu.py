@@ -314,3 +314,82 @@ def test_workspace_too_small_and_bad_args_return_before_any_launch():
     with pytest.raises(B.FiError) as e:
         B.fi_merge_states(fake, fake, 2, 3, 4, 8, 5, fake, None, stream=0)   # unknown dtype
     assert e.value.status == B.FI_ERR_INVALID_ARG
+
+
+def test_shared_prefix_plan_covers_prefix_and_suffixes():
+    """Shared-prefix decode: the prefix items cover every (row of a group,
+    head, prefix key) once; the decode items cover each grouped request's
+    keys after the prefix once (the rest as usual); every grouped request has
+    a merge task."""
+    kv = [100, 48, 300, 5000, 64, 17, 900]
+    b = _table_only(kv, 16, 2, 128, 16)
+    gi, pages = [0, 3, 3, 5], [3, 0, 4]            # group 1 is empty
+    pages[1] = 1
+    opts = {"prefix_group_indptr": gi, "prefix_pages": pages}
+    for sms in (4, 152):
+        p = B.fi_plan(B.FI_MODE_DECODE, b.batch, None, b.page_indptr, b.last_page_len, 16, 2, 128,
+                      16, 0, opts, sms)
+        info = B.fi_plan_get_info(p)
+        work = B.fi_plan_get_work(p)
+        nd, npf = info["num_decode_items"], info["num_prefix_items"]
+        assert info["num_prefix_groups"] == 3 and npf > 0
+        dec, pre = work[:nd], work[nd:]
+        seen = {}
+        for req, h, pb, npg, t0, t1, slot, qrow in pre.tolist():
+            g = req // 2
+            first = gi[g]
+            assert req % 2 == 0 and pb == b.page_indptr[first] + t0 // 16
+            assert 0 <= t0 < t1 <= pages[g] * 16 and t0 % 128 == 0
+            for r in range(qrow, min(qrow + 128, gi[g + 1])):
+                for t in range(t0, t1):
+                    seen[(r, h, t)] = seen.get((r, h, t), 0) + 1
+        want = {(r, h, t) for g in range(3) for r in range(gi[g], gi[g + 1]) for h in range(16)
+                for t in range(pages[g] * 16)}
+        assert set(seen) == want and all(c == 1 for c in seen.values())
+        prefix = {r: pages[g] * 16 for g in range(3) for r in range(gi[g], gi[g + 1])}
+        cover = {}
+        for req, kh, pb, npg, t0, t1, slot, qrow in dec.tolist():
+            assert t0 >= prefix.get(req, 0)
+            if req in prefix:
+                assert slot >= 0            # grouped rows always go through a merge
+            for t in range(t0, t1):
+                cover[(req, kh, t)] = cover.get((req, kh, t), 0) + 1
+        want = {(r, kh, t) for r in range(b.batch) for kh in range(2)
+                for t in range(prefix.get(r, 0), kv[r])}
+        assert set(cover) == want and all(c == 1 for c in cover.values())
+
+
+@pytest.mark.parametrize("case,status", [
+    ("prefix_longer_than_request", B.FI_ERR_INVALID_ARG),
+    ("prefix_not_full_pages", B.FI_ERR_INVALID_ARG),
+    ("zero_pages", B.FI_ERR_INVALID_ARG),
+    ("decreasing_groups", B.FI_ERR_INVALID_ARG),
+    ("past_the_batch", B.FI_ERR_INVALID_ARG),
+    ("prefill_plan", B.FI_ERR_UNSUPPORTED),
+    ("with_window", B.FI_ERR_UNSUPPORTED),
+    ("with_fp8_cache", B.FI_ERR_UNSUPPORTED),
+])
+def test_shared_prefix_validation(case, status):
+    kv = [40, 40, 100]           # pages 3, 3, 7; the 40-token requests end mid-page
+    b = _table_only(kv, 8, 2, 128, 16)
+    opts = {"prefix_group_indptr": [0, 2], "prefix_pages": [2]}
+    mode, qo = B.FI_MODE_DECODE, None
+    if case == "prefix_longer_than_request":
+        opts["prefix_pages"] = [4]
+    elif case == "prefix_not_full_pages":
+        opts["prefix_pages"] = [3]              # page 3 of a 40-token request holds 8 tokens
+    elif case == "zero_pages":
+        opts["prefix_pages"] = [0]
+    elif case == "decreasing_groups":
+        opts = {"prefix_group_indptr": [0, 2, 1], "prefix_pages": [2, 2]}
+    elif case == "past_the_batch":
+        opts["prefix_group_indptr"] = [0, 4]
+    elif case == "prefill_plan":
+        mode, qo = B.FI_MODE_PREFILL, [0, 1, 2, 3]
+    elif case == "with_window":
+        opts["window_left"] = 10
+    elif case == "with_fp8_cache":
+        opts["kv_dtype"] = B.FI_DTYPE_E4M3
+    with pytest.raises(B.FiError) as e:
+        B.fi_plan(mode, 3, qo, b.page_indptr, b.last_page_len, 8, 2, 128, 16, 0, opts, 152)
+    assert e.value.status == status

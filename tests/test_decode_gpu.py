@@ -259,3 +259,32 @@ def test_fp8_cache_70b_full_size_sampled():
     order = np.argsort(-b.kv_lens)
     sample = sorted(set(order[:3].tolist() + order[-3:].tolist() + [0, 5, 31, 32, 77]))
     check(b, requests=sample)
+
+
+# ---- shared-prefix (cascade) decode ------------------------------------------
+
+@pytest.mark.parametrize("g,d,P", [(8, 128, 16), (1, 128, 16), (4, 64, 32), (2, 256, 16)])
+def test_shared_prefix_decode(g, d, P):
+    """The first four requests share a 3-page prefix (one of them is exactly
+    the prefix); the others decode as usual; splits forced by few SMs."""
+    hkv = 2
+    kv = [3 * P, 3 * P + 1, 200, 9000, 77, 1, 2500]
+    b = synth.make_batch(f"cascade g{g} d{d} P{P}", kv, [1] * len(kv), g * hkv, hkv, d, P,
+                         synth.HND if g % 2 else synth.NHD, None, False, 800 + g + d + P,
+                         shared_prefix_requests=4, shared_prefix_tokens=3 * P)
+    b.cascade = True
+    (_, _), db = check(b, sms=8)
+    info = B.fi_plan_get_info(db.plan)
+    assert info["num_prefix_groups"] == 1 and info["num_prefix_items"] > 0
+
+
+def test_shared_prefix_decode_long_prefix_many_chunks():
+    b = synth.shared_prefix_decode(batch=12, prefix_tokens=20000 // 16 * 16)
+    (_, _), db = check(b, requests=[0, 5, 11])
+    assert B.fi_plan_get_info(db.plan)["num_prefix_items"] > 64   # the prefix was cut in chunks
+
+
+def test_shared_prefix_decode_70b_batch_sampled():
+    b = synth.llama70b_gqa_decode()
+    b.cascade = True                                 # its first 32 requests share 1024 tokens
+    check(b, requests=[0, 7, 31, 32, 100])
