@@ -193,7 +193,8 @@ fi_status fi_plan_get_info(fi_plan_t plan, fi_plan_info* info);
 
 /*
  * Copies the plan's work list to host memory: 8 int32 per item, in launch
- * order: {request, kv_head (decode) or qo_head (prefill), first page index
+ * order: {request, kv_head (decode), qo_head (prefill) or kv_head with all
+ * its query heads (shared prefix), first page index
  * (into page_indices), number of pages, first key, end key, partial slot or
  * -1, first row of q}. Keys are token positions within the request; the
  * first page holds the first key at slot (first key % page_size), earlier

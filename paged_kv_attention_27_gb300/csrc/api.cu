@@ -215,7 +215,8 @@ fi_status make_kv_map(CUtensorMap* map, const void* base, int layout, int num_pa
 
 // Tensor map over the packed queries [rows][num_qo_heads][head_dim] that
 // fetches 128 rows x 64 dims of one head per box (128-byte swizzled).
-fi_status make_q_map(CUtensorMap* map, const void* q, int64_t rows, int Hq, int d, int dtype) {
+fi_status make_q_map(CUtensorMap* map, const void* q, int64_t rows, int Hq, int pack, int d,
+                     int dtype) {
   auto enc = encode_fn();
   if (!enc) {
     g_last_error = "cuTensorMapEncodeTiled is not available from the driver";
@@ -223,7 +224,9 @@ fi_status make_q_map(CUtensorMap* map, const void* q, int64_t rows, int Hq, int 
   }
   const cuuint64_t dims[3] = {cuuint64_t(d), cuuint64_t(Hq), cuuint64_t(rows)};
   const cuuint64_t strides[2] = {cuuint64_t(d) * 2, cuuint64_t(Hq) * d * 2};
-  const cuuint32_t box[3] = {64, 1, cuuint32_t(fi::kPrefillTileM)};
+  // 64 dims x `pack` heads x 128 / pack rows: the 128 M rows of a tile,
+  // heads inner
+  const cuuint32_t box[3] = {64, cuuint32_t(pack), cuuint32_t(fi::kPrefillTileM / pack)};
   const cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = enc(map, tma_type(dtype), 3, const_cast<void*>(q), dims, strides,
                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -312,7 +315,11 @@ fi_status run_paged(fi_plan_t plan, bool prefill_call, const void* q, const int3
 
   CUtensorMap qmap;
   if (!P.prefill_items.empty() || !P.prefix_items.empty()) {
-    st = make_q_map(&qmap, q, P.total_q, P.num_qo_heads, P.head_dim, P.dtype);
+    // prefill tiles hold 128 rows of one head; shared-prefix tiles 128 / g
+    // rows of the g heads of a kv head (a decode plan has only the latter)
+    st = make_q_map(&qmap, q, P.total_q, P.num_qo_heads,
+                    P.prefix_items.empty() ? 1 : P.num_qo_heads / P.num_kv_heads, P.head_dim,
+                    P.dtype);
     if (st != FI_OK) return st;
   }
 
@@ -353,6 +360,7 @@ fi_status run_paged(fi_plan_t plan, bool prefill_call, const void* q, const int3
     pp.page_size = P.page_size;
     pp.num_qo_heads = P.num_qo_heads;
     pp.group = P.num_qo_heads / P.num_kv_heads;
+    pp.pack = 1;
     pp.layout = kv_layout;
     pp.causal = P.causal;
     pp.window_left = P.window_left;
@@ -387,6 +395,7 @@ fi_status run_paged(fi_plan_t plan, bool prefill_call, const void* q, const int3
     pp.page_size = P.page_size;
     pp.num_qo_heads = P.num_qo_heads;
     pp.group = P.num_qo_heads / P.num_kv_heads;
+    pp.pack = pp.group;
     pp.layout = kv_layout;
     pp.causal = 0;
     pp.window_left = -1;

@@ -15,10 +15,12 @@ namespace fi {
 // `req` for kv head `head` (all g query heads of its group), pages
 // page_indices[page_begin .. page_begin+n_pages), writing either the final
 // output row `q_row` (slot < 0) or partial-state slot `slot` of merge task
-// `merge`. Prefill items: query rows [q_row, q_row + rows) of request `req`
-// (absolute rows of q/out, at most kPrefillTileM) for query head `head`,
-// over keys [tok_begin, tok_end) — tok_end clipped to the causal bound of
-// the tile's last row, tok_begin to the page of its first row's window.
+// `merge`. Prefill items: query rows [q_row, q_row + kPrefillTileM) of
+// request `req` (absolute rows of q/out) for query head `head`, over keys
+// [tok_begin, tok_end) — tok_end clipped to the causal bound of the tile's
+// last row, tok_begin to the page of its first row's window. Shared-prefix
+// items: rows [q_row, q_row + kPrefillTileM / g) for all g query heads of
+// kv head `head` (the 128 M rows are rows x heads, heads inner).
 struct WorkItem {
   int32_t req;
   int32_t head;

@@ -55,6 +55,8 @@ struct PrefillParams {
   int32_t page_size;
   int32_t num_qo_heads;
   int32_t group;
+  int32_t pack;         // query heads per tile (1, or the group size): item.head is the
+                        // head block, query heads [head * pack, head * pack + pack)
   int32_t layout;
   int32_t causal;
   int32_t window_left;  // -1: none; else row at key position pos keeps t >= pos - window_left

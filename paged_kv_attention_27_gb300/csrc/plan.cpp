@@ -94,6 +94,12 @@ fi_status build_plan(int32_t mode, int32_t batch, const int32_t* qo_indptr,
   if (total_q > INT32_MAX) return FI_ERR_INVALID_ARG;
   p.total_q = total_q;
 
+  // prefill-kernel tiles of the shared-prefix level: 128 M rows = (128 / g
+  // rows of q) x (the g query heads of one kv head), so that every K/V tile
+  // serves the whole group. (Ordinary prefill keeps 128 rows of one query
+  // head per tile: packing measured slower on long causal prefill.)
+  const int64_t rows_per_tile = kPrefillTileM / g;
+
   // ---- shared-prefix groups (decode plans): group g's requests share their
   //      first prefix_pages[g] pages; the prefix is attended once per group
   //      and each request's decode work starts after it
@@ -143,7 +149,7 @@ fi_status build_plan(int32_t mode, int32_t batch, const int32_t* qo_indptr,
     const int64_t Lp = int64_t(opt.prefix_pages[g]) * page_size;
     prow0[g] = qo_start[b0];
     pnrow[g] = qo_start[b1 - 1] + 1 - prow0[g];
-    const int64_t per_chunk = ceil_div(pnrow[g], kPrefillTileM) * num_qo_heads;   // items
+    const int64_t per_chunk = ceil_div(pnrow[g], rows_per_tile) * num_kv_heads;   // items
     const int64_t want = std::max<int64_t>(1, ceil_div(int64_t(num_sms) * 2, per_chunk));
     const int64_t n = std::min<int64_t>(want, std::max<int64_t>(1, Lp / 1024));
     pchunk[g] = ceil_div(ceil_div(Lp, n), 128) * 128;   // whole KV tiles
@@ -235,7 +241,7 @@ fi_status build_plan(int32_t mode, int32_t batch, const int32_t* qo_indptr,
   }
 
   // ---- shared-prefix work: per group, the group's rows of q (one query
-  //      head per item, tiles of kPrefillTileM rows) against the prefix, on
+  //      kv head per item, tiles of rows_per_tile rows) against the prefix, on
   //      the prefill kernel. Virtual request 2g describes group g to it:
   //      rows [first, last) of q, prefix_pages full pages, not causal.
   if (G > 0) {
@@ -254,13 +260,13 @@ fi_status build_plan(int32_t mode, int32_t batch, const int32_t* qo_indptr,
       vl[2 * g] = page_size;
       const int64_t Lp = int64_t(opt.prefix_pages[g]) * page_size;
       for (int64_t c = 0; c < pn[g]; ++c)
-        for (int64_t r0 = prow0[g]; r0 < prow0[g] + pnrow[g]; r0 += kPrefillTileM)
+        for (int64_t r0 = prow0[g]; r0 < prow0[g] + pnrow[g]; r0 += rows_per_tile)
           ptiles.push_back(PTile{std::min(Lp, (c + 1) * pchunk[g]) - c * pchunk[g], g,
                                  int32_t(c), int32_t(r0)});
     }
     std::stable_sort(ptiles.begin(), ptiles.end(),
                      [](const PTile& x, const PTile& y) { return x.len > y.len; });
-    p.prefix_items.reserve(ptiles.size() * size_t(num_qo_heads));
+    p.prefix_items.reserve(ptiles.size() * size_t(num_kv_heads));
     for (const PTile& t : ptiles) {
       const int64_t k0 = int64_t(t.c) * pchunk[t.g];
       WorkItem w;
@@ -273,8 +279,8 @@ fi_status build_plan(int32_t mode, int32_t batch, const int32_t* qo_indptr,
       w.slot = int32_t(pslot[t.g] + int64_t(t.c) * pnrow[t.g] - prow0[t.g]);
       w.q_row = t.r0;
       w.merge = -1;
-      for (int h = 0; h < num_qo_heads; ++h) {
-        w.head = h;
+      for (int kh = 0; kh < num_kv_heads; ++kh) {
+        w.head = kh;
         p.prefix_items.push_back(w);
       }
     }

@@ -238,7 +238,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
       next_page = prm.page_indices[w.page_begin + lane];
     for (int n = 0; ok && it >= 0; ++n) {
       const int nt = item_tiles<C::N>(w);
-      const int kv_head = w.head / prm.group;
+      const int kv_head = w.head * prm.pack / prm.group;
       const int c1 = prm.layout == FI_LAYOUT_NHD ? kv_head : 0;
       const int c2 = prm.layout == FI_LAYOUT_NHD ? 0 : kv_head;
       // the next item: taken from the counter and published by the K
@@ -272,7 +272,9 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
           mbar_arrive_expect_tx(qb, C::Q_BYTES);
 #pragma unroll
           for (int c = 0; c < C::DBLK; ++c)
-            tma_load_3d(base + C::OFF_Q + c * C::M * 128, &q_map, qb, c * 64, w.head, w.q_row);
+            // 128 M rows = (128 / pack rows of q) x (pack heads), heads inner
+            tma_load_3d(base + C::OFF_Q + c * C::M * 128, &q_map, qb, c * 64, w.head * prm.pack,
+                        w.q_row);
         }
         q_loads = n + 1;
       }
@@ -399,8 +401,11 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
     __syncwarp();
   } else {
     // ------------------------------------------------------------ softmax + epilogue
-    const int t = threadIdx.x;                       // query row of the tile = TMEM lane
+    const int t = threadIdx.x;                       // M row of the tile = TMEM lane
     const uint32_t lane_off = uint32_t(warp * 32) << 16;
+    // M row t holds query head head * pack + t % pack of q row q_row + t / pack
+    // (pack > 1: heads of one kv head sharing every K/V tile)
+    const int t_row = t / prm.pack, t_head = t % prm.pack;
     const float scale = prm.sm_scale * kLog2e;
     // Row bounds of item w for this thread's row: the last key it may see
     // (causal bound, clipped to the keys), the first (left window; INT_MIN:
@@ -411,7 +416,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
       const int np_req = prm.page_indptr[w.req + 1] - prm.page_indptr[w.req];
       const int kv_len =
           np_req > 0 ? (np_req - 1) * prm.page_size + prm.last_page_len[w.req] : 0;
-      const int pos = kv_len - (q_end - q_start) + (w.q_row - q_start + t);  // key position
+      const int pos = kv_len - (q_end - q_start) + (w.q_row - q_start + t_row);  // key position
       RowBounds r;
       r.q_end = q_end;
       r.t_max = min(prm.causal ? pos : kv_len - 1, kv_len - 1);
@@ -633,12 +638,12 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
       }
       tc_fence_after();
       // ---- epilogue: O / lp (bf16 or fp16) and lse = ln(l) + m ln 2
-      const int rows = min(C::M, rb.q_end - w.q_row);
-      const bool row_ok = t < rows;
+      const bool row_ok = w.q_row + t_row < rb.q_end;
       const float inv = lp > 0.f ? prm.v_scale / lp : 0.f;
-      const size_t out_row = size_t(w.q_row) + t;
+      const size_t out_row = size_t(w.q_row) + t_row;
+      const int qo_head = w.head * prm.pack + t_head;
       uint16_t* op = reinterpret_cast<uint16_t*>(prm.out) +
-                     (out_row * prm.num_qo_heads + w.head) * HEAD_DIM;
+                     (out_row * prm.num_qo_heads + qo_head) * HEAD_DIM;
 #pragma unroll 1
       for (int c = 0; c < HEAD_DIM / 32; ++c) {
         uint32_t r[32];
@@ -653,7 +658,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
           // fp32 state for a later log-sum-exp merge (shared-prefix decode)
           const size_t srow = size_t(w.slot) + out_row;
           float4* dst = reinterpret_cast<float4*>(
-              prm.state_o + (srow * prm.num_qo_heads + w.head) * HEAD_DIM + c * 32);
+              prm.state_o + (srow * prm.num_qo_heads + qo_head) * HEAD_DIM + c * 32);
 #pragma unroll
           for (int q4 = 0; q4 < 8; ++q4) {
             const float* f = reinterpret_cast<const float*>(r) + q4 * 4;
@@ -672,7 +677,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
       float* lse_dst = prm.state_o ? prm.state_lse : prm.lse;
       const size_t lrow = prm.state_o ? size_t(w.slot) + out_row : out_row;
       if (row_ok && lse_dst)
-        lse_dst[lrow * prm.num_qo_heads + w.head] = l > 0.f ? (m + lg2(l)) * kLn2 : -INFINITY;
+        lse_dst[lrow * prm.num_qo_heads + qo_head] = l > 0.f ? (m + lg2(l)) * kLn2 : -INFINITY;
       // O has been read: the next item's first PV (issued only after this
       // warp's next p_full arrival) may overwrite it
       tc_fence_before();

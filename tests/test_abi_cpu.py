@@ -129,10 +129,13 @@ def test_split_decisions_scale_with_sm_count(sms):
     assert info["chunk_tokens"] >= 512
 
 
-def test_prefill_plan_tiles_and_causal_bounds():
+@pytest.mark.parametrize("hq,hkv", [(8, 2), (8, 8), (16, 2)])
+def test_prefill_plan_tiles_and_causal_bounds(hq, hkv):
+    """Prefill items are (128 rows, query head); every (request, query
+    head, row) exactly once."""
     kv = [300, 1, 129, 77, 5000]
     qo = [300, 1, 100, 77, 4]
-    b = _table_only(kv, 8, 2, 128, 16, qo)
+    b = _table_only(kv, hq, hkv, 128, 16, qo)
     plan = _plan(b, B.FI_MODE_PREFILL)
     info = B.fi_plan_get_info(plan)
     work = B.fi_plan_get_work(plan)
@@ -142,12 +145,12 @@ def test_prefill_plan_tiles_and_causal_bounds():
         qo_len, kv_len = qo[req], kv[req]
         r0 = qrow - b.qo_indptr[req]
         r_last = min(qo_len, r0 + 128) - 1
-        assert t0 == 0 and slot == -1
+        assert t0 == 0 and slot == -1 and 0 <= h < hq
         assert t1 == min(kv_len, kv_len - qo_len + r_last + 1)   # causal bound of the last row
         assert npg == -(-t1 // 16)
         for r in range(r0, r_last + 1):
             rows[(req, h, r)] = rows.get((req, h, r), 0) + 1
-    want = {(r, h, i) for r in range(len(kv)) if qo[r] >= 2 for h in range(8)
+    want = {(r, h, i) for r in range(len(kv)) if qo[r] >= 2 for h in range(hq)
             for i in range(qo[r])}
     assert set(rows) == want and all(c == 1 for c in rows.values())
     # the single-row request is decode work
@@ -335,14 +338,15 @@ def test_shared_prefix_plan_covers_prefix_and_suffixes():
         assert info["num_prefix_groups"] == 3 and npf > 0
         dec, pre = work[:nd], work[nd:]
         seen = {}
-        for req, h, pb, npg, t0, t1, slot, qrow in pre.tolist():
+        for req, kh, pb, npg, t0, t1, slot, qrow in pre.tolist():
             g = req // 2
             first = gi[g]
             assert req % 2 == 0 and pb == b.page_indptr[first] + t0 // 16
             assert 0 <= t0 < t1 <= pages[g] * 16 and t0 % 128 == 0
-            for r in range(qrow, min(qrow + 128, gi[g + 1])):
-                for t in range(t0, t1):
-                    seen[(r, h, t)] = seen.get((r, h, t), 0) + 1
+            for r in range(qrow, min(qrow + 128 // 8, gi[g + 1])):   # 16 rows x 8 heads
+                for h in range(kh * 8, kh * 8 + 8):
+                    for t in range(t0, t1):
+                        seen[(r, h, t)] = seen.get((r, h, t), 0) + 1
         want = {(r, h, t) for g in range(3) for r in range(gi[g], gi[g + 1]) for h in range(16)
                 for t in range(pages[g] * 16)}
         assert set(seen) == want and all(c == 1 for c in seen.values())
