@@ -644,33 +644,46 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
       const int qo_head = w.head * prm.pack + t_head;
       uint16_t* op = reinterpret_cast<uint16_t*>(prm.out) +
                      (out_row * prm.num_qo_heads + qo_head) * HEAD_DIM;
+      // O is read 64 columns (two loads) per wait, to halve the round trips
+      constexpr int BATCH = HEAD_DIM >= 64 ? 2 : 1;
 #pragma unroll 1
-      for (int c = 0; c < HEAD_DIM / 32; ++c) {
-        uint32_t r[32];
+      for (int c0 = 0; c0 < HEAD_DIM / 32; c0 += BATCH) {
+        uint32_t rb2[BATCH][32];
         if (nt > 0) {
-          tmem_ld32(tmem + lane_off + C::COL_O + c * 32, r);
+#pragma unroll
+          for (int b = 0; b < BATCH; ++b)
+            tmem_ld32(tmem + lane_off + C::COL_O + (c0 + b) * 32, rb2[b]);
           tmem_wait_ld();
         } else {
 #pragma unroll
-          for (int e = 0; e < 32; ++e) r[e] = 0u;
+          for (int b = 0; b < BATCH; ++b)
+#pragma unroll
+            for (int e = 0; e < 32; ++e) rb2[b][e] = 0u;
         }
-        if (row_ok && prm.state_o) {
-          // fp32 state for a later log-sum-exp merge (shared-prefix decode)
-          const size_t srow = size_t(w.slot) + out_row;
-          float4* dst = reinterpret_cast<float4*>(
-              prm.state_o + (srow * prm.num_qo_heads + qo_head) * HEAD_DIM + c * 32);
 #pragma unroll
-          for (int q4 = 0; q4 < 8; ++q4) {
-            const float* f = reinterpret_cast<const float*>(r) + q4 * 4;
-            dst[q4] = make_float4(f[0] * inv, f[1] * inv, f[2] * inv, f[3] * inv);
-          }
-        } else if (row_ok) {
-          uint4* dst = reinterpret_cast<uint4*>(op + c * 32);
+        for (int b = 0; b < BATCH; ++b) {
+          const int c = c0 + b;
+          const uint32_t (&r)[32] = rb2[b];
+          if (row_ok && prm.state_o) {
+            // fp32 state for a later log-sum-exp merge (shared-prefix decode)
+            const size_t srow = size_t(w.slot) + out_row;
+            float4* dst = reinterpret_cast<float4*>(
+                prm.state_o + (srow * prm.num_qo_heads + qo_head) * HEAD_DIM + c * 32);
 #pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4) {
-            const float* f = reinterpret_cast<const float*>(r) + q4 * 8;
-            dst[q4] = make_uint4(E::pack2(f[0] * inv, f[1] * inv), E::pack2(f[2] * inv, f[3] * inv),
-                                 E::pack2(f[4] * inv, f[5] * inv), E::pack2(f[6] * inv, f[7] * inv));
+            for (int q4 = 0; q4 < 8; ++q4) {
+              const float* f = reinterpret_cast<const float*>(r) + q4 * 4;
+              dst[q4] = make_float4(f[0] * inv, f[1] * inv, f[2] * inv, f[3] * inv);
+            }
+          } else if (row_ok) {
+            uint4* dst = reinterpret_cast<uint4*>(op + c * 32);
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) {
+              const float* f = reinterpret_cast<const float*>(r) + q4 * 8;
+              dst[q4] = make_uint4(E::pack2(f[0] * inv, f[1] * inv),
+                                   E::pack2(f[2] * inv, f[3] * inv),
+                                   E::pack2(f[4] * inv, f[5] * inv),
+                                   E::pack2(f[6] * inv, f[7] * inv));
+            }
           }
         }
       }
