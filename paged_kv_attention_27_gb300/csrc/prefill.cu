@@ -507,18 +507,21 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
         for (int i = 0; i < 8; ++i) mx8[i] = -INFINITY;
         if (need_mask) {
 #pragma unroll
-          for (int k = 0; k < C::N; ++k) {
-            const bool vis = col0 + k <= rb.t_max && col0 + k >= rb.t_min;
-            const float v = vis ? __uint_as_float(sr[k >> 5][k & 31]) : -INFINITY;
-            mx8[k & 7] = fmaxf(mx8[k & 7], v);
+          for (int k = 0; k < C::N; k += 2) {
+            const float a = col0 + k <= rb.t_max && col0 + k >= rb.t_min
+                                ? __uint_as_float(sr[k >> 5][k & 31]) : -INFINITY;
+            const float b = col0 + k + 1 <= rb.t_max && col0 + k + 1 >= rb.t_min
+                                ? __uint_as_float(sr[k >> 5][(k + 1) & 31]) : -INFINITY;
+            mx8[(k >> 1) & 7] = fmax3(mx8[(k >> 1) & 7], a, b);
           }
         } else {
 #pragma unroll
-          for (int k = 0; k < C::N; ++k)
-            mx8[k & 7] = fmaxf(mx8[k & 7], __uint_as_float(sr[k >> 5][k & 31]));
+          for (int k = 0; k < C::N; k += 2)
+            mx8[(k >> 1) & 7] = fmax3(mx8[(k >> 1) & 7], __uint_as_float(sr[k >> 5][k & 31]),
+                                      __uint_as_float(sr[k >> 5][(k + 1) & 31]));
         }
-        const float mx_raw = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                                   fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+        const float mx_raw = fmaxf(fmax3(mx8[0], mx8[1], mx8[2]),
+                                   fmax3(fmax3(mx8[3], mx8[4], mx8[5]), mx8[6], mx8[7]));
         const float m_tile = (mx_raw == -INFINITY) ? -INFINITY : mx_raw * scale;
         const float m_new = fmaxf(m, m_tile);
         const bool grow = m_new > m + kRescaleThreshold;
@@ -531,23 +534,30 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
           m = m_new;
         }
         const float ref = (m == -INFINITY) ? 0.f : m;
-        // p = 2^(s * scale - ref): one FFMA and one ex2 per score
+        // p = 2^(s * scale - ref): a packed FFMA per two scores, one ex2 each
         float s[C::N];
-        float rs8[8];
+        const float2 sc2 = make_float2(scale, scale), nr2 = make_float2(-ref, -ref);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) rs8[i] = 0.f;
-#pragma unroll
-        for (int k = 0; k < C::N; ++k)
-          s[k] = ex2(fmaf(__uint_as_float(sr[k >> 5][k & 31]), scale, -ref));
+        for (int k = 0; k < C::N; k += 2) {
+          const float2 x = __ffma2_rn(make_float2(__uint_as_float(sr[k >> 5][k & 31]),
+                                                  __uint_as_float(sr[k >> 5][(k + 1) & 31])),
+                                      sc2, nr2);
+          s[k] = ex2(x.x);
+          s[k + 1] = ex2(x.y);
+        }
         if (need_mask) {
 #pragma unroll
           for (int k = 0; k < C::N; ++k)
             s[k] = (col0 + k <= rb.t_max && col0 + k >= rb.t_min) ? s[k] : 0.f;
         }
+        float2 rs4[4];
 #pragma unroll
-        for (int k = 0; k < C::N; ++k) rs8[k & 7] += s[k];
-        const float rs_tile =
-            ((rs8[0] + rs8[1]) + (rs8[2] + rs8[3])) + ((rs8[4] + rs8[5]) + (rs8[6] + rs8[7]));
+        for (int i = 0; i < 4; ++i) rs4[i] = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int k = 0; k < C::N; k += 2)
+          rs4[(k >> 1) & 3] = __fadd2_rn(rs4[(k >> 1) & 3], make_float2(s[k], s[k + 1]));
+        const float2 rs2 = __fadd2_rn(__fadd2_rn(rs4[0], rs4[1]), __fadd2_rn(rs4[2], rs4[3]));
+        const float rs_tile = rs2.x + rs2.y;
         l += rs_tile;
 
         // P buffer and O are free once the previous PV of this item has
@@ -566,7 +576,13 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
               tmem_ld32(tmem + lane_off + C::COL_O + c * 32, r);
               tmem_wait_ld();
 #pragma unroll
-              for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
+              for (int e = 0; e < 32; e += 2) {
+                const float2 y = __fmul2_rn(
+                    make_float2(__uint_as_float(r[e]), __uint_as_float(r[e + 1])),
+                    make_float2(alpha, alpha));
+                r[e] = __float_as_uint(y.x);
+                r[e + 1] = __float_as_uint(y.y);
+              }
               tmem_st32(tmem + lane_off + C::COL_O + c * 32, r);
             }
             tmem_wait_st();
@@ -596,7 +612,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
         // In tiles on the causal diagonal a row may have only a few visible
         // keys, so lp adds exactly the rounded values there; elsewhere the
         // rounding errors of many weights average out and the exact sum is used.
-        float rsp4[4] = {0.f, 0.f, 0.f, 0.f};
+        float2 rsp2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll
         for (int kb = 0; kb < C::N / 64; ++kb) {
           uint32_t wv[32];
@@ -604,12 +620,13 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
           for (int e = 0; e < 32; ++e) wv[e] = E::pack2(s[kb * 64 + 2 * e], s[kb * 64 + 2 * e + 1]);
           if (need_mask) {
 #pragma unroll
-            for (int e = 0; e < 32; ++e) rsp4[e & 3] += E::lo(wv[e]) + E::hi(wv[e]);
+            for (int e = 0; e < 32; ++e)
+              rsp2[e & 1] = __fadd2_rn(rsp2[e & 1], make_float2(E::lo(wv[e]), E::hi(wv[e])));
           }
           tmem_st32(tmem + lane_off + C::COL_P + kb * 32, wv);
         }
         tmem_wait_st();
-        lp += need_mask ? (rsp4[0] + rsp4[1]) + (rsp4[2] + rsp4[3]) : rs_tile;
+        lp += need_mask ? (rsp2[0].x + rsp2[0].y) + (rsp2[1].x + rsp2[1].y) : rs_tile;
         fence_proxy_async_smem();   // zeroed V rows (generic writes) before the MMA reads them
         tc_fence_before();
         __syncwarp();

@@ -135,6 +135,14 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
+// max of three (sm_100 and later: one instruction); NaN inputs are ignored
+// like fmaxf
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float y;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(y) : "f"(a), "f"(b), "f"(c));
+  return y;
+}
+
 __device__ __forceinline__ float lg2(float x) {
   float y;
   asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
