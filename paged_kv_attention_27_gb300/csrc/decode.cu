@@ -37,8 +37,14 @@ constexpr float kLn2 = 0.6931471805599453f;
 
 template <int HEAD_DIM, int GROUP, int KVB>   // KVB: bytes per cache element (2, or 1 for FP8)
 struct DecodeCfg {
-  static constexpr int TILE = 8192 / HEAD_DIM;         // tokens per stage (32 KB of 16-bit K+V)
-  static constexpr int NSTAGE = KVB == 2 ? 3 : 4;      // FP8: 16 KB stages, one deeper
+  // GQA groups of 4 or 8 heads at head_dim <= 128 use the tensor cores: the
+  // g heads are the M rows of m16n8k16 MMAs (padded to 16), 16 tokens per step
+  static constexpr bool MMA = GROUP >= 4 && HEAD_DIM <= 128;
+  // tokens per stage: 32 KB of K+V, for 16-bit caches and the FP8 tensor-core
+  // consumer (two 16-token chunks per consumer warp and stage); 16 KB for
+  // the FP8 SIMT consumer, which runs three CTAs per SM
+  static constexpr int TILE = (KVB == 1 && MMA ? 16384 : 8192) / HEAD_DIM;
+  static constexpr int NSTAGE = KVB == 2 || MMA ? 3 : 4;   // FP8 SIMT: 16 KB stages, one deeper
   static constexpr int NCW = 4;                        // consumer warps
   static constexpr int THREADS = 32 * (NCW + 1);       // + one producer warp
   static constexpr int LPT = HEAD_DIM / 8;             // lanes per token row (8 dims each)
@@ -49,9 +55,6 @@ struct DecodeCfg {
   static constexpr int DBLK = HEAD_DIM / 64;           // 128-byte slices of a 16-bit row
   static constexpr int KBYTES = TILE * HEAD_DIM * KVB; // one K (or V) stage
   static constexpr int STAGE_BYTES = 2 * KBYTES;
-  // GQA groups of 4 or 8 heads at head_dim <= 128 use the tensor cores: the
-  // g heads are the M rows of m16n8k16 MMAs (padded to 16), 16 tokens per step
-  static constexpr bool MMA = GROUP >= 4 && HEAD_DIM <= 128;
   // FP8 rows of 128 bytes (head_dim 128) arrive 128-byte swizzled, and the
   // tensor-core consumer then loads its MMA fragments straight from them;
   // at head_dim 64 it widens 16 tokens of K and of V at a time into 16-bit
@@ -216,7 +219,9 @@ __device__ __forceinline__ bool mma_consumer(const DecodeParams& prm, const Work
         }
         __syncwarp();
       }
-      float sacc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+      // S accumulators: [k-step parity][8-token n-tile], so that each chain
+      // of dependent MMAs is half as long; the parities are added after
+      float sacc2[2][2][4] = {};
       // ldmatrix lanes 0-7 / 8-15 / 16-23 / 24-31 address matrices 0..3
       const int ltok = (lane & 7) + ((lane >> 3) & 1) * 8;   // token row this lane addresses
       if constexpr (C::SWZ8) {
@@ -228,10 +233,10 @@ __device__ __forceinline__ bool mma_consumer(const DecodeParams& prm, const Work
           const int step = ks + (lane >> 4);
           uint32_t q0, q1, q2, q3;
           ldsm_x4(kstage + tok * 128 + ((step ^ (tok & 7)) << 4), q0, q1, q2, q3);
-          ME::mma16816(sacc[0], qa[ks], E4m3::to_f16x2(q0), E4m3::to_f16x2(q0 >> 16));
-          ME::mma16816(sacc[1], qa[ks], E4m3::to_f16x2(q1), E4m3::to_f16x2(q1 >> 16));
-          ME::mma16816(sacc[0], qa[ks + 1], E4m3::to_f16x2(q2), E4m3::to_f16x2(q2 >> 16));
-          ME::mma16816(sacc[1], qa[ks + 1], E4m3::to_f16x2(q3), E4m3::to_f16x2(q3 >> 16));
+          ME::mma16816(sacc2[0][0], qa[ks], E4m3::to_f16x2(q0), E4m3::to_f16x2(q0 >> 16));
+          ME::mma16816(sacc2[0][1], qa[ks], E4m3::to_f16x2(q1), E4m3::to_f16x2(q1 >> 16));
+          ME::mma16816(sacc2[1][0], qa[ks + 1], E4m3::to_f16x2(q2), E4m3::to_f16x2(q2 >> 16));
+          ME::mma16816(sacc2[1][1], qa[ks + 1], E4m3::to_f16x2(q3), E4m3::to_f16x2(q3 >> 16));
         }
       } else {
 #pragma unroll
@@ -240,10 +245,15 @@ __device__ __forceinline__ bool mma_consumer(const DecodeParams& prm, const Work
           const int dim = ks * 16 + (mi & 1) * 8;
           uint32_t b0, b1, b2, b3;
           ldsm_x4(kbase + (dim >> 6) * slice + swz(trow, (dim & 63) >> 3), b0, b1, b2, b3);
-          ME::mma16816(sacc[0], qa[ks], b0, b1);
-          ME::mma16816(sacc[1], qa[ks], b2, b3);
+          ME::mma16816(sacc2[ks & 1][0], qa[ks], b0, b1);
+          ME::mma16816(sacc2[ks & 1][1], qa[ks], b2, b3);
         }
       }
+      float sacc[2][4];
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) sacc[nt][e] = sacc2[0][nt][e] + sacc2[1][nt][e];
       float sv[4];
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
