@@ -77,14 +77,23 @@ __device__ __forceinline__ uint32_t swz(int r, int c8) {
   return uint32_t(r * 128 + ((c8 ^ (r & 7)) << 4));
 }
 
-// Tensor-core consumer warp for GQA groups of 4 or 8 heads. Per 16-token
-// chunk of its share of a stage: S (16 x 16, rows = the group's heads padded
-// with zeros) = Q K^T by m16n8k16 MMAs with K read by ldmatrix from the
-// swizzled stage; an online softmax per head row (a quad of lanes holds a
-// row); P rounded to the element type is reused as the A fragment of O += P V, with V
-// read by ldmatrix.trans. With an FP8 cache the warp first widens each
-// 16-token chunk of K and V (exactly) into its own 16-bit scratch, laid out
-// as the TMA writes a 16-bit stage, and runs the same MMA code on it.
+// Tensor-core consumer warp for GQA groups of 4 or 8 heads, token-major: per
+// 16-token chunk of its share of a stage,
+//   S^T (16 tokens x 8 heads) = K Q^T by m16n8k16 MMAs, K the A operand
+//     (ldmatrix from the swizzled stage), Q^T the B operand held in
+//     registers (groups of 4 pad heads 4-7 with zeros);
+//   P^T = 2^(S^T - ref) per head column, rounded to the MMA type and moved
+//     into B-fragment order by two register transposes (movmatrix);
+//   O^T (head_dim x 8) += V^T P^T, V^T the A operand (ldmatrix.trans).
+// The tokens fill the MMAs' 16 rows and the heads their 8 columns, so no
+// MMA work is padding for groups of 8. A lane holds two head columns (2c,
+// 2c + 1, c = lane % 4) of every fragment; each head's reference grows only
+// when a score exceeds it by more than 2^8 (the rescale then needs the
+// chunk's exact maximum, a reduction over the 8 lanes sharing the column).
+// With an FP8 cache at head_dim 128 the K and V fragments come straight from
+// the FP8 rows (see the comments at the loads); at head_dim 64 each 16-token
+// chunk of K and V is widened (exactly) into the warp's 16-bit scratch,
+// laid out as the TMA writes a 16-bit stage.
 // Leaves the warp's (m, l, lp, O) in shared memory and returns whether any
 // consumer aborted (voted, so all agree).
 template <int HEAD_DIM, int GROUP, class E, class KV>
@@ -100,44 +109,44 @@ __device__ __forceinline__ bool mma_consumer(const DecodeParams& prm, const Work
   // instruction per pair, exactly; q (bf16 or fp16) is converted once (exact
   // within fp16's range) and P is rounded to fp16.
   using ME = std::conditional_t<FP8, Fp16, E>;
-  constexpr int KS = HEAD_DIM / 16;       // k-steps of QK^T
-  constexpr int NTO = HEAD_DIM / 8;       // 8-dim tiles of O
+  constexpr int KS = HEAD_DIM / 16;       // k-steps of K Q^T
+  constexpr int MB = HEAD_DIM / 16;       // 16-dim row blocks of O^T
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int r = lane >> 2;                // head row of this lane (valid if < GROUP)
-  const int k0 = (lane & 3) * 2;          // first of the lane's two columns
-  const int mi = lane >> 3, rr = lane & 7;   // ldmatrix: matrix and row this lane addresses
+  const int g = lane >> 2;                // fragment row group (token g / g + 8; B column g)
+  const int c = lane & 3;                 // this lane's head columns 2c, 2c + 1
   const float scale = prm.sm_scale * kLog2e;
 
-  uint32_t qa[KS][4];
+  // Q^T as B fragments: column = head g, rows (k) 2c, 2c + 1 and 2c + 8, 2c + 9
+  // of each k-step. With FP8 K fragments loaded from the cache rows, k index
+  // 2c + j of a k-step is dim 4c + j and 2c + 8 + j is dim 4c + 2 + j, so that
+  // a lane's four consecutive bytes of a key row feed both halves of its A
+  // fragment; Q's k order follows.
+  uint32_t qb[KS][2];
   {
     const uint32_t* qp = reinterpret_cast<const uint32_t*>(
         reinterpret_cast<const uint16_t*>(prm.q) +
-        (size_t(item.q_row) * prm.num_qo_heads + item.head * GROUP + (r < GROUP ? r : 0)) *
+        (size_t(item.q_row) * prm.num_qo_heads + item.head * GROUP + (g < GROUP ? g : 0)) *
             HEAD_DIM);
 #pragma unroll
     for (int ks = 0; ks < KS; ++ks) {
-      // With FP8 fragments loaded straight from the cache rows, k index 2c+j
-      // of a k-step is dim 4c+j and 2c+8+j is dim 4c+2+j (c = lane % 4): each
-      // lane's four consecutive bytes of a key row feed both of its
-      // B registers. Q's A fragment follows the same order.
-      const int w0i = C::SWZ8 ? (ks * 16 + 2 * k0) >> 1 : (ks * 16 + k0) >> 1;
-      const int w2i = C::SWZ8 ? w0i + 1 : (ks * 16 + 8 + k0) >> 1;
-      uint32_t w0 = r < GROUP ? qp[w0i] : 0u;
-      uint32_t w2 = r < GROUP ? qp[w2i] : 0u;
+      const int w0i = C::SWZ8 ? (ks * 16 + 4 * c) >> 1 : (ks * 16 + 2 * c) >> 1;
+      const int w1i = C::SWZ8 ? w0i + 1 : (ks * 16 + 8 + 2 * c) >> 1;
+      uint32_t w0 = g < GROUP ? qp[w0i] : 0u;
+      uint32_t w1 = g < GROUP ? qp[w1i] : 0u;
       if constexpr (!std::is_same<ME, E>::value) {
         w0 = ME::pack2(E::lo(w0), E::hi(w0));
-        w2 = ME::pack2(E::lo(w2), E::hi(w2));
+        w1 = ME::pack2(E::lo(w1), E::hi(w1));
       }
-      qa[ks][0] = w0;
-      qa[ks][1] = 0u;
-      qa[ks][2] = w2;
-      qa[ks][3] = 0u;
+      qb[ks][0] = w0;
+      qb[ks][1] = w1;
     }
   }
-  float o[NTO][4];
+  // O^T accumulators: block mb, rows (dims) g and g + 8, columns (heads) 2c, 2c + 1
+  float o[MB][4];
 #pragma unroll
-  for (int t = 0; t < NTO; ++t) o[t][0] = o[t][1] = o[t][2] = o[t][3] = 0.f;
-  float m = -INFINITY, l = 0.f, lp = 0.f;
+  for (int t = 0; t < MB; ++t) o[t][0] = o[t][1] = o[t][2] = o[t][3] = 0.f;
+  // per head column of this lane: reference, sum of weights, sum of rounded weights
+  float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f}, lp[2] = {0.f, 0.f};
 
   for (int i = 0; i < n_tiles; ++i) {
     const int s = i % C::NSTAGE;
@@ -219,103 +228,122 @@ __device__ __forceinline__ bool mma_consumer(const DecodeParams& prm, const Work
         }
         __syncwarp();
       }
-      // S accumulators: [k-step parity][8-token n-tile], so that each chain
-      // of dependent MMAs is half as long; the parities are added after
-      float sacc2[2][2][4] = {};
+      // S^T accumulators by k-step parity (two dependent chains of KS / 2)
+      float sacc2[2][4] = {};
       // ldmatrix lanes 0-7 / 8-15 / 16-23 / 24-31 address matrices 0..3
       const int ltok = (lane & 7) + ((lane >> 3) & 1) * 8;   // token row this lane addresses
       if constexpr (C::SWZ8) {
         // K straight from the FP8 rows: each 8x8 matrix of byte pairs is 8
-        // tokens x 16 dims; matrices (tokens 0-7 | 8-15) x (k-steps ks | ks+1)
+        // tokens x 16 dims, and a lane's register is 4 consecutive dims 4c..4c+3
+        // of token g: widened, dims 4c, 4c+1 and 4c+2, 4c+3 are the A
+        // fragment's (row g, k 2c..) and (row g, k 2c+8..) halves.
+        // Matrices: (tokens 0-7 | 8-15) x (k-steps ks | ks+1).
         const int tok = cb + ltok;
 #pragma unroll
         for (int ks = 0; ks < KS; ks += 2) {
           const int step = ks + (lane >> 4);
           uint32_t q0, q1, q2, q3;
           ldsm_x4(kstage + tok * 128 + ((step ^ (tok & 7)) << 4), q0, q1, q2, q3);
-          ME::mma16816(sacc2[0][0], qa[ks], E4m3::to_f16x2(q0), E4m3::to_f16x2(q0 >> 16));
-          ME::mma16816(sacc2[0][1], qa[ks], E4m3::to_f16x2(q1), E4m3::to_f16x2(q1 >> 16));
-          ME::mma16816(sacc2[1][0], qa[ks + 1], E4m3::to_f16x2(q2), E4m3::to_f16x2(q2 >> 16));
-          ME::mma16816(sacc2[1][1], qa[ks + 1], E4m3::to_f16x2(q3), E4m3::to_f16x2(q3 >> 16));
+          const uint32_t a0[4] = {E4m3::to_f16x2(q0), E4m3::to_f16x2(q1),
+                                  E4m3::to_f16x2(q0 >> 16), E4m3::to_f16x2(q1 >> 16)};
+          const uint32_t a1[4] = {E4m3::to_f16x2(q2), E4m3::to_f16x2(q3),
+                                  E4m3::to_f16x2(q2 >> 16), E4m3::to_f16x2(q3 >> 16)};
+          ME::mma16816(sacc2[0], a0, qb[ks][0], qb[ks][1]);
+          ME::mma16816(sacc2[1], a1, qb[ks + 1][0], qb[ks + 1][1]);
         }
       } else {
+        // matrices: (tokens 0-7 | 8-15) x (dims 0-7 | 8-15 of the k-step)
+        const int mi = lane >> 3;
+        const int trow = row0 + (mi & 1) * 8 + (lane & 7);
 #pragma unroll
         for (int ks = 0; ks < KS; ++ks) {
-          const int trow = row0 + (mi >> 1) * 8 + rr;
-          const int dim = ks * 16 + (mi & 1) * 8;
-          uint32_t b0, b1, b2, b3;
-          ldsm_x4(kbase + (dim >> 6) * slice + swz(trow, (dim & 63) >> 3), b0, b1, b2, b3);
-          ME::mma16816(sacc2[ks & 1][0], qa[ks], b0, b1);
-          ME::mma16816(sacc2[ks & 1][1], qa[ks], b2, b3);
+          const int dim = ks * 16 + (mi >> 1) * 8;
+          uint32_t a[4];
+          ldsm_x4(kbase + (dim >> 6) * slice + swz(trow, (dim & 63) >> 3), a[0], a[1], a[2], a[3]);
+          ME::mma16816(sacc2[ks & 1], a, qb[ks][0], qb[ks][1]);
         }
       }
-      float sacc[2][4];
-#pragma unroll
-      for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) sacc[nt][e] = sacc2[0][nt][e] + sacc2[1][nt][e];
+      // scores of tokens g (e = 0, 1) and g + 8 (e = 2, 3), heads 2c + (e & 1)
       float sv[4];
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        const int tok = cb + (e >> 1) * 8 + k0 + (e & 1);
-        sv[e] = (tok < ntok && tok >= lo) ? sacc[e >> 1][e & 1] * scale : -INFINITY;
+        const int tok = cb + g + (e >> 1) * 8;
+        sv[e] = (tok < ntok && tok >= lo) ? (sacc2[0][e] + sacc2[1][e]) * scale : -INFINITY;
       }
-      float mx = fmaxf(fmaxf(sv[0], sv[1]), fmaxf(sv[2], sv[3]));
-      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-      const float m_new = fmaxf(m, mx);
-      if (m_new > m + 8.0f) {        // lazy rescale: only when the max grew by > 2^8
-        const float alpha = ex2(m - m_new);
-        l *= alpha;
-        lp *= alpha;
+      float mx[2] = {fmaxf(sv[0], sv[2]), fmaxf(sv[1], sv[3])};
+      // Lazy rescale: a head's reference changes only when one of its scores
+      // exceeds it by more than 2^8 (exact: O and both sums share the stale
+      // reference). Then the chunk's maximum over the 8 lanes of the column
+      // becomes the reference, the same in every lane that holds the head.
+      if (__any_sync(0xffffffffu, mx[0] > m[0] + 8.0f || mx[1] > m[1] + 8.0f)) {
 #pragma unroll
-        for (int t = 0; t < NTO; ++t) {
-          o[t][0] *= alpha;
-          o[t][1] *= alpha;
+        for (int h = 0; h < 2; ++h) {
+          float v = mx[h];
+          v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 4));
+          v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 8));
+          v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 16));
+          const float m_new = fmaxf(m[h], v);
+          if (m_new > m[h] + 8.0f) {
+            const float alpha = ex2(m[h] - m_new);
+            l[h] *= alpha;
+            lp[h] *= alpha;
+#pragma unroll
+            for (int t = 0; t < MB; ++t) {
+              o[t][h] *= alpha;
+              o[t][h + 2] *= alpha;
+            }
+            m[h] = m_new;
+          }
         }
-        m = m_new;
       }
-      const float ref = (m == -INFINITY) ? 0.f : m;
-      float p[4];
-#pragma unroll
-      for (int e = 0; e < 4; ++e) p[e] = ex2(sv[e] - ref);
-      l += (p[0] + p[1]) + (p[2] + p[3]);
-      uint32_t pa[4];
-      pa[0] = ME::pack2(p[0], p[1]);
-      pa[1] = 0u;
-      pa[2] = ME::pack2(p[2], p[3]);
-      pa[3] = 0u;
-      lp += (ME::lo(pa[0]) + ME::hi(pa[0])) + (ME::lo(pa[2]) + ME::hi(pa[2]));
+      const float ref0 = (m[0] == -INFINITY) ? 0.f : m[0];
+      const float ref1 = (m[1] == -INFINITY) ? 0.f : m[1];
+      const float p0 = ex2(sv[0] - ref0), p1 = ex2(sv[1] - ref1);
+      const float p2 = ex2(sv[2] - ref0), p3 = ex2(sv[3] - ref1);
+      l[0] += p0 + p2;
+      l[1] += p1 + p3;
+      // P^T (tokens x heads) as the B fragment of the PV MMA: the C layout's
+      // 8x8 blocks (tokens 0-7, 8-15) x heads, transposed in registers
+      const uint32_t x0 = ME::pack2(p0, p1), x1 = ME::pack2(p2, p3);
+      lp[0] += ME::lo(x0) + ME::lo(x1);
+      lp[1] += ME::hi(x0) + ME::hi(x1);
+      const uint32_t pb0 = movmatrix_trans(x0), pb1 = movmatrix_trans(x1);
       if constexpr (C::SWZ8) {
         // V straight from the FP8 rows: a transposed 8x8 matrix of byte pairs
-        // gives a lane tokens 2c, 2c+1 of dims 2n, 2n+1 (n = lane / 4); the
-        // even dims and the odd dims become two n-tiles (O columns permuted,
-        // undone when O is written out). Matrices: (tokens 0-7 | 8-15) x
-        // (16-dim groups j | j+1).
+        // gives a lane dims 2g, 2g+1 of tokens 2c, 2c+1; a byte permute splits
+        // them into the even dim's and the odd dim's token pairs, which are
+        // taken as rows g and g + 8 of the 16-dim block (O^T's rows permuted
+        // accordingly, undone when O is written out). Matrices: (tokens 0-7 |
+        // 8-15) x (16-dim blocks j | j+1).
         const int tok = cb + ltok;
 #pragma unroll
-        for (int j = 0; j < HEAD_DIM / 16; j += 2) {
+        for (int j = 0; j < MB; j += 2) {
           const int grp = j + (lane >> 4);
           uint32_t v0, v1, v2, v3;
           ldsm_x4_trans(vstage + tok * 128 + ((grp ^ (tok & 7)) << 4), v0, v1, v2, v3);
-          ME::mma16816(o[2 * j], pa, E4m3::to_f16x2(__byte_perm(v0, 0, 0x0020)),
-                       E4m3::to_f16x2(__byte_perm(v1, 0, 0x0020)));
-          ME::mma16816(o[2 * j + 1], pa, E4m3::to_f16x2(__byte_perm(v0, 0, 0x0031)),
-                       E4m3::to_f16x2(__byte_perm(v1, 0, 0x0031)));
-          ME::mma16816(o[2 * j + 2], pa, E4m3::to_f16x2(__byte_perm(v2, 0, 0x0020)),
-                       E4m3::to_f16x2(__byte_perm(v3, 0, 0x0020)));
-          ME::mma16816(o[2 * j + 3], pa, E4m3::to_f16x2(__byte_perm(v2, 0, 0x0031)),
-                       E4m3::to_f16x2(__byte_perm(v3, 0, 0x0031)));
+          const uint32_t a0[4] = {E4m3::to_f16x2(__byte_perm(v0, 0, 0x0020)),
+                                  E4m3::to_f16x2(__byte_perm(v0, 0, 0x0031)),
+                                  E4m3::to_f16x2(__byte_perm(v1, 0, 0x0020)),
+                                  E4m3::to_f16x2(__byte_perm(v1, 0, 0x0031))};
+          const uint32_t a1[4] = {E4m3::to_f16x2(__byte_perm(v2, 0, 0x0020)),
+                                  E4m3::to_f16x2(__byte_perm(v2, 0, 0x0031)),
+                                  E4m3::to_f16x2(__byte_perm(v3, 0, 0x0020)),
+                                  E4m3::to_f16x2(__byte_perm(v3, 0, 0x0031))};
+          ME::mma16816(o[j], a0, pb0, pb1);
+          ME::mma16816(o[j + 1], a1, pb0, pb1);
         }
       } else {
+        // V^T blocks: matrices (tokens 0-7 | 8-15) x (dims 0-7 | 8-15 of the
+        // block), transposed by ldmatrix into the A fragment's order
+        const int mi = lane >> 3;
+        const int trow = row0 + (mi >> 1) * 8 + (lane & 7);
 #pragma unroll
-        for (int n2 = 0; n2 < NTO / 2; ++n2) {
-          const int trow = row0 + (mi & 1) * 8 + rr;
-          const int dim = (2 * n2 + (mi >> 1)) * 8;
-          uint32_t v0, v1, v2, v3;
-          ldsm_x4_trans(vbase + (dim >> 6) * slice + swz(trow, (dim & 63) >> 3), v0, v1, v2, v3);
-          ME::mma16816(o[2 * n2], pa, v0, v1);
-          ME::mma16816(o[2 * n2 + 1], pa, v2, v3);
+        for (int mb = 0; mb < MB; ++mb) {
+          const int dim = mb * 16 + (mi & 1) * 8;
+          uint32_t a[4];
+          ldsm_x4_trans(vbase + (dim >> 6) * slice + swz(trow, (dim & 63) >> 3), a[0], a[1], a[2],
+                        a[3]);
+          ME::mma16816(o[mb], a, pb0, pb1);
         }
       }
     }
@@ -323,26 +351,37 @@ __device__ __forceinline__ bool mma_consumer(const DecodeParams& prm, const Work
     __syncwarp();
     if (lane == 0) mbar_arrive(smem_u32(&empty_bar[s]));
   }
-  // a head row's sums are spread over the four lanes of its quad
-  l += __shfl_xor_sync(0xffffffffu, l, 1);
-  l += __shfl_xor_sync(0xffffffffu, l, 2);
-  lp += __shfl_xor_sync(0xffffffffu, lp, 1);
-  lp += __shfl_xor_sync(0xffffffffu, lp, 2);
-  const bool aborted = named_bar_or(1, C::NCW * 32, *abort_flag != 0);
-  if (!aborted && r < GROUP) {
+  // a head's sums are spread over the 8 lanes of its column
 #pragma unroll
-    for (int t = 0; t < NTO; ++t) {
-      // column 2c (+1) of n-tile t is dim 8t + 2c (+1); with FP8 fragments,
-      // n-tile t holds dims 16(t/2) + 4c + (t%2) (and + 2)
-      const int d0 = C::SWZ8 ? 16 * (t >> 1) + 2 * k0 + (t & 1) : t * 8 + k0;
-      const int d1 = C::SWZ8 ? d0 + 2 : d0 + 1;
-      red_o[(warp * GROUP + r) * HEAD_DIM + d0] = o[t][0];
-      red_o[(warp * GROUP + r) * HEAD_DIM + d1] = o[t][1];
+  for (int h = 0; h < 2; ++h) {
+#pragma unroll
+    for (int x = 4; x < 32; x <<= 1) {
+      l[h] += __shfl_xor_sync(0xffffffffu, l[h], x);
+      lp[h] += __shfl_xor_sync(0xffffffffu, lp[h], x);
     }
-    if ((lane & 3) == 0) {
-      red_m[warp * GROUP + r] = m;
-      red_l[warp * GROUP + r] = l;
-      red_lp[warp * GROUP + r] = lp;
+  }
+  const bool aborted = named_bar_or(1, C::NCW * 32, *abort_flag != 0);
+  if (!aborted) {
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int head = 2 * c + h;
+      if (head < GROUP) {
+        float* op = red_o + (warp * GROUP + head) * HEAD_DIM;
+#pragma unroll
+        for (int t = 0; t < MB; ++t) {
+          // rows g and g + 8 of block t: dims 16t + g and + 8, or with FP8
+          // fragments dims 16t + 2g and + 1
+          const int d0 = C::SWZ8 ? 16 * t + 2 * g : 16 * t + g;
+          const int d1 = C::SWZ8 ? d0 + 1 : d0 + 8;
+          op[d0] = o[t][h];
+          op[d1] = o[t][h + 2];
+        }
+        if (g == 0) {
+          red_m[warp * GROUP + head] = m[h];
+          red_l[warp * GROUP + head] = l[h];
+          red_lp[warp * GROUP + head] = lp[h];
+        }
+      }
     }
   }
   return aborted;

@@ -180,6 +180,14 @@ __device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t& r0, uint3
                : "memory");
 }
 
+// Transpose of an 8x8 matrix of 16-bit elements held in registers, in the
+// ldmatrix fragment layout (lane l: row l / 4, elements 2 (l % 4) and + 1).
+__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t a) {
+  uint32_t d;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(d) : "r"(a));
+  return d;
+}
+
 // ---- tcgen05 (5th-generation tensor cores, accumulators in TMEM) ---------
 
 // TMEM allocation: executed by one whole warp; the base address is written to
