@@ -37,14 +37,16 @@ constexpr float kLn2 = 0.6931471805599453f;
 
 template <int HEAD_DIM, int GROUP, int KVB>   // KVB: bytes per cache element (2, or 1 for FP8)
 struct DecodeCfg {
-  // GQA groups of 4 or 8 heads at head_dim <= 128 use the tensor cores: the
-  // g heads are the M rows of m16n8k16 MMAs (padded to 16), 16 tokens per step
+  // GQA groups of 4 or 8 heads at head_dim <= 128 use the tensor cores:
+  // m16n8k16 MMAs with 16 tokens as the rows and the g heads as the 8 columns
   static constexpr bool MMA = GROUP >= 4 && HEAD_DIM <= 128;
   // tokens per stage: 32 KB of K+V, for 16-bit caches and the FP8 tensor-core
   // consumer (two 16-token chunks per consumer warp and stage); 16 KB for
   // the FP8 SIMT consumer, which runs three CTAs per SM
   static constexpr int TILE = (KVB == 1 && MMA ? 16384 : 8192) / HEAD_DIM;
-  static constexpr int NSTAGE = KVB == 2 || MMA ? 3 : 4;   // FP8 SIMT: 16 KB stages, one deeper
+  // tensor-core consumer: two 32 KB stages per CTA, three CTAs per SM;
+  // 16-bit SIMT: three; FP8 SIMT: 16 KB stages, four deep
+  static constexpr int NSTAGE = MMA ? 2 : (KVB == 2 ? 3 : 4);
   static constexpr int NCW = 4;                        // consumer warps
   static constexpr int THREADS = 32 * (NCW + 1);       // + one producer warp
   static constexpr int LPT = HEAD_DIM / 8;             // lanes per token row (8 dims each)
@@ -62,9 +64,10 @@ struct DecodeCfg {
   static constexpr bool SWZ8 = KVB == 1 && HEAD_DIM == 128;
   static constexpr int CONV_BYTES = (KVB == 1 && MMA && !SWZ8) ? NCW * 2 * 16 * HEAD_DIM * 2 : 0;
   static constexpr int SMEM_BYTES = NSTAGE * STAGE_BYTES + CONV_BYTES + 1024;  // + alignment
-  // CTAs per SM: the FP8 SIMT consumer (65 KB) fits three, for more warps
-  // to hide its conversion work, where 1 or 2 heads leave registers to spare
-  static constexpr int MIN_BLOCKS = (KVB == 1 && !MMA && GROUP <= 2) ? 3 : 2;
+  // CTAs per SM: three for the tensor-core consumer (two 32 KB stages, at
+  // most 136 registers) and for the FP8 SIMT consumer of 1 or 2 heads (65 KB),
+  // for more warps to hide their latency; two otherwise
+  static constexpr int MIN_BLOCKS = (MMA || (KVB == 1 && GROUP <= 2)) ? 3 : 2;
   static_assert(PASSES % SUB == 0, "");
   static_assert(!MMA || TOK_PER_WARP % 16 == 0, "");
   static_assert(NCW * GROUP * HEAD_DIM * 4 + 3 * NCW * GROUP * 4 <= NSTAGE * STAGE_BYTES, "");
