@@ -39,7 +39,9 @@ template <int HEAD_DIM, int GROUP, int KVB>   // KVB: bytes per cache element (2
 struct DecodeCfg {
   // GQA groups of 4 or 8 heads at head_dim <= 128 use the tensor cores:
   // m16n8k16 MMAs with 16 tokens as the rows and the g heads as the 8 columns
-  static constexpr bool MMA = GROUP >= 4 && HEAD_DIM <= 128;
+  // (zero-padded); so do FP8 caches with 1 or 2 heads, where the MMAs replace
+  // the SIMT consumer's shuffle-reduced dot products
+  static constexpr bool MMA = (GROUP >= 4 || KVB == 1) && HEAD_DIM <= 128;
   // tokens per stage: 32 KB of K+V, for 16-bit caches and the FP8 tensor-core
   // consumer (two 16-token chunks per consumer warp and stage); 16 KB for
   // the FP8 SIMT consumer, which runs three CTAs per SM
