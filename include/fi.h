@@ -146,6 +146,7 @@ typedef struct {
   int64_t total_kv_tokens;  /* sum of kv_len */
   int32_t num_prefix_items; /* shared-prefix work (prefix chunk x row tile x head) */
   int32_t num_prefix_groups;
+  int64_t host_io_bytes;    /* extra workspace of fi_batch_attention_host */
 } fi_plan_info;
 
 /*
@@ -310,6 +311,48 @@ fi_status fi_batch_prefill_paged(fi_plan_t plan, const void* q, const int32_t* q
                                  const int32_t* last_page_len_d, float sm_scale, float k_scale,
                                  float v_scale, void* out, float* lse, void* workspace,
                                  size_t workspace_bytes, void* stream);
+
+/*
+ * fi_batch_attention_host — one serving step of a plan with the step's own
+ * inputs and outputs in host memory. q and the page table (with qo_indptr
+ * for a prefill plan) are copied to the device, the planned kernels run
+ * exactly as fi_batch_decode_paged / fi_batch_prefill_paged run them, out
+ * and lse are copied back, and the call returns once the step has
+ * completed (it synchronises `stream`) with the device status of the step
+ * (a device-side error word that fi_check_device_status would read is read
+ * and cleared here). The KV cache stays in device memory: it is the cache.
+ * The page table is gathered into a pinned staging buffer of the library
+ * and crosses the link in one copy; q, out and lse are copied straight
+ * from and to the caller's buffers (page-locked buffers make those copies
+ * DMA transfers; pageable ones work, through the driver's staging).
+ *   plan             from fi_plan, either mode.
+ *   q_h              host [total q rows][num_qo_heads][head_dim], the plan's
+ *                    dtype (total q rows = B for a decode plan,
+ *                    qo_indptr_h[B] for a prefill plan).
+ *   qo_indptr_h      host int32 [B+1] for a prefill plan; NULL for decode.
+ *   k_cache, v_cache, kv_layout, page_stride_elems, num_pages, sm_scale,
+ *   k_scale, v_scale as for fi_batch_decode_paged (the caches are device
+ *                    memory).
+ *   page_indptr_h, page_indices_h, last_page_len_h  host int32, the planned
+ *                    page table (page_indices_h holds page_indptr_h[B]
+ *                    entries).
+ *   out_h            host, q_h's shape and dtype.
+ *   lse_h            host fp32 [total q rows][num_qo_heads] or NULL.
+ *   workspace        device, 256-byte aligned, at least workspace_bytes +
+ *                    host_io_bytes of the plan (fi_plan_get_info): the
+ *                    step's q, page table, out and lse occupy the part after
+ *                    the run calls' workspace.
+ * Errors: as for fi_batch_decode_paged (FI_ERR_WORKSPACE_TOO_SMALL when the
+ * host-IO part does not fit), FI_ERR_DEVICE_TIMEOUT / FI_ERR_DEVICE_BOUNDS
+ * from the step's device status.
+ */
+fi_status fi_batch_attention_host(fi_plan_t plan, const void* q_h, const int32_t* qo_indptr_h,
+                                  const void* k_cache, const void* v_cache, int32_t kv_layout,
+                                  int64_t page_stride_elems, int32_t num_pages,
+                                  const int32_t* page_indptr_h, const int32_t* page_indices_h,
+                                  const int32_t* last_page_len_h, float sm_scale, float k_scale,
+                                  float v_scale, void* out_h, float* lse_h, void* workspace,
+                                  size_t workspace_bytes, void* stream);
 
 /*
  * fi_merge_states — combine attention states computed over disjoint key

@@ -40,7 +40,8 @@ LAYOUTS = {"NHD": FI_LAYOUT_NHD, "HND": FI_LAYOUT_HND}
 EXPORTED = ["fi_plan", "fi_plan_destroy", "fi_plan_get_info", "fi_plan_get_work",
             "fi_batch_decode_paged", "fi_batch_prefill_paged", "fi_merge_states",
             "fi_check_device_status", "fi_status_string", "fi_last_error_string",
-            "fi_debug_set_fault", "fi_profile_next_launch", "fi_batch_decode_paged_noalloc"]
+            "fi_debug_set_fault", "fi_profile_next_launch", "fi_batch_decode_paged_noalloc",
+            "fi_batch_attention_host"]
 
 
 class FiError(RuntimeError):
@@ -66,7 +67,8 @@ class PlanInfo(ctypes.Structure):
                 ("num_prefill_items", ctypes.c_int32), ("chunk_tokens", ctypes.c_int32),
                 ("num_split_requests", ctypes.c_int32), ("num_partial_slots", ctypes.c_int32),
                 ("workspace_bytes", ctypes.c_int64), ("total_kv_tokens", ctypes.c_int64),
-                ("num_prefix_items", ctypes.c_int32), ("num_prefix_groups", ctypes.c_int32)]
+                ("num_prefix_items", ctypes.c_int32), ("num_prefix_groups", ctypes.c_int32),
+                ("host_io_bytes", ctypes.c_int64)]
 
 
 _lib = None
@@ -105,6 +107,8 @@ def lib():
     L.fi_profile_next_launch.argtypes = [_P, _P]
     L.fi_batch_decode_paged_noalloc.argtypes = [_P, _P, _P, _P, _I32, _I64, _I32, _P, _P, _P,
                                                 _F, _F, _F, _P, _P, _P]
+    L.fi_batch_attention_host.argtypes = [_P, _P, _P, _P, _P, _I32, _I64, _I32, _P, _P, _P,
+                                          _F, _F, _F, _P, _P, _P, ctypes.c_size_t, _P]
     for name in EXPORTED:
         if name not in ("fi_status_string", "fi_last_error_string"):
             getattr(L, name).restype = _I32
@@ -240,6 +244,23 @@ def fi_batch_prefill_paged(plan: Plan, q, qo_indptr_d, k_cache, v_cache, kv_layo
                                       float(v_scale), _ptr(out), _ptr(lse), _ptr(workspace),
                                       int(wsb), _stream(stream))
     _check(st, "fi_batch_prefill_paged")
+
+
+def fi_batch_attention_host(plan: Plan, q_h, qo_indptr_h, k_cache, v_cache, kv_layout,
+                            page_stride_elems, num_pages, page_indptr_h, page_indices_h,
+                            last_page_len_h, sm_scale, k_scale, v_scale, out_h, lse_h, workspace,
+                            workspace_bytes, stream=None):
+    """q_h / out_h / lse_h: host tensors or arrays (page-locked for
+    asynchronous copies); the page-table arguments: host int32 arrays;
+    the caches and the workspace (workspace_bytes + host_io_bytes of the
+    plan): device memory."""
+    st = lib().fi_batch_attention_host(plan.handle, _ptr(q_h), _ptr(qo_indptr_h), _ptr(k_cache),
+                                       _ptr(v_cache), int(kv_layout), int(page_stride_elems),
+                                       int(num_pages), _ptr(page_indptr_h), _ptr(page_indices_h),
+                                       _ptr(last_page_len_h), float(sm_scale), float(k_scale),
+                                       float(v_scale), _ptr(out_h), _ptr(lse_h), _ptr(workspace),
+                                       int(workspace_bytes), _stream(stream))
+    _check(st, "fi_batch_attention_host")
 
 
 def fi_merge_states(v, s, n, S, H, d, out_dtype, out, lse_out, stream=None):

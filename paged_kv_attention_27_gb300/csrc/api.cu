@@ -84,7 +84,8 @@ struct Staging {
   bool pending[kStagingSlots] = {};
   int next = 0;
 };
-thread_local Staging g_staging;
+thread_local Staging g_staging;   // work lists (every run call)
+thread_local Staging g_tables;    // page tables (host-buffer calls)
 
 // The workspace prefix a run uploads: zeroed header (error word, work
 // counter), work lists, merge tasks, zeroed merge counters; alignment gaps
@@ -110,9 +111,12 @@ void fill_image(uint8_t* dst, const fi::Plan& P) {
   }
 }
 
-fi_status upload_image(void* dst, const fi::Plan& P, cudaStream_t stream) {
-  Staging& s = g_staging;
-  const size_t bytes = P.ws.partial_o;
+// Fills `bytes` bytes of a pinned slot of `s` with `fill` and copies them
+// to device `dst` on `stream` (synchronous pageable copy if pinned memory
+// cannot be had).
+template <class Fill>
+fi_status stage_and_copy(Staging& s, void* dst, size_t bytes, Fill fill, cudaStream_t stream,
+                         const char* what) {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess) return FI_ERR_NO_DEVICE;
   if (s.device != dev || bytes > s.slot_bytes) {
@@ -140,9 +144,9 @@ fi_status upload_image(void* dst, const fi::Plan& P, cudaStream_t stream) {
       s = Staging();
       cudaGetLastError();   // clear; fall back to a (synchronous) pageable copy
       std::vector<uint8_t> image(bytes);
-      fill_image(image.data(), P);
+      fill(image.data());
       const cudaError_t e = cudaMemcpy(dst, image.data(), bytes, cudaMemcpyHostToDevice);
-      return e == cudaSuccess ? FI_OK : cuda_fail(e, "work-list upload");
+      return e == cudaSuccess ? FI_OK : cuda_fail(e, what);
     }
     s.device = dev;
     s.buf = static_cast<uint8_t*>(p);
@@ -152,14 +156,19 @@ fi_status upload_image(void* dst, const fi::Plan& P, cudaStream_t stream) {
   s.next = (s.next + 1) % kStagingSlots;
   cudaError_t e = cudaSuccess;
   if (s.pending[i]) e = cudaEventSynchronize(s.done[i]);
-  if (e != cudaSuccess) return cuda_fail(e, "work-list staging");
+  if (e != cudaSuccess) return cuda_fail(e, what);
   uint8_t* src = s.buf + size_t(i) * s.slot_bytes;
-  fill_image(src, P);
+  fill(src);
   e = cudaMemcpyAsync(dst, src, bytes, cudaMemcpyHostToDevice, stream);
   if (e == cudaSuccess) e = cudaEventRecord(s.done[i], stream);
-  if (e != cudaSuccess) return cuda_fail(e, "work-list upload");
+  if (e != cudaSuccess) return cuda_fail(e, what);
   s.pending[i] = true;
   return FI_OK;
+}
+
+fi_status upload_image(void* dst, const fi::Plan& P, cudaStream_t stream) {
+  return stage_and_copy(g_staging, dst, P.ws.partial_o,
+                        [&](uint8_t* p) { fill_image(p, P); }, stream, "work-list upload");
 }
 
 // Tensor map over a paged K or V cache that fetches one (page, kv head)
@@ -250,6 +259,21 @@ fi_status check_device() {
 }
 
 // Shared body of the two paged run calls.
+// Checks of a run call's layout, scales and page stride (no device access).
+fi_status check_run_scalars(const fi::Plan& P, int32_t kv_layout, int64_t page_stride_elems,
+                            float sm_scale, float k_scale, float v_scale) {
+  if (kv_layout != FI_LAYOUT_NHD && kv_layout != FI_LAYOUT_HND) return FI_ERR_INVALID_ARG;
+  if (!(sm_scale >= 0.f) || sm_scale > 3.0e38f) return FI_ERR_INVALID_ARG;  // also rejects NaN
+  if (!(k_scale > 0.f) || k_scale > 3.0e38f || !(v_scale > 0.f) || v_scale > 3.0e38f)
+    return FI_ERR_INVALID_ARG;
+  const int64_t page_elems = int64_t(P.page_size) * P.num_kv_heads * P.head_dim;
+  if (page_stride_elems == 0) page_stride_elems = page_elems;
+  // page starts 16-byte aligned for TMA
+  if (page_stride_elems < page_elems || page_stride_elems % (16 / elem_bytes(P.kv_dtype)) != 0)
+    return FI_ERR_INVALID_ARG;
+  return FI_OK;
+}
+
 fi_status run_paged(fi_plan_t plan, bool prefill_call, const void* q, const int32_t* qo_indptr_d,
                     const void* k_cache, const void* v_cache, int32_t kv_layout,
                     int64_t page_stride_elems, int32_t num_pages, const int32_t* page_indptr_d,
@@ -268,17 +292,12 @@ fi_status run_paged(fi_plan_t plan, bool prefill_call, const void* q, const int3
   if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16) ||
       !aligned(workspace, 256) || (lse && !aligned(lse, 4)))
     return FI_ERR_INVALID_ARG;
-  if (kv_layout != FI_LAYOUT_NHD && kv_layout != FI_LAYOUT_HND) return FI_ERR_INVALID_ARG;
-  if (!(sm_scale >= 0.f) || sm_scale > 3.0e38f) return FI_ERR_INVALID_ARG;  // also rejects NaN
-  if (!(k_scale > 0.f) || k_scale > 3.0e38f || !(v_scale > 0.f) || v_scale > 3.0e38f)
-    return FI_ERR_INVALID_ARG;
+  fi_status st = check_run_scalars(P, kv_layout, page_stride_elems, sm_scale, k_scale, v_scale);
+  if (st != FI_OK) return st;
   const int64_t page_elems = int64_t(P.page_size) * P.num_kv_heads * P.head_dim;
   if (page_stride_elems == 0) page_stride_elems = page_elems;
-  // page starts 16-byte aligned for TMA
-  if (page_stride_elems < page_elems || page_stride_elems % (16 / elem_bytes(P.kv_dtype)) != 0)
-    return FI_ERR_INVALID_ARG;
   if (workspace_bytes < P.ws.total) return FI_ERR_WORKSPACE_TOO_SMALL;
-  fi_status st = check_device();
+  st = check_device();
   if (st != FI_OK) return st;
 
   cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
@@ -496,6 +515,7 @@ fi_status fi_plan_get_info(fi_plan_t plan, fi_plan_info* info) {
   info->num_partial_slots = P.num_slots;
   info->workspace_bytes = int64_t(P.ws.total);
   info->total_kv_tokens = P.total_kv;
+  info->host_io_bytes = int64_t(P.ws.hio_total);
   return FI_OK;
 }
 
@@ -543,6 +563,78 @@ fi_status fi_batch_prefill_paged(fi_plan_t plan, const void* q, const int32_t* q
   return run_paged(plan, true, q, qo_indptr_d, k_cache, v_cache, kv_layout, page_stride_elems,
                    num_pages, page_indptr_d, page_indices_d, last_page_len_d, sm_scale, k_scale,
                    v_scale, out, lse, workspace, workspace_bytes, stream);
+}
+
+fi_status fi_batch_attention_host(fi_plan_t plan, const void* q_h, const int32_t* qo_indptr_h,
+                                  const void* k_cache, const void* v_cache, int32_t kv_layout,
+                                  int64_t page_stride_elems, int32_t num_pages,
+                                  const int32_t* page_indptr_h, const int32_t* page_indices_h,
+                                  const int32_t* last_page_len_h, float sm_scale, float k_scale,
+                                  float v_scale, void* out_h, float* lse_h, void* workspace,
+                                  size_t workspace_bytes, void* stream_ptr) {
+  if (!plan) return FI_ERR_INVALID_ARG;
+  const fi::Plan& P = plan->p;
+  const bool prefill = P.mode == FI_MODE_PREFILL;
+  if (P.batch == 0) return FI_OK;
+  if (!q_h || !out_h || !page_indptr_h || !last_page_len_h || !workspace || !k_cache ||
+      !v_cache || (prefill && !qo_indptr_h) || (P.page_entries > 0 && !page_indices_h))
+    return FI_ERR_INVALID_ARG;
+  if (P.total_kv > 0 && num_pages <= 0) return FI_ERR_INVALID_ARG;
+  if (num_pages < 0 || !aligned(workspace, 256) || !aligned(k_cache, 16) || !aligned(v_cache, 16))
+    return FI_ERR_INVALID_ARG;
+  fi_status st = check_run_scalars(P, kv_layout, page_stride_elems, sm_scale, k_scale, v_scale);
+  if (st != FI_OK) return st;
+  if (workspace_bytes < P.ws.total + P.ws.hio_total) return FI_ERR_WORKSPACE_TOO_SMALL;
+  st = check_device();
+  if (st != FI_OK) return st;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  const size_t q_bytes = size_t(P.total_q) * P.num_qo_heads * P.head_dim * 2;
+  const size_t lse_bytes = size_t(P.total_q) * P.num_qo_heads * sizeof(float);
+  // device copies of the step's inputs, in the host-IO part of the workspace
+  int32_t* tab = reinterpret_cast<int32_t*>(ws + P.ws.hio_tables);
+  int32_t* indptr_d = tab;
+  int32_t* indices_d = indptr_d + (P.batch + 1);
+  int32_t* last_d = indices_d + P.page_entries;
+  int32_t* qo_d = prefill ? last_d + P.batch : nullptr;
+  const size_t table_bytes =
+      (size_t(P.batch + 1) + P.page_entries + P.batch + (prefill ? P.batch + 1 : 0)) *
+      sizeof(int32_t);
+  // the page table (and qo_indptr) in one pinned copy; q straight from the caller
+  st = stage_and_copy(
+      g_tables, tab, table_bytes,
+      [&](uint8_t* p) {
+        int32_t* t = reinterpret_cast<int32_t*>(p);
+        std::memcpy(t, page_indptr_h, size_t(P.batch + 1) * sizeof(int32_t));
+        t += P.batch + 1;
+        if (P.page_entries > 0) std::memcpy(t, page_indices_h, size_t(P.page_entries) * sizeof(int32_t));
+        t += P.page_entries;
+        std::memcpy(t, last_page_len_h, size_t(P.batch) * sizeof(int32_t));
+        t += P.batch;
+        if (prefill) std::memcpy(t, qo_indptr_h, size_t(P.batch + 1) * sizeof(int32_t));
+      },
+      stream, "page-table upload");
+  if (st != FI_OK) return st;
+  cudaError_t e = cudaMemcpyAsync(ws + P.ws.hio_q, q_h, q_bytes, cudaMemcpyHostToDevice, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "q upload");
+  void* out_d = ws + P.ws.hio_out;
+  float* lse_d = lse_h ? reinterpret_cast<float*>(ws + P.ws.hio_lse) : nullptr;
+  st = run_paged(plan, prefill, ws + P.ws.hio_q, qo_d, k_cache, v_cache, kv_layout,
+                 page_stride_elems, num_pages, indptr_d, indices_d, last_d, sm_scale, k_scale,
+                 v_scale, out_d, lse_d, workspace, P.ws.total, stream_ptr);
+  if (st != FI_OK) return st;
+  e = cudaMemcpyAsync(out_h, out_d, q_bytes, cudaMemcpyDeviceToHost, stream);
+  if (e == cudaSuccess && lse_h)
+    e = cudaMemcpyAsync(lse_h, lse_d, lse_bytes, cudaMemcpyDeviceToHost, stream);
+  // the step's device status (error word at the start of the workspace)
+  uint32_t word = 0;
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(&word, workspace, sizeof(word), cudaMemcpyDeviceToHost, stream);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+  if (e != cudaSuccess) return cuda_fail(e, "host-buffer step");
+  if (word & fi::kErrTimeout) return FI_ERR_DEVICE_TIMEOUT;
+  if (word & fi::kErrBounds) return FI_ERR_DEVICE_BOUNDS;
+  return FI_OK;
 }
 
 fi_status fi_merge_states(const float* v, const float* s, int32_t n, int32_t S, int32_t H,

@@ -62,6 +62,10 @@ struct WorkspaceLayout {
   size_t decode_items = 0, prefill_items = 0, prefix_items = 0, prefix_tables = 0, merges = 0,
          merge_counters = 0, partial_o = 0, partial_lse = 0;
   size_t total = 0;
+  // host-buffer calls only, after `total`: the step's q, page table (page
+  // indptr | page indices | last page lengths | qo indptr), out and lse
+  size_t hio_q = 0, hio_tables = 0, hio_out = 0, hio_lse = 0;
+  size_t hio_total = 0;   // bytes of that region
 };
 
 struct Plan {
@@ -86,6 +90,7 @@ struct Plan {
   int32_t num_slots = 0;
   int64_t total_kv = 0;
   int64_t total_q = 0;                   // rows of q / out
+  int32_t page_entries = 0;              // page_indptr[batch]: length of page_indices
   WorkspaceLayout ws;
 };
 

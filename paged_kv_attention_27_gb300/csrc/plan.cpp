@@ -348,6 +348,21 @@ fi_status build_plan(int32_t mode, int32_t batch, const int32_t* qo_indptr,
   p.ws.partial_lse = off;
   off = align_up(off + size_t(p.num_slots) * num_qo_heads * sizeof(float));
   p.ws.total = off;
+  // host-buffer calls: q and out of the plan's 16-bit dtype, fp32 lse, and
+  // the page table (plus qo_indptr for a prefill plan) as int32
+  p.page_entries = batch > 0 ? page_indptr[batch] : 0;
+  const size_t q_bytes = size_t(p.total_q) * num_qo_heads * head_dim * 2;
+  const size_t table_ints = size_t(batch + 1) + size_t(p.page_entries) + size_t(batch) +
+                            (mode == FI_MODE_PREFILL ? size_t(batch + 1) : 0);
+  p.ws.hio_q = off;
+  off = align_up(off + q_bytes);
+  p.ws.hio_tables = off;
+  off = align_up(off + table_ints * sizeof(int32_t));
+  p.ws.hio_out = off;
+  off = align_up(off + q_bytes);
+  p.ws.hio_lse = off;
+  off = align_up(off + size_t(p.total_q) * num_qo_heads * sizeof(float));
+  p.ws.hio_total = off - p.ws.total;
 
   *out = std::move(p);
   return FI_OK;

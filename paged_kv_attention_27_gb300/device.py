@@ -95,5 +95,30 @@ class DeviceBatch:
                                      self.out, self.lse, self.workspace, stream=stream)
         return self.out, self.lse
 
+    def run_host(self, stream=None):
+        """The same step through fi_batch_attention_host: q and the page table
+        from (pinned) host memory, out and lse back into host memory; returns
+        the host (CPU) out and lse tensors. Uses its own workspace with room
+        for the call's host-IO part."""
+        b = self.b
+        info = B.fi_plan_get_info(self.plan)
+        ws_bytes = info["workspace_bytes"] + info["host_io_bytes"]
+        if getattr(self, "_ws_host", None) is None or self._ws_host.numel() < ws_bytes:
+            self._ws_host = torch.empty(max(ws_bytes, 256), dtype=torch.uint8,
+                                        device=self.device)
+        q_h = self.q.cpu().pin_memory()
+        out_h = torch.empty(self.out.shape, dtype=self.out.dtype).pin_memory()
+        lse_h = (torch.empty(self.lse.shape, dtype=torch.float32).pin_memory()
+                 if self.lse is not None else None)
+        prefill = self.mode == B.FI_MODE_PREFILL
+        B.fi_batch_attention_host(self.plan, q_h,
+                                  b.qo_indptr.astype(np.int32) if prefill else None,
+                                  self.k, self.v, B.LAYOUTS[b.layout], 0, b.num_pages,
+                                  b.page_indptr.astype(np.int32),
+                                  b.page_indices.astype(np.int32), b.last_page_len.astype(np.int32),
+                                  b.sm_scale, b.k_scale, b.v_scale, out_h, lse_h, self._ws_host,
+                                  ws_bytes, stream=stream)
+        return out_h, lse_h
+
     def status(self, stream=None) -> int:
         return B.fi_check_device_status(self.workspace, stream)

@@ -397,3 +397,51 @@ def test_shared_prefix_validation(case, status):
     with pytest.raises(B.FiError) as e:
         B.fi_plan(mode, 3, qo, b.page_indptr, b.last_page_len, 8, 2, 128, 16, 0, opts, 152)
     assert e.value.status == status
+
+
+def test_host_buffer_call_sizes_its_region_and_checks_before_any_copy():
+    """fi_batch_attention_host: the plan reports the workspace part that holds
+    the step's q, page table, out and lse (each region 256-byte aligned); bad
+    arguments and a short workspace are refused before anything is copied, and
+    a well-formed call on a machine without a GPU reports that."""
+    torch = pytest.importorskip("torch")
+    if torch.cuda.is_available():
+        pytest.skip("uses fake device addresses; only meaningful without a GPU")
+    rnd = lambda n: (n + 255) // 256 * 256
+    # decode: 2 rows x 8 heads x d128 (bf16) for q and out; page table 3 + 3 + 2 int32
+    p = B.fi_plan(B.FI_MODE_DECODE, 2, None, [0, 2, 3], [5, 16], 8, 2, 128, 16, 0, None, 4)
+    info = B.fi_plan_get_info(p)
+    assert info["host_io_bytes"] == 2 * rnd(2 * 8 * 128 * 2) + rnd(8 * 4) + rnd(2 * 8 * 4)
+    # prefill: 4 rows; the page table gains qo_indptr (3 more int32)
+    pf = B.fi_plan(B.FI_MODE_PREFILL, 2, [0, 3, 4], [0, 2, 3], [5, 16], 8, 2, 128, 16, 1,
+                   None, 4)
+    info_f = B.fi_plan_get_info(pf)
+    assert info_f["host_io_bytes"] == 2 * rnd(4 * 8 * 128 * 2) + rnd(11 * 4) + rnd(4 * 8 * 4)
+
+    fake = 1 << 20    # aligned device address, never dereferenced here
+    q_h = np.zeros((2, 8, 128), np.uint16)
+    out_h = np.zeros_like(q_h)
+    lse_h = np.zeros((2, 8), np.float32)
+    indptr, indices, last = (np.array(a, np.int32) for a in ([0, 2, 3], [0, 1, 2], [5, 16]))
+    need = info["workspace_bytes"] + info["host_io_bytes"]
+    args = [p, q_h, None, fake, fake, B.FI_LAYOUT_NHD, 0, 4, indptr, indices, last, 0.1, 1.0,
+            1.0, out_h, lse_h, fake, need]
+    with pytest.raises(B.FiError) as e:
+        B.fi_batch_attention_host(*args[:-1], info["workspace_bytes"], stream=0)
+    assert e.value.status == B.FI_ERR_WORKSPACE_TOO_SMALL
+    for pos, bad_value in ((1, None), (14, None), (8, None), (3, None), (5, 7), (11, -1.0),
+                           (12, 0.0), (16, fake + 8)):
+        bad = list(args)
+        bad[pos] = bad_value   # q_h, out_h, page_indptr_h, k_cache, layout, scales, alignment
+        with pytest.raises(B.FiError) as e:
+            B.fi_batch_attention_host(*bad, stream=0)
+        assert e.value.status == B.FI_ERR_INVALID_ARG, pos
+    with pytest.raises(B.FiError) as e:      # a prefill plan needs qo_indptr_h
+        B.fi_batch_attention_host(pf, np.zeros((4, 8, 128), np.uint16), None, fake, fake,
+                                  B.FI_LAYOUT_NHD, 0, 4, indptr, indices, last, 0.1, 1.0, 1.0,
+                                  np.zeros((4, 8, 128), np.uint16), None, fake,
+                                  info_f["workspace_bytes"] + info_f["host_io_bytes"], stream=0)
+    assert e.value.status == B.FI_ERR_INVALID_ARG
+    with pytest.raises(B.FiError) as e:
+        B.fi_batch_attention_host(*args, stream=0)
+    assert e.value.status == B.FI_ERR_NO_DEVICE

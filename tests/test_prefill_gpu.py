@@ -251,3 +251,29 @@ def test_fp16_prefill_4k_full_size():
     b = synth.make_batch("fp16 causal prefill B2 L4096", b.kv_lens, b.qo_lens, 64, 8, 128, 16,
                          synth.NHD, None, True, 602, dtype="fp16")
     check_sampled(b, per_request=16)
+
+
+@pytest.mark.parametrize("which", ["decode", "mixed", "prefill"])
+def test_host_buffer_call_matches_device_call(which):
+    """fi_batch_attention_host copies q and the page table in, runs the same
+    kernels and copies out and lse back: bitwise the device-buffer call's
+    results, and within the oracle's tolerances."""
+    from paged_kv_attention_27_gb300.device import DeviceBatch
+    if which == "decode":
+        b, mode = synth.tiny_decode(), B.FI_MODE_DECODE
+    elif which == "mixed":
+        b, mode = synth.small_mixed(), B.FI_MODE_PREFILL
+    else:
+        kv = [1, 17, 129, 300]
+        b = synth.make_batch("host-call prefill d128 P16", kv, kv, 8, 2, 128, 16, synth.NHD, None,
+                             True, 41)
+        mode = B.FI_MODE_PREFILL
+    db = DeviceBatch(b, mode=mode)
+    out_d, lse_d = db.run()
+    torch.cuda.synchronize()
+    assert db.status() == B.FI_OK
+    out_h, lse_h = db.run_host()
+    assert torch.equal(out_h.view(torch.int16), out_d.cpu().view(torch.int16))
+    assert torch.equal(lse_h, lse_d.cpu())
+    ref_o, ref_l = _oracle(b)
+    compare(out_h, lse_h, ref_o, ref_l, what=f"host call, {b.name}")
