@@ -141,6 +141,7 @@ def io_bytes(b):
 KERNEL_SOURCES = {
     "decode_kernel": ["decode.cu", "ptx.cuh", "kernels.cuh", "fi_internal.h"],
     "prefill_kernel": ["prefill.cu", "ptx.cuh", "kernels.cuh", "fi_internal.h"],
+    "prefill_pair_kernel": ["prefill_pair.cu", "ptx.cuh", "kernels.cuh", "fi_internal.h"],
 }
 
 
@@ -407,9 +408,13 @@ def roofline_of(b, kvb, flops, kern_ms, kernel_names, workload):
 
 
 def kernels_of(b, info):
+    """The kernels a plan launches (the two-tile prefill kernel takes plain
+    prefill work at head_dim 64 and 128 with an even number of query heads
+    per kv head; the one-tile kernel the rest)."""
     names = []
     if info["num_prefill_items"]:
-        names.append("prefill_kernel")
+        pair = b.head_dim in (64, 128) and (b.num_qo_heads // b.num_kv_heads) % 2 == 0
+        names.append("prefill_pair_kernel" if pair else "prefill_kernel")
     if info["num_decode_items"]:
         names.append("decode_kernel")
     return names

@@ -21,7 +21,8 @@ BUILD = os.path.join(HERE, "_build")
 LIBDIR = os.path.join(HERE, "lib")
 LIB = os.path.join(LIBDIR, "libfi.so")
 
-SOURCES = ["plan.cpp", "api.cu", "decode.cu", "merge.cu", "prefill.cu", "noalloc.cu"]
+SOURCES = ["plan.cpp", "api.cu", "decode.cu", "merge.cu", "prefill.cu", "prefill_pair.cu",
+           "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

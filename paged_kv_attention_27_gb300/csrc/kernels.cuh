@@ -79,6 +79,14 @@ struct PrefillParams {
 cudaError_t launch_prefill(int head_dim, int dtype, const CUtensorMap& qm, const CUtensorMap& km,
                            const CUtensorMap& vm, const PrefillParams& p, int grid,
                            cudaStream_t stream);
+// The two-tile prefill kernel (prefill_pair.cu): items 2p and 2p + 1 (the
+// planner's adjacent query heads h, h + 1 of one tile, h even) run in one
+// CTA. It applies to head_dim 64 and 128, even groups, plain prefill (one
+// head per tile row, no state output); launch_prefill dispatches to it.
+bool prefill_pair_applies(int head_dim, const PrefillParams& p);
+cudaError_t launch_prefill_pair(int head_dim, int dtype, const CUtensorMap& qm,
+                                const CUtensorMap& km, const CUtensorMap& vm,
+                                const PrefillParams& p, int grid, cudaStream_t stream);
 // `dtype` (fi_dtype) selects the element type of q and out, `kv_dtype` that
 // of the cache (dtype or FI_DTYPE_E4M3).
 cudaError_t launch_decode(int head_dim, int group, int dtype, int kv_dtype, const CUtensorMap& km,

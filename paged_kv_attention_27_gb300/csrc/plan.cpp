@@ -288,7 +288,8 @@ fi_status build_plan(int32_t mode, int32_t batch, const int32_t* qo_indptr,
 
   // ---- prefill work: requests with two or more query rows, one item per
   //      (query tile of kPrefillTileM rows, query head); the tiles are
-  //      ordered longest first, the heads of a tile stay together
+  //      ordered longest first, the heads of a tile stay together, in head
+  //      order (the two-tile kernel runs items 2p and 2p + 1 in one CTA)
   struct Tile { int64_t len, kv_begin, kv_end; int32_t b, qt; };
   std::vector<Tile> tiles;
   for (int b = 0; b < batch; ++b) {

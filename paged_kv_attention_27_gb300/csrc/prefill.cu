@@ -772,6 +772,8 @@ cudaError_t launch_prefill(int head_dim, int dtype, const CUtensorMap& qm, const
                            const CUtensorMap& vm, const PrefillParams& p, int grid,
                            cudaStream_t stream) {
   if (p.n_items <= 0 || grid <= 0) return cudaSuccess;
+  if (prefill_pair_applies(head_dim, p))
+    return launch_prefill_pair(head_dim, dtype, qm, km, vm, p, grid, stream);
   grid = grid < p.n_items ? grid : p.n_items;
   switch (dtype) {
     case FI_DTYPE_BF16: return launch_prefill_e<Bf16>(head_dim, qm, km, vm, p, grid, stream);

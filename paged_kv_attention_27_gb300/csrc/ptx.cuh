@@ -180,6 +180,19 @@ __device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t& r0, uint3
                : "memory");
 }
 
+// Per-warpgroup register limits (all four warps of a warpgroup execute the
+// same instruction): `inc` waits until the registers it asks for have been
+// released by other warpgroups' `dec`, so the shares must add up to the
+// registers the block was launched with.
+template <uint32_t R>
+__device__ __forceinline__ void setmaxnreg_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(R));
+}
+template <uint32_t R>
+__device__ __forceinline__ void setmaxnreg_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(R));
+}
+
 // Transpose of an 8x8 matrix of 16-bit elements held in registers, in the
 // ldmatrix fragment layout (lane l: row l / 4, elements 2 (l % 4) and + 1).
 __device__ __forceinline__ uint32_t movmatrix_trans(uint32_t a) {
