@@ -107,8 +107,18 @@ def test_non_causal_prefill_including_empty_kv():
 
 @pytest.mark.parametrize("g", [1, 2, 4, 8])
 def test_group_sizes(g):
+    """Even groups run on the two-tile kernel (two query heads per CTA), g = 1
+    on the one-tile kernel."""
     kv = [255, 64, 390]
     b = synth.make_batch(f"prefill g{g}", kv, kv, 2 * g, 2, 128, 16, synth.NHD, None, True, 9 + g)
+    check_full(b)
+
+
+@pytest.mark.parametrize("g", [1, 2])
+def test_group_sizes_d64(g):
+    kv = [200, 17, 333]
+    b = synth.make_batch(f"prefill g{g} d64", kv, kv, 3 * g, 3, 64, 16, synth.HND, None, True,
+                         20 + g)
     check_full(b)
 
 
