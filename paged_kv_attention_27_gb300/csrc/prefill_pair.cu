@@ -165,202 +165,202 @@ prefill_pair_kernel(const __grid_constant__ CUtensorMap q_map,
   // before the launch), so the register split of the two branches adds up.
   if (warp >= 8) {
     setmaxnreg_dec<C::HELPER_REGS>();
-  if (warp >= 10) {
-    // ------------------------------------------------------------ producers
-    const bool is_v = warp == 11;
-    if (lane == 0) {
-      prefetch_tensormap(is_v ? &v_map : &k_map);
-      if (!is_v) prefetch_tensormap(&q_map);
-    }
-    const CUtensorMap* map = is_v ? &v_map : &k_map;
-    uint64_t* full = is_v ? bars.v_full : bars.k_full;
-    uint64_t* empty = is_v ? bars.v_empty : bars.k_empty;
-    const uint32_t ring = base + (is_v ? C::OFF_V : C::OFF_K);
-    const int P = prm.page_size;
-    const int ppt = C::N / P;
-    const uint32_t box = uint32_t(P) * 128u;
-    auto pages_in = [&](const WorkItem& w, int j) {
-      return (min(C::N, w.tok_end - w.tok_begin - j * C::N) + P - 1) / P;
-    };
-    bool ok = true;
-    int g = 0;
-    auto publish = [&](int n, int value) {
-      if (n >= kItemRing &&
-          !mbar_wait_bounded(smem_u32(&bars.item_empty[n % kItemRing]),
-                             ((n / kItemRing) & 1) ^ 1, limit, &abort_flag))
-        return false;
-      item_ring[n % kItemRing] = value;
-      mbar_arrive(smem_u32(&bars.item_full[n % kItemRing]));   // release: the index is visible
-      return true;
-    };
-    // pair n + 1 (n = -1: the first): warp 10 takes it from the global
-    // counter (the first is blockIdx.x) and publishes it; warp 11 reads it
-    auto next_pair = [&](int n, int& idx) {
-      int v = -1;
-      bool good = true;
+    if (warp >= 10) {
+      // ------------------------------------------------------------ producers
+      const bool is_v = warp == 11;
       if (lane == 0) {
-        if (!is_v) {
-          v = n < 0 ? int(blockIdx.x) : int(gridDim.x + atomicAdd(prm.work_counter, 1u));
-          if (v >= n_pairs) v = -1;
-          good = publish(n + 1, v);
-        } else {
-          good = item_at(n + 1, v);
-          item_done(n + 1);
-        }
+        prefetch_tensormap(is_v ? &v_map : &k_map);
+        if (!is_v) prefetch_tensormap(&q_map);
       }
-      idx = __shfl_sync(0xffffffffu, v, 0);
-      return __shfl_sync(0xffffffffu, good, 0) != 0;
-    };
-    int it = -1;
-    ok = next_pair(-1, it);
-    WorkItem w;
-    if (ok && it >= 0) w = prm.items[2 * it];
-    int next_page = -1;
-    if (ok && it >= 0 && item_tiles<C::N>(w) > 0 && lane < pages_in(w, 0))
-      next_page = prm.page_indices[w.page_begin + lane];
-    for (int n = 0; ok && it >= 0; ++n) {
-      const int nt = item_tiles<C::N>(w);
-      const int kv_head = w.head / prm.group;
-      const int c1 = prm.layout == FI_LAYOUT_NHD ? kv_head : 0;
-      const int c2 = prm.layout == FI_LAYOUT_NHD ? 0 : kv_head;
-      int it_next = -1;
-      if (!next_pair(n, it_next)) {
-        ok = false;
-        break;
-      }
-      WorkItem wn;
-      if (it_next >= 0) wn = prm.items[2 * it_next];
-      if (!is_v) {
-        // Q of both tiles, once both have issued their last S of the previous pair
-        if (n >= 1) {
-          ok = mbar_wait_warp(smem_u32(&bars.q_empty), (n - 1) & 1, limit, &abort_flag);
-          if (!ok) break;
-        }
+      const CUtensorMap* map = is_v ? &v_map : &k_map;
+      uint64_t* full = is_v ? bars.v_full : bars.k_full;
+      uint64_t* empty = is_v ? bars.v_empty : bars.k_empty;
+      const uint32_t ring = base + (is_v ? C::OFF_V : C::OFF_K);
+      const int P = prm.page_size;
+      const int ppt = C::N / P;
+      const uint32_t box = uint32_t(P) * 128u;
+      auto pages_in = [&](const WorkItem& w, int j) {
+        return (min(C::N, w.tok_end - w.tok_begin - j * C::N) + P - 1) / P;
+      };
+      bool ok = true;
+      int g = 0;
+      auto publish = [&](int n, int value) {
+        if (n >= kItemRing &&
+            !mbar_wait_bounded(smem_u32(&bars.item_empty[n % kItemRing]),
+                               ((n / kItemRing) & 1) ^ 1, limit, &abort_flag))
+          return false;
+        item_ring[n % kItemRing] = value;
+        mbar_arrive(smem_u32(&bars.item_full[n % kItemRing]));   // release: the index is visible
+        return true;
+      };
+      // pair n + 1 (n = -1: the first): warp 10 takes it from the global
+      // counter (the first is blockIdx.x) and publishes it; warp 11 reads it
+      auto next_pair = [&](int n, int& idx) {
+        int v = -1;
+        bool good = true;
         if (lane == 0) {
-          const uint32_t qb = smem_u32(&bars.q_full);
-          mbar_arrive_expect_tx(qb, 2 * C::Q_BYTES);
-#pragma unroll
-          for (int i = 0; i < 2; ++i)
-#pragma unroll
-            for (int c = 0; c < C::DBLK; ++c)
-              tma_load_3d(base + C::OFF_Q + i * C::Q_BYTES + c * C::M * 128, &q_map, qb, c * 64,
-                          w.head + i, w.q_row);
+          if (!is_v) {
+            v = n < 0 ? int(blockIdx.x) : int(gridDim.x + atomicAdd(prm.work_counter, 1u));
+            if (v >= n_pairs) v = -1;
+            good = publish(n + 1, v);
+          } else {
+            good = item_at(n + 1, v);
+            item_done(n + 1);
+          }
         }
-        q_loads = n + 1;
-      }
-      for (int j = 0; j < nt; ++j, ++g) {
-        const int st = g % C::NST;
-        const int np = pages_in(w, j);
-        int page = -1;
-        bool valid = false;
-        if (lane < np) {
-          page = next_page;
-          valid = page >= 0 && page < prm.num_pages;
-          if (!valid && !is_v) atomicOr(prm.err, kErrBounds);
-        }
-        if (j + 1 < nt) {
-          if (lane < pages_in(w, j + 1))
-            next_page = prm.page_indices[w.page_begin + (j + 1) * ppt + lane];
-        } else if (it_next >= 0 && item_tiles<C::N>(wn) > 0 && lane < pages_in(wn, 0)) {
-          next_page = prm.page_indices[wn.page_begin + lane];
-        }
-        const uint32_t bytes =
-            uint32_t(__popc(__ballot_sync(0xffffffffu, valid))) * C::DBLK * box;
-        if (g >= C::NST && !mbar_wait_warp(smem_u32(&empty[st]), ((g / C::NST) & 1) ^ 1,
-                                           limit, &abort_flag)) {
+        idx = __shfl_sync(0xffffffffu, v, 0);
+        return __shfl_sync(0xffffffffu, good, 0) != 0;
+      };
+      int it = -1;
+      ok = next_pair(-1, it);
+      WorkItem w;
+      if (ok && it >= 0) w = prm.items[2 * it];
+      int next_page = -1;
+      if (ok && it >= 0 && item_tiles<C::N>(w) > 0 && lane < pages_in(w, 0))
+        next_page = prm.page_indices[w.page_begin + lane];
+      for (int n = 0; ok && it >= 0; ++n) {
+        const int nt = item_tiles<C::N>(w);
+        const int kv_head = w.head / prm.group;
+        const int c1 = prm.layout == FI_LAYOUT_NHD ? kv_head : 0;
+        const int c2 = prm.layout == FI_LAYOUT_NHD ? 0 : kv_head;
+        int it_next = -1;
+        if (!next_pair(n, it_next)) {
           ok = false;
           break;
         }
-        const uint32_t fb = smem_u32(&full[st]);
-        const bool skip = !is_v && g == 0 && prm.fault_kind == 1 && blockIdx.x == 0;
-        if (lane == 0 && !skip) mbar_arrive_expect_tx(fb, bytes);
-        __syncwarp();
-        if (valid && !skip) {
-          const uint32_t dst = ring + st * C::KV_BYTES + lane * box;
-#pragma unroll
-          for (int c = 0; c < C::DBLK; ++c)
-            tma_load_4d(dst + c * C::N * 128, map, fb, c * 64, c1, c2, page);
-        }
-        issued = g + 1;
-      }
-      if (nt == 0 && it_next >= 0 && item_tiles<C::N>(wn) > 0 && lane < pages_in(wn, 0))
-        next_page = prm.page_indices[wn.page_begin + lane];
-      w = wn;
-      it = it_next;
-    }
-    if (!ok && lane == 0) { abort_flag = 1; atomicOr(prm.err, kErrTimeout); }
-    __syncwarp();
-  } else {
-    // ------------------------------------------------------------ MMA issuers
-    const int i = warp - 8;   // this warp's tile
-    if (lane == 0) {
-      // descriptors are linear in the address field (bits 0-13 = addr >> 4),
-      // so each MMA's descriptor is a base plus a compile-time offset
-      const uint64_t qd0 = sdesc_sw128(base + C::OFF_Q + i * C::Q_BYTES, 16, 1024);
-      const uint64_t kd0 = sdesc_sw128(base + C::OFF_K, 16, 1024);
-      const uint64_t vd0 = sdesc_sw128(base + C::OFF_V, C::N * 128, 1024);
-      const uint32_t s_col = tmem + C::col_s(i), o_col = tmem + C::col_o(i);
-      bool ok = true;
-      int g = 0;   // KV tiles of earlier pairs
-      for (int n = 0; ok; ++n) {
-        int it = -1;
-        ok = item_at(n, it);
-        item_done(n);
-        if (!ok || it < 0) break;
-        const int nt = item_tiles<C::N>(prm.items[2 * it]);
-        ok = mbar_wait_bounded(smem_u32(&bars.q_full), n & 1, limit, &abort_flag);
-        for (int j = 0; ok && j < nt; ++j) {
-          const int gq = g + j, st = gq % C::NST;
-          ok = mbar_wait_bounded(smem_u32(&bars.k_full[st]), (gq / C::NST) & 1, limit,
-                                 &abort_flag);
-          // S_i and P_i share columns, and the softmax rescales O_i after S_i
-          // is full: the previous O_i += P_i V completes first
-          if (ok && gq >= 1)
-            ok = mbar_wait_bounded(smem_u32(&bars.pv_done[i]), (gq - 1) & 1, limit,
-                                   &abort_flag);
-          if (!ok) break;
-          tc_fence_after();
-          const uint64_t kd = kd0 + uint64_t((st * C::KV_BYTES) >> 4);
-#pragma unroll
-          for (int k = 0; k < HEAD_DIM / 16; ++k) {
-            const uint64_t a = qd0 + uint64_t(((k >> 2) * C::M * 128 + (k & 3) * 32) >> 4);
-            const uint64_t b = kd + uint64_t(((k >> 2) * C::N * 128 + (k & 3) * 32) >> 4);
-            tc_mma_ss(s_col, a, b, C::IDESC_QK, k > 0 ? 1u : 0u);
+        WorkItem wn;
+        if (it_next >= 0) wn = prm.items[2 * it_next];
+        if (!is_v) {
+          // Q of both tiles, once both have issued their last S of the previous pair
+          if (n >= 1) {
+            ok = mbar_wait_warp(smem_u32(&bars.q_empty), (n - 1) & 1, limit, &abort_flag);
+            if (!ok) break;
           }
-          tc_commit(smem_u32(&bars.s_full[i]));
-          tc_commit(smem_u32(&bars.k_empty[st]));
-          if (j == nt - 1) tc_commit(smem_u32(&bars.q_empty));
-          ok = mbar_wait_bounded(smem_u32(&bars.p_full[i]), gq & 1, limit, &abort_flag);
-          if (ok)
-            ok = mbar_wait_bounded(smem_u32(&bars.v_full[st]), (gq / C::NST) & 1, limit,
-                                   &abort_flag);
-          if (!ok) break;
-          tc_fence_after();
-          const uint64_t vd = vd0 + uint64_t((st * C::KV_BYTES) >> 4);
+          if (lane == 0) {
+            const uint32_t qb = smem_u32(&bars.q_full);
+            mbar_arrive_expect_tx(qb, 2 * C::Q_BYTES);
 #pragma unroll
-          for (int k = 0; k < C::N / 16; ++k) {
-            // MN-major V: 16 tokens per step; the next 64 dims one slice further
-            const uint64_t b = vd + uint64_t((k * 16 * 128) >> 4);
-            tc_mma_ts(o_col, s_col + k * 8, b, C::IDESC_PV, (j > 0 || k > 0) ? 1u : 0u);
+            for (int i = 0; i < 2; ++i)
+#pragma unroll
+              for (int c = 0; c < C::DBLK; ++c)
+                tma_load_3d(base + C::OFF_Q + i * C::Q_BYTES + c * C::M * 128, &q_map, qb, c * 64,
+                            w.head + i, w.q_row);
           }
-          tc_commit(smem_u32(&bars.v_empty[st]));
-          tc_commit(smem_u32(&bars.pv_done[i]));
+          q_loads = n + 1;
         }
-        if (!ok) break;
-        if (nt == 0) tc_commit(smem_u32(&bars.q_empty));
-        tc_commit(smem_u32(&bars.o_final[i]));
-        g += nt;
+        for (int j = 0; j < nt; ++j, ++g) {
+          const int st = g % C::NST;
+          const int np = pages_in(w, j);
+          int page = -1;
+          bool valid = false;
+          if (lane < np) {
+            page = next_page;
+            valid = page >= 0 && page < prm.num_pages;
+            if (!valid && !is_v) atomicOr(prm.err, kErrBounds);
+          }
+          if (j + 1 < nt) {
+            if (lane < pages_in(w, j + 1))
+              next_page = prm.page_indices[w.page_begin + (j + 1) * ppt + lane];
+          } else if (it_next >= 0 && item_tiles<C::N>(wn) > 0 && lane < pages_in(wn, 0)) {
+            next_page = prm.page_indices[wn.page_begin + lane];
+          }
+          const uint32_t bytes =
+              uint32_t(__popc(__ballot_sync(0xffffffffu, valid))) * C::DBLK * box;
+          if (g >= C::NST && !mbar_wait_warp(smem_u32(&empty[st]), ((g / C::NST) & 1) ^ 1,
+                                             limit, &abort_flag)) {
+            ok = false;
+            break;
+          }
+          const uint32_t fb = smem_u32(&full[st]);
+          const bool skip = !is_v && g == 0 && prm.fault_kind == 1 && blockIdx.x == 0;
+          if (lane == 0 && !skip) mbar_arrive_expect_tx(fb, bytes);
+          __syncwarp();
+          if (valid && !skip) {
+            const uint32_t dst = ring + st * C::KV_BYTES + lane * box;
+#pragma unroll
+            for (int c = 0; c < C::DBLK; ++c)
+              tma_load_4d(dst + c * C::N * 128, map, fb, c * 64, c1, c2, page);
+          }
+          issued = g + 1;
+        }
+        if (nt == 0 && it_next >= 0 && item_tiles<C::N>(wn) > 0 && lane < pages_in(wn, 0))
+          next_page = prm.page_indices[wn.page_begin + lane];
+        w = wn;
+        it = it_next;
       }
-      if (!ok) {
-        abort_flag = 1;
-        atomicOr(prm.err, kErrTimeout);
-        // every MMA issued so far completes before the TMEM is released
-        tc_commit(smem_u32(&bars.drain[i]));
-        mbar_wait_bounded(smem_u32(&bars.drain[i]), 0, limit, nullptr);
+      if (!ok && lane == 0) { abort_flag = 1; atomicOr(prm.err, kErrTimeout); }
+      __syncwarp();
+    } else {
+      // ------------------------------------------------------------ MMA issuers
+      const int i = warp - 8;   // this warp's tile
+      if (lane == 0) {
+        // descriptors are linear in the address field (bits 0-13 = addr >> 4),
+        // so each MMA's descriptor is a base plus a compile-time offset
+        const uint64_t qd0 = sdesc_sw128(base + C::OFF_Q + i * C::Q_BYTES, 16, 1024);
+        const uint64_t kd0 = sdesc_sw128(base + C::OFF_K, 16, 1024);
+        const uint64_t vd0 = sdesc_sw128(base + C::OFF_V, C::N * 128, 1024);
+        const uint32_t s_col = tmem + C::col_s(i), o_col = tmem + C::col_o(i);
+        bool ok = true;
+        int g = 0;   // KV tiles of earlier pairs
+        for (int n = 0; ok; ++n) {
+          int it = -1;
+          ok = item_at(n, it);
+          item_done(n);
+          if (!ok || it < 0) break;
+          const int nt = item_tiles<C::N>(prm.items[2 * it]);
+          ok = mbar_wait_bounded(smem_u32(&bars.q_full), n & 1, limit, &abort_flag);
+          for (int j = 0; ok && j < nt; ++j) {
+            const int gq = g + j, st = gq % C::NST;
+            ok = mbar_wait_bounded(smem_u32(&bars.k_full[st]), (gq / C::NST) & 1, limit,
+                                   &abort_flag);
+            // S_i and P_i share columns, and the softmax rescales O_i after S_i
+            // is full: the previous O_i += P_i V completes first
+            if (ok && gq >= 1)
+              ok = mbar_wait_bounded(smem_u32(&bars.pv_done[i]), (gq - 1) & 1, limit,
+                                     &abort_flag);
+            if (!ok) break;
+            tc_fence_after();
+            const uint64_t kd = kd0 + uint64_t((st * C::KV_BYTES) >> 4);
+#pragma unroll
+            for (int k = 0; k < HEAD_DIM / 16; ++k) {
+              const uint64_t a = qd0 + uint64_t(((k >> 2) * C::M * 128 + (k & 3) * 32) >> 4);
+              const uint64_t b = kd + uint64_t(((k >> 2) * C::N * 128 + (k & 3) * 32) >> 4);
+              tc_mma_ss(s_col, a, b, C::IDESC_QK, k > 0 ? 1u : 0u);
+            }
+            tc_commit(smem_u32(&bars.s_full[i]));
+            tc_commit(smem_u32(&bars.k_empty[st]));
+            if (j == nt - 1) tc_commit(smem_u32(&bars.q_empty));
+            ok = mbar_wait_bounded(smem_u32(&bars.p_full[i]), gq & 1, limit, &abort_flag);
+            if (ok)
+              ok = mbar_wait_bounded(smem_u32(&bars.v_full[st]), (gq / C::NST) & 1, limit,
+                                     &abort_flag);
+            if (!ok) break;
+            tc_fence_after();
+            const uint64_t vd = vd0 + uint64_t((st * C::KV_BYTES) >> 4);
+#pragma unroll
+            for (int k = 0; k < C::N / 16; ++k) {
+              // MN-major V: 16 tokens per step; the next 64 dims one slice further
+              const uint64_t b = vd + uint64_t((k * 16 * 128) >> 4);
+              tc_mma_ts(o_col, s_col + k * 8, b, C::IDESC_PV, (j > 0 || k > 0) ? 1u : 0u);
+            }
+            tc_commit(smem_u32(&bars.v_empty[st]));
+            tc_commit(smem_u32(&bars.pv_done[i]));
+          }
+          if (!ok) break;
+          if (nt == 0) tc_commit(smem_u32(&bars.q_empty));
+          tc_commit(smem_u32(&bars.o_final[i]));
+          g += nt;
+        }
+        if (!ok) {
+          abort_flag = 1;
+          atomicOr(prm.err, kErrTimeout);
+          // every MMA issued so far completes before the TMEM is released
+          tc_commit(smem_u32(&bars.drain[i]));
+          mbar_wait_bounded(smem_u32(&bars.drain[i]), 0, limit, nullptr);
+        }
       }
+      __syncwarp();
     }
-    __syncwarp();
-  }
   } else {
     setmaxnreg_inc<C::SOFTMAX_REGS>();
     // ------------------------------------------------------------ softmax + epilogue
