@@ -146,11 +146,13 @@ KERNEL_SOURCES = {
 
 
 def source_digest(kernel):
-    """Hash of the sources a kernel is compiled from."""
+    """Hash of the sources a kernel is compiled from, blind to whitespace
+    (re-indenting a file does not change the kernel its counters describe)."""
+    import re
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "paged_kv_attention_27_gb300", "csrc")
     for f in KERNEL_SOURCES[kernel]:
-        h.update(open(os.path.join(csrc, f), "rb").read())
+        h.update(re.sub(rb"\s+", b"", open(os.path.join(csrc, f), "rb").read()))
     return h.hexdigest()[:16]
 
 
