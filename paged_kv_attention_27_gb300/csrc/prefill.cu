@@ -57,7 +57,10 @@ struct PrefillCfg {
   static constexpr int N = HEAD_DIM <= 128 ? 128 : 64;      // KV tokens per tile
   static constexpr int DBLK = HEAD_DIM / 64;                // 128-byte slices of a row
   static constexpr int THREADS = 224;     // 4 softmax warps, K producer, MMA issuer, V producer
-  static constexpr bool Q_TMEM = HEAD_DIM <= 128;           // Q as a TMEM operand
+  static constexpr bool Q_TMEM = true;                      // Q as a TMEM operand
+  // d = 256 leaves no TMEM columns for P: P of tile g is written over its
+  // S buffer (g & 1), which the MMA issuer then frees after that tile's PV
+  static constexpr bool P_IN_S = HEAD_DIM > 128;
   static constexpr int NST = HEAD_DIM <= 128 ? 3 : 2;       // K (and V) ring depth
   static constexpr int Q_BYTES = DBLK * M * 128;
   static constexpr int KV_BYTES = DBLK * N * 128;           // one K (or V) tile
@@ -73,7 +76,7 @@ struct PrefillCfg {
   static constexpr uint32_t COL_O = 2 * N;                  // [2N, 2N+HEAD_DIM)
   static constexpr uint32_t COL_Q = COL_O + HEAD_DIM;       // HEAD_DIM/2 columns if Q_TMEM
   static constexpr uint32_t COL_P = COL_Q + (Q_TMEM ? HEAD_DIM / 2 : 0);  // N/2 columns
-  static_assert(COL_P + N / 2 <= TMEM_COLS, "TMEM budget");
+  static_assert((P_IN_S ? COL_P : COL_P + N / 2) <= TMEM_COLS, "TMEM budget");
   static_assert(SMEM_BYTES <= 227 * 1024, "shared-memory budget");
   // K-major Q and K; K-major P with MN-major V; A and B of the element type
   static constexpr uint32_t IDESC_QK = idesc_f16kind(M, N, 0, 0, E::kMmaFmt);
@@ -161,7 +164,8 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(smem_u32(&bars.s_full[s]), 1);
-      mbar_init(smem_u32(&bars.s_free[s]), 4);
+      // S buffer free: read by the 4 softmax warps, or (P over S) read by the PV
+      mbar_init(smem_u32(&bars.s_free[s]), C::P_IN_S ? 1 : 4);
     }
     mbar_init(smem_u32(&bars.p_full), 4);
     mbar_init(smem_u32(&bars.pv_done), 1);
@@ -378,11 +382,13 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
             for (int k = 0; k < C::N / 16; ++k) {
               // MN-major V: 16 tokens per step; the next 64 dims one K-tile slice further
               const uint64_t bd = vd + uint64_t((k * 16 * 128) >> 4);
-              tc_mma_ts(tmem + C::COL_O, tmem + C::COL_P + k * 8, bd, C::IDESC_PV,
+              const uint32_t p_col = C::P_IN_S ? C::COL_S + (gp & 1) * C::N : C::COL_P;
+              tc_mma_ts(tmem + C::COL_O, tmem + p_col + k * 8, bd, C::IDESC_PV,
                         (j > 1 || k > 0) ? 1u : 0u);
             }
             tc_commit(smem_u32(&bars.v_empty[st]));
             tc_commit(smem_u32(&bars.pv_done));
+            if (C::P_IN_S) tc_commit(smem_u32(&bars.s_free[gp & 1]));
           }
         }
         if (!ok) break;
@@ -494,7 +500,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
         tmem_wait_ld();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&bars.s_free[st]));
+        if (!C::P_IN_S && lane == 0) mbar_arrive(smem_u32(&bars.s_free[st]));
 
         // Row max of the raw scores (sm_scale >= 0 commutes with max). Eight
         // independent accumulators keep the dependency chains short; the mask
@@ -623,7 +629,8 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
             for (int e = 0; e < 32; ++e)
               rsp2[e & 1] = __fadd2_rn(rsp2[e & 1], make_float2(E::lo(wv[e]), E::hi(wv[e])));
           }
-          tmem_st32(tmem + lane_off + C::COL_P + kb * 32, wv);
+          tmem_st32(tmem + lane_off + (C::P_IN_S ? C::COL_S + st * C::N : C::COL_P) + kb * 32,
+                    wv);
         }
         tmem_wait_st();
         lp += need_mask ? (rsp2[0].x + rsp2[0].y) + (rsp2[1].x + rsp2[1].y) : rs_tile;
