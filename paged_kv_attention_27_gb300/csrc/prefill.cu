@@ -20,9 +20,10 @@
 //     S_j = Q K_j^T into a double-buffered S region of TMEM, then
 //     O += P_{j-1} V_{j-1} into an O region of TMEM, so that the tensor core
 //     computes the next scores while the softmax warps work. The A operands
-//     (Q for head_dim <= 128, and P) are read from TMEM: with both operands
-//     in shared memory an M=128, N=128 MMA alone would use all of the shared
-//     memory bandwidth, which the K/V copies also need;
+//     (Q and P) are read from TMEM: with both operands in shared memory an
+//     M=128, N=128 MMA alone would use all of the shared memory bandwidth,
+//     which the K/V copies also need. At head_dim 256, O and Q leave no
+//     TMEM columns for P, so P is written over the S buffer it came from;
 //   * warps 0-3 (softmax, thread = query row = TMEM lane): copy their Q row
 //     into TMEM per item, then per tile read the S row with tcgen05.ld, apply the
 //     causal mask, keep the running max and sums (online softmax, the
@@ -57,7 +58,6 @@ struct PrefillCfg {
   static constexpr int N = HEAD_DIM <= 128 ? 128 : 64;      // KV tokens per tile
   static constexpr int DBLK = HEAD_DIM / 64;                // 128-byte slices of a row
   static constexpr int THREADS = 224;     // 4 softmax warps, K producer, MMA issuer, V producer
-  static constexpr bool Q_TMEM = true;                      // Q as a TMEM operand
   // d = 256 leaves no TMEM columns for P: P of tile g is written over its
   // S buffer (g & 1), which the MMA issuer then frees after that tile's PV
   static constexpr bool P_IN_S = HEAD_DIM > 128;
@@ -74,8 +74,8 @@ struct PrefillCfg {
   // TMEM columns: two S buffers, O, then (packed 16-bit pairs) Q and P
   static constexpr uint32_t COL_S = 0;                      // [0,N), [N,2N)
   static constexpr uint32_t COL_O = 2 * N;                  // [2N, 2N+HEAD_DIM)
-  static constexpr uint32_t COL_Q = COL_O + HEAD_DIM;       // HEAD_DIM/2 columns if Q_TMEM
-  static constexpr uint32_t COL_P = COL_Q + (Q_TMEM ? HEAD_DIM / 2 : 0);  // N/2 columns
+  static constexpr uint32_t COL_Q = COL_O + HEAD_DIM;       // HEAD_DIM/2 columns
+  static constexpr uint32_t COL_P = COL_Q + HEAD_DIM / 2;   // N/2 columns (unless P_IN_S)
   static_assert((P_IN_S ? COL_P : COL_P + N / 2) <= TMEM_COLS, "TMEM budget");
   static_assert(SMEM_BYTES <= 227 * 1024, "shared-memory budget");
   // K-major Q and K; K-major P with MN-major V; A and B of the element type
@@ -88,7 +88,7 @@ constexpr int kItemRing = 8;   // item indices handed from the K producer to the
 template <int NST>
 struct PrefillBarriers {
   uint64_t item_full[kItemRing], item_empty[kItemRing];
-  uint64_t q_full, q_tmem, q_empty;
+  uint64_t q_full, q_tmem;
   uint64_t k_full[NST], k_empty[NST];
   uint64_t v_full[NST], v_empty[NST];
   uint64_t s_full[2], s_free[2];
@@ -155,7 +155,6 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
     }
     mbar_init(smem_u32(&bars.q_full), 1);
     mbar_init(smem_u32(&bars.q_tmem), 4);
-    mbar_init(smem_u32(&bars.q_empty), 1);
     for (int s = 0; s < C::NST; ++s) {
       mbar_init(smem_u32(&bars.k_full[s]), 1);
       mbar_init(smem_u32(&bars.k_empty[s]), 1);
@@ -264,11 +263,10 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
       WorkItem wn;
       if (it_next >= 0) wn = prm.items[it_next];
       if (!is_v) {
-        // Q of item n, once the buffer is free: its previous contents were
-        // copied into TMEM (head_dim <= 128) or read by the last QK MMA
+        // Q of item n, once the buffer is free: its previous contents have
+        // been copied into TMEM
         if (n >= 1) {
-          ok = mbar_wait_warp(smem_u32(C::Q_TMEM ? &bars.q_tmem : &bars.q_empty),
-                              (n - 1) & 1, limit, &abort_flag);
+          ok = mbar_wait_warp(smem_u32(&bars.q_tmem), (n - 1) & 1, limit, &abort_flag);
           if (!ok) break;
         }
         if (lane == 0) {
@@ -327,10 +325,8 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
   } else if (warp == 5) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      const uint32_t q_base = base + C::OFF_Q;
       // descriptors are linear in the address field (bits 0-13 = addr >> 4),
       // so each MMA's descriptor is a base plus a compile-time offset
-      const uint64_t qd0 = sdesc_sw128(q_base, 16, 1024);
       const uint64_t kd0 = sdesc_sw128(base + C::OFF_K, 16, 1024);
       const uint64_t vd0 = sdesc_sw128(base + C::OFF_V, C::N * 128, 1024);
       bool ok = true;
@@ -341,8 +337,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
         item_done(n);
         if (!ok || it < 0) break;
         const int nt = item_tiles<C::N>(prm.items[it]);
-        ok = C::Q_TMEM ? mbar_wait_bounded(smem_u32(&bars.q_tmem), n & 1, limit, &abort_flag)
-                       : mbar_wait_bounded(smem_u32(&bars.q_full), n & 1, limit, &abort_flag);
+        ok = mbar_wait_bounded(smem_u32(&bars.q_tmem), n & 1, limit, &abort_flag);
         for (int j = 0; ok && j <= nt; ++j) {
           if (j < nt) {
             const int gq = g + j, st = gq % C::NST, sb = gq & 1;
@@ -358,16 +353,10 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
 #pragma unroll
             for (int k = 0; k < HEAD_DIM / 16; ++k) {
               const uint64_t bd = kd + uint64_t(((k >> 2) * C::N * 128 + (k & 3) * 32) >> 4);
-              if constexpr (C::Q_TMEM) {
-                tc_mma_ts(s_col, tmem + C::COL_Q + k * 8, bd, C::IDESC_QK, k > 0 ? 1u : 0u);
-              } else {
-                const uint64_t a = qd0 + uint64_t(((k >> 2) * C::M * 128 + (k & 3) * 32) >> 4);
-                tc_mma_ss(s_col, a, bd, C::IDESC_QK, k > 0 ? 1u : 0u);
-              }
+              tc_mma_ts(s_col, tmem + C::COL_Q + k * 8, bd, C::IDESC_QK, k > 0 ? 1u : 0u);
             }
             tc_commit(smem_u32(&bars.s_full[sb]));
             tc_commit(smem_u32(&bars.k_empty[st]));
-            if (!C::Q_TMEM && j == nt - 1) tc_commit(smem_u32(&bars.q_empty));
           }
           if (j >= 1) {
             const int gp = g + j - 1, st = gp % C::NST;
@@ -392,7 +381,6 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
           }
         }
         if (!ok) break;
-        if (!C::Q_TMEM && nt == 0) tc_commit(smem_u32(&bars.q_empty));
         tc_commit(smem_u32(&bars.o_final));
         g += nt;
       }
@@ -472,7 +460,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
     if (ok && it >= 0) {
       w = prm.items[it];
       rb = bounds_of(w);
-      if constexpr (C::Q_TMEM) ok = copy_q(0);
+      ok = copy_q(0);
     }
     for (int n = 0; ok && it >= 0; ++n) {
       const int nt = item_tiles<C::N>(w);
@@ -645,7 +633,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
       // computes the next item's first scores while this item's last PV
       // and epilogue finish. (Copying it inside the tile loop instead, right
       // after the last S read, made the loop measurably slower.)
-      if (C::Q_TMEM && has_next && !copy_q(n + 1)) {
+      if (has_next && !copy_q(n + 1)) {
         ok = false;
         break;
       }
