@@ -265,8 +265,8 @@ fi_status fi_batch_decode_paged(fi_plan_t plan, const void* q, const void* k_cac
  * argument, for callers that cannot allocate device memory where they run
  * attention (an engine plugin whose framework owns all device memory and
  * exposes no scratch allocator; a latency-critical loop where a cudaMalloc,
- * which can synchronise the device, is not acceptable). The paper has no
- * counterpart to this call; it is an interface convenience.
+ * which can synchronise the device, is not acceptable). None of the cited
+ * pages has a counterpart to this call; it is an interface convenience.
  * The scratch (work list, error word, fp32 split partials) is a 16 MiB
  * array inside the library, held by every GPU that loads the library until
  * the process exits. This call allocates nothing itself.
