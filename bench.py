@@ -74,6 +74,7 @@ WORKLOADS = {
     "causal_prefill_1k": ("causal_prefill", {"seq_len": 1024}),
     "causal_prefill_4k": ("causal_prefill", {"seq_len": 4096}),
     "causal_prefill_16k": ("causal_prefill", {"seq_len": 16384}),
+    "causal_prefill_32k": ("causal_prefill", {"seq_len": 32768, "batch": 2}),
     "causal_prefill_16k_window4k": ("causal_prefill", {"seq_len": 16384, "window_left": 4095}),
     "causal_prefill_4k_fp16": ("causal_prefill", {"seq_len": 4096, "dtype": "fp16"}),
     "llama7b_decode_fp16": ("llama7b_decode", {"dtype": "fp16"}),

@@ -196,6 +196,11 @@ def test_causal_prefill_70b_full_size(L):
     check_sampled(synth.causal_prefill(L), per_request=16 if L > 4096 else 24)
 
 
+def test_causal_prefill_32k_sampled():
+    # two 32K-token requests: 256 query tiles each, up to 256 KV tiles per item
+    check_sampled(synth.causal_prefill(32768, batch=2), per_request=12)
+
+
 def test_ragged_prefill_full_size():
     check_sampled(synth.ragged_prefill(), per_request=16)
 
