@@ -394,7 +394,8 @@ const char* fi_last_error_string(void);
  * prefill: its K producer) skips its first tile load, so that the waiting
  * warps' bounded waits run out after about `wait_limit` nanoseconds and the
  * kernel reports FI_ERR_DEVICE_TIMEOUT instead of hanging. wait_limit <= 0
- * restores the default bound. Not thread-safe; meant for tests only.
+ * restores the default bound. Process-wide: the next run call on any thread
+ * takes the fault (once). Meant for tests only.
  */
 fi_status fi_debug_set_fault(int32_t kind, int64_t wait_limit);
 

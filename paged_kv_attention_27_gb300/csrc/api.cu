@@ -5,6 +5,7 @@
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cstring>
 #include <mutex>
 #include <new>
@@ -16,8 +17,9 @@
 namespace {
 
 thread_local std::string g_last_error;
-int32_t g_fault_kind = 0;
-uint64_t g_wait_limit_ns = fi::kDefaultWaitLimitNs;
+// test hook state, process-wide (fi_debug_set_fault may run on any thread)
+std::atomic<int32_t> g_fault_kind{0};
+std::atomic<uint64_t> g_wait_limit_ns{fi::kDefaultWaitLimitNs};
 thread_local cudaEvent_t g_prof_start = nullptr, g_prof_stop = nullptr;
 
 fi_status cuda_fail(cudaError_t e, const char* what) {
@@ -344,8 +346,8 @@ fi_status run_paged(fi_plan_t plan, bool prefill_call, const void* q, const int3
 
   cudaEvent_t prof_start = g_prof_start, prof_stop = g_prof_stop;
   g_prof_start = g_prof_stop = nullptr;
-  const int32_t fault_kind = g_fault_kind;
-  g_fault_kind = 0;  // one-shot
+  const int32_t fault_kind = g_fault_kind.exchange(0);  // one-shot
+  const uint64_t wait_limit_ns = g_wait_limit_ns.load();
   if (prof_start) {
     e = cudaEventRecord(prof_start, stream);
     if (e != cudaSuccess) return cuda_fail(e, "profiling event");
@@ -388,7 +390,7 @@ fi_status run_paged(fi_plan_t plan, bool prefill_call, const void* q, const int3
     pp.out = out;
     pp.lse = lse;
     pp.err = err;
-    pp.wait_limit_ns = g_wait_limit_ns;
+    pp.wait_limit_ns = wait_limit_ns;
     pp.fault_kind = fault_kind;
     pp.n_items = int(P.prefill_items.size());
     pp.work_counter = reinterpret_cast<uint32_t*>(ws + fi::kWorkCounterOffset);
@@ -425,7 +427,7 @@ fi_status run_paged(fi_plan_t plan, bool prefill_call, const void* q, const int3
     pp.state_o = partial_o;
     pp.state_lse = partial_lse;
     pp.err = err;
-    pp.wait_limit_ns = g_wait_limit_ns;
+    pp.wait_limit_ns = wait_limit_ns;
     pp.fault_kind = 0;
     pp.n_items = int(P.prefix_items.size());
     pp.work_counter = reinterpret_cast<uint32_t*>(ws + fi::kWorkCounterOffset);
@@ -450,7 +452,7 @@ fi_status run_paged(fi_plan_t plan, bool prefill_call, const void* q, const int3
     dp.merges = reinterpret_cast<const fi::MergeTask*>(ws + P.ws.merges);
     dp.merge_counters = reinterpret_cast<uint32_t*>(ws + P.ws.merge_counters);
     dp.err = err;
-    dp.wait_limit_ns = g_wait_limit_ns;
+    dp.wait_limit_ns = wait_limit_ns;
     dp.fault_kind = fault_kind;
     e = fi::launch_decode(P.head_dim, P.num_qo_heads / P.num_kv_heads, P.dtype, P.kv_dtype, kmap,
                           vmap, dp,
@@ -702,8 +704,8 @@ fi_status fi_profile_next_launch(void* start_event, void* stop_event) {
 
 fi_status fi_debug_set_fault(int32_t kind, int64_t wait_limit) {
   if (kind < 0 || kind > 1) return FI_ERR_INVALID_ARG;
-  g_fault_kind = kind;
-  g_wait_limit_ns = wait_limit > 0 ? uint64_t(wait_limit) : fi::kDefaultWaitLimitNs;
+  g_wait_limit_ns.store(wait_limit > 0 ? uint64_t(wait_limit) : fi::kDefaultWaitLimitNs);
+  g_fault_kind.store(kind);
   return FI_OK;
 }
 
