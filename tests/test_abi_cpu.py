@@ -269,6 +269,23 @@ def test_valid_edge_plans():
     assert info["total_kv_tokens"] == 3 and info["num_decode_items"] == 4
 
 
+def test_longest_request_plans_and_one_page_more_is_rejected():
+    # a request may hold up to INT32_MAX / 2 keys (key positions and their
+    # sums stay in int32 on the device); the split covers it with bounded
+    # work lists
+    npg = (2**31 - 1) // 2 // 16
+    p = B.fi_plan(B.FI_MODE_DECODE, 1, None, [0, npg], [15], 8, 2, 128, 16, 0, None, 152)
+    info = B.fi_plan_get_info(p)
+    assert info["total_kv_tokens"] == (npg - 1) * 16 + 15
+    assert info["num_split_requests"] == 1
+    assert info["num_decode_items"] <= 4 * 152 * 2       # a few waves, not one per page
+    chunks = info["num_decode_items"] // 2                 # items: (chunk, kv head), 2 kv heads
+    assert info["chunk_tokens"] * chunks >= info["total_kv_tokens"]
+    with pytest.raises(B.FiError) as e:
+        B.fi_plan(B.FI_MODE_DECODE, 1, None, [0, npg + 1], [16], 8, 2, 128, 16, 0, None, 152)
+    assert e.value.status == B.FI_ERR_INVALID_ARG
+
+
 def test_workspace_too_small_and_bad_args_return_before_any_launch():
     """Host-side checks happen before the device is touched; on a machine
     without a GPU, a well-formed call reports that there is no device."""
