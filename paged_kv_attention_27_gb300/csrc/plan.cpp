@@ -219,7 +219,10 @@ fi_status build_plan(int32_t mode, int32_t batch, const int32_t* qo_indptr,
       if (x.len != y.len) return x.len > y.len;
       return x.b != y.b ? x.b < y.b : x.c < y.c;
     });
-    p.decode_items.reserve(groups.size() * size_t(num_kv_heads));
+    // sized once and written through a pointer (a push_back per item cost
+    // more than the rest of the plan together)
+    p.decode_items.resize(groups.size() * size_t(num_kv_heads));
+    WorkItem* dst = p.decode_items.data();
     for (const Group& g : groups) {
       const int b = g.b;
       const int64_t t0 = s0s[b] + int64_t(g.c) * chunk;   // page-aligned start of the chunk
@@ -235,7 +238,7 @@ fi_status build_plan(int32_t mode, int32_t batch, const int32_t* qo_indptr,
       w.merge = merge_of[b];
       for (int kh = 0; kh < num_kv_heads; ++kh) {
         w.head = kh;
-        p.decode_items.push_back(w);
+        *dst++ = w;
       }
     }
   }
@@ -266,7 +269,8 @@ fi_status build_plan(int32_t mode, int32_t batch, const int32_t* qo_indptr,
     }
     std::stable_sort(ptiles.begin(), ptiles.end(),
                      [](const PTile& x, const PTile& y) { return x.len > y.len; });
-    p.prefix_items.reserve(ptiles.size() * size_t(num_kv_heads));
+    p.prefix_items.resize(ptiles.size() * size_t(num_kv_heads));
+    WorkItem* dst = p.prefix_items.data();
     for (const PTile& t : ptiles) {
       const int64_t k0 = int64_t(t.c) * pchunk[t.g];
       WorkItem w;
@@ -281,7 +285,7 @@ fi_status build_plan(int32_t mode, int32_t batch, const int32_t* qo_indptr,
       w.merge = -1;
       for (int kh = 0; kh < num_kv_heads; ++kh) {
         w.head = kh;
-        p.prefix_items.push_back(w);
+        *dst++ = w;
       }
     }
   }
@@ -310,7 +314,8 @@ fi_status build_plan(int32_t mode, int32_t batch, const int32_t* qo_indptr,
     if (x.len != y.len) return x.len > y.len;
     return x.b != y.b ? x.b < y.b : x.qt < y.qt;
   });
-  p.prefill_items.reserve(tiles.size() * size_t(num_qo_heads));
+  p.prefill_items.resize(tiles.size() * size_t(num_qo_heads));
+  WorkItem* pdst = p.prefill_items.data();
   for (const Tile& t : tiles) {
     WorkItem w;
     w.req = t.b;
@@ -323,7 +328,7 @@ fi_status build_plan(int32_t mode, int32_t batch, const int32_t* qo_indptr,
     w.merge = -1;
     for (int h = 0; h < num_qo_heads; ++h) {
       w.head = h;
-      p.prefill_items.push_back(w);
+      *pdst++ = w;
     }
   }
 
