@@ -147,13 +147,18 @@ KERNEL_SOURCES = {
 
 
 def source_digest(kernel):
-    """Hash of the sources a kernel is compiled from, blind to whitespace
-    (re-indenting a file does not change the kernel its counters describe)."""
+    """Hash of the sources a kernel is compiled from, blind to comments and
+    whitespace (re-indenting a file or rewording a comment does not change the
+    kernel its counters describe; the hashed files hold no comment markers
+    inside string literals)."""
     import re
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "paged_kv_attention_27_gb300", "csrc")
     for f in KERNEL_SOURCES[kernel]:
-        h.update(re.sub(rb"\s+", b"", open(os.path.join(csrc, f), "rb").read()))
+        src = open(os.path.join(csrc, f), "rb").read()
+        src = re.sub(rb"/\*.*?\*/", b"", src, flags=re.S)
+        src = re.sub(rb"//[^\n]*", b"", src)
+        h.update(re.sub(rb"\s+", b"", src))
     return h.hexdigest()[:16]
 
 
