@@ -5,19 +5,24 @@
 // sharing). Work is HBM-bound (about 1 flop per KV byte for g = 1), so the
 // design is about moving bytes:
 //   * a producer warp walks the page table and issues one TMA box per
-//     (page, 64-dim slice) for K and for V, into a 3-stage shared-memory
-//     ring (32 KB of K+V per stage) completed on mbarriers — no register
-//     staging, as "FlashAttention-3 kernel integration in inference
-//     engines", section 1 describes for TMA;
+//     (page, 64-dim slice) for K and for V, into a shared-memory ring
+//     completed on mbarriers (three 32 KB stages of K+V for the SIMT
+//     consumer, two per CTA and three CTAs per SM for the tensor-core one)
+//     with no register staging, as "FlashAttention-3 kernel integration in
+//     inference engines", section 1 describes for TMA;
 //   * 4 consumer warps read the staged rows (128-byte-swizzled, so reads
-//     are bank-conflict free), compute scores with warp-shuffle reductions
-//     ("FlashInfer Attention Kernel optimisation analysis", sections 1.3 and
-//     2.1: warp-level reductions via __shfl_sync, no global sync) and keep a
-//     running max / sum / accumulator (the online softmax of section 1 of the
-//     FlashAttention-3 page), rescaling whenever the max grows;
+//     are bank-conflict free) and keep a running max / sum / accumulator
+//     (the online softmax of section 1 of the FlashAttention-3 page),
+//     rescaling when the max grows. With four or eight heads per kv head,
+//     or an FP8 cache, at head_dim <= 128 they compute with m16n8k16 MMAs
+//     that take the tokens as rows and the heads as columns; otherwise with
+//     warp-shuffle reductions ("FlashInfer Attention Kernel optimisation
+//     analysis", sections 1.3 and 2.1: warp-level reductions via
+//     __shfl_sync, no global sync);
 //   * the warps' states are merged in shared memory; the CTA writes either
-//     the final row (bf16 or fp16, the inputs' type) + lse, or an fp32 partial state that the merge
-//     kernel combines by log-sum-exp.
+//     the final row (bf16 or fp16, the inputs' type) + lse, or an fp32
+//     partial state, and the CTA that completes a split request's last
+//     chunk combines its partial states by log-sum-exp (no second launch).
 // Scores are kept in the log2 domain (q pre-scaled by sm_scale*log2(e)).
 #include <type_traits>
 
