@@ -177,8 +177,13 @@ typedef struct {
  * Errors: FI_ERR_INVALID_ARG (NULL pointers, negative sizes, decreasing
  * indptr, last_page_len outside [1,page_size] for a request with pages,
  * causal with qo_len > kv_len, num_qo_heads not a multiple of
- * num_kv_heads, window_left < -1, dtype not an fi_dtype),
- * FI_ERR_UNSUPPORTED (head_dim, page_size or g not built).
+ * num_kv_heads, window_left < -1, dtype not an fi_dtype, a request of more
+ * than INT32_MAX / 2 keys, more than INT32_MAX query rows in all, shared-
+ * prefix groups out of order or whose prefix is not made of full pages of
+ * every request in the group),
+ * FI_ERR_UNSUPPORTED (head_dim, page_size or g not built; an FP8 cache in a
+ * prefill plan; shared prefixes with an FP8 cache, a window or a prefill
+ * plan).
  */
 fi_status fi_plan(int32_t mode, int32_t batch_size, const int32_t* qo_indptr_h,
                   const int32_t* page_indptr_h, const int32_t* last_page_len_h,
