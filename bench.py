@@ -456,6 +456,9 @@ def run_ours(args, rank, world, local_rank):
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(b)
 
+    from paged_kv_attention_27_gb300.device import num_sms
+    plan_host = time_plan(b, num_sms(f"cuda:{local_rank}"))
+
     sampler = ClockSampler(local_rank)
     sampler.start()
     time.sleep(0.3)
@@ -492,6 +495,7 @@ def run_ours(args, rank, world, local_rank):
         "cpu_baseline": cpu,
         "e2e": e2e,
         "gpu_launches": launches_per_step * K,
+        "plan_host_us": plan_host,
         "clocks": sampler.summary(),
     }
     if secondary:
@@ -573,6 +577,33 @@ def oracle_rows_sample(b, budget_s=12.0):
                 nxt += 1
     dt = time.perf_counter() - t0
     return done_flops / dt / 1e12, dt, threads, n
+
+
+def time_plan(b, sms, calls=200):
+    """Host time of fi_plan for the batch (the planner runs on the CPU, off
+    the GPU timeline, before every step of a serving loop): median over
+    `calls` plans, with the work-item count it produced."""
+    import numpy as np
+
+    from paged_kv_attention_27_gb300 import binding as B
+    from paged_kv_attention_27_gb300.device import plan_options
+
+    decode = b.is_decode and not b.causal     # the mode DeviceBatch plans with
+    mode = B.FI_MODE_DECODE if decode else B.FI_MODE_PREFILL
+    args = (mode, b.batch, None if decode else b.qo_indptr.astype(np.int32),
+            b.page_indptr.astype(np.int32), b.last_page_len.astype(np.int32),
+            b.num_qo_heads, b.num_kv_heads, b.head_dim, b.page_size, b.causal,
+            plan_options(b), sms)
+    for _ in range(5):
+        B.fi_plan(*args)
+    ts = []
+    for _ in range(calls):
+        t0 = time.perf_counter()
+        p = B.fi_plan(*args)
+        ts.append(time.perf_counter() - t0)
+    return {"median_us": float(np.median(ts)) * 1e6, "calls": calls,
+            "items": B.fi_plan_get_info(p)["num_items"],
+            "includes": "fi_plan through the Python binding, host only"}
 
 
 def run_e2e(b, db, K, local_rank, unit):
