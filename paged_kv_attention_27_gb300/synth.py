@@ -372,6 +372,15 @@ def small_mixed(seed: int = 6) -> PagedBatch:
                       kv, qo, 16, 8, 256, 32, NHD, None, True, seed)
 
 
+def small_gqa_prefill(seed: int = 17) -> PagedBatch:
+    """Causal prefill with the 70B head ratio (8 query heads per kv head,
+    d = 128, P = 16) at a size the oracle finishes in seconds: three requests
+    of 255, 64 and 390 tokens (ragged row tiles, one shorter than a tile)."""
+    kv = [255, 64, 390]
+    return make_batch("small causal prefill Hq16 Hkv2 d128 P16 NHD", kv, kv, 16, 2, 128, 16,
+                      NHD, None, True, seed)
+
+
 def sub_batch(src: PagedBatch, requests) -> PagedBatch:
     """Copy the listed requests of ``src`` into a compact batch of their own
     (pages renumbered densely, order kept). Used to draw bounded samples."""
