@@ -462,3 +462,67 @@ def test_host_buffer_call_sizes_its_region_and_checks_before_any_copy():
     with pytest.raises(B.FiError) as e:
         B.fi_batch_attention_host(*args, stream=0)
     assert e.value.status == B.FI_ERR_NO_DEVICE
+
+
+def _check_prefill_cover(b, plan):
+    """Each (request, query head, row) of a multi-row request in exactly one
+    prefill item, whose page-aligned key range holds every key its rows may
+    see: from the page of its first row's first visible key to the causal
+    bound of its last row (or the end of the keys)."""
+    info = B.fi_plan_get_info(plan)
+    pre = B.fi_plan_get_work(plan)[info["num_decode_items"]:][:info["num_prefill_items"]]
+    P, w = b.page_size, b.window_left
+    rows = {}
+    for req, h, pb, npg, t0, t1, slot, qrow in pre.tolist():
+        qo_len, kv_len = int(b.qo_lens[req]), int(b.kv_lens[req])
+        r0 = qrow - int(b.qo_indptr[req])
+        r_last = min(qo_len, r0 + 128) - 1
+        end = min(kv_len, kv_len - qo_len + r_last + 1) if b.causal else kv_len
+        first = 0 if w < 0 else max(0, kv_len - qo_len + r0 - w)
+        assert t1 == end and slot == -1 and 0 <= h < b.num_qo_heads
+        assert t0 % P == 0 and t0 <= min(first, end) < t0 + P or t0 == t1
+        assert pb == b.page_indptr[req] + t0 // P and npg == -(-(t1 - t0) // P)
+        assert pb + npg <= b.page_indptr[req + 1]
+        for r in range(r0, r_last + 1):
+            rows[(req, h, r)] = rows.get((req, h, r), 0) + 1
+    want = {(r, h, i) for r in range(b.batch) if b.qo_lens[r] >= 2
+            for h in range(b.num_qo_heads) for i in range(int(b.qo_lens[r]))}
+    assert set(rows) == want and all(c == 1 for c in rows.values())
+    lens = pre[:, 5] - pre[:, 4]
+    assert np.all(np.diff(lens) <= 0)                 # longest first
+    if b.num_qo_heads % 2 == 0:
+        # items 2p and 2p + 1: heads h, h + 1 of one tile (the two-tile kernel's pairs)
+        assert np.all(pre[0::2, 1] % 2 == 0) and np.all(pre[0::2, 1] + 1 == pre[1::2, 1])
+        same = [0, 2, 3, 4, 5, 6, 7]                   # every field but the head
+        assert np.array_equal(pre[0::2][:, same], pre[1::2][:, same])
+
+
+@pytest.mark.parametrize("seed", range(40))
+def test_random_plans_cover_every_visible_key_once(seed):
+    """Seeded random page tables (empty requests, lengths on and off page
+    boundaries, decode rows mixed into prefill batches, left windows, 1 to
+    300 SMs) against the coverage rules of the decode and prefill work."""
+    g = np.random.default_rng(1000 + seed)
+    P = int(g.choice([16, 32]))
+    hkv = int(g.choice([1, 2, 4]))
+    hq = hkv * int(g.choice([1, 2, 4, 8]))
+    batch = int(g.integers(1, 12))
+    kv = g.integers(0, 2500, size=batch)
+    kv[g.random(batch) < 0.2] = 0
+    edge = g.random(batch) < 0.3
+    kv[edge] = (g.integers(1, 40, size=int(edge.sum())) * P + g.choice([-1, 0, 1])).clip(0)
+    prefill = bool(g.random() < 0.6)
+    if prefill:
+        qo = np.where(g.random(batch) < 0.3, 1, g.integers(1, 400, size=batch))
+        qo = np.minimum(qo, np.maximum(kv, 1))
+        qo[kv == 0] = 0                               # causal plans need qo_len <= kv_len
+    else:
+        qo = np.ones(batch, np.int64)
+    b = _table_only(kv, hq, hkv, 128, P, qo)
+    b.causal = prefill and bool(g.random() < 0.8)
+    b.window_left = int(g.choice([-1, -1, 0, 1, P - 1, P, 100, 1000]))
+    sms = int(g.integers(1, 300))
+    plan = _plan(b, B.FI_MODE_PREFILL if prefill else B.FI_MODE_DECODE, sms=sms)
+    _check_decode_cover(b, plan)
+    if prefill:
+        _check_prefill_cover(b, plan)
