@@ -336,48 +336,84 @@ def test_workspace_too_small_and_bad_args_return_before_any_launch():
     assert e.value.status == B.FI_ERR_INVALID_ARG
 
 
-def test_shared_prefix_plan_covers_prefix_and_suffixes():
+def _check_prefix_cover(b, gi, pages, sms):
     """Shared-prefix decode: the prefix items cover every (row of a group,
-    head, prefix key) once; the decode items cover each grouped request's
-    keys after the prefix once (the rest as usual); every grouped request has
-    a merge task."""
+    query head, prefix key) once; the decode items cover each grouped
+    request's keys after the prefix once (the rest as usual); every grouped
+    request goes through a merge. Returns the number of prefix chunks of the
+    longest group."""
+    P, hq, hkv = b.page_size, b.num_qo_heads, b.num_kv_heads
+    g = hq // hkv
+    rows_per_tile = 128 // g                       # a tile packs the g heads of a kv head
+    G = len(gi) - 1
+    p = B.fi_plan(B.FI_MODE_DECODE, b.batch, None, b.page_indptr, b.last_page_len, hq, hkv,
+                  b.head_dim, P, 0, {"prefix_group_indptr": gi, "prefix_pages": pages}, sms)
+    info = B.fi_plan_get_info(p)
+    work = B.fi_plan_get_work(p)
+    nd = info["num_decode_items"]
+    assert info["num_prefix_groups"] == G
+    dec, pre = work[:nd], work[nd:]
+    # counts[r, h, t]: row r of q (a grouped request), query head h, prefix key t
+    counts = {grp: np.zeros((gi[grp + 1] - gi[grp], hq, pages[grp] * P), np.int32)
+              for grp in range(G)}
+    chunks = {}
+    for req, kh, pb, npg, t0, t1, slot, qrow in pre.tolist():
+        grp = req // 2
+        assert req % 2 == 0 and pb == b.page_indptr[gi[grp]] + t0 // P
+        assert 0 <= t0 < t1 <= pages[grp] * P and t0 % 128 == 0
+        assert npg == -(-(t1 - t0) // P)
+        r0 = qrow - gi[grp]
+        counts[grp][r0:r0 + rows_per_tile, kh * g:(kh + 1) * g, t0:t1] += 1
+        chunks.setdefault(grp, set()).add(t0)
+    for grp in range(G):
+        assert np.all(counts[grp] == 1)
+    prefix = {r: pages[grp] * P for grp in range(G) for r in range(gi[grp], gi[grp + 1])}
+    cover = [np.zeros((hkv, int(k)), np.int32) for k in b.kv_lens]
+    for req, kh, pb, npg, t0, t1, slot, qrow in dec.tolist():
+        assert t0 >= prefix.get(req, 0)
+        if req in prefix:
+            assert slot >= 0            # grouped rows always go through a merge
+        cover[req][kh, t0:t1] += 1
+    for r in range(b.batch):
+        k0 = prefix.get(r, 0)
+        assert np.all(cover[r][:, :k0] == 0) and np.all(cover[r][:, k0:] == 1)
+    return max((len(c) for c in chunks.values()), default=0)
+
+
+def test_shared_prefix_plan_covers_prefix_and_suffixes():
     kv = [100, 48, 300, 5000, 64, 17, 900]
     b = _table_only(kv, 16, 2, 128, 16)
-    gi, pages = [0, 3, 3, 5], [3, 0, 4]            # group 1 is empty
-    pages[1] = 1
-    opts = {"prefix_group_indptr": gi, "prefix_pages": pages}
+    gi, pages = [0, 3, 3, 5], [3, 1, 4]            # group 1 is empty
     for sms in (4, 152):
-        p = B.fi_plan(B.FI_MODE_DECODE, b.batch, None, b.page_indptr, b.last_page_len, 16, 2, 128,
-                      16, 0, opts, sms)
-        info = B.fi_plan_get_info(p)
-        work = B.fi_plan_get_work(p)
-        nd, npf = info["num_decode_items"], info["num_prefix_items"]
-        assert info["num_prefix_groups"] == 3 and npf > 0
-        dec, pre = work[:nd], work[nd:]
-        seen = {}
-        for req, kh, pb, npg, t0, t1, slot, qrow in pre.tolist():
-            g = req // 2
-            first = gi[g]
-            assert req % 2 == 0 and pb == b.page_indptr[first] + t0 // 16
-            assert 0 <= t0 < t1 <= pages[g] * 16 and t0 % 128 == 0
-            for r in range(qrow, min(qrow + 128 // 8, gi[g + 1])):   # 16 rows x 8 heads
-                for h in range(kh * 8, kh * 8 + 8):
-                    for t in range(t0, t1):
-                        seen[(r, h, t)] = seen.get((r, h, t), 0) + 1
-        want = {(r, h, t) for g in range(3) for r in range(gi[g], gi[g + 1]) for h in range(16)
-                for t in range(pages[g] * 16)}
-        assert set(seen) == want and all(c == 1 for c in seen.values())
-        prefix = {r: pages[g] * 16 for g in range(3) for r in range(gi[g], gi[g + 1])}
-        cover = {}
-        for req, kh, pb, npg, t0, t1, slot, qrow in dec.tolist():
-            assert t0 >= prefix.get(req, 0)
-            if req in prefix:
-                assert slot >= 0            # grouped rows always go through a merge
-            for t in range(t0, t1):
-                cover[(req, kh, t)] = cover.get((req, kh, t), 0) + 1
-        want = {(r, kh, t) for r in range(b.batch) for kh in range(2)
-                for t in range(prefix.get(r, 0), kv[r])}
-        assert set(cover) == want and all(c == 1 for c in cover.values())
+        _check_prefix_cover(b, gi, pages, sms)
+
+
+@pytest.mark.parametrize("seed", range(20))
+def test_random_shared_prefix_plans(seed):
+    """Seeded random groups of consecutive requests (some empty), prefixes
+    of whole shared pages, every supported group size, 1 to 300 SMs."""
+    rng = np.random.default_rng(2000 + seed)
+    P = int(rng.choice([16, 32]))
+    hkv = int(rng.choice([1, 2]))
+    hq = hkv * int(rng.choice([1, 2, 4, 8]))
+    batch = int(rng.integers(2, 10))
+    cuts = np.sort(rng.choice(np.arange(batch + 1), size=int(rng.integers(2, 5)), replace=True))
+    gi = [int(x) for x in cuts]
+    # short prefixes (one chunk) and long ones (cut into several chunks)
+    pages = [int(rng.integers(1, 12)) if rng.random() < 0.5 else int(rng.integers(64, 400))
+             for _ in range(len(gi) - 1)]
+    kv = rng.integers(0, 1500, size=batch)
+    for grp in range(len(gi) - 1):                 # grouped requests hold the prefix pages
+        for r in range(gi[grp], gi[grp + 1]):
+            kv[r] = pages[grp] * P + int(rng.choice([0, 1, int(rng.integers(1, 600))]))
+    b = _table_only(kv, hq, hkv, 128, P)
+    _check_prefix_cover(b, gi, pages, int(rng.integers(1, 300)))
+
+
+def test_long_shared_prefix_is_cut_into_chunks():
+    kv = [9000, 8200, 8193, 5000]
+    b = _table_only(kv, 8, 1, 128, 16)
+    assert _check_prefix_cover(b, [0, 3], [512], 152) > 1
 
 
 @pytest.mark.parametrize("case,status", [
