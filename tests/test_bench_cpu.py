@@ -26,3 +26,44 @@ def test_plan_timing_of_a_prefill_batch_uses_a_prefill_plan():
     t = bench.time_plan(b, 152, calls=5)
     # 8 row tiles of 128 x 64 query heads
     assert t["items"] == 8 * 64
+
+
+def _brute_pairs(b):
+    total = 0
+    for qo, kv in zip(b.qo_lens.tolist(), b.kv_lens.tolist()):
+        for i in range(qo):
+            pos = kv - qo + i
+            for t in range(kv):
+                if b.causal and t > pos:
+                    continue
+                if b.window_left >= 0 and t < pos - b.window_left:
+                    continue
+                total += 1
+    return total
+
+
+@pytest.mark.parametrize("seed", range(8))
+def test_visible_pairs_count_the_mask(seed):
+    import numpy as np
+    g = np.random.default_rng(seed)
+    kv = g.integers(0, 90, size=5)
+    qo = np.minimum(g.integers(1, 40, size=5), np.maximum(kv, 1))
+    qo[kv == 0] = 0
+    causal = bool(seed % 2)
+    b = synth.make_batch("pairs", kv, qo, 2, 1, 64, 16, synth.NHD, None, causal, seed,
+                         window_left=int(g.choice([-1, 0, 5, 31])))
+    assert bench.visible_pairs(b) == _brute_pairs(b)
+
+
+def test_square_causal_prefill_counts_the_triangle():
+    b = synth.make_batch("tri", [300, 17], [300, 17], 2, 1, 64, 16, synth.NHD, None, True, 0)
+    assert bench.visible_pairs(b) == 300 * 301 // 2 + 17 * 18 // 2
+    assert bench.attention_flops(b) == 4 * 64 * 2 * bench.visible_pairs(b)
+
+
+def test_kv_bytes_count_shared_prefix_pages_once():
+    kv = [100, 70, 40, 33]
+    b = synth.make_batch("shared", kv, [1, 1, 1, 1], 4, 2, 64, 16, synth.NHD, None, False, 1,
+                         shared_prefix_requests=3, shared_prefix_tokens=32)
+    unique = sum(kv) - 2 * 32                         # three requests share two full pages
+    assert bench.kv_bytes(b) == unique * 2 * 2 * 64 * 2
