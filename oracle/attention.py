@@ -27,9 +27,9 @@ the varlen wrapper of section 2 of the FlashAttention-3 page):
 
 Besides this definition the module holds, as separate plain functions, the
 three restatements the pins compare it against: the online (streaming)
-softmax recurrence of FlashAttention-1/2 tiling ("in-SRAM online softmax
-that aggregates and accumulates the output in place", section 1 of the
-FlashAttention-3 page), split-KV partial states combined by log-sum-exp
+softmax recurrence of FlashAttention-1/2 tiling (section 1 of the
+FlashAttention-3 page: the softmax statistics are kept on chip and the output
+is accumulated tile by tile), split-KV partial states combined by log-sum-exp
 (``merge_states``), and an explicit additive-mask form
 ``softmax(scale*QK^T + mask) V``.
 """
