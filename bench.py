@@ -4,6 +4,10 @@
 Default workload: Llama-7B-shaped batch decode (64 requests, 32 q / 32 kv
 heads, head_dim 128, page size 16, KV lengths uniform in [512, 4096], NHD,
 shuffled page table), the configuration the headline metric is quoted on.
+The default line also carries, under "workloads", every other configuration
+of the hot path timed the same way (Llama2-70B GQA decode, causal prefill at
+1K / 4K / 16K / 32K, the ragged prefill batch and the mixed chunked-prefill +
+decode batch), each with its own roofline and clock record.
 One step = one pass of the hot path over that batch through the C ABI: the
 stream-ordered work-list upload and the decode kernel (which also merges the
 partial states of split requests). The plan itself is host work done once per
@@ -39,6 +43,13 @@ if ROOT not in sys.path:
 METRIC = "decode KV GB/s & prefill TFLOPS on 1 GB300, as % of HBM / bf16 tensor peak"
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
+NOMINAL_HBM_GBS = 8000.0      # HBM3e data-sheet figure (about 8 TB/s)
+
+# every other configuration of the hot path, timed after the headline on the
+# default line: (workload, cap on the timed steps)
+SECONDARY = [("llama70b_gqa_decode", 200), ("causal_prefill_1k", 200),
+             ("causal_prefill_4k", 100), ("causal_prefill_16k", 30),
+             ("causal_prefill_32k", 30), ("ragged_prefill", 60), ("mixed_chunk_decode", 100)]
 
 
 def parse_args():
@@ -49,7 +60,7 @@ def parse_args():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="llama7b_decode", choices=sorted(WORKLOADS))
     ap.add_argument("--no-secondary", action="store_true",
-                    help="skip the 4K causal prefill measurement added to the default line")
+                    help="skip the other workloads added to the default line")
     ap.add_argument("--batch", type=int, default=None,
                     help="override the workload's request count (smaller profiling cases)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -190,6 +201,7 @@ class ClockSampler:
         self.proc = None
         self.gpu = gpu_index
         self.t0 = self.t1 = None
+        self.windows = []       # (t0, t1) of every timed region, in order
 
     def start(self):
         try:
@@ -211,6 +223,7 @@ class ClockSampler:
 
     def mark_end(self):
         self.t1 = time.time()
+        self.windows.append((self.t0, self.t1))
 
     def stop(self):
         if self.proc:
@@ -221,11 +234,14 @@ class ClockSampler:
             except Exception:
                 self.proc.kill()
 
-    def summary(self):
+    def summary(self, window_index=-1):
+        """Clocks over one timed region (the last by default); the whole run
+        when no sample fell inside it."""
         if not self.samples:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0,
                     "note": "nvidia-smi unavailable"}
-        inside = [s for t, s in self.samples if self.t0 and self.t1 and self.t0 - 0.1 <= t <= self.t1 + 0.1]
+        t0, t1 = self.windows[window_index] if self.windows else (None, None)
+        inside = [s for t, s in self.samples if t0 and t1 and t0 - 0.1 <= t <= t1 + 0.1]
         window = "timed region"
         if not inside:
             inside = [s for _, s in self.samples]
@@ -279,32 +295,49 @@ def oracle_sample(b, budget_s=12.0, threads=None):
     return kvb / dt / 1e9, dt, threads, sorted(done)
 
 
-def run_reference(args, rank, world):
-    """The oracle as the reference arm: each step is a bounded sample."""
+def run_reference(args, rank, world, budget_s=150.0):
+    """The oracle as the reference arm, on the host cores. One untimed pass
+    over the whole batch measures its cost; every step is then the whole
+    batch when the K + W steps fit in about `budget_s`, else the first
+    requests of the batch in the number that fits."""
     if rank != 0:
         return
     b = make_workload(args.workload, args.batch)
     from paged_kv_attention_27_gb300 import synth
     threads = os.cpu_count() or 1
-    sample = list(range(min(b.batch, threads)))
-    sb = synth.sub_batch(b, sample)
-    for _ in range(args.warmup):
-        oracle_sample(sb, budget_s=0.0, threads=threads)
+    t0 = time.perf_counter()
+    oracle_sample(b, budget_s=1e9, threads=threads)
+    t_full = time.perf_counter() - t0
+    runs = max(1, args.steps + args.warmup - 1)
+    if t_full * runs <= budget_s:
+        n = b.batch
+    else:
+        n = max(min(b.batch, threads), int(b.batch * budget_s / (t_full * runs)))
+        n = min(n, b.batch)
+    sample = list(range(n))
+    sb = b if n == b.batch else synth.sub_batch(b, sample)
+    for _ in range(args.warmup - 1):
+        oracle_sample(sb, budget_s=1e9, threads=threads)
     times = []
     for _ in range(args.steps):
         t0 = time.perf_counter()
         oracle_sample(sb, budget_s=1e9, threads=threads)
         times.append(time.perf_counter() - t0)
-    kvb = int(sb.kv_lens.sum()) * 2 * sb.num_kv_heads * sb.head_dim * 2
+    kvb = kv_bytes(sb)
     step_s = sum(times) / len(times)
     value = kvb / step_s / 1e9
-    desc = (f"fp64 oracle over requests {sample[0]}..{sample[-1]} of the batch "
-            f"({int(sb.kv_lens.sum())} KV tokens per step), {threads} threads")
+    if n == b.batch:
+        desc = (f"fp64 oracle over the whole batch ({int(sb.kv_lens.sum())} KV tokens per step), "
+                f"{threads} threads")
+    else:
+        desc = (f"fp64 oracle over requests 0..{n - 1} of the batch ({int(sb.kv_lens.sum())} KV "
+                f"tokens per step; the whole batch took {t_full:.1f} s, too long for "
+                f"{runs + 1} steps), {threads} threads")
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s",
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": step_s * 1e3, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": b.name, "sample": desc},
+            "config": dict(config_of(b, None, kv_bytes(b), attention_flops(b)), sample=desc),
             "cpu_baseline": {"value": value, "unit": "GB/s", "cores": threads, "kind": "oracle",
                              "sample": desc},
             "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
@@ -334,11 +367,19 @@ def whole_job_rate(units_per_rank, world, ms_per_step_max):
     return units_per_rank * world / (ms_per_step_max / 1e3)
 
 
-def time_steps(db, K, W, dist=None, sampler=None):
+L2_BYTES = 129 * 2**20
+
+
+def time_steps(db, K, W, dist=None, sampler=None, flush_l2=False):
     """W untimed steps, then K steps bracketed by a barrier and a device
     synchronisation on both sides, timed with CUDA events on the launching
     stream. Returns (ms for the K steps, mean ms of the attention kernels
-    alone, from events the library records around them)."""
+    alone, from events the library records around them).
+
+    flush_l2: before every timed step, overwrite a buffer twice the L2 size
+    so that the step starts with none of its K/V in the L2; the step time is
+    then the sum of per-step events around each step alone (the flush is
+    not timed)."""
     import torch
     from paged_kv_attention_27_gb300 import binding as B
 
@@ -350,10 +391,14 @@ def time_steps(db, K, W, dist=None, sampler=None):
     assert st == B.FI_OK, B.status_string(st)
     ks = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
     ke = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ss = [torch.cuda.Event(enable_timing=True) for _ in range(K)] if flush_l2 else []
+    se = [torch.cuda.Event(enable_timing=True) for _ in range(K)] if flush_l2 else []
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
-    for ev in ks + ke:          # create the CUDA events (torch creates them on first record)
+    for ev in ks + ke + ss + se:   # create the CUDA events (torch creates them on first record)
         ev.record(stream)
+    scrub = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=db.device) \
+        if flush_l2 else None
     if dist:
         dist.barrier()
     torch.cuda.synchronize()
@@ -361,8 +406,13 @@ def time_steps(db, K, W, dist=None, sampler=None):
         sampler.mark_start()
     t_start.record(stream)
     for i in range(K):
+        if flush_l2:
+            scrub.fill_(float(i))
+            ss[i].record(stream)
         B.fi_profile_next_launch(ks[i], ke[i])
         db.run()
+        if flush_l2:
+            se[i].record(stream)
     t_end.record(stream)
     torch.cuda.synchronize()
     if sampler:
@@ -371,22 +421,31 @@ def time_steps(db, K, W, dist=None, sampler=None):
         dist.barrier()
     st = db.status()
     assert st == B.FI_OK, B.status_string(st)
-    ms_total = t_start.elapsed_time(t_end)
+    if flush_l2:
+        ms_total = sum(a.elapsed_time(e) for a, e in zip(ss, se))
+    else:
+        ms_total = t_start.elapsed_time(t_end)
     kern_ms = sum(a.elapsed_time(e) for a, e in zip(ks, ke)) / K
     ms_total = reduce_max(ms_total, dist, "cuda")
     return ms_total, kern_ms
 
 
 def config_of(b, info, kvb, flops):
-    return {"workload": b.name, "batch": b.batch, "num_qo_heads": b.num_qo_heads,
+    """The JSON line's config: the workload and its sizes (and, with a plan
+    summary, the plan's work split)."""
+    cfg = {"workload": b.name, "batch": b.batch, "num_qo_heads": b.num_qo_heads,
             "num_kv_heads": b.num_kv_heads, "head_dim": b.head_dim, "page_size": b.page_size,
             "layout": b.layout, "causal": b.causal, "kv_tokens": int(b.kv_lens.sum()),
             "q_rows": int(b.qo_lens.sum()), "kv_bytes_per_step": kvb,
             "attention_flops_per_step": flops, "io_bytes_per_step": io_bytes(b),
-            "l2": f"inputs larger than L2 ({(kvb + io_bytes(b)) / 1e9:.2f} GB of KV, q and out "
-                  "per step vs 129 MB L2): no flush",
-            "plan": {k: info[k] for k in ("num_decode_items", "num_prefill_items",
-                                          "chunk_tokens", "num_split_requests")}}
+            "l2": (f"inputs larger than L2 ({(kvb + io_bytes(b)) / 1e9:.2f} GB of KV, q and out "
+                   "per step vs 129 MB L2): no flush") if kvb > 2 * L2_BYTES else
+                  (f"K/V ({kvb / 1e6:.0f} MB) could stay in the 129 MB L2: L2 flushed before "
+                   "every timed step (a 258 MB write, not timed)")}
+    if info is not None:
+        cfg["plan"] = {k: info[k] for k in ("num_decode_items", "num_prefill_items",
+                                            "chunk_tokens", "num_split_requests")}
+    return cfg
 
 
 def roofline_of(b, kvb, flops, kern_ms, kernel_names, workload):
@@ -411,6 +470,7 @@ def roofline_of(b, kvb, flops, kern_ms, kernel_names, workload):
     r["kernel"] = "+".join(kernel_names)
     r["kernel_ms"] = kern_ms
     r["hbm_frac"] = f_hbm
+    r["hbm_frac_of_nominal"] = gbs / NOMINAL_HBM_GBS
     r["tensor_frac"] = f_tc
     return r
 
@@ -463,8 +523,9 @@ def run_ours(args, rank, world, local_rank):
     sampler.start()
     time.sleep(0.3)
     K = args.steps
-    ms_total, kern_ms = time_steps(db, K, args.warmup, dist, sampler)
-    sampler.stop()
+    ms_total, kern_ms = time_steps(db, K, args.warmup, dist, sampler,
+                                   flush_l2=kvb <= 2 * L2_BYTES)
+    clocks = sampler.summary()
     ms_step = ms_total / K
     if info["num_decode_items"]:          # decode or mixed: HBM-bound, KV GB/s
         value, unit = whole_job_rate(kvb, world, ms_step) / 1e9, "GB/s"
@@ -475,11 +536,16 @@ def run_ours(args, rank, world, local_rank):
     if not args.no_e2e:
         e2e = run_e2e(b, db, K, local_rank, unit)
 
-    secondary = None
+    workloads = None
     if args.workload == "llama7b_decode" and args.batch is None and not args.no_secondary:
         del db
         torch.cuda.empty_cache()
-        secondary = measure_secondary("causal_prefill_4k", max(5, min(K, 30)), args.warmup, dist)
+        workloads = {}
+        for name, cap in SECONDARY:
+            workloads[name] = measure_secondary(name, max(5, min(K, cap)), max(3, args.warmup),
+                                                dist, sampler, world)
+            torch.cuda.empty_cache()
+    sampler.stop()
 
     line = {
         "metric": METRIC, "value": value, "unit": unit, "n_gpus": world, "steps": K,
@@ -496,29 +562,50 @@ def run_ours(args, rank, world, local_rank):
         "e2e": e2e,
         "gpu_launches": launches_per_step * K,
         "plan_host_us": plan_host,
-        "clocks": sampler.summary(),
+        "clocks": clocks,
     }
-    if secondary:
-        line["prefill_4k"] = secondary
+    if workloads:
+        line["workloads"] = workloads
     if rank == 0:
         print(json.dumps(line), flush=True)
     if dist:
         dist.destroy_process_group()
 
 
-def measure_secondary(workload, K, W, dist):
-    """A second workload timed the same way (no CPU baseline, no e2e)."""
+def measure_secondary(workload, K, W, dist, sampler, world):
+    """Another configuration of the hot path, timed like the headline (no CPU
+    baseline, no e2e): whole-job rate in its own unit (KV GB/s when the batch
+    has decode rows, TFLOP/s of the causal triangle otherwise), the attention
+    kernels' own time, the roofline of that time, and the clocks seen while it
+    ran."""
+    import torch
     from paged_kv_attention_27_gb300 import binding as B
     from paged_kv_attention_27_gb300.device import DeviceBatch
     b = make_workload(workload)
-    db = DeviceBatch(b)
+    db = DeviceBatch(b, device=f"cuda:{torch.cuda.current_device()}")
     info = B.fi_plan_get_info(db.plan)
     kvb, flops = kv_bytes(b), attention_flops(b)
-    ms_total, kern_ms = time_steps(db, K, W, dist)
+    flush = kvb <= 2 * L2_BYTES     # K/V that the L2 could hold between steps
+    ms_total, kern_ms = time_steps(db, K, W, dist, sampler, flush_l2=flush)
     ms_step = ms_total / K
-    return {"workload": b.name, "value": flops / (ms_step / 1e3) / 1e12, "unit": "TFLOP/s",
-            "steps": K, "ms_per_step": ms_step, "attention_flops_per_step": flops,
-            "roofline": roofline_of(b, kvb, flops, kern_ms, kernels_of(b, info), workload)}
+    if info["num_decode_items"]:
+        value, unit = whole_job_rate(kvb, world, ms_step) / 1e9, "GB/s"
+    else:
+        value, unit = whole_job_rate(flops, world, ms_step) / 1e12, "TFLOP/s"
+    launches = (1 if info["num_decode_items"] else 0) + (1 if info["num_prefill_items"] else 0)
+    out = {"workload": b.name, "value": value, "unit": unit, "steps": K, "warmup": W,
+           "ms_per_step": ms_step, "kernel_ms": kern_ms,
+           "kv_bytes_per_step": kvb, "attention_flops_per_step": flops,
+           "tokens_per_s": int(b.qo_lens.sum()) * world / (ms_step / 1e3),
+           "kv_tokens": int(b.kv_lens.sum()), "q_rows": int(b.qo_lens.sum()),
+           "gpu_launches": launches * K,
+           "l2": (f"K/V ({kvb / 1e6:.0f} MB) could stay in the 129 MB L2: L2 flushed before "
+                  "every timed step (a 258 MB write, not timed)") if flush else
+                 f"inputs larger than L2 ({kvb / 1e9:.2f} GB of K/V per step): no flush",
+           "roofline": roofline_of(b, kvb, flops, kern_ms, kernels_of(b, info), workload),
+           "clocks": sampler.summary()}
+    del db
+    return out
 
 
 def cpu_baseline(b):

@@ -274,10 +274,15 @@ fi_status fi_batch_decode_paged(fi_plan_t plan, const void* q, const void* k_cac
  * pages has a counterpart to this call; it is an interface convenience.
  * The scratch (work list, error word, fp32 split partials) is a 16 MiB
  * array inside the library, held by every GPU that loads the library until
- * the process exits. This call allocates nothing itself.
+ * the process exits. The work list is built in a static 16 MiB host buffer
+ * of the library and copied by an ordinary pageable cudaMemcpyAsync (the
+ * CUDA driver stages it before the call returns). The call allocates
+ * nothing, host or device, pinned or not.
  *   Arguments: as for fi_batch_decode_paged, minus the workspace.
  *   First call on a device: looks up that device's address of the array
- *   (cudaGetSymbolAddress) and caches it — make it before any stream capture.
+ *   (cudaGetSymbolAddress) and caches it.
+ *   Graphs: the call cannot be captured; a stream that is capturing is
+ *   refused with FI_ERR_UNSUPPORTED before anything touches the device.
  *   Sharing: every call uses the same array, so calls whose GPU work can
  *   overlap (unordered streams) race; order them on one stream.
  *   Limits: a plan whose workspace_bytes exceeds 16 MiB returns

@@ -173,6 +173,24 @@ fi_status upload_image(void* dst, const fi::Plan& P, cudaStream_t stream) {
                         [&](uint8_t* p) { fill_image(p, P); }, stream, "work-list upload");
 }
 
+// The work-list upload of the no-allocation decode call: the image is built
+// in a static host buffer (one per process, guarded by a mutex) and copied
+// with an ordinary cudaMemcpyAsync from pageable memory. For such a copy the
+// CUDA driver copies the source into its own staging memory before the call
+// returns (no device synchronisation), so the buffer may be refilled at once
+// and this library allocates nothing, host or device.
+std::mutex g_static_image_mutex;
+uint8_t g_static_image[fi::kNoAllocScratchBytes];
+
+fi_status upload_image_static(void* dst, const fi::Plan& P, cudaStream_t stream) {
+  const size_t bytes = P.ws.partial_o;
+  if (bytes > sizeof(g_static_image)) return FI_ERR_WORKSPACE_TOO_SMALL;
+  std::lock_guard<std::mutex> lock(g_static_image_mutex);
+  fill_image(g_static_image, P);
+  const cudaError_t e = cudaMemcpyAsync(dst, g_static_image, bytes, cudaMemcpyHostToDevice, stream);
+  return e == cudaSuccess ? FI_OK : cuda_fail(e, "work-list upload");
+}
+
 // Tensor map over a paged K or V cache that fetches one (page, kv head)
 // block per box: page_size rows x 64 dims (128 bytes, 128-byte swizzled)
 // for a 16-bit cache; page_size whole rows of head_dim bytes for an FP8
@@ -281,7 +299,7 @@ fi_status run_paged(fi_plan_t plan, bool prefill_call, const void* q, const int3
                     int64_t page_stride_elems, int32_t num_pages, const int32_t* page_indptr_d,
                     const int32_t* page_indices_d, const int32_t* last_page_len_d, float sm_scale,
                     float k_scale, float v_scale, void* out, float* lse, void* workspace,
-                    size_t workspace_bytes, void* stream_ptr) {
+                    size_t workspace_bytes, void* stream_ptr, bool static_upload = false) {
   if (!plan) return FI_ERR_INVALID_ARG;
   const fi::Plan& P = plan->p;
   if (P.mode != (prefill_call ? FI_MODE_PREFILL : FI_MODE_DECODE)) return FI_ERR_INVALID_ARG;
@@ -314,7 +332,7 @@ fi_status run_paged(fi_plan_t plan, bool prefill_call, const void* q, const int3
   }
   // Upload header (zeroed error word and counters) + work lists + merge
   // tasks in one copy.
-  st = upload_image(ws, P, stream);
+  st = static_upload ? upload_image_static(ws, P, stream) : upload_image(ws, P, stream);
   if (st != FI_OK) return st;
   cudaError_t e = cudaSuccess;
 
@@ -472,6 +490,16 @@ fi_status run_paged(fi_plan_t plan, bool prefill_call, const void* q, const int3
 }
 
 }  // namespace
+
+fi_status fi::run_decode_static_upload(
+    fi_plan_t plan, const void* q, const void* k_cache, const void* v_cache, int32_t kv_layout,
+    int64_t page_stride_elems, int32_t num_pages, const int32_t* page_indptr_d,
+    const int32_t* page_indices_d, const int32_t* last_page_len_d, float sm_scale, float k_scale,
+    float v_scale, void* out, float* lse, void* workspace, size_t workspace_bytes, void* stream) {
+  return run_paged(plan, false, q, nullptr, k_cache, v_cache, kv_layout, page_stride_elems,
+                   num_pages, page_indptr_d, page_indices_d, last_page_len_d, sm_scale, k_scale,
+                   v_scale, out, lse, workspace, workspace_bytes, stream, true);
+}
 
 extern "C" {
 

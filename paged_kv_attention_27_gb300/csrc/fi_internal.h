@@ -94,6 +94,22 @@ struct Plan {
   WorkspaceLayout ws;
 };
 
+// Scratch of fi_batch_decode_paged_noalloc: a static device array of this
+// size inside the library (noalloc.cu), and a static host buffer of the same
+// size from which that call's work list is copied (api.cu).
+constexpr size_t kNoAllocScratchBytes = size_t(16) << 20;   // 16 MiB
+
+// api.cu: fi_batch_decode_paged with the work-list image filled into the
+// static host buffer and copied by an ordinary (pageable) cudaMemcpyAsync,
+// which the CUDA driver stages itself: no host or device allocation.
+fi_status run_decode_static_upload(fi_plan_t plan, const void* q, const void* k_cache,
+                                   const void* v_cache, int32_t kv_layout,
+                                   int64_t page_stride_elems, int32_t num_pages,
+                                   const int32_t* page_indptr_d, const int32_t* page_indices_d,
+                                   const int32_t* last_page_len_d, float sm_scale,
+                                   float k_scale, float v_scale, void* out, float* lse,
+                                   void* workspace, size_t workspace_bytes, void* stream);
+
 // plan.cpp
 fi_status build_plan(int32_t mode, int32_t batch, const int32_t* qo_indptr,
                      const int32_t* page_indptr, const int32_t* last_page_len,

@@ -1,5 +1,15 @@
 """Helpers shared by the GPU parity tests: build/load the library, compare
-GPU results with the fp64 oracle under the stated tolerances."""
+GPU results with the fp64 oracle under the stated tolerances, and run the
+oracle over a batch's requests on a thread pool.
+
+Every comparison also reports the rounding floor: the error of the oracle
+itself once rounded to the output type. A kernel cannot get below it, so the
+distance between the two shows how much of the budget the kernel's own
+arithmetic uses. With FI_PARITY_LOG set to a file path, each comparison
+appends one line (what, max and mean error, floor max and mean) to it."""
+import concurrent.futures as cf
+import os
+
 import numpy as np
 
 # bf16 (or fp16) outputs against the unrounded fp64 oracle; fp32 lse absolute
@@ -28,8 +38,47 @@ def ensure_built():
     build.build()
 
 
+def oracle_parallel(b, requests=None, threads=None):
+    """oracle.batch_attention over the batch's requests (all, or those
+    given), one request per task on a thread pool; rows of other requests
+    stay NaN, as in the oracle itself."""
+    import oracle
+    reqs = list(range(b.batch)) if requests is None else list(requests)
+    total, hq, d = b.q.shape
+    out = np.full((total, hq, d), np.nan)
+    lse = np.full((total, hq), np.nan)
+
+    def one(r):
+        o, l = oracle.batch_attention(b.q, b.qo_indptr, b.k_cache, b.v_cache, b.layout,
+                                      b.page_indptr, b.page_indices, b.last_page_len,
+                                      b.num_qo_heads, b.num_kv_heads, b.page_size, b.sm_scale,
+                                      b.causal, requests=[r], window_left=b.window_left,
+                                      dtype=b.dtype, kv_dtype=b.cache_dtype, k_scale=b.k_scale,
+                                      v_scale=b.v_scale)
+        r0, r1 = int(b.qo_indptr[r]), int(b.qo_indptr[r + 1])
+        return r0, r1, o[r0:r1], l[r0:r1]
+
+    with cf.ThreadPoolExecutor(max_workers=threads or os.cpu_count() or 1) as ex:
+        for r0, r1, o, l in ex.map(one, reqs):
+            out[r0:r1] = o
+            lse[r0:r1] = l
+    return out, lse
+
+
+def rounding_floor(out_ref, half: bool):
+    """|oracle rounded to the output type - oracle|: bf16 (RNE) or fp16."""
+    from paged_kv_attention_27_gb300.synth import f32_to_bf16_bits
+    if half:
+        rounded = out_ref.astype(np.float16).astype(np.float64)
+    else:
+        rounded = (f32_to_bf16_bits(out_ref.astype(np.float32)).astype(np.uint32) << 16) \
+            .view(np.float32).astype(np.float64)
+    return np.abs(rounded - out_ref), rounded
+
+
 def compare(out_gpu, lse_gpu, out_ref, lse_ref, rows=None, what=""):
     """Element-wise comparison on the rows given (all rows if None)."""
+    import torch
     o = out_gpu.float().cpu().numpy().astype(np.float64)
     l = lse_gpu.float().cpu().numpy().astype(np.float64) if lse_gpu is not None else None
     if rows is not None:
@@ -38,17 +87,16 @@ def compare(out_gpu, lse_gpu, out_ref, lse_ref, rows=None, what=""):
             l, lse_ref = l[rows], lse_ref[rows]
     assert np.all(np.isfinite(o)), f"{what}: non-finite output"
     err = np.abs(o - out_ref)
+    floor, rounded = rounding_floor(out_ref, out_gpu.dtype == torch.float16)
+    margin = (f"{what}: max-abs {err.max():.3e} mean-abs {err.mean():.3e} | rounding floor "
+              f"max {floor.max():.3e} mean {floor.mean():.3e}")
+    print(margin)
+    log = os.environ.get("FI_PARITY_LOG")
+    if log:
+        with open(log, "a") as f:
+            f.write(margin + "\n")
     detail = ""
     if err.max() > OUT_MAX_ABS or err.mean() > OUT_MEAN_ABS:
-        # diagnostic: how much of the error is the rounding of the output itself
-        from paged_kv_attention_27_gb300.synth import f32_to_bf16_bits
-        import torch
-        if out_gpu.dtype == torch.float16:
-            rounded = out_ref.astype(np.float16).astype(np.float64)
-        else:
-            rounded = (f32_to_bf16_bits(out_ref.astype(np.float32)).astype(np.uint32) << 16) \
-                .view(np.float32).astype(np.float64)
-        floor = np.abs(rounded - out_ref)
         i = np.unravel_index(np.argmax(err), err.shape)
         detail = (f"; worst at {i}: gpu {o[i]:.6f} oracle {out_ref[i]:.6f} "
                   f"(rounded oracle {rounded[i]:.6f}); rounding floor max "

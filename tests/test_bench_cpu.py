@@ -67,3 +67,27 @@ def test_kv_bytes_count_shared_prefix_pages_once():
                          shared_prefix_requests=3, shared_prefix_tokens=32)
     unique = sum(kv) - 2 * 32                         # three requests share two full pages
     assert bench.kv_bytes(b) == unique * 2 * 2 * 64 * 2
+
+
+def test_default_line_covers_every_configuration():
+    names = [n for n, _ in bench.SECONDARY]
+    assert all(n in bench.WORKLOADS for n in names)
+    # the 70B GQA decode, prefill at 1K/4K/16K/32K, the ragged and the mixed batch
+    for n in ("llama70b_gqa_decode", "causal_prefill_1k", "causal_prefill_4k",
+              "causal_prefill_16k", "causal_prefill_32k", "ragged_prefill",
+              "mixed_chunk_decode"):
+        assert n in names
+    assert all(cap >= 5 for _, cap in bench.SECONDARY)
+
+
+def test_clock_summary_reads_each_timed_window():
+    c = bench.ClockSampler(0)
+    row = lambda mhz, cap: ["0", str(mhz), "2070", "500", "0x0", "Not Active", "Not Active",
+                            "Not Active", "Active" if cap else "Not Active"]
+    c.samples = [(10.0, row(2070, False)), (10.5, row(2070, False)),
+                 (20.0, row(1500, True)), (20.5, row(1600, True))]
+    c.windows = [(9.9, 10.6), (19.9, 20.6)]
+    first, second = c.summary(0), c.summary(1)
+    assert first["sm_mhz"] == 2070 and first["reasons"] == []
+    assert second["sm_mhz"] == 1550 and second["reasons"] == ["sw_power_cap"]
+    assert second["window"] == "timed region"

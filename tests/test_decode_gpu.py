@@ -10,7 +10,7 @@ import oracle  # noqa: E402
 from paged_kv_attention_27_gb300 import binding as B  # noqa: E402
 from paged_kv_attention_27_gb300 import synth  # noqa: E402
 
-from ._gpu import compare, ensure_built, scale_v  # noqa: E402
+from ._gpu import compare, ensure_built, oracle_parallel, scale_v  # noqa: E402
 
 pytestmark = pytest.mark.gpu
 
@@ -54,18 +54,25 @@ def test_tiny_decode():
     check(synth.tiny_decode())
 
 
-def test_llama7b_decode_full_size_sampled():
-    b = synth.llama7b_decode()
-    order = np.argsort(-b.kv_lens)
-    sample = sorted(set(order[:4].tolist() + order[-4:].tolist() + list(range(0, 64, 9))))
-    check(b, requests=sample)
+def check_all(b):
+    """The whole batch against the oracle (run over the requests in parallel)."""
+    db = _dev(b)
+    out, lse = db.run()
+    torch.cuda.synchronize()
+    assert db.status() == B.FI_OK
+    ref_o, ref_l = oracle_parallel(b)
+    return compare(out, lse, ref_o, ref_l, what=b.name), db
 
 
-def test_llama70b_gqa_decode_full_size_sampled():
+def test_llama7b_decode_full_size_every_request():
+    # the benchmark's batch as the benchmark launches it: every request, every
+    # split chunk and every merge of the plan
+    check_all(synth.llama7b_decode())
+
+
+def test_llama70b_gqa_decode_full_size_every_request():
     b = synth.llama70b_gqa_decode()
-    order = np.argsort(-b.kv_lens)
-    sample = sorted(set(order[:3].tolist() + order[-3:].tolist() + [0, 5, 31, 32, 77]))
-    (_, _), db = check(b, requests=sample)
+    (_, _), db = check_all(b)
     info = B.fi_plan_get_info(db.plan)
     assert info["num_split_requests"] > 0        # long requests really were split
 

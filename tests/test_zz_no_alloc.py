@@ -1,4 +1,4 @@
-"""fi_batch_decode_paged_noalloc against fi_batch_decode_paged.
+"""fi_batch_decode_paged_noalloc against fi_batch_decode_paged and the oracle.
 
 The no-allocation variant serves callers that cannot give the library a
 workspace (an engine plugin whose framework owns all device memory, or a hot
@@ -6,8 +6,11 @@ loop where cudaMalloc is not acceptable); it keeps its scratch in a static
 device array inside libfi.so. This file is named so that pytest collects it
 last. Two calls in a row, on different batches (the second one with split-KV
 partials in the shared scratch), must each match the workspace entry point
-within the parity tolerance.
+and the fp64 oracle within the parity tolerance; a further call on the same
+batch must leave the device's allocations as they were.
 """
+import gc
+
 import numpy as np
 import pytest
 
@@ -16,7 +19,8 @@ torch = pytest.importorskip("torch")
 from paged_kv_attention_27_gb300 import binding as B  # noqa: E402
 from paged_kv_attention_27_gb300 import synth  # noqa: E402
 
-from ._gpu import LSE_MAX_ABS, OUT_MAX_ABS, OUT_MEAN_ABS, ensure_built  # noqa: E402
+from ._gpu import (LSE_MAX_ABS, OUT_MAX_ABS, OUT_MEAN_ABS, compare, ensure_built,  # noqa: E402
+                   oracle_parallel)
 
 pytestmark = pytest.mark.gpu
 
@@ -65,6 +69,32 @@ def test_noalloc_decode_matches_workspace_decode_twice():
     db, out, lse, ref_out, ref_lse = _both(b)
     assert B.fi_plan_get_info(db.plan)["num_split_requests"] >= 2
     _close(out, lse, ref_out, ref_lse)
+    o_ref, l_ref = oracle_parallel(b)
+    compare(out, lse, o_ref, l_ref, what="noalloc splits vs oracle")
+    # the call exists for callers that cannot allocate: once the kernel is
+    # loaded, another call changes neither torch's allocations nor the
+    # device's free memory
+    # (Python's garbage collector is kept from freeing unrelated tensors
+    # meanwhile)
+    out2 = torch.full_like(out, float("nan"))
+    lse2 = torch.full_like(lse, float("nan"))
+    gc.collect()
+    gc.disable()
+    try:
+        torch.cuda.synchronize()
+        alloc1 = torch.cuda.memory_allocated()
+        free1, _ = torch.cuda.mem_get_info()
+        B.fi_batch_decode_paged_noalloc(db.plan, db.q, db.k, db.v, B.LAYOUTS[b.layout], 0,
+                                        b.num_pages, db.page_indptr, db.page_indices,
+                                        db.last_page_len, b.sm_scale, 1.0, 1.0, out2, lse2)
+        torch.cuda.synchronize()
+        alloc2 = torch.cuda.memory_allocated()
+        free2, _ = torch.cuda.mem_get_info()
+    finally:
+        gc.enable()
+    assert alloc2 == alloc1
+    assert free2 == free1
+    assert torch.equal(out2, out) and torch.equal(lse2, lse)   # same plan: bitwise the same
 
 
 def test_noalloc_rejects_plans_beyond_its_scratch():
