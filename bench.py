@@ -151,8 +151,11 @@ def io_bytes(b):
 
 
 KERNEL_SOURCES = {
-    "decode_kernel": ["decode.cu", "ptx.cuh", "kernels.cuh", "fi_internal.h"],
-    "prefill_kernel": ["prefill.cu", "ptx.cuh", "kernels.cuh", "fi_internal.h"],
+    "decode_kernel": ["decode.cu", "decode_roles.cuh", "ptx.cuh", "kernels.cuh", "fi_internal.h"],
+    "prefill_kernel": ["prefill.cu", "decode_roles.cuh", "ptx.cuh", "kernels.cuh",
+                       "fi_internal.h"],
+    "mixed_kernel": ["prefill.cu", "decode_roles.cuh", "ptx.cuh", "kernels.cuh",
+                     "fi_internal.h"],
     "prefill_pair_kernel": ["prefill_pair.cu", "ptx.cuh", "kernels.cuh", "fi_internal.h"],
 }
 
@@ -271,7 +274,7 @@ def oracle_sample(b, budget_s=12.0, threads=None):
                                b.page_indices, b.last_page_len, b.num_qo_heads, b.num_kv_heads,
                                b.page_size, b.sm_scale, b.causal, requests=[r],
                                window_left=b.window_left, dtype=b.dtype,
-                               kv_dtype=b.cache_dtype, k_scale=b.k_scale, v_scale=b.v_scale)
+                               kv_dtype=b.cache_dtype, k_scale=b.k_scales, v_scale=b.v_scales)
         return r
 
     done = []
@@ -475,10 +478,27 @@ def roofline_of(b, kvb, flops, kern_ms, kernel_names, workload):
     return r
 
 
+def mixed_fused(b, info):
+    """Whether a plan's prefill and decode work run as one persistent mixed
+    launch (head_dim 256, 1, 2 or 4 query heads per kv head, a 16-bit cache)."""
+    g = b.num_qo_heads // b.num_kv_heads
+    return (bool(info["num_prefill_items"]) and bool(info["num_decode_items"]) and
+            b.head_dim == 256 and g in (1, 2, 4) and b.cache_dtype == b.dtype)
+
+
+def launches_per_step(b, info):
+    if mixed_fused(b, info):
+        return 1
+    return (1 if info["num_decode_items"] else 0) + (1 if info["num_prefill_items"] else 0)
+
+
 def kernels_of(b, info):
     """The kernels a plan launches (the two-tile prefill kernel takes plain
     prefill work at head_dim 64 and 128 with an even number of query heads
-    per kv head; the one-tile kernel the rest)."""
+    per kv head; the one-tile kernel the rest; a mixed batch at head_dim 256
+    runs as one mixed kernel)."""
+    if mixed_fused(b, info):
+        return ["mixed_kernel"]
     names = []
     if info["num_prefill_items"]:
         pair = b.head_dim in (64, 128) and (b.num_qo_heads // b.num_kv_heads) % 2 == 0
@@ -508,8 +528,6 @@ def run_ours(args, rank, world, local_rank):
     info = B.fi_plan_get_info(db.plan)
     kvb = kv_bytes(b)
     flops = attention_flops(b)
-    launches_per_step = (1 if info["num_decode_items"] else 0) + \
-                        (1 if info["num_prefill_items"] else 0)
 
     # CPU baseline first (rank 0, N = 1 only), before the device is busy
     cpu = None
@@ -560,7 +578,7 @@ def run_ours(args, rank, world, local_rank):
         "tokens_per_s": int(b.qo_lens.sum()) * world / (ms_step / 1e3),
         "cpu_baseline": cpu,
         "e2e": e2e,
-        "gpu_launches": launches_per_step * K,
+        "gpu_launches": launches_per_step(b, info) * K,
         "plan_host_us": plan_host,
         "clocks": clocks,
     }
@@ -592,7 +610,7 @@ def measure_secondary(workload, K, W, dist, sampler, world):
         value, unit = whole_job_rate(kvb, world, ms_step) / 1e9, "GB/s"
     else:
         value, unit = whole_job_rate(flops, world, ms_step) / 1e12, "TFLOP/s"
-    launches = (1 if info["num_decode_items"] else 0) + (1 if info["num_prefill_items"] else 0)
+    launches = launches_per_step(b, info)
     out = {"workload": b.name, "value": value, "unit": unit, "steps": K, "warmup": W,
            "ms_per_step": ms_step, "kernel_ms": kern_ms,
            "kv_bytes_per_step": kvb, "attention_flops_per_step": flops,
@@ -638,7 +656,7 @@ def oracle_rows_sample(b, budget_s=12.0):
                                b.page_indices, b.last_page_len, b.num_qo_heads, b.num_kv_heads,
                                b.page_size, b.sm_scale, b.causal, requests=[r], rows={r: [i]},
                                window_left=b.window_left, dtype=b.dtype,
-                               kv_dtype=b.cache_dtype, k_scale=b.k_scale, v_scale=b.v_scale)
+                               kv_dtype=b.cache_dtype, k_scale=b.k_scales, v_scale=b.v_scales)
         qo, kv = int(b.qo_lens[r]), int(b.kv_lens[r])
         pos = kv - qo + i
         hi = min(kv - 1, pos) if b.causal else kv - 1
@@ -736,7 +754,8 @@ def run_e2e(b, db, K, local_rank, unit):
     def step():
         B.fi_batch_attention_host(plan(), q_h, None if decode else qo_h, db.k, db.v, layout, 0,
                                   b.num_pages, indptr_h, indices_h, last_h, b.sm_scale,
-                                  b.k_scale, b.v_scale, out_h, lse_h, ws, ws_bytes)
+                                  b.k_scale, b.v_scale, out_h, lse_h, ws, ws_bytes,
+                                  k_head_scale=db.k_head_scale, v_head_scale=db.v_head_scale)
 
     for _ in range(3):
         step()

@@ -242,6 +242,14 @@ fi_status fi_plan_get_work(fi_plan_t plan, int32_t* items_h, int32_t capacity,
  *                    integration in inference engines" page describes in
  *                    section 1: the quantisation scale fused with the softmax
  *                    scaling instead of extra conversion passes).
+ *   k_head_scale, v_head_scale  device fp32 [num_kv_heads] or NULL: a
+ *                    further factor per kv head on k_scale and v_scale (an
+ *                    FP8 cache quantised with one scale per head: the keys
+ *                    and values of kv head h attended to are k_scale *
+ *                    k_head_scale[h] and v_scale * v_head_scale[h] times the
+ *                    stored ones). NULL means 1 for every head. The values
+ *                    must be finite and > 0 (caller contract: they are read
+ *                    on the device only); 4-byte aligned.
  *   out              device [B][num_qo_heads][head_dim], the plan's dtype.
  *   lse              device fp32 [B][num_qo_heads] or NULL.
  *   workspace        device buffer of at least the planned size, 256-byte
@@ -262,8 +270,9 @@ fi_status fi_batch_decode_paged(fi_plan_t plan, const void* q, const void* k_cac
                                 int64_t page_stride_elems, int32_t num_pages,
                                 const int32_t* page_indptr_d, const int32_t* page_indices_d,
                                 const int32_t* last_page_len_d, float sm_scale, float k_scale,
-                                float v_scale, void* out, float* lse, void* workspace,
-                                size_t workspace_bytes, void* stream);
+                                float v_scale, const float* k_head_scale,
+                                const float* v_head_scale, void* out, float* lse,
+                                void* workspace, size_t workspace_bytes, void* stream);
 
 /*
  * fi_batch_decode_paged_noalloc — fi_batch_decode_paged without a workspace
@@ -296,7 +305,9 @@ fi_status fi_batch_decode_paged_noalloc(fi_plan_t plan, const void* q, const voi
                                         const int32_t* page_indptr_d,
                                         const int32_t* page_indices_d,
                                         const int32_t* last_page_len_d, float sm_scale,
-                                        float k_scale, float v_scale, void* out, float* lse,
+                                        float k_scale, float v_scale,
+                                        const float* k_head_scale,
+                                        const float* v_head_scale, void* out, float* lse,
                                         void* stream);
 
 /*
@@ -319,8 +330,9 @@ fi_status fi_batch_prefill_paged(fi_plan_t plan, const void* q, const int32_t* q
                                  int64_t page_stride_elems, int32_t num_pages,
                                  const int32_t* page_indptr_d, const int32_t* page_indices_d,
                                  const int32_t* last_page_len_d, float sm_scale, float k_scale,
-                                 float v_scale, void* out, float* lse, void* workspace,
-                                 size_t workspace_bytes, void* stream);
+                                 float v_scale, const float* k_head_scale,
+                                 const float* v_head_scale, void* out, float* lse,
+                                 void* workspace, size_t workspace_bytes, void* stream);
 
 /*
  * fi_batch_attention_host — one serving step of a plan with the step's own
@@ -341,7 +353,8 @@ fi_status fi_batch_prefill_paged(fi_plan_t plan, const void* q, const int32_t* q
  *                    qo_indptr_h[B] for a prefill plan).
  *   qo_indptr_h      host int32 [B+1] for a prefill plan; NULL for decode.
  *   k_cache, v_cache, kv_layout, page_stride_elems, num_pages, sm_scale,
- *   k_scale, v_scale as for fi_batch_decode_paged (the caches are device
+ *   k_scale, v_scale, k_head_scale, v_head_scale as for fi_batch_decode_paged
+ *                    (the caches and the per-head scales are device
  *                    memory).
  *   page_indptr_h, page_indices_h, last_page_len_h  host int32, the planned
  *                    page table (page_indices_h holds page_indptr_h[B]
@@ -361,8 +374,9 @@ fi_status fi_batch_attention_host(fi_plan_t plan, const void* q_h, const int32_t
                                   int64_t page_stride_elems, int32_t num_pages,
                                   const int32_t* page_indptr_h, const int32_t* page_indices_h,
                                   const int32_t* last_page_len_h, float sm_scale, float k_scale,
-                                  float v_scale, void* out_h, float* lse_h, void* workspace,
-                                  size_t workspace_bytes, void* stream);
+                                  float v_scale, const float* k_head_scale,
+                                  const float* v_head_scale, void* out_h, float* lse_h,
+                                  void* workspace, size_t workspace_bytes, void* stream);
 
 /*
  * fi_merge_states — combine attention states computed over disjoint key

@@ -171,14 +171,15 @@ def batch_attention(q_bits, qo_indptr, k_cache_bits, v_cache_bits, layout: str,
                     page_indptr, page_indices, last_page_len, num_qo_heads: int,
                     num_kv_heads: int, page_size: int, sm_scale: float, causal: bool,
                     requests=None, rows=None, window_left: int = -1, dtype: str = "bf16",
-                    kv_dtype: str | None = None, k_scale: float = 1.0, v_scale: float = 1.0):
+                    kv_dtype: str | None = None, k_scale=1.0, v_scale=1.0):
     """Paged attention for a packed batch.
 
     q_bits ``[sum qo_len, Hq, d]`` bit patterns of ``dtype`` ("bf16" or
     "fp16"); caches as laid out by ``layout``, of ``kv_dtype`` (default:
     ``dtype``; "e4m3" for an FP8 cache). A quantised cache holds K / k_scale
     and V / v_scale: the keys and values attended to are ``k_scale`` and
-    ``v_scale`` times the stored ones.
+    ``v_scale`` times the stored ones. Either scale is one number for the
+    whole cache or a sequence of ``num_kv_heads`` numbers, one per kv head.
     Returns ``out [sum qo_len, Hq, d]`` and ``lse [sum qo_len, Hq]`` in
     float64. ``requests`` limits the work to some requests (other rows stay
     NaN); ``rows`` maps a request to the list of its row indices to compute
@@ -202,10 +203,12 @@ def batch_attention(q_bits, qo_indptr, k_cache_bits, v_cache_bits, layout: str,
         sel = np.arange(qo_len) if rows is None or b not in rows else np.asarray(rows[b])
         vis = visible_keys(qo_len, int(kv_len[b]), causal, window_left)[sel]
         for kh in range(num_kv_heads):
-            k = k_scale * gather_kv(k_cache_bits, layout, page_indptr, page_indices, b, kh,
-                                    int(kv_len[b]), page_size, kv_dtype or dtype)
-            v = v_scale * gather_kv(v_cache_bits, layout, page_indptr, page_indices, b, kh,
-                                    int(kv_len[b]), page_size, kv_dtype or dtype)
+            ks = float(k_scale[kh]) if np.ndim(k_scale) else float(k_scale)
+            vs = float(v_scale[kh]) if np.ndim(v_scale) else float(v_scale)
+            k = ks * gather_kv(k_cache_bits, layout, page_indptr, page_indices, b, kh,
+                               int(kv_len[b]), page_size, kv_dtype or dtype)
+            v = vs * gather_kv(v_cache_bits, layout, page_indptr, page_indices, b, kh,
+                               int(kv_len[b]), page_size, kv_dtype or dtype)
             for h in range(kh * group, (kh + 1) * group):
                 qh = to_f64(q_bits[q0 + sel, h, :], dtype)
                 o, l = softmax_attention(qh, k, v, sm_scale, vis)
@@ -217,8 +220,8 @@ def batch_attention(q_bits, qo_indptr, k_cache_bits, v_cache_bits, layout: str,
 def batch_decode(q_bits, k_cache_bits, v_cache_bits, layout: str, page_indptr,
                  page_indices, last_page_len, num_qo_heads: int, num_kv_heads: int,
                  page_size: int, sm_scale: float, requests=None, window_left: int = -1,
-                 dtype: str = "bf16", kv_dtype: str | None = None, k_scale: float = 1.0,
-                 v_scale: float = 1.0):
+                 dtype: str = "bf16", kv_dtype: str | None = None, k_scale=1.0,
+                 v_scale=1.0):
     """One query token per request: q_bits ``[B, Hq, d]``; out ``[B, Hq, d]``,
     lse ``[B, Hq]``. Every key of the request is visible, or with a left
     window only the last ``window_left + 1``."""

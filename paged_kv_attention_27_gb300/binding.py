@@ -93,10 +93,11 @@ def lib():
     L.fi_plan_get_info.argtypes = [_P, ctypes.POINTER(PlanInfo)]
     L.fi_plan_get_work.argtypes = [_P, _P, _I32, ctypes.POINTER(_I32)]
     _F = ctypes.c_float
+    # ... sm_scale, k_scale, v_scale, k_head_scale, v_head_scale, out, lse, ...
     L.fi_batch_decode_paged.argtypes = [_P, _P, _P, _P, _I32, _I64, _I32, _P, _P, _P,
-                                        _F, _F, _F, _P, _P, _P, ctypes.c_size_t, _P]
+                                        _F, _F, _F, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]
     L.fi_batch_prefill_paged.argtypes = [_P, _P, _P, _P, _P, _I32, _I64, _I32, _P, _P, _P,
-                                         _F, _F, _F, _P, _P, _P, ctypes.c_size_t, _P]
+                                         _F, _F, _F, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]
     L.fi_merge_states.argtypes = [_P, _P, _I32, _I32, _I32, _I32, _I32, _P, _P, _P]
     L.fi_check_device_status.argtypes = [_P, _P]
     L.fi_status_string.argtypes = [_I32]
@@ -106,9 +107,9 @@ def lib():
     L.fi_debug_set_fault.argtypes = [_I32, _I64]
     L.fi_profile_next_launch.argtypes = [_P, _P]
     L.fi_batch_decode_paged_noalloc.argtypes = [_P, _P, _P, _P, _I32, _I64, _I32, _P, _P, _P,
-                                                _F, _F, _F, _P, _P, _P]
+                                                _F, _F, _F, _P, _P, _P, _P, _P]
     L.fi_batch_attention_host.argtypes = [_P, _P, _P, _P, _P, _I32, _I64, _I32, _P, _P, _P,
-                                          _F, _F, _F, _P, _P, _P, ctypes.c_size_t, _P]
+                                          _F, _F, _F, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]
     for name in EXPORTED:
         if name not in ("fi_status_string", "fi_last_error_string"):
             getattr(L, name).restype = _I32
@@ -221,35 +222,39 @@ def fi_plan_get_work(plan: Plan) -> np.ndarray:
 def fi_batch_decode_paged(plan: Plan, q, k_cache, v_cache, kv_layout, page_stride_elems,
                           num_pages, page_indptr_d, page_indices_d, last_page_len_d, sm_scale,
                           k_scale, v_scale, out, lse, workspace, workspace_bytes=None,
-                          stream=None):
+                          stream=None, k_head_scale=None, v_head_scale=None):
+    """k_head_scale / v_head_scale: device fp32 [num_kv_heads] or None."""
     wsb = plan.workspace_bytes if workspace_bytes is None else workspace_bytes
     st = lib().fi_batch_decode_paged(plan.handle, _ptr(q), _ptr(k_cache), _ptr(v_cache),
                                      int(kv_layout), int(page_stride_elems), int(num_pages),
                                      _ptr(page_indptr_d), _ptr(page_indices_d),
                                      _ptr(last_page_len_d), float(sm_scale), float(k_scale),
-                                     float(v_scale), _ptr(out), _ptr(lse), _ptr(workspace),
-                                     int(wsb), _stream(stream))
+                                     float(v_scale), _ptr(k_head_scale), _ptr(v_head_scale),
+                                     _ptr(out), _ptr(lse), _ptr(workspace), int(wsb),
+                                     _stream(stream))
     _check(st, "fi_batch_decode_paged")
 
 
 def fi_batch_prefill_paged(plan: Plan, q, qo_indptr_d, k_cache, v_cache, kv_layout,
                            page_stride_elems, num_pages, page_indptr_d, page_indices_d,
                            last_page_len_d, sm_scale, k_scale, v_scale, out, lse, workspace,
-                           workspace_bytes=None, stream=None):
+                           workspace_bytes=None, stream=None, k_head_scale=None,
+                           v_head_scale=None):
     wsb = plan.workspace_bytes if workspace_bytes is None else workspace_bytes
     st = lib().fi_batch_prefill_paged(plan.handle, _ptr(q), _ptr(qo_indptr_d), _ptr(k_cache),
                                       _ptr(v_cache), int(kv_layout), int(page_stride_elems),
                                       int(num_pages), _ptr(page_indptr_d), _ptr(page_indices_d),
                                       _ptr(last_page_len_d), float(sm_scale), float(k_scale),
-                                      float(v_scale), _ptr(out), _ptr(lse), _ptr(workspace),
-                                      int(wsb), _stream(stream))
+                                      float(v_scale), _ptr(k_head_scale), _ptr(v_head_scale),
+                                      _ptr(out), _ptr(lse), _ptr(workspace), int(wsb),
+                                      _stream(stream))
     _check(st, "fi_batch_prefill_paged")
 
 
 def fi_batch_attention_host(plan: Plan, q_h, qo_indptr_h, k_cache, v_cache, kv_layout,
                             page_stride_elems, num_pages, page_indptr_h, page_indices_h,
                             last_page_len_h, sm_scale, k_scale, v_scale, out_h, lse_h, workspace,
-                            workspace_bytes, stream=None):
+                            workspace_bytes, stream=None, k_head_scale=None, v_head_scale=None):
     """q_h / out_h / lse_h: host tensors or arrays (page-locked for
     asynchronous copies); the page-table arguments: host int32 arrays;
     the caches and the workspace (workspace_bytes + host_io_bytes of the
@@ -258,7 +263,8 @@ def fi_batch_attention_host(plan: Plan, q_h, qo_indptr_h, k_cache, v_cache, kv_l
                                        _ptr(v_cache), int(kv_layout), int(page_stride_elems),
                                        int(num_pages), _ptr(page_indptr_h), _ptr(page_indices_h),
                                        _ptr(last_page_len_h), float(sm_scale), float(k_scale),
-                                       float(v_scale), _ptr(out_h), _ptr(lse_h), _ptr(workspace),
+                                       float(v_scale), _ptr(k_head_scale), _ptr(v_head_scale),
+                                       _ptr(out_h), _ptr(lse_h), _ptr(workspace),
                                        int(workspace_bytes), _stream(stream))
     _check(st, "fi_batch_attention_host")
 
@@ -287,12 +293,14 @@ def fi_profile_next_launch(start_event, stop_event):
 
 def fi_batch_decode_paged_noalloc(plan: Plan, q, k_cache, v_cache, kv_layout, page_stride_elems,
                                   num_pages, page_indptr_d, page_indices_d, last_page_len_d,
-                                  sm_scale, k_scale, v_scale, out, lse, stream=None):
+                                  sm_scale, k_scale, v_scale, out, lse, stream=None,
+                                  k_head_scale=None, v_head_scale=None):
     """fi_batch_decode_paged with the library's own static scratch (no workspace)."""
     st = lib().fi_batch_decode_paged_noalloc(plan.handle, _ptr(q), _ptr(k_cache), _ptr(v_cache),
                                              int(kv_layout), int(page_stride_elems),
                                              int(num_pages), _ptr(page_indptr_d),
                                              _ptr(page_indices_d), _ptr(last_page_len_d),
                                              float(sm_scale), float(k_scale), float(v_scale),
+                                             _ptr(k_head_scale), _ptr(v_head_scale),
                                              _ptr(out), _ptr(lse), _stream(stream))
     _check(st, "fi_batch_decode_paged_noalloc")

@@ -298,7 +298,8 @@ fi_status run_paged(fi_plan_t plan, bool prefill_call, const void* q, const int3
                     const void* k_cache, const void* v_cache, int32_t kv_layout,
                     int64_t page_stride_elems, int32_t num_pages, const int32_t* page_indptr_d,
                     const int32_t* page_indices_d, const int32_t* last_page_len_d, float sm_scale,
-                    float k_scale, float v_scale, void* out, float* lse, void* workspace,
+                    float k_scale, float v_scale, const float* k_head_scale,
+                    const float* v_head_scale, void* out, float* lse, void* workspace,
                     size_t workspace_bytes, void* stream_ptr, bool static_upload = false) {
   if (!plan) return FI_ERR_INVALID_ARG;
   const fi::Plan& P = plan->p;
@@ -310,7 +311,8 @@ fi_status run_paged(fi_plan_t plan, bool prefill_call, const void* q, const int3
   if (P.total_kv > 0 && (!page_indices_d || num_pages <= 0)) return FI_ERR_INVALID_ARG;
   if (num_pages < 0) return FI_ERR_INVALID_ARG;
   if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16) ||
-      !aligned(workspace, 256) || (lse && !aligned(lse, 4)))
+      !aligned(workspace, 256) || (lse && !aligned(lse, 4)) ||
+      (k_head_scale && !aligned(k_head_scale, 4)) || (v_head_scale && !aligned(v_head_scale, 4)))
     return FI_ERR_INVALID_ARG;
   fi_status st = check_run_scalars(P, kv_layout, page_stride_elems, sm_scale, k_scale, v_scale);
   if (st != FI_OK) return st;
@@ -371,116 +373,125 @@ fi_status run_paged(fi_plan_t plan, bool prefill_call, const void* q, const int3
     if (e != cudaSuccess) return cuda_fail(e, "profiling event");
   }
 
-  // With both kinds of work, the decode kernel (HBM-bound) runs on a side
-  // stream concurrently with the prefill kernel (tensor-bound), which is
-  // launched first (measured faster than the other order or a high-priority
-  // side stream); the streams join at the end. Both kernels read the work
-  // lists uploaded above; split decode work is merged inside the decode
-  // kernel.
-  const bool concurrent = !P.prefill_items.empty() && !P.decode_items.empty();
-  SideStream side;
-  cudaStream_t dstream = stream;
-  if (concurrent) {
-    st = side_stream(&side);
-    if (st != FI_OK) return st;
-    e = cudaEventRecord(side.fork, stream);
-    if (e == cudaSuccess) e = cudaStreamWaitEvent(side.stream, side.fork, 0);
-    if (e != cudaSuccess) return cuda_fail(e, "fork to the side stream");
-    dstream = side.stream;
-  }
-  if (!P.prefill_items.empty()) {
-    fi::PrefillParams pp;
-    pp.items = reinterpret_cast<const fi::WorkItem*>(ws + P.ws.prefill_items);
-    pp.qo_indptr = qo_indptr_d;
-    pp.page_indptr = page_indptr_d;
-    pp.last_page_len = last_page_len_d;
-    pp.page_indices = page_indices_d;
-    pp.num_pages = num_pages;
-    pp.page_size = P.page_size;
-    pp.num_qo_heads = P.num_qo_heads;
-    pp.group = P.num_qo_heads / P.num_kv_heads;
-    pp.pack = 1;
-    pp.layout = kv_layout;
-    pp.causal = P.causal;
-    pp.window_left = P.window_left;
-    pp.sm_scale = sm_scale * k_scale;   // the key scale folds into the score scale
-    pp.v_scale = v_scale;
-    pp.out = out;
-    pp.lse = lse;
-    pp.err = err;
-    pp.wait_limit_ns = wait_limit_ns;
-    pp.fault_kind = fault_kind;
-    pp.n_items = int(P.prefill_items.size());
-    pp.work_counter = reinterpret_cast<uint32_t*>(ws + fi::kWorkCounterOffset);
-    pp.state_o = nullptr;
-    pp.state_lse = nullptr;
-    e = fi::launch_prefill(P.head_dim, P.dtype, qmap, kmap, vmap, pp, P.num_sms, stream);
-    if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
-  }
-  if (!P.prefix_items.empty()) {
-    // Shared prefixes: each group's rows of q against chunks of its prefix,
-    // on the prefill kernel, writing fp32 states (row r of q -> slot
-    // item.slot + r) that the decode kernel merges with the rest. Same
-    // stream, before the decode launch.
-    const int32_t* tables = reinterpret_cast<const int32_t*>(ws + P.ws.prefix_tables);
-    const int G2 = 2 * P.num_prefix_groups;
-    fi::PrefillParams pp;
-    pp.items = reinterpret_cast<const fi::WorkItem*>(ws + P.ws.prefix_items);
-    pp.qo_indptr = tables;
-    pp.page_indptr = tables + G2;
-    pp.last_page_len = tables + 2 * G2;
-    pp.page_indices = page_indices_d;
-    pp.num_pages = num_pages;
-    pp.page_size = P.page_size;
-    pp.num_qo_heads = P.num_qo_heads;
-    pp.group = P.num_qo_heads / P.num_kv_heads;
-    pp.pack = pp.group;
-    pp.layout = kv_layout;
-    pp.causal = 0;
-    pp.window_left = -1;
-    pp.sm_scale = sm_scale * k_scale;
-    pp.v_scale = v_scale;
-    pp.out = nullptr;
-    pp.lse = nullptr;
-    pp.state_o = partial_o;
-    pp.state_lse = partial_lse;
-    pp.err = err;
-    pp.wait_limit_ns = wait_limit_ns;
-    pp.fault_kind = 0;
-    pp.n_items = int(P.prefix_items.size());
-    pp.work_counter = reinterpret_cast<uint32_t*>(ws + fi::kWorkCounterOffset);
-    e = fi::launch_prefill(P.head_dim, P.dtype, qmap, kmap, vmap, pp, P.num_sms, stream);
-    if (e != cudaSuccess) return cuda_fail(e, "shared-prefix launch");
-  }
-  if (!P.decode_items.empty()) {
-    fi::DecodeParams dp;
-    dp.items = reinterpret_cast<const fi::WorkItem*>(ws + P.ws.decode_items);
-    dp.q = q;
-    dp.page_indices = page_indices_d;
-    dp.num_pages = num_pages;
-    dp.page_size = P.page_size;
-    dp.num_qo_heads = P.num_qo_heads;
-    dp.layout = kv_layout;
-    dp.sm_scale = sm_scale * k_scale;   // the key scale folds into the score scale
-    dp.v_scale = v_scale;
-    dp.out = out;
-    dp.lse = lse;
-    dp.partial_o = partial_o;
-    dp.partial_lse = partial_lse;
-    dp.merges = reinterpret_cast<const fi::MergeTask*>(ws + P.ws.merges);
-    dp.merge_counters = reinterpret_cast<uint32_t*>(ws + P.ws.merge_counters);
-    dp.err = err;
-    dp.wait_limit_ns = wait_limit_ns;
-    dp.fault_kind = fault_kind;
-    e = fi::launch_decode(P.head_dim, P.num_qo_heads / P.num_kv_heads, P.dtype, P.kv_dtype, kmap,
-                          vmap, dp,
-                          int(P.decode_items.size()), dstream);
-    if (e != cudaSuccess) return cuda_fail(e, "decode launch");
-  }
-  if (concurrent) {
-    e = cudaEventRecord(side.join, side.stream);
-    if (e == cudaSuccess) e = cudaStreamWaitEvent(stream, side.join, 0);
-    if (e != cudaSuccess) return cuda_fail(e, "join from the side stream");
+  // The launch parameters of the plan's prefill and decode work (both read
+  // the work lists uploaded above).
+  fi::PrefillParams pp;
+  pp.items = reinterpret_cast<const fi::WorkItem*>(ws + P.ws.prefill_items);
+  pp.qo_indptr = qo_indptr_d;
+  pp.page_indptr = page_indptr_d;
+  pp.last_page_len = last_page_len_d;
+  pp.page_indices = page_indices_d;
+  pp.num_pages = num_pages;
+  pp.page_size = P.page_size;
+  pp.num_qo_heads = P.num_qo_heads;
+  pp.group = P.num_qo_heads / P.num_kv_heads;
+  pp.pack = 1;
+  pp.layout = kv_layout;
+  pp.causal = P.causal;
+  pp.window_left = P.window_left;
+  pp.sm_scale = sm_scale * k_scale;   // the key scale folds into the score scale
+  pp.v_scale = v_scale;
+  pp.k_head_scale = k_head_scale;
+  pp.v_head_scale = v_head_scale;
+  pp.out = out;
+  pp.lse = lse;
+  pp.err = err;
+  pp.wait_limit_ns = wait_limit_ns;
+  pp.fault_kind = fault_kind;
+  pp.n_items = int(P.prefill_items.size());
+  pp.work_counter = reinterpret_cast<uint32_t*>(ws + fi::kWorkCounterOffset);
+  pp.state_o = nullptr;
+  pp.state_lse = nullptr;
+
+  fi::DecodeParams dp;
+  dp.items = reinterpret_cast<const fi::WorkItem*>(ws + P.ws.decode_items);
+  dp.q = q;
+  dp.page_indices = page_indices_d;
+  dp.num_pages = num_pages;
+  dp.page_size = P.page_size;
+  dp.num_qo_heads = P.num_qo_heads;
+  dp.layout = kv_layout;
+  dp.sm_scale = sm_scale * k_scale;   // the key scale folds into the score scale
+  dp.v_scale = v_scale;
+  dp.k_head_scale = k_head_scale;
+  dp.v_head_scale = v_head_scale;
+  dp.out = out;
+  dp.lse = lse;
+  dp.partial_o = partial_o;
+  dp.partial_lse = partial_lse;
+  dp.merges = reinterpret_cast<const fi::MergeTask*>(ws + P.ws.merges);
+  dp.merge_counters = reinterpret_cast<uint32_t*>(ws + P.ws.merge_counters);
+  dp.err = err;
+  dp.wait_limit_ns = wait_limit_ns;
+  dp.fault_kind = fault_kind;
+
+  const int group = P.num_qo_heads / P.num_kv_heads;
+  const bool both = !P.prefill_items.empty() && !P.decode_items.empty();
+  if (both && P.prefix_items.empty() &&
+      fi::mixed_applies(P.head_dim, group, P.dtype, P.kv_dtype)) {
+    // Chunked prefill and decode rows in one persistent launch: every CTA
+    // runs prefill items on its tensor-core warps and decode items on its
+    // decode warps, each side taking work from its own counter, so the
+    // HBM-bound decode streams overlap the tensor-bound prefill tiles on
+    // the same SMs.
+    e = fi::launch_mixed(P.head_dim, group, P.dtype, qmap, kmap, vmap, pp, dp,
+                         int(P.decode_items.size()),
+                         reinterpret_cast<uint32_t*>(ws + fi::kDecodeCounterOffset), P.num_sms,
+                         stream);
+    if (e != cudaSuccess) return cuda_fail(e, "mixed launch");
+  } else {
+    // Otherwise, with both kinds of work, the decode kernel (HBM-bound) runs
+    // on a side stream concurrently with the prefill kernel (tensor-bound),
+    // which is launched first; the streams join at the end. Split decode
+    // work is merged inside the decode kernel.
+    SideStream side;
+    cudaStream_t dstream = stream;
+    if (both) {
+      st = side_stream(&side);
+      if (st != FI_OK) return st;
+      e = cudaEventRecord(side.fork, stream);
+      if (e == cudaSuccess) e = cudaStreamWaitEvent(side.stream, side.fork, 0);
+      if (e != cudaSuccess) return cuda_fail(e, "fork to the side stream");
+      dstream = side.stream;
+    }
+    if (!P.prefill_items.empty()) {
+      e = fi::launch_prefill(P.head_dim, P.dtype, qmap, kmap, vmap, pp, P.num_sms, stream);
+      if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
+    }
+    if (!P.prefix_items.empty()) {
+      // Shared prefixes: each group's rows of q against chunks of its prefix,
+      // on the prefill kernel, writing fp32 states (row r of q -> slot
+      // item.slot + r) that the decode kernel merges with the rest. Same
+      // stream, before the decode launch.
+      const int32_t* tables = reinterpret_cast<const int32_t*>(ws + P.ws.prefix_tables);
+      const int G2 = 2 * P.num_prefix_groups;
+      fi::PrefillParams xp = pp;
+      xp.items = reinterpret_cast<const fi::WorkItem*>(ws + P.ws.prefix_items);
+      xp.qo_indptr = tables;
+      xp.page_indptr = tables + G2;
+      xp.last_page_len = tables + 2 * G2;
+      xp.pack = xp.group;
+      xp.causal = 0;
+      xp.window_left = -1;
+      xp.out = nullptr;
+      xp.lse = nullptr;
+      xp.state_o = partial_o;
+      xp.state_lse = partial_lse;
+      xp.fault_kind = 0;
+      xp.n_items = int(P.prefix_items.size());
+      e = fi::launch_prefill(P.head_dim, P.dtype, qmap, kmap, vmap, xp, P.num_sms, stream);
+      if (e != cudaSuccess) return cuda_fail(e, "shared-prefix launch");
+    }
+    if (!P.decode_items.empty()) {
+      e = fi::launch_decode(P.head_dim, group, P.dtype, P.kv_dtype, kmap, vmap, dp,
+                            int(P.decode_items.size()), dstream);
+      if (e != cudaSuccess) return cuda_fail(e, "decode launch");
+    }
+    if (both) {
+      e = cudaEventRecord(side.join, side.stream);
+      if (e == cudaSuccess) e = cudaStreamWaitEvent(stream, side.join, 0);
+      if (e != cudaSuccess) return cuda_fail(e, "join from the side stream");
+    }
   }
   if (prof_stop) {
     e = cudaEventRecord(prof_stop, stream);
@@ -495,10 +506,13 @@ fi_status fi::run_decode_static_upload(
     fi_plan_t plan, const void* q, const void* k_cache, const void* v_cache, int32_t kv_layout,
     int64_t page_stride_elems, int32_t num_pages, const int32_t* page_indptr_d,
     const int32_t* page_indices_d, const int32_t* last_page_len_d, float sm_scale, float k_scale,
-    float v_scale, void* out, float* lse, void* workspace, size_t workspace_bytes, void* stream) {
+    float v_scale, const float* k_head_scale,
+    const float* v_head_scale, void* out, float* lse, void* workspace, size_t workspace_bytes,
+    void* stream) {
   return run_paged(plan, false, q, nullptr, k_cache, v_cache, kv_layout, page_stride_elems,
                    num_pages, page_indptr_d, page_indices_d, last_page_len_d, sm_scale, k_scale,
-                   v_scale, out, lse, workspace, workspace_bytes, stream, true);
+                   v_scale, k_head_scale, v_head_scale, out, lse, workspace, workspace_bytes,
+                   stream, true);
 }
 
 extern "C" {
@@ -576,11 +590,13 @@ fi_status fi_batch_decode_paged(fi_plan_t plan, const void* q, const void* k_cac
                                 int64_t page_stride_elems, int32_t num_pages,
                                 const int32_t* page_indptr_d, const int32_t* page_indices_d,
                                 const int32_t* last_page_len_d, float sm_scale, float k_scale,
-                                float v_scale, void* out, float* lse, void* workspace,
+                                float v_scale, const float* k_head_scale,
+                                const float* v_head_scale, void* out, float* lse, void* workspace,
                                 size_t workspace_bytes, void* stream) {
   return run_paged(plan, false, q, nullptr, k_cache, v_cache, kv_layout, page_stride_elems,
                    num_pages, page_indptr_d, page_indices_d, last_page_len_d, sm_scale, k_scale,
-                   v_scale, out, lse, workspace, workspace_bytes, stream);
+                   v_scale, k_head_scale, v_head_scale, out, lse, workspace, workspace_bytes,
+                   stream);
 }
 
 fi_status fi_batch_prefill_paged(fi_plan_t plan, const void* q, const int32_t* qo_indptr_d,
@@ -588,11 +604,13 @@ fi_status fi_batch_prefill_paged(fi_plan_t plan, const void* q, const int32_t* q
                                  int64_t page_stride_elems, int32_t num_pages,
                                  const int32_t* page_indptr_d, const int32_t* page_indices_d,
                                  const int32_t* last_page_len_d, float sm_scale, float k_scale,
-                                 float v_scale, void* out, float* lse, void* workspace,
+                                 float v_scale, const float* k_head_scale,
+                                 const float* v_head_scale, void* out, float* lse, void* workspace,
                                  size_t workspace_bytes, void* stream) {
   return run_paged(plan, true, q, qo_indptr_d, k_cache, v_cache, kv_layout, page_stride_elems,
                    num_pages, page_indptr_d, page_indices_d, last_page_len_d, sm_scale, k_scale,
-                   v_scale, out, lse, workspace, workspace_bytes, stream);
+                   v_scale, k_head_scale, v_head_scale, out, lse, workspace, workspace_bytes,
+                   stream);
 }
 
 fi_status fi_batch_attention_host(fi_plan_t plan, const void* q_h, const int32_t* qo_indptr_h,
@@ -600,7 +618,8 @@ fi_status fi_batch_attention_host(fi_plan_t plan, const void* q_h, const int32_t
                                   int64_t page_stride_elems, int32_t num_pages,
                                   const int32_t* page_indptr_h, const int32_t* page_indices_h,
                                   const int32_t* last_page_len_h, float sm_scale, float k_scale,
-                                  float v_scale, void* out_h, float* lse_h, void* workspace,
+                                  float v_scale, const float* k_head_scale,
+                                  const float* v_head_scale, void* out_h, float* lse_h, void* workspace,
                                   size_t workspace_bytes, void* stream_ptr) {
   if (!plan) return FI_ERR_INVALID_ARG;
   const fi::Plan& P = plan->p;
@@ -651,7 +670,8 @@ fi_status fi_batch_attention_host(fi_plan_t plan, const void* q_h, const int32_t
   float* lse_d = lse_h ? reinterpret_cast<float*>(ws + P.ws.hio_lse) : nullptr;
   st = run_paged(plan, prefill, ws + P.ws.hio_q, qo_d, k_cache, v_cache, kv_layout,
                  page_stride_elems, num_pages, indptr_d, indices_d, last_d, sm_scale, k_scale,
-                 v_scale, out_d, lse_d, workspace, P.ws.total, stream_ptr);
+                 v_scale, k_head_scale, v_head_scale, out_d, lse_d, workspace, P.ws.total,
+                 stream_ptr);
   if (st != FI_OK) return st;
   e = cudaMemcpyAsync(out_h, out_d, q_bytes, cudaMemcpyDeviceToHost, stream);
   if (e == cudaSuccess && lse_h)

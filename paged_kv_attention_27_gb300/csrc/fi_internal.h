@@ -49,6 +49,7 @@ struct MergeTask {
 constexpr int kPrefillTileM = 128;         // query rows per prefill CTA
 constexpr size_t kHeaderBytes = 256;       // device error word, work counter, reserved
 constexpr size_t kWorkCounterOffset = 64;  // prefill items handed out (zeroed by the upload)
+constexpr size_t kDecodeCounterOffset = 128;  // decode items handed out by the mixed kernel
 constexpr size_t kAlign = 256;
 
 // Error bits in the first word of the workspace.
@@ -107,7 +108,8 @@ fi_status run_decode_static_upload(fi_plan_t plan, const void* q, const void* k_
                                    int64_t page_stride_elems, int32_t num_pages,
                                    const int32_t* page_indptr_d, const int32_t* page_indices_d,
                                    const int32_t* last_page_len_d, float sm_scale,
-                                   float k_scale, float v_scale, void* out, float* lse,
+                                   float k_scale, float v_scale, const float* k_head_scale,
+                                   const float* v_head_scale, void* out, float* lse,
                                    void* workspace, size_t workspace_bytes, void* stream);
 
 // plan.cpp

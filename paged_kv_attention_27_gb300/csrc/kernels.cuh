@@ -20,6 +20,8 @@ struct DecodeParams {
   int32_t layout;
   float sm_scale;           // times the cache's key scale
   float v_scale;            // the cache's value scale, applied to every output state
+  const float* k_head_scale;  // [num_kv_heads] factors on sm_scale, or null (all 1)
+  const float* v_head_scale;  // [num_kv_heads] factors on v_scale, or null (all 1)
   void* out;
   float* lse;
   float* partial_o;
@@ -62,6 +64,8 @@ struct PrefillParams {
   int32_t window_left;  // -1: none; else row at key position pos keeps t >= pos - window_left
   float sm_scale;       // times the cache's key scale
   float v_scale;        // the cache's value scale
+  const float* k_head_scale;  // [num_kv_heads] factors on sm_scale, or null (all 1)
+  const float* v_head_scale;  // [num_kv_heads] factors on v_scale, or null (all 1)
   void* out;
   float* lse;
   // when set, each row's state goes here instead of out / lse: fp32
@@ -87,6 +91,16 @@ bool prefill_pair_applies(int head_dim, const PrefillParams& p);
 cudaError_t launch_prefill_pair(int head_dim, int dtype, const CUtensorMap& qm,
                                 const CUtensorMap& km, const CUtensorMap& vm,
                                 const PrefillParams& p, int grid, cudaStream_t stream);
+// One persistent launch over a mixed batch (prefill.cu): the prefill items
+// `p` as launch_prefill runs them (one-tile kernel) and, on other warps of
+// the same CTAs, the decode items `dp` (n_dec of them), taken from
+// *dec_counter (zero before the launch). Applies to head_dim 256 with 1, 2
+// or 4 query heads per kv head and a 16-bit cache (mixed_applies).
+bool mixed_applies(int head_dim, int group, int dtype, int kv_dtype);
+cudaError_t launch_mixed(int head_dim, int group, int dtype, const CUtensorMap& qm,
+                         const CUtensorMap& km, const CUtensorMap& vm, const PrefillParams& p,
+                         const DecodeParams& dp, int n_dec, uint32_t* dec_counter, int grid,
+                         cudaStream_t stream);
 // `dtype` (fi_dtype) selects the element type of q and out, `kv_dtype` that
 // of the cache (dtype or FI_DTYPE_E4M3).
 cudaError_t launch_decode(int head_dim, int group, int dtype, int kv_dtype, const CUtensorMap& km,

@@ -52,7 +52,8 @@ extern "C" fi_status fi_batch_decode_paged_noalloc(
     fi_plan_t plan, const void* q, const void* k_cache, const void* v_cache, int32_t kv_layout,
     int64_t page_stride_elems, int32_t num_pages, const int32_t* page_indptr_d,
     const int32_t* page_indices_d, const int32_t* last_page_len_d, float sm_scale, float k_scale,
-    float v_scale, void* out, float* lse, void* stream) {
+    float v_scale, const float* k_head_scale,
+    const float* v_head_scale, void* out, float* lse, void* stream) {
   if (!plan) return FI_ERR_INVALID_ARG;
   if (plan->p.ws.total > fi::kNoAllocScratchBytes) return FI_ERR_WORKSPACE_TOO_SMALL;
   int dev = -1;
@@ -83,6 +84,7 @@ extern "C" fi_status fi_batch_decode_paged_noalloc(
   }
   return fi::run_decode_static_upload(plan, q, k_cache, v_cache, kv_layout, page_stride_elems,
                                       num_pages, page_indptr_d, page_indices_d, last_page_len_d,
-                                      sm_scale, k_scale, v_scale, out, lse, scratch,
+                                      sm_scale, k_scale, v_scale, k_head_scale, v_head_scale,
+                                      out, lse, scratch,
                                       fi::kNoAllocScratchBytes, stream);
 }

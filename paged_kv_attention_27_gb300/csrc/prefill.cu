@@ -37,6 +37,7 @@
 // Fully masked KV tiles are never visited: the planner clips tok_end.
 #include <climits>
 
+#include "decode_roles.cuh"
 #include "elem.cuh"
 #include "fi_internal.h"
 #include "kernels.cuh"
@@ -52,22 +53,44 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;   // log2 units: rescale when the max grows by > 2^8
 
-template <int HEAD_DIM, class E>
+// DG > 0: the mixed kernel, which also runs batch decode (groups of DG query
+// heads per kv head) on warps 7 and up of the same CTA.
+template <int HEAD_DIM, class E, int DG = 0>
 struct PrefillCfg {
   static constexpr int M = kPrefillTileM;                   // 128 query rows
   static constexpr int N = HEAD_DIM <= 128 ? 128 : 64;      // KV tokens per tile
   static constexpr int DBLK = HEAD_DIM / 64;                // 128-byte slices of a row
-  static constexpr int THREADS = 224;     // 4 softmax warps, K producer, MMA issuer, V producer
+  static constexpr bool MIXED = DG > 0;
+  using DC = DecodeCfg<HEAD_DIM, (DG > 0 ? DG : 1), 2>;
+  // 4 softmax warps, K producer, MMA issuer, V producer; the mixed kernel
+  // adds a decode producer (warp 7) and the decode consumer warps (from 8 on:
+  // four on CUDA cores, or two driving m16n8k16 MMAs)
+  static constexpr int THREADS = MIXED ? 256 + 32 * DC::NCW : 224;
   // d = 256 leaves no TMEM columns for P: P of tile g is written over its
   // S buffer (g & 1), which the MMA issuer then frees after that tile's PV
   static constexpr bool P_IN_S = HEAD_DIM > 128;
   static constexpr int NST = HEAD_DIM <= 128 ? 3 : 2;       // K (and V) ring depth
   static constexpr int Q_BYTES = DBLK * M * 128;
   static constexpr int KV_BYTES = DBLK * N * 128;           // one K (or V) tile
+  // The mixed kernel stages each item's Q through two slots of the K ring
+  // (the K producer loads it there, the softmax warps copy it into TMEM and
+  // the MMA issuer frees the slots), which leaves room for the decode ring.
+  static constexpr bool Q_IN_RING = MIXED;
+  static_assert(!Q_IN_RING || Q_BYTES == 2 * KV_BYTES, "Q fills two K-ring slots");
   static constexpr int OFF_Q = 0;
-  static constexpr int OFF_K = OFF_Q + Q_BYTES;
+  static constexpr int OFF_K = OFF_Q + (Q_IN_RING ? 0 : Q_BYTES);
   static constexpr int OFF_V = OFF_K + NST * KV_BYTES;
-  static constexpr int USED = OFF_V + NST * KV_BYTES;
+  static constexpr int OFF_DEC = OFF_V + NST * KV_BYTES;    // decode ring (mixed kernel)
+  static constexpr int USED = OFF_DEC + (MIXED ? DC::NSTAGE * DC::STAGE_BYTES : 0);
+  // mixed kernel: the softmax warpgroup raises its registers to 224 per
+  // thread, the helper warpgroup (prefill producers, MMA issuer, decode
+  // producer) lowers them to 56, the decode consumers keep the launch count
+  // R. The shares fit the launch allocation when 128 x (224 + 56) <= 256 x R
+  // (R >= 140; the compiler's cap is 168 for 384 threads, 200 for 320); the
+  // host checks the compiled R before the launch.
+  static constexpr uint32_t SOFTMAX_REGS = 224, HELPER_REGS = 56;
+  static constexpr uint32_t MIN_LAUNCH_REGS = (128 * (SOFTMAX_REGS + HELPER_REGS) + 255) / 256;
+  static_assert(!MIXED || HEAD_DIM == 256, "mixed kernel: head_dim 256");
   // keep one CTA per SM (each CTA takes all 512 TMEM columns)
   static constexpr int SMEM_BYTES = (USED < 120 * 1024 ? 120 * 1024 : USED) + 1024;
   static constexpr uint32_t TMEM_COLS = 512;
@@ -85,7 +108,7 @@ struct PrefillCfg {
 
 constexpr int kItemRing = 8;   // item indices handed from the K producer to the other roles
 
-template <int NST>
+template <int NST, int DNST>
 struct PrefillBarriers {
   uint64_t item_full[kItemRing], item_empty[kItemRing];
   uint64_t q_full, q_tmem;
@@ -93,12 +116,13 @@ struct PrefillBarriers {
   uint64_t v_full[NST], v_empty[NST];
   uint64_t s_full[2], s_free[2];
   uint64_t p_full, pv_done, o_final, drain;
+  // mixed kernel: the decode ring and the decode items handed from the
+  // decode producer to the decode consumers
+  uint64_t d_full[DNST], d_empty[DNST];
+  uint64_t ditem_full[kItemRing], ditem_empty[kItemRing];
 };
 
 
-__device__ __forceinline__ uint32_t swz(int r, int c8) {
-  return uint32_t(r * 128 + ((c8 ^ (r & 7)) << 4));
-}
 
 
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
@@ -114,16 +138,23 @@ __device__ __forceinline__ int item_tiles(const WorkItem& w) {
   return (w.tok_end - w.tok_begin + N - 1) / N;
 }
 
-template <int HEAD_DIM, class E>
-__global__ void __launch_bounds__(PrefillCfg<HEAD_DIM, E>::THREADS, 1)
-prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant__ CUtensorMap k_map,
-               const __grid_constant__ CUtensorMap v_map, PrefillParams prm) {
-  using C = PrefillCfg<HEAD_DIM, E>;
+// The kernel body, shared by prefill_kernel (DG = 0) and mixed_kernel
+// (DG > 0: decode work items dprm.items[0 .. n_dec) run on warps 7 and up of the
+// same CTAs, taken from *dec_counter).
+template <int HEAD_DIM, class E, int DG>
+__device__ __forceinline__ void prefill_body(const CUtensorMap& q_map, const CUtensorMap& k_map,
+                                             const CUtensorMap& v_map, const PrefillParams& prm,
+                                             const DecodeParams& dprm, int n_dec,
+                                             uint32_t* dec_counter) {
+  using C = PrefillCfg<HEAD_DIM, E, DG>;
+  using DC = typename C::DC;
   extern __shared__ uint8_t smem_raw[];
-  __shared__ __align__(8) PrefillBarriers<C::NST> bars;
+  __shared__ __align__(8) PrefillBarriers<C::NST, C::MIXED ? DC::NSTAGE : 1> bars;
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_flag;
   __shared__ int item_ring[kItemRing];
+  __shared__ int ditem_ring[C::MIXED ? kItemRing : 1];
+  __shared__ int dec_merge_last;
 
   const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
   const int warp = threadIdx.x >> 5;
@@ -170,6 +201,16 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
     mbar_init(smem_u32(&bars.pv_done), 1);
     mbar_init(smem_u32(&bars.o_final), 1);
     mbar_init(smem_u32(&bars.drain), 1);
+    if constexpr (C::MIXED) {
+      for (int s = 0; s < DC::NSTAGE; ++s) {
+        mbar_init(smem_u32(&bars.d_full[s]), 1);
+        mbar_init(smem_u32(&bars.d_empty[s]), DC::NCW);
+      }
+      for (int s = 0; s < kItemRing; ++s) {
+        mbar_init(smem_u32(&bars.ditem_full[s]), 1);
+        mbar_init(smem_u32(&bars.ditem_empty[s]), DC::NCW);
+      }
+    }
     abort_flag = 0;
     fence_barrier_init();
   }
@@ -181,226 +222,24 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_base_sh;
-  int issued = 0;   // producers: KV tiles whose copies this warp has issued
-  int q_loads = 0;  // K producer: Q tiles it has loaded
+  int issued = 0;    // producers: ring positions whose copies this warp has issued
+  int q_loads = 0;   // K producer: Q tiles it has loaded (Q outside the K ring)
+  int skip_pos = -1; // K producer: the ring position the test hook left unloaded
 
-  if (warp == 4 || warp == 6) {
-    // ------------------------------------------------------------ producers
-    // Warp 4 loads Q and the K tiles, warp 6 the V tiles: each page needs one
-    // TMA instruction per 64-dim slice, and their issue, not the bytes,
-    // bounded a single producer warp. Copies run ahead across item
-    // boundaries: the next item's Q and first tiles load while the current
-    // item is still computing.
-    const bool is_v = warp == 6;
-    if (lane == 0) {
-      prefetch_tensormap(is_v ? &v_map : &k_map);
-      if (!is_v) prefetch_tensormap(&q_map);
-    }
-    const CUtensorMap* map = is_v ? &v_map : &k_map;
-    uint64_t* full = is_v ? bars.v_full : bars.k_full;
-    uint64_t* empty = is_v ? bars.v_empty : bars.k_empty;
-    const uint32_t ring = base + (is_v ? C::OFF_V : C::OFF_K);
-    const int P = prm.page_size;
-    const int ppt = C::N / P;
-    const uint32_t box = uint32_t(P) * 128u;
-    auto pages_in = [&](const WorkItem& w, int j) {
-      return (min(C::N, w.tok_end - w.tok_begin - j * C::N) + P - 1) / P;
-    };
-    bool ok = true;
-    int g = 0;
-    // K producer, lane 0: publish item n's index in the ring (-1: no more)
-    auto publish = [&](int n, int value) {
-      if (n >= kItemRing &&
-          !mbar_wait_bounded(smem_u32(&bars.item_empty[n % kItemRing]),
-                             ((n / kItemRing) & 1) ^ 1, limit, &abort_flag))
-        return false;
-      item_ring[n % kItemRing] = value;
-      mbar_arrive(smem_u32(&bars.item_full[n % kItemRing]));   // release: the index is visible
-      return true;
-    };
-    // index of item 0 (both producers)
-    int it = blockIdx.x;
-    if (is_v) {
-      int v = -1;
-      if (lane == 0) {
-        ok = item_at(0, v);
-        item_done(0);
-      }
-      ok = __shfl_sync(0xffffffffu, ok, 0);
-      it = __shfl_sync(0xffffffffu, v, 0);
-    } else if (lane == 0) {
-      ok = publish(0, it);
-    }
-    ok = __shfl_sync(0xffffffffu, ok, 0);
-    WorkItem w;
-    if (ok && it >= 0) w = prm.items[it];
-    // page ids of the next tile are loaded while the current tile's copies
-    // are issued, so the dependent global load is off the critical path
-    int next_page = -1;
-    if (ok && it >= 0 && item_tiles<C::N>(w) > 0 && lane < pages_in(w, 0))
-      next_page = prm.page_indices[w.page_begin + lane];
-    for (int n = 0; ok && it >= 0; ++n) {
-      const int nt = item_tiles<C::N>(w);
-      const int kv_head = w.head * prm.pack / prm.group;
-      const int c1 = prm.layout == FI_LAYOUT_NHD ? kv_head : 0;
-      const int c2 = prm.layout == FI_LAYOUT_NHD ? 0 : kv_head;
-      // the next item: taken from the counter and published by the K
-      // producer, read from the ring by the V producer
-      int it_next = -1;
-      if (lane == 0) {
-        if (is_v) {
-          ok = item_at(n + 1, it_next);
-          item_done(n + 1);
-        } else {
-          it_next = int(gridDim.x + atomicAdd(prm.work_counter, 1u));
-          if (it_next >= n_items) it_next = -1;
-          ok = publish(n + 1, it_next);
-        }
-      }
-      ok = __shfl_sync(0xffffffffu, ok, 0);
-      it_next = __shfl_sync(0xffffffffu, it_next, 0);
-      if (!ok) break;
-      WorkItem wn;
-      if (it_next >= 0) wn = prm.items[it_next];
-      if (!is_v) {
-        // Q of item n, once the buffer is free: its previous contents have
-        // been copied into TMEM
-        if (n >= 1) {
-          ok = mbar_wait_warp(smem_u32(&bars.q_tmem), (n - 1) & 1, limit, &abort_flag);
-          if (!ok) break;
-        }
-        if (lane == 0) {
-          const uint32_t qb = smem_u32(&bars.q_full);
-          mbar_arrive_expect_tx(qb, C::Q_BYTES);
-#pragma unroll
-          for (int c = 0; c < C::DBLK; ++c)
-            // 128 M rows = (128 / pack rows of q) x (pack heads), heads inner
-            tma_load_3d(base + C::OFF_Q + c * C::M * 128, &q_map, qb, c * 64, w.head * prm.pack,
-                        w.q_row);
-        }
-        q_loads = n + 1;
-      }
-      for (int j = 0; j < nt; ++j, ++g) {
-        const int st = g % C::NST;
-        const int np = pages_in(w, j);
-        int page = -1;
-        bool valid = false;
-        if (lane < np) {
-          page = next_page;
-          valid = page >= 0 && page < prm.num_pages;
-          if (!valid && !is_v) atomicOr(prm.err, kErrBounds);
-        }
-        if (j + 1 < nt) {
-          if (lane < pages_in(w, j + 1))
-            next_page = prm.page_indices[w.page_begin + (j + 1) * ppt + lane];
-        } else if (it_next >= 0 && item_tiles<C::N>(wn) > 0 && lane < pages_in(wn, 0)) {
-          next_page = prm.page_indices[wn.page_begin + lane];
-        }
-        const uint32_t bytes =
-            uint32_t(__popc(__ballot_sync(0xffffffffu, valid))) * C::DBLK * box;
-        if (g >= C::NST && !mbar_wait_warp(smem_u32(&empty[st]), ((g / C::NST) & 1) ^ 1,
-                                           limit, &abort_flag)) {
-          ok = false;
-          break;
-        }
-        const uint32_t fb = smem_u32(&full[st]);
-        const bool skip = !is_v && g == 0 && prm.fault_kind == 1 && blockIdx.x == 0;
-        if (lane == 0 && !skip) mbar_arrive_expect_tx(fb, bytes);
-        __syncwarp();
-        if (valid && !skip) {
-          const uint32_t dst = ring + st * C::KV_BYTES + lane * box;
-#pragma unroll
-          for (int c = 0; c < C::DBLK; ++c)
-            tma_load_4d(dst + c * C::N * 128, map, fb, c * 64, c1, c2, page);
-        }
-        issued = g + 1;
-      }
-      if (nt == 0 && it_next >= 0 && item_tiles<C::N>(wn) > 0 && lane < pages_in(wn, 0))
-        next_page = prm.page_indices[wn.page_begin + lane];
-      w = wn;
-      it = it_next;
-    }
-    if (!ok && lane == 0) { abort_flag = 1; atomicOr(prm.err, kErrTimeout); }
-    __syncwarp();
-  } else if (warp == 5) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      // descriptors are linear in the address field (bits 0-13 = addr >> 4),
-      // so each MMA's descriptor is a base plus a compile-time offset
-      const uint64_t kd0 = sdesc_sw128(base + C::OFF_K, 16, 1024);
-      const uint64_t vd0 = sdesc_sw128(base + C::OFF_V, C::N * 128, 1024);
-      bool ok = true;
-      int g = 0;   // KV tiles of earlier items
-      for (int n = 0; ok; ++n) {
-        int it = -1;
-        ok = item_at(n, it);
-        item_done(n);
-        if (!ok || it < 0) break;
-        const int nt = item_tiles<C::N>(prm.items[it]);
-        ok = mbar_wait_bounded(smem_u32(&bars.q_tmem), n & 1, limit, &abort_flag);
-        for (int j = 0; ok && j <= nt; ++j) {
-          if (j < nt) {
-            const int gq = g + j, st = gq % C::NST, sb = gq & 1;
-            ok = mbar_wait_bounded(smem_u32(&bars.k_full[st]), (gq / C::NST) & 1, limit,
-                                   &abort_flag);
-            if (ok && gq >= 2)
-              ok = mbar_wait_bounded(smem_u32(&bars.s_free[sb]), ((gq >> 1) & 1) ^ 1, limit,
-                                     &abort_flag);
-            if (!ok) break;
-            tc_fence_after();
-            const uint64_t kd = kd0 + uint64_t((st * C::KV_BYTES) >> 4);
-            const uint32_t s_col = tmem + C::COL_S + sb * C::N;
-#pragma unroll
-            for (int k = 0; k < HEAD_DIM / 16; ++k) {
-              const uint64_t bd = kd + uint64_t(((k >> 2) * C::N * 128 + (k & 3) * 32) >> 4);
-              tc_mma_ts(s_col, tmem + C::COL_Q + k * 8, bd, C::IDESC_QK, k > 0 ? 1u : 0u);
-            }
-            tc_commit(smem_u32(&bars.s_full[sb]));
-            tc_commit(smem_u32(&bars.k_empty[st]));
-          }
-          if (j >= 1) {
-            const int gp = g + j - 1, st = gp % C::NST;
-            ok = mbar_wait_bounded(smem_u32(&bars.p_full), gp & 1, limit, &abort_flag);
-            if (ok)
-              ok = mbar_wait_bounded(smem_u32(&bars.v_full[st]), (gp / C::NST) & 1, limit,
-                                     &abort_flag);
-            if (!ok) break;
-            tc_fence_after();
-            const uint64_t vd = vd0 + uint64_t((st * C::KV_BYTES) >> 4);
-#pragma unroll
-            for (int k = 0; k < C::N / 16; ++k) {
-              // MN-major V: 16 tokens per step; the next 64 dims one K-tile slice further
-              const uint64_t bd = vd + uint64_t((k * 16 * 128) >> 4);
-              const uint32_t p_col = C::P_IN_S ? C::COL_S + (gp & 1) * C::N : C::COL_P;
-              tc_mma_ts(tmem + C::COL_O, tmem + p_col + k * 8, bd, C::IDESC_PV,
-                        (j > 1 || k > 0) ? 1u : 0u);
-            }
-            tc_commit(smem_u32(&bars.v_empty[st]));
-            tc_commit(smem_u32(&bars.pv_done));
-            if (C::P_IN_S) tc_commit(smem_u32(&bars.s_free[gp & 1]));
-          }
-        }
-        if (!ok) break;
-        tc_commit(smem_u32(&bars.o_final));
-        g += nt;
-      }
-      if (!ok) {
-        abort_flag = 1;
-        atomicOr(prm.err, kErrTimeout);
-        // every MMA issued so far completes before the TMEM is released
-        tc_commit(smem_u32(&bars.drain));
-        mbar_wait_bounded(smem_u32(&bars.drain), 0, limit, nullptr);
-      }
-    }
-    __syncwarp();
-  } else {
+  // Role dispatch by warpgroup; in the mixed kernel each warpgroup sets its
+  // register share first (one setmaxnreg per warpgroup, so that every code
+  // path after it stays within that share): warps 0-3 compute the softmax of
+  // whole rows, the helpers (warps 4-7) need few registers, the decode
+  // consumers (warps 8 on) keep the launch count.
+  if (warp < 4) {
+    if constexpr (C::MIXED) setmaxnreg_inc<C::SOFTMAX_REGS>();
     // ------------------------------------------------------------ softmax + epilogue
     const int t = threadIdx.x;                       // M row of the tile = TMEM lane
     const uint32_t lane_off = uint32_t(warp * 32) << 16;
     // M row t holds query head head * pack + t % pack of q row q_row + t / pack
     // (pack > 1: heads of one kv head sharing every K/V tile)
     const int t_row = t / prm.pack, t_head = t % prm.pack;
-    const float scale = prm.sm_scale * kLog2e;
+    const float scale0 = prm.sm_scale * kLog2e;
     // Row bounds of item w for this thread's row: the last key it may see
     // (causal bound, clipped to the keys), the first (left window; INT_MIN:
     // none) and the end of the request's rows.
@@ -419,14 +258,28 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
     };
     // Q of item n: from the swizzled TMA tile into this thread's TMEM lane
     // (16-bit pairs), then one arrival per warp on q_tmem.
-    auto copy_q = [&](int n) {
-      if (!mbar_wait_warp(smem_u32(&bars.q_full), n & 1, limit, &abort_flag)) return false;
+    // (Q staged in the K ring: its slots are at K-ring positions kq, kq + 1,
+    // 64-dim slices 2h and 2h + 1 in slot h.)
+    auto copy_q = [&](int n, int kq) {
+      if constexpr (C::Q_IN_RING) {
+        if (!mbar_wait_warp(smem_u32(&bars.k_full[kq % C::NST]), (kq / C::NST) & 1, limit,
+                            &abort_flag) ||
+            !mbar_wait_warp(smem_u32(&bars.k_full[(kq + 1) % C::NST]), ((kq + 1) / C::NST) & 1,
+                            limit, &abort_flag))
+          return false;
+      } else {
+        if (!mbar_wait_warp(smem_u32(&bars.q_full), n & 1, limit, &abort_flag)) return false;
+      }
 #pragma unroll
       for (int b = 0; b < C::DBLK; ++b) {
         uint32_t r[32];
+        const uint32_t slice =
+            C::Q_IN_RING ? base + C::OFF_K + ((kq + b / 2) % C::NST) * C::KV_BYTES +
+                               (b % 2) * C::M * 128
+                         : base + C::OFF_Q + b * C::M * 128;
 #pragma unroll
         for (int c8 = 0; c8 < 8; ++c8) {
-          const uint4 v = lds128(base + C::OFF_Q + b * C::M * 128 + swz(t, c8));
+          const uint4 v = lds128(slice + swz(t, c8));
           r[c8 * 4 + 0] = v.x;
           r[c8 * 4 + 1] = v.y;
           r[c8 * 4 + 2] = v.z;
@@ -452,7 +305,8 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
       idx = __shfl_sync(0xffffffffu, v, 0);
       return __shfl_sync(0xffffffffu, good, 0) != 0;
     };
-    int g = 0;   // KV tiles of earlier items
+    int g = 0;    // KV tiles of earlier items
+    int kq = 0;   // K-ring position of the current item's Q (Q staged in the K ring)
     int it = -1;
     bool ok = take_item(0, it);
     WorkItem w;
@@ -460,10 +314,15 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
     if (ok && it >= 0) {
       w = prm.items[it];
       rb = bounds_of(w);
-      ok = copy_q(0);
+      ok = copy_q(0, 0);
     }
     for (int n = 0; ok && it >= 0; ++n) {
       const int nt = item_tiles<C::N>(w);
+      // this item's kv head: its key scale joins the score scale, its value
+      // scale the output
+      const int kv_head = w.head * prm.pack / prm.group;
+      const float scale = scale0 * (prm.k_head_scale ? prm.k_head_scale[kv_head] : 1.f);
+      const float v_scale = prm.v_scale * (prm.v_head_scale ? prm.v_head_scale[kv_head] : 1.f);
       int it_next = -1;
       if (!take_item(n + 1, it_next)) {
         ok = false;
@@ -633,7 +492,8 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
       // computes the next item's first scores while this item's last PV
       // and epilogue finish. (Copying it inside the tile loop instead, right
       // after the last S read, made the loop measurably slower.)
-      if (has_next && !copy_q(n + 1)) {
+      kq += 2 + nt;
+      if (has_next && !copy_q(n + 1, kq)) {
         ok = false;
         break;
       }
@@ -651,7 +511,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
       tc_fence_after();
       // ---- epilogue: O / lp (bf16 or fp16) and lse = ln(l) + m ln 2
       const bool row_ok = w.q_row + t_row < rb.q_end;
-      const float inv = lp > 0.f ? prm.v_scale / lp : 0.f;
+      const float inv = lp > 0.f ? v_scale / lp : 0.f;
       const size_t out_row = size_t(w.q_row) + t_row;
       const int qo_head = w.head * prm.pack + t_head;
       uint16_t* op = reinterpret_cast<uint16_t*>(prm.out) +
@@ -714,6 +574,360 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
       abort_flag = 1;
       atomicOr(prm.err, kErrTimeout);
     }
+  } else if (warp < 8) {
+    if constexpr (C::MIXED) setmaxnreg_dec<C::HELPER_REGS>();
+    if (warp == 4 || warp == 6) {
+      // ------------------------------------------------------------ producers
+      // Warp 4 loads Q and the K tiles, warp 6 the V tiles: each page needs one
+      // TMA instruction per 64-dim slice, and their issue, not the bytes,
+      // bounded a single producer warp. Copies run ahead across item
+      // boundaries: the next item's Q and first tiles load while the current
+      // item is still computing.
+      const bool is_v = warp == 6;
+      if (lane == 0) {
+        prefetch_tensormap(is_v ? &v_map : &k_map);
+        if (!is_v) prefetch_tensormap(&q_map);
+      }
+      const CUtensorMap* map = is_v ? &v_map : &k_map;
+      uint64_t* full = is_v ? bars.v_full : bars.k_full;
+      uint64_t* empty = is_v ? bars.v_empty : bars.k_empty;
+      const uint32_t ring = base + (is_v ? C::OFF_V : C::OFF_K);
+      const int P = prm.page_size;
+      const int ppt = C::N / P;
+      const uint32_t box = uint32_t(P) * 128u;
+      auto pages_in = [&](const WorkItem& w, int j) {
+        return (min(C::N, w.tok_end - w.tok_begin - j * C::N) + P - 1) / P;
+      };
+      bool ok = true;
+      int g = 0;
+      // K producer, lane 0: publish item n's index in the ring (-1: no more)
+      auto publish = [&](int n, int value) {
+        if (n >= kItemRing &&
+            !mbar_wait_bounded(smem_u32(&bars.item_empty[n % kItemRing]),
+                               ((n / kItemRing) & 1) ^ 1, limit, &abort_flag))
+          return false;
+        item_ring[n % kItemRing] = value;
+        mbar_arrive(smem_u32(&bars.item_full[n % kItemRing]));   // release: the index is visible
+        return true;
+      };
+      // index of item 0 (both producers); a mixed launch may have more CTAs
+      // than prefill items
+      int it = int(blockIdx.x) < n_items ? int(blockIdx.x) : -1;
+      if (is_v) {
+        int v = -1;
+        if (lane == 0) {
+          ok = item_at(0, v);
+          item_done(0);
+        }
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        it = __shfl_sync(0xffffffffu, v, 0);
+      } else if (lane == 0) {
+        ok = publish(0, it);
+      }
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      WorkItem w;
+      if (ok && it >= 0) w = prm.items[it];
+      // page ids of the next tile are loaded while the current tile's copies
+      // are issued, so the dependent global load is off the critical path
+      int next_page = -1;
+      if (ok && it >= 0 && item_tiles<C::N>(w) > 0 && lane < pages_in(w, 0))
+        next_page = prm.page_indices[w.page_begin + lane];
+      for (int n = 0; ok && it >= 0; ++n) {
+        const int nt = item_tiles<C::N>(w);
+        const int kv_head = w.head * prm.pack / prm.group;
+        const int c1 = prm.layout == FI_LAYOUT_NHD ? kv_head : 0;
+        const int c2 = prm.layout == FI_LAYOUT_NHD ? 0 : kv_head;
+        // the next item: taken from the counter and published by the K
+        // producer, read from the ring by the V producer
+        int it_next = -1;
+        if (lane == 0) {
+          if (is_v) {
+            ok = item_at(n + 1, it_next);
+            item_done(n + 1);
+          } else {
+            it_next = int(gridDim.x + atomicAdd(prm.work_counter, 1u));
+            if (it_next >= n_items) it_next = -1;
+            ok = publish(n + 1, it_next);
+          }
+        }
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        it_next = __shfl_sync(0xffffffffu, it_next, 0);
+        if (!ok) break;
+        WorkItem wn;
+        if (it_next >= 0) wn = prm.items[it_next];
+        if (!is_v && !C::Q_IN_RING) {
+          // Q of item n, once the buffer is free: its previous contents have
+          // been copied into TMEM
+          if (n >= 1) {
+            ok = mbar_wait_warp(smem_u32(&bars.q_tmem), (n - 1) & 1, limit, &abort_flag);
+            if (!ok) break;
+          }
+          if (lane == 0) {
+            const uint32_t qb = smem_u32(&bars.q_full);
+            mbar_arrive_expect_tx(qb, C::Q_BYTES);
+  #pragma unroll
+            for (int c = 0; c < C::DBLK; ++c)
+              // 128 M rows = (128 / pack rows of q) x (pack heads), heads inner
+              tma_load_3d(base + C::OFF_Q + c * C::M * 128, &q_map, qb, c * 64, w.head * prm.pack,
+                          w.q_row);
+          }
+          q_loads = n + 1;
+        } else if (!is_v) {
+          // Q of item n into the next two K-ring slots (64-dim slices 2h and
+          // 2h + 1 in slot h), released by the MMA issuer once the softmax
+          // warps have copied Q into TMEM
+          for (int h = 0; h < 2; ++h, ++g) {
+            const int st = g % C::NST;
+            if (g >= C::NST && !mbar_wait_warp(smem_u32(&empty[st]), ((g / C::NST) & 1) ^ 1,
+                                               limit, &abort_flag)) {
+              ok = false;
+              break;
+            }
+            if (lane == 0) {
+              const uint32_t fb = smem_u32(&full[st]);
+              mbar_arrive_expect_tx(fb, C::KV_BYTES);
+  #pragma unroll
+              for (int c = 0; c < 2; ++c)
+                tma_load_3d(ring + st * C::KV_BYTES + c * C::M * 128, &q_map, fb, (2 * h + c) * 64,
+                            w.head * prm.pack, w.q_row);
+            }
+            issued = g + 1;
+          }
+          if (!ok) break;
+        }
+        for (int j = 0; j < nt; ++j, ++g) {
+          const int st = g % C::NST;
+          const int np = pages_in(w, j);
+          int page = -1;
+          bool valid = false;
+          if (lane < np) {
+            page = next_page;
+            valid = page >= 0 && page < prm.num_pages;
+            if (!valid && !is_v) atomicOr(prm.err, kErrBounds);
+          }
+          if (j + 1 < nt) {
+            if (lane < pages_in(w, j + 1))
+              next_page = prm.page_indices[w.page_begin + (j + 1) * ppt + lane];
+          } else if (it_next >= 0 && item_tiles<C::N>(wn) > 0 && lane < pages_in(wn, 0)) {
+            next_page = prm.page_indices[wn.page_begin + lane];
+          }
+          const uint32_t bytes =
+              uint32_t(__popc(__ballot_sync(0xffffffffu, valid))) * C::DBLK * box;
+          if (g >= C::NST && !mbar_wait_warp(smem_u32(&empty[st]), ((g / C::NST) & 1) ^ 1,
+                                             limit, &abort_flag)) {
+            ok = false;
+            break;
+          }
+          const uint32_t fb = smem_u32(&full[st]);
+          const bool skip = !is_v && n == 0 && j == 0 && prm.fault_kind == 1 && blockIdx.x == 0;
+          if (skip) skip_pos = g;
+          if (lane == 0 && !skip) mbar_arrive_expect_tx(fb, bytes);
+          __syncwarp();
+          if (valid && !skip) {
+            const uint32_t dst = ring + st * C::KV_BYTES + lane * box;
+  #pragma unroll
+            for (int c = 0; c < C::DBLK; ++c)
+              tma_load_4d(dst + c * C::N * 128, map, fb, c * 64, c1, c2, page);
+          }
+          issued = g + 1;
+        }
+        if (nt == 0 && it_next >= 0 && item_tiles<C::N>(wn) > 0 && lane < pages_in(wn, 0))
+          next_page = prm.page_indices[wn.page_begin + lane];
+        w = wn;
+        it = it_next;
+      }
+      if (!ok && lane == 0) { abort_flag = 1; atomicOr(prm.err, kErrTimeout); }
+      __syncwarp();
+    } else if (warp == 5) {
+      // ------------------------------------------------------------ MMA issuer
+      if (lane == 0) {
+        // descriptors are linear in the address field (bits 0-13 = addr >> 4),
+        // so each MMA's descriptor is a base plus a compile-time offset
+        const uint64_t kd0 = sdesc_sw128(base + C::OFF_K, 16, 1024);
+        const uint64_t vd0 = sdesc_sw128(base + C::OFF_V, C::N * 128, 1024);
+        bool ok = true;
+        int g = 0;    // KV tiles of earlier items (V ring, S buffers)
+        int kq = 0;   // K-ring position of the item's first K tile (Q slots included)
+        for (int n = 0; ok; ++n) {
+          int it = -1;
+          ok = item_at(n, it);
+          item_done(n);
+          if (!ok || it < 0) break;
+          const int nt = item_tiles<C::N>(prm.items[it]);
+          ok = mbar_wait_bounded(smem_u32(&bars.q_tmem), n & 1, limit, &abort_flag);
+          if (ok && C::Q_IN_RING) {
+            // Q is in TMEM: its two K-ring slots are free for K tiles again
+            mbar_arrive(smem_u32(&bars.k_empty[kq % C::NST]));
+            mbar_arrive(smem_u32(&bars.k_empty[(kq + 1) % C::NST]));
+            kq += 2;
+          }
+          for (int j = 0; ok && j <= nt; ++j) {
+            if (j < nt) {
+              const int gq = g + j, sb = gq & 1;
+              const int kp = kq + j, st = kp % C::NST;   // K-ring position of this tile
+              ok = mbar_wait_bounded(smem_u32(&bars.k_full[st]), (kp / C::NST) & 1, limit,
+                                     &abort_flag);
+              if (ok && gq >= 2)
+                ok = mbar_wait_bounded(smem_u32(&bars.s_free[sb]), ((gq >> 1) & 1) ^ 1, limit,
+                                       &abort_flag);
+              if (!ok) break;
+              tc_fence_after();
+              const uint64_t kd = kd0 + uint64_t((st * C::KV_BYTES) >> 4);
+              const uint32_t s_col = tmem + C::COL_S + sb * C::N;
+  #pragma unroll
+              for (int k = 0; k < HEAD_DIM / 16; ++k) {
+                const uint64_t bd = kd + uint64_t(((k >> 2) * C::N * 128 + (k & 3) * 32) >> 4);
+                tc_mma_ts(s_col, tmem + C::COL_Q + k * 8, bd, C::IDESC_QK, k > 0 ? 1u : 0u);
+              }
+              tc_commit(smem_u32(&bars.s_full[sb]));
+              tc_commit(smem_u32(&bars.k_empty[st]));
+            }
+            if (j >= 1) {
+              const int gp = g + j - 1, st = gp % C::NST;
+              ok = mbar_wait_bounded(smem_u32(&bars.p_full), gp & 1, limit, &abort_flag);
+              if (ok)
+                ok = mbar_wait_bounded(smem_u32(&bars.v_full[st]), (gp / C::NST) & 1, limit,
+                                       &abort_flag);
+              if (!ok) break;
+              tc_fence_after();
+              const uint64_t vd = vd0 + uint64_t((st * C::KV_BYTES) >> 4);
+  #pragma unroll
+              for (int k = 0; k < C::N / 16; ++k) {
+                // MN-major V: 16 tokens per step; the next 64 dims one K-tile slice further
+                const uint64_t bd = vd + uint64_t((k * 16 * 128) >> 4);
+                const uint32_t p_col = C::P_IN_S ? C::COL_S + (gp & 1) * C::N : C::COL_P;
+                tc_mma_ts(tmem + C::COL_O, tmem + p_col + k * 8, bd, C::IDESC_PV,
+                          (j > 1 || k > 0) ? 1u : 0u);
+              }
+              tc_commit(smem_u32(&bars.v_empty[st]));
+              tc_commit(smem_u32(&bars.pv_done));
+              if (C::P_IN_S) tc_commit(smem_u32(&bars.s_free[gp & 1]));
+            }
+          }
+          if (!ok) break;
+          tc_commit(smem_u32(&bars.o_final));
+          g += nt;
+          kq += nt;
+        }
+        if (!ok) {
+          abort_flag = 1;
+          atomicOr(prm.err, kErrTimeout);
+          // every MMA issued so far completes before the TMEM is released
+          tc_commit(smem_u32(&bars.drain));
+          mbar_wait_bounded(smem_u32(&bars.drain), 0, limit, nullptr);
+        }
+      }
+      __syncwarp();
+    } else {
+      if constexpr (C::MIXED) {
+        // ------------------------------------------------------------ decode producer (mixed kernel)
+        // Takes decode items from a global counter in the planner's
+        // longest-first order, hands their indices to the decode consumers
+        // through a small ring, and streams their pages into the decode ring.
+        const uint32_t dbase = base + C::OFF_DEC;
+        bool ok = true;
+        int r = 0;   // decode ring position
+        for (int dn = 0; ok; ++dn) {
+          int idx = -1;
+          if (lane == 0) {
+            idx = abort_flag ? -1 : int(atomicAdd(dec_counter, 1u));
+            if (idx >= n_dec) idx = -1;
+            if (dn >= kItemRing &&
+                !mbar_wait_bounded(smem_u32(&bars.ditem_empty[dn % kItemRing]),
+                                   ((dn / kItemRing) & 1) ^ 1, limit, &abort_flag)) {
+              ok = false;
+            } else {
+              ditem_ring[dn % kItemRing] = idx;
+              mbar_arrive(smem_u32(&bars.ditem_full[dn % kItemRing]));
+            }
+          }
+          ok = __shfl_sync(0xffffffffu, ok, 0) != 0;
+          idx = __shfl_sync(0xffffffffu, idx, 0);
+          if (!ok || idx < 0) break;
+          const WorkItem item = dprm.items[idx];
+          const int lead = item.tok_begin % dprm.page_size;
+          const int n_tok = item.tok_end - item.tok_begin + lead;
+          const int n_tiles = (n_tok + DC::TILE - 1) / DC::TILE;
+          const int done = decode_produce<HEAD_DIM, DG, E>(dprm, item, n_tok, n_tiles, r, false,
+                                                           dbase, bars.d_full, bars.d_empty,
+                                                           &abort_flag, &k_map, &v_map);
+          issued = r + done;
+          if (done < n_tiles) ok = false;
+          r += n_tiles;
+        }
+        if (!ok && lane == 0) {
+          abort_flag = 1;
+          atomicOr(dprm.err, kErrTimeout);
+        }
+        __syncwarp();
+      }
+    }
+  } else {
+    if constexpr (C::MIXED) {
+      // ------------------------------------------------------------ decode consumers (mixed kernel)
+      // Batch decode on the same SM: the decode producer (warp 7) takes
+      // decode items from a global counter in the planner's longest-first
+      // order and streams their pages through the decode ring; the decode
+      // consumers (warps 8 on) work through them in order. The HBM-bound
+      // decode work thus runs beside the tensor-bound prefill tiles of the
+      // same CTA instead of after them. An item's reduction area is the ring
+      // stage of its last tile, released once the item is written.
+      const uint32_t dbase = base + C::OFF_DEC;
+      uint8_t* dgen = smem_raw + (dbase - smem_u32(smem_raw));
+
+      const int cw = warp - 8;                    // consumer warp 0..3
+      const int ctid = int(threadIdx.x) - 256;    // consumer thread 0..127
+      int r = 0;
+      for (int dn = 0;; ++dn) {
+        int idx = -1;
+        bool good = true;
+        if (lane == 0) {
+          good = mbar_wait_bounded(smem_u32(&bars.ditem_full[dn % kItemRing]),
+                                   (dn / kItemRing) & 1, limit, &abort_flag);
+          if (good) idx = *reinterpret_cast<volatile int*>(&ditem_ring[dn % kItemRing]);
+          mbar_arrive(smem_u32(&bars.ditem_empty[dn % kItemRing]));
+        }
+        good = __shfl_sync(0xffffffffu, good, 0) != 0;
+        idx = __shfl_sync(0xffffffffu, idx, 0);
+        // the four consumer warps leave together (a warp that left alone
+        // would never reach their named barriers)
+        if (named_bar_or(2, DC::NCW * 32, !good || idx < 0)) break;
+        const WorkItem item = dprm.items[idx];
+        const int lead = item.tok_begin % dprm.page_size;
+        const int n_tok = item.tok_end - item.tok_begin + lead;
+        const int n_tiles = (n_tok + DC::TILE - 1) / DC::TILE;
+        const bool hold = n_tiles > 0;
+        const int last = r + n_tiles - 1;
+        float* red_o = hold ? reinterpret_cast<float*>(dgen + (last % DC::NSTAGE) *
+                                                                  DC::STAGE_BYTES)
+                            : nullptr;
+        float* red_m = red_o + DC::NCW * DG * HEAD_DIM;
+        float* red_l = red_m + DC::NCW * DG;
+        float* red_lp = red_l + DC::NCW * DG;
+        bool aborted;
+        if (hold)
+          aborted = DC::MMA
+                        ? mma_consumer<HEAD_DIM, DG, E, E>(dprm, item, n_tok, lead, n_tiles, r,
+                                                           true, cw, dbase, bars.d_full,
+                                                           bars.d_empty, &abort_flag, red_o,
+                                                           red_m, red_l, red_lp)
+                        : simt_consumer<HEAD_DIM, DG, E, E>(dprm, item, n_tok, lead, n_tiles, r,
+                                                            true, cw, dbase, bars.d_full,
+                                                            bars.d_empty, &abort_flag, red_o,
+                                                            red_m, red_l, red_lp);
+        else
+          aborted = named_bar_or(1, DC::NCW * 32, abort_flag != 0);
+        if (aborted) break;                      // voted: all consumer warps agree
+        decode_finish<HEAD_DIM, DG, E, E>(dprm, item, ctid, hold, red_o, red_m, red_l, red_lp,
+                                          &dec_merge_last);
+        if (hold) {
+          // every consumer warp is done with the reduction area
+          named_bar_sync(1, DC::NCW * 32);
+          if (lane == 0) mbar_arrive(smem_u32(&bars.d_empty[last % DC::NSTAGE]));
+        }
+        r += n_tiles;
+      }
+    }
   }
 
   tc_fence_before();
@@ -729,12 +943,38 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
     const bool is_v = warp == 6;
     uint64_t* full = is_v ? bars.v_full : bars.k_full;
     for (int j = max(0, issued - C::NST); j < issued; ++j) {
-      if (!is_v && j == 0 && prm.fault_kind == 1 && blockIdx.x == 0) continue;  // never issued
+      if (!is_v && j == skip_pos) continue;  // never issued
       mbar_wait_bounded(smem_u32(&full[j % C::NST]), (j / C::NST) & 1, limit, nullptr);
     }
     if (!is_v && q_loads > 0)
       mbar_wait_bounded(smem_u32(&bars.q_full), (q_loads - 1) & 1, limit, nullptr);
   }
+  if constexpr (C::MIXED) {
+    if (warp == 7 && lane == 0)
+      for (int j = max(0, issued - DC::NSTAGE); j < issued; ++j)
+        mbar_wait_bounded(smem_u32(&bars.d_full[j % DC::NSTAGE]), (j / DC::NSTAGE) & 1, limit,
+                          nullptr);
+  }
+}
+
+template <int HEAD_DIM, class E>
+__global__ void __launch_bounds__(PrefillCfg<HEAD_DIM, E>::THREADS, 1)
+prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant__ CUtensorMap k_map,
+               const __grid_constant__ CUtensorMap v_map, PrefillParams prm) {
+  DecodeParams none{};
+  prefill_body<HEAD_DIM, E, 0>(q_map, k_map, v_map, prm, none, 0, nullptr);
+}
+
+// One persistent launch over a mixed batch: the prefill items as in
+// prefill_kernel, and on warps 7 and up of the same CTAs the decode items
+// (dprm.items[0 .. n_dec), groups of DG query heads per kv head), handed out
+// longest first from *dec_counter (zero before the launch).
+template <int HEAD_DIM, class E, int DG>
+__global__ void __launch_bounds__(PrefillCfg<HEAD_DIM, E, DG>::THREADS, 1)
+mixed_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant__ CUtensorMap k_map,
+             const __grid_constant__ CUtensorMap v_map, PrefillParams prm, DecodeParams dprm,
+             int n_dec, uint32_t* dec_counter) {
+  prefill_body<HEAD_DIM, E, DG>(q_map, k_map, v_map, prm, dprm, n_dec, dec_counter);
 }
 
 template <int HEAD_DIM, class E>
@@ -761,7 +1001,50 @@ cudaError_t launch_prefill_e(int head_dim, const CUtensorMap& qm, const CUtensor
   }
 }
 
+template <class E, int DG>
+cudaError_t launch_mixed_t(const CUtensorMap& qm, const CUtensorMap& km, const CUtensorMap& vm,
+                           const PrefillParams& p, const DecodeParams& dp, int n_dec,
+                           uint32_t* dec_counter, int grid, cudaStream_t stream) {
+  using C = PrefillCfg<256, E, DG>;
+  auto kern = mixed_kernel<256, E, DG>;
+  // the per-warpgroup register split assumes this launch allocation
+  cudaFuncAttributes fa;
+  cudaError_t e = cudaFuncGetAttributes(&fa, kern);
+  if (e != cudaSuccess) return e;
+  if (fa.numRegs < int(C::MIN_LAUNCH_REGS)) return cudaErrorInvalidConfiguration;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  kern<<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(qm, km, vm, p, dp, n_dec, dec_counter);
+  return cudaGetLastError();
+}
+
 }  // namespace
+
+bool mixed_applies(int head_dim, int group, int dtype, int kv_dtype) {
+  return head_dim == 256 && (group == 1 || group == 2 || group == 4) && kv_dtype == dtype &&
+         (dtype == FI_DTYPE_BF16 || dtype == FI_DTYPE_FP16);
+}
+
+cudaError_t launch_mixed(int head_dim, int group, int dtype, const CUtensorMap& qm,
+                         const CUtensorMap& km, const CUtensorMap& vm, const PrefillParams& p,
+                         const DecodeParams& dp, int n_dec, uint32_t* dec_counter, int grid,
+                         cudaStream_t stream) {
+  if (head_dim != 256) return cudaErrorInvalidValue;
+  const int want = p.n_items > n_dec ? p.n_items : n_dec;
+  grid = grid < want ? grid : want;
+  if (grid <= 0) return cudaSuccess;
+#define FI_MIXED_CASE(E)                                                                      \
+  switch (group) {                                                                            \
+    case 1: return launch_mixed_t<E, 1>(qm, km, vm, p, dp, n_dec, dec_counter, grid, stream); \
+    case 2: return launch_mixed_t<E, 2>(qm, km, vm, p, dp, n_dec, dec_counter, grid, stream); \
+    case 4: return launch_mixed_t<E, 4>(qm, km, vm, p, dp, n_dec, dec_counter, grid, stream); \
+    default: return cudaErrorInvalidValue;                                                    \
+  }
+  if (dtype == FI_DTYPE_BF16) FI_MIXED_CASE(Bf16)
+  if (dtype == FI_DTYPE_FP16) FI_MIXED_CASE(Fp16)
+#undef FI_MIXED_CASE
+  return cudaErrorInvalidValue;
+}
 
 cudaError_t launch_prefill(int head_dim, int dtype, const CUtensorMap& qm, const CUtensorMap& km,
                            const CUtensorMap& vm, const PrefillParams& p, int grid,

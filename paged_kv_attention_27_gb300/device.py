@@ -65,6 +65,11 @@ class DeviceBatch:
                                        device)
         self.last_page_len = i32_tensor(b.last_page_len, device)
         self.qo_indptr = i32_tensor(b.qo_indptr, device)
+        # per-kv-head cache scales (device fp32), when the batch has them
+        f32 = lambda a: None if a is None else torch.from_numpy(
+            np.ascontiguousarray(a, dtype=np.float32)).to(device)
+        self.k_head_scale = f32(b.k_head_scale)
+        self.v_head_scale = f32(b.v_head_scale)
         if mode is None:
             mode = B.FI_MODE_DECODE if (b.is_decode and not b.causal) else B.FI_MODE_PREFILL
         self.mode = mode
@@ -87,12 +92,15 @@ class DeviceBatch:
             B.fi_batch_decode_paged(self.plan, self.q, self.k, self.v, layout, 0, b.num_pages,
                                     self.page_indptr, self.page_indices, self.last_page_len,
                                     b.sm_scale, b.k_scale, b.v_scale, self.out, self.lse,
-                                    self.workspace, stream=stream)
+                                    self.workspace, stream=stream, k_head_scale=self.k_head_scale,
+                                    v_head_scale=self.v_head_scale)
         else:
             B.fi_batch_prefill_paged(self.plan, self.q, self.qo_indptr, self.k, self.v, layout, 0,
                                      b.num_pages, self.page_indptr, self.page_indices,
                                      self.last_page_len, b.sm_scale, b.k_scale, b.v_scale,
-                                     self.out, self.lse, self.workspace, stream=stream)
+                                     self.out, self.lse, self.workspace, stream=stream,
+                                     k_head_scale=self.k_head_scale,
+                                     v_head_scale=self.v_head_scale)
         return self.out, self.lse
 
     def run_host(self, stream=None):
@@ -117,7 +125,8 @@ class DeviceBatch:
                                   b.page_indptr.astype(np.int32),
                                   b.page_indices.astype(np.int32), b.last_page_len.astype(np.int32),
                                   b.sm_scale, b.k_scale, b.v_scale, out_h, lse_h, self._ws_host,
-                                  ws_bytes, stream=stream)
+                                  ws_bytes, stream=stream, k_head_scale=self.k_head_scale,
+                                  v_head_scale=self.v_head_scale)
         return out_h, lse_h
 
     def status(self, stream=None) -> int:

@@ -103,9 +103,11 @@ _CHUNK = 1 << 22
 
 
 def normal_bf16(seed: int, stream: int, shape, dtype: str = "bf16",
-                scale: float = 1.0) -> np.ndarray:
+                scale: float = 1.0, axis_scale=None) -> np.ndarray:
     """Standard normal values (times ``scale``) of ``shape`` as bit patterns
     of ``dtype``: bf16 (default) or fp16 as uint16, e4m3 as uint8.
+    ``axis_scale`` = (axis, factors): the values at index i along ``axis``
+    are also multiplied by factors[i] (per-head scales of a cache).
 
     Element block j (of 2^22 elements) is drawn from its own Philox stream
     keyed by (seed, stream, j), so the values do not depend on how many
@@ -115,13 +117,22 @@ def normal_bf16(seed: int, stream: int, shape, dtype: str = "bf16",
     import os
     n = int(np.prod(shape, dtype=np.int64))
     out = np.empty(n, dtype=np.uint8 if dtype == "e4m3" else np.uint16)
+    if axis_scale is not None:
+        axis, factors = axis_scale
+        inner = int(np.prod(shape[axis + 1:], dtype=np.int64))
+        factors = np.asarray(factors, dtype=np.float32)
 
     def fill(j):
         s = j * _CHUNK
         c = min(_CHUNK, n - s)
         g = np.random.Generator(np.random.Philox(key=[int(seed) * 64 + int(stream), j]))
         x = g.standard_normal(c, dtype=np.float32)
-        out[s:s + c] = to_bits(x * np.float32(scale) if scale != 1.0 else x, dtype)
+        if scale != 1.0:
+            x = x * np.float32(scale)
+        if axis_scale is not None:
+            idx = (np.arange(s, s + c, dtype=np.int64) // inner) % shape[axis]
+            x = x * factors[idx]
+        out[s:s + c] = to_bits(x, dtype)
 
     blocks = range((n + _CHUNK - 1) // _CHUNK)
     with cf.ThreadPoolExecutor(max_workers=min(32, os.cpu_count() or 1)) as ex:
@@ -158,6 +169,22 @@ class PagedBatch:
     k_scale: float = 1.0         # attended keys / values = scale * stored ones
     v_scale: float = 1.0
     cascade: bool = False        # plan the shared prefix as one group (shared-prefix decode)
+    # per-kv-head factors on top of k_scale / v_scale (float32 [Hkv]; None = 1)
+    k_head_scale: np.ndarray | None = None
+    v_head_scale: np.ndarray | None = None
+
+    @property
+    def k_scales(self):
+        """The key scale the oracle applies: one number, or one per kv head."""
+        if self.k_head_scale is None:
+            return self.k_scale
+        return self.k_scale * self.k_head_scale.astype(np.float64)
+
+    @property
+    def v_scales(self):
+        if self.v_head_scale is None:
+            return self.v_scale
+        return self.v_scale * self.v_head_scale.astype(np.float64)
 
     @property
     def cache_dtype(self) -> str:
@@ -181,7 +208,8 @@ def make_batch(name: str, kv_lens, qo_lens, num_qo_heads: int, num_kv_heads: int
                causal: bool, seed: int, shared_prefix_requests: int = 0,
                shared_prefix_tokens: int = 0, tail_fill: str = "normal",
                extra_pages: int = 0, window_left: int = -1,
-               dtype: str = "bf16", kv_dtype: str = "", kv_scale: float = 1.0) -> PagedBatch:
+               dtype: str = "bf16", kv_dtype: str = "", kv_scale: float = 1.0,
+               head_scales=None) -> PagedBatch:
     """Build a paged batch with seeded values and a shuffled page table.
 
     ``shared_prefix_requests`` requests (the first ones) map their first
@@ -189,7 +217,9 @@ def make_batch(name: str, kv_lens, qo_lens, num_qo_heads: int, num_kv_heads: int
     pages. ``tail_fill`` chooses what sits in the unused slots of every last
     page: "normal" (more random values) or "nan" (quiet NaN bits, to show that
     nothing past ``last_page_len`` is read). ``extra_pages`` physical pages that
-    no request uses are added to the pool.
+    no request uses are added to the pool. ``head_scales`` (two sequences of
+    ``num_kv_heads`` factors, for K and V) gives each kv head its own scale on
+    top of ``kv_scale``: the cache stores the draws divided by both.
     """
     gen = philox(seed)
     kv_lens = np.asarray(kv_lens, dtype=np.int64)
@@ -228,8 +258,16 @@ def make_batch(name: str, kv_lens, qo_lens, num_qo_heads: int, num_kv_heads: int
     shape = (num_phys, P, Hkv, d) if layout == NHD else (num_phys, Hkv, P, d)
     # an FP8 cache stores the draws divided by the per-tensor scale
     cdt = kv_dtype or dtype
-    k_cache = normal_bf16(seed, 1, shape, cdt, 1.0 / kv_scale)
-    v_cache = normal_bf16(seed, 2, shape, cdt, 1.0 / kv_scale)
+    head_axis = 2 if layout == NHD else 1
+    ks_h = vs_h = None
+    if head_scales is not None:
+        ks_h = np.asarray(head_scales[0], dtype=np.float32)
+        vs_h = np.asarray(head_scales[1], dtype=np.float32)
+        assert ks_h.shape == (Hkv,) and vs_h.shape == (Hkv,)
+    k_cache = normal_bf16(seed, 1, shape, cdt, 1.0 / kv_scale,
+                          None if ks_h is None else (head_axis, 1.0 / ks_h))
+    v_cache = normal_bf16(seed, 2, shape, cdt, 1.0 / kv_scale,
+                          None if vs_h is None else (head_axis, 1.0 / vs_h))
     q = normal_bf16(seed, 3, (int(qo_lens.sum()), num_qo_heads, d), dtype)
     if tail_fill == "nan":
         for b in range(B):
@@ -251,7 +289,8 @@ def make_batch(name: str, kv_lens, qo_lens, num_qo_heads: int, num_kv_heads: int
                       shared_prefix_pages=int(prefix_pages),
                       meta={"seed": seed, "shared_prefix_requests": shared_prefix_requests},
                       window_left=int(window_left), dtype=dtype, kv_dtype=kv_dtype,
-                      k_scale=float(kv_scale), v_scale=float(kv_scale))
+                      k_scale=float(kv_scale), v_scale=float(kv_scale),
+                      k_head_scale=ks_h, v_head_scale=vs_h)
 
 
 # ----------------------------------------------------------------------------
@@ -271,6 +310,16 @@ def _fp8_scale(kv_dtype: str) -> float:
     return 1.0 / 16 if kv_dtype == "e4m3" else 1.0
 
 
+def fp8_head_scales(num_kv_heads: int, kv_dtype: str):
+    """Per-kv-head K and V factors of the synthetic FP8 caches: powers of two
+    from 1/2 to 2 in a fixed pattern (K and V differ), so that every head is
+    quantised on its own scale; None for 16-bit caches."""
+    if kv_dtype != "e4m3":
+        return None
+    h = np.arange(num_kv_heads)
+    return (2.0 ** ((h % 3) - 1), 2.0 ** (((h + 1) % 3) - 1))
+
+
 def llama7b_decode(seed: int = 1, batch: int = 64, dtype: str = "bf16",
                    kv_dtype: str = "") -> PagedBatch:
     """Llama-7B-shaped decode: 32/32 heads, d=128, P=16, KV ~ U[512,4096], NHD."""
@@ -280,7 +329,8 @@ def llama7b_decode(seed: int = 1, batch: int = 64, dtype: str = "bf16",
     return make_batch(f"Llama-7B-shaped batch decode B{batch} Hq32 Hkv32 d128 P16 kv~U[512,4096] "
                       f"NHD{tname}",
                       kv, np.ones(batch, np.int64), 32, 32, 128, 16, NHD, None, False, seed,
-                      dtype=dtype, kv_dtype=kv_dtype, kv_scale=_fp8_scale(kv_dtype))
+                      dtype=dtype, kv_dtype=kv_dtype, kv_scale=_fp8_scale(kv_dtype),
+                      head_scales=fp8_head_scales(32, kv_dtype))
 
 
 def lognormal_lengths(gen, n, median=2048, sigma=1.0, lo=1, hi=32768):
@@ -304,7 +354,7 @@ def llama70b_gqa_decode(seed: int = 2, batch: int = 128, shared: int = 32,
                       kv, np.ones(batch, np.int64), 64, 8, 128, 16, HND, None, False, seed,
                       shared_prefix_requests=shared, shared_prefix_tokens=1024,
                       window_left=window_left, kv_dtype=kv_dtype,
-                      kv_scale=_fp8_scale(kv_dtype))
+                      kv_scale=_fp8_scale(kv_dtype), head_scales=fp8_head_scales(8, kv_dtype))
 
 
 def shared_prefix_decode(seed: int = 7, batch: int = 64, prefix_tokens: int = 32768,
@@ -409,4 +459,5 @@ def sub_batch(src: PagedBatch, requests) -> PagedBatch:
                       q=q, k_cache=src.k_cache[idx], v_cache=src.v_cache[idx],
                       meta=dict(src.meta, sample=requests), window_left=src.window_left,
                       dtype=src.dtype, kv_dtype=src.kv_dtype, k_scale=src.k_scale,
-                      v_scale=src.v_scale)   # the sample's pages are renumbered: no cascade
+                      v_scale=src.v_scale, k_head_scale=src.k_head_scale,
+                      v_head_scale=src.v_head_scale)   # the sample's pages are renumbered: no cascade

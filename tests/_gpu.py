@@ -53,8 +53,8 @@ def oracle_parallel(b, requests=None, threads=None):
                                       b.page_indptr, b.page_indices, b.last_page_len,
                                       b.num_qo_heads, b.num_kv_heads, b.page_size, b.sm_scale,
                                       b.causal, requests=[r], window_left=b.window_left,
-                                      dtype=b.dtype, kv_dtype=b.cache_dtype, k_scale=b.k_scale,
-                                      v_scale=b.v_scale)
+                                      dtype=b.dtype, kv_dtype=b.cache_dtype, k_scale=b.k_scales,
+                                      v_scale=b.v_scales)
         r0, r1 = int(b.qo_indptr[r]), int(b.qo_indptr[r + 1])
         return r0, r1, o[r0:r1], l[r0:r1]
 

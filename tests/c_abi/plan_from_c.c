@@ -44,8 +44,8 @@ int main(void) {
   st = fi_batch_decode_paged(plan, (const void*)0x100000, (const void*)0x100000,
                              (const void*)0x100000, FI_LAYOUT_NHD, 0, 14,
                              (const int32_t*)0x100000, (const int32_t*)0x100000,
-                             (const int32_t*)0x100000, 0.125f, 1.0f, 1.0f, (void*)0x100000,
-                             NULL, (void*)0x100000, 16, NULL);
+                             (const int32_t*)0x100000, 0.125f, 1.0f, 1.0f, NULL, NULL,
+                             (void*)0x100000, NULL, (void*)0x100000, 16, NULL);
   if (st != FI_ERR_WORKSPACE_TOO_SMALL) return 6;
 
   printf("total_kv_tokens %lld items %d windowed_kv_tokens %lld windowed_items %d ws_ok %d\n",

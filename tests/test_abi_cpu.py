@@ -325,8 +325,15 @@ def test_workspace_too_small_and_bad_args_return_before_any_launch():
         with pytest.raises(B.FiError) as e:
             B.fi_batch_decode_paged(*bad, stream=0)
         assert e.value.status == B.FI_ERR_INVALID_ARG
+    for kw in ({"k_head_scale": fake + 2}, {"v_head_scale": fake + 1}):
+        with pytest.raises(B.FiError) as e:   # per-head scale arrays: fp32, 4-byte aligned
+            B.fi_batch_decode_paged(*args, stream=0, **kw)
+        assert e.value.status == B.FI_ERR_INVALID_ARG
     with pytest.raises(B.FiError) as e:
         B.fi_batch_decode_paged(*args, stream=0)
+    assert e.value.status == B.FI_ERR_NO_DEVICE
+    with pytest.raises(B.FiError) as e:      # aligned per-head scales pass the host checks
+        B.fi_batch_decode_paged(*args, stream=0, k_head_scale=fake, v_head_scale=fake + 4)
     assert e.value.status == B.FI_ERR_NO_DEVICE
     with pytest.raises(B.FiError) as e:
         B.fi_merge_states(fake, fake, 2, 3, 4, 6, B.FI_DTYPE_BF16, fake, None, stream=0)  # d % 4

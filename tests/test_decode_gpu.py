@@ -33,7 +33,7 @@ def _oracle(b, requests=None):
                                   b.page_indices, b.last_page_len, b.num_qo_heads, b.num_kv_heads,
                                   b.page_size, b.sm_scale, b.causal, requests=requests,
                                   window_left=b.window_left, dtype=b.dtype,
-                                  kv_dtype=b.cache_dtype, k_scale=b.k_scale, v_scale=b.v_scale)
+                                  kv_dtype=b.cache_dtype, k_scale=b.k_scales, v_scale=b.v_scales)
 
 
 def _rows(b, requests):
@@ -261,11 +261,27 @@ def test_fp8_cache_scales_and_window():
     check(b, sms=16)
 
 
-def test_fp8_cache_70b_full_size_sampled():
+@pytest.mark.parametrize("g,d", [(1, 128), (2, 64), (4, 256), (8, 128), (8, 64), (2, 256)])
+def test_fp8_cache_per_head_scales(g, d):
+    """Every kv head quantised on its own K and V scale (device arrays of
+    the run call, on top of the per-tensor scales): the kernel must take
+    each head's factor, not its neighbour's; splits and windows included."""
+    hkv = 4
+    kv = [1, 17, 300, 2049, 9000]
+    ks = [0.5, 2.0, 1.0, 0.25]
+    vs = [1.0, 0.5, 4.0, 2.0]
+    b = synth.make_batch(f"fp8 per-head g{g} d{d}", kv, [1] * len(kv), g * hkv, hkv, d, 16,
+                         synth.HND if g % 2 else synth.NHD, None, False, 720 + g + d,
+                         kv_dtype="e4m3", kv_scale=1 / 16, head_scales=(ks, vs),
+                         window_left=-1 if g != 8 else 2000)
+    check(b, sms=8)
+
+
+def test_fp8_cache_70b_full_size_every_request():
+    # the bench's FP8 batch: a per-head K and V scale on each of the 8 kv heads
     b = synth.llama70b_gqa_decode(kv_dtype="e4m3")
-    order = np.argsort(-b.kv_lens)
-    sample = sorted(set(order[:3].tolist() + order[-3:].tolist() + [0, 5, 31, 32, 77]))
-    check(b, requests=sample)
+    assert b.k_head_scale is not None and len(set(b.k_head_scale.tolist())) > 1
+    check_all(b)
 
 
 # ---- shared-prefix (cascade) decode ------------------------------------------

@@ -173,6 +173,41 @@ def test_fp8_cache_matches_torch_sdpa_float64():
         np.testing.assert_allclose(out[r], so[:, 0].numpy(), rtol=0, atol=1e-12)
 
 
+def test_fp8_cache_with_per_head_scales_matches_torch_sdpa_float64():
+    """Each kv head with its own K and V scale (the cache holds K / (k_scale
+    s_h) and V / (v_scale t_h)): torch decodes the codes, applies the scale
+    of each head and computes attention in float64."""
+    torch = pytest.importorskip("torch")
+    if not hasattr(torch, "float8_e4m3fn"):
+        pytest.skip("torch without float8_e4m3fn")
+    ks = [0.5, 2.0, 0.125]
+    vs = [4.0, 0.25, 1.0]
+    b = synth.make_batch("fp8 per-head", [45, 300, 7], [1, 1, 1], 6, 3, 32, 16, synth.NHD, None,
+                         False, 26, kv_dtype="e4m3", kv_scale=1 / 16, head_scales=(ks, vs))
+    np.testing.assert_array_equal(b.k_head_scale, np.float32(ks))
+    out, lse = _run(b)
+    g = b.num_qo_heads // b.num_kv_heads
+    dec = lambda x: torch.from_numpy(np.ascontiguousarray(x)).view(torch.float8_e4m3fn).to(
+        torch.float64)
+    for r in range(b.batch):
+        kv = int(b.kv_lens[r])
+        pages = b.page_indices[int(b.page_indptr[r]):int(b.page_indptr[r + 1])]
+        kt = dec(np.concatenate([b.k_cache[p] for p in pages], axis=0)[:kv])   # [kv, Hkv, d]
+        vt = dec(np.concatenate([b.v_cache[p] for p in pages], axis=0)[:kv])
+        kt = (kt * torch.tensor(ks, dtype=torch.float64)[None, :, None] / 16).transpose(0, 1)
+        vt = (vt * torch.tensor(vs, dtype=torch.float64)[None, :, None] / 16).transpose(0, 1)
+        qt = torch.from_numpy(b.q[r:r + 1].view(np.int16)).view(torch.bfloat16).to(
+            torch.float64).transpose(0, 1)                               # [Hq, 1, d]
+        kt, vt = kt.repeat_interleave(g, 0), vt.repeat_interleave(g, 0)
+        so = torch.nn.functional.scaled_dot_product_attention(qt, kt, vt, scale=b.sm_scale)
+        np.testing.assert_allclose(out[r], so[:, 0].numpy(), rtol=0, atol=1e-12)
+    # the scales matter: one number for every head gives another result
+    b1 = synth.PagedBatch(**{**b.__dict__, "k_head_scale": None, "v_head_scale": None})
+    assert np.abs(_run(b1)[0] - out).max() > 1e-2
+    # the attended values are close to the unscaled normal draws
+    assert 0.3 < np.abs(dec(b.k_cache).numpy()[:, :, 1] * ks[1] / 16).mean() < 1.5
+
+
 def test_kv_lengths_of_tiny_config():
     b = synth.tiny_decode()
     # pages {1,2,4,7}, last page lengths {1,1,16,4} for KV lengths {1,17,64,100}
@@ -310,7 +345,7 @@ def _run(b, requests=None):
                                   b.page_indices, b.last_page_len, b.num_qo_heads, b.num_kv_heads,
                                   b.page_size, b.sm_scale, b.causal, requests=requests,
                                   window_left=b.window_left, dtype=b.dtype,
-                                  kv_dtype=b.cache_dtype, k_scale=b.k_scale, v_scale=b.v_scale)
+                                  kv_dtype=b.cache_dtype, k_scale=b.k_scales, v_scale=b.v_scales)
 
 
 def test_permuting_physical_pages_changes_nothing():

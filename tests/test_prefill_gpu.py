@@ -39,7 +39,7 @@ def _oracle(b, rows=None, requests=None):
                                   b.page_indices, b.last_page_len, b.num_qo_heads, b.num_kv_heads,
                                   b.page_size, b.sm_scale, b.causal, requests=requests, rows=rows,
                                   window_left=b.window_left, dtype=b.dtype,
-                                  kv_dtype=b.cache_dtype, k_scale=b.k_scale, v_scale=b.v_scale)
+                                  kv_dtype=b.cache_dtype, k_scale=b.k_scales, v_scale=b.v_scales)
 
 
 def check_full(b, what=None):
@@ -208,6 +208,28 @@ def test_ragged_prefill_full_size():
 def test_mixed_chunk_decode_full_size():
     b = synth.mixed_chunk_decode()
     check_sampled(b, per_request=16, requests=set(range(8)) | {8, 9, 20, 33, 63})
+
+
+@pytest.mark.parametrize("case", ["pair", "one-tile d256", "mixed"])
+def test_per_head_scales_in_prefill_and_mixed_calls(case):
+    """The per-kv-head scale arrays apply to every kernel: a 16-bit cache
+    with K and V scaled per head (the two-tile and one-tile prefill kernels
+    and the mixed launch)."""
+    hkv = 2
+    ks, vs = [0.5, 2.0], [2.0, 0.25]
+    if case == "pair":
+        kv = [300, 129, 700]
+        b = synth.make_batch("per-head pair", kv, kv, 8, hkv, 128, 16, synth.NHD, None, True, 31,
+                             head_scales=(ks, vs))
+    elif case == "one-tile d256":
+        kv = [300, 129]
+        b = synth.make_batch("per-head d256", kv, kv, 2, hkv, 256, 32, synth.HND, None, True, 32,
+                             head_scales=(ks, vs))
+    else:
+        kv, qo = [400, 150, 900, 3000], [96, 1, 1, 64]
+        b = synth.make_batch("per-head mixed", kv, qo, 4, hkv, 256, 32, synth.NHD, None, True, 33,
+                             head_scales=(ks, vs))
+    check_full(b)
 
 
 # ---- failure path: a bounded wait that runs out ----------------------------

@@ -92,8 +92,9 @@ def test_noalloc_decode_matches_workspace_decode_twice():
         free2, _ = torch.cuda.mem_get_info()
     finally:
         gc.enable()
-    assert alloc2 == alloc1
-    assert free2 == free1
+    # nothing grew (torch may release an unrelated cached block meanwhile)
+    assert alloc2 <= alloc1, (alloc1, alloc2)
+    assert free2 >= free1, (free1, free2)
     assert torch.equal(out2, out) and torch.equal(lse2, lse)   # same plan: bitwise the same
 
 
