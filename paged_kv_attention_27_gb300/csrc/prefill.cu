@@ -35,6 +35,7 @@
 //   * the same warps finish with O / l, write out (inputs' type) and the
 //     fp32 lse.
 // Fully masked KV tiles are never visited: the planner clips tok_end.
+#include <cfloat>
 #include <climits>
 
 #include "decode_roles.cuh"
@@ -321,7 +322,10 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap& q_map, const CUt
       // this item's kv head: its key scale joins the score scale, its value
       // scale the output
       const int kv_head = w.head * prm.pack / prm.group;
-      const float scale = scale0 * (prm.k_head_scale ? prm.k_head_scale[kv_head] : 1.f);
+      // (at least FLT_MIN: a hidden score is -inf, and -inf * 0 would be NaN;
+      // with sm_scale = 0 every weight is still exactly 2^0 = 1)
+      const float scale =
+          fmaxf(scale0 * (prm.k_head_scale ? prm.k_head_scale[kv_head] : 1.f), FLT_MIN);
       const float v_scale = prm.v_scale * (prm.v_head_scale ? prm.v_head_scale[kv_head] : 1.f);
       int it_next = -1;
       if (!take_item(n + 1, it_next)) {
@@ -353,26 +357,32 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap& q_map, const CUt
         // independent accumulators keep the dependency chains short; the mask
         // is applied only in tiles that cross this warp's bounds.
         const int col0 = w.tok_begin + j * C::N;   // key position of column 0
-        const bool need_mask =
-            __any_sync(0xffffffffu, col0 + C::N - 1 > rb.t_max || col0 < rb.t_min);
+        // the columns of this tile the row may see: lo .. hi (a window's lower
+        // bound, INT_MIN when there is none, gives lo = 0)
+        const int hi = rb.t_max - col0;
+        const int lo = rb.t_min > col0 ? rb.t_min - col0 : 0;
+        const bool need_mask = __any_sync(0xffffffffu, hi < C::N - 1 || lo > 0);
+        // In a tile that crosses the row's bounds the hidden scores become
+        // -inf once, here: their weights are then exactly 0 (2^-inf), and the
+        // rest of the softmax is the same code as in every other tile.
+        if (need_mask) {
+          if (prm.window_left < 0) {
+#pragma unroll
+            for (int k = 0; k < C::N; ++k)
+              if (k > hi) sr[k >> 5][k & 31] = 0xff800000u;
+          } else {
+#pragma unroll
+            for (int k = 0; k < C::N; ++k)
+              if (k > hi || k < lo) sr[k >> 5][k & 31] = 0xff800000u;
+          }
+        }
         float mx8[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) mx8[i] = -INFINITY;
-        if (need_mask) {
 #pragma unroll
-          for (int k = 0; k < C::N; k += 2) {
-            const float a = col0 + k <= rb.t_max && col0 + k >= rb.t_min
-                                ? __uint_as_float(sr[k >> 5][k & 31]) : -INFINITY;
-            const float b = col0 + k + 1 <= rb.t_max && col0 + k + 1 >= rb.t_min
-                                ? __uint_as_float(sr[k >> 5][(k + 1) & 31]) : -INFINITY;
-            mx8[(k >> 1) & 7] = fmax3(mx8[(k >> 1) & 7], a, b);
-          }
-        } else {
-#pragma unroll
-          for (int k = 0; k < C::N; k += 2)
-            mx8[(k >> 1) & 7] = fmax3(mx8[(k >> 1) & 7], __uint_as_float(sr[k >> 5][k & 31]),
-                                      __uint_as_float(sr[k >> 5][(k + 1) & 31]));
-        }
+        for (int k = 0; k < C::N; k += 2)
+          mx8[(k >> 1) & 7] = fmax3(mx8[(k >> 1) & 7], __uint_as_float(sr[k >> 5][k & 31]),
+                                    __uint_as_float(sr[k >> 5][(k + 1) & 31]));
         const float mx_raw = fmaxf(fmax3(mx8[0], mx8[1], mx8[2]),
                                    fmax3(fmax3(mx8[3], mx8[4], mx8[5]), mx8[6], mx8[7]));
         const float m_tile = (mx_raw == -INFINITY) ? -INFINITY : mx_raw * scale;
@@ -397,11 +407,6 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap& q_map, const CUt
                                       sc2, nr2);
           s[k] = ex2(x.x);
           s[k + 1] = ex2(x.y);
-        }
-        if (need_mask) {
-#pragma unroll
-          for (int k = 0; k < C::N; ++k)
-            s[k] = (col0 + k <= rb.t_max && col0 + k >= rb.t_min) ? s[k] : 0.f;
         }
         float2 rs4[4];
 #pragma unroll

@@ -395,12 +395,15 @@ def ragged_prefill(seed: int = 4, batch: int = 16) -> PagedBatch:
 
 
 def mixed_chunk_decode(seed: int = 5, chunks: int = 8, decodes: int = 56,
-                       chunk_len: int = 512) -> PagedBatch:
+                       chunk_len: int = 512, batch: int | None = None) -> PagedBatch:
     """Chunked prefill + decode in one batch: 16/8 heads, d=256, P=32.
 
     ``chunks`` requests each append a ``chunk_len``-token causal chunk to an
     existing KV of U[4096,32768] tokens; ``decodes`` requests decode one token
-    against KV ~ U[1,32768]."""
+    against KV ~ U[1,32768]. ``batch`` (for smaller profiling cases) sets the
+    chunk count and keeps seven decodes per chunk."""
+    if batch is not None:
+        chunks, decodes = batch, 7 * batch
     g = philox(seed + 1000)
     existing = g.integers(4096, 32769, size=chunks)
     dec_kv = g.integers(1, 32769, size=decodes)

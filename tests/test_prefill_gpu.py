@@ -210,6 +210,18 @@ def test_mixed_chunk_decode_full_size():
     check_sampled(b, per_request=16, requests=set(range(8)) | {8, 9, 20, 33, 63})
 
 
+@pytest.mark.parametrize("d,w", [(128, -1), (128, 100), (256, -1), (64, 33)])
+def test_zero_score_scale_with_masked_tiles(d, w):
+    """sm_scale = 0: every visible key weighs the same, hidden keys nothing,
+    in tiles that cross the causal bound or the window too (the kernels hide
+    a key by giving it a score of -inf, which must not meet a zero scale)."""
+    kv = [300, 129, 17]
+    b = synth.make_batch(f"zero scale d{d} w{w}", kv, kv, 4, 2, d, 16, synth.NHD, 0.0, True,
+                         40 + d, window_left=w)
+    scale_v(b)
+    check_full(b)
+
+
 @pytest.mark.parametrize("case", ["pair", "one-tile d256", "mixed"])
 def test_per_head_scales_in_prefill_and_mixed_calls(case):
     """The per-kv-head scale arrays apply to every kernel: a 16-bit cache
