@@ -18,24 +18,16 @@
 //     columns of S_i once S_i has been read.
 //   * shared memory: Q_0, Q_1 (both MMA operands of S come from shared
 //     memory), a two-deep K ring and a two-deep V ring.
-// Roles (16 warps, four warpgroups):
+// Roles (12 warps):
 //   * warps 0-3 / 4-7: softmax of tile 0 / tile 1 (thread = query row = TMEM
-//     lane). At the end of an item a thread hands its row's 1 / l and lse to
-//     the epilogue warpgroup through shared memory and goes on to the next
-//     item's first scores at once;
+//     lane), then the epilogue of their tile;
 //   * warp 8 / 9: MMA issuer of tile 0 / tile 1 (warp 8 owns the TMEM
 //     allocation). Before issuing S_i of the next KV tile a warp waits for
 //     its previous O_i += P_i V: P_i lives in S_i's columns, and O_i is then
 //     settled for the softmax's rescale. The other tile's MMAs keep the
-//     tensor core busy meanwhile. The first PV of an item, which overwrites
-//     O_i, waits until the epilogue warpgroup has read the previous item's O_i;
+//     tensor core busy meanwhile;
 //   * warp 10: Q of both tiles and the K tiles (one TMA box per page and
-//     64-dim slice), and the work items; warp 11: the V tiles;
-//   * warps 12-15 (epilogue, one lane quarter of TMEM each): once an item's
-//     last PV into O_i has completed, read O_i, scale each row by its 1 / l,
-//     write the rows out in the inputs' type with their lse. Off the softmax
-//     warps, the epilogue no longer sits in their turn-taking: the next
-//     item's softmax runs while it writes.
+//     64-dim slice), and the work items; warp 11: the V tiles.
 // The launch is persistent over pairs of the planner's work items (items 2p
 // and 2p + 1: the same rows and keys, query heads h and h + 1 of one kv
 // group), longest first, as in the one-tile kernel.
@@ -64,13 +56,12 @@ struct PairCfg {
   static constexpr int M = kPrefillTileM;                   // 128 query rows per tile
   static constexpr int N = 128;                             // KV tokens per tile
   static constexpr int DBLK = HEAD_DIM / 64;                // 128-byte slices of a row
-  static constexpr int THREADS = 512;
-  // registers per thread: 128 at launch (512 x 128 = 65536, the whole
-  // register file); the softmax warpgroups take 200, the helper warpgroup
-  // (MMA issuers, copy producers) and the epilogue warpgroup keep 56 each:
-  // 2 x 128 x 200 + 2 x 128 x 56 = 65536
-  static constexpr uint32_t LAUNCH_REGS = 128, SOFTMAX_REGS = 200, HELPER_REGS = 56;
-  static_assert(2 * 128 * SOFTMAX_REGS + 2 * 128 * HELPER_REGS == THREADS * LAUNCH_REGS, "");
+  static constexpr int THREADS = 384;
+  // registers per thread: 168 at launch (384 x 168 = 64512); the softmax
+  // warpgroups take 224, the helper warpgroup (MMA issuers, copy producers)
+  // keeps 56: 2 x 128 x 224 + 128 x 56 = 64512
+  static constexpr uint32_t LAUNCH_REGS = 168, SOFTMAX_REGS = 224, HELPER_REGS = 56;
+  static_assert(2 * 128 * SOFTMAX_REGS + 128 * HELPER_REGS == THREADS * LAUNCH_REGS, "");
   static constexpr int NST = 2;                             // K (and V) ring depth
   static constexpr int Q_BYTES = DBLK * M * 128;            // one tile's Q
   static constexpr int KV_BYTES = DBLK * N * 128;           // one K (or V) tile
@@ -98,11 +89,6 @@ struct PairBarriers {
   uint64_t k_full[2], k_empty[2];
   uint64_t v_full[2], v_empty[2];
   uint64_t s_full[2], p_full[2], pv_done[2], o_final[2], drain[2];
-  // softmax -> epilogue: a tile's row statistics of an item are in
-  // row_stats; epilogue -> softmax: they have been read; epilogue -> MMA
-  // issuer: O_i of the item has been read (the next item's first PV may
-  // overwrite it)
-  uint64_t stats_full[2], stats_empty[2], o_free[2];
 };
 
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
@@ -128,9 +114,6 @@ prefill_pair_kernel(const __grid_constant__ CUtensorMap q_map,
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_flag;
   __shared__ int item_ring[kItemRing];
-  // per tile and row: (v_scale / l of the rounded weights, lse) of the item
-  // the epilogue warpgroup is to write
-  __shared__ float2 row_stats[2][C::M];
 
   const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
   const int warp = threadIdx.x >> 5;
@@ -150,8 +133,7 @@ prefill_pair_kernel(const __grid_constant__ CUtensorMap q_map,
   if (threadIdx.x == 0) {
     for (int s = 0; s < kItemRing; ++s) {
       mbar_init(smem_u32(&bars.item_full[s]), 1);
-      // 8 softmax warps, 2 MMA warps, the V producer, 4 epilogue warps
-      mbar_init(smem_u32(&bars.item_empty[s]), 15);
+      mbar_init(smem_u32(&bars.item_empty[s]), 11);   // 8 softmax warps, 2 MMA warps, V producer
     }
     mbar_init(smem_u32(&bars.q_full), 1);
     mbar_init(smem_u32(&bars.q_empty), 2);            // both tiles' last S of the item
@@ -165,9 +147,6 @@ prefill_pair_kernel(const __grid_constant__ CUtensorMap q_map,
       mbar_init(smem_u32(&bars.pv_done[s]), 1);
       mbar_init(smem_u32(&bars.o_final[s]), 1);
       mbar_init(smem_u32(&bars.drain[s]), 1);
-      mbar_init(smem_u32(&bars.stats_full[s]), 4);    // the tile's 4 softmax warps
-      mbar_init(smem_u32(&bars.stats_empty[s]), 4);   // the 4 epilogue warps
-      mbar_init(smem_u32(&bars.o_free[s]), 4);        // the 4 epilogue warps
     }
     abort_flag = 0;
     fence_barrier_init();
@@ -187,78 +166,7 @@ prefill_pair_kernel(const __grid_constant__ CUtensorMap q_map,
   // before the launch), so the register split of the two branches adds up.
   if (warp >= 8) {
     setmaxnreg_dec<C::HELPER_REGS>();
-    if (warp >= 12) {
-      // ------------------------------------------------------------ epilogue
-      // Lane quarter (warp & 3) of both tiles: rows t of O_0 and O_1.
-      const int t = (warp & 3) * 32 + lane;
-      const uint32_t lane_off = uint32_t((warp & 3) * 32) << 16;
-      bool ok = true;
-      for (int n = 0; ok; ++n) {
-        int it = -1;
-        if (lane == 0) {
-          ok = item_at(n, it);
-          item_done(n);
-        }
-        ok = __shfl_sync(0xffffffffu, ok, 0) != 0;
-        it = __shfl_sync(0xffffffffu, it, 0);
-        if (!ok || it < 0) break;
-        const WorkItem w = prm.items[2 * it];
-        const int nt = item_tiles<C::N>(w);
-        const bool row_ok = w.q_row + t < prm.qo_indptr[w.req + 1];
-        const size_t out_row = size_t(w.q_row) + t;
-#pragma unroll 1
-        for (int i = 0; i < 2; ++i) {
-          // the row's statistics, then the slot is free for the next item's
-          if (!mbar_wait_warp(smem_u32(&bars.stats_full[i]), n & 1, limit, &abort_flag)) {
-            ok = false;
-            break;
-          }
-          const float2 rs = row_stats[i][t];
-          __syncwarp();
-          if (lane == 0) mbar_arrive(smem_u32(&bars.stats_empty[i]));
-          if (!mbar_wait_warp(smem_u32(&bars.o_final[i]), n & 1, limit, &abort_flag)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t o_col = tmem + lane_off + C::col_o(i);
-          uint16_t* op = reinterpret_cast<uint16_t*>(prm.out) +
-                         (out_row * prm.num_qo_heads + w.head + i) * HEAD_DIM;
-          // 16 columns per wait: O / l in the inputs' type, 16-byte stores
-#pragma unroll 1
-          for (int c = 0; c < HEAD_DIM / 16; ++c) {
-            uint32_t r[16];
-            if (nt > 0) {
-              tmem_ld16(o_col + c * 16, r);
-              tmem_wait_ld();
-            } else {
-#pragma unroll
-              for (int e = 0; e < 16; ++e) r[e] = 0u;
-            }
-            if (row_ok) {
-              uint4* dst = reinterpret_cast<uint4*>(op + c * 16);
-              const float* f = reinterpret_cast<const float*>(r);
-#pragma unroll
-              for (int q4 = 0; q4 < 2; ++q4)
-                dst[q4] = make_uint4(E::pack2(f[8 * q4 + 0] * rs.x, f[8 * q4 + 1] * rs.x),
-                                     E::pack2(f[8 * q4 + 2] * rs.x, f[8 * q4 + 3] * rs.x),
-                                     E::pack2(f[8 * q4 + 4] * rs.x, f[8 * q4 + 5] * rs.x),
-                                     E::pack2(f[8 * q4 + 6] * rs.x, f[8 * q4 + 7] * rs.x));
-            }
-          }
-          // O_i has been read: the MMA warp may start the next item's O_i
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(smem_u32(&bars.o_free[i]));
-          if (row_ok && prm.lse) prm.lse[out_row * prm.num_qo_heads + w.head + i] = rs.y;
-        }
-      }
-      if (!ok && lane == 0) {
-        abort_flag = 1;
-        atomicOr(prm.err, kErrTimeout);
-      }
-      __syncwarp();
-    } else if (warp >= 10) {
+    if (warp >= 10) {
       // ------------------------------------------------------------ producers
       const bool is_v = warp == 11;
       if (lane == 0) {
@@ -427,11 +335,6 @@ prefill_pair_kernel(const __grid_constant__ CUtensorMap q_map,
             if (ok)
               ok = mbar_wait_bounded(smem_u32(&bars.v_full[st]), (gq / C::NST) & 1, limit,
                                      &abort_flag);
-            // the item's first PV overwrites O_i: the epilogue warpgroup has
-            // read the previous item's O_i first
-            if (ok && j == 0 && n >= 1)
-              ok = mbar_wait_bounded(smem_u32(&bars.o_free[i]), (n - 1) & 1, limit,
-                                     &abort_flag);
             if (!ok) break;
             tc_fence_after();
             const uint64_t vd = vd0 + uint64_t((st * C::KV_BYTES) >> 4);
@@ -469,9 +372,9 @@ prefill_pair_kernel(const __grid_constant__ CUtensorMap q_map,
     const uint32_t o_col = tmem + lane_off + C::col_o(i);
     const float scale0 = prm.sm_scale * kLog2e;
     // Row bounds of pair w for this thread's row: the last key it may see
-    // (causal bound, clipped to the keys) and the first (left window;
-    // INT_MIN: none).
-    struct RowBounds { int t_max, t_min; };
+    // (causal bound, clipped to the keys), the first (left window; INT_MIN:
+    // none) and the end of the request's rows.
+    struct RowBounds { int q_end, t_max, t_min; };
     auto bounds_of = [&](const WorkItem& w) {
       const int q_start = prm.qo_indptr[w.req], q_end = prm.qo_indptr[w.req + 1];
       const int np_req = prm.page_indptr[w.req + 1] - prm.page_indptr[w.req];
@@ -479,6 +382,7 @@ prefill_pair_kernel(const __grid_constant__ CUtensorMap q_map,
           np_req > 0 ? (np_req - 1) * prm.page_size + prm.last_page_len[w.req] : 0;
       const int pos = kv_len - (q_end - q_start) + (w.q_row - q_start + t);  // key position
       RowBounds r;
+      r.q_end = q_end;
       r.t_max = min(prm.causal ? pos : kv_len - 1, kv_len - 1);
       r.t_min = prm.window_left >= 0 ? pos - prm.window_left : INT_MIN;
       return r;
@@ -504,11 +408,11 @@ prefill_pair_kernel(const __grid_constant__ CUtensorMap q_map,
     }
     for (int n = 0; ok && it >= 0; ++n) {
       const int nt = item_tiles<C::N>(w);
-      // this item's kv head: its key scale joins the score scale, its value
-      // scale the output
       const int kv_head = w.head / prm.group;
-      // (at least FLT_MIN: a hidden score is -inf, and -inf * 0 would be NaN;
-      // with sm_scale = 0 every weight is still exactly 2^0 = 1)
+      // this item's kv head: its key scale joins the score scale (at least
+      // FLT_MIN: a hidden score is -inf, and -inf * 0 would be NaN; with
+      // sm_scale = 0 every weight is still exactly 2^0 = 1), its value scale
+      // the output
       const float scale =
           fmaxf(scale0 * (prm.k_head_scale ? prm.k_head_scale[kv_head] : 1.f), FLT_MIN);
       const float v_scale = prm.v_scale * (prm.v_head_scale ? prm.v_head_scale[kv_head] : 1.f);
@@ -668,23 +572,61 @@ prefill_pair_kernel(const __grid_constant__ CUtensorMap q_map,
         if (lane == 0) mbar_arrive(smem_u32(&bars.p_full[i]));
       }
       if (!ok) break;
-      // Hand the row's statistics of this item to the epilogue warpgroup
-      // (which writes O / l and lse once the item's last PV has completed)
-      // and go on to the next item at once. The slot is free once the
-      // epilogue has read the previous item's.
-      if (n >= 1 &&
-          !mbar_wait_warp(smem_u32(&bars.stats_empty[i]), (n - 1) & 1, limit, &abort_flag)) {
+      // the next pair's bounds load while this pair's last PV completes
+      WorkItem wn;
+      RowBounds rn;
+      if (it_next >= 0) {
+        wn = prm.items[2 * it_next];
+        rn = bounds_of(wn);
+      }
+      if (!mbar_wait_warp(smem_u32(&bars.o_final[i]), n & 1, limit, &abort_flag)) {
         ok = false;
         break;
       }
-      row_stats[i][t] = make_float2(lp > 0.f ? v_scale / lp : 0.f,
-                                    l > 0.f ? (m + lg2(l)) * kLn2 : -INFINITY);
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&bars.stats_full[i]));
-      if (it_next >= 0) {
-        w = prm.items[2 * it_next];
-        rb = bounds_of(w);
+      tc_fence_after();
+      // ---- epilogue: O / lp (the inputs' type), lse = ln(l) + m ln 2
+      const bool row_ok = w.q_row + t < rb.q_end;
+      const float inv = lp > 0.f ? v_scale / lp : 0.f;
+      const size_t out_row = size_t(w.q_row) + t;
+      const int qo_head = w.head + i;
+      uint16_t* op = reinterpret_cast<uint16_t*>(prm.out) +
+                     (out_row * prm.num_qo_heads + qo_head) * HEAD_DIM;
+#pragma unroll 1
+      for (int c0 = 0; c0 < HEAD_DIM / 32; c0 += 2) {
+        uint32_t rb2[2][32];
+        if (nt > 0) {
+          tmem_ld32(o_col + c0 * 32, rb2[0]);
+          tmem_ld32(o_col + (c0 + 1) * 32, rb2[1]);
+          tmem_wait_ld();
+        } else {
+#pragma unroll
+          for (int b = 0; b < 2; ++b)
+#pragma unroll
+            for (int e = 0; e < 32; ++e) rb2[b][e] = 0u;
+        }
+        if (row_ok) {
+#pragma unroll
+          for (int b = 0; b < 2; ++b) {
+            uint4* dst = reinterpret_cast<uint4*>(op + (c0 + b) * 32);
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) {
+              const float* f = reinterpret_cast<const float*>(rb2[b]) + q4 * 8;
+              dst[q4] = make_uint4(E::pack2(f[0] * inv, f[1] * inv),
+                                   E::pack2(f[2] * inv, f[3] * inv),
+                                   E::pack2(f[4] * inv, f[5] * inv),
+                                   E::pack2(f[6] * inv, f[7] * inv));
+            }
+          }
+        }
       }
+      if (row_ok && prm.lse)
+        prm.lse[out_row * prm.num_qo_heads + qo_head] =
+            l > 0.f ? (m + lg2(l)) * kLn2 : -INFINITY;
+      // O has been read: the next pair's first PV (issued only after this
+      // warp's next p_full arrival) may overwrite it
+      tc_fence_before();
+      w = wn;
+      rb = rn;
       it = it_next;
     }
     if (!ok && lane == 0) {
