@@ -49,7 +49,8 @@ NOMINAL_HBM_GBS = 8000.0      # HBM3e data-sheet figure (about 8 TB/s)
 # default line: (workload, cap on the timed steps)
 SECONDARY = [("llama70b_gqa_decode", 200), ("causal_prefill_1k", 200),
              ("causal_prefill_4k", 100), ("causal_prefill_16k", 30),
-             ("causal_prefill_32k", 30), ("ragged_prefill", 60), ("mixed_chunk_decode", 100)]
+             ("causal_prefill_32k", 30), ("ragged_prefill", 60), ("mixed_chunk_decode", 100),
+             ("gqa_decode_d256", 100)]
 
 
 def parse_args():
@@ -95,6 +96,7 @@ WORKLOADS = {
     "llama70b_gqa_decode_fp8kv": ("llama70b_gqa_decode", {"kv_dtype": "e4m3"}),
     "ragged_prefill": ("ragged_prefill", {}),
     "mixed_chunk_decode": ("mixed_chunk_decode", {}),
+    "gqa_decode_d256": ("gqa_decode_d256", {}),
 }
 
 

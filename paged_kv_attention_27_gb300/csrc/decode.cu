@@ -51,9 +51,9 @@ decode_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant__
       prefetch_tensormap(&k_map);
       prefetch_tensormap(&v_map);
     }
-    const int issued = decode_produce<HEAD_DIM, GROUP, KV>(prm, item, n_tok, n_tiles, 0,
-                                                          skip_first, smem_base, full_bar,
-                                                          empty_bar, &abort_flag, &k_map, &v_map);
+    const DecRing ring = contiguous_ring(smem_base, C::NSTAGE, full_bar, empty_bar);
+    const int issued = decode_produce<HEAD_DIM, GROUP, KV, C::NSTAGE>(
+        prm, item, n_tok, n_tiles, 0, skip_first, ring, &abort_flag, &k_map, &v_map);
     // Before leaving, make sure no copy this CTA issued is still in flight,
     // whether or not a consumer gave up (in a normal run the consumers have
     // already seen these phases complete, so the waits return at once).
@@ -71,15 +71,16 @@ decode_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant__
     float* red_m = red_o + C::NCW * GROUP * HEAD_DIM;                // [NCW][GROUP]
     float* red_l = red_m + C::NCW * GROUP;                           // exact weight sums
     float* red_lp = red_l + C::NCW * GROUP;                          // weights applied to O
+    const DecRing ring = contiguous_ring(smem_base, C::NSTAGE, full_bar, empty_bar);
     bool aborted;
     if constexpr (!C::MMA)
-      aborted = simt_consumer<HEAD_DIM, GROUP, E, KV>(prm, item, n_tok, lead, n_tiles, 0, false,
-                                                      warp, smem_base, full_bar, empty_bar,
-                                                      &abort_flag, red_o, red_m, red_l, red_lp);
+      aborted = simt_consumer<HEAD_DIM, GROUP, E, KV, C::NSTAGE>(
+          prm, item, n_tok, lead, n_tiles, 0, false, warp, ring, &abort_flag, red_o, red_m,
+          red_l, red_lp);
     else
-      aborted = mma_consumer<HEAD_DIM, GROUP, E, KV>(prm, item, n_tok, lead, n_tiles, 0, false,
-                                                     warp, smem_base, full_bar, empty_bar,
-                                                     &abort_flag, red_o, red_m, red_l, red_lp);
+      aborted = mma_consumer<HEAD_DIM, GROUP, E, KV, C::NSTAGE>(
+          prm, item, n_tok, lead, n_tiles, 0, false, warp, ring, &abort_flag, red_o, red_m,
+          red_l, red_lp);
     if (!aborted)
       decode_finish<HEAD_DIM, GROUP, E, KV>(prm, item, threadIdx.x, true, red_o, red_m, red_l,
                                             red_lp, &merge_last);

@@ -100,6 +100,37 @@ __device__ __forceinline__ uint32_t swz(int r, int c8) {
   return uint32_t(r * 128 + ((c8 ^ (r & 7)) << 4));
 }
 
+// A ring of decode stages: `n` stages of `stage_bytes`, the first `n_lo` at
+// shared address `lo`, the rest at `hi` (two separate blocks of shared
+// memory, each 1024-aligned), completed on `full[s]` (the producer's bytes)
+// and `empty[s]` (one arrival per consumer warp).
+struct DecRing {
+  uint32_t lo, hi;
+  int n_lo, n;
+  uint64_t* full;
+  uint64_t* empty;
+};
+
+__device__ __forceinline__ DecRing contiguous_ring(uint32_t base, int n, uint64_t* full,
+                                                   uint64_t* empty) {
+  return DecRing{base, base, n, n, full, empty};
+}
+
+// Stage and phase of ring position r, and the stage's shared address. NS > 0
+// is the stage count known at compile time (the decode kernel's ring); 0
+// takes R.n.
+template <int NS>
+__device__ __forceinline__ int ring_stage(const DecRing& R, int r) {
+  return NS > 0 ? r % NS : r % R.n;
+}
+template <int NS>
+__device__ __forceinline__ uint32_t ring_phase(const DecRing& R, int r) {
+  return uint32_t((NS > 0 ? r / NS : r / R.n) & 1);
+}
+__device__ __forceinline__ uint32_t ring_addr(const DecRing& R, int s, int stage_bytes) {
+  return s < R.n_lo ? R.lo + uint32_t(s * stage_bytes) : R.hi + uint32_t((s - R.n_lo) * stage_bytes);
+}
+
 // Tensor-core consumer warp for GQA groups of 4 or 8 heads, token-major: per
 // 16-token chunk of its share of a stage,
 //   S^T (16 tokens x 8 heads) = K Q^T by m16n8k16 MMAs, K the A operand
@@ -120,11 +151,10 @@ __device__ __forceinline__ uint32_t swz(int r, int c8) {
 // Leaves the warp's (m, l, lp, O) in shared memory and returns whether any
 // consumer aborted (voted, so all agree). Ring positions, `cw`, `hold_last`
 // and the reduction arrays as for simt_consumer.
-template <int HEAD_DIM, int GROUP, class E, class KV>
+template <int HEAD_DIM, int GROUP, class E, class KV, int NS>
 __device__ __forceinline__ bool mma_consumer(const DecodeParams& prm, const WorkItem& item,
                                              int n_tok, int lead, int n_tiles, int r0,
-                                             bool hold_last, int cw, uint32_t smem_base,
-                                             uint64_t* full_bar, uint64_t* empty_bar,
+                                             bool hold_last, int cw, const DecRing& R,
                                              int* abort_flag, float* red_o, float* red_m,
                                              float* red_l, float* red_lp) {
   constexpr bool FP8 = std::is_same<KV, E4m3>::value;
@@ -175,15 +205,15 @@ __device__ __forceinline__ bool mma_consumer(const DecodeParams& prm, const Work
   float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f}, lp[2] = {0.f, 0.f};
 
   for (int i = 0; i < n_tiles; ++i) {
-    const int s = (r0 + i) % C::NSTAGE;
-    if (!mbar_wait_warp(smem_u32(&full_bar[s]), ((r0 + i) / C::NSTAGE) & 1, prm.wait_limit_ns,
+    const int s = ring_stage<NS>(R, r0 + i);
+    if (!mbar_wait_warp(smem_u32(&R.full[s]), ring_phase<NS>(R, r0 + i), prm.wait_limit_ns,
                         abort_flag)) {
       if (lane == 0) { *abort_flag = 1; atomicOr(prm.err, kErrTimeout); }
       break;
     }
     const int ntok = min(C::TILE, n_tok - i * C::TILE);
     const int lo = i == 0 ? lead : 0;        // rows below lo are outside the window
-    const uint32_t kstage = smem_base + s * C::STAGE_BYTES;
+    const uint32_t kstage = ring_addr(R, s, C::STAGE_BYTES);
     const uint32_t vstage = kstage + C::KBYTES;
 #pragma unroll 1
     for (int cb = warp * C::TOK_PER_WARP; cb < (warp + 1) * C::TOK_PER_WARP; cb += 16) {
@@ -206,7 +236,8 @@ __device__ __forceinline__ bool mma_consumer(const DecodeParams& prm, const Work
           __syncwarp();
         }
       } else if constexpr (FP8) {
-        kbase = smem_base + C::NSTAGE * C::STAGE_BYTES + warp * (2 * 16 * HEAD_DIM * 2);
+        // (the decode kernel's FP8 scratch follows its ring)
+        kbase = R.lo + C::NSTAGE * C::STAGE_BYTES + warp * (2 * 16 * HEAD_DIM * 2);
         vbase = kbase + 16 * HEAD_DIM * 2;
         slice = 16 * 128;
         row0 = 0;
@@ -375,7 +406,7 @@ __device__ __forceinline__ bool mma_consumer(const DecodeParams& prm, const Work
     }
     fence_proxy_async_smem();   // any zeroed rows before the producer's next TMA into the stage
     __syncwarp();
-    if (lane == 0 && !(hold_last && i == n_tiles - 1)) mbar_arrive(smem_u32(&empty_bar[s]));
+    if (lane == 0 && !(hold_last && i == n_tiles - 1)) mbar_arrive(smem_u32(&R.empty[s]));
   }
   // a head's sums are spread over the 8 lanes of its column
 #pragma unroll
@@ -420,11 +451,10 @@ __device__ __forceinline__ bool mma_consumer(const DecodeParams& prm, const Work
 // `skip_first` (test hook) leaves the first tile's copies out, so that the
 // consumers' bounded waits run out. Returns the number of tiles whose copies
 // were issued (n_tiles, unless a wait for a free stage ran out).
-template <int HEAD_DIM, int GROUP, class KV>
+template <int HEAD_DIM, int GROUP, class KV, int NS>
 __device__ __forceinline__ int decode_produce(const DecodeParams& prm, const WorkItem& item,
                                                int n_tok, int n_tiles, int r0, bool skip_first,
-                                               uint32_t smem_base, uint64_t* full_bar,
-                                               uint64_t* empty_bar, int* abort_flag,
+                                               const DecRing& R, int* abort_flag,
                                                const CUtensorMap* k_map, const CUtensorMap* v_map) {
   constexpr bool FP8 = std::is_same<KV, E4m3>::value;
   using C = DecodeCfg<HEAD_DIM, GROUP, FP8 ? 1 : 2>;
@@ -434,10 +464,10 @@ __device__ __forceinline__ int decode_produce(const DecodeParams& prm, const Wor
   constexpr int BOXES = FP8 ? 1 : C::DBLK;
   for (int i = 0; i < n_tiles; ++i) {
     const int r = r0 + i;
-    const int s = r % C::NSTAGE;
-    if (r >= C::NSTAGE) {
-      const uint32_t ph = ((r / C::NSTAGE) & 1) ^ 1;
-      if (!mbar_wait_warp(smem_u32(&empty_bar[s]), ph, prm.wait_limit_ns, abort_flag)) {
+    const int s = ring_stage<NS>(R, r);
+    if (r >= (NS > 0 ? NS : R.n)) {
+      const uint32_t ph = ring_phase<NS>(R, r) ^ 1u;
+      if (!mbar_wait_warp(smem_u32(&R.empty[s]), ph, prm.wait_limit_ns, abort_flag)) {
         if (lane == 0) { *abort_flag = 1; atomicOr(prm.err, kErrTimeout); }
         return i;
       }
@@ -454,12 +484,12 @@ __device__ __forceinline__ int decode_produce(const DecodeParams& prm, const Wor
     }
     const uint32_t vmask = __ballot_sync(0xffffffffu, valid);
     const uint32_t bytes = uint32_t(__popc(vmask)) * 2u * BOXES * box_bytes;
-    const uint32_t fb = smem_u32(&full_bar[s]);
+    const uint32_t fb = smem_u32(&R.full[s]);
     const bool skip = skip_first && i == 0;
     if (lane == 0 && !skip) mbar_arrive_expect_tx(fb, bytes);
     __syncwarp();
     if (valid && !skip) {
-      const uint32_t kdst = smem_base + s * C::STAGE_BYTES + lane * box_bytes;
+      const uint32_t kdst = ring_addr(R, s, C::STAGE_BYTES) + lane * box_bytes;
       const uint32_t vdst = kdst + C::KBYTES;
 #pragma unroll
       for (int c = 0; c < BOXES; ++c) {
@@ -484,11 +514,10 @@ __device__ __forceinline__ int decode_produce(const DecodeParams& prm, const Wor
 // `hold_last` (the caller reduces in it and releases it afterwards). Leaves
 // the warp's (m, l, lp, O) in the reduction arrays and returns whether any
 // consumer aborted (voted, so all agree).
-template <int HEAD_DIM, int GROUP, class E, class KV>
+template <int HEAD_DIM, int GROUP, class E, class KV, int NS>
 __device__ __forceinline__ bool simt_consumer(const DecodeParams& prm, const WorkItem& item,
                                               int n_tok, int lead, int n_tiles, int r0,
-                                              bool hold_last, int cw, uint32_t smem_base,
-                                              uint64_t* full_bar, uint64_t* empty_bar,
+                                              bool hold_last, int cw, const DecRing& R,
                                               int* abort_flag, float* red_o, float* red_m,
                                               float* red_l, float* red_lp) {
   constexpr bool FP8 = std::is_same<KV, E4m3>::value;
@@ -523,8 +552,8 @@ __device__ __forceinline__ bool simt_consumer(const DecodeParams& prm, const Wor
   }
 
   for (int i = 0; i < n_tiles; ++i) {
-    const int s = (r0 + i) % C::NSTAGE;
-    if (!mbar_wait_warp(smem_u32(&full_bar[s]), ((r0 + i) / C::NSTAGE) & 1, prm.wait_limit_ns,
+    const int s = ring_stage<NS>(R, r0 + i);
+    if (!mbar_wait_warp(smem_u32(&R.full[s]), ring_phase<NS>(R, r0 + i), prm.wait_limit_ns,
                         abort_flag)) {
       if (lane == 0) { *abort_flag = 1; atomicOr(prm.err, kErrTimeout); }
       break;
@@ -533,7 +562,8 @@ __device__ __forceinline__ bool simt_consumer(const DecodeParams& prm, const Wor
     const int lo = i == 0 ? lead : 0;      // rows below lo are outside the window
     // 16-bit cache: the lane's 16 bytes in its 64-dim slice (swizzled);
     // FP8 cache: its 8 bytes of a HEAD_DIM-byte row (128-byte rows swizzled)
-    const uint32_t kbase = smem_base + s * C::STAGE_BYTES + (FP8 ? 0 : blk * C::TILE * 128);
+    const uint32_t kbase =
+        ring_addr(R, s, C::STAGE_BYTES) + (FP8 ? 0 : blk * C::TILE * 128);
     const uint32_t vbase = kbase + C::KBYTES;
     auto row8 = [&](int r) -> uint32_t {
       return C::SWZ8 ? uint32_t(r * 128 + ((((ch >> 1) ^ (r & 7))) << 4) + (ch & 1) * 8)
@@ -591,7 +621,7 @@ __device__ __forceinline__ bool simt_consumer(const DecodeParams& prm, const Wor
       }
     }
     __syncwarp();
-    if (lane == 0 && !(hold_last && i == n_tiles - 1)) mbar_arrive(smem_u32(&empty_bar[s]));
+    if (lane == 0 && !(hold_last && i == n_tiles - 1)) mbar_arrive(smem_u32(&R.empty[s]));
   }
 
   // merge the token slots of this warp

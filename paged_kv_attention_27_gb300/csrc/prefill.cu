@@ -83,6 +83,11 @@ struct PrefillCfg {
   static constexpr int OFF_V = OFF_K + NST * KV_BYTES;
   static constexpr int OFF_DEC = OFF_V + NST * KV_BYTES;    // decode ring (mixed kernel)
   static constexpr int USED = OFF_DEC + (MIXED ? DC::NSTAGE * DC::STAGE_BYTES : 0);
+  // mixed kernel: once a CTA's prefill side has no more items, the prefill K
+  // and V rings (contiguous from OFF_K) join the decode ring as further stages
+  static constexpr int DEC_STAGES_EXT =
+      MIXED ? DC::NSTAGE + (OFF_DEC - OFF_K) / DC::STAGE_BYTES : 1;
+  static_assert(!MIXED || (OFF_DEC - OFF_K) % DC::STAGE_BYTES == 0, "");
   // mixed kernel: the softmax warpgroup raises its registers to 224 per
   // thread, the helper warpgroup (prefill producers, MMA issuer, decode
   // producer) lowers them to 56, the decode consumers keep the launch count
@@ -109,7 +114,7 @@ struct PrefillCfg {
 
 constexpr int kItemRing = 8;   // item indices handed from the K producer to the other roles
 
-template <int NST, int DNST>
+template <int NST, int DNST, int DNST2>
 struct PrefillBarriers {
   uint64_t item_full[kItemRing], item_empty[kItemRing];
   uint64_t q_full, q_tmem;
@@ -121,6 +126,9 @@ struct PrefillBarriers {
   // decode producer to the decode consumers
   uint64_t d_full[DNST], d_empty[DNST];
   uint64_t ditem_full[kItemRing], ditem_empty[kItemRing];
+  // the extended decode ring (the decode stages plus the prefill K and V
+  // rings, once this CTA's prefill side has no more work)
+  uint64_t e_full[DNST2], e_empty[DNST2];
 };
 
 
@@ -150,12 +158,14 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap& q_map, const CUt
   using C = PrefillCfg<HEAD_DIM, E, DG>;
   using DC = typename C::DC;
   extern __shared__ uint8_t smem_raw[];
-  __shared__ __align__(8) PrefillBarriers<C::NST, C::MIXED ? DC::NSTAGE : 1> bars;
+  __shared__ __align__(8)
+      PrefillBarriers<C::NST, C::MIXED ? DC::NSTAGE : 1, C::MIXED ? C::DEC_STAGES_EXT : 1> bars;
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_flag;
   __shared__ int item_ring[kItemRing];
   __shared__ int ditem_ring[C::MIXED ? kItemRing : 1];
   __shared__ int dec_merge_last;
+  __shared__ int prefill_free;   // mixed kernel: the prefill side is done, its rings are idle
 
   const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
   const int warp = threadIdx.x >> 5;
@@ -211,7 +221,12 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap& q_map, const CUt
         mbar_init(smem_u32(&bars.ditem_full[s]), 1);
         mbar_init(smem_u32(&bars.ditem_empty[s]), DC::NCW);
       }
+      for (int s = 0; s < C::DEC_STAGES_EXT; ++s) {
+        mbar_init(smem_u32(&bars.e_full[s]), 1);
+        mbar_init(smem_u32(&bars.e_empty[s]), DC::NCW);
+      }
     }
+    prefill_free = 0;
     abort_flag = 0;
     fence_barrier_init();
   }
@@ -226,6 +241,7 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap& q_map, const CUt
   int issued = 0;    // producers: ring positions whose copies this warp has issued
   int q_loads = 0;   // K producer: Q tiles it has loaded (Q outside the K ring)
   int skip_pos = -1; // K producer: the ring position the test hook left unloaded
+  bool dec_extended = false;  // mixed kernel, decode producer: on the extended ring
 
   // Role dispatch by warpgroup; in the mixed kernel each warpgroup sets its
   // register share first (one setmaxnreg per warpgroup, so that every code
@@ -579,6 +595,15 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap& q_map, const CUt
       abort_flag = 1;
       atomicOr(prm.err, kErrTimeout);
     }
+    if constexpr (C::MIXED) {
+      // No prefill item is left for this CTA: every MMA of its last item has
+      // completed (its epilogue waited for them) and no copy into the K and V
+      // rings is pending, so the decode side may take those rings over.
+      if (!named_bar_or(3, 128, !ok) && threadIdx.x == 0) {
+        __threadfence_block();
+        *reinterpret_cast<volatile int*>(&prefill_free) = 1;
+      }
+    }
   } else if (warp < 8) {
     if constexpr (C::MIXED) setmaxnreg_dec<C::HELPER_REGS>();
     if (warp == 4 || warp == 6) {
@@ -829,13 +854,33 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap& q_map, const CUt
         // Takes decode items from a global counter in the planner's
         // longest-first order, hands their indices to the decode consumers
         // through a small ring, and streams their pages into the decode ring.
-        const uint32_t dbase = base + C::OFF_DEC;
+        // Once the CTA's prefill side has no more work, the decode ring grows
+        // into the prefill K and V rings: between two items the producer
+        // waits until the consumers have released every stage of the short
+        // ring, then sends them a switch marker (-2), and both sides go on
+        // from position 0 of the long ring (barriers of its own).
+        const DecRing ring_a = contiguous_ring(base + C::OFF_DEC, DC::NSTAGE, bars.d_full,
+                                               bars.d_empty);
+        const DecRing ring_b{base + C::OFF_DEC, base + C::OFF_K, DC::NSTAGE, C::DEC_STAGES_EXT,
+                             bars.e_full, bars.e_empty};
         bool ok = true;
-        int r = 0;   // decode ring position
+        int r = 0;   // position in the current ring
         for (int dn = 0; ok; ++dn) {
+          int grow = 0;
+          if (lane == 0)
+            grow = !dec_extended && *reinterpret_cast<volatile int*>(&prefill_free) != 0;
+          grow = __shfl_sync(0xffffffffu, grow, 0);
+          if (grow) {
+            // every stage of the short ring released by the consumers
+            for (int q = max(0, r - DC::NSTAGE); ok && q < r; ++q)
+              ok = mbar_wait_warp(smem_u32(&bars.d_empty[q % DC::NSTAGE]), (q / DC::NSTAGE) & 1,
+                                  limit, &abort_flag);
+            if (!ok) break;
+          }
           int idx = -1;
           if (lane == 0) {
-            idx = abort_flag ? -1 : int(atomicAdd(dec_counter, 1u));
+            if (grow) idx = -2;
+            else idx = abort_flag ? -1 : int(atomicAdd(dec_counter, 1u));
             if (idx >= n_dec) idx = -1;
             if (dn >= kItemRing &&
                 !mbar_wait_bounded(smem_u32(&bars.ditem_empty[dn % kItemRing]),
@@ -848,14 +893,21 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap& q_map, const CUt
           }
           ok = __shfl_sync(0xffffffffu, ok, 0) != 0;
           idx = __shfl_sync(0xffffffffu, idx, 0);
-          if (!ok || idx < 0) break;
+          if (!ok) break;
+          if (idx == -2) {
+            dec_extended = true;
+            r = 0;
+            issued = 0;
+            continue;
+          }
+          if (idx < 0) break;
           const WorkItem item = dprm.items[idx];
           const int lead = item.tok_begin % dprm.page_size;
           const int n_tok = item.tok_end - item.tok_begin + lead;
           const int n_tiles = (n_tok + DC::TILE - 1) / DC::TILE;
-          const int done = decode_produce<HEAD_DIM, DG, E>(dprm, item, n_tok, n_tiles, r, false,
-                                                           dbase, bars.d_full, bars.d_empty,
-                                                           &abort_flag, &k_map, &v_map);
+          const int done = decode_produce<HEAD_DIM, DG, E, 0>(
+              dprm, item, n_tok, n_tiles, r, false, dec_extended ? ring_b : ring_a, &abort_flag,
+              &k_map, &v_map);
           issued = r + done;
           if (done < n_tiles) ok = false;
           r += n_tiles;
@@ -877,11 +929,13 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap& q_map, const CUt
       // decode work thus runs beside the tensor-bound prefill tiles of the
       // same CTA instead of after them. An item's reduction area is the ring
       // stage of its last tile, released once the item is written.
-      const uint32_t dbase = base + C::OFF_DEC;
-      uint8_t* dgen = smem_raw + (dbase - smem_u32(smem_raw));
-
-      const int cw = warp - 8;                    // consumer warp 0..3
-      const int ctid = int(threadIdx.x) - 256;    // consumer thread 0..127
+      const DecRing ring_a = contiguous_ring(base + C::OFF_DEC, DC::NSTAGE, bars.d_full,
+                                             bars.d_empty);
+      const DecRing ring_b{base + C::OFF_DEC, base + C::OFF_K, DC::NSTAGE, C::DEC_STAGES_EXT,
+                           bars.e_full, bars.e_empty};
+      bool extended = false;                      // on the long ring (switch marker seen)
+      const int cw = warp - 8;                    // consumer warp 0..NCW-1
+      const int ctid = int(threadIdx.x) - 256;    // consumer thread
       int r = 0;
       for (int dn = 0;; ++dn) {
         int idx = -1;
@@ -894,17 +948,23 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap& q_map, const CUt
         }
         good = __shfl_sync(0xffffffffu, good, 0) != 0;
         idx = __shfl_sync(0xffffffffu, idx, 0);
-        // the four consumer warps leave together (a warp that left alone
-        // would never reach their named barriers)
-        if (named_bar_or(2, DC::NCW * 32, !good || idx < 0)) break;
+        // the consumer warps leave together (a warp that left alone would
+        // never reach their named barriers); all read the same index
+        if (named_bar_or(2, DC::NCW * 32, !good || idx == -1)) break;
+        if (idx == -2) {                          // the ring grows: position 0 of the long one
+          extended = true;
+          r = 0;
+          continue;
+        }
+        const DecRing& ring = extended ? ring_b : ring_a;
         const WorkItem item = dprm.items[idx];
         const int lead = item.tok_begin % dprm.page_size;
         const int n_tok = item.tok_end - item.tok_begin + lead;
         const int n_tiles = (n_tok + DC::TILE - 1) / DC::TILE;
         const bool hold = n_tiles > 0;
-        const int last = r + n_tiles - 1;
-        float* red_o = hold ? reinterpret_cast<float*>(dgen + (last % DC::NSTAGE) *
-                                                                  DC::STAGE_BYTES)
+        const int last_stage = ring_stage<0>(ring, r + n_tiles - 1);
+        const uint32_t red_addr = ring_addr(ring, last_stage, DC::STAGE_BYTES);
+        float* red_o = hold ? reinterpret_cast<float*>(smem_raw + (red_addr - smem_u32(smem_raw)))
                             : nullptr;
         float* red_m = red_o + DC::NCW * DG * HEAD_DIM;
         float* red_l = red_m + DC::NCW * DG;
@@ -912,14 +972,12 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap& q_map, const CUt
         bool aborted;
         if (hold)
           aborted = DC::MMA
-                        ? mma_consumer<HEAD_DIM, DG, E, E>(dprm, item, n_tok, lead, n_tiles, r,
-                                                           true, cw, dbase, bars.d_full,
-                                                           bars.d_empty, &abort_flag, red_o,
-                                                           red_m, red_l, red_lp)
-                        : simt_consumer<HEAD_DIM, DG, E, E>(dprm, item, n_tok, lead, n_tiles, r,
-                                                            true, cw, dbase, bars.d_full,
-                                                            bars.d_empty, &abort_flag, red_o,
-                                                            red_m, red_l, red_lp);
+                        ? mma_consumer<HEAD_DIM, DG, E, E, 0>(dprm, item, n_tok, lead, n_tiles, r,
+                                                              true, cw, ring, &abort_flag, red_o,
+                                                              red_m, red_l, red_lp)
+                        : simt_consumer<HEAD_DIM, DG, E, E, 0>(dprm, item, n_tok, lead, n_tiles,
+                                                               r, true, cw, ring, &abort_flag,
+                                                               red_o, red_m, red_l, red_lp);
         else
           aborted = named_bar_or(1, DC::NCW * 32, abort_flag != 0);
         if (aborted) break;                      // voted: all consumer warps agree
@@ -928,7 +986,7 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap& q_map, const CUt
         if (hold) {
           // every consumer warp is done with the reduction area
           named_bar_sync(1, DC::NCW * 32);
-          if (lane == 0) mbar_arrive(smem_u32(&bars.d_empty[last % DC::NSTAGE]));
+          if (lane == 0) mbar_arrive(smem_u32(&ring.empty[last_stage]));
         }
         r += n_tiles;
       }
@@ -955,10 +1013,13 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap& q_map, const CUt
       mbar_wait_bounded(smem_u32(&bars.q_full), (q_loads - 1) & 1, limit, nullptr);
   }
   if constexpr (C::MIXED) {
-    if (warp == 7 && lane == 0)
-      for (int j = max(0, issued - DC::NSTAGE); j < issued; ++j)
-        mbar_wait_bounded(smem_u32(&bars.d_full[j % DC::NSTAGE]), (j / DC::NSTAGE) & 1, limit,
-                          nullptr);
+    // the decode producer's copies, on the ring it ended on
+    if (warp == 7 && lane == 0) {
+      const int n = dec_extended ? C::DEC_STAGES_EXT : DC::NSTAGE;
+      uint64_t* full = dec_extended ? bars.e_full : bars.d_full;
+      for (int j = max(0, issued - n); j < issued; ++j)
+        mbar_wait_bounded(smem_u32(&full[j % n]), (j / n) & 1, limit, nullptr);
+    }
   }
 }
 

@@ -357,6 +357,16 @@ def llama70b_gqa_decode(seed: int = 2, batch: int = 128, shared: int = 32,
                       kv_scale=_fp8_scale(kv_dtype), head_scales=fp8_head_scales(8, kv_dtype))
 
 
+def gqa_decode_d256(seed: int = 9, batch: int = 64) -> PagedBatch:
+    """GQA decode at the mixed batch's head_dim with a Llama2-70B-style group:
+    64 q / 8 kv heads (8 per kv head), head_dim 256, P=32, HND, KV ~ U[1,32768]
+    (the decode rows' length distribution of the mixed batch)."""
+    g = philox(seed + 1000)
+    kv = g.integers(1, 32769, size=batch)
+    return make_batch(f"GQA decode d256 B{batch} Hq64 Hkv8 P32 HND kv~U[1,32K]",
+                      kv, np.ones(batch, np.int64), 64, 8, 256, 32, HND, None, False, seed)
+
+
 def shared_prefix_decode(seed: int = 7, batch: int = 64, prefix_tokens: int = 32768,
                          cascade: bool = True) -> PagedBatch:
     """Decode of ``batch`` requests that share one long prefix (a system

@@ -77,6 +77,21 @@ def test_llama70b_gqa_decode_full_size_every_request():
     assert info["num_split_requests"] > 0        # long requests really were split
 
 
+def test_gqa_decode_d256_full_size_sampled():
+    """The d = 256, 8-heads-per-kv-head benchmark batch on the tensor-core
+    consumer: 16 of its 64 requests (the longest, the shortest and a spread)
+    against the oracle, computed in parallel."""
+    b = synth.gqa_decode_d256()
+    order = np.argsort(-b.kv_lens)
+    sample = sorted(set(order[:4].tolist() + order[-4:].tolist() + list(range(0, 64, 8))))
+    db = _dev(b)
+    out, lse = db.run()
+    torch.cuda.synchronize()
+    assert db.status() == B.FI_OK
+    ref_o, ref_l = oracle_parallel(b, requests=sample)
+    compare(out, lse, ref_o, ref_l, rows=np.array(sample), what=b.name)
+
+
 @pytest.mark.parametrize("d", [64, 128, 256])
 @pytest.mark.parametrize("g", [1, 2, 4, 8])
 @pytest.mark.parametrize("P", [16, 32])
