@@ -343,10 +343,12 @@ fi_status fi_batch_prefill_paged(fi_plan_t plan, const void* q, const int32_t* q
  * completed (it synchronises `stream`) with the device status of the step
  * (a device-side error word that fi_check_device_status would read is read
  * and cleared here). The KV cache stays in device memory: it is the cache.
- * The page table is gathered into a pinned staging buffer of the library
- * and crosses the link in one copy; q, out and lse are copied straight
- * from and to the caller's buffers (page-locked buffers make those copies
- * DMA transfers; pageable ones work, through the driver's staging).
+ * The page table is gathered, together with the plan's work list, into a
+ * pinned staging buffer of the library and crosses the link in one copy;
+ * q, out and lse are copied straight from and to the caller's buffers
+ * (page-locked buffers make those copies DMA transfers; pageable ones
+ * work, through the driver's staging). A stream that is being captured is
+ * refused (FI_ERR_UNSUPPORTED) before anything is copied.
  *   plan             from fi_plan, either mode.
  *   q_h              host [total q rows][num_qo_heads][head_dim], the plan's
  *                    dtype (total q rows = B for a decode plan,
@@ -363,8 +365,9 @@ fi_status fi_batch_prefill_paged(fi_plan_t plan, const void* q, const int32_t* q
  *   lse_h            host fp32 [total q rows][num_qo_heads] or NULL.
  *   workspace        device, 256-byte aligned, at least workspace_bytes +
  *                    host_io_bytes of the plan (fi_plan_get_info): the
- *                    step's q, page table, out and lse occupy the part after
- *                    the run calls' workspace.
+ *                    step's q, out and lse occupy the part after the run
+ *                    calls' workspace (the page table has its place inside
+ *                    that workspace, after the work lists).
  * Errors: as for fi_batch_decode_paged (FI_ERR_WORKSPACE_TOO_SMALL when the
  * host-IO part does not fit), FI_ERR_DEVICE_TIMEOUT / FI_ERR_DEVICE_BOUNDS
  * from the step's device status.
@@ -377,6 +380,42 @@ fi_status fi_batch_attention_host(fi_plan_t plan, const void* q_h, const int32_t
                                   float v_scale, const float* k_head_scale,
                                   const float* v_head_scale, void* out_h, float* lse_h,
                                   void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * fi_batch_attention_host_async — fi_batch_attention_host without the wait:
+ * the same checks, copies and kernels are enqueued on `stream` and the call
+ * returns at once with a ticket for the step in *ticket (0 for an empty
+ * plan). The page table (and qo_indptr) is staged before the call returns
+ * and may be changed at once; q_h, out_h and lse_h belong to the step
+ * until fi_host_step_wait on its ticket returns (the copy engine reads a
+ * page-locked q_h when the step's copy runs). This lets a serving loop
+ * plan and stage step t+1 while the device runs step t; steps on one
+ * stream run in the order they were issued, so consecutive steps may
+ * share the workspace.
+ *   ticket           receives the step's ticket (must not be NULL).
+ * At most 8 steps may be in flight per host thread (issued, not yet
+ * waited for); a ticket is waited for on the thread that issued it.
+ * Errors: as for fi_batch_attention_host, except the device status, which
+ * fi_host_step_wait returns; FI_ERR_INVALID_ARG with 8 steps in flight on
+ * this thread, or steps of another device still in flight on it.
+ */
+fi_status fi_batch_attention_host_async(
+    fi_plan_t plan, const void* q_h, const int32_t* qo_indptr_h, const void* k_cache,
+    const void* v_cache, int32_t kv_layout, int64_t page_stride_elems, int32_t num_pages,
+    const int32_t* page_indptr_h, const int32_t* page_indices_h, const int32_t* last_page_len_h,
+    float sm_scale, float k_scale, float v_scale, const float* k_head_scale,
+    const float* v_head_scale, void* out_h, float* lse_h, void* workspace, size_t workspace_bytes,
+    void* stream, uint64_t* ticket);
+
+/*
+ * fi_host_step_wait — blocks until the step of `ticket` has completed (its
+ * out and lse are in the caller's host buffers) and returns its device
+ * status: FI_OK, FI_ERR_DEVICE_TIMEOUT or FI_ERR_DEVICE_BOUNDS, or
+ * FI_ERR_CUDA if the stream failed. Ticket 0 returns FI_OK. A ticket that
+ * this thread did not issue, or that was already waited for, gives
+ * FI_ERR_INVALID_ARG.
+ */
+fi_status fi_host_step_wait(uint64_t ticket);
 
 /*
  * fi_merge_states — combine attention states computed over disjoint key

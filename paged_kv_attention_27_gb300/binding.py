@@ -41,7 +41,7 @@ EXPORTED = ["fi_plan", "fi_plan_destroy", "fi_plan_get_info", "fi_plan_get_work"
             "fi_batch_decode_paged", "fi_batch_prefill_paged", "fi_merge_states",
             "fi_check_device_status", "fi_status_string", "fi_last_error_string",
             "fi_debug_set_fault", "fi_profile_next_launch", "fi_batch_decode_paged_noalloc",
-            "fi_batch_attention_host"]
+            "fi_batch_attention_host", "fi_batch_attention_host_async", "fi_host_step_wait"]
 
 
 class FiError(RuntimeError):
@@ -110,6 +110,9 @@ def lib():
                                                 _F, _F, _F, _P, _P, _P, _P, _P]
     L.fi_batch_attention_host.argtypes = [_P, _P, _P, _P, _P, _I32, _I64, _I32, _P, _P, _P,
                                           _F, _F, _F, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]
+    L.fi_batch_attention_host_async.argtypes = (L.fi_batch_attention_host.argtypes +
+                                                [ctypes.POINTER(ctypes.c_uint64)])
+    L.fi_host_step_wait.argtypes = [ctypes.c_uint64]
     for name in EXPORTED:
         if name not in ("fi_status_string", "fi_last_error_string"):
             getattr(L, name).restype = _I32
@@ -267,6 +270,29 @@ def fi_batch_attention_host(plan: Plan, q_h, qo_indptr_h, k_cache, v_cache, kv_l
                                        _ptr(out_h), _ptr(lse_h), _ptr(workspace),
                                        int(workspace_bytes), _stream(stream))
     _check(st, "fi_batch_attention_host")
+
+
+def fi_batch_attention_host_async(plan: Plan, q_h, qo_indptr_h, k_cache, v_cache, kv_layout,
+                                  page_stride_elems, num_pages, page_indptr_h, page_indices_h,
+                                  last_page_len_h, sm_scale, k_scale, v_scale, out_h, lse_h,
+                                  workspace, workspace_bytes, stream=None, k_head_scale=None,
+                                  v_head_scale=None) -> int:
+    """fi_batch_attention_host without the wait; returns the step's ticket
+    for fi_host_step_wait (q_h, out_h and lse_h belong to the step until
+    then)."""
+    ticket = ctypes.c_uint64(0)
+    st = lib().fi_batch_attention_host_async(
+        plan.handle, _ptr(q_h), _ptr(qo_indptr_h), _ptr(k_cache), _ptr(v_cache), int(kv_layout),
+        int(page_stride_elems), int(num_pages), _ptr(page_indptr_h), _ptr(page_indices_h),
+        _ptr(last_page_len_h), float(sm_scale), float(k_scale), float(v_scale),
+        _ptr(k_head_scale), _ptr(v_head_scale), _ptr(out_h), _ptr(lse_h), _ptr(workspace),
+        int(workspace_bytes), _stream(stream), ctypes.byref(ticket))
+    _check(st, "fi_batch_attention_host_async")
+    return ticket.value
+
+
+def fi_host_step_wait(ticket: int):
+    _check(lib().fi_host_step_wait(int(ticket)), "fi_host_step_wait")
 
 
 def fi_merge_states(v, s, n, S, H, d, out_dtype, out, lse_out, stream=None):

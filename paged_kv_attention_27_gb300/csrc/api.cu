@@ -86,12 +86,11 @@ struct Staging {
   bool pending[kStagingSlots] = {};
   int next = 0;
 };
-thread_local Staging g_staging;   // work lists (every run call)
-thread_local Staging g_tables;    // page tables (host-buffer calls)
+thread_local Staging g_staging;   // work lists (and a host-buffer call's page table)
 
 // The workspace prefix a run uploads: zeroed header (error word, work
 // counter), work lists, merge tasks, zeroed merge counters; alignment gaps
-// zeroed too. `dst` holds P.ws.partial_o bytes.
+// zeroed too. `dst` holds P.ws.image_end bytes.
 void fill_image(uint8_t* dst, const fi::Plan& P) {
   // consecutive regions [offset, next offset): the data, then zeros
   struct Region { size_t off, end; const void* src; size_t bytes; };
@@ -105,7 +104,7 @@ void fill_image(uint8_t* dst, const fi::Plan& P) {
        P.prefix_items.size() * sizeof(fi::WorkItem)},
       {P.ws.prefix_tables, P.ws.merges, P.prefix_tables.data(),
        P.prefix_tables.size() * sizeof(int32_t)},
-      {P.ws.merges, P.ws.partial_o, P.merges.data(), P.merges.size() * sizeof(fi::MergeTask)},
+      {P.ws.merges, P.ws.image_end, P.merges.data(), P.merges.size() * sizeof(fi::MergeTask)},
   };
   for (const Region& r : regions) {
     if (r.bytes) std::memcpy(dst + r.off, r.src, r.bytes);
@@ -168,8 +167,60 @@ fi_status stage_and_copy(Staging& s, void* dst, size_t bytes, Fill fill, cudaStr
   return FI_OK;
 }
 
+// Host-buffer steps in flight on this host thread: each holds a pinned word
+// that receives the step's device status and an event recorded after the
+// step's last copy. A ticket is a sequence number; its slot is the number
+// modulo the ring size, and a slot takes a new step only once the ticket it
+// held has been waited for. Nothing is freed at exit.
+constexpr int kHostSteps = 8;
+struct HostSteps {
+  int device = -1;
+  uint32_t* words = nullptr;           // pinned, kHostSteps words
+  cudaEvent_t done[kHostSteps] = {};
+  uint64_t ticket[kHostSteps] = {};    // 0: free
+  uint64_t next = 1;
+};
+thread_local HostSteps g_host_steps;
+
+fi_status host_steps_ready(HostSteps& h) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return FI_ERR_NO_DEVICE;
+  if (h.device == dev) return FI_OK;
+  for (int i = 0; i < kHostSteps; ++i)
+    if (h.ticket[i]) {
+      g_last_error = "host-buffer steps of another device are still in flight on this thread";
+      return FI_ERR_INVALID_ARG;
+    }
+  for (int i = 0; i < kHostSteps; ++i)
+    if (h.done[i]) cudaEventDestroy(h.done[i]);
+  if (h.words) cudaFreeHost(h.words);
+  const uint64_t next = h.next;
+  h = HostSteps();
+  h.next = next;
+  void* p = nullptr;
+  cudaError_t e = cudaHostAlloc(&p, kHostSteps * sizeof(uint32_t), cudaHostAllocPortable);
+  for (int i = 0; e == cudaSuccess && i < kHostSteps; ++i)
+    e = cudaEventCreateWithFlags(&h.done[i], cudaEventDisableTiming);
+  if (e != cudaSuccess) {
+    for (int i = 0; i < kHostSteps; ++i)
+      if (h.done[i]) cudaEventDestroy(h.done[i]);
+    if (p) cudaFreeHost(p);
+    h = HostSteps();
+    h.next = next;
+    return cuda_fail(e, "host-step status words");
+  }
+  h.words = static_cast<uint32_t*>(p);
+  h.device = dev;
+  return FI_OK;
+}
+
+// How a run call gets its work-list image into the workspace: from the
+// pinned staging ring, from the static host buffer (the no-allocation call),
+// or not at all (the host-buffer call uploads it with the page table).
+enum class Upload { kStaged, kStatic, kDone };
+
 fi_status upload_image(void* dst, const fi::Plan& P, cudaStream_t stream) {
-  return stage_and_copy(g_staging, dst, P.ws.partial_o,
+  return stage_and_copy(g_staging, dst, P.ws.image_end,
                         [&](uint8_t* p) { fill_image(p, P); }, stream, "work-list upload");
 }
 
@@ -183,7 +234,7 @@ std::mutex g_static_image_mutex;
 uint8_t g_static_image[fi::kNoAllocScratchBytes];
 
 fi_status upload_image_static(void* dst, const fi::Plan& P, cudaStream_t stream) {
-  const size_t bytes = P.ws.partial_o;
+  const size_t bytes = P.ws.image_end;
   if (bytes > sizeof(g_static_image)) return FI_ERR_WORKSPACE_TOO_SMALL;
   std::lock_guard<std::mutex> lock(g_static_image_mutex);
   fill_image(g_static_image, P);
@@ -267,6 +318,65 @@ fi_status make_q_map(CUtensorMap* map, const void* q, int64_t rows, int Hq, int 
   return FI_OK;
 }
 
+// Encoded tensor maps of recent calls (per host thread). A serving loop
+// calls with the same caches, and often the same q buffer, step after step;
+// the same arguments encode the same map, so it is reused instead of
+// encoded again. Keyed by every argument of the encoding and the device.
+struct MapKey {
+  const void* base;
+  int64_t a, b, c, d, e, f;
+  int dev, kind;
+  bool operator==(const MapKey& o) const {
+    return base == o.base && a == o.a && b == o.b && c == o.c && d == o.d && e == o.e &&
+           f == o.f && dev == o.dev && kind == o.kind;
+  }
+};
+constexpr int kMapCache = 8;
+struct MapCache {
+  MapKey key[kMapCache];
+  CUtensorMap map[kMapCache];
+  bool used[kMapCache] = {};
+  int next = 0;
+};
+thread_local MapCache g_maps;
+
+template <class Encode>
+fi_status cached_map(CUtensorMap* out, const MapKey& k, Encode encode) {
+  for (int i = 0; i < kMapCache; ++i)
+    if (g_maps.used[i] && g_maps.key[i] == k) {
+      *out = g_maps.map[i];
+      return FI_OK;
+    }
+  const fi_status st = encode(out);
+  if (st != FI_OK) return st;
+  const int i = g_maps.next;
+  g_maps.next = (i + 1) % kMapCache;
+  g_maps.key[i] = k;
+  g_maps.map[i] = *out;
+  g_maps.used[i] = true;
+  return FI_OK;
+}
+
+fi_status kv_map(CUtensorMap* map, const void* base, int layout, int num_pages, int P, int Hkv,
+                 int d, int64_t page_stride, int dtype) {
+  int dev = -1;
+  cudaGetDevice(&dev);
+  const MapKey k{base, layout, num_pages, P, Hkv, d * 16 + dtype, page_stride, dev, 0};
+  return cached_map(map, k, [&](CUtensorMap* m) {
+    return make_kv_map(m, base, layout, num_pages, P, Hkv, d, page_stride, dtype);
+  });
+}
+
+fi_status q_map(CUtensorMap* map, const void* q, int64_t rows, int Hq, int pack, int d,
+                int dtype) {
+  int dev = -1;
+  cudaGetDevice(&dev);
+  const MapKey k{q, rows, Hq, pack, d, dtype, 0, dev, 1};
+  return cached_map(map, k, [&](CUtensorMap* m) {
+    return make_q_map(m, q, rows, Hq, pack, d, dtype);
+  });
+}
+
 fi_status check_device() {
   int dev = -1;
   cudaError_t e = cudaGetDevice(&dev);
@@ -300,7 +410,7 @@ fi_status run_paged(fi_plan_t plan, bool prefill_call, const void* q, const int3
                     const int32_t* page_indices_d, const int32_t* last_page_len_d, float sm_scale,
                     float k_scale, float v_scale, const float* k_head_scale,
                     const float* v_head_scale, void* out, float* lse, void* workspace,
-                    size_t workspace_bytes, void* stream_ptr, bool static_upload = false) {
+                    size_t workspace_bytes, void* stream_ptr, Upload upload = Upload::kStaged) {
   if (!plan) return FI_ERR_INVALID_ARG;
   const fi::Plan& P = plan->p;
   if (P.mode != (prefill_call ? FI_MODE_PREFILL : FI_MODE_DECODE)) return FI_ERR_INVALID_ARG;
@@ -334,17 +444,18 @@ fi_status run_paged(fi_plan_t plan, bool prefill_call, const void* q, const int3
   }
   // Upload header (zeroed error word and counters) + work lists + merge
   // tasks in one copy.
-  st = static_upload ? upload_image_static(ws, P, stream) : upload_image(ws, P, stream);
+  if (upload == Upload::kStaged) st = upload_image(ws, P, stream);
+  else if (upload == Upload::kStatic) st = upload_image_static(ws, P, stream);
   if (st != FI_OK) return st;
   cudaError_t e = cudaSuccess;
 
   CUtensorMap kmap, vmap;
   if (P.total_kv > 0) {
-    st = make_kv_map(&kmap, k_cache, kv_layout, num_pages, P.page_size, P.num_kv_heads,
-                     P.head_dim, page_stride_elems, P.kv_dtype);
+    st = kv_map(&kmap, k_cache, kv_layout, num_pages, P.page_size, P.num_kv_heads, P.head_dim,
+                page_stride_elems, P.kv_dtype);
     if (st != FI_OK) return st;
-    st = make_kv_map(&vmap, v_cache, kv_layout, num_pages, P.page_size, P.num_kv_heads,
-                     P.head_dim, page_stride_elems, P.kv_dtype);
+    st = kv_map(&vmap, v_cache, kv_layout, num_pages, P.page_size, P.num_kv_heads, P.head_dim,
+                page_stride_elems, P.kv_dtype);
     if (st != FI_OK) return st;
   } else {
     std::memset(&kmap, 0, sizeof(kmap));
@@ -358,7 +469,7 @@ fi_status run_paged(fi_plan_t plan, bool prefill_call, const void* q, const int3
   if (!P.prefill_items.empty() || !P.prefix_items.empty()) {
     // prefill tiles hold 128 rows of one head; shared-prefix tiles 128 / g
     // rows of the g heads of a kv head (a decode plan has only the latter)
-    st = make_q_map(&qmap, q, P.total_q, P.num_qo_heads,
+    st = q_map(&qmap, q, P.total_q, P.num_qo_heads,
                     P.prefix_items.empty() ? 1 : P.num_qo_heads / P.num_kv_heads, P.head_dim,
                     P.dtype);
     if (st != FI_OK) return st;
@@ -512,7 +623,7 @@ fi_status fi::run_decode_static_upload(
   return run_paged(plan, false, q, nullptr, k_cache, v_cache, kv_layout, page_stride_elems,
                    num_pages, page_indptr_d, page_indices_d, last_page_len_d, sm_scale, k_scale,
                    v_scale, k_head_scale, v_head_scale, out, lse, workspace, workspace_bytes,
-                   stream, true);
+                   stream, Upload::kStatic);
 }
 
 extern "C" {
@@ -613,15 +724,15 @@ fi_status fi_batch_prefill_paged(fi_plan_t plan, const void* q, const int32_t* q
                    stream);
 }
 
-fi_status fi_batch_attention_host(fi_plan_t plan, const void* q_h, const int32_t* qo_indptr_h,
-                                  const void* k_cache, const void* v_cache, int32_t kv_layout,
-                                  int64_t page_stride_elems, int32_t num_pages,
-                                  const int32_t* page_indptr_h, const int32_t* page_indices_h,
-                                  const int32_t* last_page_len_h, float sm_scale, float k_scale,
-                                  float v_scale, const float* k_head_scale,
-                                  const float* v_head_scale, void* out_h, float* lse_h, void* workspace,
-                                  size_t workspace_bytes, void* stream_ptr) {
-  if (!plan) return FI_ERR_INVALID_ARG;
+fi_status fi_batch_attention_host_async(
+    fi_plan_t plan, const void* q_h, const int32_t* qo_indptr_h, const void* k_cache,
+    const void* v_cache, int32_t kv_layout, int64_t page_stride_elems, int32_t num_pages,
+    const int32_t* page_indptr_h, const int32_t* page_indices_h, const int32_t* last_page_len_h,
+    float sm_scale, float k_scale, float v_scale, const float* k_head_scale,
+    const float* v_head_scale, void* out_h, float* lse_h, void* workspace, size_t workspace_bytes,
+    void* stream_ptr, uint64_t* ticket_out) {
+  if (!plan || !ticket_out) return FI_ERR_INVALID_ARG;
+  *ticket_out = 0;
   const fi::Plan& P = plan->p;
   const bool prefill = P.mode == FI_MODE_PREFILL;
   if (P.batch == 0) return FI_OK;
@@ -649,20 +760,39 @@ fi_status fi_batch_attention_host(fi_plan_t plan, const void* q_h, const int32_t
   const size_t table_bytes =
       (size_t(P.batch + 1) + P.page_entries + P.batch + (prefill ? P.batch + 1 : 0)) *
       sizeof(int32_t);
-  // the page table (and qo_indptr) in one pinned copy; q straight from the caller
+  // A captured copy would replay from a staging slot that later calls
+  // refill (as in the run calls).
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(stream, &cap) != cudaSuccess || cap != cudaStreamCaptureStatusNone) {
+    g_last_error = "run calls cannot be captured into a CUDA graph";
+    return FI_ERR_UNSUPPORTED;
+  }
+  HostSteps& hs = g_host_steps;
+  st = host_steps_ready(hs);
+  if (st != FI_OK) return st;
+  const int slot = int(hs.next % kHostSteps);
+  if (hs.ticket[slot]) {
+    g_last_error = "more than 8 host-buffer steps in flight on this thread";
+    return FI_ERR_INVALID_ARG;
+  }
+  // the work-list image and, right after it in the workspace, the page
+  // table (and qo_indptr): one pinned staging fill, one copy; q comes
+  // straight from the caller's buffer
   st = stage_and_copy(
-      g_tables, tab, table_bytes,
+      g_staging, ws, P.ws.hio_tables + table_bytes,
       [&](uint8_t* p) {
-        int32_t* t = reinterpret_cast<int32_t*>(p);
+        fill_image(p, P);
+        int32_t* t = reinterpret_cast<int32_t*>(p + P.ws.hio_tables);
         std::memcpy(t, page_indptr_h, size_t(P.batch + 1) * sizeof(int32_t));
         t += P.batch + 1;
-        if (P.page_entries > 0) std::memcpy(t, page_indices_h, size_t(P.page_entries) * sizeof(int32_t));
+        if (P.page_entries > 0)
+          std::memcpy(t, page_indices_h, size_t(P.page_entries) * sizeof(int32_t));
         t += P.page_entries;
         std::memcpy(t, last_page_len_h, size_t(P.batch) * sizeof(int32_t));
         t += P.batch;
         if (prefill) std::memcpy(t, qo_indptr_h, size_t(P.batch + 1) * sizeof(int32_t));
       },
-      stream, "page-table upload");
+      stream, "work-list and page-table upload");
   if (st != FI_OK) return st;
   cudaError_t e = cudaMemcpyAsync(ws + P.ws.hio_q, q_h, q_bytes, cudaMemcpyHostToDevice, stream);
   if (e != cudaSuccess) return cuda_fail(e, "q upload");
@@ -671,20 +801,56 @@ fi_status fi_batch_attention_host(fi_plan_t plan, const void* q_h, const int32_t
   st = run_paged(plan, prefill, ws + P.ws.hio_q, qo_d, k_cache, v_cache, kv_layout,
                  page_stride_elems, num_pages, indptr_d, indices_d, last_d, sm_scale, k_scale,
                  v_scale, k_head_scale, v_head_scale, out_d, lse_d, workspace, P.ws.total,
-                 stream_ptr);
+                 stream_ptr, Upload::kDone);
   if (st != FI_OK) return st;
   e = cudaMemcpyAsync(out_h, out_d, q_bytes, cudaMemcpyDeviceToHost, stream);
   if (e == cudaSuccess && lse_h)
     e = cudaMemcpyAsync(lse_h, lse_d, lse_bytes, cudaMemcpyDeviceToHost, stream);
   // the step's device status (error word at the start of the workspace)
-  uint32_t word = 0;
+  // into the slot's pinned word; the next step's upload zeroes the header
+  hs.words[slot] = 0;
   if (e == cudaSuccess)
-    e = cudaMemcpyAsync(&word, workspace, sizeof(word), cudaMemcpyDeviceToHost, stream);
-  if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+    e = cudaMemcpyAsync(&hs.words[slot], workspace, sizeof(uint32_t), cudaMemcpyDeviceToHost,
+                        stream);
+  if (e == cudaSuccess) e = cudaEventRecord(hs.done[slot], stream);
   if (e != cudaSuccess) return cuda_fail(e, "host-buffer step");
+  hs.ticket[slot] = hs.next;
+  *ticket_out = hs.next++;
+  return FI_OK;
+}
+
+fi_status fi_host_step_wait(uint64_t ticket) {
+  if (ticket == 0) return FI_OK;   // an empty step
+  HostSteps& hs = g_host_steps;
+  const int slot = int(ticket % kHostSteps);
+  if (hs.device < 0 || hs.ticket[slot] != ticket) {
+    g_last_error = "not a host-buffer step of this thread that is still to be waited for";
+    return FI_ERR_INVALID_ARG;
+  }
+  const cudaError_t e = cudaEventSynchronize(hs.done[slot]);
+  hs.ticket[slot] = 0;
+  if (e != cudaSuccess) return cuda_fail(e, "host-buffer step");
+  const uint32_t word = hs.words[slot];
   if (word & fi::kErrTimeout) return FI_ERR_DEVICE_TIMEOUT;
   if (word & fi::kErrBounds) return FI_ERR_DEVICE_BOUNDS;
   return FI_OK;
+}
+
+fi_status fi_batch_attention_host(fi_plan_t plan, const void* q_h, const int32_t* qo_indptr_h,
+                                  const void* k_cache, const void* v_cache, int32_t kv_layout,
+                                  int64_t page_stride_elems, int32_t num_pages,
+                                  const int32_t* page_indptr_h, const int32_t* page_indices_h,
+                                  const int32_t* last_page_len_h, float sm_scale, float k_scale,
+                                  float v_scale, const float* k_head_scale,
+                                  const float* v_head_scale, void* out_h, float* lse_h, void* workspace,
+                                  size_t workspace_bytes, void* stream) {
+  uint64_t ticket = 0;
+  const fi_status st = fi_batch_attention_host_async(
+      plan, q_h, qo_indptr_h, k_cache, v_cache, kv_layout, page_stride_elems, num_pages,
+      page_indptr_h, page_indices_h, last_page_len_h, sm_scale, k_scale, v_scale, k_head_scale,
+      v_head_scale, out_h, lse_h, workspace, workspace_bytes, stream, &ticket);
+  if (st != FI_OK) return st;
+  return fi_host_step_wait(ticket);
 }
 
 fi_status fi_merge_states(const float* v, const float* s, int32_t n, int32_t S, int32_t H,

@@ -92,8 +92,11 @@ cudaError_t launch_decode_t(const CUtensorMap& km, const CUtensorMap& vm, const 
                             int n_items, cudaStream_t stream) {
   using C = DecodeCfg<HEAD_DIM, GROUP, std::is_same<KV, E4m3>::value ? 1 : 2>;
   auto kern = decode_kernel<HEAD_DIM, GROUP, E, KV>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       C::SMEM_BYTES);
+  static std::atomic<uint64_t> configured{0};
+  cudaError_t e = once_per_device(configured, [&] {
+    return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                C::SMEM_BYTES);
+  });
   if (e != cudaSuccess) return e;
   kern<<<n_items, C::THREADS, C::SMEM_BYTES, stream>>>(km, vm, p);
   return cudaGetLastError();

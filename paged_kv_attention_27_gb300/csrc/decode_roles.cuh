@@ -150,8 +150,11 @@ __device__ __forceinline__ uint32_t ring_addr(const DecRing& R, int s, int stage
 // laid out as the TMA writes a 16-bit stage.
 // Leaves the warp's (m, l, lp, O) in shared memory and returns whether any
 // consumer aborted (voted, so all agree). Ring positions, `cw`, `hold_last`
-// and the reduction arrays as for simt_consumer.
-template <int HEAD_DIM, int GROUP, class E, class KV, int NS>
+// and the reduction arrays as for simt_consumer. With NPAIR = 2 there are
+// two sets of NCW consumer warps (cw = set * NCW + warp in the set) that
+// take turns on stages: set (r % 2) consumes ring position r, so a stage
+// needs NCW arrivals, and twice as many warps work on the item.
+template <int HEAD_DIM, int GROUP, class E, class KV, int NS, int NPAIR = 1>
 __device__ __forceinline__ bool mma_consumer(const DecodeParams& prm, const WorkItem& item,
                                              int n_tok, int lead, int n_tiles, int r0,
                                              bool hold_last, int cw, const DecRing& R,
@@ -165,7 +168,8 @@ __device__ __forceinline__ bool mma_consumer(const DecodeParams& prm, const Work
   using ME = std::conditional_t<FP8, Fp16, E>;
   constexpr int KS = HEAD_DIM / 16;       // k-steps of K Q^T
   constexpr int MB = HEAD_DIM / 16;       // 16-dim row blocks of O^T
-  const int warp = cw, lane = threadIdx.x & 31;
+  const int warp = cw % C::NCW, lane = threadIdx.x & 31;   // warp: its part of a stage
+  const int set = cw / C::NCW;                               // its turn among the stages
   const int g = lane >> 2;                // fragment row group (token g / g + 8; B column g)
   const int c = lane & 3;                 // this lane's head columns 2c, 2c + 1
   // score scale in the log2 domain, with the kv head's key scale
@@ -205,6 +209,7 @@ __device__ __forceinline__ bool mma_consumer(const DecodeParams& prm, const Work
   float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f}, lp[2] = {0.f, 0.f};
 
   for (int i = 0; i < n_tiles; ++i) {
+    if (NPAIR > 1 && (r0 + i) % NPAIR != set) continue;   // the other set's stage
     const int s = ring_stage<NS>(R, r0 + i);
     if (!mbar_wait_warp(smem_u32(&R.full[s]), ring_phase<NS>(R, r0 + i), prm.wait_limit_ns,
                         abort_flag)) {
@@ -417,13 +422,13 @@ __device__ __forceinline__ bool mma_consumer(const DecodeParams& prm, const Work
       lp[h] += __shfl_xor_sync(0xffffffffu, lp[h], x);
     }
   }
-  const bool aborted = named_bar_or(1, C::NCW * 32, *abort_flag != 0);
+  const bool aborted = named_bar_or(1, C::NCW * NPAIR * 32, *abort_flag != 0);
   if (!aborted) {
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
       const int head = 2 * c + h;
       if (head < GROUP) {
-        float* op = red_o + (warp * GROUP + head) * HEAD_DIM;
+        float* op = red_o + (cw * GROUP + head) * HEAD_DIM;
 #pragma unroll
         for (int t = 0; t < MB; ++t) {
           // rows g and g + 8 of block t: dims 16t + g and + 8, or with FP8
@@ -434,9 +439,9 @@ __device__ __forceinline__ bool mma_consumer(const DecodeParams& prm, const Work
           op[d1] = o[t][h + 2];
         }
         if (g == 0) {
-          red_m[warp * GROUP + head] = m[h];
-          red_l[warp * GROUP + head] = l[h];
-          red_lp[warp * GROUP + head] = lp[h];
+          red_m[cw * GROUP + head] = m[h];
+          red_l[cw * GROUP + head] = l[h];
+          red_lp[cw * GROUP + head] = lp[h];
         }
       }
     }
@@ -670,27 +675,29 @@ __device__ __forceinline__ bool simt_consumer(const DecodeParams& prm, const Wor
 // is a shared-memory word. `red_ok` false means the item had no keys and no
 // reduction area: every warp's state is empty, and the split merge reads its
 // weights from global memory.
-template <int HEAD_DIM, int GROUP, class E, class KV>
+template <int HEAD_DIM, int GROUP, class E, class KV, int NCONS = 0>
 __device__ __forceinline__ void decode_finish(const DecodeParams& prm, const WorkItem& item,
                                               int ctid, bool red_ok, float* red_o, float* red_m,
                                               float* red_l, float* red_lp, int* merge_last) {
   constexpr bool FP8 = std::is_same<KV, E4m3>::value;
   using C = DecodeCfg<HEAD_DIM, GROUP, FP8 ? 1 : 2>;
+  // consumer warps whose states are merged (NCONS, or the configuration's)
+  constexpr int NW = NCONS > 0 ? NCONS : C::NCW;
   const int tid = ctid;
   // the value scale of the cache, with the kv head's factor
   const float v_scale =
       prm.v_scale * (prm.v_head_scale ? prm.v_head_scale[item.head] : 1.f);
-  named_bar_sync(1, C::NCW * 32);
-  for (int idx = tid; idx < GROUP * HEAD_DIM; idx += C::NCW * 32) {
+  named_bar_sync(1, NW * 32);
+  for (int idx = tid; idx < GROUP * HEAD_DIM; idx += NW * 32) {
     const int h = idx / HEAD_DIM, dd = idx % HEAD_DIM;
     float rf = 0.f, L = 0.f, LP = 0.f, O = 0.f;
     if (red_ok) {
       float M = -INFINITY;
 #pragma unroll
-      for (int w = 0; w < C::NCW; ++w) M = fmaxf(M, red_m[w * GROUP + h]);
+      for (int w = 0; w < NW; ++w) M = fmaxf(M, red_m[w * GROUP + h]);
       rf = (M == -INFINITY) ? 0.f : M;
 #pragma unroll
-      for (int w = 0; w < C::NCW; ++w) {
+      for (int w = 0; w < NW; ++w) {
         const float sc = ex2(red_m[w * GROUP + h] - rf);
         L = fmaf(red_l[w * GROUP + h], sc, L);
         LP = fmaf(red_lp[w * GROUP + h], sc, LP);
@@ -717,7 +724,7 @@ __device__ __forceinline__ void decode_finish(const DecodeParams& prm, const Wor
   // states (bypassing L1). The merge order is fixed by the slots, so the
   // result does not depend on which CTA comes last.
   if (item.slot >= 0) {
-    named_bar_sync(1, C::NCW * 32);
+    named_bar_sync(1, NW * 32);
     if (tid == 0) {
       const MergeTask mt = prm.merges[item.merge];
       const int hkv = prm.num_qo_heads / GROUP;
@@ -726,7 +733,7 @@ __device__ __forceinline__ void decode_finish(const DecodeParams& prm, const Wor
       *merge_last = prev == uint32_t(mt.n_states - 1);
       if (*merge_last) __threadfence();
     }
-    named_bar_sync(1, C::NCW * 32);
+    named_bar_sync(1, NW * 32);
     if (*reinterpret_cast<volatile int*>(merge_last)) {
       const MergeTask mt = prm.merges[item.merge];
       // per head: M = max_i lse_i and w_i = exp(lse_i - M) / sum_j exp(lse_j - M),
@@ -734,7 +741,7 @@ __device__ __forceinline__ void decode_finish(const DecodeParams& prm, const Wor
       float* wgt = red_o;                       // [n_states][GROUP] when it fits
       float* hm = red_m;                        // [GROUP]: M
       float* hs = red_l;                        // [GROUP]: sum of exp(lse_i - M)
-      const bool fits = red_ok && mt.n_states * GROUP <= C::NCW * GROUP * HEAD_DIM;
+      const bool fits = red_ok && mt.n_states * GROUP <= NW * GROUP * HEAD_DIM;
       __shared__ float hm_g[GROUP], hs_g[GROUP];  // when there is no reduction area
       if (!red_ok) {
         hm = hm_g;
@@ -768,8 +775,8 @@ __device__ __forceinline__ void decode_finish(const DecodeParams& prm, const Wor
         const size_t orow = size_t(mt.out_row) * prm.num_qo_heads + hq;
         if (prm.lse) prm.lse[orow] = sw > 0.f ? M + lg2(sw) * kDecLn2 : -INFINITY;
       }
-      named_bar_sync(1, C::NCW * 32);
-      for (int idx = tid; idx < GROUP * HEAD_DIM; idx += C::NCW * 32) {
+      named_bar_sync(1, NW * 32);
+      for (int idx = tid; idx < GROUP * HEAD_DIM; idx += NW * 32) {
         const int h = idx / HEAD_DIM, dd = idx % HEAD_DIM;
         const int hq = item.head * GROUP + h;
         const float M = hm[h], sw = hs[h];

@@ -62,10 +62,13 @@ inline int prefill_kv_tile(int head_dim) { return head_dim <= 128 ? 128 : 64; }
 struct WorkspaceLayout {
   size_t decode_items = 0, prefill_items = 0, prefix_items = 0, prefix_tables = 0, merges = 0,
          merge_counters = 0, partial_o = 0, partial_lse = 0;
+  size_t image_end = 0;   // the run calls upload [0, image_end): header, work lists, merges
+  // the page table of a host-buffer call (page indptr | page indices | last
+  // page lengths | qo indptr), right after the image, uploaded with it
+  size_t hio_tables = 0;
   size_t total = 0;
-  // host-buffer calls only, after `total`: the step's q, page table (page
-  // indptr | page indices | last page lengths | qo indptr), out and lse
-  size_t hio_q = 0, hio_tables = 0, hio_out = 0, hio_lse = 0;
+  // host-buffer calls only, after `total`: the step's q, out and lse
+  size_t hio_q = 0, hio_out = 0, hio_lse = 0;
   size_t hio_total = 0;   // bytes of that region
 };
 

@@ -4,11 +4,27 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
+
 #include "fi_internal.h"
 
 namespace fi {
 
 constexpr uint64_t kDefaultWaitLimitNs = 1000000000ull;  // 1 s per bounded wait
+
+// Runs `fn` (a kernel's attribute setup and checks) the first time a launch
+// site is used on a device; later launches on that device skip it. `mask`
+// holds a bit per device (devices 64 and up always run `fn`).
+template <class F>
+inline cudaError_t once_per_device(std::atomic<uint64_t>& mask, F fn) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return cudaGetLastError();
+  const bool tracked = dev >= 0 && dev < 64;
+  if (tracked && ((mask.load(std::memory_order_acquire) >> dev) & 1u)) return cudaSuccess;
+  const cudaError_t e = fn();
+  if (e == cudaSuccess && tracked) mask.fetch_or(uint64_t(1) << dev, std::memory_order_acq_rel);
+  return e;
+}
 
 struct DecodeParams {
   const WorkItem* items;

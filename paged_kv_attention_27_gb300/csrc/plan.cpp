@@ -333,7 +333,8 @@ fi_status build_plan(int32_t mode, int32_t batch, const int32_t* qo_indptr,
   }
 
   // ---- workspace: header | decode items | prefill items | prefix items |
-  //      prefix tables | merges | merge counters | partial o | partial lse
+  //      prefix tables | merges | merge counters (the uploaded image ends
+  //      here) | host-buffer page table | partial o | partial lse
   size_t off = kHeaderBytes;
   p.ws.decode_items = off;
   off = align_up(off + p.decode_items.size() * sizeof(WorkItem));
@@ -349,21 +350,23 @@ fi_status build_plan(int32_t mode, int32_t batch, const int32_t* qo_indptr,
   // run: the CTA that completes a split's last chunk merges it
   p.ws.merge_counters = off;
   off = align_up(off + p.merges.size() * size_t(num_kv_heads) * sizeof(uint32_t));
+  p.ws.image_end = off;
+  // the page table (plus qo_indptr for a prefill plan) of a host-buffer
+  // call, as int32, right after the image: both cross the link in one copy
+  p.page_entries = batch > 0 ? page_indptr[batch] : 0;
+  const size_t table_ints = size_t(batch + 1) + size_t(p.page_entries) + size_t(batch) +
+                            (mode == FI_MODE_PREFILL ? size_t(batch + 1) : 0);
+  p.ws.hio_tables = off;
+  off = align_up(off + table_ints * sizeof(int32_t));
   p.ws.partial_o = off;
   off = align_up(off + size_t(p.num_slots) * num_qo_heads * head_dim * sizeof(float));
   p.ws.partial_lse = off;
   off = align_up(off + size_t(p.num_slots) * num_qo_heads * sizeof(float));
   p.ws.total = off;
-  // host-buffer calls: q and out of the plan's 16-bit dtype, fp32 lse, and
-  // the page table (plus qo_indptr for a prefill plan) as int32
-  p.page_entries = batch > 0 ? page_indptr[batch] : 0;
+  // host-buffer calls: q and out of the plan's 16-bit dtype, fp32 lse
   const size_t q_bytes = size_t(p.total_q) * num_qo_heads * head_dim * 2;
-  const size_t table_ints = size_t(batch + 1) + size_t(p.page_entries) + size_t(batch) +
-                            (mode == FI_MODE_PREFILL ? size_t(batch + 1) : 0);
   p.ws.hio_q = off;
   off = align_up(off + q_bytes);
-  p.ws.hio_tables = off;
-  off = align_up(off + table_ints * sizeof(int32_t));
   p.ws.hio_out = off;
   off = align_up(off + q_bytes);
   p.ws.hio_lse = off;

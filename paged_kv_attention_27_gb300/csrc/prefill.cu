@@ -55,7 +55,7 @@ constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;   // log2 units: rescale when the max grows by > 2^8
 
 // DG > 0: the mixed kernel, which also runs batch decode (groups of DG query
-// heads per kv head) on warps 7 and up of the same CTA.
+// heads per kv head) on warps 7-11 of the same CTA.
 template <int HEAD_DIM, class E, int DG = 0>
 struct PrefillCfg {
   static constexpr int M = kPrefillTileM;                   // 128 query rows
@@ -64,9 +64,14 @@ struct PrefillCfg {
   static constexpr bool MIXED = DG > 0;
   using DC = DecodeCfg<HEAD_DIM, (DG > 0 ? DG : 1), 2>;
   // 4 softmax warps, K producer, MMA issuer, V producer; the mixed kernel
-  // adds a decode producer (warp 7) and the decode consumer warps (from 8 on:
-  // four on CUDA cores, or two driving m16n8k16 MMAs)
-  static constexpr int THREADS = MIXED ? 256 + 32 * DC::NCW : 224;
+  // adds a decode producer (warp 7) and four decode consumer warps (8-11):
+  // on CUDA cores, or as two sets of two m16n8k16 warps taking turns on
+  // stages (two warps alone could not keep pace with one SM's share of HBM)
+  static constexpr int DEC_PAIRS = (MIXED && DC::MMA) ? 2 : 1;
+  static constexpr int DEC_WARPS = DC::NCW * DEC_PAIRS;
+  static constexpr int THREADS = MIXED ? 256 + 32 * DEC_WARPS : 224;
+  static_assert(!MIXED || DEC_WARPS * DG * HEAD_DIM * 4 + 3 * DEC_WARPS * DG * 4 <=
+                              DC::STAGE_BYTES, "reduction area within one decode stage");
   // d = 256 leaves no TMEM columns for P: P of tile g is written over its
   // S buffer (g & 1), which the MMA issuer then frees after that tile's PV
   static constexpr bool P_IN_S = HEAD_DIM > 128;
@@ -88,14 +93,16 @@ struct PrefillCfg {
   static constexpr int DEC_STAGES_EXT =
       MIXED ? DC::NSTAGE + (OFF_DEC - OFF_K) / DC::STAGE_BYTES : 1;
   static_assert(!MIXED || (OFF_DEC - OFF_K) % DC::STAGE_BYTES == 0, "");
-  // mixed kernel: the softmax warpgroup raises its registers to 224 per
-  // thread, the helper warpgroup (prefill producers, MMA issuer, decode
-  // producer) lowers them to 56, the decode consumers keep the launch count
-  // R. The shares fit the launch allocation when 128 x (224 + 56) <= 256 x R
-  // (R >= 140; the compiler's cap is 168 for 384 threads, 200 for 320); the
-  // host checks the compiled R before the launch.
-  static constexpr uint32_t SOFTMAX_REGS = 224, HELPER_REGS = 56;
-  static constexpr uint32_t MIN_LAUNCH_REGS = (128 * (SOFTMAX_REGS + HELPER_REGS) + 255) / 256;
+  // mixed kernel (384 threads): the softmax warpgroup raises its registers
+  // to 224 per thread, the helper warpgroup (prefill producers, MMA issuer,
+  // decode producer) lowers them to 56, the decode consumer warpgroup raises
+  // them to 184. The shares fit the launch allocation of R per thread when
+  // 128 x (224 + 56 + 184) <= 384 x R, i.e. R >= 155 (the compiler's cap for
+  // 384 threads is 168); the host checks the compiled R before the launch.
+  static constexpr uint32_t SOFTMAX_REGS = 224, HELPER_REGS = 56, DECODE_REGS = 184;
+  static constexpr uint32_t MIN_LAUNCH_REGS =
+      (128 * (SOFTMAX_REGS + HELPER_REGS + DECODE_REGS) + 383) / 384;
+  static_assert(!MIXED || THREADS == 384, "four warpgroups");
   static_assert(!MIXED || HEAD_DIM == 256, "mixed kernel: head_dim 256");
   // keep one CTA per SM (each CTA takes all 512 TMEM columns)
   static constexpr int SMEM_BYTES = (USED < 120 * 1024 ? 120 * 1024 : USED) + 1024;
@@ -148,7 +155,7 @@ __device__ __forceinline__ int item_tiles(const WorkItem& w) {
 }
 
 // The kernel body, shared by prefill_kernel (DG = 0) and mixed_kernel
-// (DG > 0: decode work items dprm.items[0 .. n_dec) run on warps 7 and up of the
+// (DG > 0: decode work items dprm.items[0 .. n_dec) run on warps 7-11 of the
 // same CTAs, taken from *dec_counter).
 template <int HEAD_DIM, class E, int DG>
 __device__ __forceinline__ void prefill_body(const CUtensorMap& q_map, const CUtensorMap& k_map,
@@ -219,7 +226,7 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap& q_map, const CUt
       }
       for (int s = 0; s < kItemRing; ++s) {
         mbar_init(smem_u32(&bars.ditem_full[s]), 1);
-        mbar_init(smem_u32(&bars.ditem_empty[s]), DC::NCW);
+        mbar_init(smem_u32(&bars.ditem_empty[s]), C::DEC_WARPS);
       }
       for (int s = 0; s < C::DEC_STAGES_EXT; ++s) {
         mbar_init(smem_u32(&bars.e_full[s]), 1);
@@ -247,7 +254,7 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap& q_map, const CUt
   // register share first (one setmaxnreg per warpgroup, so that every code
   // path after it stays within that share): warps 0-3 compute the softmax of
   // whole rows, the helpers (warps 4-7) need few registers, the decode
-  // consumers (warps 8 on) keep the launch count.
+  // consumers (warps 8-11) hold the MMA fragments of a 256-dim row.
   if (warp < 4) {
     if constexpr (C::MIXED) setmaxnreg_inc<C::SOFTMAX_REGS>();
     // ------------------------------------------------------------ softmax + epilogue
@@ -921,11 +928,12 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap& q_map, const CUt
     }
   } else {
     if constexpr (C::MIXED) {
+      setmaxnreg_inc<C::DECODE_REGS>();
       // ------------------------------------------------------------ decode consumers (mixed kernel)
       // Batch decode on the same SM: the decode producer (warp 7) takes
       // decode items from a global counter in the planner's longest-first
       // order and streams their pages through the decode ring; the decode
-      // consumers (warps 8 on) work through them in order. The HBM-bound
+      // consumers (warps 8-11) work through them in order. The HBM-bound
       // decode work thus runs beside the tensor-bound prefill tiles of the
       // same CTA instead of after them. An item's reduction area is the ring
       // stage of its last tile, released once the item is written.
@@ -934,7 +942,7 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap& q_map, const CUt
       const DecRing ring_b{base + C::OFF_DEC, base + C::OFF_K, DC::NSTAGE, C::DEC_STAGES_EXT,
                            bars.e_full, bars.e_empty};
       bool extended = false;                      // on the long ring (switch marker seen)
-      const int cw = warp - 8;                    // consumer warp 0..NCW-1
+      const int cw = warp - 8;                    // consumer warp 0..DEC_WARPS-1
       const int ctid = int(threadIdx.x) - 256;    // consumer thread
       int r = 0;
       for (int dn = 0;; ++dn) {
@@ -950,7 +958,7 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap& q_map, const CUt
         idx = __shfl_sync(0xffffffffu, idx, 0);
         // the consumer warps leave together (a warp that left alone would
         // never reach their named barriers); all read the same index
-        if (named_bar_or(2, DC::NCW * 32, !good || idx == -1)) break;
+        if (named_bar_or(2, C::DEC_WARPS * 32, !good || idx == -1)) break;
         if (idx == -2) {                          // the ring grows: position 0 of the long one
           extended = true;
           r = 0;
@@ -966,27 +974,29 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap& q_map, const CUt
         const uint32_t red_addr = ring_addr(ring, last_stage, DC::STAGE_BYTES);
         float* red_o = hold ? reinterpret_cast<float*>(smem_raw + (red_addr - smem_u32(smem_raw)))
                             : nullptr;
-        float* red_m = red_o + DC::NCW * DG * HEAD_DIM;
-        float* red_l = red_m + DC::NCW * DG;
-        float* red_lp = red_l + DC::NCW * DG;
+        float* red_m = red_o + C::DEC_WARPS * DG * HEAD_DIM;
+        float* red_l = red_m + C::DEC_WARPS * DG;
+        float* red_lp = red_l + C::DEC_WARPS * DG;
         bool aborted;
         if (hold)
           aborted = DC::MMA
-                        ? mma_consumer<HEAD_DIM, DG, E, E, 0>(dprm, item, n_tok, lead, n_tiles, r,
-                                                              true, cw, ring, &abort_flag, red_o,
-                                                              red_m, red_l, red_lp)
+                        ? mma_consumer<HEAD_DIM, DG, E, E, 0, C::DEC_PAIRS>(
+                              dprm, item, n_tok, lead, n_tiles, r, true, cw, ring, &abort_flag,
+                              red_o, red_m, red_l, red_lp)
                         : simt_consumer<HEAD_DIM, DG, E, E, 0>(dprm, item, n_tok, lead, n_tiles,
                                                                r, true, cw, ring, &abort_flag,
                                                                red_o, red_m, red_l, red_lp);
         else
-          aborted = named_bar_or(1, DC::NCW * 32, abort_flag != 0);
+          aborted = named_bar_or(1, C::DEC_WARPS * 32, abort_flag != 0);
         if (aborted) break;                      // voted: all consumer warps agree
-        decode_finish<HEAD_DIM, DG, E, E>(dprm, item, ctid, hold, red_o, red_m, red_l, red_lp,
-                                          &dec_merge_last);
+        decode_finish<HEAD_DIM, DG, E, E, C::DEC_WARPS>(dprm, item, ctid, hold, red_o, red_m,
+                                                        red_l, red_lp, &dec_merge_last);
         if (hold) {
-          // every consumer warp is done with the reduction area
-          named_bar_sync(1, DC::NCW * 32);
-          if (lane == 0) mbar_arrive(smem_u32(&ring.empty[last_stage]));
+          // every consumer warp is done with the reduction area; the set that
+          // consumed the last tile releases its stage
+          named_bar_sync(1, C::DEC_WARPS * 32);
+          if (lane == 0 && cw / DC::NCW == (r + n_tiles - 1) % C::DEC_PAIRS)
+            mbar_arrive(smem_u32(&ring.empty[last_stage]));
         }
         r += n_tiles;
       }
@@ -1032,7 +1042,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
 }
 
 // One persistent launch over a mixed batch: the prefill items as in
-// prefill_kernel, and on warps 7 and up of the same CTAs the decode items
+// prefill_kernel, and on warps 7-11 of the same CTAs the decode items
 // (dprm.items[0 .. n_dec), groups of DG query heads per kv head), handed out
 // longest first from *dec_counter (zero before the launch).
 template <int HEAD_DIM, class E, int DG>
@@ -1048,8 +1058,11 @@ cudaError_t launch_prefill_t(const CUtensorMap& qm, const CUtensorMap& km, const
                              const PrefillParams& p, int grid, cudaStream_t stream) {
   using C = PrefillCfg<HEAD_DIM, E>;
   auto kern = prefill_kernel<HEAD_DIM, E>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       C::SMEM_BYTES);
+  static std::atomic<uint64_t> configured{0};
+  cudaError_t e = once_per_device(configured, [&] {
+    return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                C::SMEM_BYTES);
+  });
   if (e != cudaSuccess) return e;
   kern<<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(qm, km, vm, p);
   return cudaGetLastError();
@@ -1073,12 +1086,16 @@ cudaError_t launch_mixed_t(const CUtensorMap& qm, const CUtensorMap& km, const C
                            uint32_t* dec_counter, int grid, cudaStream_t stream) {
   using C = PrefillCfg<256, E, DG>;
   auto kern = mixed_kernel<256, E, DG>;
-  // the per-warpgroup register split assumes this launch allocation
-  cudaFuncAttributes fa;
-  cudaError_t e = cudaFuncGetAttributes(&fa, kern);
-  if (e != cudaSuccess) return e;
-  if (fa.numRegs < int(C::MIN_LAUNCH_REGS)) return cudaErrorInvalidConfiguration;
-  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+  static std::atomic<uint64_t> configured{0};
+  cudaError_t e = once_per_device(configured, [&] {
+    // the per-warpgroup register split assumes this launch allocation
+    cudaFuncAttributes fa;
+    cudaError_t r = cudaFuncGetAttributes(&fa, kern);
+    if (r != cudaSuccess) return r;
+    if (fa.numRegs < int(C::MIN_LAUNCH_REGS)) return cudaErrorInvalidConfiguration;
+    return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                C::SMEM_BYTES);
+  });
   if (e != cudaSuccess) return e;
   kern<<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(qm, km, vm, p, dp, n_dec, dec_counter);
   return cudaGetLastError();

@@ -660,12 +660,16 @@ cudaError_t launch_pair_t(const CUtensorMap& qm, const CUtensorMap& km, const CU
                           const PrefillParams& p, int grid, cudaStream_t stream) {
   using C = PairCfg<HEAD_DIM, E>;
   auto kern = prefill_pair_kernel<HEAD_DIM, E>;
-  // the per-warpgroup register split assumes this launch allocation
-  cudaFuncAttributes fa;
-  cudaError_t e = cudaFuncGetAttributes(&fa, kern);
-  if (e != cudaSuccess) return e;
-  if (fa.numRegs != int(C::LAUNCH_REGS)) return cudaErrorInvalidConfiguration;
-  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+  static std::atomic<uint64_t> configured{0};
+  cudaError_t e = once_per_device(configured, [&] {
+    // the per-warpgroup register split assumes this launch allocation
+    cudaFuncAttributes fa;
+    cudaError_t r = cudaFuncGetAttributes(&fa, kern);
+    if (r != cudaSuccess) return r;
+    if (fa.numRegs != int(C::LAUNCH_REGS)) return cudaErrorInvalidConfiguration;
+    return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                C::SMEM_BYTES);
+  });
   if (e != cudaSuccess) return e;
   kern<<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(qm, km, vm, p);
   return cudaGetLastError();

@@ -461,22 +461,27 @@ def test_shared_prefix_validation(case, status):
 
 def test_host_buffer_call_sizes_its_region_and_checks_before_any_copy():
     """fi_batch_attention_host: the plan reports the workspace part that holds
-    the step's q, page table, out and lse (each region 256-byte aligned); bad
-    arguments and a short workspace are refused before anything is copied, and
-    a well-formed call on a machine without a GPU reports that."""
+    the step's q, out and lse (each region 256-byte aligned; the page table
+    sits in the run calls' part, right after the work lists, and crosses the
+    link with them); bad arguments and a short workspace are refused before
+    anything is copied, and a well-formed call on a machine without a GPU
+    reports that."""
     torch = pytest.importorskip("torch")
     if torch.cuda.is_available():
         pytest.skip("uses fake device addresses; only meaningful without a GPU")
     rnd = lambda n: (n + 255) // 256 * 256
-    # decode: 2 rows x 8 heads x d128 (bf16) for q and out; page table 3 + 3 + 2 int32
+    # decode: 2 rows x 8 heads x d128 (bf16) for q and out, fp32 lse
     p = B.fi_plan(B.FI_MODE_DECODE, 2, None, [0, 2, 3], [5, 16], 8, 2, 128, 16, 0, None, 4)
     info = B.fi_plan_get_info(p)
-    assert info["host_io_bytes"] == 2 * rnd(2 * 8 * 128 * 2) + rnd(8 * 4) + rnd(2 * 8 * 4)
+    assert info["host_io_bytes"] == 2 * rnd(2 * 8 * 128 * 2) + rnd(2 * 8 * 4)
+    # the page table (3 + 3 + 2 int32) is part of the run calls' workspace
+    p0 = B.fi_plan(B.FI_MODE_DECODE, 0, None, [0], [], 8, 2, 128, 16, 0, None, 4)
     # prefill: 4 rows; the page table gains qo_indptr (3 more int32)
     pf = B.fi_plan(B.FI_MODE_PREFILL, 2, [0, 3, 4], [0, 2, 3], [5, 16], 8, 2, 128, 16, 1,
                    None, 4)
     info_f = B.fi_plan_get_info(pf)
-    assert info_f["host_io_bytes"] == 2 * rnd(4 * 8 * 128 * 2) + rnd(11 * 4) + rnd(4 * 8 * 4)
+    assert info_f["host_io_bytes"] == 2 * rnd(4 * 8 * 128 * 2) + rnd(4 * 8 * 4)
+    del p0
 
     fake = 1 << 20    # aligned device address, never dereferenced here
     q_h = np.zeros((2, 8, 128), np.uint16)
@@ -505,6 +510,28 @@ def test_host_buffer_call_sizes_its_region_and_checks_before_any_copy():
     with pytest.raises(B.FiError) as e:
         B.fi_batch_attention_host(*args, stream=0)
     assert e.value.status == B.FI_ERR_NO_DEVICE
+    # the asynchronous form checks the same way, before a ticket exists
+    with pytest.raises(B.FiError) as e:
+        B.fi_batch_attention_host_async(*args[:-1], info["workspace_bytes"], stream=0)
+    assert e.value.status == B.FI_ERR_WORKSPACE_TOO_SMALL
+    with pytest.raises(B.FiError) as e:
+        B.fi_batch_attention_host_async(*args, stream=0)
+    assert e.value.status == B.FI_ERR_NO_DEVICE
+
+
+def test_host_step_tickets_without_a_device():
+    """An empty plan's step has ticket 0, which is always complete; a ticket
+    that was never issued is refused."""
+    p0 = B.fi_plan(B.FI_MODE_DECODE, 0, None, [0], [], 8, 2, 128, 16, 0, None, 4)
+    t = B.fi_batch_attention_host_async(p0, None, None, None, None, B.FI_LAYOUT_NHD, 0, 0,
+                                        None, None, None, 0.1, 1.0, 1.0, None, None, None, 0,
+                                        stream=0)
+    assert t == 0
+    B.fi_host_step_wait(0)
+    for bogus in (1, 9, 2**63 + 5):
+        with pytest.raises(B.FiError) as e:
+            B.fi_host_step_wait(bogus)
+        assert e.value.status == B.FI_ERR_INVALID_ARG
 
 
 def _check_prefill_cover(b, plan):

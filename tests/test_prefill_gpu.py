@@ -326,3 +326,45 @@ def test_host_buffer_call_matches_device_call(which):
     assert torch.equal(lse_h, lse_d.cpu())
     ref_o, ref_l = _oracle(b)
     compare(out_h, lse_h, ref_o, ref_l, what=f"host call, {b.name}")
+
+
+def test_async_host_steps_in_flight():
+    """fi_batch_attention_host_async: eight steps with their own q and
+    outputs in flight on one workspace; a ninth is refused while they are;
+    waiting for each in issue order gives, bitwise, what the device-buffer
+    call gives for that step's q; a ticket waited for twice is refused."""
+    from paged_kv_attention_27_gb300.device import DeviceBatch
+    b = synth.tiny_decode()
+    db = DeviceBatch(b)
+    info = B.fi_plan_get_info(db.plan)
+    ws_bytes = info["workspace_bytes"] + info["host_io_bytes"]
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=db.device)
+    g = torch.Generator().manual_seed(77)
+    qs = [torch.randn(db.q.shape, generator=g).to(db.q.dtype).pin_memory() for _ in range(8)]
+    outs = [(torch.empty(db.out.shape, dtype=db.out.dtype).pin_memory(),
+             torch.empty(db.lse.shape, dtype=torch.float32).pin_memory()) for _ in range(8)]
+    tables = (b.page_indptr.astype(np.int32), b.page_indices.astype(np.int32),
+              b.last_page_len.astype(np.int32))
+
+    def issue(q_h, out_h, lse_h):
+        return B.fi_batch_attention_host_async(
+            db.plan, q_h, None, db.k, db.v, B.LAYOUTS[b.layout], 0, b.num_pages, *tables,
+            b.sm_scale, b.k_scale, b.v_scale, out_h, lse_h, ws, ws_bytes,
+            k_head_scale=db.k_head_scale, v_head_scale=db.v_head_scale)
+
+    tickets = [issue(q, *o) for q, o in zip(qs, outs)]
+    assert len(set(tickets)) == 8 and 0 not in tickets
+    with pytest.raises(B.FiError) as e:
+        issue(qs[0], *outs[0])
+    assert e.value.status == B.FI_ERR_INVALID_ARG
+    for t in tickets:
+        B.fi_host_step_wait(t)
+    with pytest.raises(B.FiError) as e:
+        B.fi_host_step_wait(tickets[0])
+    assert e.value.status == B.FI_ERR_INVALID_ARG
+    for q_h, (out_h, lse_h) in zip(qs, outs):
+        db.q.copy_(q_h)
+        out_d, lse_d = db.run()
+        torch.cuda.synchronize()
+        assert torch.equal(out_h.view(torch.int16), out_d.cpu().view(torch.int16))
+        assert torch.equal(lse_h, lse_d.cpu())
