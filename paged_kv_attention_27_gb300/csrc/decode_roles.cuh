@@ -162,9 +162,10 @@ __device__ __forceinline__ bool mma_consumer(const DecodeParams& prm, const Work
                                              float* red_l, float* red_lp) {
   constexpr bool FP8 = std::is_same<KV, E4m3>::value;
   using C = DecodeCfg<HEAD_DIM, GROUP, FP8 ? 1 : 2>;
-  // With an FP8 cache the MMAs run in fp16: e4m3 widens to fp16 in one
-  // instruction per pair, exactly; q (bf16 or fp16) is converted once (exact
-  // within fp16's range) and P is rounded to fp16.
+  // With an FP8 cache the P V MMAs run in fp16: e4m3 widens to fp16 in one
+  // instruction per pair, exactly, and P is rounded to fp16. K Q^T runs in
+  // fp16 too at head_dim 64 (q converted once, exact within fp16's range)
+  // and in e4m3 at head_dim 128 (below).
   using ME = std::conditional_t<FP8, Fp16, E>;
   constexpr int KS = HEAD_DIM / 16;       // k-steps of K Q^T
   constexpr int MB = HEAD_DIM / 16;       // 16-dim row blocks of O^T
@@ -177,12 +178,81 @@ __device__ __forceinline__ bool mma_consumer(const DecodeParams& prm, const Work
       prm.sm_scale * kDecLog2e * (prm.k_head_scale ? prm.k_head_scale[item.head] : 1.f);
 
   // Q^T as B fragments: column = head g, rows (k) 2c, 2c + 1 and 2c + 8, 2c + 9
-  // of each k-step. With FP8 K fragments loaded from the cache rows, k index
-  // 2c + j of a k-step is dim 4c + j and 2c + 8 + j is dim 4c + 2 + j, so that
-  // a lane's four consecutive bytes of a key row feed both halves of its A
-  // fragment; Q's k order follows.
-  uint32_t qb[KS][2];
-  {
+  // of each k-step. With fp16 MMAs on FP8 K rows (fp16 q), k index 2c + j of
+  // a k-step is dim 4c + j and 2c + 8 + j is dim 4c + 2 + j, so that a lane's
+  // four consecutive bytes of a key row feed both halves of its A fragment;
+  // Q's k order follows.
+  uint32_t qb[C::SWZ8 && std::is_same<E, Bf16>::value ? 1 : KS][2];
+  // With FP8 K rows of 128 bytes and bf16 q, K Q^T runs as e4m3 MMAs
+  // (m16n8k32) on the cache bytes themselves: an ldmatrix of the rows gives a lane four
+  // consecutive dims 4c..4c+3 (and 16 + 4c..) of token g (and g + 8), the A
+  // fragment's layout, so K is never widened. Q enters as a sum of two e4m3
+  // terms, each the e4m3 rounding of what the terms before it left: the
+  // first after a power-of-two scale per head that puts the head's largest
+  // |element| in [128, 256), the others (whose inputs are at most 8 there)
+  // after a further 2^5, so that they do not fall into e4m3's subnormal
+  // range. Each term accumulates on its own and the two sums are scaled
+  // back when the scores are formed. The two terms hold a bf16 element (8
+  // significant bits) exactly for every element above 2^-14 of the head's
+  // largest; the error below that is under 2^-22 of the largest. B
+  // fragment: dims 32 ks + 4c..4c+3 and 32 ks + 16 + 4c.. of head g, one
+  // byte each. (fp16 q, 11 bits, would take three terms, which do not fit
+  // the registers: it keeps the fp16 MMAs.)
+  constexpr bool K8 = C::SWZ8 && std::is_same<E, Bf16>::value;
+  constexpr int KS8 = HEAD_DIM / 32;
+  constexpr int NQ = 2;
+  uint32_t q8[K8 ? KS8 : 1][NQ][2];
+  float qinv[2] = {1.f, 1.f};   // 2^-qe of heads 2c, 2c + 1 (this lane's score columns)
+  if constexpr (K8) {
+    const uint16_t* qh = reinterpret_cast<const uint16_t*>(prm.q) +
+        (size_t(item.q_row) * prm.num_qo_heads + item.head * GROUP + (g < GROUP ? g : 0)) *
+            HEAD_DIM;
+    float qf[KS8][2][4];
+    float amax = 0.f;
+#pragma unroll
+    for (int ks = 0; ks < KS8; ++ks)
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf) {
+        const uint2 u = g < GROUP
+            ? *reinterpret_cast<const uint2*>(qh + ks * 32 + hf * 16 + 4 * c)
+            : make_uint2(0u, 0u);
+        qf[ks][hf][0] = E::lo(u.x);
+        qf[ks][hf][1] = E::hi(u.x);
+        qf[ks][hf][2] = E::lo(u.y);
+        qf[ks][hf][3] = E::hi(u.y);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) amax = fmaxf(amax, fabsf(qf[ks][hf][j]));
+      }
+    // the head's largest |element| (its four lanes); a non-finite one gives NaN scores
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+    int ex = 0;
+    if (amax > 0.f && amax <= 3.0e38f) frexpf(amax, &ex);   // amax in [2^(ex-1), 2^ex)
+    ex = max(ex, -100);   // (a head of subnormal q: fewer bits, no overflow of the scale)
+    const float qsc = ldexpf(1.f, 8 - ex);
+    const float inv = amax <= 3.0e38f ? ldexpf(1.f, ex - 8) : __int_as_float(0x7fffffff);
+    qinv[0] = __shfl_sync(0xffffffffu, inv, 8 * c);
+    qinv[1] = __shfl_sync(0xffffffffu, inv, 8 * c + 4);
+#pragma unroll
+    for (int ks = 0; ks < KS8; ++ks)
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf) {
+        float x[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) x[j] = qf[ks][hf][j] * qsc;
+#pragma unroll
+        for (int t = 0; t < NQ; ++t) {
+          const uint32_t lo = E4m3::from_f32x2(x[0], x[1]), hi = E4m3::from_f32x2(x[2], x[3]);
+          q8[ks][t][hf] = lo | (hi << 16);
+          if (t + 1 < NQ) {
+            float r[4];
+            E4m3::unpack4(q8[ks][t][hf], r);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) x[j] = (x[j] - r[j]) * 32.f;
+          }
+        }
+      }
+  } else {
     const uint32_t* qp = reinterpret_cast<const uint32_t*>(
         reinterpret_cast<const uint16_t*>(prm.q) +
         (size_t(item.q_row) * prm.num_qo_heads + item.head * GROUP + (g < GROUP ? g : 0)) *
@@ -294,10 +364,25 @@ __device__ __forceinline__ bool mma_consumer(const DecodeParams& prm, const Work
       float sacc2[2][4] = {};
       // ldmatrix lanes 0-7 / 8-15 / 16-23 / 24-31 address matrices 0..3
       const int ltok = (lane & 7) + ((lane >> 3) & 1) * 8;   // token row this lane addresses
-      if constexpr (C::SWZ8) {
-        // K straight from the FP8 rows: each 8x8 matrix of byte pairs is 8
-        // tokens x 16 dims, and a lane's register is 4 consecutive dims 4c..4c+3
-        // of token g: widened, dims 4c, 4c+1 and 4c+2, 4c+3 are the A
+      if constexpr (K8) {
+        // K straight from the FP8 rows as the e4m3 A fragment: each 8x8
+        // matrix of byte pairs is 8 tokens x 16 dims, so a lane's register is
+        // dims 4c..4c+3 of one token. Matrices: (tokens 0-7 | 8-15) x (dims
+        // 32 ks .. +15 | 32 ks + 16 .. +31). Term 0 of Q goes to
+        // accumulator 0, term 1 (2^5 finer) to accumulator 1.
+        const int tok = cb + ltok;
+#pragma unroll
+        for (int ks = 0; ks < KS8; ++ks) {
+          const int ch = 2 * ks + (lane >> 4);
+          uint32_t a[4];
+          ldsm_x4(kstage + tok * 128 + ((ch ^ (tok & 7)) << 4), a[0], a[1], a[2], a[3]);
+#pragma unroll
+          for (int t = 0; t < NQ; ++t) E4m3::mma16832(sacc2[t > 0], a, q8[ks][t][0], q8[ks][t][1]);
+        }
+      } else if constexpr (C::SWZ8) {
+        // fp16 q: K widened from the FP8 rows. Each 8x8 matrix of byte pairs
+        // is 8 tokens x 16 dims, and a lane's register is 4 consecutive dims
+        // 4c..4c+3 of token g: widened, dims 4c, 4c+1 and 4c+2, 4c+3 are the A
         // fragment's (row g, k 2c..) and (row g, k 2c+8..) halves.
         // Matrices: (tokens 0-7 | 8-15) x (k-steps ks | ks+1).
         const int tok = cb + ltok;
@@ -330,7 +415,9 @@ __device__ __forceinline__ bool mma_consumer(const DecodeParams& prm, const Work
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const int tok = cb + g + (e >> 1) * 8;
-        sv[e] = (tok < ntok && tok >= lo) ? (sacc2[0][e] + sacc2[1][e]) * scale : -INFINITY;
+        const float acc = K8 ? fmaf(sacc2[1][e], 1.f / 32.f, sacc2[0][e])
+                                  : sacc2[0][e] + sacc2[1][e];
+        sv[e] = (tok < ntok && tok >= lo) ? acc * (scale * qinv[e & 1]) : -INFINITY;
       }
       float mx[2] = {fmaxf(sv[0], sv[2]), fmaxf(sv[1], sv[3])};
       // Lazy rescale: a head's reference changes only when one of its scores

@@ -88,6 +88,21 @@ struct E4m3 {
     const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(__nv_fp8x2_storage_t(w & 0xffffu), __NV_E4M3);
     return uint32_t(h.x) | (uint32_t(h.y) << 16);
   }
+  // two floats -> two packed e4m3 in the low 16 bits (a in the low byte),
+  // rounded to nearest even, finite values saturated at +-448
+  __device__ static __forceinline__ uint32_t from_f32x2(float a, float b) {
+    return uint32_t(__nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3));
+  }
+  // D += A B for A 16x32 (row-major) and B 32x8 (column-major) e4m3
+  // operands, four elements per register, fp32 accumulators
+  __device__ static __forceinline__ void mma16832(float (&d)[4], const uint32_t (&a)[4],
+                                                  uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k32.row.col.f32.e4m3.e4m3.f32 "
+        "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+  }
 };
 
 // Eight packed elements (one 16-byte chunk) -> eight floats.

@@ -292,6 +292,28 @@ def test_fp8_cache_per_head_scales(g, d):
     check(b, sms=8)
 
 
+@pytest.mark.parametrize("g", [1, 4, 8])
+@pytest.mark.parametrize("dtype", ["bf16", "fp16"])
+def test_fp8_cache_q_dynamic_range(g, dtype):
+    """With an FP8 cache at head_dim 128 and bf16 q, K Q^T runs as e4m3 MMAs
+    with q as a sum of two e4m3 terms under power-of-two scales per head
+    (fp16 q keeps fp16 MMAs). Elements spread over 2^-10..2^2 inside a head,
+    heads scaled by 2^-12, 1 or 2^6, one head all zeros, fp16 q using all 11
+    bits: the scores must still be those of the exact q."""
+    hkv = 2
+    kv = [1, 16, 300, 2049, 9000]
+    b = synth.make_batch(f"fp8 q range g{g} {dtype}", kv, [1] * len(kv), g * hkv, hkv, 128, 16,
+                         synth.NHD, None, False, 730 + g, dtype=dtype, kv_dtype="e4m3",
+                         kv_scale=1 / 16)
+    gen = synth.philox(731 + g)
+    shape = b.q.shape
+    q = gen.standard_normal(shape) * np.exp2(gen.uniform(-10, 2, shape))
+    q *= np.exp2(np.array([-12.0, 0.0, 6.0])[gen.integers(0, 3, shape[:2])])[..., None]
+    q[1, 0] = 0.0
+    b.q = synth.to_bits(q.astype(np.float32), dtype)
+    check(b, sms=8)
+
+
 def test_fp8_cache_70b_full_size_every_request():
     # the bench's FP8 batch: a per-head K and V scale on each of the 8 kv heads
     b = synth.llama70b_gqa_decode(kv_dtype="e4m3")
