@@ -55,9 +55,11 @@ struct DecodeCfg {
   // 16-bit cache with 2 or more heads per kv head takes them too: a shuffle-
   // reduced dot product of 256 dims costs a warp far more instructions per
   // token than the 16 + 16 MMAs of a 16-token chunk (and 8 heads did not fit
-  // the SIMT consumer's registers).
+  // the SIMT consumer's registers); so does an FP8 cache with 8 heads, whose
+  // SIMT consumer spilled.
   static constexpr bool MMA = (HEAD_DIM <= 128 && (GROUP >= 4 || KVB == 1)) ||
-                              (HEAD_DIM == 256 && KVB == 2 && GROUP >= 2);
+                              (HEAD_DIM == 256 && KVB == 2 && GROUP >= 2) ||
+                              (HEAD_DIM == 256 && KVB == 1 && GROUP >= 8);
   // tokens per stage: 32 KB of K+V, for 16-bit caches and the FP8 tensor-core
   // consumer (two 16-token chunks per consumer warp and stage); 16 KB for
   // the FP8 SIMT consumer, which runs three CTAs per SM
@@ -86,8 +88,11 @@ struct DecodeCfg {
   static constexpr int SMEM_BYTES = NSTAGE * STAGE_BYTES + CONV_BYTES + 1024;  // + alignment
   // CTAs per SM: three for the tensor-core consumer (two 32 KB stages, at
   // most 136 registers) and for the FP8 SIMT consumer of 1 or 2 heads (65 KB),
-  // for more warps to hide their latency; two otherwise
-  static constexpr int MIN_BLOCKS = (MMA || (KVB == 1 && GROUP <= 2)) ? 3 : 2;
+  // for more warps to hide their latency; two otherwise, and for the FP8
+  // tensor-core consumer at head_dim 256, whose 32 KB widening scratch
+  // makes a CTA 97 KB
+  static constexpr int MIN_BLOCKS =
+      ((MMA && !(KVB == 1 && HEAD_DIM == 256)) || (KVB == 1 && GROUP <= 2)) ? 3 : 2;
   static_assert(PASSES % SUB == 0, "");
   static_assert(!MMA || TOK_PER_WARP % 16 == 0, "");
   static_assert(NCW * GROUP * HEAD_DIM * 4 + 3 * NCW * GROUP * 4 <= NSTAGE * STAGE_BYTES, "");
@@ -539,7 +544,14 @@ __device__ __forceinline__ bool mma_consumer(const DecodeParams& prm, const Work
 
 // Producer warp: the TMA copies of one item's tiles into ring positions r0,
 // r0 + 1, ... One box per (page, 64-dim slice) of a 16-bit cache, per page
-// of an FP8 cache; the lanes read up to 32 page ids of a tile at once.
+// of an FP8 cache. The lanes read a tile's page ids (up to 32) at once, after
+// the wait for its stage. On a ring sized at run time (NS = 0: the mixed
+// kernel, where the decode copies share the SM with prefill work) the page
+// ids are read 32 at a time instead (lane j holds page j of the batch), the
+// next batch as soon as the current one is started, and each tile takes its
+// 1-16 pages from the batch by a shuffle, so that a freed stage is refilled
+// without a page-table round trip. (In the decode kernel, three CTAs per SM
+// hide that round trip, and the batched form measured 1-2 % slower.)
 // `skip_first` (test hook) leaves the first tile's copies out, so that the
 // consumers' bounded waits run out. Returns the number of tiles whose copies
 // were issued (n_tiles, unless a wait for a free stage ran out).
@@ -554,9 +566,29 @@ __device__ __forceinline__ int decode_produce(const DecodeParams& prm, const Wor
   const int pages_per_tile = C::TILE / prm.page_size;
   const uint32_t box_bytes = uint32_t(prm.page_size) * (FP8 ? HEAD_DIM : 128u);
   constexpr int BOXES = FP8 ? 1 : C::DBLK;
+  // pages per tile: 1-16 (page size 16 or 32), a divisor of 32
+  const int item_pages = (n_tok + prm.page_size - 1) / prm.page_size;
+  const int tiles_per_batch = 32 / pages_per_tile;
+  auto batch_ids = [&](int b) {   // this lane's page id of 32-page batch b (-1 past the item)
+    const int p = b * 32 + lane;
+    return p < item_pages ? prm.page_indices[item.page_begin + p] : -1;
+  };
+  constexpr bool BATCHED = NS == 0;
+  int cur = BATCHED && n_tiles > 0 ? batch_ids(0) : -1;
+  int nxt = BATCHED && item_pages > 32 ? batch_ids(1) : -1;
   for (int i = 0; i < n_tiles; ++i) {
     const int r = r0 + i;
     const int s = ring_stage<NS>(R, r);
+    int page = -1;
+    if constexpr (BATCHED) {
+      const int k = i % tiles_per_batch;
+      if (k == 0 && i > 0) {
+        const int b = i / tiles_per_batch;
+        cur = nxt;
+        if ((b + 1) * 32 < item_pages) nxt = batch_ids(b + 1);
+      }
+      page = __shfl_sync(0xffffffffu, cur, k * pages_per_tile + lane % pages_per_tile);
+    }
     if (r >= (NS > 0 ? NS : R.n)) {
       const uint32_t ph = ring_phase<NS>(R, r) ^ 1u;
       if (!mbar_wait_warp(smem_u32(&R.empty[s]), ph, prm.wait_limit_ns, abort_flag)) {
@@ -564,13 +596,10 @@ __device__ __forceinline__ int decode_produce(const DecodeParams& prm, const Wor
         return i;
       }
     }
-    const int tok0 = i * C::TILE;                 // relative to the first page
-    const int tok_in_tile = min(C::TILE, n_tok - tok0);
-    const int np = (tok_in_tile + prm.page_size - 1) / prm.page_size;
-    int page = -1;
+    const int np = (min(C::TILE, n_tok - i * C::TILE) + prm.page_size - 1) / prm.page_size;
     bool valid = false;
     if (lane < np) {
-      page = prm.page_indices[item.page_begin + i * pages_per_tile + lane];
+      if constexpr (!BATCHED) page = prm.page_indices[item.page_begin + i * pages_per_tile + lane];
       valid = page >= 0 && page < prm.num_pages;
       if (!valid) atomicOr(prm.err, kErrBounds);
     }

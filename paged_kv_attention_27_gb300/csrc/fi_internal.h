@@ -57,6 +57,13 @@ constexpr uint32_t kErrTimeout = 1u;
 constexpr uint32_t kErrBounds = 2u;
 
 inline int decode_tile_tokens(int head_dim) { return 8192 / head_dim; }  // 32 KB of K+V
+// A batch with both decode rows and multi-row (chunked prefill) requests runs
+// as one persistent launch of the mixed kernel for these shapes (q/out and
+// cache of one 16-bit type, head_dim 256, 1, 2 or 4 query heads per kv head).
+inline bool mixed_kernel_applies(int head_dim, int group, int dtype, int kv_dtype) {
+  return head_dim == 256 && (group == 1 || group == 2 || group == 4) && kv_dtype == dtype &&
+         (dtype == FI_DTYPE_BF16 || dtype == FI_DTYPE_FP16);
+}
 inline int prefill_kv_tile(int head_dim) { return head_dim <= 128 ? 128 : 64; }
 
 struct WorkspaceLayout {

@@ -1104,8 +1104,7 @@ cudaError_t launch_mixed_t(const CUtensorMap& qm, const CUtensorMap& km, const C
 }  // namespace
 
 bool mixed_applies(int head_dim, int group, int dtype, int kv_dtype) {
-  return head_dim == 256 && (group == 1 || group == 2 || group == 4) && kv_dtype == dtype &&
-         (dtype == FI_DTYPE_BF16 || dtype == FI_DTYPE_FP16);
+  return mixed_kernel_applies(head_dim, group, dtype, kv_dtype);
 }
 
 cudaError_t launch_mixed(int head_dim, int group, int dtype, const CUtensorMap& qm,
