@@ -50,7 +50,8 @@ NOMINAL_HBM_GBS = 8000.0      # HBM3e data-sheet figure (about 8 TB/s)
 SECONDARY = [("llama70b_gqa_decode", 200), ("causal_prefill_1k", 200),
              ("causal_prefill_4k", 100), ("causal_prefill_16k", 30),
              ("causal_prefill_32k", 30), ("ragged_prefill", 60), ("mixed_chunk_decode", 100),
-             ("gqa_decode_d256", 100)]
+             ("gqa_decode_d256", 100), ("long_context_chunk", 100),
+             ("long_context_chunk_hq32", 100)]
 
 
 def parse_args():
@@ -97,6 +98,8 @@ WORKLOADS = {
     "ragged_prefill": ("ragged_prefill", {}),
     "mixed_chunk_decode": ("mixed_chunk_decode", {}),
     "gqa_decode_d256": ("gqa_decode_d256", {}),
+    "long_context_chunk": ("long_context_chunk", {}),
+    "long_context_chunk_hq32": ("long_context_chunk", {"num_qo_heads": 32}),
 }
 
 
@@ -159,6 +162,7 @@ KERNEL_SOURCES = {
     "mixed_kernel": ["prefill.cu", "decode_roles.cuh", "ptx.cuh", "kernels.cuh",
                      "fi_internal.h"],
     "prefill_pair_kernel": ["prefill_pair.cu", "ptx.cuh", "kernels.cuh", "fi_internal.h"],
+    "merge_kernel": ["merge.cu", "kernels.cuh", "fi_internal.h"],
 }
 
 
@@ -449,7 +453,8 @@ def config_of(b, info, kvb, flops):
                    "every timed step (a 258 MB write, not timed)")}
     if info is not None:
         cfg["plan"] = {k: info[k] for k in ("num_decode_items", "num_prefill_items",
-                                            "chunk_tokens", "num_split_requests")}
+                                            "chunk_tokens", "num_split_requests",
+                                            "num_partial_slots")}
     return cfg
 
 
@@ -488,10 +493,18 @@ def mixed_fused(b, info):
             b.head_dim == 256 and g in (1, 2, 4) and b.cache_dtype == b.dtype)
 
 
+def prefill_split(info):
+    """Whether a plan cut its prefill tiles into pieces (a launch of under two
+    waves; only plans without decode rows): one merge launch follows."""
+    return (bool(info["num_prefill_items"]) and not info["num_decode_items"] and
+            info["num_partial_slots"] > 0)
+
+
 def launches_per_step(b, info):
     if mixed_fused(b, info):
         return 1
-    return (1 if info["num_decode_items"] else 0) + (1 if info["num_prefill_items"] else 0)
+    return ((1 if info["num_decode_items"] else 0) + (1 if info["num_prefill_items"] else 0) +
+            (1 if prefill_split(info) else 0))
 
 
 def kernels_of(b, info):
@@ -507,6 +520,8 @@ def kernels_of(b, info):
         names.append("prefill_pair_kernel" if pair else "prefill_kernel")
     if info["num_decode_items"]:
         names.append("decode_kernel")
+    if prefill_split(info):
+        names.append("merge_kernel")
     return names
 
 

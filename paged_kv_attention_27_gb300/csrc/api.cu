@@ -102,8 +102,10 @@ void fill_image(uint8_t* dst, const fi::Plan& P) {
        P.prefill_items.size() * sizeof(fi::WorkItem)},
       {P.ws.prefix_items, P.ws.prefix_tables, P.prefix_items.data(),
        P.prefix_items.size() * sizeof(fi::WorkItem)},
-      {P.ws.prefix_tables, P.ws.merges, P.prefix_tables.data(),
+      {P.ws.prefix_tables, P.ws.prefill_merges, P.prefix_tables.data(),
        P.prefix_tables.size() * sizeof(int32_t)},
+      {P.ws.prefill_merges, P.ws.merges, P.prefill_merges.data(),
+       P.prefill_merges.size() * sizeof(fi::MergeTask)},
       {P.ws.merges, P.ws.image_end, P.merges.data(), P.merges.size() * sizeof(fi::MergeTask)},
   };
   for (const Region& r : regions) {
@@ -513,6 +515,8 @@ fi_status run_paged(fi_plan_t plan, bool prefill_call, const void* q, const int3
   pp.work_counter = reinterpret_cast<uint32_t*>(ws + fi::kWorkCounterOffset);
   pp.state_o = nullptr;
   pp.state_lse = nullptr;
+  pp.piece_o = partial_o;
+  pp.piece_lse = partial_lse;
 
   fi::DecodeParams dp;
   dp.items = reinterpret_cast<const fi::WorkItem*>(ws + P.ws.decode_items);
@@ -568,6 +572,22 @@ fi_status run_paged(fi_plan_t plan, bool prefill_call, const void* q, const int3
     if (!P.prefill_items.empty()) {
       e = fi::launch_prefill(P.head_dim, P.dtype, qmap, kmap, vmap, pp, P.num_sms, stream);
       if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
+    }
+    if (!P.prefill_merges.empty()) {
+      // Split prefill tiles: each row's piece states, merged by log-sum-exp
+      // into out and lse (same stream, after the prefill launch)
+      fi::MergeParams mp;
+      mp.v = partial_o;
+      mp.s = partial_lse;
+      mp.tasks = reinterpret_cast<const fi::MergeTask*>(ws + P.ws.prefill_merges);
+      mp.S = 0;
+      mp.H = P.num_qo_heads;
+      mp.d = P.head_dim;
+      mp.out = out;
+      mp.lse = lse;
+      mp.dtype = P.dtype;
+      e = fi::launch_merge(mp, int(P.prefill_merges.size()), stream);
+      if (e != cudaSuccess) return cuda_fail(e, "prefill merge launch");
     }
     if (!P.prefix_items.empty()) {
       // Shared prefixes: each group's rows of q against chunks of its prefix,

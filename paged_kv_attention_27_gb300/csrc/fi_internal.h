@@ -30,7 +30,9 @@ struct WorkItem {
   int32_t tok_end;
   int32_t slot;
   int32_t q_row;
-  int32_t merge;   // split decode work: index of its merge task; else -1
+  int32_t merge;   // split decode work: index of its merge task; a prefill piece:
+                   // the tile's piece count (row r's state at slot + r * merge);
+                   // else -1
 };
 static_assert(sizeof(WorkItem) == 36, "work item is 9 int32");
 
@@ -65,10 +67,21 @@ inline bool mixed_kernel_applies(int head_dim, int group, int dtype, int kv_dtyp
          (dtype == FI_DTYPE_BF16 || dtype == FI_DTYPE_FP16);
 }
 inline int prefill_kv_tile(int head_dim) { return head_dim <= 128 ? 128 : 64; }
+// KV split of prefill tiles: at most this many pieces per tile; the cost of a
+// piece in KV tiles of one CTA (item start and end, about 2.4; writing its
+// fp32 states and reading them back in the merge at an SM's share of HBM,
+// about 2.8 at head_dim 128) that the planner weighs against a shorter
+// finish; a split only where the estimate is this fraction of the unsplit
+// one or less (it leaves out the merge launch), and only when the longest
+// tile has kMinSplitTiles KV tiles or more
+constexpr int kMaxPrefillPieces = 16;
+constexpr int kSplitPieceCost = 5;
+constexpr double kSplitMaxRatio = 0.85;
+constexpr int kMinSplitTiles = 16;
 
 struct WorkspaceLayout {
-  size_t decode_items = 0, prefill_items = 0, prefix_items = 0, prefix_tables = 0, merges = 0,
-         merge_counters = 0, partial_o = 0, partial_lse = 0;
+  size_t decode_items = 0, prefill_items = 0, prefix_items = 0, prefix_tables = 0,
+         prefill_merges = 0, merges = 0, merge_counters = 0, partial_o = 0, partial_lse = 0;
   size_t image_end = 0;   // the run calls upload [0, image_end): header, work lists, merges
   // the page table of a host-buffer call (page indptr | page indices | last
   // page lengths | qo indptr), right after the image, uploaded with it
@@ -88,6 +101,9 @@ struct Plan {
   std::vector<WorkItem> decode_items;    // launch order
   std::vector<WorkItem> prefill_items;   // launch order
   std::vector<MergeTask> merges;
+  // split prefill tiles: one task per row, merging the row's piece states
+  // (after the prefill launch, by the merge kernel)
+  std::vector<MergeTask> prefill_merges;
   // shared-prefix decode: prefill-kernel items over chunks of each group's
   // prefix (virtual request 2g = group g: its rows of q, one head, the
   // prefix keys; an item's `slot` plus a row of q is the row's state slot),

@@ -89,6 +89,11 @@ struct PrefillParams {
   // slot = item.slot + row of q
   float* state_o;
   float* state_lse;
+  // states of split prefill tiles (items with merge > 0): fp32 o
+  // [slot][head][d] (normalised, times v_scale) and lse [slot][head], slot =
+  // item.slot + row within the tile * item.merge; merged by the merge kernel
+  float* piece_o;
+  float* piece_lse;
   uint32_t* err;
   uint64_t wait_limit_ns;
   int32_t fault_kind;   // test hook: 1 = CTA 0's K producer skips its first tile

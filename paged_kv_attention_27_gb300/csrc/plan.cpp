@@ -316,18 +316,82 @@ fi_status build_plan(int32_t mode, int32_t batch, const int32_t* qo_indptr,
     if (x.len != y.len) return x.len > y.len;
     return x.b != y.b ? x.b < y.b : x.qt < y.qt;
   });
-  p.prefill_items.resize(tiles.size() * size_t(num_qo_heads));
+
+  // ---- KV split of prefill tiles when the launch has under two waves of
+  //      work units (a CTA's unit: a tile with one head, or with a head pair
+  //      on the two-tile kernel). Long tiles are then cut into pieces of
+  //      whole KV tiles, so that more SMs share the longest ones ("FlashInfer
+  //      Attention Kernel optimisation analysis", section 2.2: balance the
+  //      load by sequence length); each piece writes fp32 states (O / l and
+  //      lse per row and head) and one merge launch combines a row's pieces
+  //      by log-sum-exp. The piece count k of the longest tile minimises
+  //      ceil(units * k / SMs) * (tiles / k + c0), the finish time of units
+  //      of that length handed out in rounds, with c0 = kSplitPieceCost KV
+  //      tiles per piece, and is taken only if that beats the whole tiles'
+  //      estimate by the margin kSplitMaxRatio; shorter tiles are cut at the
+  //      same length. Only a longest tile of kMinSplitTiles KV tiles or more
+  //      is worth a merge launch, and plans with decode rows (the mixed
+  //      kernel, concurrent decode) are not split.
+  struct Piece { int64_t len, kv_begin, kv_end; int32_t b, qt, slot, k; };
+  std::vector<Piece> pieces;
+  pieces.reserve(tiles.size());
+  {
+    const int64_t kv_tile = prefill_kv_tile(head_dim);
+    const int64_t heads_per_unit = (head_dim <= 128 && g % 2 == 0) ? 2 : 1;
+    const int64_t units = int64_t(tiles.size()) * (num_qo_heads / heads_per_unit);
+    int64_t split_len = 0;   // keys per piece (whole KV tiles); 0: no split
+    if (dec.empty() && !tiles.empty() && units < 2 * int64_t(num_sms)) {
+      const int64_t max_tiles = ceil_div(tiles[0].len, kv_tile);
+      int64_t best_k = 1;
+      if (max_tiles < kMinSplitTiles) best_k = 0;   // (no candidate below)
+      const double whole = double(ceil_div(units, num_sms)) * double(max_tiles + kSplitPieceCost);
+      double best = whole * kSplitMaxRatio;          // a split must beat this
+      for (int64_t k = 2; best_k > 0 && k <= kMaxPrefillPieces && max_tiles >= 2 * k; ++k) {
+        const double f = double(ceil_div(units * k, num_sms)) *
+                         (double(max_tiles) / double(k) + double(kSplitPieceCost));
+        if (f < best) {
+          best = f;
+          best_k = k;
+        }
+      }
+      if (best_k > 1) split_len = ceil_div(max_tiles, best_k) * kv_tile;
+    }
+    for (const Tile& t : tiles) {
+      const int64_t k = split_len > 0 ? std::max<int64_t>(1, ceil_div(t.len, split_len)) : 1;
+      if (k == 1) {
+        pieces.push_back(Piece{t.len, t.kv_begin, t.kv_end, t.b, t.qt, -1, -1});
+        continue;
+      }
+      // slots of the tile's rows: row r, piece j -> slot s0 + r * k + j
+      const int64_t rows = std::min<int64_t>(kPrefillTileM, qo_len[t.b] - int64_t(t.qt) * kPrefillTileM);
+      const int64_t s0 = p.num_slots;
+      p.num_slots += int32_t(rows * k);
+      for (int64_t r = 0; r < rows; ++r) {
+        MergeTask mt{int32_t(qo_start[t.b] + int64_t(t.qt) * kPrefillTileM + r),
+                     int32_t(s0 + r * k), int32_t(k), -1, 0, 0, {0, 0}};
+        p.prefill_merges.push_back(mt);
+      }
+      for (int64_t j = 0; j < k; ++j) {
+        const int64_t b0 = t.kv_begin + j * split_len;
+        const int64_t b1 = std::min(t.kv_end, b0 + split_len);
+        pieces.push_back(Piece{b1 - b0, b0, b1, t.b, t.qt, int32_t(s0 + j), int32_t(k)});
+      }
+    }
+    std::stable_sort(pieces.begin(), pieces.end(),
+                     [](const Piece& x, const Piece& y) { return x.len > y.len; });
+  }
+  p.prefill_items.resize(pieces.size() * size_t(num_qo_heads));
   WorkItem* pdst = p.prefill_items.data();
-  for (const Tile& t : tiles) {
+  for (const Piece& t : pieces) {
     WorkItem w;
     w.req = t.b;
     w.page_begin = int32_t(page_indptr[t.b] + t.kv_begin / page_size);
     w.n_pages = int32_t(ceil_div(t.kv_end - t.kv_begin, page_size));
     w.tok_begin = int32_t(t.kv_begin);
     w.tok_end = int32_t(t.kv_end);
-    w.slot = -1;
+    w.slot = t.slot;   // a piece: its state of row r at slot + r * merge
     w.q_row = int32_t(qo_start[t.b] + int64_t(t.qt) * kPrefillTileM);
-    w.merge = -1;
+    w.merge = t.k;     // a piece: the tile's piece count; else -1
     for (int h = 0; h < num_qo_heads; ++h) {
       w.head = h;
       *pdst++ = w;
@@ -335,7 +399,7 @@ fi_status build_plan(int32_t mode, int32_t batch, const int32_t* qo_indptr,
   }
 
   // ---- workspace: header | decode items | prefill items | prefix items |
-  //      prefix tables | merges | merge counters (the uploaded image ends
+  //      prefix tables | prefill merges | merges | merge counters (the uploaded image ends
   //      here) | host-buffer page table | partial o | partial lse
   size_t off = kHeaderBytes;
   p.ws.decode_items = off;
@@ -346,6 +410,8 @@ fi_status build_plan(int32_t mode, int32_t batch, const int32_t* qo_indptr,
   off = align_up(off + p.prefix_items.size() * sizeof(WorkItem));
   p.ws.prefix_tables = off;
   off = align_up(off + p.prefix_tables.size() * sizeof(int32_t));
+  p.ws.prefill_merges = off;
+  off = align_up(off + p.prefill_merges.size() * sizeof(MergeTask));
   p.ws.merges = off;
   off = align_up(off + p.merges.size() * sizeof(MergeTask));
   // one arrival counter per (merge task, kv head), zero at the start of a

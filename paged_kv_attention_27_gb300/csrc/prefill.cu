@@ -542,6 +542,12 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap& q_map, const CUt
       const float inv = lp > 0.f ? v_scale / lp : 0.f;
       const size_t out_row = size_t(w.q_row) + t_row;
       const int qo_head = w.head * prm.pack + t_head;
+      // state slot of the row: shared-prefix items item.slot + row of q; a
+      // piece of a split tile item.slot + row within the tile * item.merge
+      // (mixed plans are never split)
+      const bool piece = !C::MIXED && w.merge > 0;
+      const size_t srow = piece ? size_t(w.slot) + size_t(t_row) * size_t(w.merge)
+                                : size_t(w.slot) + out_row;
       uint16_t* op = reinterpret_cast<uint16_t*>(prm.out) +
                      (out_row * prm.num_qo_heads + qo_head) * HEAD_DIM;
       // O is read 64 columns (two loads) per wait, to halve the round trips
@@ -564,11 +570,12 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap& q_map, const CUt
         for (int b = 0; b < BATCH; ++b) {
           const int c = c0 + b;
           const uint32_t (&r)[32] = rb2[b];
-          if (row_ok && prm.state_o) {
-            // fp32 state for a later log-sum-exp merge (shared-prefix decode)
-            const size_t srow = size_t(w.slot) + out_row;
+          if (row_ok && (prm.state_o || piece)) {
+            // fp32 state for a later log-sum-exp merge (shared-prefix decode,
+            // or a piece of a split tile)
             float4* dst = reinterpret_cast<float4*>(
-                prm.state_o + (srow * prm.num_qo_heads + qo_head) * HEAD_DIM + c * 32);
+                (piece ? prm.piece_o : prm.state_o) + (srow * prm.num_qo_heads + qo_head) *
+                HEAD_DIM + c * 32);
 #pragma unroll
             for (int q4 = 0; q4 < 8; ++q4) {
               const float* f = reinterpret_cast<const float*>(r) + q4 * 4;
@@ -587,8 +594,8 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap& q_map, const CUt
           }
         }
       }
-      float* lse_dst = prm.state_o ? prm.state_lse : prm.lse;
-      const size_t lrow = prm.state_o ? size_t(w.slot) + out_row : out_row;
+      float* lse_dst = piece ? prm.piece_lse : (prm.state_o ? prm.state_lse : prm.lse);
+      const size_t lrow = (piece || prm.state_o) ? srow : out_row;
       if (row_ok && lse_dst)
         lse_dst[lrow * prm.num_qo_heads + qo_head] = l > 0.f ? (m + lg2(l)) * kLn2 : -INFINITY;
       // O has been read: the next item's first PV (issued only after this

@@ -585,10 +585,14 @@ prefill_pair_kernel(const __grid_constant__ CUtensorMap q_map,
       }
       tc_fence_after();
       // ---- epilogue: O / lp (the inputs' type), lse = ln(l) + m ln 2
+      // (a piece of a split tile writes the row's fp32 state instead: O / l
+      // times v_scale and lse, at slot item.slot + t * item.merge)
       const bool row_ok = w.q_row + t < rb.q_end;
       const float inv = lp > 0.f ? v_scale / lp : 0.f;
       const size_t out_row = size_t(w.q_row) + t;
       const int qo_head = w.head + i;
+      const bool piece = w.merge > 0;
+      const size_t srow = piece ? size_t(w.slot) + size_t(t) * size_t(w.merge) : 0;
       uint16_t* op = reinterpret_cast<uint16_t*>(prm.out) +
                      (out_row * prm.num_qo_heads + qo_head) * HEAD_DIM;
 #pragma unroll 1
@@ -604,7 +608,18 @@ prefill_pair_kernel(const __grid_constant__ CUtensorMap q_map,
 #pragma unroll
             for (int e = 0; e < 32; ++e) rb2[b][e] = 0u;
         }
-        if (row_ok) {
+        if (row_ok && piece) {
+#pragma unroll
+          for (int b = 0; b < 2; ++b) {
+            float4* dst = reinterpret_cast<float4*>(
+                prm.piece_o + (srow * prm.num_qo_heads + qo_head) * HEAD_DIM + (c0 + b) * 32);
+#pragma unroll
+            for (int q4 = 0; q4 < 8; ++q4) {
+              const float* f = reinterpret_cast<const float*>(rb2[b]) + q4 * 4;
+              dst[q4] = make_float4(f[0] * inv, f[1] * inv, f[2] * inv, f[3] * inv);
+            }
+          }
+        } else if (row_ok) {
 #pragma unroll
           for (int b = 0; b < 2; ++b) {
             uint4* dst = reinterpret_cast<uint4*>(op + (c0 + b) * 32);
@@ -619,9 +634,10 @@ prefill_pair_kernel(const __grid_constant__ CUtensorMap q_map,
           }
         }
       }
-      if (row_ok && prm.lse)
-        prm.lse[out_row * prm.num_qo_heads + qo_head] =
-            l > 0.f ? (m + lg2(l)) * kLn2 : -INFINITY;
+      float* lse_dst = piece ? prm.piece_lse : prm.lse;
+      const size_t lrow = piece ? srow : out_row;
+      if (row_ok && lse_dst)
+        lse_dst[lrow * prm.num_qo_heads + qo_head] = l > 0.f ? (m + lg2(l)) * kLn2 : -INFINITY;
       // O has been read: the next pair's first PV (issued only after this
       // warp's next p_full arrival) may overwrite it
       tc_fence_before();

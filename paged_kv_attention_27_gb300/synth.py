@@ -396,6 +396,19 @@ def causal_prefill(seq_len: int, batch: int = 8, seed: int = 3,
                       window_left=window_left, dtype=dtype)
 
 
+def long_context_chunk(seed: int = 11, batch: int = 1, chunk_len: int = 512,
+                       context: int = 32768, num_qo_heads: int = 64) -> PagedBatch:
+    """Chunked prefill of a long prompt (8 kv heads, d=128, P=16; 64 query
+    heads: the 70B shape, 32: an 8B-class shape): each request appends
+    ``chunk_len`` causal rows to a context of ``context`` keys in all (the
+    chunk's own keys included)."""
+    kv = np.full(batch, context, np.int64)
+    qo = np.full(batch, chunk_len, np.int64)
+    return make_batch(f"long-context chunk B{batch} {chunk_len} rows on {context} keys "
+                      f"Hq{num_qo_heads} Hkv8 d128 P16 NHD", kv, qo, num_qo_heads, 8, 128, 16,
+                      NHD, None, True, seed)
+
+
 def ragged_prefill(seed: int = 4, batch: int = 16) -> PagedBatch:
     """Causal varlen prefill, 70B shape, 16 requests with L ~ U[128,8192]."""
     g = philox(seed + 1000)

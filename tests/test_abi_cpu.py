@@ -174,26 +174,8 @@ def test_windowed_prefill_items_start_on_the_page_of_the_first_row_window(causal
     b = _table_only(kv, 8, 2, 128, 16, qo)
     b.causal = causal
     b.window_left = w
-    plan = _plan(b, B.FI_MODE_PREFILL)
-    info = B.fi_plan_get_info(plan)
-    pre = B.fi_plan_get_work(plan)[info["num_decode_items"]:]
-    rows = {}
-    for req, h, pb, npg, t0, t1, slot, qrow in pre.tolist():
-        qo_len, kv_len = qo[req], kv[req]
-        r0 = qrow - b.qo_indptr[req]
-        r_last = min(qo_len, r0 + 128) - 1
-        first = max(0, kv_len - qo_len + r0 - w)          # first key of the tile's first row
-        assert t0 % 16 == 0 and t0 <= first < t0 + 16 or (t0 == t1 == 0)
-        assert t1 == (min(kv_len, kv_len - qo_len + r_last + 1) if causal else kv_len)
-        assert pb == b.page_indptr[req] + t0 // 16
-        assert npg == -(-(t1 - t0) // 16)
-        for r in range(r0, r_last + 1):
-            rows[(req, h, r)] = rows.get((req, h, r), 0) + 1
-    want = {(r, h, i) for r in range(len(kv)) if qo[r] >= 2 for h in range(8)
-            for i in range(qo[r])}
-    assert set(rows) == want and all(c == 1 for c in rows.values())
-    lens = pre[:, 5] - pre[:, 4]
-    assert np.all(np.diff(lens) <= 0)
+    for sms in (152, 4):   # split tiles (few work units for 152 SMs) and whole ones
+        _check_prefill_cover(b, _plan(b, B.FI_MODE_PREFILL, sms=sms))
 
 
 @pytest.mark.parametrize("case,status", [
@@ -536,25 +518,49 @@ def test_host_step_tickets_without_a_device():
 
 def _check_prefill_cover(b, plan):
     """Each (request, query head, row) of a multi-row request in exactly one
-    prefill item, whose page-aligned key range holds every key its rows may
+    prefill tile, whose page-aligned key range holds every key its rows may
     see: from the page of its first row's first visible key to the causal
-    bound of its last row (or the end of the keys)."""
+    bound of its last row (or the end of the keys). A tile is one item, or
+    (a split tile) pieces of whole KV tiles that cover its range once, in
+    order, each with its own state slots (row r of piece j: slot s0 + r * k
+    + j, k pieces), disjoint from every other tile's."""
     info = B.fi_plan_get_info(plan)
     pre = B.fi_plan_get_work(plan)[info["num_decode_items"]:][:info["num_prefill_items"]]
     P, w = b.page_size, b.window_left
-    rows = {}
+    kv_tile = 128 if b.head_dim <= 128 else 64
+    tiles = {}
     for req, h, pb, npg, t0, t1, slot, qrow in pre.tolist():
+        assert 0 <= h < b.num_qo_heads
+        assert pb == b.page_indptr[req] + t0 // P and npg == -(-(t1 - t0) // P)
+        assert pb + npg <= b.page_indptr[req + 1]
+        tiles.setdefault((req, h, qrow), []).append((t0, t1, slot))
+    rows, slots = {}, set()
+    for (req, h, qrow), pieces in tiles.items():
         qo_len, kv_len = int(b.qo_lens[req]), int(b.kv_lens[req])
         r0 = qrow - int(b.qo_indptr[req])
         r_last = min(qo_len, r0 + 128) - 1
         end = min(kv_len, kv_len - qo_len + r_last + 1) if b.causal else kv_len
         first = 0 if w < 0 else max(0, kv_len - qo_len + r0 - w)
-        assert t1 == end and slot == -1 and 0 <= h < b.num_qo_heads
-        assert t0 % P == 0 and t0 <= min(first, end) < t0 + P or t0 == t1
-        assert pb == b.page_indptr[req] + t0 // P and npg == -(-(t1 - t0) // P)
-        assert pb + npg <= b.page_indptr[req + 1]
+        pieces.sort()
+        t0 = pieces[0][0]
+        assert t0 % P == 0 and t0 <= min(first, end) < t0 + P or t0 == pieces[-1][1]
+        assert pieces[-1][1] == end
+        k = len(pieces)
+        if k == 1:
+            assert pieces[0][2] == -1
+        else:
+            s0 = pieces[0][2]
+            for j, (a, z, slot) in enumerate(pieces):
+                assert (a - t0) % kv_tile == 0 and a < z and slot == s0 + j
+                assert j == 0 or a == pieces[j - 1][1]
+            if h == 0:
+                for r in range(r_last + 1 - r0):
+                    for j in range(k):
+                        assert s0 + r * k + j not in slots
+                        slots.add(s0 + r * k + j)
         for r in range(r0, r_last + 1):
             rows[(req, h, r)] = rows.get((req, h, r), 0) + 1
+    assert all(0 <= s < info["num_partial_slots"] for s in slots)
     want = {(r, h, i) for r in range(b.batch) if b.qo_lens[r] >= 2
             for h in range(b.num_qo_heads) for i in range(int(b.qo_lens[r]))}
     assert set(rows) == want and all(c == 1 for c in rows.values())
@@ -565,6 +571,42 @@ def _check_prefill_cover(b, plan):
         assert np.all(pre[0::2, 1] % 2 == 0) and np.all(pre[0::2, 1] + 1 == pre[1::2, 1])
         same = [0, 2, 3, 4, 5, 6, 7]                   # every field but the head
         assert np.array_equal(pre[0::2][:, same], pre[1::2][:, same])
+    return tiles
+
+
+def test_short_prefill_launches_split_their_long_tiles():
+    """Under two waves of work units, long tiles are cut into pieces when the
+    estimate gains enough: a 512-row chunk on 32K keys with 32/8 heads (4
+    tiles x 16 head pairs = 64 units on 152 SMs) is split; with 64/8 heads
+    (128 units) the estimated gain is too small; with two waves or more, with
+    decode rows in the plan, or with short tiles nothing is split."""
+    b = _table_only([32768], 32, 8, 128, 16, [512])
+    b.causal = True
+    plan = _plan(b, B.FI_MODE_PREFILL, sms=152)
+    tiles = _check_prefill_cover(b, plan)
+    ks = {len(p) for p in tiles.values()}
+    assert len(ks) == 1 and min(ks) > 1
+    k = ks.pop()
+    # 64 units of ~256 KV tiles: k minimises ceil(64 k / 152) (256 / k + 5)
+    f = lambda k: -(-64 * k // 152) * (256 / k + 5)
+    assert f(k) == min(f(j) for j in range(1, 17)) and f(k) <= 0.85 * f(1)
+    info = B.fi_plan_get_info(plan)
+    assert info["num_partial_slots"] == 512 * k
+    for hq, sms in ((64, 152), (32, 32)):   # a small gain; two waves of units
+        b1 = _table_only([32768], hq, 8, 128, 16, [512])
+        b1.causal = True
+        tiles = _check_prefill_cover(b1, _plan(b1, B.FI_MODE_PREFILL, sms=sms))
+        assert all(len(p) == 1 for p in tiles.values())
+    # a decode row in the batch: whole tiles
+    b2 = _table_only([32768, 900], 32, 8, 128, 16, [512, 1])
+    b2.causal = True
+    tiles = _check_prefill_cover(b2, _plan(b2, B.FI_MODE_PREFILL, sms=152))
+    assert all(len(p) == 1 for p in tiles.values())
+    # short tiles (under 16 KV tiles) stay whole
+    b3 = _table_only([1900], 8, 2, 128, 16, [300])
+    b3.causal = True
+    tiles = _check_prefill_cover(b3, _plan(b3, B.FI_MODE_PREFILL, sms=152))
+    assert all(len(p) == 1 for p in tiles.values())
 
 
 @pytest.mark.parametrize("seed", range(40))

@@ -91,6 +91,37 @@ def test_causal_prefill_small(d, P):
     check_full(b)
 
 
+@pytest.mark.parametrize("case", ["pair_d128", "pair_d64_fp16", "one_tile_d256", "one_tile_g1",
+                                  "window", "non_causal", "ragged"])
+def test_split_prefill_tiles(case):
+    """A launch of under two waves of work units cuts its long tiles into
+    pieces of whole KV tiles; each piece writes fp32 states and one merge
+    launch combines a row's pieces by log-sum-exp. Every row against the
+    oracle, on the two-tile and the one-tile kernel, with a window, without
+    the causal mask, and with tiles of different lengths."""
+    mk = synth.make_batch
+    if case == "pair_d128":
+        b = mk("split pair d128", [9000], [300], 8, 2, 128, 16, synth.NHD, None, True, 901)
+    elif case == "pair_d64_fp16":
+        b = mk("split pair d64 fp16", [7000], [200], 8, 2, 64, 16, synth.HND, None, True, 902,
+               dtype="fp16")
+    elif case == "one_tile_d256":
+        b = mk("split d256", [5000], [200], 16, 8, 256, 32, synth.HND, None, True, 903)
+    elif case == "one_tile_g1":
+        b = mk("split g1", [6000], [256], 4, 4, 128, 16, synth.NHD, None, True, 904)
+    elif case == "window":
+        b = mk("split window", [9000], [300], 8, 2, 128, 16, synth.NHD, None, True, 905,
+               window_left=2500)
+    elif case == "non_causal":
+        b = mk("split non-causal", [8000], [200], 8, 2, 128, 16, synth.NHD, None, False, 906)
+    else:
+        b = mk("split ragged", [9000, 300, 4000, 2500], [300, 300, 129, 2], 8, 2, 128, 16,
+               synth.NHD, None, True, 907)
+    db = check_full(b)
+    info = B.fi_plan_get_info(db.plan)
+    assert info["num_partial_slots"] > 0   # the plan did split
+
+
 def test_chunked_prefill_bottom_right_causal():
     kv = [700, 200, 129, 1000]
     qo = [37, 200, 128, 300]          # chunks appended to existing KV
