@@ -609,20 +609,22 @@ __device__ __forceinline__ int decode_produce(const DecodeParams& prm, const Wor
     const bool skip = skip_first && i == 0;
     if (lane == 0 && !skip) mbar_arrive_expect_tx(fb, bytes);
     __syncwarp();
-    if (valid && !skip) {
-      const uint32_t kdst = ring_addr(R, s, C::STAGE_BYTES) + lane * box_bytes;
-      const uint32_t vdst = kdst + C::KBYTES;
-#pragma unroll
-      for (int c = 0; c < BOXES; ++c) {
-        const uint32_t off = uint32_t(c) * C::TILE * 128u;   // 0 for FP8
-        if (prm.layout == FI_LAYOUT_NHD) {
-          tma_load_4d(kdst + off, k_map, fb, c * 64, item.head, 0, page);
-          tma_load_4d(vdst + off, v_map, fb, c * 64, item.head, 0, page);
-        } else {
-          tma_load_4d(kdst + off, k_map, fb, c * 64, 0, item.head, page);
-          tma_load_4d(vdst + off, v_map, fb, c * 64, 0, item.head, page);
-        }
-      }
+    // One copy per lane: copy o = lane is box (o / 2) % BOXES of K (o even)
+    // or V (o odd) of the tile's page o / (2 BOXES); a tile has at most 32
+    // (pages x boxes x 2). A single lane issuing a tile's copies one after
+    // another paced the ring (about 0.8 us per 32 KB tile with 8 copies).
+    const int pi = min(lane / (2 * BOXES), 31);          // the copy's page in the tile
+    const int opage = __shfl_sync(0xffffffffu, page, pi);
+    const bool ovalid = (vmask >> pi) & 1u && lane < np * 2 * BOXES;
+    if (ovalid && !skip) {
+      const int c = (lane >> 1) % BOXES, is_v = lane & 1;
+      const uint32_t dst = ring_addr(R, s, C::STAGE_BYTES) + uint32_t(is_v) * C::KBYTES +
+                           uint32_t(pi) * box_bytes + uint32_t(c) * C::TILE * 128u;  // c = 0 for FP8
+      const CUtensorMap* map = is_v ? v_map : k_map;
+      if (prm.layout == FI_LAYOUT_NHD)
+        tma_load_4d(dst, map, fb, c * 64, item.head, 0, opage);
+      else
+        tma_load_4d(dst, map, fb, c * 64, 0, item.head, opage);
     }
   }
   return n_tiles;

@@ -95,11 +95,11 @@ struct PrefillCfg {
   static_assert(!MIXED || (OFF_DEC - OFF_K) % DC::STAGE_BYTES == 0, "");
   // mixed kernel (384 threads): the softmax warpgroup raises its registers
   // to 224 per thread, the helper warpgroup (prefill producers, MMA issuer,
-  // decode producer) lowers them to 56, the decode consumer warpgroup raises
+  // decode producer) lowers them to 64, the decode consumer warpgroup raises
   // them to 184. The shares fit the launch allocation of R per thread when
-  // 128 x (224 + 56 + 184) <= 384 x R, i.e. R >= 155 (the compiler's cap for
+  // 128 x (224 + 64 + 184) <= 384 x R, i.e. R >= 158 (the compiler's cap for
   // 384 threads is 168); the host checks the compiled R before the launch.
-  static constexpr uint32_t SOFTMAX_REGS = 224, HELPER_REGS = 56, DECODE_REGS = 184;
+  static constexpr uint32_t SOFTMAX_REGS = 224, HELPER_REGS = 64, DECODE_REGS = 184;
   static constexpr uint32_t MIN_LAUNCH_REGS =
       (128 * (SOFTMAX_REGS + HELPER_REGS + DECODE_REGS) + 383) / 384;
   static_assert(!MIXED || THREADS == 384, "four warpgroups");
@@ -755,8 +755,8 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap& q_map, const CUt
           } else if (it_next >= 0 && item_tiles<C::N>(wn) > 0 && lane < pages_in(wn, 0)) {
             next_page = prm.page_indices[wn.page_begin + lane];
           }
-          const uint32_t bytes =
-              uint32_t(__popc(__ballot_sync(0xffffffffu, valid))) * C::DBLK * box;
+          const uint32_t vmask = __ballot_sync(0xffffffffu, valid);
+          const uint32_t bytes = uint32_t(__popc(vmask)) * C::DBLK * box;
           if (g >= C::NST && !mbar_wait_warp(smem_u32(&empty[st]), ((g / C::NST) & 1) ^ 1,
                                              limit, &abort_flag)) {
             ok = false;
@@ -767,11 +767,15 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap& q_map, const CUt
           if (skip) skip_pos = g;
           if (lane == 0 && !skip) mbar_arrive_expect_tx(fb, bytes);
           __syncwarp();
-          if (valid && !skip) {
-            const uint32_t dst = ring + st * C::KV_BYTES + lane * box;
-  #pragma unroll
-            for (int c = 0; c < C::DBLK; ++c)
-              tma_load_4d(dst + c * C::N * 128, map, fb, c * 64, c1, c2, page);
+          // one copy per lane: box lane % DBLK of the tile's page lane / DBLK
+          // (at most 32); one lane issuing its page's boxes in turn paced
+          // the ring
+          const int pi = min(lane / C::DBLK, 31);
+          const int opage = __shfl_sync(0xffffffffu, page, pi);
+          if (((vmask >> pi) & 1u) && lane < np * C::DBLK && !skip) {
+            const int c = lane % C::DBLK;
+            tma_load_4d(ring + st * C::KV_BYTES + pi * box + c * C::N * 128, map, fb, c * 64, c1,
+                        c2, opage);
           }
           issued = g + 1;
         }
