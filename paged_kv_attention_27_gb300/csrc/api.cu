@@ -539,6 +539,10 @@ fi_status run_paged(fi_plan_t plan, bool prefill_call, const void* q, const int3
   dp.err = err;
   dp.wait_limit_ns = wait_limit_ns;
   dp.fault_kind = fault_kind;
+  dp.n_items = int(P.decode_items.size());
+  // the decode kernel's item counter (the mixed kernel's decode side uses the
+  // same word; a call launches one or the other)
+  dp.work_counter = reinterpret_cast<uint32_t*>(ws + fi::kDecodeCounterOffset);
 
   const int group = P.num_qo_heads / P.num_kv_heads;
   const bool both = !P.prefill_items.empty() && !P.decode_items.empty();
@@ -615,7 +619,7 @@ fi_status run_paged(fi_plan_t plan, bool prefill_call, const void* q, const int3
     }
     if (!P.decode_items.empty()) {
       e = fi::launch_decode(P.head_dim, group, P.dtype, P.kv_dtype, kmap, vmap, dp,
-                            int(P.decode_items.size()), dstream);
+                            int(P.decode_items.size()), P.num_sms, dstream);
       if (e != cudaSuccess) return cuda_fail(e, "decode launch");
     }
     if (both) {

@@ -51,7 +51,7 @@ struct MergeTask {
 constexpr int kPrefillTileM = 128;         // query rows per prefill CTA
 constexpr size_t kHeaderBytes = 256;       // device error word, work counter, reserved
 constexpr size_t kWorkCounterOffset = 64;  // prefill items handed out (zeroed by the upload)
-constexpr size_t kDecodeCounterOffset = 128;  // decode items handed out by the mixed kernel
+constexpr size_t kDecodeCounterOffset = 128;  // decode items handed out (decode or mixed kernel)
 constexpr size_t kAlign = 256;
 
 // Error bits in the first word of the workspace.

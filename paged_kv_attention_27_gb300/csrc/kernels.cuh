@@ -47,6 +47,10 @@ struct DecodeParams {
   uint32_t* err;
   uint64_t wait_limit_ns;
   int32_t fault_kind;
+  // the decode kernel's persistent launch: items [0, n_items), CTA c starts
+  // with item c and takes the next ones from *work_counter (zero at launch)
+  int32_t n_items;
+  uint32_t* work_counter;
 };
 
 struct MergeParams {
@@ -125,7 +129,7 @@ cudaError_t launch_mixed(int head_dim, int group, int dtype, const CUtensorMap& 
 // `dtype` (fi_dtype) selects the element type of q and out, `kv_dtype` that
 // of the cache (dtype or FI_DTYPE_E4M3).
 cudaError_t launch_decode(int head_dim, int group, int dtype, int kv_dtype, const CUtensorMap& km,
-                          const CUtensorMap& vm, const DecodeParams& p, int n_items,
+                          const CUtensorMap& vm, const DecodeParams& p, int n_items, int num_sms,
                           cudaStream_t stream);
 cudaError_t launch_merge(const MergeParams& p, int n_rows, cudaStream_t stream);
 

@@ -180,9 +180,14 @@ def test_merge_states_abi(n, S, H, d):
     compare(out, lse, ref_o, ref_l, what="merge_states")
 
 
-def test_bounded_wait_times_out_and_context_survives():
-    b = synth.make_batch("timeout", [4000, 100], [1, 1], 8, 2, 128, 16, synth.NHD, None, False, 10)
-    db = _dev(b)
+@pytest.mark.parametrize("hq", [8, 2])
+def test_bounded_wait_times_out_and_context_survives(hq):
+    """4 heads per kv head: one item per CTA (tensor-core consumer); 1 head:
+    the persistent launch (SIMT consumer), where the CTA that times out holds
+    further items from the counter."""
+    b = synth.make_batch(f"timeout hq{hq}", [4000, 100, 9000, 1], [1, 1, 1, 1], hq, 2, 128, 16,
+                         synth.NHD, None, False, 10)
+    db = _dev(b, sms=2)
     B.fi_debug_set_fault(1, 2_000_000)          # 2 ms bound; producer skips one load
     try:
         db.run()
@@ -196,8 +201,10 @@ def test_bounded_wait_times_out_and_context_survives():
     compare(out, lse, ref_o, ref_l, what="after timeout")
 
 
-def test_out_of_range_page_index_is_reported_not_read():
-    b = synth.make_batch("bounds", [40, 40], [1, 1], 8, 2, 64, 16, synth.NHD, None, False, 11)
+@pytest.mark.parametrize("hq", [8, 2])
+def test_out_of_range_page_index_is_reported_not_read(hq):
+    b = synth.make_batch(f"bounds hq{hq}", [40, 40], [1, 1], hq, 2, 64, 16, synth.NHD, None,
+                         False, 11)
     db = _dev(b)
     bad = b.page_indices.copy()
     bad[1] = b.num_pages + 1000
