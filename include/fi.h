@@ -161,7 +161,10 @@ typedef struct {
  *   mode             FI_MODE_DECODE (one query row per request; qo_indptr_h
  *                    must be NULL) or FI_MODE_PREFILL (qo_indptr_h required;
  *                    requests with one row are planned as decode work).
- *   batch_size       number of requests B >= 0 (0 gives an empty plan).
+ *   batch_size       number of requests B >= 0 (0 gives an empty plan; a
+ *                    plan without query rows, B = 0 or every qo_len 0, makes
+ *                    every run call return FI_OK at once, reading no
+ *                    argument but the plan).
  *   qo_indptr_h      host int32 [B+1], non-decreasing, qo_indptr_h[0] == 0.
  *   page_indptr_h    host int32 [B+1], non-decreasing, page_indptr_h[0] >= 0.
  *   last_page_len_h  host int32 [B].

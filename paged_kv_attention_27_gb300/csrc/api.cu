@@ -416,7 +416,7 @@ fi_status run_paged(fi_plan_t plan, bool prefill_call, const void* q, const int3
   if (!plan) return FI_ERR_INVALID_ARG;
   const fi::Plan& P = plan->p;
   if (P.mode != (prefill_call ? FI_MODE_PREFILL : FI_MODE_DECODE)) return FI_ERR_INVALID_ARG;
-  if (P.batch == 0) return FI_OK;
+  if (P.batch == 0 || P.total_q == 0) return FI_OK;   // no query rows: nothing to run
   if (!q || !k_cache || !v_cache || !out || !workspace || !page_indptr_d || !last_page_len_d)
     return FI_ERR_INVALID_ARG;
   if (prefill_call && !qo_indptr_d) return FI_ERR_INVALID_ARG;
@@ -759,7 +759,7 @@ fi_status fi_batch_attention_host_async(
   *ticket_out = 0;
   const fi::Plan& P = plan->p;
   const bool prefill = P.mode == FI_MODE_PREFILL;
-  if (P.batch == 0) return FI_OK;
+  if (P.batch == 0 || P.total_q == 0) return FI_OK;   // no query rows: nothing to run
   if (!q_h || !out_h || !page_indptr_h || !last_page_len_h || !workspace || !k_cache ||
       !v_cache || (prefill && !qo_indptr_h) || (P.page_entries > 0 && !page_indices_h))
     return FI_ERR_INVALID_ARG;

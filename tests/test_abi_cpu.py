@@ -501,6 +501,22 @@ def test_host_buffer_call_sizes_its_region_and_checks_before_any_copy():
     assert e.value.status == B.FI_ERR_NO_DEVICE
 
 
+def test_plans_without_query_rows_run_nothing():
+    """A plan without query rows (every request's qo_len 0, keys or not) makes
+    the run calls return FI_OK at once, reading no argument but the plan."""
+    for kv in ([0, 0], [0, 37]):
+        p = B.fi_plan(B.FI_MODE_PREFILL, 2, [0, 0, 0], [0, 0, -(-kv[1] // 16)],
+                      [0, kv[1] - 16 * (-(-kv[1] // 16) - 1) if kv[1] else 0], 8, 2, 128, 16,
+                      1, None, 152)
+        assert B.fi_plan_get_info(p)["num_items"] == 0
+        B.fi_batch_prefill_paged(p, None, None, None, None, B.FI_LAYOUT_NHD, 0, 0, None, None,
+                                 None, 0.1, 1.0, 1.0, None, None, None, 0, stream=0)
+        t = B.fi_batch_attention_host_async(p, None, None, None, None, B.FI_LAYOUT_NHD, 0, 0,
+                                            None, None, None, 0.1, 1.0, 1.0, None, None, None,
+                                            0, stream=0)
+        assert t == 0
+
+
 def test_host_step_tickets_without_a_device():
     """An empty plan's step has ticket 0, which is always complete; a ticket
     that was never issued is refused."""
