@@ -54,7 +54,9 @@
  * Device errors: kernels never trap and never wait without a bound. A
  *   page index outside [0, num_pages) is skipped and recorded; a bounded
  *   wait that runs out is recorded. fi_check_device_status() reports
- *   either after the stream has been synchronised.
+ *   either after the stream has been synchronised. (A run of a plan without
+ *   query rows touches nothing, so the workspace's status word is then
+ *   whatever the last run before it left.)
  */
 #ifndef FI_H
 #define FI_H

@@ -876,6 +876,15 @@ __device__ __forceinline__ void decode_finish(const DecodeParams& prm, const Wor
         hm = hm_g;
         hs = hs_g;
       }
+      // every chunk state's lse of every head, loaded by all the consumer
+      // threads at once (a few threads walking the states one L2 round trip
+      // after another made the merging CTA the launch's last)
+      if (fits) {
+        for (int x = tid; x < mt.n_states * GROUP; x += NW * 32)
+          wgt[x] = __ldcg(&prm.partial_lse[size_t(mt.slot_base + x / GROUP) * prm.num_qo_heads +
+                                           item.head * GROUP + x % GROUP]);
+        named_bar_sync(1, NW * 32);
+      }
       if (tid < GROUP) {
         const int hq = item.head * GROUP + tid;
         // the chunks' states, and the row's shared-prefix states (if any)
@@ -883,16 +892,18 @@ __device__ __forceinline__ void decode_finish(const DecodeParams& prm, const Wor
           return __ldcg(&prm.partial_lse[size_t(mt.extra_slot + e * mt.extra_stride) *
                                          prm.num_qo_heads + hq]);
         };
+        auto slse = [&](int i) {
+          return fits ? wgt[i * GROUP + tid]
+                      : __ldcg(&prm.partial_lse[size_t(mt.slot_base + i) * prm.num_qo_heads + hq]);
+        };
         float M = -INFINITY;
         for (int e = 0; e < mt.n_extra; ++e) M = fmaxf(M, xlse(e));
-        for (int i = 0; i < mt.n_states; ++i)
-          M = fmaxf(M, __ldcg(&prm.partial_lse[size_t(mt.slot_base + i) * prm.num_qo_heads + hq]));
+        for (int i = 0; i < mt.n_states; ++i) M = fmaxf(M, slse(i));
         float sw = 0.f;
         if (M != -INFINITY) {
           for (int i = 0; i < mt.n_states; ++i) {
-            const float w = ex2((__ldcg(&prm.partial_lse[size_t(mt.slot_base + i) *
-                                                         prm.num_qo_heads + hq]) - M) * kDecLog2e);
-            if (fits) wgt[i * GROUP + tid] = w;   // -inf -> 0
+            const float w = ex2((slse(i) - M) * kDecLog2e);
+            if (fits) wgt[i * GROUP + tid] = w;   // -inf -> 0; this thread's column only
             sw += w;
           }
           for (int e = 0; e < mt.n_extra; ++e) sw += ex2((xlse(e) - M) * kDecLog2e);
@@ -911,6 +922,7 @@ __device__ __forceinline__ void decode_finish(const DecodeParams& prm, const Wor
         const float M = hm[h], sw = hs[h];
         float acc = 0.f;
         if (sw > 0.f) {
+#pragma unroll 4
           for (int i = 0; i < mt.n_states; ++i) {
             const size_t row = size_t(mt.slot_base + i) * prm.num_qo_heads + hq;
             const float w = fits ? wgt[i * GROUP + h]
