@@ -312,8 +312,11 @@ prefill_pair_kernel(const __grid_constant__ CUtensorMap q_map,
           ok = mbar_wait_bounded(smem_u32(&bars.q_full), n & 1, limit, &abort_flag);
           for (int j = 0; ok && j < nt; ++j) {
             const int gq = g + j, st = gq % C::NST;
-            ok = mbar_wait_bounded(smem_u32(&bars.k_full[st]), (gq / C::NST) & 1, limit,
-                                   &abort_flag);
+            // (the K of later tiles was waited for while the previous tile's
+            // softmax ran)
+            if (j == 0)
+              ok = mbar_wait_bounded(smem_u32(&bars.k_full[st]), (gq / C::NST) & 1, limit,
+                                     &abort_flag);
             // S_i and P_i share columns, and the softmax rescales O_i after S_i
             // is full: the previous O_i += P_i V completes first
             if (ok && gq >= 1)
@@ -331,10 +334,18 @@ prefill_pair_kernel(const __grid_constant__ CUtensorMap q_map,
             tc_commit(smem_u32(&bars.s_full[i]));
             tc_commit(smem_u32(&bars.k_empty[st]));
             if (j == nt - 1) tc_commit(smem_u32(&bars.q_empty));
-            ok = mbar_wait_bounded(smem_u32(&bars.p_full[i]), gq & 1, limit, &abort_flag);
+            // The next tile's K and this tile's V are waited for here, while the
+            // softmax works on S_i: a wait costs this thread a few hundred
+            // cycles even when its phase has long completed, and after P_i
+            // that sat between the softmax and the PV (+5 % at 1K-16K).
+            if (j + 1 < nt)
+              ok = mbar_wait_bounded(smem_u32(&bars.k_full[(gq + 1) % C::NST]),
+                                     ((gq + 1) / C::NST) & 1, limit, &abort_flag);
             if (ok)
               ok = mbar_wait_bounded(smem_u32(&bars.v_full[st]), (gq / C::NST) & 1, limit,
                                      &abort_flag);
+            if (ok)
+              ok = mbar_wait_bounded(smem_u32(&bars.p_full[i]), gq & 1, limit, &abort_flag);
             if (!ok) break;
             tc_fence_after();
             const uint64_t vd = vd0 + uint64_t((st * C::KV_BYTES) >> 4);
