@@ -33,6 +33,7 @@
 // group), longest first, as in the one-tile kernel.
 #include <cfloat>
 #include <climits>
+#include <type_traits>
 
 #include "elem.cuh"
 #include "fi_internal.h"
@@ -435,6 +436,17 @@ prefill_pair_kernel(const __grid_constant__ CUtensorMap q_map,
       // l: sum of the exact weights (gives lse); lp: of the rounded weights
       // the PV MMA multiplies (normalises O)
       float m = -INFINITY, l = 0.f, lp = 0.f;
+      // lp differs from l only where a row of the warp sees fewer than N keys
+      // in all (from its first visible key to its last; one or two are
+      // possible there): in the tiles that cross such a row's bounds, lp
+      // adds the rounded weights. Elsewhere the rounding errors of many
+      // weights average out and lp = l. The two cases run separate copies
+      // of the tile loop: with the rounded sums compiled out, the loop
+      // measured 1K +4 %, 4K +3 %.
+      const bool few_keys =
+          __any_sync(0xffffffffu, rb.t_max - (rb.t_min > 0 ? rb.t_min : 0) + 1 < C::N);
+      auto tiles = [&](auto rounded_sums) {
+      constexpr bool RS = decltype(rounded_sums)::value;
       for (int j = 0; j < nt; ++j, ++g) {
         const int kvst = g % C::NST;
         // The warpgroups take turns: tile g of warpgroup 1 after tile g of
@@ -536,16 +548,16 @@ prefill_pair_kernel(const __grid_constant__ CUtensorMap q_map,
         for (int k = 0; k < C::N; k += 2)
           rs4[(k >> 1) & 3] = __fadd2_rn(rs4[(k >> 1) & 3], make_float2(s[k], s[k + 1]));
         // P as packed 16-bit pairs over S_i's first 64 columns (all read
-        // above). lp adds the rounded values the tensor core multiplies in
-        // tiles that cross the row's bounds (few keys may be visible there),
-        // the exact sum elsewhere.
+        // above). With RS, lp adds the rounded values the tensor core
+        // multiplies in tiles that cross the row's bounds, the exact sum
+        // elsewhere.
         float2 rsp2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll
         for (int kb = 0; kb < 2; ++kb) {
           uint32_t wv[32];
 #pragma unroll
           for (int e = 0; e < 32; ++e) wv[e] = E::pack2(s[kb * 64 + 2 * e], s[kb * 64 + 2 * e + 1]);
-          if (need_mask) {
+          if (RS && need_mask) {
 #pragma unroll
             for (int e = 0; e < 32; ++e)
               rsp2[e & 1] = __fadd2_rn(rsp2[e & 1], make_float2(E::lo(wv[e]), E::hi(wv[e])));
@@ -556,7 +568,7 @@ prefill_pair_kernel(const __grid_constant__ CUtensorMap q_map,
         const float2 rs2 = __fadd2_rn(__fadd2_rn(rs4[0], rs4[1]), __fadd2_rn(rs4[2], rs4[3]));
         const float rs_tile = rs2.x + rs2.y;
         l += rs_tile;
-        lp += need_mask ? (rsp2[0].x + rsp2[0].y) + (rsp2[1].x + rsp2[1].y) : rs_tile;
+        lp += (RS && need_mask) ? (rsp2[0].x + rsp2[0].y) + (rsp2[1].x + rsp2[1].y) : rs_tile;
         // Last tile: V rows past the valid keys may hold unused page slots or
         // stale data; zero them so that P = 0 there cannot meet a NaN. (Both
         // warpgroups write the same zeros; each orders its own writes before
@@ -582,6 +594,11 @@ prefill_pair_kernel(const __grid_constant__ CUtensorMap q_map,
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&bars.p_full[i]));
       }
+      };
+      if (few_keys)
+        tiles(std::true_type{});
+      else
+        tiles(std::false_type{});
       if (!ok) break;
       // the next pair's bounds load while this pair's last PV completes
       WorkItem wn;
