@@ -469,6 +469,11 @@ prefill_pair_kernel(const __grid_constant__ CUtensorMap q_map,
         const int hi = rb.t_max - col0;
         const int lo = rb.t_min > col0 ? rb.t_min - col0 : 0;
         const bool need_mask = __any_sync(0xffffffffu, hi < C::N - 1 || lo > 0);
+        // The tile body in two copies: tiles that cross some row's bounds
+        // (the mask, the rounded sums, the V zeroing of a last tile) and the
+        // rest, which need none of it.
+        auto body = [&](auto masked) -> bool {
+        constexpr bool MK = decltype(masked)::value;
         // The row's 128 scores in registers (one wait), the row max
         // (sm_scale >= 0 commutes with max; two scores per three-input max)
         uint32_t sr[4][32];
@@ -478,7 +483,7 @@ prefill_pair_kernel(const __grid_constant__ CUtensorMap q_map,
         // In a tile that crosses the row's bounds the hidden scores become
         // -inf once, here: their weights are then exactly 0 (2^-inf), and the
         // rest of the softmax is the same code as in every other tile.
-        if (need_mask) {
+        if (MK) {
           if (prm.window_left < 0) {
 #pragma unroll
             for (int k = 0; k < C::N; ++k)
@@ -557,7 +562,7 @@ prefill_pair_kernel(const __grid_constant__ CUtensorMap q_map,
           uint32_t wv[32];
 #pragma unroll
           for (int e = 0; e < 32; ++e) wv[e] = E::pack2(s[kb * 64 + 2 * e], s[kb * 64 + 2 * e + 1]);
-          if (RS && need_mask) {
+          if (RS && MK) {
 #pragma unroll
             for (int e = 0; e < 32; ++e)
               rsp2[e & 1] = __fadd2_rn(rsp2[e & 1], make_float2(E::lo(wv[e]), E::hi(wv[e])));
@@ -568,18 +573,16 @@ prefill_pair_kernel(const __grid_constant__ CUtensorMap q_map,
         const float2 rs2 = __fadd2_rn(__fadd2_rn(rs4[0], rs4[1]), __fadd2_rn(rs4[2], rs4[3]));
         const float rs_tile = rs2.x + rs2.y;
         l += rs_tile;
-        lp += (RS && need_mask) ? (rsp2[0].x + rsp2[0].y) + (rsp2[1].x + rsp2[1].y) : rs_tile;
+        lp += (RS && MK) ? (rsp2[0].x + rsp2[0].y) + (rsp2[1].x + rsp2[1].y) : rs_tile;
         // Last tile: V rows past the valid keys may hold unused page slots or
         // stale data; zero them so that P = 0 there cannot meet a NaN. (Both
         // warpgroups write the same zeros; each orders its own writes before
         // its tile's MMA.)
         const int valid = w.tok_end - col0;
-        if (valid < C::N) {
+        if (MK && valid < C::N) {
           if (!mbar_wait_warp(smem_u32(&bars.v_full[kvst]), (g / C::NST) & 1, limit,
-                              &abort_flag)) {
-            ok = false;
-            break;
-          }
+                              &abort_flag))
+            return false;
           if (t >= valid) {
 #pragma unroll
             for (int c = 0; c < C::DBLK; ++c)
@@ -588,6 +591,12 @@ prefill_pair_kernel(const __grid_constant__ CUtensorMap q_map,
                 st_shared_v4(base + C::OFF_V + kvst * C::KV_BYTES + c * C::N * 128 + t * 128 +
                                  c8 * 16, 0u, 0u, 0u, 0u);
           }
+        }
+        return true;
+        };
+        if (!(need_mask ? body(std::true_type{}) : body(std::false_type{}))) {
+          ok = false;
+          break;
         }
         fence_proxy_async_smem();   // zeroed V rows (generic writes) before the MMA reads them
         tc_fence_before();
