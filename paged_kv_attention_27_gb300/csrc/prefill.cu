@@ -37,6 +37,7 @@
 // Fully masked KV tiles are never visited: the planner clips tok_end.
 #include <cfloat>
 #include <climits>
+#include <type_traits>
 
 #include "decode_roles.cuh"
 #include "elem.cuh"
@@ -385,10 +386,12 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap& q_map, const CUt
         const int hi = rb.t_max - col0;
         const int lo = rb.t_min > col0 ? rb.t_min - col0 : 0;
         const bool need_mask = __any_sync(0xffffffffu, hi < C::N - 1 || lo > 0);
+        auto body = [&](auto masked) -> bool {
+        constexpr bool MK = decltype(masked)::value;
         // In a tile that crosses the row's bounds the hidden scores become
         // -inf once, here: their weights are then exactly 0 (2^-inf), and the
         // rest of the softmax is the same code as in every other tile.
-        if (need_mask) {
+        if (MK) {
           if (prm.window_left < 0) {
 #pragma unroll
             for (int k = 0; k < C::N; ++k)
@@ -445,10 +448,8 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap& q_map, const CUt
         // completed (the last PV of the previous item completed before its
         // epilogue read O)
         if (j >= 1) {
-          if (!mbar_wait_warp(smem_u32(&bars.pv_done), (g - 1) & 1, limit, &abort_flag)) {
-            ok = false;
-            break;
-          }
+          if (!mbar_wait_warp(smem_u32(&bars.pv_done), (g - 1) & 1, limit, &abort_flag))
+            return false;
           tc_fence_after();
           if (__any_sync(0xffffffffu, o_live)) {
 #pragma unroll 1
@@ -472,12 +473,10 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap& q_map, const CUt
         // Last tile: V rows past the valid keys may hold unused page slots or
         // stale data; zero them so that P = 0 there cannot meet a NaN.
         const int valid = w.tok_end - col0;
-        if (valid < C::N) {
+        if (MK && valid < C::N) {
           if (!mbar_wait_warp(smem_u32(&bars.v_full[kvst]), (g / C::NST) & 1, limit,
-                              &abort_flag)) {
-            ok = false;
-            break;
-          }
+                              &abort_flag))
+            return false;
           if (t >= valid && t < C::N) {
 #pragma unroll
             for (int c = 0; c < C::DBLK; ++c)
@@ -499,7 +498,7 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap& q_map, const CUt
           uint32_t wv[32];
 #pragma unroll
           for (int e = 0; e < 32; ++e) wv[e] = E::pack2(s[kb * 64 + 2 * e], s[kb * 64 + 2 * e + 1]);
-          if (need_mask) {
+          if (MK) {
 #pragma unroll
             for (int e = 0; e < 32; ++e)
               rsp2[e & 1] = __fadd2_rn(rsp2[e & 1], make_float2(E::lo(wv[e]), E::hi(wv[e])));
@@ -508,7 +507,13 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap& q_map, const CUt
                     wv);
         }
         tmem_wait_st();
-        lp += need_mask ? (rsp2[0].x + rsp2[0].y) + (rsp2[1].x + rsp2[1].y) : rs_tile;
+        lp += MK ? (rsp2[0].x + rsp2[0].y) + (rsp2[1].x + rsp2[1].y) : rs_tile;
+        return true;
+        };
+        if (!(need_mask ? body(std::true_type{}) : body(std::false_type{}))) {
+          ok = false;
+          break;
+        }
         fence_proxy_async_smem();   // zeroed V rows (generic writes) before the MMA reads them
         tc_fence_before();
         __syncwarp();
